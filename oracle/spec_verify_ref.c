@@ -1,0 +1,337 @@
+/*
+ * spec_verify_ref.c -- float64 CPU oracle of the batched speculative-sampling
+ * verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg load this library.  The CUDA path shares no code, header,
+ * table or helper with it, and it imports nothing from the CUDA path.
+ *
+ * Every step follows the pages in the order they state it, with no blocking,
+ * fusion or reordering:
+ *
+ *  - Temperature softmax of each target row and each draft row:
+ *    p = softmax(z / T), q likewise, with the same T for both.
+ *    ("Fast Inference from Transformers via Speculative Decoding" explainer,
+ *    PyTorch sketch, Step 1 and Step 2: softmax(logits / temperature);
+ *    toolsku "LLM speculative decoding optimisation", verify sketch.)
+ *  - Acceptance of draft token x_i with probability min(1, p_i(x_i)/q_i(x_i)),
+ *    decided by u_i < p_i(x_i)/q_i(x_i).
+ *    (disassemble-channel "Speculative Decoding theory", Step 3 acceptance
+ *    formula and the simulation's `random() < acceptance_prob`.)
+ *  - The first rejected position k truncates the draft: x_0..x_{k-1} are kept.
+ *    (same page, Step 3: everything after the first rejection is discarded.)
+ *  - At k, one token is drawn from the residual
+ *    p'(x) = max(0, p(x) - q(x)) / sum_x' max(0, p(x') - q(x')),
+ *    falling back to p when that sum is zero.
+ *    (same page, "modified distribution" definition, and the simulation's
+ *    fallback branch.)
+ *  - When every draft is accepted, a bonus token is drawn from the target row
+ *    at position gamma_b + 1.  (same page, Step 3 last paragraph; toolsku verify
+ *    sketch, bonus branch.)
+ *  - Greedy mode: with temperature -> 0 acceptance reduces to argmax matching.
+ *    (explainer, "Implementation points", greedy paragraph; zvxbase
+ *    "draft length by load", K=3 worked example.)
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *  - accept is strict: u < ratio; q(x) == 0 accepts.
+ *  - no epsilons are added to q or to the residual sum.
+ *  - the resample/bonus draws use their own uniform u[b][G]; the inverse CDF
+ *    runs over ascending token id and returns the smallest j with C_j > u*S.
+ *    If rounding leaves no such j, the largest j with r_j > 0 is returned.
+ *  - num_accepted counts accepted drafts only (emitted = num_accepted + 1).
+ *  - greedy argmax ties go to the lowest token id.
+ *
+ * Inputs are widened exactly (bf16 -> float32 -> double; float32 -> double).
+ * Temperature is widened from float32.  Uniforms are passed as double so that
+ * tests can probe decision boundaries finer than float32 allows; the public
+ * float32 uniforms widen to double exactly.
+ *
+ * Layout: target logits [B][G+1][V], draft logits [B][G][V], draft tokens
+ * [B][G], gamma [B], uniforms [B][G+1] (column i < gamma_b is the acceptance
+ * draw of position i, column G is the resample/bonus draw), temperature [B],
+ * out_tokens [B][G+1] (-1 after the emitted tokens), num_accepted [B].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define REF_F32 0
+#define REF_BF16 1
+
+/* Exact widening of one logit to double. */
+static double logit_at(const void *base, int dtype, size_t idx) {
+  if (dtype == REF_F32) return (double)((const float *)base)[idx];
+  uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+static size_t target_row(int b, int i, int G, int V) {
+  return ((size_t)b * (size_t)(G + 1) + (size_t)i) * (size_t)V;
+}
+
+static size_t draft_row(int b, int i, int G, int V) {
+  return ((size_t)b * (size_t)G + (size_t)i) * (size_t)V;
+}
+
+/*
+ * Temperature softmax of one row in float64: m = max z, then
+ * p[v] = exp((z[v] - m) / T) / sum_v' exp((z[v'] - m) / T), summed in plain
+ * ascending order.  Writes p when p_out is non-NULL; returns the sum s and m.
+ */
+static void softmax_row(const void *base, int dtype, size_t off, int V, double T,
+                        double *p_out, double *m_out, double *s_out) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double z = logit_at(base, dtype, off + (size_t)v);
+    if (z > m) m = z;
+  }
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double e = exp((logit_at(base, dtype, off + (size_t)v) - m) / T);
+    if (p_out) p_out[v] = e;
+    s += e;
+  }
+  if (p_out)
+    for (int v = 0; v < V; ++v) p_out[v] /= s;
+  *m_out = m;
+  *s_out = s;
+}
+
+/* Probability of token x in a row whose max and sum are already known. */
+static double prob_of(const void *base, int dtype, size_t off, int x, double T,
+                      double m, double s) {
+  return exp((logit_at(base, dtype, off + (size_t)x) - m) / T) / s;
+}
+
+/*
+ * Inverse-CDF draw over weights r[0..V-1] with total S, driven by u in [0,1):
+ * the smallest j whose inclusive prefix C_j exceeds u*S.  If rounding leaves
+ * none, the largest j with r[j] > 0.  *margin gets the distance of u*S to the
+ * nearer edge of j's interval, divided by S.
+ */
+static int inverse_cdf(const double *r, int V, double S, double u, double *margin) {
+  double target = u * S;
+  double c_prev = 0.0, c = 0.0;
+  for (int j = 0; j < V; ++j) {
+    c_prev = c;
+    c += r[j];
+    if (c > target) {
+      double lo = target - c_prev, hi = c - target;
+      *margin = (lo < hi ? lo : hi) / S;
+      return j;
+    }
+  }
+  for (int j = V - 1; j >= 0; --j) {
+    if (r[j] > 0.0) {
+      *margin = 0.0;
+      return j;
+    }
+  }
+  *margin = 0.0;
+  return 0;
+}
+
+typedef struct {
+  const void *target;
+  const void *draft;
+  int dtype, B, G, V;
+  const int32_t *tokens;
+  const int32_t *gamma;
+  const double *u;
+  const float *temperature;
+  int32_t *out_tokens;
+  int32_t *num_accepted;
+  double *p_tok, *q_tok, *margin_accept, *margin_cdf;
+} sample_args;
+
+/* One request of the sampling verify step; returns 0, or -3 on malloc failure. */
+static int sample_one(const sample_args *a, int b) {
+  const int G = a->G, V = a->V, gb = a->gamma[b];
+  const double T = (double)a->temperature[b];
+  const double *u = a->u + (size_t)b * (size_t)(G + 1);
+  int32_t *out = a->out_tokens + (size_t)b * (size_t)(G + 1);
+  for (int i = 0; i <= G; ++i) out[i] = -1;
+  if (a->margin_accept)
+    for (int i = 0; i < G; ++i) a->margin_accept[(size_t)b * G + i] = NAN;
+  if (a->p_tok)
+    for (int i = 0; i < G; ++i) a->p_tok[(size_t)b * G + i] = NAN;
+  if (a->q_tok)
+    for (int i = 0; i < G; ++i) a->q_tok[(size_t)b * G + i] = NAN;
+
+  /* Steps 1-2: per position, softmax both rows, gather at x_i, accept/reject. */
+  int k = gb;
+  for (int i = 0; i < gb; ++i) {
+    const int x = a->tokens[(size_t)b * G + i];
+    double mt, st, md, sd;
+    softmax_row(a->target, a->dtype, target_row(b, i, G, V), V, T, NULL, &mt, &st);
+    softmax_row(a->draft, a->dtype, draft_row(b, i, G, V), V, T, NULL, &md, &sd);
+    const double p = prob_of(a->target, a->dtype, target_row(b, i, G, V), x, T, mt, st);
+    const double q = prob_of(a->draft, a->dtype, draft_row(b, i, G, V), x, T, md, sd);
+    if (a->p_tok) a->p_tok[(size_t)b * G + i] = p;
+    if (a->q_tok) a->q_tok[(size_t)b * G + i] = q;
+    const double ratio = (q == 0.0) ? INFINITY : p / q;
+    if (a->margin_accept) a->margin_accept[(size_t)b * G + i] = fabs(u[i] - ratio);
+    const int accept = (q == 0.0) || (u[i] < ratio);
+    if (!accept) {
+      k = i;
+      break;
+    }
+    out[i] = x;
+  }
+
+  /* Step 3: residual at k, or the bonus row when every draft was accepted. */
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  double *r = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!p || !r) {
+    free(p);
+    free(r);
+    return -3;
+  }
+  double m, s, S = 0.0;
+  softmax_row(a->target, a->dtype, target_row(b, k, G, V), V, T, p, &m, &s);
+  if (k < gb) {
+    double *q = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!q) {
+      free(p);
+      free(r);
+      return -3;
+    }
+    softmax_row(a->draft, a->dtype, draft_row(b, k, G, V), V, T, q, &m, &s);
+    for (int v = 0; v < V; ++v) {
+      const double d = p[v] - q[v];
+      r[v] = d > 0.0 ? d : 0.0;
+      S += r[v];
+    }
+    free(q);
+    if (S == 0.0) { /* residual vanished: fall back to p */
+      for (int v = 0; v < V; ++v) {
+        r[v] = p[v];
+        S += r[v];
+      }
+    }
+  } else {
+    for (int v = 0; v < V; ++v) {
+      r[v] = p[v];
+      S += r[v];
+    }
+  }
+  double margin = 0.0;
+  out[k] = inverse_cdf(r, V, S, u[G], &margin);
+  if (a->margin_cdf) a->margin_cdf[b] = margin;
+  a->num_accepted[b] = k;
+  free(p);
+  free(r);
+  return 0;
+}
+
+static int check_common(int B, int G, int V, int dtype, const int32_t *tokens,
+                        const int32_t *gamma) {
+  if (B < 0 || G < 0 || V < 1 || (dtype != REF_F32 && dtype != REF_BF16)) return -1;
+  for (int b = 0; b < B; ++b) {
+    if (gamma[b] < 0 || gamma[b] > G) return -1;
+    for (int i = 0; i < gamma[b]; ++i) {
+      const int32_t x = tokens[(size_t)b * G + i];
+      if (x < 0 || x >= V) return -1;
+    }
+  }
+  return 0;
+}
+
+/*
+ * Sampling verify step for B requests.  p_tok, q_tok, margin_accept ([B][G])
+ * and margin_cdf ([B]) are optional (NULL).  margin_accept[b][i] is |u - ratio|
+ * for every evaluated position, NaN elsewhere.  Returns 0, -1 on invalid input,
+ * -3 on allocation failure.  nthreads <= 0 uses the OpenMP default.
+ */
+int sv_ref_sample(const void *target_logits, const void *draft_logits, int dtype, int B,
+                  int G, int V, const int32_t *draft_tokens, const int32_t *gamma,
+                  const double *uniforms, const float *temperature, int32_t *out_tokens,
+                  int32_t *num_accepted, double *p_tok, double *q_tok,
+                  double *margin_accept, double *margin_cdf, int nthreads) {
+  if (check_common(B, G, V, dtype, draft_tokens, gamma)) return -1;
+  for (int b = 0; b < B; ++b) {
+    if (!(temperature[b] > 0.0f)) return -1;
+    for (int i = 0; i <= G; ++i) {
+      const double u = uniforms[(size_t)b * (G + 1) + i];
+      if (!(u >= 0.0 && u < 1.0)) return -1;
+    }
+  }
+  sample_args a = {target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma,
+                   uniforms, temperature, out_tokens, num_accepted, p_tok, q_tok,
+                   margin_accept, margin_cdf};
+  int err = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(min : err)
+#endif
+  for (int b = 0; b < B; ++b) {
+    const int e = sample_one(&a, b);
+    if (e < err) err = e;
+  }
+  (void)nthreads;
+  return err;
+}
+
+/*
+ * Greedy verify step: g_i = argmax_v t[b][i][v] (lowest id on ties),
+ * k = first i < gamma_b with x_i != g_i (else gamma_b),
+ * out = x_0..x_{k-1}, g_k.  exact_tie ([B][G+1], optional) flags rows whose
+ * maximum occurs more than once.  Returns 0 or -1 on invalid input.
+ */
+int sv_ref_greedy(const void *target_logits, int dtype, int B, int G, int V,
+                  const int32_t *draft_tokens, const int32_t *gamma, int32_t *out_tokens,
+                  int32_t *num_accepted, int32_t *exact_tie, int nthreads) {
+  if (check_common(B, G, V, dtype, draft_tokens, gamma)) return -1;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int b = 0; b < B; ++b) {
+    int32_t *out = out_tokens + (size_t)b * (size_t)(G + 1);
+    for (int i = 0; i <= G; ++i) {
+      out[i] = -1;
+      if (exact_tie) exact_tie[(size_t)b * (G + 1) + i] = 0;
+    }
+    const int gb = gamma[b];
+    int k = gb;
+    for (int i = 0; i <= gb; ++i) {
+      const size_t off = target_row(b, i, G, V);
+      int best = 0, ties = 0;
+      double zbest = logit_at(target_logits, dtype, off);
+      for (int v = 1; v < V; ++v) {
+        const double z = logit_at(target_logits, dtype, off + (size_t)v);
+        if (z > zbest) {
+          zbest = z;
+          best = v;
+          ties = 0;
+        } else if (z == zbest) {
+          ties = 1;
+        }
+      }
+      if (exact_tie) exact_tie[(size_t)b * (G + 1) + i] = ties;
+      if (i == gb || draft_tokens[(size_t)b * G + i] != best) {
+        k = i;
+        out[i] = best;
+        break;
+      }
+      out[i] = best; /* equals the accepted draft token */
+    }
+    num_accepted[b] = k;
+  }
+  (void)nthreads;
+  return 0;
+}
+
+/* Temperature softmax of one row (for the oracle's own tests). */
+int sv_ref_softmax_row(const void *row, int dtype, int V, double T, double *p_out) {
+  if (V < 1 || !(T > 0.0)) return -1;
+  double m, s;
+  softmax_row(row, dtype, 0, V, T, p_out, &m, &s);
+  return 0;
+}

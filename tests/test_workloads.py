@@ -1,0 +1,46 @@
+"""The seeded input generator: determinism, shapes and the draft-token law (CPU)."""
+import numpy as np
+import torch
+from scipy.special import softmax as scipy_softmax
+
+from speculative_decoding_verification_62_gb300 import workloads as W
+
+
+def test_deterministic_and_shaped():
+    a = W.make_random(5, 3, 100, "bf16", seed=3, gamma="ragged", temperature=[0.5, 1, 1.5, 2, 1])
+    b = W.make_random(5, 3, 100, "bf16", seed=3, gamma="ragged", temperature=[0.5, 1, 1.5, 2, 1])
+    for k in ("target", "draft", "draft_tokens", "gamma", "uniforms", "temperature"):
+        assert torch.equal(getattr(a, k), getattr(b, k))
+    assert a.target.shape == (5, 4, 100) and a.draft.shape == (5, 3, 100)
+    assert a.target.dtype == torch.bfloat16
+    assert a.draft_tokens.dtype == torch.int32 and a.gamma.dtype == torch.int32
+    assert torch.all((a.uniforms >= 0) & (a.uniforms < 1))
+    assert torch.all((a.gamma >= 0) & (a.gamma <= 3))
+    assert torch.all((a.draft_tokens >= 0) & (a.draft_tokens < 100))
+
+
+def test_config1_shapes():
+    w = W.make("1")
+    assert (w.B, w.G, w.V) == (1, 4, 32000) and w.target.dtype == torch.float32
+    assert w.bytes_min() > 4 * 32000 * 9
+
+
+def test_gumbel_max_draws_follow_q():
+    """x ~ softmax(d/T): frequencies over 200k rows match scipy's softmax."""
+    g = torch.Generator().manual_seed(0)
+    d = torch.tensor([0.0, 1.0, -0.5, 2.0])
+    n = 200_000
+    rows = d.view(1, 1, 4).expand(n, 1, 4).contiguous()
+    T = torch.full((n,), 0.8)
+    x = W.gumbel_max_tokens(rows, T, g).view(-1).numpy()
+    freq = np.bincount(x, minlength=4) / n
+    q = scipy_softmax(d.double().numpy() / np.float64(np.float32(0.8)))
+    assert np.all(np.abs(freq - q) < 5 * np.sqrt(q * (1 - q) / n))
+
+
+def test_oracle_inputs_roundtrip_bf16_bits():
+    w = W.make_random(2, 2, 16, "bf16", seed=1)
+    o = W.oracle_inputs(w)
+    assert o["target"].dtype == np.uint16
+    back = torch.from_numpy(o["target"].view(np.int16)).view(torch.bfloat16)
+    assert torch.equal(back, w.target)
