@@ -1,0 +1,374 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched speculative-sampling verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--mode sample]
+    python bench.py --impl reference ...   # the float64 CPU oracle on host cores
+
+One step = one verify call over one batch of synthetic inputs (all rows read
+once, acceptance, first-reject scan, residual/bonus draw).  The default
+workload is config 2 (B=8, gamma=3, V=128256, bf16, T=0.8).  Inputs are
+rotated over enough device copies that each step reads logits that are not
+in L2.  Rank 0 prints one JSON line.  Under torchrun each rank runs its own
+batch (requests are independent: no data-path collective), so scaling is
+weak and the value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/sec per verify call"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="2", help="workload: 1, 2, 3, 4, 5a, 5b")
+    ap.add_argument("--mode", choices=["sample", "greedy"], default="sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(w, mode):
+    from speculative_decoding_verification_62_gb300 import workloads as W
+    return {"workload": f"config {w.name}: {W.CONFIGS[w.name]['desc']}", "B": w.B,
+            "gamma_max": w.G, "gamma_sum": w.gamma_sum(), "V": w.V, "mode": mode}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_time(w, mode, budget_s=4.0, max_calls=100000, min_calls=1):
+    """Time the float64 oracle on the whole batch, repeated for ~budget_s."""
+    import oracle
+    from speculative_decoding_verification_62_gb300 import workloads as W
+    inp = W.oracle_inputs(w)
+    cores = os.cpu_count() or 1
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        if mode == "sample":
+            oracle.sample(**inp, nthreads=cores)
+        else:
+            oracle.greedy(inp["target"], inp["draft_tokens"], inp["gamma"], nthreads=cores)
+        calls += 1
+        el = time.perf_counter() - t0
+        if calls >= max_calls or (el >= budget_s and calls >= min_calls):
+            break
+    used = min(cores, w.B)  # OpenMP over requests: one thread per request at most
+    return dict(value=w.gamma_sum() * calls / el, unit=UNIT, cores=used, kind="oracle",
+                sample=f"{calls} call(s) of the full batch ({w.B} requests) of config {w.name}, "
+                       f"float64 C oracle, OpenMP over requests ({used} of {cores} host "
+                       f"threads busy), {el:.2f} s wall",
+                seconds=el, calls=calls)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401  (inputs are drawn with torch's CPU generator)
+    from speculative_decoding_verification_62_gb300 import workloads as W
+    w = W.make(args.config, device="cpu")
+    t = []
+    for _ in range(args.warmup):
+        oracle_time(w, args.mode, budget_s=0.0, max_calls=1)
+    for _ in range(args.steps):
+        t.append(oracle_time(w, args.mode, budget_s=0.0, max_calls=1)["seconds"])
+    total = sum(t)
+    value = w.gamma_sum() * args.steps / total
+    cores = min(os.cpu_count() or 1, w.B)  # OpenMP over requests
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_desc(w, args.mode),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step is one call of the float64 C oracle on the "
+                                       f"full batch of config {w.name} ({w.B} requests), "
+                                       f"OpenMP over {cores} host threads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_62_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config, mode):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(f"{config}/{mode}")
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from speculative_decoding_verification_62_gb300 import binding
+    from speculative_decoding_verification_62_gb300 import workloads as W
+
+    # each rank draws its own batch (different seed): weak scaling by request
+    base = W.make(args.config, device=dev)
+    if rank:
+        base = W.make(args.config, device=dev, seed=base.meta["seed"] * 1000 + rank)
+    mode = args.mode
+    B, G, V = base.B, base.G, base.V
+    launches_per_call = 1
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+    per_copy = base.target.numel() * base.target.element_size()
+    if mode == "sample":
+        per_copy += base.draft.numel() * base.draft.element_size()
+    ncopy = max(2, math.ceil(4 * l2 / per_copy))
+    ncopy = min(ncopy, max(2, int(0.3 * torch.cuda.mem_get_info(dev)[0] // per_copy)))
+    targets = [base.target] + [base.target.clone() for _ in range(ncopy - 1)]
+    drafts = [base.draft] + [base.draft.clone() for _ in range(ncopy - 1)] \
+        if mode == "sample" else [None] * ncopy
+    v = binding.Verifier(B, G, V, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % ncopy
+        if mode == "sample":
+            v.sample(targets[j], drafts[j], base.draft_tokens, base.gamma, base.uniforms,
+                     base.temperature, stream=stream)
+        else:
+            v.greedy(targets[j], base.draft_tokens, base.gamma, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    status = binding.spec_verify_status(v.workspace, stream)
+    if status:
+        raise RuntimeError(f"device status flags: {binding.status_names(status)}")
+
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    gsum = base.gamma_sum()
+    emitted = int(v.num_accepted.sum().item()) + B
+    value = world * gsum / (ms_step * 1e-3)
+
+    bytes_min = base.bytes_min(mode)
+    achieved = bytes_min / (ms_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak_hbm()
+
+    # ---- end to end through the public API from pinned host memory ----
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(base, k).cpu().pin_memory() for k in
+                ("target", "draft", "draft_tokens", "gamma", "uniforms", "temperature")}
+        dbuf = {k: torch.empty_like(getattr(base, k)) for k in host}
+        out_h = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
+        nacc_h = torch.empty((B,), dtype=torch.int32).pin_memory()
+        keys = [k for k in host if mode == "sample" or k not in ("draft", "uniforms",
+                                                                   "temperature")]
+        h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+        d2h = out_h.numel() * 4 + nacc_h.numel() * 4
+
+        def e2e_step():
+            for k in keys:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            if mode == "sample":
+                v.sample(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["gamma"],
+                         dbuf["uniforms"], dbuf["temperature"], stream=stream)
+            else:
+                v.greedy(dbuf["target"], dbuf["draft_tokens"], dbuf["gamma"], stream=stream)
+            out_h.copy_(v.out_tokens, non_blocking=True)
+            nacc_h.copy_(v.num_accepted, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        k2 = max(10, min(args.steps, 100))
+        if world > 1:
+            dist.barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * gsum / (float(te.item()) / k2 * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": float(te.item()) / k2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_time(W.make(args.config, device="cpu"), mode)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        cfg = workload_desc(base, mode)
+        cfg.update({"parallelism": f"replicas x{world} (independent requests)",
+                    "l2": f"rotating {ncopy} device copies of the logits "
+                          f"({ncopy * per_copy / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
+                    "emitted_tokens_per_s": world * emitted / (ms_step * 1e-3),
+                    "bytes_min_per_step": bytes_min})
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if base.target.dtype == torch.bfloat16 else "f32",
+                "data": "synthetic", "config": cfg,
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "peak_source": peak_src,
+                             "traffic": profiled_traffic(args.config, mode),
+                             "kernel": "verify_kernel (one launch per step)"},
+                "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * launches_per_call,
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,144 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched speculative-sampling
+ * verify step.
+ *
+ * The operation (one call, B independent requests):
+ *   For request b with gamma_b draft tokens x_0..x_{gamma_b-1}:
+ *   1. p_i = softmax(t[b][i] / T_b) for the gamma_b + 1 target rows and
+ *      q_i = softmax(d[b][i] / T_b) for the gamma_b draft rows.
+ *      ("Fast Inference from Transformers via Speculative Decoding" explainer,
+ *      PyTorch sketch Steps 1-2; toolsku "LLM speculative decoding
+ *      optimisation", verify sketch.)
+ *   2. Draft i is accepted iff u[b][i] < p_i(x_i) / q_i(x_i), the
+ *      min(1, p/q) acceptance test; k is the first rejected position, or
+ *      gamma_b when none is rejected.
+ *      (disassemble-channel "Speculative Decoding theory", Step 3.)
+ *   3. If k < gamma_b, one token is drawn at k from the residual
+ *      max(0, p_k - q_k) / sum max(0, p_k - q_k) (from p_k if that sum is 0);
+ *      otherwise a bonus token is drawn from p_{gamma_b}.  The draw is the
+ *      inverse CDF over ascending token id driven by u[b][G]: the smallest j
+ *      whose prefix sum exceeds u[b][G] times the total.
+ *      (disassemble-channel, "modified distribution" and Step 3 bonus token.)
+ *   Greedy mode replaces 1-3 by argmax matching: g_i = argmax t[b][i]
+ *   (lowest id on ties), k = first i with x_i != g_i, and g_k is emitted.
+ *   (explainer, "Implementation points", greedy paragraph; zvxbase "draft
+ *   length by load", K = 3 worked example.)
+ *
+ * Layouts (all row-major, rows contiguous with pitch V elements):
+ *   target_logits  [B][G+1][V]  float32 or bf16
+ *   draft_logits   [B][G][V]    same dtype as target_logits
+ *   draft_tokens   [B][G]       int32, entries past gamma_b are ignored
+ *   gamma          [B]          int32, 0 <= gamma_b <= G
+ *   uniforms       [B][G+1]     float32 in [0,1): column i < gamma_b is the
+ *                               acceptance draw of position i, column G the
+ *                               resample/bonus draw
+ *   temperature    [B]          float32, > 0
+ *   out_tokens     [B][G+1]     int32: x_0..x_{k-1}, the drawn token, then -1
+ *   num_accepted   [B]          int32: accepted drafts k (emitted = k + 1)
+ *
+ * Ownership and concurrency: every pointer is caller-owned DEVICE memory, except
+ * where a comment says host.  The library allocates and frees nothing and never
+ * synchronises the stream (spec_verify_status excepted).  The workspace must be
+ * zero-filled once when allocated; every call leaves it zeroed again, so one
+ * workspace serves any number of calls issued in order on one stream.  Two
+ * calls that may run concurrently need two workspaces.
+ *
+ * Errors: each entry point returns SV_OK (0) or a negative SV_ERR_* code, and
+ * on error launches nothing.  Values inside device arrays cannot be checked on
+ * the host: a gamma_b outside [0, G], a draft token outside [0, V), a uniform
+ * outside [0, 1), a non-positive or non-finite temperature, or a row with no
+ * finite logit sets a bit in the workspace's status word (read it with
+ * spec_verify_status) and is clamped to a legal value, so no call reads or
+ * writes outside the arrays described above.  NaN logits are not supported.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL means the legacy default stream. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+enum {
+  SV_OK = 0,
+  SV_ERR_SCALAR = -1,    /* B < 0, G outside [0, SV_MAX_GAMMA], V outside [1, SV_MAX_VOCAB], bad dtype */
+  SV_ERR_NULL = -2,      /* a required pointer is NULL */
+  SV_ERR_ALIGN = -3,     /* a pointer is not aligned to its element (workspace: 256 bytes) */
+  SV_ERR_WORKSPACE = -4, /* ws_bytes < spec_verify_workspace_size(B, G, V) */
+  SV_ERR_CUDA = -5       /* the kernel launch failed (cudaGetLastError) */
+};
+
+/* Status-word bits set on the device for invalid values inside arrays. */
+enum {
+  SV_STATUS_BAD_GAMMA = 1u,       /* gamma_b outside [0, G]: clamped */
+  SV_STATUS_BAD_TOKEN = 2u,       /* draft token outside [0, V): clamped */
+  SV_STATUS_BAD_UNIFORM = 4u,     /* uniform outside [0, 1) or NaN: replaced by 0 */
+  SV_STATUS_BAD_TEMPERATURE = 8u, /* temperature <= 0, inf or NaN: replaced by 1 */
+  SV_STATUS_NONFINITE_ROW = 16u,  /* a row whose maximum is not finite */
+  SV_STATUS_INTERNAL = 32u,       /* an inverse-CDF draw found no token (never expected) */
+  SV_STATUS_TIMEOUT = 64u         /* a bounded wait for a request's decision ran out; the
+                                     request's outputs are incomplete and the workspace must
+                                     be zero-filled again before reuse */
+};
+
+#define SV_MAX_GAMMA 31
+#define SV_MAX_VOCAB (1 << 24)
+
+/*
+ * Bytes of device workspace that spec_verify_sample / spec_verify_greedy need
+ * for these sizes (a multiple of 256); 0 if the sizes are invalid.
+ */
+size_t spec_verify_workspace_size(int B, int G, int V);
+
+/*
+ * Sampling verify step (steps 1-3 above) for B requests on `stream`.
+ *   target_logits, draft_logits: device, dtype `dtype`, layouts above;
+ *     draft_logits may be NULL when G == 0.
+ *   draft_tokens: device int32 [B][G] (may be NULL when G == 0).
+ *   gamma, uniforms, temperature: device, layouts above.
+ *   out_tokens, num_accepted: device outputs, layouts above.
+ *   p_tok, q_tok: optional device float64 [B][G] outputs (NULL to skip):
+ *     p_i(x_i) and q_i(x_i) for evaluated positions i <= k (i < gamma_b), NaN
+ *     elsewhere.
+ *   workspace: device, 256-byte aligned, ws_bytes >= spec_verify_workspace_size,
+ *     zero-filled before its first use.
+ * B == 0 is a no-op.  Returns SV_OK or an SV_ERR_* code.
+ */
+int spec_verify_sample(const void *target_logits, const void *draft_logits, sv_dtype dtype,
+                       int B, int G, int V, const int32_t *draft_tokens,
+                       const int32_t *gamma, const float *uniforms,
+                       const float *temperature, int32_t *out_tokens,
+                       int32_t *num_accepted, double *p_tok, double *q_tok,
+                       void *workspace, size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Greedy (argmax-match) verify step on the target rows only; no draft logits,
+ * uniforms or temperature.  Arguments as for spec_verify_sample.
+ */
+int spec_verify_greedy(const void *target_logits, sv_dtype dtype, int B, int G, int V,
+                       const int32_t *draft_tokens, const int32_t *gamma,
+                       int32_t *out_tokens, int32_t *num_accepted, void *workspace,
+                       size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Copies the workspace's status word (SV_STATUS_* bits accumulated since the
+ * last read) to *status_host (a HOST pointer), then clears it.  Synchronises
+ * `stream`.  Returns SV_OK, SV_ERR_NULL or SV_ERR_CUDA.
+ */
+int spec_verify_status(void *workspace, sv_stream_t stream, uint32_t *status_host);
+
+/* Static English text for an SV_OK / SV_ERR_* code. */
+const char *spec_verify_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */
