@@ -11,30 +11,34 @@
 //   speculative decoding optimisation", verify sketch with the bonus token.)
 //   Greedy: argmax match (explainer, "Implementation points", greedy note).
 //
-// One persistent kernel per call.  CTAs claim work items from one atomic
-// counter, in a fixed global order:
-//   A item  16 KB of one logit row (row statistics).  Per warp: the chunk
-//           maximum and the sum of exp2((z - max) log2(e)/T) (sampling), or
-//           the argmax (greedy), written as a per-warp partial.
-//   R item  8 KB of the target row k and the same 8 KB of the draft row k
-//           of one request (sampling only): the fixed-point (2^-39) sum of the
-//           residual weights max(0, p_k - q_k) (or of p for the bonus draw).
-// The order is request-major: the A items of request b, then the R items of
-// request b - L.  The lag L keeps R items behind their request's decision,
-// while the rows are still in L2.  The CTA whose A item completes a request
-// (atomic arrival count) combines the partials in float64, runs the
-// acceptance tests with a warp-ballot first-reject scan, and publishes the
-// request's decision; the CTA whose R item completes it locates the chunk that
-// holds u*S and scans only that chunk for the token.  A CTA waits for a
-// decision only while it holds no unfinished item, so waits always end; every
-// wait is also bounded by an iteration limit that sets SV_STATUS_TIMEOUT.
+// One persistent kernel per call, one CTA of 12 warps per SM.  Work items,
+// in one fixed request-major order:
+//   A item  4 KB of one logit row: max and sum of exp2((z - max) log2(e)/T)
+//           (sampling) or argmax (greedy) -> one partial per item.
+//   R item  2 KB of target row k and the same 2 KB of draft row k of one
+//           request (sampling): fixed-point (2^-39) sums of the residual
+//           max(0, p_k - q_k) and of p_k -> one partial per item.
+// The A items of request b are followed by the R items of request b - L, so
+// that a request's residual rows are re-read after its decision, from L2.
+// Every warp runs its own pipeline: it claims small batches of items from one
+// global counter (the next batch is claimed while the current one runs, and
+// its lanes decode a batch in parallel), keeps kNB TMA bulk copies
+// (cp.async.bulk) in flight into private shared-memory buffers, each tracked
+// by one mbarrier, and processes the items in order.  Arrivals are counted
+// per request in batches; the warp that completes a request's A items runs
+// its decision (float64 normalisers, acceptance tests, warp-ballot first
+// reject) and publishes it; the warp that completes its R items locates the
+// chunk holding u*S and scans only that chunk for the token.  A warp waits
+// for an undecided request only with its pipeline drained and its arrivals
+// published; everything it still holds comes later in the order, so every
+// wait ends.  Each wait is also bounded (2 s) and sets SV_STATUS_TIMEOUT.
 // Counters are reset by their last user, so the workspace stays zeroed.
 //
 // Numerics: inputs widen exactly to float32.  Exponent arguments use a
-// two-term log2(e)/T (hi + lo); exp2 is the SFU's ex2.approx; sums inside a
-// warp are float32, sums across warps and chunks float64.  The acceptance
-// ratio is formed in float64.  The residual CDF is summed in exact 64-bit
-// fixed point, so chunk sums and the final in-chunk scan agree bit for bit.
+// two-term log2(e)/T (hi + lo); exp2 is the SFU's ex2.approx; sums inside an
+// item are float32, sums across items float64.  The acceptance ratio is
+// formed in float64.  The residual CDF is summed in exact 64-bit fixed point,
+// so chunk sums and the final in-chunk scan agree bit for bit.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -45,24 +49,31 @@
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kVecA = 4;                              // 16-byte vectors per thread per A item
-constexpr int kTileBytes = kThreads * kVecA * 16;     // 16 KB of one row per A item
-constexpr int kHalfBytes = kTileBytes / 2;            // 8 KB of each row per R item
-constexpr int kMaxBatch = 8192;                       // requests per launch (smem prefix)
-constexpr unsigned kSpinLimit = 1u << 22;             // bounded waits
+#ifndef SV_WARPS
+#define SV_WARPS 12
+#endif
+#ifndef SV_BUFFERS
+#define SV_BUFFERS 4
+#endif
+constexpr int kWarps = SV_WARPS;                      // warps per CTA (one CTA per SM)
+constexpr int kThreads = 32 * kWarps;
+constexpr int kNB = SV_BUFFERS;                       // TMA buffers per warp
+constexpr int kItemBytes = 4096;                      // A item: 4 KB of one row
+constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
+constexpr int kMaxBatch = 4096;                       // requests per launch (smem prefix)
+constexpr int kMaxK = 8;                              // work items per claimed batch
+constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
 constexpr float kFix = 549755813888.0f;               // 2^39: fixed-point scale of probabilities
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
 constexpr float kLog2eLo = 1.925963033500011e-08f;          // log2(e) - kLog2eHi
 
-enum { KIND_A = 0, KIND_R = 1, KIND_RWAIT = 2, KIND_EXIT = 3 };
+enum { KIND_A = 0, KIND_R = 1 };
 enum { MODE_SAMPLE = 0, MODE_GREEDY = 1 };
 
 // ---------------------------------------------------------------------------
 // Workspace
 // ---------------------------------------------------------------------------
-struct Decision {      // per request, published by the deciding CTA
+struct Decision {      // per request, published by the deciding warp
   int k;               // first rejected position (gamma_b if none)
   int reject;          // 1: residual at k; 0: bonus from target row k = gamma_b
   float mt, md;        // maxima of target row k and draft row k
@@ -80,7 +91,7 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size
 
 __host__ __device__ inline Layout make_layout(int B, int G, int V) {
   Layout L;
-  L.NC = (V + kTileBytes / 4 - 1) / (kTileBytes / 4);
+  L.NC = (V + kItemBytes / 4 - 1) / (kItemBytes / 4);
   L.NCR = (V + kHalfBytes / 4 - 1) / (kHalfBytes / 4);
   L.status = 0;
   L.next_item = 64;
@@ -90,7 +101,7 @@ __host__ __device__ inline Layout make_layout(int B, int G, int V) {
   L.cnt_r = off; off = align256(off + (size_t)B * 4);
   L.ready = off; off = align256(off + (size_t)B * 4);
   L.dec = off;   off = align256(off + (size_t)B * sizeof(Decision));
-  L.stats = off; off = align256(off + (size_t)B * (2 * G + 1) * L.NC * kWarps * sizeof(float2));
+  L.stats = off; off = align256(off + (size_t)B * (2 * G + 1) * L.NC * sizeof(float2));
   L.resid = off; off = align256(off + (size_t)B * L.NCR * sizeof(ulonglong2));
   L.total = off;
   return L;
@@ -110,51 +121,93 @@ struct Params {
   double* p_tok;
   double* q_tok;
   unsigned int* status;
-  unsigned int* next_item;
+  unsigned int* next_item;   // next work item to claim
   unsigned int* exit_count;
-  unsigned int* cnt_a;
-  unsigned int* cnt_r;
-  unsigned int* ready;
+  unsigned int* cnt_a;       // [B] A items completed
+  unsigned int* cnt_r;       // [B] R items completed
+  unsigned int* ready;       // [B] 1 once the request's decision is published
   Decision* dec;
-  float2* stats;       // [B][2G+1][stride_nc][kWarps] (m, s) or (m, idx bits)
-  ulonglong2* resid;   // [B][stride_ncr] (residual sum, p sum)
+  float2* stats;       // [B][2G+1][stride_nc]: (max, sum) or (max, argmax bits)
+  ulonglong2* resid;   // [B][stride_ncr]: (residual sum, p sum)
 };
 
-// Work item, decoded by thread 0 into shared memory.
-struct Slot {
+// A decoded work item (one per lane of a claimed batch; stored per buffer).
+struct Meta {
   int kind;
   int b;
-  int pslot;    // A: partial row slot; R: k
+  int pslot;    // A: partial row slot
   int c;        // chunk index
-  int n;        // valid elements (A: in the tile; R: per row)
-  int aligned;  // all row pointers 16-byte aligned
+  int n;        // valid elements (A: in the item; R: per row)
+  int direct;   // 1: bytes not copied (unaligned); read them from global memory
   int reject;   // R
   int pad;
-  const char* p0;  // A: tile start; R: target half-tile
-  const char* p1;  // R: draft half-tile, or null for the bonus draw
+  const char* p0;  // A: item start; R: target half
+  const char* p1;  // R: draft half, or null for the bonus draw
   float mt, md, inv_st, rho, c_hi, c_lo;
 };
 
 // ---------------------------------------------------------------------------
-// Device helpers
+// PTX helpers: mbarriers, bulk copies, loads
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
-
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (now_ns() - t0 > kWaitNs) return false;
+  }
+}
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
   unsigned int v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Decision record read through L2 (it was written by another CTA).
@@ -184,13 +237,19 @@ __device__ __forceinline__ float load_elem(const char* base, size_t idx) {
   }
 }
 
-// element j of a 16-byte vector holding VEC = 16/EB logits
+// element j of a 16-byte vector holding 16/EB logits
 template <int EB>
 __device__ __forceinline__ float vec_elem(const uint4& v, int j) {
   const uint32_t w = j < (EB == 2 ? 2 : 1) ? v.x : j < (EB == 2 ? 4 : 2) ? v.y
                    : j < (EB == 2 ? 6 : 3) ? v.z : v.w;
   if (EB == 2) return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
   return __uint_as_float(w);
+}
+
+// a 16-byte vector of -inf logits
+__device__ __forceinline__ uint4 neg_inf_vec(int eb) {
+  const uint32_t f = eb == 2 ? 0xff80ff80u : 0xff800000u;
+  return make_uint4(f, f, f, f);
 }
 
 __device__ __forceinline__ int clamp_gamma(int g, int G) { return g < 0 ? 0 : (g > G ? G : g); }
@@ -261,6 +320,15 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
 __device__ __forceinline__ void argmax_combine(float& v, int& i, float v2, int i2) {
   if (v2 > v || (v2 == v && i2 < i)) {
     v = v2;
@@ -274,43 +342,6 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
     argmax_combine(v, i, v2, i2);
   }
-}
-
-// Loads NV 16-byte vectors per thread (vector index threadIdx.x + k*kThreads)
-// of a tile starting at p with n valid elements into buf[off..off+NV).  The
-// fast path is one non-caching 16-byte load per vector; vectors past the end
-// or in an unaligned tile are assembled from scalar loads, with -inf filling
-// missing elements.
-template <int EB, int NV>
-__device__ __forceinline__ void load_tile(uint4* buf, const char* p, int n, bool aligned) {
-  constexpr int VEC = 16 / EB;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int e0 = ((int)threadIdx.x + k * kThreads) * VEC;
-    if (aligned && e0 + VEC <= n) {
-      buf[k] = ldg_stream(p + (size_t)e0 * EB);
-    } else {
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (EB == 2) {
-          const int ea = e0 + 2 * q, eb = ea + 1;
-          const uint32_t lo = ea < n ? __ldg(reinterpret_cast<const unsigned short*>(p) + ea) : 0xff80u;
-          const uint32_t hi = eb < n ? __ldg(reinterpret_cast<const unsigned short*>(p) + eb) : 0xff80u;
-          w[q] = lo | (hi << 16);
-        } else {
-          const int e = e0 + q;
-          w[q] = e < n ? __float_as_uint(__ldg(reinterpret_cast<const float*>(p) + e)) : 0xff800000u;
-        }
-      }
-      buf[k] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-}
-
-__device__ __forceinline__ void fill_neg_inf(uint4* buf, int nv, int eb) {
-  const uint32_t f = eb == 2 ? 0xff80ff80u : 0xff800000u;
-  for (int k = 0; k < nv; ++k) buf[k] = make_uint4(f, f, f, f);
 }
 
 // ---------------------------------------------------------------------------
@@ -348,291 +379,448 @@ __device__ __forceinline__ unsigned long long scaled_target(float u, unsigned lo
   return shift >= 128 ? 0ull : (unsigned long long)(prod >> shift);
 }
 
-__device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long long v,
-                                                                   unsigned long long* sh,
-                                                                   unsigned long long* total) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned long long incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sh[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const unsigned long long w = lane < kWarps ? sh[lane] : 0ull;
-    unsigned long long wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    if (lane < kWarps) sh[kWarps + lane] = wi - w;
-    if (lane == kWarps - 1) sh[2 * kWarps] = wi;
-  }
-  __syncthreads();
-  const unsigned long long excl = sh[kWarps + warp] + (incl - v);
-  *total = sh[2 * kWarps];
-  __syncthreads();
-  return excl;
-}
-
 // ---------------------------------------------------------------------------
-// Per-request decision (sampling), run by the whole CTA that completed the
-// request's last A item.
+// Per-request decision (sampling), run by one warp: the one that completed
+// the request's last A item.
 // ---------------------------------------------------------------------------
 template <int EB>
 __device__ __noinline__ void decide_sample(const Params& P, int b) {
-  __shared__ float s_m[2 * SV_MAX_GAMMA + 1];
-  __shared__ double s_s[2 * SV_MAX_GAMMA + 1];
   const int G = P.G, V = P.V, NC = P.NC;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int gb = clamp_gamma(P.gamma[b], G);
   unsigned int flags = (P.gamma[b] != gb) ? SV_STATUS_BAD_GAMMA : 0u;
   const float T = sanitize_temperature(P.temperature[b], flags);
   const TempC tc = temp_consts(T);
   const double cd = (double)tc.hi + (double)tc.lo;
   const int nrows = 2 * gb + 1;
-  const int nparts = NC * kWarps;
 
-  // Row maximum M and normaliser S = sum_w s_w 2^((m_w - M) c) over the
-  // per-warp partials, combined in float64.
-  for (int r = warp; r < nrows; r += kWarps) {
-    const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
-    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc * kWarps;
-    float M = -INFINITY;
-    for (int j = lane; j < nparts; j += 32) M = fmaxf(M, __ldcg(&pr[j]).x);
-    M = warp_max(M);
-    double S = 0.0;
-    if (M > -INFINITY) {
-      for (int j = lane; j < nparts; j += 32) {
-        const float2 ms = __ldcg(&pr[j]);
-        if (ms.x > -INFINITY) S += (double)ms.y * (double)ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo));
-      }
+  // Row maximum M and normaliser S = sum_c s_c 2^((m_c - M) c) over the
+  // per-item partials, in float64.  Lane (r & 31) keeps row r in slot r >> 5.
+  // Four rows at a time, each lane loading chunks lane and lane + 32, so the
+  // loads of a group are in flight together.
+  float rowM[2] = {-INFINITY, -INFINITY};
+  double rowS[2] = {0.0, 0.0};
+  const float2 none = make_float2(-INFINITY, 0.0f);
+  for (int r0 = 0; r0 < nrows; r0 += 4) {
+    float2 v[4][2];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int r = r0 + g;
+      const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
+      const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc;
+      v[g][0] = (r < nrows && lane < NC) ? __ldcg(&pr[lane]) : none;
+      v[g][1] = (r < nrows && lane + 32 < NC) ? __ldcg(&pr[lane + 32]) : none;
     }
-    S = warp_sum_d(S);
-    if (lane == 0) {
-      s_m[r] = M;
-      s_s[r] = S;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int r = r0 + g;
+      if (r >= nrows) break;
+      const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
+      const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc;
+      float M = fmaxf(v[g][0].x, v[g][1].x);
+      for (int c = lane + 64; c < NC; c += 32) M = fmaxf(M, __ldcg(&pr[c]).x);
+      M = warp_max(M);
+      double S = 0.0;
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (v[g][h].x > -INFINITY)
+            S += (double)v[g][h].y * (double)ex2_approx(exp_arg(v[g][h].x, M, tc.hi, tc.lo));
+        for (int c = lane + 64; c < NC; c += 32) {
+          const float2 ms = __ldcg(&pr[c]);
+          if (ms.x > -INFINITY) S += (double)ms.y * (double)ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo));
+        }
+      }
+      S = warp_sum_d(S);
       if (!isfinite(M) || !(S > 0.0)) flags |= SV_STATUS_NONFINITE_ROW;
-    }
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    const int i = lane;
-    bool reject = false;
-    double p = NAN, q = NAN;
-    int x = 0;
-    if (i < gb) {
-      x = P.tokens[(size_t)b * G + i];
-      if (x < 0 || x >= V) {
-        flags |= SV_STATUS_BAD_TOKEN;
-        x = x < 0 ? 0 : V - 1;
+      if (lane == (r & 31)) {
+        rowM[r >> 5] = M;
+        rowS[r >> 5] = S;
       }
-      const float zt = load_elem<EB>(P.target, target_row(b, i, G, V) + (size_t)x);
-      const float zd = load_elem<EB>(P.draft, draft_row(b, i, G, V) + (size_t)x);
-      p = exp2(((double)zt - (double)s_m[i]) * cd) / s_s[i];
-      q = exp2(((double)zd - (double)s_m[gb + 1 + i]) * cd) / s_s[gb + 1 + i];
-      const double u = (double)sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + i], flags);
-      reject = !((q == 0.0) || (u < p / q));
-    }
-    const unsigned int rej = __ballot_sync(0xffffffffu, reject);
-    const int k = rej ? (__ffs(rej) - 1) : gb;
-    if (i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
-    if (i < G) {
-      const bool evaluated = i < gb && i <= k;
-      if (P.p_tok) P.p_tok[(size_t)b * G + i] = evaluated ? p : NAN;
-      if (P.q_tok) P.q_tok[(size_t)b * G + i] = evaluated ? q : NAN;
-    }
-    const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
-    if (i == 0) {
-      P.num_accepted[b] = k;
-      Decision d;
-      d.k = k;
-      d.reject = k < gb ? 1 : 0;
-      d.mt = s_m[k];
-      d.md = d.reject ? s_m[gb + 1 + k] : 0.0f;
-      d.inv_st = (float)(1.0 / s_s[k]);
-      d.rho = d.reject ? (float)(s_s[k] / s_s[gb + 1 + k]) : 0.0f;
-      d.c_hi = tc.hi;
-      d.c_lo = tc.lo;
-      P.dec[b] = d;
-      if (any) atomicOr(P.status, any);
-      P.cnt_a[b] = 0;
-      __threadfence();
-      atomicExch(&P.ready[b], 1u);
     }
   }
-  __syncthreads();
+  // row r's statistics, fetched from lane r & 31
+  auto row_m = [&](int r) {
+    const float a = __shfl_sync(0xffffffffu, rowM[0], r & 31);
+    const float c = __shfl_sync(0xffffffffu, rowM[1], r & 31);
+    return r < 32 ? a : c;
+  };
+  auto row_s = [&](int r) {
+    const double a = __shfl_sync(0xffffffffu, rowS[0], r & 31);
+    const double c = __shfl_sync(0xffffffffu, rowS[1], r & 31);
+    return r < 32 ? a : c;
+  };
+
+  // Acceptance test per position (lane i), then the first-reject ballot.
+  const int i = lane;
+  const int ri = i < gb ? i : 0;
+  const float mt_i = row_m(ri), md_i = row_m(gb + 1 + ri);
+  const double st_i = row_s(ri), sd_i = row_s(gb + 1 + ri);
+  bool reject = false;
+  double p = NAN, q = NAN;
+  int x = 0;
+  if (i < gb) {
+    x = P.tokens[(size_t)b * G + i];
+    if (x < 0 || x >= V) {
+      flags |= SV_STATUS_BAD_TOKEN;
+      x = x < 0 ? 0 : V - 1;
+    }
+    const float zt = load_elem<EB>(P.target, target_row(b, i, G, V) + (size_t)x);
+    const float zd = load_elem<EB>(P.draft, draft_row(b, i, G, V) + (size_t)x);
+    p = exp2(((double)zt - (double)mt_i) * cd) / st_i;
+    q = exp2(((double)zd - (double)md_i) * cd) / sd_i;
+    const double u = (double)sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + i], flags);
+    reject = !((q == 0.0) || (u < p / q));
+  }
+  const unsigned int rej = __ballot_sync(0xffffffffu, reject);
+  const int k = rej ? (__ffs(rej) - 1) : gb;
+  const float mt_k = row_m(k);
+  const double st_k = row_s(k);
+  const int kd = gb + 1 + (k < gb ? k : 0);
+  const float md_k = row_m(kd);
+  const double sd_k = row_s(kd);
+  if (i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
+  if (i < G) {
+    const bool evaluated = i < gb && i <= k;
+    if (P.p_tok) P.p_tok[(size_t)b * G + i] = evaluated ? p : NAN;
+    if (P.q_tok) P.q_tok[(size_t)b * G + i] = evaluated ? q : NAN;
+  }
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0) {
+    P.num_accepted[b] = k;
+    Decision d;
+    d.k = k;
+    d.reject = k < gb ? 1 : 0;
+    d.mt = mt_k;
+    d.md = d.reject ? md_k : 0.0f;
+    d.inv_st = (float)(1.0 / st_k);
+    d.rho = d.reject ? (float)(st_k / sd_k) : 0.0f;
+    d.c_hi = tc.hi;
+    d.c_lo = tc.lo;
+    P.dec[b] = d;
+    if (any) atomicOr(P.status, any);
+    P.cnt_a[b] = 0;
+    // publish the decision
+    __threadfence();
+    st_release(&P.ready[b], 1u);
+  }
+  __syncwarp();
 }
 
-// Greedy decision: argmax per target row from the per-warp partials, then the
+// Greedy decision: argmax per target row from the per-item partials, then the
 // first mismatch by warp ballot.
 __device__ __noinline__ void decide_greedy(const Params& P, int b) {
-  __shared__ int s_g[SV_MAX_GAMMA + 1];
   const int G = P.G, V = P.V, NC = P.NC;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int gb = clamp_gamma(P.gamma[b], G);
   unsigned int flags = (P.gamma[b] != gb) ? SV_STATUS_BAD_GAMMA : 0u;
-  const int nparts = NC * kWarps;
-  for (int r = warp; r <= gb; r += kWarps) {
-    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + r) * P.stride_nc * kWarps;
+  int g_mine = 0;  // lane r holds the argmax of row r
+  for (int r = 0; r <= gb; ++r) {
+    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + r) * P.stride_nc;
     float v = -INFINITY;
     int idx = 0x7fffffff;
-    for (int j = lane; j < nparts; j += 32) {
-      const float2 mi = __ldcg(&pr[j]);
+    for (int c = lane; c < NC; c += 32) {
+      const float2 mi = __ldcg(&pr[c]);
       argmax_combine(v, idx, mi.x, __float_as_int(mi.y));
     }
     warp_argmax(v, idx);
-    if (lane == 0) {
-      if (!isfinite(v)) flags |= SV_STATUS_NONFINITE_ROW;
-      s_g[r] = (idx >= 0 && idx < V) ? idx : 0;
-    }
+    if (!isfinite(v)) flags |= SV_STATUS_NONFINITE_ROW;
+    if (lane == r) g_mine = (idx >= 0 && idx < V) ? idx : 0;
   }
-  __syncthreads();
-  if (warp == 0) {
-    const int i = lane;
-    int x = 0;
-    bool mismatch = false;
-    if (i < gb) {
-      x = P.tokens[(size_t)b * G + i];
-      if (x < 0 || x >= V) flags |= SV_STATUS_BAD_TOKEN;
-      mismatch = x != s_g[i];
-    }
-    const unsigned int mm = __ballot_sync(0xffffffffu, mismatch);
-    const int k = mm ? (__ffs(mm) - 1) : gb;
-    if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? s_g[k] : -1);
-    const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
-    if (i == 0) {
-      P.num_accepted[b] = k;
-      if (any) atomicOr(P.status, any);
-      P.cnt_a[b] = 0;
-    }
+  const int i = lane;
+  int x = 0;
+  bool mismatch = false;
+  if (i < gb) {
+    x = P.tokens[(size_t)b * G + i];
+    if (x < 0 || x >= V) flags |= SV_STATUS_BAD_TOKEN;
+    mismatch = x != g_mine;
   }
-  __syncthreads();
+  const unsigned int mm = __ballot_sync(0xffffffffu, mismatch);
+  const int k = mm ? (__ffs(mm) - 1) : gb;
+  const int gk = __shfl_sync(0xffffffffu, g_mine, k);
+  if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? gk : -1);
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0) {
+    P.num_accepted[b] = k;
+    if (any) atomicOr(P.status, any);
+    P.cnt_a[b] = 0;
+  }
+  __syncwarp();
 }
 
-// Final draw for request b, run by the whole CTA that completed its last R item.
+// Final draw for request b, run by the warp that completed its last R item:
+// the chunk whose prefix passes u*S, then a scan of that chunk only.
 template <int EB>
 __device__ __noinline__ void final_draw(const Params& P, int b) {
-  __shared__ unsigned long long sh_scan[2 * kWarps + 1];
-  __shared__ int sh_chunk, sh_usep, sh_tok;
-  __shared__ unsigned long long sh_base, sh_target;
-  constexpr int RE = kHalfBytes / EB;          // elements per R chunk
-  constexpr int EPT = RE / kThreads;           // elements per thread in the scan
+  constexpr int RE = kHalfBytes / EB;  // elements per R chunk
+  constexpr int EPL = RE / 32;         // contiguous elements per lane in the scan
   const int G = P.G, V = P.V, NCR = P.NCR;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const Decision d = load_decision(&P.dec[b]);
   unsigned int flags = 0;
   const float u_s = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + G], flags);
   const ulonglong2* rp = P.resid + (size_t)b * P.stride_ncr;
 
-  if (warp == 0) {
-    unsigned long long tr = 0, tp = 0;
-    for (int c = lane; c < NCR; c += 32) {
-      const ulonglong2 w = __ldcg(&rp[c]);
-      tr += w.x;
-      tp += w.y;
-    }
-    tr = warp_sum_u64(tr);
-    tp = warp_sum_u64(tp);
-    const int usep = (tr == 0ull);  // residual vanished: draw from p_k
-    const unsigned long long S = usep ? tp : tr;
-    const unsigned long long target = scaled_target(u_s, S);
-    unsigned long long carry = 0, base = 0;
-    int found = -1;
-    for (int c0 = 0; c0 < NCR && found < 0; c0 += 32) {
-      const int c = c0 + lane;
-      unsigned long long w = 0;
-      if (c < NCR) {
-        const ulonglong2 ww = __ldcg(&rp[c]);
-        w = usep ? ww.y : ww.x;
-      }
-      unsigned long long incl = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned int hit = __ballot_sync(0xffffffffu, c < NCR && carry + incl > target);
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        found = c0 + l;
-        base = carry + __shfl_sync(0xffffffffu, incl - w, l);
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      sh_chunk = found;
-      sh_usep = usep;
-      sh_base = base;
-      sh_target = target;
-      sh_tok = -1;
-    }
+  unsigned long long tr = 0, tp = 0;
+  for (int c = lane; c < NCR; c += 32) {
+    const ulonglong2 w = __ldcg(&rp[c]);
+    tr += w.x;
+    tp += w.y;
   }
-  __syncthreads();
-  const int cs = sh_chunk;
+  tr = warp_sum_u64(tr);
+  tp = warp_sum_u64(tp);
+  const int usep = (tr == 0ull);  // residual vanished: draw from p_k
+  const unsigned long long S = usep ? tp : tr;
+  const unsigned long long target = scaled_target(u_s, S);
+  unsigned long long carry = 0, base = 0;
+  int cs = -1;
+  for (int c0 = 0; c0 < NCR && cs < 0; c0 += 32) {
+    const int c = c0 + lane;
+    unsigned long long w = 0;
+    if (c < NCR) {
+      const ulonglong2 ww = __ldcg(&rp[c]);
+      w = usep ? ww.y : ww.x;
+    }
+    const unsigned long long incl = warp_incl_scan_u64(w);
+    const unsigned int hit = __ballot_sync(0xffffffffu, c < NCR && carry + incl > target);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      cs = c0 + l;
+      base = carry + __shfl_sync(0xffffffffu, incl - w, l);
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
+  int tok = -1;
   if (cs >= 0) {
     ResidC kc;
     kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
-    kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = d.reject;
-    const char* trow = P.target + target_row(b, d.k, G, V) * EB;
-    const char* drow = d.reject ? P.draft + draft_row(b, d.k, G, V) * EB : nullptr;
-    const int e0 = (int)threadIdx.x * EPT;
-    const int usep = sh_usep;
-    // weight of element j of this thread's run (recomputed, bit-identical)
-    auto weight = [&](int j) -> unsigned long long {
-      const size_t e = (size_t)cs * RE + (size_t)(e0 + j);
-      unsigned long long wr = 0, wp = 0;
-      if (e < (size_t)V) {
-        const float zt = load_elem<EB>(trow, e);
-        const float zd = drow ? load_elem<EB>(drow, e) : -INFINITY;
-        resid_weights(zt, zd, kc, wr, wp);
+    kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
+    const char* trow = P.target + target_row(b, k, G, V) * EB;
+    const char* drow = kc.reject ? P.draft + draft_row(b, k, G, V) * EB : nullptr;
+    // This lane's EPL contiguous logits of the chosen chunk (16-byte loads
+    // when the rows allow it; -inf past the end of the row).
+    constexpr int NV = EPL * EB / 16;  // 8 vectors per lane
+    const size_t e0 = (size_t)cs * RE + (size_t)lane * EPL;
+    uint4 tv[NV], dv[NV];
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(trow) |
+                          reinterpret_cast<uintptr_t>(drow)) & 15) == 0 &&
+                        e0 + EPL <= (size_t)V;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      if (vec_ok) {
+        tv[q] = __ldcg(reinterpret_cast<const uint4*>(trow + (e0 + (size_t)q * (16 / EB)) * EB));
+        dv[q] = drow ? __ldcg(reinterpret_cast<const uint4*>(drow + (e0 + (size_t)q * (16 / EB)) * EB))
+                     : neg_inf_vec(EB);
+      } else {
+        uint32_t wt[4], wd[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          if (EB == 2) {
+            const size_t ea = e0 + (size_t)q * 8 + 2 * h, eb = ea + 1;
+            const uint32_t ta = ea < (size_t)V ? reinterpret_cast<const unsigned short*>(trow)[ea] : 0xff80u;
+            const uint32_t tb = eb < (size_t)V ? reinterpret_cast<const unsigned short*>(trow)[eb] : 0xff80u;
+            const uint32_t da = (drow && ea < (size_t)V) ? reinterpret_cast<const unsigned short*>(drow)[ea] : 0xff80u;
+            const uint32_t db = (drow && eb < (size_t)V) ? reinterpret_cast<const unsigned short*>(drow)[eb] : 0xff80u;
+            wt[h] = ta | (tb << 16);
+            wd[h] = da | (db << 16);
+          } else {
+            const size_t e = e0 + (size_t)q * 4 + h;
+            wt[h] = e < (size_t)V ? __float_as_uint(reinterpret_cast<const float*>(trow)[e]) : 0xff800000u;
+            wd[h] = (drow && e < (size_t)V) ? __float_as_uint(reinterpret_cast<const float*>(drow)[e])
+                                            : 0xff800000u;
+          }
+        }
+        tv[q] = make_uint4(wt[0], wt[1], wt[2], wt[3]);
+        dv[q] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
+    }
+    auto weight = [&](int j) -> unsigned long long {
+      unsigned long long wr, wp;
+      resid_weights(vec_elem<EB>(tv[j / (16 / EB)], j % (16 / EB)),
+                    vec_elem<EB>(dv[j / (16 / EB)], j % (16 / EB)), kc, wr, wp);
       return usep ? wp : wr;
     };
-    unsigned long long tsum = 0;
-#pragma unroll 4
-    for (int j = 0; j < EPT; ++j) tsum += weight(j);
-    unsigned long long total;
-    const unsigned long long excl = block_exclusive_scan(tsum, sh_scan, &total);
-    const unsigned long long target = sh_target;
-    unsigned long long run = sh_base + excl;
-    if (run <= target && run + tsum > target) {
-      for (int j = 0; j < EPT; ++j) {
+    unsigned long long lsum = 0;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) lsum += weight(j);
+    const unsigned long long incl = warp_incl_scan_u64(lsum);
+    unsigned long long run = base + incl - lsum;
+    if (run <= target && run + lsum > target) {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
         const unsigned long long nxt = run + weight(j);
-        if (run <= target && nxt > target) {
-          sh_tok = cs * RE + e0 + j;
-          break;
-        }
+        if (tok < 0 && nxt > target) tok = (int)(e0 + (size_t)j);
         run = nxt;
       }
     }
+    const unsigned int own = __ballot_sync(0xffffffffu, tok >= 0);
+    tok = own ? __shfl_sync(0xffffffffu, tok, __ffs(own) - 1) : -1;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int tok = sh_tok;
+  if (lane == 0) {
     if (tok < 0) {
       flags |= SV_STATUS_INTERNAL;
       tok = V - 1;
     }
-    P.out_tokens[(size_t)b * (G + 1) + d.k] = tok;
+    P.out_tokens[(size_t)b * (G + 1) + k] = tok;
     if (flags) atomicOr(P.status, flags);
     P.cnt_r[b] = 0;
-    P.ready[b] = 0;
+    P.ready[b] = 0;  // every R item of b is done: nobody reads the flag again
   }
-  __syncthreads();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// Work-item order and decoding (thread 0)
+// Item processing (one warp per item)
 // ---------------------------------------------------------------------------
+// Element e of the item's row half h (0: p0, 1: p1) from global memory
+// (unaligned items, which are not copied into the stage).
+template <int EB>
+__device__ __forceinline__ float direct_elem(const Meta& m, int h, int e) {
+  return load_elem<EB>(h ? m.p1 : m.p0, (size_t)e);
+}
+
+
+// A item, sampling: (max, sum of exp2) over the item.
+template <int EB>
+__device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage) {
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = kItemBytes / 16 / 32;  // vectors per lane (16)
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY, sum = 0.0f;
+  if (!m.direct) {
+    // two passes over the stage: the maximum, then the exponentials
+    const int nvec = m.n / VEC;  // n * EB is a multiple of 16 on this path
+    uint4 v[NV];  // one pass over the stage; the item stays in registers
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int vi = lane + 32 * j;
+      v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+    }
+    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) mq[q & 3] = fmaxf(mq[q & 3], vec_elem<EB>(v[j], q));
+    mx = warp_max(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
+    if (mx > -INFINITY) {
+      float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        float e[VEC];
+#pragma unroll
+        for (int q = 0; q < VEC; ++q)
+          e[q] = ex2_approx(exp_arg(vec_elem<EB>(v[j], q), mx, m.c_hi, m.c_lo));
+#pragma unroll
+        for (int w = VEC; w > 1; w >>= 1)
+#pragma unroll
+          for (int q = 0; q < w / 2; ++q) e[q] = e[2 * q] + e[2 * q + 1];
+        sq[j & 3] += e[0];
+      }
+      sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+    }
+  } else {
+    for (int e = lane; e < m.n; e += 32) mx = fmaxf(mx, direct_elem<EB>(m, 0, e));
+    mx = warp_max(mx);
+    if (mx > -INFINITY)
+      for (int e = lane; e < m.n; e += 32)
+        sum += ex2_approx(exp_arg(direct_elem<EB>(m, 0, e), mx, m.c_hi, m.c_lo));
+  }
+  sum = warp_sum(sum);
+  return make_float2(mx, sum);
+}
+
+// A item, greedy: (max, lowest row-global index of the max).
+template <int EB>
+__device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage) {
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = kItemBytes / 16 / 32;
+  constexpr int AE = kItemBytes / EB;
+  const int lane = threadIdx.x & 31;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  if (!m.direct) {
+    // the maximum (independent chains), then the lowest index holding it
+    const int nvec = m.n / VEC;
+    uint4 v[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int vi = lane + 32 * j;
+      v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+    }
+    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) mq[q & 3] = fmaxf(mq[q & 3], vec_elem<EB>(v[j], q));
+    bv = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+    // this lane's elements in increasing index order: vector j, element q
+#pragma unroll
+    for (int j = NV - 1; j >= 0; --j)
+#pragma unroll
+      for (int q = VEC - 1; q >= 0; --q) {
+        const int vi = lane + 32 * j;
+        if (vi < nvec && vec_elem<EB>(v[j], q) == bv) bi = vi * VEC + q;
+      }
+  } else {
+    for (int e = lane; e < m.n; e += 32) argmax_combine(bv, bi, direct_elem<EB>(m, 0, e), e);
+  }
+  warp_argmax(bv, bi);
+  return make_float2(bv, __int_as_float(bi == 0x7fffffff ? bi : m.c * AE + bi));
+}
+
+// R item: fixed-point sums of the residual weights and of p over the chunk.
+template <int EB>
+__device__ __forceinline__ ulonglong2 r_item(const Meta& m, const char* stage) {
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = kHalfBytes / 16 / 32;  // vectors per lane per row (8)
+  const int lane = threadIdx.x & 31;
+  ResidC kc;
+  kc.mt = m.mt; kc.md = m.md; kc.inv_st = m.inv_st; kc.rho = m.rho;
+  kc.hi = m.c_hi; kc.lo = m.c_lo; kc.reject = m.reject;
+  unsigned long long sr = 0, sp = 0;
+  if (!m.direct) {
+    const int nvec = m.n / VEC;
+    unsigned long long ar[2] = {0, 0}, ap[2] = {0, 0};  // independent chains
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int vi = lane + 32 * j;
+      if (vi < nvec) {
+        const uint4 t = lds128(stage + vi * 16);
+        const uint4 d = m.reject ? lds128(stage + kHalfBytes + vi * 16) : neg_inf_vec(EB);
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) {
+          unsigned long long wr, wp;
+          resid_weights(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc, wr, wp);
+          ar[q & 1] += wr;
+          ap[q & 1] += wp;
+        }
+      }
+    }
+    sr = ar[0] + ar[1];
+    sp = ap[0] + ap[1];
+  } else {
+    for (int e = lane; e < m.n; e += 32) {
+      unsigned long long wr, wp;
+      const float zd = m.reject ? direct_elem<EB>(m, 1, e) : -INFINITY;
+      resid_weights(direct_elem<EB>(m, 0, e), zd, kc, wr, wp);
+      sr += wr;
+      sp += wp;
+    }
+  }
+  return make_ulonglong2(warp_sum_u64(sr), warp_sum_u64(sp));
+}
+
+// ---------------------------------------------------------------------------
+// Work items: one fixed order, claimed in small batches
+// ---------------------------------------------------------------------------
+// Segment k of the order holds the A items of request k (rows, then chunks)
+// followed by the R items of request k - L; the R items of the last L
+// requests form a tail.  The lag L places a request's R items after its
+// decision while its rows are still in L2.
 struct Sched {
   const int* rowpre;  // [B+1] exclusive prefix of rows per request (shared memory)
-  int B, L, NC, NCR;
-  int mode;
+  int B, L, NC, NCR;  // NCR = 0 in greedy mode
   unsigned int total;
 };
 
@@ -642,224 +830,113 @@ __device__ __forceinline__ unsigned int seg_start(const Sched& s, int k) {
   return (unsigned int)s.rowpre[k] * s.NC + (r > 0 ? (unsigned int)r * s.NCR : 0u);
 }
 
-// Fill `out` for item j.  For R items whose request has not been decided
-// yet, returns KIND_RWAIT (nothing is read from the decision).
-template <int EB>
-__device__ __noinline__ void decode_item(const Params& P, const Sched& s, unsigned int j, Slot& out,
-                            int& kcache) {
-  if (j >= s.total) {
-    out.kind = KIND_EXIT;
-    return;
-  }
-  int req = -1, c = 0;
-  bool is_r = false;
-  if (s.mode == MODE_SAMPLE && j >= seg_start(s, s.B)) {
+// Decode item j.  A items come back complete; R items carry only their
+// request and chunk (their rows depend on the request's decision).
+template <int EB, int MODE>
+__device__ void decode_item(const Params& P, const Sched& s, unsigned int j, Meta& m) {
+  constexpr int AE = kItemBytes / EB;
+  if (MODE == MODE_SAMPLE && j >= seg_start(s, s.B)) {
     const unsigned int t = j - seg_start(s, s.B);
-    req = (s.B > s.L ? s.B - s.L : 0) + (int)(t / s.NCR);
-    c = (int)(t % s.NCR);
-    is_r = true;
-  } else {
-    // largest k with seg_start(k) <= j, searching up from the last answer
-    int lo = kcache, hi = s.B - 1;
-    if (seg_start(s, lo) > j) lo = 0;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (seg_start(s, mid) <= j) lo = mid; else hi = mid - 1;
-    }
-    kcache = lo;
-    const unsigned int off = j - seg_start(s, lo);
-    const unsigned int na = (unsigned int)(s.rowpre[lo + 1] - s.rowpre[lo]) * s.NC;
-    if (off < na) {
-      const int G = P.G, V = P.V;
-      const int row = (int)(off / s.NC);
-      c = (int)(off % s.NC);
-      const int gb = (s.mode == MODE_SAMPLE) ? (s.rowpre[lo + 1] - s.rowpre[lo] - 1) / 2
-                                             : (s.rowpre[lo + 1] - s.rowpre[lo] - 1);
-      size_t roff;
-      if (row <= gb) {
-        out.pslot = row;
-        roff = target_row(lo, row, G, V);
-      } else {
-        const int i = row - gb - 1;
-        out.pslot = G + 1 + i;
-        roff = draft_row(lo, i, G, V);
-      }
-      constexpr int AE = kTileBytes / EB;
-      const char* base = row <= gb ? P.target : P.draft;
-      out.kind = KIND_A;
-      out.b = lo;
-      out.c = c;
-      out.n = min(AE, V - c * AE);
-      out.p0 = base + (roff + (size_t)c * AE) * EB;
-      out.p1 = nullptr;
-      out.aligned = (reinterpret_cast<uintptr_t>(out.p0) & 15) == 0;
-      if (s.mode == MODE_SAMPLE) {
-        unsigned int fl = 0;
-        const TempC tc = temp_consts(sanitize_temperature(P.temperature[lo], fl));
-        out.c_hi = tc.hi;
-        out.c_lo = tc.lo;
-      }
-      return;
-    }
-    req = lo - s.L;
-    c = (int)(off - na);
-    is_r = true;
-  }
-  (void)is_r;
-  out.b = req;
-  out.c = c;
-  if (!ld_acquire(&P.ready[req])) {
-    out.kind = KIND_RWAIT;
+    m.kind = KIND_R;
+    m.b = (s.B > s.L ? s.B - s.L : 0) + (int)(t / s.NCR);
+    m.c = (int)(t % s.NCR);
     return;
   }
-  // decision published: read it and build the R item
-  const Decision d = load_decision(&P.dec[req]);
+  int lo = 0, hi = s.B - 1;  // largest k with seg_start(k) <= j
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (seg_start(s, mid) <= j) lo = mid; else hi = mid - 1;
+  }
+  const unsigned int off = j - seg_start(s, lo);
+  const int rows = s.rowpre[lo + 1] - s.rowpre[lo];
+  const unsigned int na = (unsigned int)rows * s.NC;
+  if (off >= na) {
+    m.kind = KIND_R;
+    m.b = lo - s.L;
+    m.c = (int)(off - na);
+    return;
+  }
   const int G = P.G, V = P.V;
+  const int row = (int)(off / s.NC);
+  const int c = (int)(off % s.NC);
+  const int gb = MODE == MODE_SAMPLE ? (rows - 1) / 2 : rows - 1;
+  size_t roff;
+  const char* base;
+  if (row <= gb) {
+    m.pslot = row;
+    roff = target_row(lo, row, G, V);
+    base = P.target;
+  } else {
+    const int i = row - gb - 1;
+    m.pslot = G + 1 + i;
+    roff = draft_row(lo, i, G, V);
+    base = P.draft;
+  }
+  m.kind = KIND_A;
+  m.b = lo;
+  m.c = c;
+  m.n = min(AE, V - c * AE);
+  m.p0 = base + (roff + (size_t)c * AE) * EB;
+  m.p1 = nullptr;
+  m.direct = (((reinterpret_cast<uintptr_t>(m.p0)) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+  if (MODE == MODE_SAMPLE) {
+    unsigned int fl = 0;
+    const TempC tc = temp_consts(sanitize_temperature(P.temperature[lo], fl));
+    m.c_hi = tc.hi;
+    m.c_lo = tc.lo;
+  }
+}
+
+// Complete R item m (request m.b, chunk m.c) from its request's decision.
+template <int EB>
+__device__ __forceinline__ void fill_r_item(const Params& P, const Decision& d, Meta& m) {
+  constexpr int RE = kHalfBytes / EB;
+  const int G = P.G, V = P.V, req = m.b, c = m.c;
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   const int reject = (d.reject && k < G) ? 1 : 0;
-  constexpr int RE = kHalfBytes / EB;
-  out.kind = KIND_R;
-  out.pslot = k;
-  out.reject = reject;
-  out.n = min(RE, V - c * RE);
-  out.p0 = P.target + (target_row(req, k, G, V) + (size_t)c * RE) * EB;
-  out.p1 = reject ? P.draft + (draft_row(req, k, G, V) + (size_t)c * RE) * EB : nullptr;
-  out.aligned = ((reinterpret_cast<uintptr_t>(out.p0) | reinterpret_cast<uintptr_t>(out.p1)) & 15) == 0;
-  out.mt = d.mt;
-  out.md = d.md;
-  out.inv_st = d.inv_st;
-  out.rho = d.rho;
-  out.c_hi = d.c_hi;
-  out.c_lo = d.c_lo;
+  m.pslot = k;
+  m.reject = reject;
+  m.n = min(RE, V - c * RE);
+  m.p0 = P.target + (target_row(req, k, G, V) + (size_t)c * RE) * EB;
+  m.p1 = reject ? P.draft + (draft_row(req, k, G, V) + (size_t)c * RE) * EB : nullptr;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
+  m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+  m.mt = d.mt;
+  m.md = d.md;
+  m.inv_st = d.inv_st;
+  m.rho = d.rho;
+  m.c_hi = d.c_hi;
+  m.c_lo = d.c_lo;
 }
 
 // ---------------------------------------------------------------------------
-// Item compute
+// The kernel
 // ---------------------------------------------------------------------------
-template <int EB>
-__device__ __forceinline__ void issue_loads(const Slot& s, uint4 (&buf)[kVecA]) {
-  if (s.kind == KIND_A) {
-    load_tile<EB, kVecA>(buf, s.p0, s.n, s.aligned);
-  } else if (s.kind == KIND_R) {
-    load_tile<EB, kVecA / 2>(buf, s.p0, s.n, s.aligned);
-    if (s.p1) load_tile<EB, kVecA / 2>(buf + kVecA / 2, s.p1, s.n, s.aligned);
-    else fill_neg_inf(buf + kVecA / 2, kVecA / 2, EB);
-  }
-}
-
 template <int EB, int MODE>
-__device__ __forceinline__ void compute_a(const Params& P, const Slot& s,
-                                          const uint4 (&buf)[kVecA]) {
-  constexpr int VEC = 16 / EB;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float2* part = P.stats + (((size_t)s.b * (2 * P.G + 1) + s.pslot) * P.stride_nc + s.c) * kWarps + warp;
-  if (MODE == MODE_SAMPLE) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kVecA; ++k)
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) m = fmaxf(m, vec_elem<EB>(buf[k], j));
-    m = warp_max(m);
-    float sum = 0.0f;
-    if (m > -INFINITY) {
-#pragma unroll
-      for (int k = 0; k < kVecA; ++k) {
-        float e[VEC];
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) e[j] = ex2_approx(exp_arg(vec_elem<EB>(buf[k], j), m, s.c_hi, s.c_lo));
-#pragma unroll
-        for (int w = VEC; w > 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w / 2; ++j) e[j] = e[2 * j] + e[2 * j + 1];
-        sum += e[0];
-      }
-    }
-    sum = warp_sum(sum);
-    if (lane == 0) {
-      *part = make_float2(m, sum);
-      __threadfence();
-    }
-  } else {
-    constexpr int AE = kTileBytes / EB;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int k = 0; k < kVecA; ++k)
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const int e = ((int)threadIdx.x + k * kThreads) * VEC + j;
-        argmax_combine(bv, bi, vec_elem<EB>(buf[k], j), s.c * AE + e);
-      }
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      *part = make_float2(bv, __int_as_float(bi));
-      __threadfence();
-    }
-  }
-}
-
-template <int EB>
-__device__ __forceinline__ void compute_r(const Slot& s, const uint4 (&buf)[kVecA],
-                                          unsigned long long* sh_r, unsigned long long* sh_p) {
-  constexpr int VEC = 16 / EB;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  ResidC kc;
-  kc.mt = s.mt; kc.md = s.md; kc.inv_st = s.inv_st; kc.rho = s.rho;
-  kc.hi = s.c_hi; kc.lo = s.c_lo; kc.reject = s.reject;
-  unsigned long long sr = 0, sp = 0;
-#pragma unroll
-  for (int k = 0; k < kVecA / 2; ++k)
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      unsigned long long wr, wp;
-      resid_weights(vec_elem<EB>(buf[k], j), vec_elem<EB>(buf[kVecA / 2 + k], j), kc, wr, wp);
-      sr += wr;
-      sp += wp;
-    }
-  sr = warp_sum_u64(sr);
-  sp = warp_sum_u64(sp);
-  if (lane == 0) {
-    sh_r[warp] = sr;
-    sh_p[warp] = sp;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// The persistent kernel
-// ---------------------------------------------------------------------------
-struct Pending {  // thread 0's record of the last item's arrival
-  int kind;       // KIND_A / KIND_R / -1 (none)
-  int b;
-  unsigned int old, total;
-};
-
-template <int EB, int MODE>
-__device__ __forceinline__ void run_pending(const Params& P, const int* work) {
-  // work[0] = kind of completed request (-1 none), work[1] = request
-  if (work[0] == KIND_A) {
-    if (MODE == MODE_SAMPLE) decide_sample<EB>(P, work[1]);
-    else decide_greedy(P, work[1]);
-  } else if (work[0] == KIND_R) {
-    final_draw<EB>(P, work[1]);
-  }
-}
-
-template <int EB, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params P) {
-  extern __shared__ int rowpre[];  // [B + 1]
-  __shared__ Slot slots[3];
-  __shared__ int sh_work[2][2];
-  __shared__ unsigned long long sh_r[2][kWarps], sh_p[2][kWarps];
+__global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  int* rowpre = reinterpret_cast<int*>(dsmem + kWarps * kNB * kItemBytes);  // [B+1]
+  __shared__ __align__(8) uint64_t bar[kWarps][kNB];
+  __shared__ Meta meta[kWarps][kNB];   // the item in each buffer
+  __shared__ Meta batchq[kWarps][kMaxK];  // the warp's current batch
+  __shared__ Decision dcache[kWarps];  // the last decision the warp fetched
   __shared__ int sh_carry;
-  const int tid = threadIdx.x;
-  const int G = P.G, B = P.B;
+  __shared__ int wsum[kWarps];
+  __shared__ int sh_last;
 
-  // rows per request -> exclusive prefix in shared memory
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int G = P.G, B = P.B, NC = P.NC;
+
   if (tid == 0) {
     rowpre[0] = 0;
     sh_carry = 0;
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < kNB; ++s) mbar_init(&bar[w][s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // rows per request -> exclusive prefix in shared memory
   for (int base = 0; base < B; base += kThreads) {
     const int b = base + tid;
     int v = 0;
@@ -867,14 +944,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params P) {
       const int gb = clamp_gamma(P.gamma[b], G);
       v = MODE == MODE_SAMPLE ? 2 * gb + 1 : gb + 1;
     }
-    const int lane = tid & 31, warp = tid >> 5;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    __shared__ int wsum[kWarps];
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     int off = sh_carry;
@@ -888,161 +963,185 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params P) {
   Sched sc;
   sc.rowpre = rowpre;
   sc.B = B;
-  sc.NC = P.NC;
+  sc.NC = NC;
   sc.NCR = MODE == MODE_SAMPLE ? P.NCR : 0;
-  sc.mode = MODE;
+  const unsigned int nA = (unsigned int)rowpre[B] * NC;
+  sc.total = nA + (MODE == MODE_SAMPLE ? (unsigned int)B * P.NCR : 0u);
+  const unsigned int nwarps = gridDim.x * kWarps;
+  // batches: about 1/16 of a warp's share, at most 8 items
+  const unsigned int K = min((unsigned int)kMaxK, max(1u, sc.total / (nwarps * 16u)));
   {
-    const unsigned int totalA = (unsigned int)rowpre[B] * P.NC;
-    int L = 1;
-    if (MODE == MODE_SAMPLE) {
-      // keep R items about three grids of items behind their decisions
-      const double per_req = (double)totalA / (double)B;
-      L = (int)ceil(3.0 * gridDim.x / per_req);
-      if (L < 1) L = 1;
-    }
-    sc.L = L;
-    sc.total = totalA + (MODE == MODE_SAMPLE ? (unsigned int)B * P.NCR : 0u);
+    // R items trail their request's A items by about the items in flight
+    const double per_req = (double)nA / (double)(B > 0 ? B : 1);
+    const double inflight = (double)nwarps * (kNB + 2 * K);
+    int L = MODE == MODE_SAMPLE ? (int)ceil(inflight / per_req) : 1;
+    sc.L = L < 1 ? 1 : L;
   }
 
-  uint4 bufX[kVecA], bufY[kVecA];
-  Pending pend;
-  pend.kind = -1;
-  int kcache = 0;
-  unsigned int flags0 = 0;
-  if (tid == 0) {
-    decode_item<EB>(P, sc, atomicAdd(P.next_item, 1u), slots[0], kcache);
-    decode_item<EB>(P, sc, atomicAdd(P.next_item, 1u), slots[1], kcache);
-    sh_work[0][0] = sh_work[1][0] = -1;
-  }
-  __syncthreads();
-  issue_loads<EB>(slots[0], bufX);
+  unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
+  uint64_t* mybar = bar[warp];
+  Meta* mymeta = meta[warp];
 
-  int cur = 0, parity = 0;
-  // One iteration: claim item n+2, prefetch item n+1, compute item n, then
-  // publish item n's arrival (its follow-up work runs one iteration later).
-  auto step = [&](uint4 (&X)[kVecA], uint4 (&Y)[kVecA]) -> bool {
-    Slot& s = slots[cur];
-    if (s.kind == KIND_EXIT) return false;
-    if (s.kind == KIND_RWAIT) {
-      // Finish everything held (the previous item's follow-up) before waiting.
-      if (tid == 0) {
-        int wk = -1;
-        if (pend.kind == KIND_A && pend.old == pend.total - 1) wk = KIND_A;
-        if (pend.kind == KIND_R && pend.old == pend.total - 1) wk = KIND_R;
-        if (wk >= 0) __threadfence();
-        sh_work[parity][0] = wk;
-        sh_work[parity][1] = pend.b;
-        pend.kind = -1;
-      }
-      __syncthreads();
-      run_pending<EB, MODE>(P, sh_work[parity]);
-      if (tid == 0) {
-        unsigned int it = 0;
-        while (!ld_acquire(&P.ready[s.b])) {
-          if (++it > kSpinLimit) {
-            flags0 |= SV_STATUS_TIMEOUT;
-            break;
-          }
-          __nanosleep(256);
-        }
-      }
-      // rebuild the item from the now-published decision
-      if (tid == 0) {
-        if (!(flags0 & SV_STATUS_TIMEOUT)) {
-          const Decision d = load_decision(&P.dec[s.b]);
-          const int V = P.V;
-          const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
-          const int reject = (d.reject && k < G) ? 1 : 0;
-          constexpr int RE = kHalfBytes / EB;
-          s.kind = KIND_R;
-          s.pslot = k;
-          s.reject = reject;
-          s.n = min(RE, V - s.c * RE);
-          s.p0 = P.target + (target_row(s.b, k, G, V) + (size_t)s.c * RE) * EB;
-          s.p1 = reject ? P.draft + (draft_row(s.b, k, G, V) + (size_t)s.c * RE) * EB : nullptr;
-          s.aligned = ((reinterpret_cast<uintptr_t>(s.p0) | reinterpret_cast<uintptr_t>(s.p1)) & 15) == 0;
-          s.mt = d.mt; s.md = d.md; s.inv_st = d.inv_st; s.rho = d.rho;
-          s.c_hi = d.c_hi; s.c_lo = d.c_lo;
-        } else {
-          s.kind = KIND_EXIT;  // give up: the status word reports it
-        }
-      }
-      __syncthreads();
-      if (s.kind == KIND_EXIT) return false;
-      issue_loads<EB>(s, X);
+  unsigned int nb = 0;  // lane 0: start of the pre-claimed next batch
+  if (lane == 0) nb = atomicAdd(P.next_item, K);
+
+  Meta* myq = batchq[warp];
+  int qlen = 0, qhead = 0;
+  bool more = true;  // batches may remain
+  unsigned int issued = 0, processed = 0;
+  int dec_b = -1;  // request whose decision is in dcache[warp] (warp-uniform)
+  int acc_kind = KIND_A, acc_b = 0;
+  unsigned int acc_n = 0;  // arrivals held for (acc_kind, acc_b)
+  unsigned int flags = 0;
+  bool failed = false;
+
+  // Publish held arrivals; the warp completing a request runs its follow-up.
+  auto flush = [&]() {
+    if (acc_n == 0) return;
+    unsigned int last = 0;
+    if (lane == 0) {
+      __threadfence();
+      unsigned int* cnt = acc_kind == KIND_A ? &P.cnt_a[acc_b] : &P.cnt_r[acc_b];
+      const unsigned int total = acc_kind == KIND_A
+          ? (unsigned int)(rowpre[acc_b + 1] - rowpre[acc_b]) * (unsigned int)NC
+          : (unsigned int)P.NCR;
+      last = (atomicAdd(cnt, acc_n) + acc_n == total) ? 1u : 0u;
+      if (last) __threadfence();
     }
-
-    unsigned int ticket = 0;
-    if (tid == 0) ticket = atomicAdd(P.next_item, 1u);
-    Slot& sn = slots[(cur + 1) % 3];
-    issue_loads<EB>(sn, Y);
-
-    if (s.kind == KIND_A) compute_a<EB, MODE>(P, s, X);
-    else compute_r<EB>(s, X, sh_r[parity], sh_p[parity]);
-
-    if (tid == 0) {
-      decode_item<EB>(P, sc, ticket, slots[(cur + 2) % 3], kcache);
-      int wk = -1;
-      if (pend.kind >= 0 && pend.old == pend.total - 1) {
-        wk = pend.kind;
-        __threadfence();
-      }
-      sh_work[parity][0] = wk;
-      sh_work[parity][1] = pend.b;
-      pend.kind = -1;
-    }
-    __syncthreads();
-    run_pending<EB, MODE>(P, sh_work[parity]);
-    if (tid == 0) {
-      if (s.kind == KIND_A) {
-        const int rows = rowpre[s.b + 1] - rowpre[s.b];
-        pend.kind = KIND_A;
-        pend.b = s.b;
-        pend.total = (unsigned int)rows * P.NC;
-        pend.old = atomicAdd(&P.cnt_a[s.b], 1u);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      if (acc_kind == KIND_A) {
+        if (MODE == MODE_SAMPLE) decide_sample<EB>(P, acc_b);
+        else decide_greedy(P, acc_b);
       } else {
-        unsigned long long tr = 0, tp = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          tr += sh_r[parity][w];
-          tp += sh_p[parity][w];
-        }
-        P.resid[(size_t)s.b * P.stride_ncr + s.c] = make_ulonglong2(tr, tp);
-        __threadfence();
-        pend.kind = KIND_R;
-        pend.b = s.b;
-        pend.total = (unsigned int)P.NCR;
-        pend.old = atomicAdd(&P.cnt_r[s.b], 1u);
+        final_draw<EB>(P, acc_b);
       }
     }
-    cur = (cur + 1) % 3;
-    parity ^= 1;
-    return true;
+    acc_n = 0;
   };
 
-  for (;;) {
-    if (!step(bufX, bufY)) break;
-    if (!step(bufY, bufX)) break;
+  while (!failed) {
+    // 1. keep kNB copies in flight
+    while (issued - processed < (unsigned int)kNB) {
+      if (qhead == qlen) {
+        if (!more) break;
+        const unsigned int base = __shfl_sync(0xffffffffu, nb, 0);
+        if (base >= sc.total) {
+          more = false;
+          break;
+        }
+        qlen = (int)min(K, sc.total - base);
+        qhead = 0;
+        if (lane < qlen) decode_item<EB, MODE>(P, sc, base + lane, myq[lane]);
+        if (lane == 0) nb = atomicAdd(P.next_item, K);  // pre-claim the next batch
+        __syncwarp();
+      }
+      Meta& it = myq[qhead];
+      if (MODE == MODE_SAMPLE && it.kind == KIND_R) {
+        const int b = it.b;
+        if (b != dec_b) {
+          unsigned int ok = 0;
+          if (lane == 0 && ld_acquire(&P.ready[b])) {
+            ok = 1;
+            dcache[warp] = load_decision(&P.dec[b]);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            // not decided yet: work off what is in flight first
+            if (issued != processed) break;
+            // Nothing in flight: publish held arrivals, then wait.  Every
+            // item this warp still holds comes later in the order, so the
+            // decision does not depend on it.
+            flush();
+            if (lane == 0) {
+              const unsigned long long t0 = now_ns();
+              while (!ld_acquire(&P.ready[b])) {
+                if (now_ns() - t0 > kWaitNs) {
+                  ok = 2;
+                  break;
+                }
+                __nanosleep(128);
+              }
+              if (ok != 2) dcache[warp] = load_decision(&P.dec[b]);
+            }
+            if (__shfl_sync(0xffffffffu, ok, 0) == 2) {
+              flags |= SV_STATUS_TIMEOUT;
+              failed = true;
+              break;
+            }
+          }
+          dec_b = b;
+        }
+      }
+      // lane 0 completes the item and starts its copy into the next buffer
+      const int s = (int)(issued % kNB);
+      if (lane == 0) {
+        Meta mine = it;
+        if (MODE == MODE_SAMPLE && mine.kind == KIND_R) fill_r_item<EB>(P, dcache[warp], mine);
+        mymeta[s] = mine;
+        unsigned char* dst = mybuf + s * kItemBytes;
+        // order earlier generic reads of this buffer before the async-proxy write
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (mine.direct) {
+          mbar_arrive(&mybar[s]);
+        } else {
+          const unsigned int bytes = (unsigned int)(mine.n * EB);
+          const bool two = mine.kind == KIND_R && mine.p1 != nullptr;
+          mbar_arrive_expect_tx(&mybar[s], two ? 2 * bytes : bytes);
+          bulk_copy_g2s(dst, mine.p0, bytes, &mybar[s]);
+          if (two) bulk_copy_g2s(dst + kHalfBytes, mine.p1, bytes, &mybar[s]);
+        }
+      }
+      __syncwarp();
+      ++qhead;
+      ++issued;
+    }
+    if (failed) break;
+    if (issued == processed) {
+      if (!more && qhead == qlen) break;  // all work done
+      continue;
+    }
+
+    // 2. process the oldest item
+    const int s = (int)(processed % kNB);
+    if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+      flags |= SV_STATUS_TIMEOUT;
+      failed = true;
+      break;
+    }
+    const Meta& m = mymeta[s];
+    const int m_kind = m.kind, m_b = m.b;
+    const char* stage = reinterpret_cast<const char*>(mybuf + s * kItemBytes);
+    if (m_kind == KIND_A) {
+      const float2 part = MODE == MODE_SAMPLE ? a_item_sample<EB>(m, stage)
+                                              : a_item_greedy<EB>(m, stage);
+      if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
+    } else {
+      const ulonglong2 part = r_item<EB>(m, stage);
+      if (lane == 0) P.resid[(size_t)m_b * P.stride_ncr + m.c] = part;
+    }
+    __syncwarp();  // every lane is done with the buffer before it is reused
+    ++processed;
+    if (acc_n && (m_kind != acc_kind || m_b != acc_b)) flush();
+    acc_kind = m_kind;
+    acc_b = m_b;
+    ++acc_n;
   }
 
-  // drain the last item's follow-up, then leave; the last CTA out resets the
-  // shared counters so the workspace is zeroed for the next call
-  if (tid == 0) {
-    int wk = -1;
-    if (pend.kind >= 0 && pend.old == pend.total - 1) {
-      wk = pend.kind;
-      __threadfence();
-    }
-    sh_work[parity][0] = wk;
-    sh_work[parity][1] = pend.b;
+  // No copy may still be landing in this warp's buffers when it leaves.
+  if (failed) {
+    for (unsigned int p = processed; p < issued; ++p)
+      (void)mbar_wait(&mybar[p % kNB], (p / kNB) & 1u);
+  } else {
+    flush();
   }
+  if (lane == 0 && flags) atomicOr(P.status, flags);
   __syncthreads();
-  run_pending<EB, MODE>(P, sh_work[parity]);
+  // the last CTA out resets the claim counter for the next call
   if (tid == 0) {
-    if (flags0) atomicOr(P.status, flags0);
     __threadfence();
-    const unsigned int done = atomicAdd(P.exit_count, 1u);
-    if (done == gridDim.x - 1) {
+    sh_last = atomicAdd(P.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
+    if (sh_last) {
       *P.next_item = 0;
       *P.exit_count = 0;
       __threadfence();
@@ -1061,19 +1160,33 @@ int check_scalars(sv_dtype dtype, int B, int G, int V) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+constexpr size_t kMaxSmem =
+    (size_t)kWarps * kNB * kItemBytes + (size_t)(kMaxBatch + 1) * sizeof(int);
+
+// Persistent grid: as many CTAs as fit on the device (cached per device).
 template <int EB, int MODE>
-int grid_size(size_t smem) {
-  int dev = 0, sms = 0, per_sm = 0;
+int grid_size() {
+  static int cached_dev = -1, cached_grid = 0;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev == cached_dev && cached_grid > 0) return cached_grid;
+  int sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<EB, MODE>, kThreads,
-                                                    smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(verify_kernel<EB, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kMaxSmem) != cudaSuccess)
     return 0;
-  return sms * (per_sm > 0 ? per_sm : 1);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<EB, MODE>, kThreads,
+                                                    kMaxSmem) != cudaSuccess)
+    return 0;
+  cached_dev = dev;
+  cached_grid = sms * (per_sm > 0 ? per_sm : 1);
+  return cached_grid;
 }
 
 template <int EB, int MODE>
-int launch(Params P, const Layout& L, char* ws, cudaStream_t stream) {
+int launch(const Params& P, cudaStream_t stream) {
+  const int grid = grid_size<EB, MODE>();
+  if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch
   const int B = P.B;
   for (int b0 = 0; b0 < B; b0 += kMaxBatch) {
@@ -1094,24 +1207,20 @@ int launch(Params P, const Layout& L, char* ws, cudaStream_t stream) {
     Q.cnt_r = P.cnt_r + b0;
     Q.ready = P.ready + b0;
     Q.dec = P.dec + b0;
-    Q.stats = P.stats + (size_t)b0 * (2 * G + 1) * P.stride_nc * kWarps;
+    Q.stats = P.stats + (size_t)b0 * (2 * G + 1) * P.stride_nc;
     Q.resid = P.resid + (size_t)b0 * P.stride_ncr;
-    const size_t smem = (size_t)(Q.B + 1) * sizeof(int);
-    const int grid = grid_size<EB, MODE>(smem);
-    if (grid <= 0) return SV_ERR_CUDA;
+    const size_t smem = (size_t)kWarps * kNB * kItemBytes + (size_t)(Q.B + 1) * sizeof(int);
     verify_kernel<EB, MODE><<<grid, kThreads, smem, stream>>>(Q);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   }
-  (void)L;
-  (void)ws;
   return SV_OK;
 }
 
 int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype, int B, int G,
                 int V, const int32_t* tokens, const int32_t* gamma, const float* uniforms,
                 const float* temperature, int32_t* out_tokens, int32_t* num_accepted,
-                double* p_tok, double* q_tok, void* ws, size_t ws_bytes, Layout& L) {
-  L = make_layout(B, G, V);
+                double* p_tok, double* q_tok, void* ws, size_t ws_bytes) {
+  const Layout L = make_layout(B, G, V);
   if (ws_bytes < L.total) return SV_ERR_WORKSPACE;
   const size_t eb = dtype == SV_BF16 ? 2 : 4;
   if (!aligned(target, eb) || (draft && !aligned(draft, eb))) return SV_ERR_ALIGN;
@@ -1125,7 +1234,7 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.B = B;
   P.G = G;
   P.V = V;
-  P.NC = (int)((V + kTileBytes / eb - 1) / (kTileBytes / eb));
+  P.NC = (int)((V + kItemBytes / eb - 1) / (kItemBytes / eb));
   P.NCR = (int)((V + kHalfBytes / eb - 1) / (kHalfBytes / eb));
   P.stride_nc = L.NC;
   P.stride_ncr = L.NCR;
@@ -1170,15 +1279,12 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, sv_d
     return SV_ERR_NULL;
   if (G > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL;
   Params P;
-  Layout L;
   rc = fill_params(P, target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma, uniforms,
-                   temperature, out_tokens, num_accepted, p_tok, q_tok, workspace, ws_bytes, L);
+                   temperature, out_tokens, num_accepted, p_tok, q_tok, workspace, ws_bytes);
   if (rc) return rc;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace);
-  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, L, ws, s)
-                          : launch<4, MODE_SAMPLE>(P, L, ws, s);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
 }
 
 int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, int V,
@@ -1191,15 +1297,12 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, 
     return SV_ERR_NULL;
   if (G > 0 && !draft_tokens) return SV_ERR_NULL;
   Params P;
-  Layout L;
   rc = fill_params(P, target_logits, nullptr, dtype, B, G, V, draft_tokens, gamma, nullptr,
-                   nullptr, out_tokens, num_accepted, nullptr, nullptr, workspace, ws_bytes, L);
+                   nullptr, out_tokens, num_accepted, nullptr, nullptr, workspace, ws_bytes);
   if (rc) return rc;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace);
-  return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, L, ws, s)
-                          : launch<4, MODE_GREEDY>(P, L, ws, s);
+  return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);
 }
 
 int spec_verify_status(void* workspace, sv_stream_t stream, uint32_t* status_host) {
