@@ -11,28 +11,31 @@
 //   speculative decoding optimisation", verify sketch with the bonus token.)
 //   Greedy: argmax match (explainer, "Implementation points", greedy note).
 //
-// One persistent kernel per call, one CTA of 12 warps per SM.  Work items,
-// in one fixed request-major order:
-//   A item  4 KB of one logit row: max and sum of exp2((z - max) log2(e)/T)
-//           (sampling) or argmax (greedy) -> one partial per item.
-//   R item  2 KB of target row k and the same 2 KB of draft row k of one
-//           request (sampling): fixed-point (2^-39) sums of the residual
-//           max(0, p_k - q_k) and of p_k -> one partial per item.
-// The A items of request b are followed by the R items of request b - L, so
-// that a request's residual rows are re-read after its decision, from L2.
+// One persistent kernel per call, one CTA of 12 warps per SM.  Work items, in
+// one fixed order:
+//   A items  4 KB of one logit row: max and sum of exp2((z - max) log2(e)/T)
+//            (sampling) or argmax (greedy) -> one partial per item.  All A
+//            items come first, request-major.
+//   R items  2 KB of target row k and the same 2 KB of draft row k of one
+//            request (sampling): fixed-point (2^-39) sums of the residual
+//            max(0, p_k - q_k) and of p_k -> one partial per item.  They form
+//            a tail that starts a few requests before the end and walks
+//            backwards, so the first ones re-read rows still in L2.
 // Every warp runs its own pipeline: it claims small batches of items from one
 // global counter (the next batch is claimed while the current one runs, and
 // its lanes decode a batch in parallel), keeps kNB TMA bulk copies
 // (cp.async.bulk) in flight into private shared-memory buffers, each tracked
 // by one mbarrier, and processes the items in order.  Arrivals are counted
-// per request in batches; the warp that completes a request's A items runs
-// its decision (float64 normalisers, acceptance tests, warp-ballot first
-// reject) and publishes it; the warp that completes its R items locates the
-// chunk holding u*S and scans only that chunk for the token.  A warp waits
-// for an undecided request only with its pipeline drained and its arrivals
-// published; everything it still holds comes later in the order, so every
-// wait ends.  Each wait is also bounded (2 s) and sets SV_STATUS_TIMEOUT.
-// Counters are reset by their last user, so the workspace stays zeroed.
+// per request with one acquire-release atomic per batch; the warp that
+// completes a request's A items runs its decision (float-float normalisers,
+// float64 acceptance ratios, warp-ballot first reject) and publishes it; the
+// warp that completes its R items locates the chunk holding u*S and scans
+// only that chunk for the token.  An R item whose request is not decided yet
+// is deferred while other items remain; a warp waits for a decision only
+// with its pipeline drained and its arrivals published, and only in the R
+// tail (it has then issued all its A items), so every wait ends.  Each wait
+// is also bounded (2 s) and sets SV_STATUS_TIMEOUT.  Counters are reset by
+// their last user, so the workspace stays zeroed.
 //
 // Numerics: inputs widen exactly to float32.  Exponent arguments use a
 // two-term log2(e)/T (hi + lo); exp2 is the SFU's ex2.approx; sums inside an
@@ -62,6 +65,7 @@ constexpr int kItemBytes = 4096;                      // A item: 4 KB of one row
 constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
 constexpr int kMaxBatch = 4096;                       // requests per launch (smem prefix)
 constexpr int kMaxK = 8;                              // work items per claimed batch
+constexpr int kDefer = 32;                            // deferred R items per warp
 constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
 constexpr float kFix = 549755813888.0f;               // 2^39: fixed-point scale of probabilities
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
@@ -196,6 +200,13 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
   return v;
 }
+// Atomic add with acquire-release semantics: publishes this thread's earlier
+// writes and, for the last arriver, makes the other arrivers' writes visible.
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -208,6 +219,49 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed arithmetic: max of two bf16 pairs (exact), and pairs of float32
+// lanes in one 64-bit register (each lane an ordinary IEEE round-to-nearest
+// operation).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// the two bf16 logits of a 32-bit word as a float32 pair (low element first)
+__device__ __forceinline__ unsigned long long bf16x2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ float bf16x2_hmax(uint32_t w) {
+  return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t vec_word(const uint4& v, int q) {
+  return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
 // Decision record read through L2 (it was written by another CTA).
@@ -310,11 +364,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -379,6 +428,32 @@ __device__ __forceinline__ unsigned long long scaled_target(float u, unsigned lo
   return shift >= 128 ? 0ull : (unsigned long long)(prod >> shift);
 }
 
+// Float-float (hi + lo) sums: about 48 bits of precision from float32 adds.
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return FF{s, e};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const FF s = ff_two_sum(a.hi, b.hi);
+  const float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  return ff_two_sum(s.hi, e);
+}
+__device__ __forceinline__ FF warp_sum_ff(FF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FF w;
+    w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+    w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+    v = ff_add(v, w);
+  }
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // Per-request decision (sampling), run by one warp: the one that completed
 // the request's last A item.
@@ -395,16 +470,16 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
   const int nrows = 2 * gb + 1;
 
   // Row maximum M and normaliser S = sum_c s_c 2^((m_c - M) c) over the
-  // per-item partials, in float64.  Lane (r & 31) keeps row r in slot r >> 5.
-  // Four rows at a time, each lane loading chunks lane and lane + 32, so the
-  // loads of a group are in flight together.
+  // per-item partials, summed in float-float.  Lane (r & 31) keeps row r in
+  // slot r >> 5.  Eight rows at a time, each lane loading chunks lane and
+  // lane + 32, so the loads of a group are in flight together.
   float rowM[2] = {-INFINITY, -INFINITY};
   double rowS[2] = {0.0, 0.0};
   const float2 none = make_float2(-INFINITY, 0.0f);
-  for (int r0 = 0; r0 < nrows; r0 += 4) {
-    float2 v[4][2];
+  for (int r0 = 0; r0 < nrows; r0 += 8) {
+    float2 v[8][2];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 8; ++g) {
       const int r = r0 + g;
       const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
       const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc;
@@ -412,7 +487,7 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
       v[g][1] = (r < nrows && lane + 32 < NC) ? __ldcg(&pr[lane + 32]) : none;
     }
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 8; ++g) {
       const int r = r0 + g;
       if (r >= nrows) break;
       const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
@@ -420,22 +495,24 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
       float M = fmaxf(v[g][0].x, v[g][1].x);
       for (int c = lane + 64; c < NC; c += 32) M = fmaxf(M, __ldcg(&pr[c]).x);
       M = warp_max(M);
-      double S = 0.0;
+      FF S{0.0f, 0.0f};
       if (M > -INFINITY) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           if (v[g][h].x > -INFINITY)
-            S += (double)v[g][h].y * (double)ex2_approx(exp_arg(v[g][h].x, M, tc.hi, tc.lo));
+            S = ff_add(S, FF{__fmul_rn(v[g][h].y, ex2_approx(exp_arg(v[g][h].x, M, tc.hi, tc.lo))), 0.0f});
         for (int c = lane + 64; c < NC; c += 32) {
           const float2 ms = __ldcg(&pr[c]);
-          if (ms.x > -INFINITY) S += (double)ms.y * (double)ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo));
+          if (ms.x > -INFINITY)
+            S = ff_add(S, FF{__fmul_rn(ms.y, ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo))), 0.0f});
         }
       }
-      S = warp_sum_d(S);
-      if (!isfinite(M) || !(S > 0.0)) flags |= SV_STATUS_NONFINITE_ROW;
+      S = warp_sum_ff(S);
+      const double Sd = (double)S.hi + (double)S.lo;
+      if (!isfinite(M) || !(Sd > 0.0)) flags |= SV_STATUS_NONFINITE_ROW;
       if (lane == (r & 31)) {
         rowM[r >> 5] = M;
-        rowS[r >> 5] = S;
+        rowS[r >> 5] = Sd;
       }
     }
   }
@@ -467,10 +544,19 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
     }
     const float zt = load_elem<EB>(P.target, target_row(b, i, G, V) + (size_t)x);
     const float zd = load_elem<EB>(P.draft, draft_row(b, i, G, V) + (size_t)x);
-    p = exp2(((double)zt - (double)mt_i) * cd) / st_i;
-    q = exp2(((double)zd - (double)md_i) * cd) / sd_i;
+    const double et = ((double)zt - (double)mt_i) * cd;  // log2 of S_t p(x)
+    const double ed = ((double)zd - (double)md_i) * cd;  // log2 of S_d q(x)
     const double u = (double)sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + i], flags);
-    reject = !((q == 0.0) || (u < p / q));
+    // ratio p/q = 2^(et - ed) * S_d / S_t.  A draft probability q(x) that is
+    // 0 in float64 (a -inf logit, or one far enough below the maximum to
+    // underflow) accepts.
+    const bool qzero = ed == -INFINITY || (ed < -1000.0 && exp2(ed) / sd_i == 0.0);
+    const double ratio = exp2(et - ed) * (sd_i / st_i);
+    reject = !(qzero || (u < ratio));
+    if (P.p_tok || P.q_tok) {
+      p = exp2(et) / st_i;
+      q = exp2(ed) / sd_i;
+    }
   }
   const unsigned int rej = __ballot_sync(0xffffffffu, reject);
   const int k = rej ? (__ffs(rej) - 1) : gb;
@@ -697,6 +783,36 @@ __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage
       const int vi = lane + 32 * j;
       v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
     }
+    if (EB == 2) {
+      // maximum on the packed bf16 pairs (exact), four independent chains
+      uint32_t mw[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mw[q] = bf16x2_max(mw[q], vec_word(v[j], q));
+      mx = warp_max(bf16x2_hmax(bf16x2_max(bf16x2_max(mw[0], mw[1]), bf16x2_max(mw[2], mw[3]))));
+      if (mx > -INFINITY) {
+        // (z - m) * (hi + lo) and the sum on float32 pairs
+        const unsigned long long negm = f2_pack(-mx, -mx);
+        const unsigned long long chi = f2_pack(m.c_hi, m.c_hi), clo = f2_pack(m.c_lo, m.c_lo);
+        unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const unsigned long long d = f2_add(bf16x2_to_f2(vec_word(v[j], q)), negm);
+            const unsigned long long a = f2_fma(d, chi, f2_mul(d, clo));
+            float a0, a1;
+            f2_unpack(a, a0, a1);
+            acc[q] = f2_add(acc[q], f2_pack(ex2_approx(a0), ex2_approx(a1)));
+          }
+        const unsigned long long t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        float s0, s1;
+        f2_unpack(t, s0, s1);
+        sum = s0 + s1;
+      }
+      return make_float2(mx, warp_sum(sum));
+    }
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
     for (int j = 0; j < NV; ++j)
@@ -747,6 +863,29 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
       v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+    }
+    if (EB == 2) {
+      // maximum on packed bf16 pairs; only a lane holding the warp maximum
+      // looks for its lowest index
+      uint32_t mw[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mw[q] = bf16x2_max(mw[q], vec_word(v[j], q));
+      const float lm = bf16x2_hmax(bf16x2_max(bf16x2_max(mw[0], mw[1]), bf16x2_max(mw[2], mw[3])));
+      bv = warp_max(lm);
+      unsigned int idx = 0x7fffffffu;
+      if (lm == bv) {
+        for (int j = 0; j < NV && idx == 0x7fffffffu; ++j) {
+          const int vi = lane + 32 * j;
+          if (vi >= nvec) break;
+#pragma unroll
+          for (int q = 0; q < VEC; ++q)
+            if (idx == 0x7fffffffu && vec_elem<EB>(v[j], q) == bv) idx = (unsigned int)(vi * VEC + q);
+        }
+      }
+      bi = (int)__reduce_min_sync(0xffffffffu, idx);
+      return make_float2(bv, __int_as_float(bi == 0x7fffffff ? bi : m.c * AE + bi));
     }
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -814,48 +953,38 @@ __device__ __forceinline__ ulonglong2 r_item(const Meta& m, const char* stage) {
 // ---------------------------------------------------------------------------
 // Work items: one fixed order, claimed in small batches
 // ---------------------------------------------------------------------------
-// Segment k of the order holds the A items of request k (rows, then chunks)
-// followed by the R items of request k - L; the R items of the last L
-// requests form a tail.  The lag L places a request's R items after its
-// decision while its rows are still in L2.
+// First the A items of every request (request-major: rows, then chunks), then
+// the R items of every request.  The R tail starts D requests before the end
+// and walks backwards (wrapping to the last D at the very end): the first R
+// items re-read the most recently streamed rows, which are still in L2, while
+// the last D requests, decided last, come last.
 struct Sched {
   const int* rowpre;  // [B+1] exclusive prefix of rows per request (shared memory)
-  int B, L, NC, NCR;  // NCR = 0 in greedy mode
-  unsigned int total;
+  int B, D, NC, NCR;  // NCR = 0 in greedy mode
+  unsigned int nA, total;
 };
-
-// start of segment k: A items of requests < k plus R items of requests < k - L
-__device__ __forceinline__ unsigned int seg_start(const Sched& s, int k) {
-  const int r = k - s.L;
-  return (unsigned int)s.rowpre[k] * s.NC + (r > 0 ? (unsigned int)r * s.NCR : 0u);
-}
 
 // Decode item j.  A items come back complete; R items carry only their
 // request and chunk (their rows depend on the request's decision).
 template <int EB, int MODE>
 __device__ void decode_item(const Params& P, const Sched& s, unsigned int j, Meta& m) {
   constexpr int AE = kItemBytes / EB;
-  if (MODE == MODE_SAMPLE && j >= seg_start(s, s.B)) {
-    const unsigned int t = j - seg_start(s, s.B);
+  if (MODE == MODE_SAMPLE && j >= s.nA) {
+    const unsigned int t = j - s.nA;
+    const int rank = (int)(t / s.NCR);
     m.kind = KIND_R;
-    m.b = (s.B > s.L ? s.B - s.L : 0) + (int)(t / s.NCR);
+    m.b = (2 * s.B - 1 - s.D - rank) % s.B;
     m.c = (int)(t % s.NCR);
     return;
   }
-  int lo = 0, hi = s.B - 1;  // largest k with seg_start(k) <= j
+  const int NC = s.NC;
+  int lo = 0, hi = s.B - 1;  // largest request with rowpre[b] * NC <= j
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (seg_start(s, mid) <= j) lo = mid; else hi = mid - 1;
+    if ((unsigned int)s.rowpre[mid] * NC <= j) lo = mid; else hi = mid - 1;
   }
-  const unsigned int off = j - seg_start(s, lo);
+  const unsigned int off = j - (unsigned int)s.rowpre[lo] * NC;
   const int rows = s.rowpre[lo + 1] - s.rowpre[lo];
-  const unsigned int na = (unsigned int)rows * s.NC;
-  if (off >= na) {
-    m.kind = KIND_R;
-    m.b = lo - s.L;
-    m.c = (int)(off - na);
-    return;
-  }
   const int G = P.G, V = P.V;
   const int row = (int)(off / s.NC);
   const int c = (int)(off % s.NC);
@@ -920,6 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   __shared__ Meta meta[kWarps][kNB];   // the item in each buffer
   __shared__ Meta batchq[kWarps][kMaxK];  // the warp's current batch
   __shared__ Decision dcache[kWarps];  // the last decision the warp fetched
+  __shared__ int2 defq[kWarps][kDefer];  // deferred R items (request, chunk)
   __shared__ int sh_carry;
   __shared__ int wsum[kWarps];
   __shared__ int sh_last;
@@ -966,16 +1096,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   sc.NC = NC;
   sc.NCR = MODE == MODE_SAMPLE ? P.NCR : 0;
   const unsigned int nA = (unsigned int)rowpre[B] * NC;
+  sc.nA = nA;
   sc.total = nA + (MODE == MODE_SAMPLE ? (unsigned int)B * P.NCR : 0u);
   const unsigned int nwarps = gridDim.x * kWarps;
   // batches: about 1/16 of a warp's share, at most 8 items
   const unsigned int K = min((unsigned int)kMaxK, max(1u, sc.total / (nwarps * 16u)));
   {
-    // R items trail their request's A items by about the items in flight
+    // requests whose A items may still be in flight when the tail starts
     const double per_req = (double)nA / (double)(B > 0 ? B : 1);
-    const double inflight = (double)nwarps * (kNB + 2 * K);
-    int L = MODE == MODE_SAMPLE ? (int)ceil(inflight / per_req) : 1;
-    sc.L = L < 1 ? 1 : L;
+    const int D = (int)ceil((double)nwarps * (kNB + K) / per_req) + 1;
+    sc.D = D < B ? D : B - 1;
   }
 
   unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
@@ -995,137 +1125,191 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   unsigned int flags = 0;
   bool failed = false;
 
-  // Publish held arrivals; the warp completing a request runs its follow-up.
-  auto flush = [&]() {
-    if (acc_n == 0) return;
+  // Arrivals are published asynchronously: flush() adds the held count with
+  // one acquire-release atomic; its result is examined at the next settle(),
+  // and the warp that completed a request then runs the request's follow-up.
+  unsigned int pend_old = 0, pend_n = 0, pend_total = 0;  // lane 0
+  int pend_kind = KIND_A, pend_b = -1;                      // warp-uniform
+  auto settle = [&]() {
+    if (pend_b < 0) return;
     unsigned int last = 0;
-    if (lane == 0) {
-      __threadfence();
-      unsigned int* cnt = acc_kind == KIND_A ? &P.cnt_a[acc_b] : &P.cnt_r[acc_b];
-      const unsigned int total = acc_kind == KIND_A
-          ? (unsigned int)(rowpre[acc_b + 1] - rowpre[acc_b]) * (unsigned int)NC
-          : (unsigned int)P.NCR;
-      last = (atomicAdd(cnt, acc_n) + acc_n == total) ? 1u : 0u;
-      if (last) __threadfence();
-    }
+    if (lane == 0) last = (pend_old + pend_n == pend_total) ? 1u : 0u;
     last = __shfl_sync(0xffffffffu, last, 0);
+    const int b = pend_b;
+    pend_b = -1;
     if (last) {
-      if (acc_kind == KIND_A) {
-        if (MODE == MODE_SAMPLE) decide_sample<EB>(P, acc_b);
-        else decide_greedy(P, acc_b);
+      if (pend_kind == KIND_A) {
+        if (MODE == MODE_SAMPLE) decide_sample<EB>(P, b);
+        else decide_greedy(P, b);
       } else {
-        final_draw<EB>(P, acc_b);
+        final_draw<EB>(P, b);
       }
     }
+  };
+  auto flush = [&]() {
+    if (acc_n == 0) return;
+    settle();
+    if (lane == 0) {
+      unsigned int* cnt = acc_kind == KIND_A ? &P.cnt_a[acc_b] : &P.cnt_r[acc_b];
+      pend_total = acc_kind == KIND_A
+          ? (unsigned int)(rowpre[acc_b + 1] - rowpre[acc_b]) * (unsigned int)NC
+          : (unsigned int)P.NCR;
+      pend_n = acc_n;
+      pend_old = atom_add_acq_rel(cnt, acc_n);
+    }
+    pend_kind = acc_kind;
+    pend_b = acc_b;
     acc_n = 0;
+  };
+
+  int2* mydef = defq[warp];
+  int defhead = 0, ndef = 0;  // ring of deferred R items (warp-uniform)
+  bool blocked = false;       // waiting for the oldest deferred item's decision
+
+  // Is request b decided?  If so its decision is fetched into dcache[warp].
+  auto decided = [&](int b) -> bool {
+    if (b == dec_b) return true;
+    unsigned int ok = 0;
+    if (lane == 0 && ld_acquire(&P.ready[b])) {
+      ok = 1;
+      dcache[warp] = load_decision(&P.dec[b]);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    if (ok) dec_b = b;
+    return ok != 0;
+  };
+
+  // Lane 0 completes the item (R items from dcache[warp]) and starts its copy
+  // into the next buffer.
+  auto issue = [&](const Meta& item) {
+    const int s = (int)(issued % kNB);
+    if (lane == 0) {
+      Meta mine = item;
+      if (MODE == MODE_SAMPLE && mine.kind == KIND_R) fill_r_item<EB>(P, dcache[warp], mine);
+      mymeta[s] = mine;
+      unsigned char* dst = mybuf + s * kItemBytes;
+      // order earlier generic reads of this buffer before the async-proxy write
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (mine.direct) {
+        mbar_arrive(&mybar[s]);
+      } else {
+        const unsigned int bytes = (unsigned int)(mine.n * EB);
+        const bool two = mine.kind == KIND_R && mine.p1 != nullptr;
+        mbar_arrive_expect_tx(&mybar[s], two ? 2 * bytes : bytes);
+        bulk_copy_g2s(dst, mine.p0, bytes, &mybar[s]);
+        if (two) bulk_copy_g2s(dst + kHalfBytes, mine.p1, bytes, &mybar[s]);
+      }
+    }
+    __syncwarp();
+    ++issued;
   };
 
   while (!failed) {
     // 1. keep kNB copies in flight
-    while (issued - processed < (unsigned int)kNB) {
+    while (!blocked && issued - processed < (unsigned int)kNB) {
       if (qhead == qlen) {
-        if (!more) break;
-        const unsigned int base = __shfl_sync(0xffffffffu, nb, 0);
-        if (base >= sc.total) {
-          more = false;
+        // batch boundary: first the oldest deferred R item, if now decided
+        if (ndef > 0 && decided(mydef[defhead].x)) {
+          Meta r;
+          r.kind = KIND_R;
+          r.b = mydef[defhead].x;
+          r.c = mydef[defhead].y;
+          issue(r);
+          defhead = (defhead + 1) % kDefer;
+          --ndef;
+          continue;
+        }
+        if (more) {
+          const unsigned int base = __shfl_sync(0xffffffffu, nb, 0);
+          if (base >= sc.total) {
+            more = false;
+          } else {
+            qlen = (int)min(K, sc.total - base);
+            qhead = 0;
+            if (lane < qlen) decode_item<EB, MODE>(P, sc, base + lane, myq[lane]);
+            if (lane == 0) nb = atomicAdd(P.next_item, K);  // pre-claim the next batch
+            __syncwarp();
+          }
+        }
+        if (qhead == qlen) {
+          if (ndef > 0) blocked = true;  // only deferred items remain
           break;
         }
-        qlen = (int)min(K, sc.total - base);
-        qhead = 0;
-        if (lane < qlen) decode_item<EB, MODE>(P, sc, base + lane, myq[lane]);
-        if (lane == 0) nb = atomicAdd(P.next_item, K);  // pre-claim the next batch
+      }
+      const Meta& it = myq[qhead];
+      if (MODE == MODE_SAMPLE && it.kind == KIND_R && !decided(it.b)) {
+        // not decided yet: set it aside and keep streaming later items
+        if (ndef == kDefer) {
+          blocked = true;
+          break;
+        }
+        if (lane == 0) mydef[(defhead + ndef) % kDefer] = make_int2(it.b, it.c);
         __syncwarp();
+        ++ndef;
+        ++qhead;
+        continue;
       }
-      Meta& it = myq[qhead];
-      if (MODE == MODE_SAMPLE && it.kind == KIND_R) {
-        const int b = it.b;
-        if (b != dec_b) {
-          unsigned int ok = 0;
-          if (lane == 0 && ld_acquire(&P.ready[b])) {
-            ok = 1;
-            dcache[warp] = load_decision(&P.dec[b]);
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            // not decided yet: work off what is in flight first
-            if (issued != processed) break;
-            // Nothing in flight: publish held arrivals, then wait.  Every
-            // item this warp still holds comes later in the order, so the
-            // decision does not depend on it.
-            flush();
-            if (lane == 0) {
-              const unsigned long long t0 = now_ns();
-              while (!ld_acquire(&P.ready[b])) {
-                if (now_ns() - t0 > kWaitNs) {
-                  ok = 2;
-                  break;
-                }
-                __nanosleep(128);
-              }
-              if (ok != 2) dcache[warp] = load_decision(&P.dec[b]);
-            }
-            if (__shfl_sync(0xffffffffu, ok, 0) == 2) {
-              flags |= SV_STATUS_TIMEOUT;
-              failed = true;
-              break;
-            }
-          }
-          dec_b = b;
-        }
-      }
-      // lane 0 completes the item and starts its copy into the next buffer
-      const int s = (int)(issued % kNB);
-      if (lane == 0) {
-        Meta mine = it;
-        if (MODE == MODE_SAMPLE && mine.kind == KIND_R) fill_r_item<EB>(P, dcache[warp], mine);
-        mymeta[s] = mine;
-        unsigned char* dst = mybuf + s * kItemBytes;
-        // order earlier generic reads of this buffer before the async-proxy write
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (mine.direct) {
-          mbar_arrive(&mybar[s]);
-        } else {
-          const unsigned int bytes = (unsigned int)(mine.n * EB);
-          const bool two = mine.kind == KIND_R && mine.p1 != nullptr;
-          mbar_arrive_expect_tx(&mybar[s], two ? 2 * bytes : bytes);
-          bulk_copy_g2s(dst, mine.p0, bytes, &mybar[s]);
-          if (two) bulk_copy_g2s(dst + kHalfBytes, mine.p1, bytes, &mybar[s]);
-        }
-      }
-      __syncwarp();
+      issue(it);
       ++qhead;
-      ++issued;
     }
-    if (failed) break;
-    if (issued == processed) {
-      if (!more && qhead == qlen) break;  // all work done
+
+    // 2. process the oldest item in flight
+    if (issued != processed) {
+      const int s = (int)(processed % kNB);
+      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+        flags |= SV_STATUS_TIMEOUT;
+        failed = true;
+        break;
+      }
+      const Meta& m = mymeta[s];
+      const int m_kind = m.kind, m_b = m.b;
+      const char* stage = reinterpret_cast<const char*>(mybuf + s * kItemBytes);
+      if (m_kind == KIND_A) {
+        const float2 part = MODE == MODE_SAMPLE ? a_item_sample<EB>(m, stage)
+                                                : a_item_greedy<EB>(m, stage);
+        if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
+      } else {
+        const ulonglong2 part = r_item<EB>(m, stage);
+        if (lane == 0) P.resid[(size_t)m_b * P.stride_ncr + m.c] = part;
+      }
+      __syncwarp();  // every lane is done with the buffer before it is reused
+      ++processed;
+      settle();
+      if (acc_n && (m_kind != acc_kind || m_b != acc_b)) flush();
+      acc_kind = m_kind;
+      acc_b = m_b;
+      ++acc_n;
       continue;
     }
 
-    // 2. process the oldest item
-    const int s = (int)(processed % kNB);
-    if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
-      flags |= SV_STATUS_TIMEOUT;
-      failed = true;
-      break;
+    // 3. nothing in flight
+    if (blocked) {
+      // Publish held arrivals, then wait for the oldest deferred item's
+      // request.  Everything this warp still holds is either a deferred R item
+      // (no decision depends on one) or comes later in the order.
+      flush();
+      settle();
+      int state = 0;
+      if (lane == 0) {
+        const unsigned long long t0 = now_ns();
+        while (!ld_acquire(&P.ready[mydef[defhead].x])) {
+          if (now_ns() - t0 > kWaitNs) {
+            state = 1;
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+      if (__shfl_sync(0xffffffffu, state, 0)) {
+        flags |= SV_STATUS_TIMEOUT;
+        failed = true;
+        break;
+      }
+      blocked = false;
+      continue;
     }
-    const Meta& m = mymeta[s];
-    const int m_kind = m.kind, m_b = m.b;
-    const char* stage = reinterpret_cast<const char*>(mybuf + s * kItemBytes);
-    if (m_kind == KIND_A) {
-      const float2 part = MODE == MODE_SAMPLE ? a_item_sample<EB>(m, stage)
-                                              : a_item_greedy<EB>(m, stage);
-      if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
-    } else {
-      const ulonglong2 part = r_item<EB>(m, stage);
-      if (lane == 0) P.resid[(size_t)m_b * P.stride_ncr + m.c] = part;
-    }
-    __syncwarp();  // every lane is done with the buffer before it is reused
-    ++processed;
-    if (acc_n && (m_kind != acc_kind || m_b != acc_b)) flush();
-    acc_kind = m_kind;
-    acc_b = m_b;
-    ++acc_n;
+    if (!more && qhead == qlen && ndef == 0) break;  // all work done
   }
 
   // No copy may still be landing in this warp's buffers when it leaves.
@@ -1134,6 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       (void)mbar_wait(&mybar[p % kNB], (p / kNB) & 1u);
   } else {
     flush();
+    settle();
   }
   if (lane == 0 && flags) atomicOr(P.status, flags);
   __syncthreads();
