@@ -13,10 +13,10 @@
 //
 // One persistent kernel per call, one CTA of 12 warps per SM.  Work items, in
 // one fixed order:
-//   A items  4 KB of one logit row: max and sum of exp2((z - max) log2(e)/T)
+//   A items  8 KB of one logit row: max and sum of exp2((z - max) log2(e)/T)
 //            (sampling) or argmax (greedy) -> one partial per item.  All A
 //            items come first, request-major.
-//   R items  2 KB of target row k and the same 2 KB of draft row k of one
+//   R items  4 KB of target row k and the same 4 KB of draft row k of one
 //            request (sampling): fixed-point (2^-39) sums of the residual
 //            max(0, p_k - q_k) and of p_k -> one partial per item.  They form
 //            a tail that starts a few requests before the end and walks
@@ -56,15 +56,16 @@ namespace {
 #define SV_WARPS 12
 #endif
 #ifndef SV_BUFFERS
-#define SV_BUFFERS 4
+#define SV_BUFFERS 2
 #endif
 constexpr int kWarps = SV_WARPS;                      // warps per CTA (one CTA per SM)
 constexpr int kThreads = 32 * kWarps;
 constexpr int kNB = SV_BUFFERS;                       // TMA buffers per warp
-constexpr int kItemBytes = 4096;                      // A item: 4 KB of one row
+constexpr int kItemBytes = 8192;                      // A item: 8 KB of one row
 constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
 constexpr int kMaxBatch = 4096;                       // requests per launch (smem prefix)
 constexpr int kMaxK = 8;                              // work items per claimed batch
+constexpr unsigned int kBatchDiv = 4;                 // batches per warp's share, at least
 constexpr int kDefer = 32;                            // deferred R items per warp
 constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
 constexpr float kFix = 549755813888.0f;               // 2^39: fixed-point scale of probabilities
@@ -260,6 +261,12 @@ __device__ __forceinline__ unsigned long long bf16x2_to_f2(uint32_t w) {
 __device__ __forceinline__ float bf16x2_hmax(uint32_t w) {
   return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
+// per-half equality of two bf16 pairs (0xffff in each equal half)
+__device__ __forceinline__ uint32_t bf16x2_eq(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ uint32_t vec_word(const uint4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
@@ -355,9 +362,9 @@ __device__ __forceinline__ size_t draft_row(int b, int i, int G, int V) {
 }
 
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -471,15 +478,15 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
 
   // Row maximum M and normaliser S = sum_c s_c 2^((m_c - M) c) over the
   // per-item partials, summed in float-float.  Lane (r & 31) keeps row r in
-  // slot r >> 5.  Eight rows at a time, each lane loading chunks lane and
+  // slot r >> 5.  Four rows at a time, each lane loading chunks lane and
   // lane + 32, so the loads of a group are in flight together.
   float rowM[2] = {-INFINITY, -INFINITY};
   double rowS[2] = {0.0, 0.0};
   const float2 none = make_float2(-INFINITY, 0.0f);
-  for (int r0 = 0; r0 < nrows; r0 += 8) {
-    float2 v[8][2];
+  for (int r0 = 0; r0 < nrows; r0 += 4) {
+    float2 v[4][2];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
+    for (int g = 0; g < 4; ++g) {
       const int r = r0 + g;
       const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
       const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc;
@@ -487,7 +494,7 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
       v[g][1] = (r < nrows && lane + 32 < NC) ? __ldcg(&pr[lane + 32]) : none;
     }
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
+    for (int g = 0; g < 4; ++g) {
       const int r = r0 + g;
       if (r >= nrows) break;
       const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
@@ -684,60 +691,58 @@ __device__ __noinline__ void final_draw(const Params& P, int b) {
     kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
     const char* trow = P.target + target_row(b, k, G, V) * EB;
     const char* drow = kc.reject ? P.draft + draft_row(b, k, G, V) * EB : nullptr;
-    // This lane's EPL contiguous logits of the chosen chunk (16-byte loads
-    // when the rows allow it; -inf past the end of the row).
-    constexpr int NV = EPL * EB / 16;  // 8 vectors per lane
+    // This lane's EPL contiguous logits of the chosen chunk, one 16-byte
+    // vector at a time (scalar loads when the rows do not allow it; -inf past
+    // the end of the row).  Pass 1 sums the weights, pass 2 (one lane) finds
+    // the token.
+    constexpr int VEC = 16 / EB;
+    constexpr int NV = EPL / VEC;
     const size_t e0 = (size_t)cs * RE + (size_t)lane * EPL;
-    uint4 tv[NV], dv[NV];
     const bool vec_ok = ((reinterpret_cast<uintptr_t>(trow) |
                           reinterpret_cast<uintptr_t>(drow)) & 15) == 0 &&
                         e0 + EPL <= (size_t)V;
+    auto load_vec = [&](const char* row, int q) -> uint4 {
+      if (!row) return neg_inf_vec(EB);
+      if (vec_ok) return __ldcg(reinterpret_cast<const uint4*>(row + (e0 + (size_t)q * VEC) * EB));
+      uint32_t w[4];
 #pragma unroll
-    for (int q = 0; q < NV; ++q) {
-      if (vec_ok) {
-        tv[q] = __ldcg(reinterpret_cast<const uint4*>(trow + (e0 + (size_t)q * (16 / EB)) * EB));
-        dv[q] = drow ? __ldcg(reinterpret_cast<const uint4*>(drow + (e0 + (size_t)q * (16 / EB)) * EB))
-                     : neg_inf_vec(EB);
-      } else {
-        uint32_t wt[4], wd[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          if (EB == 2) {
-            const size_t ea = e0 + (size_t)q * 8 + 2 * h, eb = ea + 1;
-            const uint32_t ta = ea < (size_t)V ? reinterpret_cast<const unsigned short*>(trow)[ea] : 0xff80u;
-            const uint32_t tb = eb < (size_t)V ? reinterpret_cast<const unsigned short*>(trow)[eb] : 0xff80u;
-            const uint32_t da = (drow && ea < (size_t)V) ? reinterpret_cast<const unsigned short*>(drow)[ea] : 0xff80u;
-            const uint32_t db = (drow && eb < (size_t)V) ? reinterpret_cast<const unsigned short*>(drow)[eb] : 0xff80u;
-            wt[h] = ta | (tb << 16);
-            wd[h] = da | (db << 16);
-          } else {
-            const size_t e = e0 + (size_t)q * 4 + h;
-            wt[h] = e < (size_t)V ? __float_as_uint(reinterpret_cast<const float*>(trow)[e]) : 0xff800000u;
-            wd[h] = (drow && e < (size_t)V) ? __float_as_uint(reinterpret_cast<const float*>(drow)[e])
-                                            : 0xff800000u;
-          }
+      for (int h = 0; h < 4; ++h) {
+        if (EB == 2) {
+          const size_t ea = e0 + (size_t)q * 8 + 2 * h, eb = ea + 1;
+          const uint32_t lo = ea < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[ea] : 0xff80u;
+          const uint32_t hi = eb < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[eb] : 0xff80u;
+          w[h] = lo | (hi << 16);
+        } else {
+          const size_t e = e0 + (size_t)q * 4 + h;
+          w[h] = e < (size_t)V ? __float_as_uint(reinterpret_cast<const float*>(row)[e]) : 0xff800000u;
         }
-        tv[q] = make_uint4(wt[0], wt[1], wt[2], wt[3]);
-        dv[q] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
-    }
-    auto weight = [&](int j) -> unsigned long long {
-      unsigned long long wr, wp;
-      resid_weights(vec_elem<EB>(tv[j / (16 / EB)], j % (16 / EB)),
-                    vec_elem<EB>(dv[j / (16 / EB)], j % (16 / EB)), kc, wr, wp);
-      return usep ? wp : wr;
+      return make_uint4(w[0], w[1], w[2], w[3]);
     };
     unsigned long long lsum = 0;
+#pragma unroll 2
+    for (int q = 0; q < NV; ++q) {
+      const uint4 tv = load_vec(trow, q), dv = load_vec(drow, q);
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) lsum += weight(j);
+      for (int h = 0; h < VEC; ++h) {
+        unsigned long long wr, wp;
+        resid_weights(vec_elem<EB>(tv, h), vec_elem<EB>(dv, h), kc, wr, wp);
+        lsum += usep ? wp : wr;
+      }
+    }
     const unsigned long long incl = warp_incl_scan_u64(lsum);
     unsigned long long run = base + incl - lsum;
     if (run <= target && run + lsum > target) {
+      for (int q = 0; q < NV && tok < 0; ++q) {
+        const uint4 tv = load_vec(trow, q), dv = load_vec(drow, q);
 #pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        const unsigned long long nxt = run + weight(j);
-        if (tok < 0 && nxt > target) tok = (int)(e0 + (size_t)j);
-        run = nxt;
+        for (int h = 0; h < VEC; ++h) {
+          unsigned long long wr, wp;
+          resid_weights(vec_elem<EB>(tv, h), vec_elem<EB>(dv, h), kc, wr, wp);
+          const unsigned long long nxt = run + (usep ? wp : wr);
+          if (tok < 0 && nxt > target) tok = (int)(e0 + (size_t)(q * VEC + h));
+          run = nxt;
+        }
       }
     }
     const unsigned int own = __ballot_sync(0xffffffffu, tok >= 0);
@@ -777,41 +782,58 @@ __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage
   if (!m.direct) {
     // two passes over the stage: the maximum, then the exponentials
     const int nvec = m.n / VEC;  // n * EB is a multiple of 16 on this path
-    uint4 v[NV];  // one pass over the stage; the item stays in registers
+    if constexpr (EB == 2) {
+      // The item's 2*NV*4 logits stay in registers as bf16 pairs.
+      constexpr int NW = NV * 4;
+      uint32_t w[NW];
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int vi = lane + 32 * j;
+        const uint4 v = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+      }
+      // maximum on the packed pairs (exact), as a log-depth tree
+      uint32_t t[NW / 2];
+#pragma unroll
+      for (int i = 0; i < NW / 2; ++i) t[i] = bf16x2_max(w[i], w[i + NW / 2]);
+#pragma unroll
+      for (int width = NW / 4; width >= 1; width >>= 1)
+#pragma unroll
+        for (int i = 0; i < width; ++i) t[i] = bf16x2_max(t[i], t[i + width]);
+      mx = warp_max(bf16x2_hmax(t[0]));
+      if (mx > -INFINITY) {
+        // (z - m) * (hi + lo) and the sum, on float32 pairs, 8 accumulators
+        const unsigned long long negm = f2_pack(-mx, -mx);
+        const unsigned long long chi = f2_pack(m.c_hi, m.c_hi), clo = f2_pack(m.c_lo, m.c_lo);
+        unsigned long long acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0ull;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+          const unsigned long long d = f2_add(bf16x2_to_f2(w[i]), negm);
+          const unsigned long long a = f2_fma(d, chi, f2_mul(d, clo));
+          float a0, a1;
+          f2_unpack(a, a0, a1);
+          acc[i & 7] = f2_add(acc[i & 7], f2_pack(ex2_approx(a0), ex2_approx(a1)));
+        }
+#pragma unroll
+        for (int width = 4; width >= 1; width >>= 1)
+#pragma unroll
+          for (int i = 0; i < width; ++i) acc[i] = f2_add(acc[i], acc[i + width]);
+        float s0, s1;
+        f2_unpack(acc[0], s0, s1);
+        sum = s0 + s1;
+      }
+      return make_float2(mx, warp_sum(sum));
+    }
+    uint4 v[NV];  // float32: the item stays in registers
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
       v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
-    }
-    if (EB == 2) {
-      // maximum on the packed bf16 pairs (exact), four independent chains
-      uint32_t mw[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
-#pragma unroll
-      for (int j = 0; j < NV; ++j)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) mw[q] = bf16x2_max(mw[q], vec_word(v[j], q));
-      mx = warp_max(bf16x2_hmax(bf16x2_max(bf16x2_max(mw[0], mw[1]), bf16x2_max(mw[2], mw[3]))));
-      if (mx > -INFINITY) {
-        // (z - m) * (hi + lo) and the sum on float32 pairs
-        const unsigned long long negm = f2_pack(-mx, -mx);
-        const unsigned long long chi = f2_pack(m.c_hi, m.c_hi), clo = f2_pack(m.c_lo, m.c_lo);
-        unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int j = 0; j < NV; ++j)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const unsigned long long d = f2_add(bf16x2_to_f2(vec_word(v[j], q)), negm);
-            const unsigned long long a = f2_fma(d, chi, f2_mul(d, clo));
-            float a0, a1;
-            f2_unpack(a, a0, a1);
-            acc[q] = f2_add(acc[q], f2_pack(ex2_approx(a0), ex2_approx(a1)));
-          }
-        const unsigned long long t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-        float s0, s1;
-        f2_unpack(t, s0, s1);
-        sum = s0 + s1;
-      }
-      return make_float2(mx, warp_sum(sum));
     }
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
@@ -858,34 +880,57 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
   if (!m.direct) {
     // the maximum (independent chains), then the lowest index holding it
     const int nvec = m.n / VEC;
+    if constexpr (EB == 2) {
+      // maximum on the packed pairs as a log-depth tree; a lane holding the
+      // warp maximum finds its first vector holding it, then the element
+      constexpr int NW = NV * 4;
+      uint32_t w[NW];
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int vi = lane + 32 * j;
+        const uint4 v = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+      }
+      uint32_t t[NW / 2];
+#pragma unroll
+      for (int i = 0; i < NW / 2; ++i) t[i] = bf16x2_max(w[i], w[i + NW / 2]);
+#pragma unroll
+      for (int width = NW / 4; width >= 1; width >>= 1)
+#pragma unroll
+        for (int i = 0; i < width; ++i) t[i] = bf16x2_max(t[i], t[i + width]);
+      const float lm = bf16x2_hmax(t[0]);
+      bv = warp_max(lm);
+      unsigned int idx = 0x7fffffffu;
+      if (lm == bv) {
+        const uint32_t b16 = __float_as_uint(bv) >> 16;
+        const uint32_t b2 = b16 | (b16 << 16);
+        unsigned int mask = 0;  // bit j: vector j holds the maximum
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const uint32_t e = bf16x2_eq(w[4 * j], b2) | bf16x2_eq(w[4 * j + 1], b2) |
+                             bf16x2_eq(w[4 * j + 2], b2) | bf16x2_eq(w[4 * j + 3], b2);
+          mask |= (e != 0u ? 1u : 0u) << j;
+        }
+        if (mask) {
+          const int j = __ffs(mask) - 1;
+          const int vi = lane + 32 * j;
+          const uint4 v = lds128(stage + vi * 16);
+#pragma unroll
+          for (int q = VEC - 1; q >= 0; --q)
+            if (vec_elem<EB>(v, q) == bv) idx = (unsigned int)(vi * VEC + q);
+        }
+      }
+      bi = (int)__reduce_min_sync(0xffffffffu, idx);
+      return make_float2(bv, __int_as_float(bi == 0x7fffffff ? bi : m.c * AE + bi));
+    }
     uint4 v[NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
       v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
-    }
-    if (EB == 2) {
-      // maximum on packed bf16 pairs; only a lane holding the warp maximum
-      // looks for its lowest index
-      uint32_t mw[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
-#pragma unroll
-      for (int j = 0; j < NV; ++j)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) mw[q] = bf16x2_max(mw[q], vec_word(v[j], q));
-      const float lm = bf16x2_hmax(bf16x2_max(bf16x2_max(mw[0], mw[1]), bf16x2_max(mw[2], mw[3])));
-      bv = warp_max(lm);
-      unsigned int idx = 0x7fffffffu;
-      if (lm == bv) {
-        for (int j = 0; j < NV && idx == 0x7fffffffu; ++j) {
-          const int vi = lane + 32 * j;
-          if (vi >= nvec) break;
-#pragma unroll
-          for (int q = 0; q < VEC; ++q)
-            if (idx == 0x7fffffffu && vec_elem<EB>(v[j], q) == bv) idx = (unsigned int)(vi * VEC + q);
-        }
-      }
-      bi = (int)__reduce_min_sync(0xffffffffu, idx);
-      return make_float2(bv, __int_as_float(bi == 0x7fffffff ? bi : m.c * AE + bi));
     }
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -957,63 +1002,98 @@ __device__ __forceinline__ ulonglong2 r_item(const Meta& m, const char* stage) {
 // the R items of every request.  The R tail starts D requests before the end
 // and walks backwards (wrapping to the last D at the very end): the first R
 // items re-read the most recently streamed rows, which are still in L2, while
-// the last D requests, decided last, come last.
-struct Sched {
-  const int* rowpre;  // [B+1] exclusive prefix of rows per request (shared memory)
-  int B, D, NC, NCR;  // NCR = 0 in greedy mode
-  unsigned int nA, total;
+// the last D requests, decided last, come last.  A warp walks its batch with
+// a cursor that advances in O(1) per item.
+struct Cursor {
+  unsigned int j;   // item index
+  int req, row, c;  // A: request, row within the request, chunk
+  int rows, gb;     // A: rows of req, and its gamma
+  int rank;         // R: position in the tail
 };
 
-// Decode item j.  A items come back complete; R items carry only their
-// request and chunk (their rows depend on the request's decision).
-template <int EB, int MODE>
-__device__ void decode_item(const Params& P, const Sched& s, unsigned int j, Meta& m) {
-  constexpr int AE = kItemBytes / EB;
-  if (MODE == MODE_SAMPLE && j >= s.nA) {
-    const unsigned int t = j - s.nA;
-    const int rank = (int)(t / s.NCR);
-    m.kind = KIND_R;
-    m.b = (2 * s.B - 1 - s.D - rank) % s.B;
-    m.c = (int)(t % s.NCR);
+template <int MODE>
+__device__ __forceinline__ int rows_of(const int* rowpre, int b) {
+  return rowpre[b + 1] - rowpre[b];
+}
+
+// Place the cursor on item j.
+template <int MODE>
+__device__ __forceinline__ void cursor_seek(Cursor& k, unsigned int j, const int* rowpre, int B,
+                                            int NC, int NCR, unsigned int nA) {
+  k.j = j;
+  if (MODE == MODE_SAMPLE && j >= nA) {
+    k.rank = (int)((j - nA) / NCR);
+    k.c = (int)((j - nA) % NCR);
     return;
   }
-  const int NC = s.NC;
-  int lo = 0, hi = s.B - 1;  // largest request with rowpre[b] * NC <= j
+  int lo = 0, hi = B - 1;  // largest request with rowpre[b] * NC <= j
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if ((unsigned int)s.rowpre[mid] * NC <= j) lo = mid; else hi = mid - 1;
+    if ((unsigned int)rowpre[mid] * NC <= j) lo = mid; else hi = mid - 1;
   }
-  const unsigned int off = j - (unsigned int)s.rowpre[lo] * NC;
-  const int rows = s.rowpre[lo + 1] - s.rowpre[lo];
+  const unsigned int off = j - (unsigned int)rowpre[lo] * NC;
+  k.req = lo;
+  k.row = (int)(off / NC);
+  k.c = (int)(off % NC);
+  k.rows = rows_of<MODE>(rowpre, lo);
+  k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
+}
+
+// Advance the cursor by one item.
+template <int MODE>
+__device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int NC, int NCR,
+                                            unsigned int nA) {
+  ++k.j;
+  if (MODE == MODE_SAMPLE && k.j > nA) {  // inside the R tail
+    if (++k.c == NCR) {
+      k.c = 0;
+      ++k.rank;
+    }
+    return;
+  }
+  if (MODE == MODE_SAMPLE && k.j == nA) {  // first R item
+    k.rank = 0;
+    k.c = 0;
+    return;
+  }
+  if (++k.c == NC) {
+    k.c = 0;
+    if (++k.row == k.rows) {
+      k.row = 0;
+      ++k.req;
+      k.rows = rows_of<MODE>(rowpre, k.req);
+      k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
+    }
+  }
+}
+
+// The A item under the cursor.
+template <int EB, int MODE>
+__device__ __forceinline__ void a_item_at(const Params& P, const Cursor& k, float c_hi,
+                                          float c_lo, Meta& m) {
+  constexpr int AE = kItemBytes / EB;
   const int G = P.G, V = P.V;
-  const int row = (int)(off / s.NC);
-  const int c = (int)(off % s.NC);
-  const int gb = MODE == MODE_SAMPLE ? (rows - 1) / 2 : rows - 1;
   size_t roff;
   const char* base;
-  if (row <= gb) {
-    m.pslot = row;
-    roff = target_row(lo, row, G, V);
+  if (k.row <= k.gb) {
+    m.pslot = k.row;
+    roff = target_row(k.req, k.row, G, V);
     base = P.target;
   } else {
-    const int i = row - gb - 1;
+    const int i = k.row - k.gb - 1;
     m.pslot = G + 1 + i;
-    roff = draft_row(lo, i, G, V);
+    roff = draft_row(k.req, i, G, V);
     base = P.draft;
   }
   m.kind = KIND_A;
-  m.b = lo;
-  m.c = c;
-  m.n = min(AE, V - c * AE);
-  m.p0 = base + (roff + (size_t)c * AE) * EB;
+  m.b = k.req;
+  m.c = k.c;
+  m.n = min(AE, V - k.c * AE);
+  m.p0 = base + (roff + (size_t)k.c * AE) * EB;
   m.p1 = nullptr;
   m.direct = (((reinterpret_cast<uintptr_t>(m.p0)) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-  if (MODE == MODE_SAMPLE) {
-    unsigned int fl = 0;
-    const TempC tc = temp_consts(sanitize_temperature(P.temperature[lo], fl));
-    m.c_hi = tc.hi;
-    m.c_lo = tc.lo;
-  }
+  m.c_hi = c_hi;
+  m.c_lo = c_lo;
 }
 
 // Complete R item m (request m.b, chunk m.c) from its request's decision.
@@ -1023,6 +1103,7 @@ __device__ __forceinline__ void fill_r_item(const Params& P, const Decision& d, 
   const int G = P.G, V = P.V, req = m.b, c = m.c;
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   const int reject = (d.reject && k < G) ? 1 : 0;
+  m.kind = KIND_R;
   m.pslot = k;
   m.reject = reject;
   m.n = min(RE, V - c * RE);
@@ -1046,9 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   int* rowpre = reinterpret_cast<int*>(dsmem + kWarps * kNB * kItemBytes);  // [B+1]
   __shared__ __align__(8) uint64_t bar[kWarps][kNB];
-  __shared__ Meta meta[kWarps][kNB];   // the item in each buffer
-  __shared__ Meta batchq[kWarps][kMaxK];  // the warp's current batch
-  __shared__ Decision dcache[kWarps];  // the last decision the warp fetched
+  __shared__ Meta meta[kWarps][kNB];     // the item in each buffer
   __shared__ int2 defq[kWarps][kDefer];  // deferred R items (request, chunk)
   __shared__ int sh_carry;
   __shared__ int wsum[kWarps];
@@ -1057,6 +1136,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = P.G, B = P.B, NC = P.NC;
+  const int NCR = MODE == MODE_SAMPLE ? P.NCR : 1;
 
   if (tid == 0) {
     rowpre[0] = 0;
@@ -1090,38 +1170,40 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     __syncthreads();
   }
 
-  Sched sc;
-  sc.rowpre = rowpre;
-  sc.B = B;
-  sc.NC = NC;
-  sc.NCR = MODE == MODE_SAMPLE ? P.NCR : 0;
   const unsigned int nA = (unsigned int)rowpre[B] * NC;
-  sc.nA = nA;
-  sc.total = nA + (MODE == MODE_SAMPLE ? (unsigned int)B * P.NCR : 0u);
+  const unsigned int total = nA + (MODE == MODE_SAMPLE ? (unsigned int)B * NCR : 0u);
   const unsigned int nwarps = gridDim.x * kWarps;
-  // batches: about 1/16 of a warp's share, at most 8 items
-  const unsigned int K = min((unsigned int)kMaxK, max(1u, sc.total / (nwarps * 16u)));
+  // batches: about 1/kBatchDiv of a warp's share, at most kMaxK items
+  const unsigned int K = min((unsigned int)kMaxK, max(1u, total / (nwarps * kBatchDiv)));
+  int D = 1;  // requests whose A items may still be in flight when the tail starts
   {
-    // requests whose A items may still be in flight when the tail starts
     const double per_req = (double)nA / (double)(B > 0 ? B : 1);
-    const int D = (int)ceil((double)nwarps * (kNB + K) / per_req) + 1;
-    sc.D = D < B ? D : B - 1;
+    D = (int)ceil((double)nwarps * (kNB + K) / per_req) + 1;
+    D = D < B ? D : B - 1;
   }
 
   unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
   uint64_t* mybar = bar[warp];
   Meta* mymeta = meta[warp];
+  int2* mydef = defq[warp];
 
   unsigned int nb = 0;  // lane 0: start of the pre-claimed next batch
   if (lane == 0) nb = atomicAdd(P.next_item, K);
 
-  Meta* myq = batchq[warp];
-  int qlen = 0, qhead = 0;
-  bool more = true;  // batches may remain
+  Cursor cur;
+  cur.j = 0;
+  unsigned int cur_end = 0;  // the current batch is [cur.j, cur_end)
+  int a_tb = -1;             // request whose temperature constants are in a_hi/a_lo
+  float a_hi = 0.0f, a_lo = 0.0f;
+  bool more = true;          // batches may remain
   unsigned int issued = 0, processed = 0;
-  int dec_b = -1;  // request whose decision is in dcache[warp] (warp-uniform)
+  int dec_b = -1;            // request whose decision is in dc (warp-uniform)
+  Decision dc;
+  dc.k = 0;
+  int defhead = 0, ndef = 0;  // ring of deferred R items (warp-uniform)
+  bool blocked = false;       // waiting for the oldest deferred item's decision
   int acc_kind = KIND_A, acc_b = 0;
-  unsigned int acc_n = 0;  // arrivals held for (acc_kind, acc_b)
+  unsigned int acc_n = 0;     // arrivals held for (acc_kind, acc_b)
   unsigned int flags = 0;
   bool failed = false;
 
@@ -1151,9 +1233,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     settle();
     if (lane == 0) {
       unsigned int* cnt = acc_kind == KIND_A ? &P.cnt_a[acc_b] : &P.cnt_r[acc_b];
-      pend_total = acc_kind == KIND_A
-          ? (unsigned int)(rowpre[acc_b + 1] - rowpre[acc_b]) * (unsigned int)NC
-          : (unsigned int)P.NCR;
+      pend_total = acc_kind == KIND_A ? (unsigned int)rows_of<MODE>(rowpre, acc_b) * (unsigned int)NC
+                                      : (unsigned int)NCR;
       pend_n = acc_n;
       pend_old = atom_add_acq_rel(cnt, acc_n);
     }
@@ -1162,43 +1243,47 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     acc_n = 0;
   };
 
-  int2* mydef = defq[warp];
-  int defhead = 0, ndef = 0;  // ring of deferred R items (warp-uniform)
-  bool blocked = false;       // waiting for the oldest deferred item's decision
-
-  // Is request b decided?  If so its decision is fetched into dcache[warp].
+  // Is request b decided?  If so its decision is fetched into dc.
   auto decided = [&](int b) -> bool {
     if (b == dec_b) return true;
     unsigned int ok = 0;
+    Decision d;
+    d.k = 0;
     if (lane == 0 && ld_acquire(&P.ready[b])) {
       ok = 1;
-      dcache[warp] = load_decision(&P.dec[b]);
+      d = load_decision(&P.dec[b]);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    if (ok) dec_b = b;
+    if (ok) {
+      dc.k = __shfl_sync(0xffffffffu, d.k, 0);
+      dc.reject = __shfl_sync(0xffffffffu, d.reject, 0);
+      dc.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+      dc.md = __shfl_sync(0xffffffffu, d.md, 0);
+      dc.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+      dc.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+      dc.c_hi = __shfl_sync(0xffffffffu, d.c_hi, 0);
+      dc.c_lo = __shfl_sync(0xffffffffu, d.c_lo, 0);
+      dec_b = b;
+    }
     return ok != 0;
   };
 
-  // Lane 0 completes the item (R items from dcache[warp]) and starts its copy
-  // into the next buffer.
-  auto issue = [&](const Meta& item) {
+  // Start the copy of item m into the next buffer (lane 0).
+  auto issue = [&](const Meta& m) {
     const int s = (int)(issued % kNB);
     if (lane == 0) {
-      Meta mine = item;
-      if (MODE == MODE_SAMPLE && mine.kind == KIND_R) fill_r_item<EB>(P, dcache[warp], mine);
-      mymeta[s] = mine;
+      mymeta[s] = m;
       unsigned char* dst = mybuf + s * kItemBytes;
-      // order earlier generic reads of this buffer before the async-proxy write
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (mine.direct) {
+      // The buffer's previous item was fully read: its values were consumed by
+      // the reductions before the __syncwarp that ended its processing.
+      if (m.direct) {
         mbar_arrive(&mybar[s]);
       } else {
-        const unsigned int bytes = (unsigned int)(mine.n * EB);
-        const bool two = mine.kind == KIND_R && mine.p1 != nullptr;
+        const unsigned int bytes = (unsigned int)(m.n * EB);
+        const bool two = m.kind == KIND_R && m.p1 != nullptr;
         mbar_arrive_expect_tx(&mybar[s], two ? 2 * bytes : bytes);
-        bulk_copy_g2s(dst, mine.p0, bytes, &mybar[s]);
-        if (two) bulk_copy_g2s(dst + kHalfBytes, mine.p1, bytes, &mybar[s]);
+        bulk_copy_g2s(dst, m.p0, bytes, &mybar[s]);
+        if (two) bulk_copy_g2s(dst + kHalfBytes, m.p1, bytes, &mybar[s]);
       }
     }
     __syncwarp();
@@ -1208,13 +1293,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   while (!failed) {
     // 1. keep kNB copies in flight
     while (!blocked && issued - processed < (unsigned int)kNB) {
-      if (qhead == qlen) {
+      if (cur.j == cur_end) {
         // batch boundary: first the oldest deferred R item, if now decided
-        if (ndef > 0 && decided(mydef[defhead].x)) {
+        if (MODE == MODE_SAMPLE && ndef > 0 && decided(mydef[defhead].x)) {
           Meta r;
-          r.kind = KIND_R;
           r.b = mydef[defhead].x;
           r.c = mydef[defhead].y;
+          fill_r_item<EB>(P, dc, r);
           issue(r);
           defhead = (defhead + 1) % kDefer;
           --ndef;
@@ -1222,36 +1307,50 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         }
         if (more) {
           const unsigned int base = __shfl_sync(0xffffffffu, nb, 0);
-          if (base >= sc.total) {
+          if (base >= total) {
             more = false;
           } else {
-            qlen = (int)min(K, sc.total - base);
-            qhead = 0;
-            if (lane < qlen) decode_item<EB, MODE>(P, sc, base + lane, myq[lane]);
+            cursor_seek<MODE>(cur, base, rowpre, B, NC, NCR, nA);
+            cur_end = min(base + K, total);
             if (lane == 0) nb = atomicAdd(P.next_item, K);  // pre-claim the next batch
-            __syncwarp();
           }
         }
-        if (qhead == qlen) {
+        if (cur.j == cur_end) {
           if (ndef > 0) blocked = true;  // only deferred items remain
           break;
         }
       }
-      const Meta& it = myq[qhead];
-      if (MODE == MODE_SAMPLE && it.kind == KIND_R && !decided(it.b)) {
-        // not decided yet: set it aside and keep streaming later items
-        if (ndef == kDefer) {
-          blocked = true;
-          break;
+      if (MODE == MODE_SAMPLE && cur.j >= nA) {
+        // R item: its request's rows depend on the decision
+        Meta r;
+        r.b = (2 * B - 1 - D - cur.rank) % B;
+        r.c = cur.c;
+        if (decided(r.b)) {
+          fill_r_item<EB>(P, dc, r);
+          issue(r);
+        } else {
+          // not decided yet: set it aside and keep streaming later items
+          if (ndef == kDefer) {
+            blocked = true;
+            break;
+          }
+          if (lane == 0) mydef[(defhead + ndef) % kDefer] = make_int2(r.b, r.c);
+          __syncwarp();
+          ++ndef;
         }
-        if (lane == 0) mydef[(defhead + ndef) % kDefer] = make_int2(it.b, it.c);
-        __syncwarp();
-        ++ndef;
-        ++qhead;
-        continue;
+      } else {
+        if (MODE == MODE_SAMPLE && cur.req != a_tb) {
+          unsigned int fl = 0;
+          const TempC tc = temp_consts(sanitize_temperature(P.temperature[cur.req], fl));
+          a_hi = tc.hi;
+          a_lo = tc.lo;
+          a_tb = cur.req;
+        }
+        Meta a;
+        a_item_at<EB, MODE>(P, cur, a_hi, a_lo, a);
+        issue(a);
       }
-      issue(it);
-      ++qhead;
+      cursor_next<MODE>(cur, rowpre, NC, NCR, nA);
     }
 
     // 2. process the oldest item in flight
@@ -1309,7 +1408,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       blocked = false;
       continue;
     }
-    if (!more && qhead == qlen && ndef == 0) break;  // all work done
+    if (!more && cur.j == cur_end && ndef == 0) break;  // all work done
   }
 
   // No copy may still be landing in this warp's buffers when it leaves.
