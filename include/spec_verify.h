@@ -72,7 +72,9 @@ enum {
   SV_ERR_NULL = -2,      /* a required pointer is NULL */
   SV_ERR_ALIGN = -3,     /* a pointer is not aligned to its element (workspace: 256 bytes) */
   SV_ERR_WORKSPACE = -4, /* ws_bytes < spec_verify_workspace_size(B, G, V) */
-  SV_ERR_CUDA = -5       /* the kernel launch failed (cudaGetLastError) */
+  SV_ERR_CUDA = -5,      /* the kernel launch failed (cudaGetLastError) */
+  SV_ERR_STATIC_LIMIT = -6 /* spec_verify_sample_noalloc: the sizes need more scratch than
+                              SV_NOALLOC_SCRATCH_BYTES */
 };
 
 /* Status-word bits set on the device for invalid values inside arrays. */
@@ -90,6 +92,8 @@ enum {
 
 #define SV_MAX_GAMMA 31
 #define SV_MAX_VOCAB (1 << 24)
+/* Size of the scratch array built into the library for spec_verify_sample_noalloc. */
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /*
  * Bytes of device workspace that spec_verify_sample / spec_verify_greedy need
@@ -126,6 +130,47 @@ int spec_verify_greedy(const void *target_logits, sv_dtype dtype, int B, int G, 
                        const int32_t *draft_tokens, const int32_t *gamma,
                        int32_t *out_tokens, int32_t *num_accepted, void *workspace,
                        size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * spec_verify_sample_noalloc: spec_verify_sample with no caller workspace.
+ * The pages on speculative decoding describe no such call: this is a
+ * convenience of this library's interface, not a step of the method.
+ *
+ * Who needs it: callers that may not obtain device memory when they verify.
+ * A serving loop that handed all free device memory to weights and the KV
+ * cache when it started, and must not grow its footprint later, is one; C
+ * code that drives this library without any device allocator of its own is
+ * another.  This call allocates and frees nothing.
+ *
+ * Scratch: an array of SV_NOALLOC_SCRATCH_BYTES (4 MiB) that lives in the
+ * library's device image.  If spec_verify_workspace_size(B, G, V) is larger,
+ * the call returns SV_ERR_STATIC_LIMIT and runs nothing (4 MiB holds, for
+ * example, B = 512 requests with G = 3 and V = 128256).
+ *
+ * First call on a device: it looks up the array's device address with
+ * cudaGetSymbolAddress while that device is current and keeps it for later
+ * calls on the same device (SV_ERR_CUDA if the look-up fails).  Make that
+ * first call before any stream capture begins.
+ *
+ * Sharing: every call in the process uses the same array.  Each call first
+ * zeroes the array's counters and flags (an asynchronous memset on `stream`),
+ * then launches the same kernel as spec_verify_sample; the per-chunk partial
+ * results stay in the array as the last call left them.  Calls that can
+ * overlap on the GPU (other streams without ordering between them, other host
+ * threads) race on the array and produce wrong results: issue them in order
+ * on one stream.  Because of the memset, the status bits of spec_verify_status
+ * are not available from this call; invalid device values are still clamped
+ * as described at the top of this file.
+ *
+ * Arguments, layouts and the other return codes: as spec_verify_sample,
+ * without workspace and ws_bytes.
+ */
+int spec_verify_sample_noalloc(const void *target_logits, const void *draft_logits,
+                               sv_dtype dtype, int B, int G, int V,
+                               const int32_t *draft_tokens, const int32_t *gamma,
+                               const float *uniforms, const float *temperature,
+                               int32_t *out_tokens, int32_t *num_accepted, double *p_tok,
+                               double *q_tok, sv_stream_t stream);
 
 /*
  * Copies the workspace's status word (SV_STATUS_* bits accumulated since the

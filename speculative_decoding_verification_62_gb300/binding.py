@@ -20,8 +20,9 @@ SV_MAX_GAMMA = 31
 SV_MAX_VOCAB = 1 << 24
 STATUS_BITS = {1: "BAD_GAMMA", 2: "BAD_TOKEN", 4: "BAD_UNIFORM", 8: "BAD_TEMPERATURE",
                16: "NONFINITE_ROW", 32: "INTERNAL", 64: "TIMEOUT"}
+SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy",
-           "spec_verify_status", "spec_verify_strerror")
+           "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror")
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +49,9 @@ def load_library():
                                            vp, vp, sz, vp]
         lib.spec_verify_greedy.restype = ci
         lib.spec_verify_greedy.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_sample_noalloc.restype = ci
+        lib.spec_verify_sample_noalloc.argtypes = [vp, vp, ci, ci, ci, ci, vp, vp, vp, vp, vp,
+                                                   vp, vp, vp, vp]
         lib.spec_verify_status.restype = ci
         lib.spec_verify_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.spec_verify_strerror.restype = ctypes.c_char_p
@@ -120,6 +124,31 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, gamma, uniform
         _dev(q_tok, "q_tok", torch.float64, (B, G)),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     rc = load_library().spec_verify_sample(*args)
+    if rc != 0:
+        raise SpecVerifyError(rc)
+
+
+def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, gamma, uniforms,
+                               temperature, out_tokens, num_accepted, p_tok=None, q_tok=None,
+                               stream=None) -> None:
+    """Sampling verify step on the library's built-in scratch array (no workspace)."""
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    code = _dtype_code(target_logits)
+    args = (
+        _dev(target_logits, "target_logits"),
+        _dev(draft_logits, "draft_logits", target_logits.dtype, (B, G, V)),
+        code, B, G, V,
+        _dev(draft_tokens, "draft_tokens", torch.int32, (B, G)),
+        _dev(gamma, "gamma", torch.int32, (B,)),
+        _dev(uniforms, "uniforms", torch.float32, (B, G + 1)),
+        _dev(temperature, "temperature", torch.float32, (B,)),
+        _dev(out_tokens, "out_tokens", torch.int32, (B, G + 1)),
+        _dev(num_accepted, "num_accepted", torch.int32, (B,)),
+        _dev(p_tok, "p_tok", torch.float64, (B, G)),
+        _dev(q_tok, "q_tok", torch.float64, (B, G)),
+        _stream(stream))
+    rc = load_library().spec_verify_sample_noalloc(*args)
     if rc != 0:
         raise SpecVerifyError(rc)
 

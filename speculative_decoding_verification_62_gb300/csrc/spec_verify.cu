@@ -44,6 +44,7 @@
 // so chunk sums and the final in-chunk scan agree bit for bit.
 
 #include <cuda_runtime.h>
+#include <mutex>
 #include <stdint.h>
 #include <math.h>
 #include <float.h>
@@ -1542,6 +1543,32 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   return SV_OK;
 }
 
+// Scratch for spec_verify_sample_noalloc: part of the library's device
+// image, so using it allocates nothing.  Its device address is looked up once
+// per device.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char sv_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> guard(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, sv_noalloc_scratch) != cudaSuccess || !p) return SV_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1589,6 +1616,34 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, 
   return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);
 }
 
+int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                               sv_dtype dtype, int B, int G, int V,
+                               const int32_t* draft_tokens, const int32_t* gamma,
+                               const float* uniforms, const float* temperature,
+                               int32_t* out_tokens, int32_t* num_accepted, double* p_tok,
+                               double* q_tok, sv_stream_t stream) {
+  int rc = check_scalars(dtype, B, G, V);
+  if (rc) return rc;
+  if (!target_logits || !gamma || !uniforms || !temperature || !out_tokens || !num_accepted)
+    return SV_ERR_NULL;
+  if (G > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL;
+  const Layout L = make_layout(B, G, V);
+  if (L.total > (size_t)SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_STATIC_LIMIT;
+  if (B == 0) return SV_OK;
+  void* ws = nullptr;
+  rc = noalloc_scratch(&ws);
+  if (rc) return rc;
+  Params P;
+  rc = fill_params(P, target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma, uniforms,
+                   temperature, out_tokens, num_accepted, p_tok, q_tok, ws,
+                   (size_t)SV_NOALLOC_SCRATCH_BYTES);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // counters, arrival counts and decision flags start at zero for every call
+  if (cudaMemsetAsync(ws, 0, L.dec, s) != cudaSuccess) return SV_ERR_CUDA;
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
+}
+
 int spec_verify_status(void* workspace, sv_stream_t stream, uint32_t* status_host) {
   if (!workspace || !status_host) return SV_ERR_NULL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1608,6 +1663,7 @@ const char* spec_verify_strerror(int code) {
     case SV_ERR_ALIGN: return "a pointer is not suitably aligned";
     case SV_ERR_WORKSPACE: return "workspace smaller than spec_verify_workspace_size()";
     case SV_ERR_CUDA: return "CUDA launch or copy failed";
+    case SV_ERR_STATIC_LIMIT: return "sizes need more scratch than the built-in 4 MiB array";
     default: return "unknown error code";
   }
 }

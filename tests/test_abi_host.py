@@ -91,8 +91,23 @@ def test_greedy_host_errors():
     assert call(B=0) == 0
 
 
+def test_noalloc_rejects_sizes_beyond_its_scratch_without_cuda():
+    lib = binding.load_library()
+    f = _fake()
+    call = lambda B, G, V, **k: lib.spec_verify_sample_noalloc(  # noqa: E731
+        k.get("t", f), f, 1, B, G, V, f, f, f, f, f, f, None, None, None)
+    too_big = (4096, 7, 128256)
+    assert binding.spec_verify_workspace_size(*too_big) > binding.SV_NOALLOC_SCRATCH_BYTES
+    assert call(*too_big) == -6
+    assert "4 MiB" in binding.spec_verify_strerror(-6)
+    assert binding.spec_verify_workspace_size(512, 3, 128256) <= binding.SV_NOALLOC_SCRATCH_BYTES
+    assert call(2, 3, 64, t=None) == -2
+    assert call(2, 32, 64) == -1
+    assert call(0, 3, 64) == 0  # B == 0: nothing to do, no CUDA call
+
+
 def test_strerror_texts():
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert binding.spec_verify_strerror(code)
     assert "unknown" in binding.spec_verify_strerror(-99)
 
