@@ -64,10 +64,10 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kNB = SV_BUFFERS;                       // TMA buffers per warp
 constexpr int kItemBytes = 8192;                      // A item: 8 KB of one row
 constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
-constexpr int kMaxBatch = 4096;                       // requests per launch (smem prefix)
-constexpr int kMaxK = 8;                              // work items per claimed batch
+constexpr int kMaxBatch = 2048;                       // requests per launch (smem tables)
+constexpr int kMaxK = 8;                              // A items per claimed batch
+constexpr unsigned int kMaxRBatch = 4;                // R items per claim, at most
 constexpr unsigned int kBatchDiv = 4;                 // batches per warp's share, at least
-constexpr int kDefer = 32;                            // deferred R items per warp
 constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
 constexpr float kFix = 549755813888.0f;               // 2^39: fixed-point scale of probabilities
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
@@ -79,17 +79,28 @@ enum { MODE_SAMPLE = 0, MODE_GREEDY = 1 };
 // ---------------------------------------------------------------------------
 // Workspace
 // ---------------------------------------------------------------------------
-struct Decision {      // per request, published by the deciding warp
+// Per-request decision.
+struct Decision {
   int k;               // first rejected position (gamma_b if none)
   int reject;          // 1: residual at k; 0: bonus from target row k = gamma_b
   float mt, md;        // maxima of target row k and draft row k
-  float inv_st, rho;   // 1/S_t and S_t/S_d of those rows (float64-derived)
+  float inv_st, rho;   // 1/S_t and S_t/S_d of those rows (from float-float sums)
   float c_hi, c_lo;    // log2(e)/T as hi + lo
+};
+// A published decision in the workspace: two 16-byte halves, each written and
+// read with one 128-bit atomic and each carrying the tag kDecTag | reject << 8
+// | k, so a reader that finds both tags set holds a consistent record without
+// further ordering.  The same record serves as a request's own entry and as
+// an entry of the decision queue (which also names the request).
+constexpr uint32_t kDecTag = 0x80000000u;
+struct __align__(16) DecRecord {
+  uint32_t tag_a; int b; float mt, md;
+  uint32_t tag_b; float inv_st, rho; uint32_t pad;
 };
 
 struct Layout {
-  size_t status, next_item, exit_count;  // header words
-  size_t cnt_a, cnt_r, ready, dec, stats, resid, total;
+  size_t status, next_item, exit_count, r_next, q_tail;  // header words
+  size_t cnt_a, cnt_r, dec, queue, stats, resid, total;
   int NC, NCR;  // worst-case chunk counts (float32 logits)
 };
 
@@ -99,16 +110,19 @@ __host__ __device__ inline Layout make_layout(int B, int G, int V) {
   Layout L;
   L.NC = (V + kItemBytes / 4 - 1) / (kItemBytes / 4);
   L.NCR = (V + kHalfBytes / 4 - 1) / (kHalfBytes / 4);
+  // header words on separate 128-byte lines
   L.status = 0;
-  L.next_item = 64;
-  L.exit_count = 128;
-  size_t off = 256;
+  L.next_item = 128;
+  L.exit_count = 256;
+  L.r_next = 384;
+  L.q_tail = 512;
+  size_t off = 1024;
   L.cnt_a = off; off = align256(off + (size_t)B * 4);
   L.cnt_r = off; off = align256(off + (size_t)B * 4);
-  L.ready = off; off = align256(off + (size_t)B * 4);
-  L.dec = off;   off = align256(off + (size_t)B * sizeof(Decision));
+  L.dec = off;   off = align256(off + (size_t)B * sizeof(DecRecord));
+  L.queue = off; off = align256(off + (size_t)B * sizeof(DecRecord));
   L.stats = off; off = align256(off + (size_t)B * (2 * G + 1) * L.NC * sizeof(float2));
-  L.resid = off; off = align256(off + (size_t)B * L.NCR * sizeof(ulonglong2));
+  L.resid = off; off = align256(off + (size_t)B * L.NCR * sizeof(unsigned long long));
   L.total = off;
   return L;
 }
@@ -127,14 +141,17 @@ struct Params {
   double* p_tok;
   double* q_tok;
   unsigned int* status;
-  unsigned int* next_item;   // next work item to claim
+  unsigned int* next_item;   // next A item to claim (past the fixed first batches)
+  unsigned int* r_next;      // next R item to claim: item i is chunk i % NCR of the
+                             // request in queue slot i / NCR
+  unsigned int* q_tail;      // decisions published to the queue
   unsigned int* exit_count;
   unsigned int* cnt_a;       // [B] A items completed
   unsigned int* cnt_r;       // [B] R items completed
-  unsigned int* ready;       // [B] 1 once the request's decision is published
-  Decision* dec;
-  float2* stats;       // [B][2G+1][stride_nc]: (max, sum) or (max, argmax bits)
-  ulonglong2* resid;   // [B][stride_ncr]: (residual sum, p sum)
+  DecRecord* dec;            // [B] decision of each request (tags 0 until decided)
+  DecRecord* queue;          // [B] decisions in the order they were made
+  float2* stats;              // [B][2G+1][stride_nc]: (max, sum) or (max, argmax bits)
+  unsigned long long* resid;  // [B][stride_ncr]: fixed-point sum of the draw weights
 };
 
 // A decoded work item (one per lane of a claimed batch; stored per buffer).
@@ -196,6 +213,10 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void sts128(void* p, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+               ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 __device__ __forceinline__ uint4 lds128(const void* p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -211,6 +232,11 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsign
 }
 __device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_relaxed(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
   unsigned int v;
@@ -268,25 +294,47 @@ __device__ __forceinline__ uint32_t bf16x2_eq(uint32_t a, uint32_t b) {
   asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-__device__ __forceinline__ uint32_t vec_word(const uint4& v, int q) {
-  return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+
+// 128-bit atomics on global memory: a 16-byte exchange, and a 16-byte read as
+// a compare-and-swap of zero with zero (it never changes the value).
+__device__ __forceinline__ void atom_store_b128(void* p, uint4 v) {
+  const unsigned long long lo = ((unsigned long long)v.y << 32) | v.x;
+  const unsigned long long hi = ((unsigned long long)v.w << 32) | v.z;
+  asm volatile(
+      "{\n .reg .b128 nv, ov;\n mov.b128 nv, {%1, %2};\n"
+      " atom.relaxed.gpu.global.exch.b128 ov, [%0], nv;\n}\n"
+      ::"l"(p), "l"(lo), "l"(hi) : "memory");
+}
+__device__ __forceinline__ uint4 atom_load_b128(const void* p) {
+  unsigned long long lo, hi;
+  const unsigned long long z = 0ull;
+  asm volatile(
+      "{\n .reg .b128 cz, ov;\n mov.b128 cz, {%2, %2};\n"
+      " atom.relaxed.gpu.global.cas.b128 ov, [%3], cz, cz;\n mov.b128 {%0, %1}, ov;\n}\n"
+      : "=l"(lo), "=l"(hi) : "l"(z), "l"(p) : "memory");
+  return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
 }
 
-// Decision record read through L2 (it was written by another CTA).
-__device__ __forceinline__ Decision load_decision(const Decision* p) {
-  static_assert(sizeof(Decision) == 32, "Decision is two 16-byte words");
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-  const uint4 a = __ldcg(q), b = __ldcg(q + 1);
-  Decision d;
-  d.k = (int)a.x;
-  d.reject = (int)a.y;
+__device__ __forceinline__ void write_record(DecRecord* r, int b, const Decision& d) {
+  const uint32_t tag = kDecTag | ((uint32_t)d.reject << 8) | (uint32_t)d.k;
+  atom_store_b128(&r->tag_b, make_uint4(tag, __float_as_uint(d.inv_st), __float_as_uint(d.rho), 0u));
+  atom_store_b128(&r->tag_a, make_uint4(tag, (uint32_t)b, __float_as_uint(d.mt), __float_as_uint(d.md)));
+}
+
+// A published record (both halves, one round trip): its request and decision
+// (without the temperature constants).  False while it is not yet complete.
+__device__ __forceinline__ bool read_record(const DecRecord* r, int& b, Decision& d) {
+  const uint4 a = atom_load_b128(&r->tag_a);
+  const uint4 h = atom_load_b128(&r->tag_b);
+  if (!(a.x & kDecTag) || a.x != h.x) return false;
+  d.k = (int)(a.x & 0xffu);
+  d.reject = (int)((a.x >> 8) & 1u);
+  b = (int)a.y;
   d.mt = __uint_as_float(a.z);
   d.md = __uint_as_float(a.w);
-  d.inv_st = __uint_as_float(b.x);
-  d.rho = __uint_as_float(b.y);
-  d.c_hi = __uint_as_float(b.z);
-  d.c_lo = __uint_as_float(b.w);
-  return d;
+  d.inv_st = __uint_as_float(h.y);
+  d.rho = __uint_as_float(h.z);
+  return true;
 }
 
 template <int EB>
@@ -402,26 +450,72 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 }
 
 // ---------------------------------------------------------------------------
-// Residual weights (shared by R items and the final in-chunk scan)
-// r = max(0, p - q) = (1/S_t) * max(0, e_t - e_d * S_t/S_d), in fixed point.
+// Draw weights (shared by R items and the final in-chunk scan)
+// After a rejection at k the weight of a token is the residual
+// r = max(0, p - q) = (1/S_t) * max(0, e_t - e_d * S_t/S_d); for the bonus
+// draw it is p = e_t / S_t.  Weights are kept in 2^39 fixed point so that
+// chunk sums are exact and independent of summation order.
 // ---------------------------------------------------------------------------
 struct ResidC {
   float mt, md, inv_st, rho, hi, lo;
   int reject;
 };
 
-__device__ __forceinline__ void resid_weights(float zt, float zd, const ResidC& k,
-                                              unsigned long long& wr, unsigned long long& wp) {
+// round(x) (to nearest, ties to even) as an unsigned 64-bit integer, for
+// 0 <= x <= 2^39 (a weight is at most about 2^39), with float and 32-bit
+// integer operations only: the float-to-integer conversions run at a
+// fraction of the ALU rate on this GPU.  x = 2^16 y: adding 2^23 rounds y to
+// an integer held in the low mantissa bits; the remainder x - 2^16 RNE(y) is
+// exact (|rem| <= 2^15, a multiple of x's ulp) and is rounded the same way
+// with 1.5 * 2^23, which also covers negative values.  Ties go to even in
+// both steps, as 2^16 RNE(y) is even.
+__device__ __forceinline__ unsigned long long fix_round(float x) {
+  const float t = __fadd_rn(__fmul_rn(x, 1.52587890625e-05f), 8388608.0f);
+  const uint32_t yr = __float_as_uint(t) - 0x4b000000u;
+  const float rem = __fmaf_rn(-__fsub_rn(t, 8388608.0f), 65536.0f, x);
+  const int rr = (int)(__float_as_uint(__fadd_rn(rem, 12582912.0f)) - 0x4b400000u);
+  return ((unsigned long long)yr << 16) + (unsigned long long)(long long)rr;
+}
+
+// Sums of round(x) over many x, as two 32-bit sums of raw float bits (the
+// two steps of fix_round); the constant offsets are removed once per sum.
+// Exact while the sum of the x is below 2^48 (at most 64 terms of <= 2^39
+// per sum here).
+struct FixAcc {
+  uint32_t hi, lo, n;
+};
+__device__ __forceinline__ void fix_add(FixAcc& a, float x) {
+  const float t = __fadd_rn(__fmul_rn(x, 1.52587890625e-05f), 8388608.0f);
+  const float rem = __fmaf_rn(-__fsub_rn(t, 8388608.0f), 65536.0f, x);
+  a.hi += __float_as_uint(t);
+  a.lo += __float_as_uint(__fadd_rn(rem, 12582912.0f));
+  ++a.n;
+}
+__device__ __forceinline__ unsigned long long fix_value(const FixAcc& a) {
+  const uint32_t hs = a.hi - a.n * 0x4b000000u;
+  const int ls = (int)(a.lo - a.n * 0x4b400000u);
+  return ((unsigned long long)hs << 16) + (unsigned long long)(long long)ls;
+}
+
+// The draw weight of one token before rounding: x = w 2^39 for the weight w.
+template <bool REJECT>
+__device__ __forceinline__ float draw_x(float zt, float zd, const ResidC& k) {
   const float et = ex2_approx(exp_arg(zt, k.mt, k.hi, k.lo));
-  const float pv = __fmul_rn(et, k.inv_st);
-  wp = __float2ull_rn(__fmul_rn(pv, kFix));
-  if (k.reject) {
+  float v = et;
+  if (REJECT) {
     const float ed = ex2_approx(exp_arg(zd, k.md, k.hi, k.lo));
-    const float rv = __fmul_rn(fmaxf(__fmaf_rn(-ed, k.rho, et), 0.0f), k.inv_st);
-    wr = __float2ull_rn(__fmul_rn(rv, kFix));
-  } else {
-    wr = wp;
+    v = fmaxf(__fmaf_rn(-ed, k.rho, et), 0.0f);
   }
+  return __fmul_rn(__fmul_rn(v, k.inv_st), kFix);
+}
+
+template <bool REJECT>
+__device__ __forceinline__ unsigned long long draw_weight(float zt, float zd, const ResidC& k) {
+  return fix_round(draw_x<REJECT>(zt, zd, k));
+}
+
+__device__ __forceinline__ unsigned long long draw_weight(float zt, float zd, const ResidC& k) {
+  return k.reject ? draw_weight<true>(zt, zd, k) : draw_weight<false>(zt, zd, k);
 }
 
 // floor(u * S) exactly, for u a float in [0, 1).
@@ -451,6 +545,24 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
   const float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
   return ff_two_sum(s.hi, e);
 }
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+// (a.hi + a.lo) * (bh + bl)
+__device__ __forceinline__ FF ff_mul(FF a, float bh, float bl) {
+  const float p = __fmul_rn(a.hi, bh);
+  const float e = __fmaf_rn(a.hi, bh, -p);
+  const float t = __fmaf_rn(a.hi, bl, __fmaf_rn(a.lo, bh, e));
+  return ff_fast_two_sum(p, t);
+}
+// (a.hi + a.lo) / (b.hi + b.lo), rounded to float (within about one ulp)
+__device__ __forceinline__ float ff_div(FF a, FF b) {
+  const float q = __fdiv_rn(a.hi, b.hi);
+  const float r = __fmaf_rn(-q, b.hi, a.hi);  // exact remainder of the leading quotient
+  const float c = __fmaf_rn(-q, b.lo, __fadd_rn(r, a.lo));
+  return __fadd_rn(q, __fdiv_rn(c, b.hi));
+}
 __device__ __forceinline__ FF warp_sum_ff(FF v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -462,117 +574,154 @@ __device__ __forceinline__ FF warp_sum_ff(FF v) {
   return v;
 }
 
-// ---------------------------------------------------------------------------
-// Per-request decision (sampling), run by one warp: the one that completed
-// the request's last A item.
-// ---------------------------------------------------------------------------
-template <int EB>
-__device__ __noinline__ void decide_sample(const Params& P, int b) {
-  const int G = P.G, V = P.V, NC = P.NC;
-  const int lane = threadIdx.x & 31;
-  const int gb = clamp_gamma(P.gamma[b], G);
-  unsigned int flags = (P.gamma[b] != gb) ? SV_STATUS_BAD_GAMMA : 0u;
-  const float T = sanitize_temperature(P.temperature[b], flags);
-  const TempC tc = temp_consts(T);
-  const double cd = (double)tc.hi + (double)tc.lo;
-  const int nrows = 2 * gb + 1;
+// Shuffle of a float-float value.
+__device__ __forceinline__ FF shfl_xor_ff(FF v, int o) {
+  return FF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
 
-  // Row maximum M and normaliser S = sum_c s_c 2^((m_c - M) c) over the
-  // per-item partials, summed in float-float.  Lane (r & 31) keeps row r in
-  // slot r >> 5.  Four rows at a time, each lane loading chunks lane and
-  // lane + 32, so the loads of a group are in flight together.
-  float rowM[2] = {-INFINITY, -INFINITY};
-  double rowS[2] = {0.0, 0.0};
+// The per-item partials of a request's rows are reduced eight rows at a time:
+// lanes 4r..4r+3 take row r of the group, each every fourth chunk (up to
+// kHeld chunks held in registers, the rest in a tail loop).  The code is kept
+// compact: it runs once per request, usually with a cold instruction cache.
+constexpr int kHeld = 10;
+
+// Row statistics (sampling): M = max, S = sum_c s_c 2^((m_c - M) c) in
+// float-float, written to rs[r] (M), rs[64 + r] (S hi), rs[128 + r] (S lo).
+template <int EB>
+__device__ __forceinline__ unsigned int row_stats(const Params& P, int b, int gb, TempC tc,
+                                                  float* rs) {
+  const int G = P.G, NC = P.NC;
+  const int lane = threadIdx.x & 31, part = lane & 3;
+  const int nrows = 2 * gb + 1;
   const float2 none = make_float2(-INFINITY, 0.0f);
-  for (int r0 = 0; r0 < nrows; r0 += 4) {
-    float2 v[4][2];
+  unsigned int flags = 0;
+#pragma unroll 1
+  for (int r0 = 0; r0 < nrows; r0 += 8) {
+    const int r = r0 + (lane >> 2);
+    const bool live = r < nrows;
+    const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
+    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + (live ? slot : 0)) * P.stride_nc;
+    float2 v[kHeld];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int r = r0 + g;
-      const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
-      const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc;
-      v[g][0] = (r < nrows && lane < NC) ? __ldcg(&pr[lane]) : none;
-      v[g][1] = (r < nrows && lane + 32 < NC) ? __ldcg(&pr[lane + 32]) : none;
+    for (int j = 0; j < kHeld; ++j) {
+      const int c = part + 4 * j;
+      v[j] = (live && c < NC) ? __ldcg(&pr[c]) : none;
     }
+    float m = -INFINITY;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int r = r0 + g;
-      if (r >= nrows) break;
-      const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
-      const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + slot) * P.stride_nc;
-      float M = fmaxf(v[g][0].x, v[g][1].x);
-      for (int c = lane + 64; c < NC; c += 32) M = fmaxf(M, __ldcg(&pr[c]).x);
-      M = warp_max(M);
-      FF S{0.0f, 0.0f};
-      if (M > -INFINITY) {
+    for (int j = 0; j < kHeld; ++j) m = fmaxf(m, v[j].x);
+#pragma unroll 1
+    for (int c = part + 4 * kHeld; live && c < NC; c += 4) m = fmaxf(m, __ldcg(&pr[c]).x);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    FF S{0.0f, 0.0f};
+    if (m > -INFINITY) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (v[g][h].x > -INFINITY)
-            S = ff_add(S, FF{__fmul_rn(v[g][h].y, ex2_approx(exp_arg(v[g][h].x, M, tc.hi, tc.lo))), 0.0f});
-        for (int c = lane + 64; c < NC; c += 32) {
-          const float2 ms = __ldcg(&pr[c]);
-          if (ms.x > -INFINITY)
-            S = ff_add(S, FF{__fmul_rn(ms.y, ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo))), 0.0f});
-        }
+      for (int j = 0; j < kHeld; ++j)
+        if (v[j].x > -INFINITY)
+          S = ff_add(S, FF{__fmul_rn(v[j].y, ex2_approx(exp_arg(v[j].x, m, tc.hi, tc.lo))), 0.0f});
+#pragma unroll 1
+      for (int c = part + 4 * kHeld; live && c < NC; c += 4) {
+        const float2 ms = __ldcg(&pr[c]);
+        if (ms.x > -INFINITY)
+          S = ff_add(S, FF{__fmul_rn(ms.y, ex2_approx(exp_arg(ms.x, m, tc.hi, tc.lo))), 0.0f});
       }
-      S = warp_sum_ff(S);
-      const double Sd = (double)S.hi + (double)S.lo;
-      if (!isfinite(M) || !(Sd > 0.0)) flags |= SV_STATUS_NONFINITE_ROW;
-      if (lane == (r & 31)) {
-        rowM[r >> 5] = M;
-        rowS[r >> 5] = Sd;
-      }
+    }
+    S = ff_add(S, shfl_xor_ff(S, 1));
+    S = ff_add(S, shfl_xor_ff(S, 2));
+    if (live && part == 0) {
+      if (!isfinite(m) || !(S.hi > 0.0f)) flags |= SV_STATUS_NONFINITE_ROW;
+      rs[r] = m;
+      rs[64 + r] = S.hi;
+      rs[128 + r] = S.lo;
     }
   }
-  // row r's statistics, fetched from lane r & 31
-  auto row_m = [&](int r) {
-    const float a = __shfl_sync(0xffffffffu, rowM[0], r & 31);
-    const float c = __shfl_sync(0xffffffffu, rowM[1], r & 31);
-    return r < 32 ? a : c;
-  };
-  auto row_s = [&](int r) {
-    const double a = __shfl_sync(0xffffffffu, rowS[0], r & 31);
-    const double c = __shfl_sync(0xffffffffu, rowS[1], r & 31);
-    return r < 32 ? a : c;
-  };
+  __syncwarp();
+  return flags;
+}
 
-  // Acceptance test per position (lane i), then the first-reject ballot.
+// ---------------------------------------------------------------------------
+// Per-request decision (sampling), run by one warp: the one that completed
+// the request's last A item.  Float and float-float arithmetic only on the
+// common path; float64 appears where an exponent is extreme and for the
+// optional probability outputs.  rs: 192 floats of the warp's free shared
+// staging buffer.
+// ---------------------------------------------------------------------------
+
+// 2^e / S in float64, e and S float-float (the probability p(x) or q(x)).
+__device__ __noinline__ double prob_f64(FF e, FF S) {
+  if (!(e.hi > -INFINITY)) return 0.0;
+  const float n = rintf(e.hi);
+  const float f = __fadd_rn(__fsub_rn(e.hi, n), e.lo);
+  const float v = __fmul_rn(ex2_approx(f), ff_div(FF{1.0f, 0.0f}, S));
+  return ldexp((double)v, (int)fmaxf(n, -2000.0f));
+}
+
+// q(x) = 2^e / S is 0 in float64 (only reachable for e far below -1000).
+__device__ __noinline__ bool q_underflows(FF e, FF S) {
+  return exp2((double)e.hi + (double)e.lo) / ((double)S.hi + (double)S.lo) == 0.0;
+}
+
+template <int EB>
+__device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC tc, float* rs) {
+  const int G = P.G, V = P.V;
+  const int lane = threadIdx.x & 31;
   const int i = lane;
-  const int ri = i < gb ? i : 0;
-  const float mt_i = row_m(ri), md_i = row_m(gb + 1 + ri);
-  const double st_i = row_s(ri), sd_i = row_s(gb + 1 + ri);
-  bool reject = false;
-  double p = NAN, q = NAN;
+  unsigned int flags = 0;
+  // the drafted tokens, their uniforms and logits are requested first
   int x = 0;
+  float u = 0.0f, zt = 0.0f, zd = 0.0f;
   if (i < gb) {
     x = P.tokens[(size_t)b * G + i];
+    u = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + i], flags);
     if (x < 0 || x >= V) {
       flags |= SV_STATUS_BAD_TOKEN;
       x = x < 0 ? 0 : V - 1;
     }
-    const float zt = load_elem<EB>(P.target, target_row(b, i, G, V) + (size_t)x);
-    const float zd = load_elem<EB>(P.draft, draft_row(b, i, G, V) + (size_t)x);
-    const double et = ((double)zt - (double)mt_i) * cd;  // log2 of S_t p(x)
-    const double ed = ((double)zd - (double)md_i) * cd;  // log2 of S_d q(x)
-    const double u = (double)sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + i], flags);
-    // ratio p/q = 2^(et - ed) * S_d / S_t.  A draft probability q(x) that is
-    // 0 in float64 (a -inf logit, or one far enough below the maximum to
-    // underflow) accepts.
-    const bool qzero = ed == -INFINITY || (ed < -1000.0 && exp2(ed) / sd_i == 0.0);
-    const double ratio = exp2(et - ed) * (sd_i / st_i);
-    reject = !(qzero || (u < ratio));
+    zt = load_elem<EB>(P.target, target_row(b, i, G, V) + (size_t)x);
+    zd = load_elem<EB>(P.draft, draft_row(b, i, G, V) + (size_t)x);
+  }
+  flags |= row_stats<EB>(P, b, gb, tc, rs);
+
+  // Acceptance test per position (lane i), then the first-reject ballot.
+  // ratio p/q = 2^(e_t - e_d) * S_d / S_t with e = (z - m) log2(e)/T in
+  // float-float; 2^(e_t - e_d) = 2^n * 2^f with |f| <= 1/2.
+  bool reject = false;
+  double p = NAN, q = NAN;
+  if (i < gb) {
+    const float mt = rs[i], md = rs[gb + 1 + i];
+    const FF st{rs[64 + i], rs[128 + i]}, sd{rs[64 + gb + 1 + i], rs[128 + gb + 1 + i]};
+    const FF et = ff_mul(ff_two_sum(zt, -mt), tc.hi, tc.lo);  // log2 of S_t p(x)
+    const FF ed = ff_mul(ff_two_sum(zd, -md), tc.hi, tc.lo);  // log2 of S_d q(x)
+    bool accept;
+    if (!(zd > -INFINITY)) {
+      accept = true;  // q(x) = 0 accepts
+    } else if (!(zt > -INFINITY)) {
+      accept = false;  // p(x) = 0: the ratio is 0
+    } else if (ed.hi < -1000.0f && q_underflows(ed, sd)) {
+      accept = true;  // q(x) is 0 in float64
+    } else {
+      const FF e = ff_add(et, FF{-ed.hi, -ed.lo});
+      float ratio;
+      if (e.hi >= 256.0f) {
+        ratio = INFINITY;
+      } else if (e.hi <= -256.0f) {
+        ratio = 0.0f;
+      } else {
+        const float n = rintf(e.hi);
+        const float f = __fadd_rn(__fsub_rn(e.hi, n), e.lo);
+        ratio = ldexpf(__fmul_rn(ex2_approx(f), ff_div(sd, st)), (int)n);
+      }
+      accept = u < ratio;
+    }
+    reject = !accept;
     if (P.p_tok || P.q_tok) {
-      p = exp2(et) / st_i;
-      q = exp2(ed) / sd_i;
+      p = (zt > -INFINITY) ? prob_f64(et, st) : 0.0;
+      q = (zd > -INFINITY) ? prob_f64(ed, sd) : 0.0;
     }
   }
   const unsigned int rej = __ballot_sync(0xffffffffu, reject);
   const int k = rej ? (__ffs(rej) - 1) : gb;
-  const float mt_k = row_m(k);
-  const double st_k = row_s(k);
-  const int kd = gb + 1 + (k < gb ? k : 0);
-  const float md_k = row_m(kd);
-  const double sd_k = row_s(kd);
   if (i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
   if (i < G) {
     const bool evaluated = i < gb && i <= k;
@@ -581,57 +730,76 @@ __device__ __noinline__ void decide_sample(const Params& P, int b) {
   }
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0) {
+    const int kd = gb + 1 + (k < gb ? k : 0);
+    const FF st_k{rs[64 + k], rs[128 + k]}, sd_k{rs[64 + kd], rs[128 + kd]};
     P.num_accepted[b] = k;
     Decision d;
     d.k = k;
     d.reject = k < gb ? 1 : 0;
-    d.mt = mt_k;
-    d.md = d.reject ? md_k : 0.0f;
-    d.inv_st = (float)(1.0 / st_k);
-    d.rho = d.reject ? (float)(st_k / sd_k) : 0.0f;
+    d.mt = rs[k];
+    d.md = d.reject ? rs[kd] : 0.0f;
+    d.inv_st = ff_div(FF{1.0f, 0.0f}, st_k);
+    d.rho = d.reject ? ff_div(st_k, sd_k) : 0.0f;
     d.c_hi = tc.hi;
     d.c_lo = tc.lo;
-    P.dec[b] = d;
     if (any) atomicOr(P.status, any);
     P.cnt_a[b] = 0;
-    // publish the decision
-    __threadfence();
-    st_release(&P.ready[b], 1u);
+    write_record(&P.dec[b], b, d);
+    write_record(&P.queue[atomicAdd(P.q_tail, 1u)], b, d);
   }
   __syncwarp();
 }
 
-// Greedy decision: argmax per target row from the per-item partials, then the
+// Greedy decision: argmax per target row from the per-item partials (rows
+// reduced eight at a time as above; rs holds the row argmaxes), then the
 // first mismatch by warp ballot.
-__device__ __noinline__ void decide_greedy(const Params& P, int b) {
+__device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* rs) {
   const int G = P.G, V = P.V, NC = P.NC;
-  const int lane = threadIdx.x & 31;
-  const int gb = clamp_gamma(P.gamma[b], G);
-  unsigned int flags = (P.gamma[b] != gb) ? SV_STATUS_BAD_GAMMA : 0u;
-  int g_mine = 0;  // lane r holds the argmax of row r
-  for (int r = 0; r <= gb; ++r) {
-    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + r) * P.stride_nc;
-    float v = -INFINITY;
-    int idx = 0x7fffffff;
-    for (int c = lane; c < NC; c += 32) {
-      const float2 mi = __ldcg(&pr[c]);
-      argmax_combine(v, idx, mi.x, __float_as_int(mi.y));
-    }
-    warp_argmax(v, idx);
-    if (!isfinite(v)) flags |= SV_STATUS_NONFINITE_ROW;
-    if (lane == r) g_mine = (idx >= 0 && idx < V) ? idx : 0;
-  }
+  const int lane = threadIdx.x & 31, part = lane & 3;
+  unsigned int flags = 0;
   const int i = lane;
   int x = 0;
+  if (i < gb) x = P.tokens[(size_t)b * G + i];
+#pragma unroll 1
+  for (int r0 = 0; r0 <= gb; r0 += 8) {
+    const int r = r0 + (lane >> 2);
+    const bool live = r <= gb;
+    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + (live ? r : 0)) * P.stride_nc;
+    float2 v[kHeld];
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j) {
+      const int c = part + 4 * j;
+      v[j] = (live && c < NC) ? __ldcg(&pr[c]) : make_float2(-INFINITY, __int_as_float(0x7fffffff));
+    }
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j) argmax_combine(bv, bi, v[j].x, __float_as_int(v[j].y));
+#pragma unroll 1
+    for (int c = part + 4 * kHeld; live && c < NC; c += 4) {
+      const float2 mi = __ldcg(&pr[c]);
+      argmax_combine(bv, bi, mi.x, __float_as_int(mi.y));
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      argmax_combine(bv, bi, v2, i2);
+    }
+    if (live && part == 0) {
+      if (!isfinite(bv)) flags |= SV_STATUS_NONFINITE_ROW;
+      rs[r] = (bi >= 0 && bi < V) ? bi : 0;
+    }
+  }
+  __syncwarp();
   bool mismatch = false;
   if (i < gb) {
-    x = P.tokens[(size_t)b * G + i];
     if (x < 0 || x >= V) flags |= SV_STATUS_BAD_TOKEN;
-    mismatch = x != g_mine;
+    mismatch = x != rs[i];
   }
   const unsigned int mm = __ballot_sync(0xffffffffu, mismatch);
   const int k = mm ? (__ffs(mm) - 1) : gb;
-  const int gk = __shfl_sync(0xffffffffu, g_mine, k);
+  const int gk = rs[k];
   if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? gk : -1);
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0) {
@@ -644,110 +812,194 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b) {
 
 // Final draw for request b, run by the warp that completed its last R item:
 // the chunk whose prefix passes u*S, then a scan of that chunk only.
+// Sum over R chunk c of the draw weights, read from global memory by the
+// whole warp.
 template <int EB>
-__device__ __noinline__ void final_draw(const Params& P, int b) {
+__device__ unsigned long long chunk_weight_sum(const char* trow, const char* drow, int V, int c,
+                                               const ResidC& kc) {
+  constexpr int RE = kHalfBytes / EB;
+  const int lane = threadIdx.x & 31;
+  unsigned long long s = 0;
+  const int e1 = min(V, (c + 1) * RE);
+  for (int e = c * RE + lane; e < e1; e += 32)
+    s += draw_weight(load_elem<EB>(trow, (size_t)e), drow ? load_elem<EB>(drow, (size_t)e) : -INFINITY, kc);
+  return warp_sum_u64(s);
+}
+
+template <int EB>
+__device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsigned char* stage) {
   constexpr int RE = kHalfBytes / EB;  // elements per R chunk
   constexpr int EPL = RE / 32;         // contiguous elements per lane in the scan
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = EPL / VEC;        // vectors per lane per row (8)
   const int G = P.G, V = P.V, NCR = P.NCR;
   const int lane = threadIdx.x & 31;
-  const Decision d = load_decision(&P.dec[b]);
+  Decision d;
+  d.k = 0;
+  d.reject = 0;
+  d.mt = d.md = d.inv_st = d.rho = 0.0f;
   unsigned int flags = 0;
-  const float u_s = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + G], flags);
-  const ulonglong2* rp = P.resid + (size_t)b * P.stride_ncr;
-
-  unsigned long long tr = 0, tp = 0;
-  for (int c = lane; c < NCR; c += 32) {
-    const ulonglong2 w = __ldcg(&rp[c]);
-    tr += w.x;
-    tp += w.y;
-  }
-  tr = warp_sum_u64(tr);
-  tp = warp_sum_u64(tp);
-  const int usep = (tr == 0ull);  // residual vanished: draw from p_k
-  const unsigned long long S = usep ? tp : tr;
-  const unsigned long long target = scaled_target(u_s, S);
-  unsigned long long carry = 0, base = 0;
-  int cs = -1;
-  for (int c0 = 0; c0 < NCR && cs < 0; c0 += 32) {
-    const int c = c0 + lane;
-    unsigned long long w = 0;
-    if (c < NCR) {
-      const ulonglong2 ww = __ldcg(&rp[c]);
-      w = usep ? ww.y : ww.x;
+  {
+    // every R item of b read b's decision before arriving, so it is published
+    int rb = -1;
+    bool ok = false;
+    if (lane == 0) {
+      const unsigned long long t0 = now_ns();
+      while (!(ok = read_record(&P.dec[b], rb, d)) && now_ns() - t0 < kWaitNs) __nanosleep(64);
     }
-    const unsigned long long incl = warp_incl_scan_u64(w);
-    const unsigned int hit = __ballot_sync(0xffffffffu, c < NCR && carry + incl > target);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) flags |= SV_STATUS_TIMEOUT;
+    d.k = __shfl_sync(0xffffffffu, d.k, 0);
+    d.reject = __shfl_sync(0xffffffffu, d.reject, 0);
+    d.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+    d.md = __shfl_sync(0xffffffffu, d.md, 0);
+    d.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+    d.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+  }
+  d.c_hi = tc.hi;
+  d.c_lo = tc.lo;
+  const float u_s = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + G], flags);
+  const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
+  ResidC kc;
+  kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
+  kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
+  const char* trow = P.target + target_row(b, k, G, V) * EB;
+  const char* drow = kc.reject ? P.draft + draft_row(b, k, G, V) * EB : nullptr;
+  unsigned long long* rp = P.resid + (size_t)b * P.stride_ncr;
+
+  // 1. The chunk: lane l owns chunks [c0, c1); a scan over the lanes' sums
+  //    finds the lane, that lane walks its chunks.
+  const int cpl = (NCR + 31) >> 5;
+  const int c0 = min(NCR, lane * cpl), c1 = min(NCR, c0 + cpl);
+  unsigned long long own = 0;
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) own += __ldcg(&rp[c]);
+  unsigned long long incl = warp_incl_scan_u64(own);
+  unsigned long long S = __shfl_sync(0xffffffffu, incl, 31);
+  if (S == 0ull) {
+    // The residual vanished in fixed point (p_k and q_k agree within its
+    // resolution): draw from p_k instead; its chunk sums replace the
+    // residual ones.
+    kc.reject = 0;
+    drow = nullptr;
+    own = 0;
+#pragma unroll 1
+    for (int c = 0; c < NCR; ++c) {
+      const unsigned long long sc = chunk_weight_sum<EB>(trow, nullptr, V, c, kc);
+      if (c >= c0 && c < c1) {
+        rp[c] = sc;
+        own += sc;
+      }
+    }
+    incl = warp_incl_scan_u64(own);
+    S = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const unsigned long long target = scaled_target(u_s, S);  // < S
+  int cs = -1;
+  unsigned long long base = 0;
+  {
+    const unsigned long long excl = incl - own;
+    const unsigned int hit = __ballot_sync(0xffffffffu, excl <= target && target < incl);
     if (hit) {
       const int l = __ffs(hit) - 1;
-      cs = c0 + l;
-      base = carry + __shfl_sync(0xffffffffu, incl - w, l);
+      if (lane == l) {
+        unsigned long long run = excl;
+#pragma unroll 1
+        for (int c = c0; c < c1; ++c) {
+          const unsigned long long w = __ldcg(&rp[c]);
+          if (run + w > target) {
+            cs = c;
+            break;
+          }
+          run += w;
+        }
+        base = run;
+      }
+      cs = __shfl_sync(0xffffffffu, cs, l);
+      base = __shfl_sync(0xffffffffu, base, l);
     }
-    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
-  const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
+
+  // 2. The token inside chunk cs.  Every lane loads its EPL contiguous logits
+  //    at once (scalar loads where the rows do not allow 16-byte vectors; -inf
+  //    past the end of the row) into the warp's free staging buffer (target
+  //    half, then draft half, vectors swizzled per lane), sums their weights,
+  //    and the lane whose range holds the target walks to the token.
   int tok = -1;
   if (cs >= 0) {
-    ResidC kc;
-    kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
-    kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
-    const char* trow = P.target + target_row(b, k, G, V) * EB;
-    const char* drow = kc.reject ? P.draft + draft_row(b, k, G, V) * EB : nullptr;
-    // This lane's EPL contiguous logits of the chosen chunk, one 16-byte
-    // vector at a time (scalar loads when the rows do not allow it; -inf past
-    // the end of the row).  Pass 1 sums the weights, pass 2 (one lane) finds
-    // the token.
-    constexpr int VEC = 16 / EB;
-    constexpr int NV = EPL / VEC;
     const size_t e0 = (size_t)cs * RE + (size_t)lane * EPL;
     const bool vec_ok = ((reinterpret_cast<uintptr_t>(trow) |
                           reinterpret_cast<uintptr_t>(drow)) & 15) == 0 &&
                         e0 + EPL <= (size_t)V;
-    auto load_vec = [&](const char* row, int q) -> uint4 {
-      if (!row) return neg_inf_vec(EB);
-      if (vec_ok) return __ldcg(reinterpret_cast<const uint4*>(row + (e0 + (size_t)q * VEC) * EB));
-      uint32_t w[4];
+    auto slot_of = [&](int q) { return (lane * NV + (q ^ (lane & (NV - 1)))) * 16; };
+    if (vec_ok) {
+      uint4 tv[NV], dv[NV];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        if (EB == 2) {
-          const size_t ea = e0 + (size_t)q * 8 + 2 * h, eb = ea + 1;
-          const uint32_t lo = ea < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[ea] : 0xff80u;
-          const uint32_t hi = eb < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[eb] : 0xff80u;
-          w[h] = lo | (hi << 16);
-        } else {
-          const size_t e = e0 + (size_t)q * 4 + h;
-          w[h] = e < (size_t)V ? __float_as_uint(reinterpret_cast<const float*>(row)[e]) : 0xff800000u;
-        }
+      for (int q = 0; q < NV; ++q) {
+        tv[q] = __ldcg(reinterpret_cast<const uint4*>(trow + (e0 + (size_t)q * VEC) * EB));
+        dv[q] = drow ? __ldcg(reinterpret_cast<const uint4*>(drow + (e0 + (size_t)q * VEC) * EB))
+                     : neg_inf_vec(EB);
       }
-      return make_uint4(w[0], w[1], w[2], w[3]);
-    };
-    unsigned long long lsum = 0;
-#pragma unroll 2
-    for (int q = 0; q < NV; ++q) {
-      const uint4 tv = load_vec(trow, q), dv = load_vec(drow, q);
 #pragma unroll
-      for (int h = 0; h < VEC; ++h) {
-        unsigned long long wr, wp;
-        resid_weights(vec_elem<EB>(tv, h), vec_elem<EB>(dv, h), kc, wr, wp);
-        lsum += usep ? wp : wr;
+      for (int q = 0; q < NV; ++q) {
+        sts128(stage + slot_of(q), tv[q]);
+        sts128(stage + kHalfBytes + slot_of(q), dv[q]);
+      }
+    } else {
+      // element by element, -inf past the end of the row
+#pragma unroll 1
+      for (int q = 0; q < NV; ++q) {
+        uint32_t w[2][4];
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const char* row = r ? drow : trow;
+            if (EB == 2) {
+              const size_t ea = e0 + (size_t)q * 8 + 2 * h, eb = ea + 1;
+              const uint32_t lo = row && ea < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[ea] : 0xff80u;
+              const uint32_t hi = row && eb < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[eb] : 0xff80u;
+              w[r][h] = lo | (hi << 16);
+            } else {
+              const size_t e = e0 + (size_t)q * 4 + h;
+              w[r][h] = row && e < (size_t)V ? __float_as_uint(reinterpret_cast<const float*>(row)[e])
+                                              : 0xff800000u;
+            }
+          }
+        }
+        sts128(stage + slot_of(q), make_uint4(w[0][0], w[0][1], w[0][2], w[0][3]));
+        sts128(stage + kHalfBytes + slot_of(q), make_uint4(w[1][0], w[1][1], w[1][2], w[1][3]));
       }
     }
-    const unsigned long long incl = warp_incl_scan_u64(lsum);
-    unsigned long long run = base + incl - lsum;
-    if (run <= target && run + lsum > target) {
+    // A bonus draw runs the residual formula with a -inf draft row: the draft
+    // term is exactly 0 and the weight equals the bonus weight bit for bit.
+    FixAcc acc{0u, 0u, 0u};
+#pragma unroll 1
+    for (int q = 0; q < NV; ++q) {
+      const uint4 t = lds128(stage + slot_of(q)), dd = lds128(stage + kHalfBytes + slot_of(q));
+#pragma unroll
+      for (int h = 0; h < VEC; ++h) fix_add(acc, draw_x<true>(vec_elem<EB>(t, h), vec_elem<EB>(dd, h), kc));
+    }
+    own = fix_value(acc);
+    incl = warp_incl_scan_u64(own);
+    unsigned long long run = base + incl - own;
+    if (run <= target && target < run + own) {
+      // this lane holds the token
+#pragma unroll 1
       for (int q = 0; q < NV && tok < 0; ++q) {
-        const uint4 tv = load_vec(trow, q), dv = load_vec(drow, q);
+        const uint4 t = lds128(stage + slot_of(q)), dd = lds128(stage + kHalfBytes + slot_of(q));
 #pragma unroll
         for (int h = 0; h < VEC; ++h) {
-          unsigned long long wr, wp;
-          resid_weights(vec_elem<EB>(tv, h), vec_elem<EB>(dv, h), kc, wr, wp);
-          const unsigned long long nxt = run + (usep ? wp : wr);
+          const unsigned long long nxt =
+              run + draw_weight<true>(vec_elem<EB>(t, h), vec_elem<EB>(dd, h), kc);
           if (tok < 0 && nxt > target) tok = (int)(e0 + (size_t)(q * VEC + h));
           run = nxt;
         }
       }
     }
-    const unsigned int own = __ballot_sync(0xffffffffu, tok >= 0);
-    tok = own ? __shfl_sync(0xffffffffu, tok, __ffs(own) - 1) : -1;
+    const unsigned int holder = __ballot_sync(0xffffffffu, tok >= 0);
+    tok = holder ? __shfl_sync(0xffffffffu, tok, __ffs(holder) - 1) : -1;
+    // the buffer goes back to the bulk copies
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (lane == 0) {
     if (tok < 0) {
@@ -757,7 +1009,9 @@ __device__ __noinline__ void final_draw(const Params& P, int b) {
     P.out_tokens[(size_t)b * (G + 1) + k] = tok;
     if (flags) atomicOr(P.status, flags);
     P.cnt_r[b] = 0;
-    P.ready[b] = 0;  // every R item of b is done: nobody reads the flag again
+    // every R item of b is done: nobody reads the decision again in this call
+    atom_store_b128(&P.dec[b].tag_a, make_uint4(0u, 0u, 0u, 0u));
+    atom_store_b128(&P.dec[b].tag_b, make_uint4(0u, 0u, 0u, 0u));
   }
   __syncwarp();
 }
@@ -954,46 +1208,47 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
   return make_float2(bv, __int_as_float(bi == 0x7fffffff ? bi : m.c * AE + bi));
 }
 
-// R item: fixed-point sums of the residual weights and of p over the chunk.
-template <int EB>
-__device__ __forceinline__ ulonglong2 r_item(const Meta& m, const char* stage) {
+// R item: fixed-point sum of the draw weights over the chunk.
+template <int EB, bool REJECT>
+__device__ __forceinline__ unsigned long long r_item_sum(const Meta& m, const char* stage,
+                                                         const ResidC& kc) {
   constexpr int VEC = 16 / EB;
   constexpr int NV = kHalfBytes / 16 / 32;  // vectors per lane per row (8)
+  const int lane = threadIdx.x & 31;
+  const int nvec = m.n / VEC;
+  FixAcc a0{0u, 0u, 0u}, a1{0u, 0u, 0u};  // independent chains
+#pragma unroll 2
+  for (int j = 0; j < NV; ++j) {
+    const int vi = lane + 32 * j;
+    if (vi < nvec) {
+      const uint4 t = lds128(stage + vi * 16);
+      const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) {
+        const float x = draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc);
+        if (q & 1) fix_add(a1, x); else fix_add(a0, x);
+      }
+    }
+  }
+  return fix_value(a0) + fix_value(a1);
+}
+
+template <int EB>
+__device__ __forceinline__ unsigned long long r_item(const Meta& m, const char* stage) {
   const int lane = threadIdx.x & 31;
   ResidC kc;
   kc.mt = m.mt; kc.md = m.md; kc.inv_st = m.inv_st; kc.rho = m.rho;
   kc.hi = m.c_hi; kc.lo = m.c_lo; kc.reject = m.reject;
-  unsigned long long sr = 0, sp = 0;
+  unsigned long long sr = 0;
   if (!m.direct) {
-    const int nvec = m.n / VEC;
-    unsigned long long ar[2] = {0, 0}, ap[2] = {0, 0};  // independent chains
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int vi = lane + 32 * j;
-      if (vi < nvec) {
-        const uint4 t = lds128(stage + vi * 16);
-        const uint4 d = m.reject ? lds128(stage + kHalfBytes + vi * 16) : neg_inf_vec(EB);
-#pragma unroll
-        for (int q = 0; q < VEC; ++q) {
-          unsigned long long wr, wp;
-          resid_weights(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc, wr, wp);
-          ar[q & 1] += wr;
-          ap[q & 1] += wp;
-        }
-      }
-    }
-    sr = ar[0] + ar[1];
-    sp = ap[0] + ap[1];
+    sr = m.reject ? r_item_sum<EB, true>(m, stage, kc) : r_item_sum<EB, false>(m, stage, kc);
   } else {
     for (int e = lane; e < m.n; e += 32) {
-      unsigned long long wr, wp;
       const float zd = m.reject ? direct_elem<EB>(m, 1, e) : -INFINITY;
-      resid_weights(direct_elem<EB>(m, 0, e), zd, kc, wr, wp);
-      sr += wr;
-      sp += wp;
+      sr += draw_weight(direct_elem<EB>(m, 0, e), zd, kc);
     }
   }
-  return make_ulonglong2(warp_sum_u64(sr), warp_sum_u64(sp));
+  return warp_sum_u64(sr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1007,9 +1262,8 @@ __device__ __forceinline__ ulonglong2 r_item(const Meta& m, const char* stage) {
 // a cursor that advances in O(1) per item.
 struct Cursor {
   unsigned int j;   // item index
-  int req, row, c;  // A: request, row within the request, chunk
-  int rows, gb;     // A: rows of req, and its gamma
-  int rank;         // R: position in the tail
+  int req, row, c;  // request, row within the request, chunk
+  int rows, gb;     // rows of req, and its gamma
 };
 
 template <int MODE>
@@ -1017,16 +1271,11 @@ __device__ __forceinline__ int rows_of(const int* rowpre, int b) {
   return rowpre[b + 1] - rowpre[b];
 }
 
-// Place the cursor on item j.
+// Place the cursor on A item j.
 template <int MODE>
 __device__ __forceinline__ void cursor_seek(Cursor& k, unsigned int j, const int* rowpre, int B,
-                                            int NC, int NCR, unsigned int nA) {
+                                            int NC) {
   k.j = j;
-  if (MODE == MODE_SAMPLE && j >= nA) {
-    k.rank = (int)((j - nA) / NCR);
-    k.c = (int)((j - nA) % NCR);
-    return;
-  }
   int lo = 0, hi = B - 1;  // largest request with rowpre[b] * NC <= j
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -1040,30 +1289,18 @@ __device__ __forceinline__ void cursor_seek(Cursor& k, unsigned int j, const int
   k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
 }
 
-// Advance the cursor by one item.
+// Advance the cursor by one A item (never past the last one's successor).
 template <int MODE>
-__device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int NC, int NCR,
-                                            unsigned int nA) {
+__device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int B, int NC) {
   ++k.j;
-  if (MODE == MODE_SAMPLE && k.j > nA) {  // inside the R tail
-    if (++k.c == NCR) {
-      k.c = 0;
-      ++k.rank;
-    }
-    return;
-  }
-  if (MODE == MODE_SAMPLE && k.j == nA) {  // first R item
-    k.rank = 0;
-    k.c = 0;
-    return;
-  }
   if (++k.c == NC) {
     k.c = 0;
     if (++k.row == k.rows) {
       k.row = 0;
-      ++k.req;
-      k.rows = rows_of<MODE>(rowpre, k.req);
-      k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
+      if (++k.req < B) {
+        k.rows = rows_of<MODE>(rowpre, k.req);
+        k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
+      }
     }
   }
 }
@@ -1127,9 +1364,10 @@ template <int EB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   int* rowpre = reinterpret_cast<int*>(dsmem + kWarps * kNB * kItemBytes);  // [B+1]
+  // [B] (hi, lo) of log2(e)/T per request (sampling)
+  TempC* tconst = reinterpret_cast<TempC*>(rowpre + ((P.B + 2) & ~1));
   __shared__ __align__(8) uint64_t bar[kWarps][kNB];
   __shared__ Meta meta[kWarps][kNB];     // the item in each buffer
-  __shared__ int2 defq[kWarps][kDefer];  // deferred R items (request, chunk)
   __shared__ int sh_carry;
   __shared__ int wsum[kWarps];
   __shared__ int sh_last;
@@ -1152,8 +1390,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     const int b = base + tid;
     int v = 0;
     if (b < B) {
-      const int gb = clamp_gamma(P.gamma[b], G);
+      const int g_in = P.gamma[b];
+      const int gb = clamp_gamma(g_in, G);
+      unsigned int fl = g_in != gb ? SV_STATUS_BAD_GAMMA : 0u;
       v = MODE == MODE_SAMPLE ? 2 * gb + 1 : gb + 1;
+      if (MODE == MODE_SAMPLE) tconst[b] = temp_consts(sanitize_temperature(P.temperature[b], fl));
+      if (fl && blockIdx.x == 0) atomicOr(P.status, fl);  // reported once
     }
     int incl = v;
 #pragma unroll
@@ -1171,38 +1413,59 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     __syncthreads();
   }
 
-  const unsigned int nA = (unsigned int)rowpre[B] * NC;
-  const unsigned int total = nA + (MODE == MODE_SAMPLE ? (unsigned int)B * NCR : 0u);
+  const unsigned int nA = (unsigned int)rowpre[B] * NC;                        // A items
+  const unsigned int nR = MODE == MODE_SAMPLE ? (unsigned int)B * NCR : 0u;  // R items
   const unsigned int nwarps = gridDim.x * kWarps;
-  // batches: about 1/kBatchDiv of a warp's share, at most kMaxK items
-  const unsigned int K = min((unsigned int)kMaxK, max(1u, total / (nwarps * kBatchDiv)));
-  int D = 1;  // requests whose A items may still be in flight when the tail starts
-  {
-    const double per_req = (double)nA / (double)(B > 0 ? B : 1);
-    D = (int)ceil((double)nwarps * (kNB + K) / per_req) + 1;
-    D = D < B ? D : B - 1;
-  }
+  // batches: about 1/kBatchDiv of a warp's share, at most kMaxK A items or
+  // kMaxRBatch R items
+  const unsigned int K = min((unsigned int)kMaxK, max(1u, nA / (nwarps * kBatchDiv)));
+  const unsigned int KR = min(kMaxRBatch, max(1u, nR / (nwarps * kBatchDiv)));
 
   unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
   uint64_t* mybar = bar[warp];
   Meta* mymeta = meta[warp];
-  int2* mydef = defq[warp];
 
-  unsigned int nb = 0;  // lane 0: start of the pre-claimed next batch
-  if (lane == 0) nb = atomicAdd(P.next_item, K);
+  // ---- Work selection -----------------------------------------------------
+  // A items come in a fixed order: the first batch of every warp is fixed by
+  // its index, later batches are claimed from next_item asynchronously (the
+  // claim for the batch after the current one is started when the current
+  // one begins).  R items exist only for decided requests: a deciding warp
+  // appends its request to the decision queue, and R batches are claimed
+  // from r_next (item i = chunk i % NCR of queue slot i / NCR).  A warp takes
+  // R work first whenever the queue holds unclaimed R items (an estimate from
+  // loads started one batch earlier), so that R re-reads follow their rows'
+  // A pass closely (L2 hits) and the tail stays short.
+  bool a_done = false;         // lane 0: next_item ran past the A items
+  unsigned int a_raw = 0;      // lane 0: result of the pending A claim
+  bool a_pending = false;      // lane 0
+  unsigned int pf_q = 0, pf_r = 0;  // lane 0: q_tail and r_next loaded one batch ago
+  auto claim_a = [&]() {
+    a_raw = atomicAdd(P.next_item, K);
+    a_pending = true;
+  };
+  auto prefetch = [&]() {
+    if (MODE == MODE_SAMPLE) {
+      pf_q = ld_relaxed(P.q_tail);
+      pf_r = ld_relaxed(P.r_next);
+    }
+  };
+  unsigned int a_first = (blockIdx.x * kWarps + warp) * K;  // fixed first batch
+  if (a_first >= nA) a_first = ~0u;
+  if (lane == 0) {
+    claim_a();
+    prefetch();
+  }
 
-  Cursor cur;
+  Cursor cur;        // current A batch [cur.j, a_end)
   cur.j = 0;
-  unsigned int cur_end = 0;  // the current batch is [cur.j, cur_end)
-  int a_tb = -1;             // request whose temperature constants are in a_hi/a_lo
-  float a_hi = 0.0f, a_lo = 0.0f;
-  bool more = true;          // batches may remain
+  unsigned int a_end = 0;
+  unsigned int r_i = 0, r_end = 0;  // current R batch [r_i, r_end)
+  bool more = true;                 // batches may remain
+  bool wait_slot = false;           // the next R item's queue slot is not yet published
   unsigned int issued = 0, processed = 0;
-  int dec_b = -1;            // request whose decision is in dc (warp-uniform)
+  int dec_p = -1, dec_b = 0;        // queue slot and request whose decision is in dc
   Decision dc;
   dc.k = 0;
-  int defhead = 0, ndef = 0;  // ring of deferred R items (warp-uniform)
-  bool blocked = false;       // waiting for the oldest deferred item's decision
   int acc_kind = KIND_A, acc_b = 0;
   unsigned int acc_n = 0;     // arrivals held for (acc_kind, acc_b)
   unsigned int flags = 0;
@@ -1221,12 +1484,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     const int b = pend_b;
     pend_b = -1;
     if (last) {
+      // The most recently consumed buffer is free until the next copy is
+      // issued: the follow-up uses it as scratch.
+      unsigned char* scratch = mybuf + ((processed + kNB - 1) % kNB) * kItemBytes;
+      const int gb = MODE == MODE_SAMPLE ? (rows_of<MODE>(rowpre, b) - 1) / 2
+                                         : rows_of<MODE>(rowpre, b) - 1;
       if (pend_kind == KIND_A) {
-        if (MODE == MODE_SAMPLE) decide_sample<EB>(P, b);
-        else decide_greedy(P, b);
+        if (MODE == MODE_SAMPLE) decide_sample<EB>(P, b, gb, tconst[b], reinterpret_cast<float*>(scratch));
+        else decide_greedy(P, b, gb, reinterpret_cast<int*>(scratch));
       } else {
-        final_draw<EB>(P, b);
+        final_draw<EB>(P, b, tconst[b], scratch);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
   };
   auto flush = [&]() {
@@ -1244,27 +1513,29 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     acc_n = 0;
   };
 
-  // Is request b decided?  If so its decision is fetched into dc.
-  auto decided = [&](int b) -> bool {
-    if (b == dec_b) return true;
+  // Fetch the decision in queue slot p into dc (dec_p, dec_b); false while
+  // the slot is not yet published.
+  auto load_slot = [&](int p) -> bool {
+    if (p == dec_p) return true;
     unsigned int ok = 0;
+    int b = 0;
     Decision d;
-    d.k = 0;
-    if (lane == 0 && ld_acquire(&P.ready[b])) {
-      ok = 1;
-      d = load_decision(&P.dec[b]);
-    }
+    d.k = d.reject = 0;
+    d.mt = d.md = d.inv_st = d.rho = 0.0f;
+    if (lane == 0) ok = read_record(&P.queue[p], b, d) ? 1u : 0u;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
+      dec_b = __shfl_sync(0xffffffffu, b, 0);
       dc.k = __shfl_sync(0xffffffffu, d.k, 0);
       dc.reject = __shfl_sync(0xffffffffu, d.reject, 0);
       dc.mt = __shfl_sync(0xffffffffu, d.mt, 0);
       dc.md = __shfl_sync(0xffffffffu, d.md, 0);
       dc.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
       dc.rho = __shfl_sync(0xffffffffu, d.rho, 0);
-      dc.c_hi = __shfl_sync(0xffffffffu, d.c_hi, 0);
-      dc.c_lo = __shfl_sync(0xffffffffu, d.c_lo, 0);
-      dec_b = b;
+      const TempC tc = tconst[dec_b];
+      dc.c_hi = tc.hi;
+      dc.c_lo = tc.lo;
+      dec_p = p;
     }
     return ok != 0;
   };
@@ -1291,67 +1562,99 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     ++issued;
   };
 
+  // lane 0: the next A batch [lo, hi) from the pending claim; false once the
+  // A items are all claimed.
+  auto take_a = [&](unsigned int& lo, unsigned int& hi) -> bool {
+    if (a_done) return false;
+    if (!a_pending) claim_a();
+    const unsigned long long j = (unsigned long long)nwarps * K + a_raw;
+    a_pending = false;
+    if (j >= nA) {
+      a_done = true;
+      return false;
+    }
+    lo = (unsigned int)j;
+    hi = min(lo + K, nA);
+    claim_a();  // the batch after this one
+    return true;
+  };
+
+  // Choose the next batch at a batch boundary.  0: none left, 1: A, 2: R.
+  auto next_batch = [&]() -> int {
+    unsigned int kind = 0, lo = 0, hi = 0;
+    if (lane == 0) {
+      if (a_first != ~0u) {  // the fixed first batch
+        kind = 1;
+        lo = a_first;
+        hi = min(a_first + K, nA);
+        a_first = ~0u;
+      }
+      // R work if the queue (as loaded a batch ago) holds unclaimed R items
+      if (kind == 0 && MODE == MODE_SAMPLE && pf_r < nR && pf_r < pf_q * (unsigned int)NCR) {
+        const unsigned int i = atomicAdd(P.r_next, KR);
+        if (i < nR) {
+          kind = 2;
+          lo = i;
+          hi = min(i + KR, nR);
+        }
+      }
+      if (kind == 0 && take_a(lo, hi)) kind = 1;
+      // no A items left: R items not yet published are claimed too (their
+      // slots are waited for once this warp's pipeline is drained)
+      if (kind == 0 && MODE == MODE_SAMPLE) {
+        const unsigned int i = atomicAdd(P.r_next, KR);
+        if (i < nR) {
+          kind = 2;
+          lo = i;
+          hi = min(i + KR, nR);
+        }
+      }
+      prefetch();
+    }
+    kind = __shfl_sync(0xffffffffu, kind, 0);
+    lo = __shfl_sync(0xffffffffu, lo, 0);
+    hi = __shfl_sync(0xffffffffu, hi, 0);
+    if (kind == 1) {
+      cursor_seek<MODE>(cur, lo, rowpre, B, NC);
+      a_end = hi;
+    } else if (kind == 2) {
+      r_i = lo;
+      r_end = hi;
+    }
+    return (int)kind;
+  };
+
   while (!failed) {
     // 1. keep kNB copies in flight
-    while (!blocked && issued - processed < (unsigned int)kNB) {
-      if (cur.j == cur_end) {
-        // batch boundary: first the oldest deferred R item, if now decided
-        if (MODE == MODE_SAMPLE && ndef > 0 && decided(mydef[defhead].x)) {
-          Meta r;
-          r.b = mydef[defhead].x;
-          r.c = mydef[defhead].y;
-          fill_r_item<EB>(P, dc, r);
-          issue(r);
-          defhead = (defhead + 1) % kDefer;
-          --ndef;
-          continue;
-        }
-        if (more) {
-          const unsigned int base = __shfl_sync(0xffffffffu, nb, 0);
-          if (base >= total) {
-            more = false;
-          } else {
-            cursor_seek<MODE>(cur, base, rowpre, B, NC, NCR, nA);
-            cur_end = min(base + K, total);
-            if (lane == 0) nb = atomicAdd(P.next_item, K);  // pre-claim the next batch
-          }
-        }
-        if (cur.j == cur_end) {
-          if (ndef > 0) blocked = true;  // only deferred items remain
+    while (!wait_slot && issued - processed < (unsigned int)kNB) {
+      if (cur.j == a_end && r_i == r_end) {
+        if (!more || next_batch() == 0) {
+          more = false;
           break;
         }
       }
-      if (MODE == MODE_SAMPLE && cur.j >= nA) {
-        // R item: its request's rows depend on the decision
-        Meta r;
-        r.b = (2 * B - 1 - D - cur.rank) % B;
-        r.c = cur.c;
-        if (decided(r.b)) {
-          fill_r_item<EB>(P, dc, r);
-          issue(r);
-        } else {
-          // not decided yet: set it aside and keep streaming later items
-          if (ndef == kDefer) {
-            blocked = true;
-            break;
-          }
-          if (lane == 0) mydef[(defhead + ndef) % kDefer] = make_int2(r.b, r.c);
-          __syncwarp();
-          ++ndef;
-        }
-      } else {
-        if (MODE == MODE_SAMPLE && cur.req != a_tb) {
-          unsigned int fl = 0;
-          const TempC tc = temp_consts(sanitize_temperature(P.temperature[cur.req], fl));
-          a_hi = tc.hi;
-          a_lo = tc.lo;
-          a_tb = cur.req;
-        }
+      if (cur.j < a_end) {
         Meta a;
-        a_item_at<EB, MODE>(P, cur, a_hi, a_lo, a);
+        if (MODE == MODE_SAMPLE) {
+          const TempC tc = tconst[cur.req];
+          a_item_at<EB, MODE>(P, cur, tc.hi, tc.lo, a);
+        } else {
+          a_item_at<EB, MODE>(P, cur, 0.0f, 0.0f, a);
+        }
         issue(a);
+        cursor_next<MODE>(cur, rowpre, B, NC);
+      } else if (MODE == MODE_SAMPLE) {
+        if (!load_slot((int)(r_i / (unsigned int)NCR))) {
+          wait_slot = true;  // decided soon: wait once the pipeline is drained
+          break;
+        }
+        Meta r;
+        r.b = dec_b;
+        r.c = (int)(r_i % (unsigned int)NCR);
+        fill_r_item<EB>(P, dc, r);
+        issue(r);
+        ++r_i;
       }
-      cursor_next<MODE>(cur, rowpre, NC, NCR, nA);
     }
 
     // 2. process the oldest item in flight
@@ -1370,7 +1673,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
                                                 : a_item_greedy<EB>(m, stage);
         if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
       } else {
-        const ulonglong2 part = r_item<EB>(m, stage);
+        const unsigned long long part = r_item<EB>(m, stage);
         if (lane == 0) P.resid[(size_t)m_b * P.stride_ncr + m.c] = part;
       }
       __syncwarp();  // every lane is done with the buffer before it is reused
@@ -1384,21 +1687,35 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     }
 
     // 3. nothing in flight
-    if (blocked) {
-      // Publish held arrivals, then wait for the oldest deferred item's
-      // request.  Everything this warp still holds is either a deferred R item
-      // (no decision depends on one) or comes later in the order.
+    if (wait_slot) {
+      // While A items remain, do those first (the R batch is kept): a warp
+      // never waits while A work that a decision may need is unclaimed.
+      unsigned int got = 0, lo = 0, hi = 0;
+      if (lane == 0) got = take_a(lo, hi) ? 1u : 0u;
+      if (__shfl_sync(0xffffffffu, got, 0)) {
+        lo = __shfl_sync(0xffffffffu, lo, 0);
+        hi = __shfl_sync(0xffffffffu, hi, 0);
+        cursor_seek<MODE>(cur, lo, rowpre, B, NC);
+        a_end = hi;
+        wait_slot = false;
+        continue;
+      }
+      // Publish held arrivals (a decision may depend on them), then wait for
+      // the queue slot of the next R item.
       flush();
       settle();
+      const int p = (int)(r_i / (unsigned int)NCR);
       int state = 0;
       if (lane == 0) {
         const unsigned long long t0 = now_ns();
-        while (!ld_acquire(&P.ready[mydef[defhead].x])) {
+        unsigned int ns = 64;
+        while (!(ld_acquire(&P.queue[p].tag_a) & kDecTag)) {
           if (now_ns() - t0 > kWaitNs) {
             state = 1;
             break;
           }
-          __nanosleep(128);
+          __nanosleep(ns);
+          ns = ns < 1024 ? 2 * ns : ns;
         }
       }
       if (__shfl_sync(0xffffffffu, state, 0)) {
@@ -1406,10 +1723,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         failed = true;
         break;
       }
-      blocked = false;
+      wait_slot = false;  // the record is complete shortly after its tag
       continue;
     }
-    if (!more && cur.j == cur_end && ndef == 0) break;  // all work done
+    if (!more) break;  // all work done
   }
 
   // No copy may still be landing in this warp's buffers when it leaves.
@@ -1422,15 +1739,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   }
   if (lane == 0 && flags) atomicOr(P.status, flags);
   __syncthreads();
-  // the last CTA out resets the claim counter for the next call
+  // the last CTA out resets the claim counters and the queue for the next call
   if (tid == 0) {
     __threadfence();
     sh_last = atomicAdd(P.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
-    if (sh_last) {
+  }
+  __syncthreads();
+  if (sh_last) {
+    if (tid == 0) {
       *P.next_item = 0;
+      *P.r_next = 0;
+      *P.q_tail = 0;
       *P.exit_count = 0;
-      __threadfence();
     }
+    if (MODE == MODE_SAMPLE)
+      for (int p = tid; p < B; p += kThreads) {
+        P.queue[p].tag_a = 0u;
+        P.queue[p].tag_b = 0u;
+      }
+    __threadfence();
   }
 }
 
@@ -1445,8 +1772,13 @@ int check_scalars(sv_dtype dtype, int B, int G, int V) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-constexpr size_t kMaxSmem =
-    (size_t)kWarps * kNB * kItemBytes + (size_t)(kMaxBatch + 1) * sizeof(int);
+// staging buffers, then rowpre [B+1] (padded to even) and tconst [B]
+__host__ __device__ constexpr size_t smem_bytes(int B) {
+  return (size_t)kWarps * kNB * kItemBytes + (size_t)((B + 2) & ~1) * sizeof(int) +
+         (size_t)B * sizeof(TempC);
+}
+constexpr size_t kMaxSmem = smem_bytes(kMaxBatch);
+static_assert(kMaxSmem <= 227 * 1024 - 8 * 1024, "shared memory budget");
 
 // Persistent grid: as many CTAs as fit on the device (cached per device).
 template <int EB, int MODE>
@@ -1490,11 +1822,11 @@ int launch(const Params& P, cudaStream_t stream) {
     Q.q_tok = P.q_tok ? P.q_tok + (size_t)b0 * G : nullptr;
     Q.cnt_a = P.cnt_a + b0;
     Q.cnt_r = P.cnt_r + b0;
-    Q.ready = P.ready + b0;
     Q.dec = P.dec + b0;
+    Q.queue = P.queue + b0;
     Q.stats = P.stats + (size_t)b0 * (2 * G + 1) * P.stride_nc;
     Q.resid = P.resid + (size_t)b0 * P.stride_ncr;
-    const size_t smem = (size_t)kWarps * kNB * kItemBytes + (size_t)(Q.B + 1) * sizeof(int);
+    const size_t smem = smem_bytes(Q.B);
     verify_kernel<EB, MODE><<<grid, kThreads, smem, stream>>>(Q);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   }
@@ -1534,12 +1866,14 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.status = reinterpret_cast<unsigned int*>(w + L.status);
   P.next_item = reinterpret_cast<unsigned int*>(w + L.next_item);
   P.exit_count = reinterpret_cast<unsigned int*>(w + L.exit_count);
+  P.r_next = reinterpret_cast<unsigned int*>(w + L.r_next);
+  P.q_tail = reinterpret_cast<unsigned int*>(w + L.q_tail);
   P.cnt_a = reinterpret_cast<unsigned int*>(w + L.cnt_a);
   P.cnt_r = reinterpret_cast<unsigned int*>(w + L.cnt_r);
-  P.ready = reinterpret_cast<unsigned int*>(w + L.ready);
-  P.dec = reinterpret_cast<Decision*>(w + L.dec);
+  P.dec = reinterpret_cast<DecRecord*>(w + L.dec);
+  P.queue = reinterpret_cast<DecRecord*>(w + L.queue);
   P.stats = reinterpret_cast<float2*>(w + L.stats);
-  P.resid = reinterpret_cast<ulonglong2*>(w + L.resid);
+  P.resid = reinterpret_cast<unsigned long long*>(w + L.resid);
   return SV_OK;
 }
 
@@ -1639,8 +1973,8 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
                    (size_t)SV_NOALLOC_SCRATCH_BYTES);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // counters, arrival counts and decision flags start at zero for every call
-  if (cudaMemsetAsync(ws, 0, L.dec, s) != cudaSuccess) return SV_ERR_CUDA;
+  // counters, arrival counts and decision records start at zero for every call
+  if (cudaMemsetAsync(ws, 0, L.stats, s) != cudaSuccess) return SV_ERR_CUDA;
   return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
 }
 

@@ -32,8 +32,10 @@ def run_gpu_sample(w, with_probs=True):
 
 
 def counters_end(B):
-    """End of the header words and the three per-request counter arrays."""
-    return 256 + 3 * ((4 * B + 255) // 256 * 256)
+    """End of the header words (1 KiB), the two per-request arrival counters
+    and the per-request decision records: all zero again after every call."""
+    a256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    return 1024 + 2 * a256(4 * B) + a256(32 * B)
 
 
 def check_sample_parity(w, requests=None):
