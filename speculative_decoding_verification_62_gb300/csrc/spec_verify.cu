@@ -1420,6 +1420,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   // kMaxRBatch R items
   const unsigned int K = min((unsigned int)kMaxK, max(1u, nA / (nwarps * kBatchDiv)));
   const unsigned int KR = min(kMaxRBatch, max(1u, nR / (nwarps * kBatchDiv)));
+  const unsigned int r_backlog = 2u * nwarps * KR;
 
   unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
   uint64_t* mybar = bar[warp];
@@ -1431,10 +1432,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   // claim for the batch after the current one is started when the current
   // one begins).  R items exist only for decided requests: a deciding warp
   // appends its request to the decision queue, and R batches are claimed
-  // from r_next (item i = chunk i % NCR of queue slot i / NCR).  A warp takes
-  // R work first whenever the queue holds unclaimed R items (an estimate from
-  // loads started one batch earlier), so that R re-reads follow their rows'
-  // A pass closely (L2 hits) and the tail stays short.
+  // from r_next (item i = chunk i % NCR of queue slot i / NCR).  While A
+  // items remain, a warp takes R work only when the published, unclaimed R
+  // items (an estimate from loads started one batch earlier) exceed a small
+  // backlog: R re-reads then follow their rows' A pass closely (L2 hits)
+  // without delaying the A items that gate later decisions.
   bool a_done = false;         // lane 0: next_item ran past the A items
   unsigned int a_raw = 0;      // lane 0: result of the pending A claim
   bool a_pending = false;      // lane 0
@@ -1589,8 +1591,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         hi = min(a_first + K, nA);
         a_first = ~0u;
       }
-      // R work if the queue (as loaded a batch ago) holds unclaimed R items
-      if (kind == 0 && MODE == MODE_SAMPLE && pf_r < nR && pf_r < pf_q * (unsigned int)NCR) {
+      // R work while A items remain only if the published, unclaimed R items
+      // (as loaded a batch ago) exceed a backlog of about two batches per
+      // warp: A items, which gate the decisions, go first, and the R work
+      // left when they run out is small enough to finish in parallel.
+      if (kind == 0 && MODE == MODE_SAMPLE && pf_r < nR &&
+          (a_done ? pf_r < pf_q * (unsigned int)NCR
+                  : pf_r + r_backlog < pf_q * (unsigned int)NCR)) {
         const unsigned int i = atomicAdd(P.r_next, KR);
         if (i < nR) {
           kind = 2;
