@@ -55,6 +55,26 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s batch: rank 0 keeps the workload's own seed, so a
+    1-GPU run and rank 0 of an N-GPU run verify the same requests."""
+    return base_seed if rank == 0 else base_seed * 1000 + rank
+
+
+def across_ranks(ms: float, units, world: int, device=None):
+    """Slowest rank's time and the sum over ranks of each count in `units`
+    (verified tokens, emitted tokens, bytes).  Requests are independent, so
+    this is the only exchange between ranks: no collective in the data path."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(x) for x in units], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), [float(x) for x in u.tolist()]
+
+
 def workload_desc(w, mode):
     from speculative_decoding_verification_62_gb300 import workloads as W
     return {"workload": f"config {w.name}: {W.CONFIGS[w.name]['desc']}", "B": w.B,
@@ -227,7 +247,7 @@ def run_ours(args):
     # each rank draws its own batch (different seed): weak scaling by request
     base = W.make(args.config, device=dev)
     if rank:
-        base = W.make(args.config, device=dev, seed=base.meta["seed"] * 1000 + rank)
+        base = W.make(args.config, device=dev, seed=rank_seed(base.meta["seed"], rank))
     mode = args.mode
     B, G, V = base.B, base.G, base.V
     launches_per_call = 1
@@ -293,17 +313,15 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     ms = e0.elapsed_time(e1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    emitted_local = int(v.num_accepted.sum().item()) + B
+    ms_max, (gsum_all, emitted_all) = across_ranks(
+        ms, [base.gamma_sum(), emitted_local], world, dev)
     ms_step = ms_max / args.steps
-    gsum = base.gamma_sum()
-    emitted = int(v.num_accepted.sum().item()) + B
-    value = world * gsum / (ms_step * 1e-3)
+    value = gsum_all / (ms_step * 1e-3)
 
     bytes_min = base.bytes_min(mode)
-    achieved = bytes_min / (ms_step * 1e-3) / 1e9
+    # roofline of one GPU: this rank's algorithmic bytes over its own step time
+    achieved = bytes_min / (ms / args.steps * 1e-3) / 1e9
     peak, peak_src = measured_peak_hbm()
 
     # ---- end to end through the public API from pinned host memory ----
@@ -343,12 +361,10 @@ def run_ours(args):
             e2e_step()
         f1.record(stream)
         torch.cuda.synchronize(dev)
-        te = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * gsum / (float(te.item()) / k2 * 1e-3), "unit": UNIT,
+        te_max, (gsum_e2e,) = across_ranks(f0.elapsed_time(f1), [base.gamma_sum()], world, dev)
+        e2e = {"value": gsum_e2e / (te_max / k2 * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": float(te.item()) / k2}
+               "ms_per_step": te_max / k2}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -364,7 +380,7 @@ def run_ours(args):
                               else "one Python call per step",
                     "l2": f"rotating {ncopy} device copies of the logits "
                           f"({ncopy * per_copy / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
-                    "emitted_tokens_per_s": world * emitted / (ms_step * 1e-3),
+                    "emitted_tokens_per_s": emitted_all / (ms_step * 1e-3),
                     "bytes_min_per_step": bytes_min})
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
