@@ -56,6 +56,9 @@ namespace {
 #ifndef SV_WARPS
 #define SV_WARPS 12
 #endif
+#ifndef SV_BACKLOG_X4
+#define SV_BACKLOG_X4 64u  // R backlog, in quarter-batches per warp
+#endif
 #ifndef SV_BUFFERS
 #define SV_BUFFERS 2
 #endif
@@ -99,7 +102,7 @@ struct __align__(16) DecRecord {
 };
 
 struct Layout {
-  size_t status, next_item, exit_count, r_next, q_tail;  // header words
+  size_t status, next_item, exit_count, r_next, q_tail, dec_count;  // header words
   size_t cnt_a, cnt_r, dec, queue, stats, resid, total;
   int NC, NCR;  // worst-case chunk counts (float32 logits)
 };
@@ -116,6 +119,7 @@ __host__ __device__ inline Layout make_layout(int B, int G, int V) {
   L.exit_count = 256;
   L.r_next = 384;
   L.q_tail = 512;
+  L.dec_count = 640;
   size_t off = 1024;
   L.cnt_a = off; off = align256(off + (size_t)B * 4);
   L.cnt_r = off; off = align256(off + (size_t)B * 4);
@@ -144,7 +148,8 @@ struct Params {
   unsigned int* next_item;   // next A item to claim (past the fixed first batches)
   unsigned int* r_next;      // next R item to claim: item i is chunk i % NCR of the
                              // request in queue slot i / NCR
-  unsigned int* q_tail;      // decisions published to the queue
+  unsigned int* q_tail;      // decisions published to the queue (rejections only)
+  unsigned int* dec_count;   // requests decided (written after any queue entry)
   unsigned int* exit_count;
   unsigned int* cnt_a;       // [B] A items completed
   unsigned int* cnt_r;       // [B] R items completed
@@ -223,15 +228,18 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
   return v;
 }
-// Atomic add with acquire-release semantics: publishes this thread's earlier
-// writes and, for the last arriver, makes the other arrivers' writes visible.
-__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v) {
+// Atomic add with release semantics: publishes this thread's earlier writes
+// (the partials of the items it counts).  The last arriver then issues
+// fence_acquire() before reading the other arrivers' partials; the other
+// arrivers need no acquire, and later memory operations do not wait for the
+// atomic.
+__device__ __forceinline__ unsigned int atom_add_release(unsigned int* p, unsigned int v) {
   unsigned int old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
-__device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void fence_acquire() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 __device__ __forceinline__ unsigned int ld_relaxed(const unsigned int* p) {
   unsigned int v;
@@ -648,6 +656,174 @@ __device__ __forceinline__ unsigned int row_stats(const Params& P, int b, int gb
 // staging buffer.
 // ---------------------------------------------------------------------------
 
+// Float-float helpers for the bonus draw: warp inclusive scan and order.
+__device__ __forceinline__ FF warp_incl_scan_ff(FF v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    FF y;
+    y.hi = __shfl_up_sync(0xffffffffu, v.hi, o);
+    y.lo = __shfl_up_sync(0xffffffffu, v.lo, o);
+    if (lane >= o) v = ff_add(v, y);
+  }
+  return v;
+}
+__device__ __forceinline__ bool ff_le(FF a, FF b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo);
+}
+__device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b.lo}); }
+
+// Bonus draw (every draft accepted): the token comes from p of target row gb,
+// whose per-item partials (m_c, s_c) the A pass already wrote, so no R pass
+// is needed.  Chunk weights W_c = s_c 2^((m_c - M) c) and their float-float
+// prefix sums locate the A chunk holding u S; one pass over that chunk's
+// logits (weights 2^((z - M) c), float-float prefix) walks to the smallest
+// token whose prefix exceeds u S.  If rounding leaves u S past a chunk's own
+// total the walk continues into the next chunk, and past the last one the
+// highest-indexed token of positive weight is taken.  The CDF is accurate to
+// about 1e-7 of S, like the residual path's.
+template <int EB>
+__device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC tc, float M,
+                                         unsigned char* stage) {
+  constexpr int AE = kItemBytes / EB;  // logits per A chunk
+  constexpr int EPL = AE / 32;         // contiguous logits per lane
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = EPL / VEC;        // 16-byte vectors per lane
+  const int G = P.G, V = P.V, NC = P.NC;
+  const int lane = threadIdx.x & 31;
+  unsigned int flags = 0;
+  const float u = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + G], flags);
+  const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + gb) * P.stride_nc;
+  auto chunk_w = [&](int c) -> float {
+    const float2 ms = __ldcg(&pr[c]);
+    return ms.x > -INFINITY ? __fmul_rn(ms.y, ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo))) : 0.0f;
+  };
+  // 1. the chunk: lane l owns chunks [c0, c1)
+  const int cpl = (NC + 31) >> 5;
+  const int c0 = min(NC, lane * cpl), c1 = min(NC, c0 + cpl);
+  FF own{0.0f, 0.0f};
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) own = ff_add(own, FF{chunk_w(c), 0.0f});
+  FF incl = warp_incl_scan_ff(own);
+  FF tot;
+  tot.hi = __shfl_sync(0xffffffffu, incl.hi, 31);
+  tot.lo = __shfl_sync(0xffffffffu, incl.lo, 31);
+  const FF target = ff_mul(tot, u, 0.0f);
+  int cs = NC - 1;
+  FF base{0.0f, 0.0f};
+  {
+    const FF excl = ff_sub(incl, own);
+    const unsigned int hit = __ballot_sync(0xffffffffu, c0 < c1 && ff_le(excl, target) &&
+                                                        !ff_le(incl, target));
+    int l = hit ? __ffs(hit) - 1 : -1;
+    int csl = -1;
+    FF run = excl;
+    if (lane == l) {
+#pragma unroll 1
+      for (int c = c0; c < c1; ++c) {
+        const FF nxt = ff_add(run, FF{chunk_w(c), 0.0f});
+        if (!ff_le(nxt, target)) {
+          csl = c;
+          break;
+        }
+        run = nxt;
+      }
+    }
+    if (l >= 0) {
+      cs = __shfl_sync(0xffffffffu, csl, l);
+      base.hi = __shfl_sync(0xffffffffu, run.hi, l);
+      base.lo = __shfl_sync(0xffffffffu, run.lo, l);
+      if (cs < 0) cs = NC - 1;  // rounding: take the last chunk
+    } else {
+      // u S at or past the total (rounding): the last chunk, from its start
+      base = ff_sub(tot, FF{chunk_w(NC - 1), 0.0f});
+    }
+  }
+
+  // 2. the token: walk chunk cs (then the next ones if rounding requires)
+  const char* row = P.target + target_row(b, gb, G, V) * EB;
+  int tok = -1, last_pos = -1;
+  auto slot_of = [&](int q) { return (lane * NV + (q ^ (lane & (NV - 1)))) * 16; };
+#pragma unroll 1
+  for (int c = cs; c < NC && tok < 0; ++c) {
+    const size_t e0 = (size_t)c * AE + (size_t)lane * EPL;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15) == 0 && e0 + EPL <= (size_t)V;
+    if (vec_ok) {
+#pragma unroll 4
+      for (int q = 0; q < NV; ++q)
+        sts128(stage + slot_of(q), __ldcg(reinterpret_cast<const uint4*>(row + (e0 + (size_t)q * VEC) * EB)));
+    } else {
+#pragma unroll 1
+      for (int q = 0; q < NV; ++q) {
+        uint32_t w[4];
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          if (EB == 2) {
+            const size_t ea = e0 + (size_t)q * 8 + 2 * h, eb = ea + 1;
+            const uint32_t lo = ea < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[ea] : 0xff80u;
+            const uint32_t hi = eb < (size_t)V ? reinterpret_cast<const unsigned short*>(row)[eb] : 0xff80u;
+            w[h] = lo | (hi << 16);
+          } else {
+            const size_t e = e0 + (size_t)q * 4 + h;
+            w[h] = e < (size_t)V ? __float_as_uint(reinterpret_cast<const float*>(row)[e]) : 0xff800000u;
+          }
+        }
+        sts128(stage + slot_of(q), make_uint4(w[0], w[1], w[2], w[3]));
+      }
+    }
+    FF lsum{0.0f, 0.0f};
+#pragma unroll 1
+    for (int q = 0; q < NV; ++q) {
+      const uint4 t = lds128(stage + slot_of(q));
+      float vs = 0.0f;  // one vector's weights: at most 8 terms, float is exact enough
+#pragma unroll
+      for (int h = 0; h < VEC; ++h) {
+        const float w = ex2_approx(exp_arg(vec_elem<EB>(t, h), M, tc.hi, tc.lo));
+        if (w > 0.0f) last_pos = (int)(e0 + (size_t)(q * VEC + h));
+        vs = __fadd_rn(vs, w);
+      }
+      lsum = ff_add(lsum, FF{vs, 0.0f});
+    }
+    const FF li = warp_incl_scan_ff(lsum);
+    FF run = ff_add(base, ff_sub(li, lsum));
+    if (ff_le(run, target) && !ff_le(ff_add(run, lsum), target)) {
+#pragma unroll 1
+      for (int q = 0; q < NV && tok < 0; ++q) {
+        const uint4 t = lds128(stage + slot_of(q));
+#pragma unroll
+        for (int h = 0; h < VEC; ++h) {
+          const float w = ex2_approx(exp_arg(vec_elem<EB>(t, h), M, tc.hi, tc.lo));
+          const FF nxt = ff_add(run, FF{w, 0.0f});
+          if (tok < 0 && w > 0.0f && !ff_le(nxt, target)) tok = (int)(e0 + (size_t)(q * VEC + h));
+          run = nxt;
+        }
+      }
+    }
+    const unsigned int holder = __ballot_sync(0xffffffffu, tok >= 0);
+    tok = holder ? __shfl_sync(0xffffffffu, tok, __ffs(holder) - 1) : -1;
+    FF ctot;
+    ctot.hi = __shfl_sync(0xffffffffu, li.hi, 31);
+    ctot.lo = __shfl_sync(0xffffffffu, li.lo, 31);
+    base = ff_add(base, ctot);
+  }
+  if (tok < 0) {  // past the last chunk: the highest-indexed token of positive weight
+    int lp = last_pos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    tok = lp;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (lane == 0) {
+    if (tok < 0) {
+      flags |= SV_STATUS_INTERNAL;
+      tok = V - 1;
+    }
+    P.out_tokens[(size_t)b * (G + 1) + gb] = tok;
+    if (flags) atomicOr(P.status, flags);
+  }
+  __syncwarp();
+}
+
 // 2^e / S in float64, e and S float-float (the probability p(x) or q(x)).
 __device__ __noinline__ double prob_f64(FF e, FF S) {
   if (!(e.hi > -INFINITY)) return 0.0;
@@ -744,8 +920,17 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
     d.c_lo = tc.lo;
     if (any) atomicOr(P.status, any);
     P.cnt_a[b] = 0;
-    write_record(&P.dec[b], b, d);
-    write_record(&P.queue[atomicAdd(P.q_tail, 1u)], b, d);
+    if (d.reject) {
+      // R work: the decision goes to the request's record and the queue
+      write_record(&P.dec[b], b, d);
+      write_record(&P.queue[atomicAdd(P.q_tail, 1u)], b, d);
+    }
+  }
+  __syncwarp();
+  if (k == gb) final_bonus<EB>(P, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
+  if (lane == 0) {
+    __threadfence();  // a queue entry is visible before the count that covers it
+    atomicAdd(P.dec_count, 1u);
   }
   __syncwarp();
 }
@@ -1420,7 +1605,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   // kMaxRBatch R items
   const unsigned int K = min((unsigned int)kMaxK, max(1u, nA / (nwarps * kBatchDiv)));
   const unsigned int KR = min(kMaxRBatch, max(1u, nR / (nwarps * kBatchDiv)));
-  const unsigned int r_backlog = 2u * nwarps * KR;
+  const unsigned int r_backlog = (unsigned int)(SV_BACKLOG_X4 * nwarps * KR / 4u);
 
   unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
   uint64_t* mybar = bar[warp];
@@ -1464,6 +1649,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   unsigned int r_i = 0, r_end = 0;  // current R batch [r_i, r_end)
   bool more = true;                 // batches may remain
   bool wait_slot = false;           // the next R item's queue slot is not yet published
+  bool r_done = false;              // R claims ran past the last rejected request
   unsigned int issued = 0, processed = 0;
   int dec_p = -1, dec_b = 0;        // queue slot and request whose decision is in dc
   Decision dc;
@@ -1486,6 +1672,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     const int b = pend_b;
     pend_b = -1;
     if (last) {
+      fence_acquire();  // the other arrivers' partials are visible from here
       // The most recently consumed buffer is free until the next copy is
       // issued: the follow-up uses it as scratch.
       unsigned char* scratch = mybuf + ((processed + kNB - 1) % kNB) * kItemBytes;
@@ -1508,7 +1695,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       pend_total = acc_kind == KIND_A ? (unsigned int)rows_of<MODE>(rowpre, acc_b) * (unsigned int)NC
                                       : (unsigned int)NCR;
       pend_n = acc_n;
-      pend_old = atom_add_acq_rel(cnt, acc_n);
+      pend_old = atom_add_release(cnt, acc_n);
     }
     pend_kind = acc_kind;
     pend_b = acc_b;
@@ -1595,7 +1782,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       // (as loaded a batch ago) exceed a backlog of about two batches per
       // warp: A items, which gate the decisions, go first, and the R work
       // left when they run out is small enough to finish in parallel.
-      if (kind == 0 && MODE == MODE_SAMPLE && pf_r < nR &&
+      if (kind == 0 && MODE == MODE_SAMPLE && !r_done && pf_r < nR &&
           (a_done ? pf_r < pf_q * (unsigned int)NCR
                   : pf_r + r_backlog < pf_q * (unsigned int)NCR)) {
         const unsigned int i = atomicAdd(P.r_next, KR);
@@ -1608,7 +1795,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       if (kind == 0 && take_a(lo, hi)) kind = 1;
       // no A items left: R items not yet published are claimed too (their
       // slots are waited for once this warp's pipeline is drained)
-      if (kind == 0 && MODE == MODE_SAMPLE) {
+      if (kind == 0 && MODE == MODE_SAMPLE && !r_done) {
         const unsigned int i = atomicAdd(P.r_next, KR);
         if (i < nR) {
           kind = 2;
@@ -1711,12 +1898,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       // the queue slot of the next R item.
       flush();
       settle();
+      // Requests whose drafts were all accepted have no R work and no queue
+      // slot: once every request is decided, a slot at or past the queue's
+      // end never comes and the batch is void.
       const int p = (int)(r_i / (unsigned int)NCR);
       int state = 0;
       if (lane == 0) {
         const unsigned long long t0 = now_ns();
         unsigned int ns = 64;
         while (!(ld_acquire(&P.queue[p].tag_a) & kDecTag)) {
+          if (ld_acquire(P.dec_count) == (unsigned int)B && (unsigned int)p >= ld_acquire(P.q_tail)) {
+            state = 2;
+            break;
+          }
           if (now_ns() - t0 > kWaitNs) {
             state = 1;
             break;
@@ -1725,12 +1919,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
           ns = ns < 1024 ? 2 * ns : ns;
         }
       }
-      if (__shfl_sync(0xffffffffu, state, 0)) {
+      state = __shfl_sync(0xffffffffu, state, 0);
+      if (state == 1) {
         flags |= SV_STATUS_TIMEOUT;
         failed = true;
         break;
       }
       wait_slot = false;  // the record is complete shortly after its tag
+      if (state == 2) {   // no R work left
+        r_i = r_end;
+        r_done = true;
+      }
       continue;
     }
     if (!more) break;  // all work done
@@ -1757,6 +1956,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       *P.next_item = 0;
       *P.r_next = 0;
       *P.q_tail = 0;
+      *P.dec_count = 0;
       *P.exit_count = 0;
     }
     if (MODE == MODE_SAMPLE)
@@ -1875,6 +2075,7 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.exit_count = reinterpret_cast<unsigned int*>(w + L.exit_count);
   P.r_next = reinterpret_cast<unsigned int*>(w + L.r_next);
   P.q_tail = reinterpret_cast<unsigned int*>(w + L.q_tail);
+  P.dec_count = reinterpret_cast<unsigned int*>(w + L.dec_count);
   P.cnt_a = reinterpret_cast<unsigned int*>(w + L.cnt_a);
   P.cnt_r = reinterpret_cast<unsigned int*>(w + L.cnt_r);
   P.dec = reinterpret_cast<DecRecord*>(w + L.dec);
