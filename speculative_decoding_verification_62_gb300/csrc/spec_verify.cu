@@ -72,7 +72,7 @@ constexpr int kMaxK = 8;                              // A items per claimed bat
 constexpr unsigned int kMaxRBatch = 4;                // R items per claim, at most
 constexpr unsigned int kBatchDiv = 4;                 // batches per warp's share, at least
 constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
-constexpr float kFix = 549755813888.0f;               // 2^39: fixed-point scale of probabilities
+
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
 constexpr float kLog2eLo = 1.925963033500011e-08f;          // log2(e) - kLog2eHi
 
@@ -296,6 +296,9 @@ __device__ __forceinline__ unsigned long long bf16x2_to_f2(uint32_t w) {
 __device__ __forceinline__ float bf16x2_hmax(uint32_t w) {
   return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
+__device__ __forceinline__ uint32_t vec_word(const uint4& v, int q) {
+  return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
 // per-half equality of two bf16 pairs (0xffff in each equal half)
 __device__ __forceinline__ uint32_t bf16x2_eq(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -467,37 +470,54 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 struct ResidC {
   float mt, md, inv_st, rho, hi, lo;
   int reject;
+  float c16;   // inv_st * 2^23 (exact): a weight in units of 2^-23
+  float nrho;  // -rho
 };
+__device__ __forceinline__ void resid_scales(ResidC& k) {
+  k.c16 = __fmul_rn(k.inv_st, 8388608.0f);
+  k.nrho = -k.rho;
+}
 
-// round(x) (to nearest, ties to even) as an unsigned 64-bit integer, for
-// 0 <= x <= 2^39 (a weight is at most about 2^39), with float and 32-bit
-// integer operations only: the float-to-integer conversions run at a
-// fraction of the ALU rate on this GPU.  x = 2^16 y: adding 2^23 rounds y to
-// an integer held in the low mantissa bits; the remainder x - 2^16 RNE(y) is
-// exact (|rem| <= 2^15, a multiple of x's ulp) and is rounded the same way
-// with 1.5 * 2^23, which also covers negative values.  Ties go to even in
-// both steps, as 2^16 RNE(y) is even.
-__device__ __forceinline__ unsigned long long fix_round(float x) {
-  const float t = __fadd_rn(__fmul_rn(x, 1.52587890625e-05f), 8388608.0f);
-  const uint32_t yr = __float_as_uint(t) - 0x4b000000u;
-  const float rem = __fmaf_rn(-__fsub_rn(t, 8388608.0f), 65536.0f, x);
-  const int rr = (int)(__float_as_uint(__fadd_rn(rem, 12582912.0f)) - 0x4b400000u);
+// A weight w in [0, 1] is used in 2^39 fixed point, round(w 2^39), computed
+// from y = w 2^23 with float and 32-bit integer operations only (the
+// float-to-integer conversions run at a fraction of the ALU rate on this
+// GPU).  Adding 2^23 rounds y to an integer held in the low mantissa bits,
+// t = RN(y + 2^23); the remainder y - (t - 2^23) is exact, and 2^16 times it
+// is rounded the same way with 1.5 * 2^23 (which also covers negative
+// values): t2 = RN(2^16 (y - (t - 2^23)) + 1.5 * 2^23).  Then
+// round(w 2^39) = 2^16 (bits(t) - bits(2^23)) + (bits(t2) - bits(1.5 * 2^23)),
+// ties to even in both steps.  Valid for 0 <= y <= 2^23 (a little more is
+// fine).
+struct FixParts {
+  float t, t2;
+};
+__device__ __forceinline__ FixParts fix_parts(float y) {
+  const float t = __fadd_rn(y, 8388608.0f);
+  const float dl = __fsub_rn(y, __fadd_rn(t, -8388608.0f));
+  return FixParts{t, __fmaf_rn(dl, 65536.0f, 12582912.0f)};
+}
+__device__ __forceinline__ unsigned long long fix_round(float y) {
+  const FixParts f = fix_parts(y);
+  const uint32_t yr = __float_as_uint(f.t) - 0x4b000000u;
+  const int rr = (int)(__float_as_uint(f.t2) - 0x4b400000u);
   return ((unsigned long long)yr << 16) + (unsigned long long)(long long)rr;
 }
 
-// Sums of round(x) over many x, as two 32-bit sums of raw float bits (the
-// two steps of fix_round); the constant offsets are removed once per sum.
-// Exact while the sum of the x is below 2^48 (at most 64 terms of <= 2^39
-// per sum here).
+// Sums of round(w 2^39) over many weights, as two 32-bit sums of raw float
+// bits (of t and t2 above); the constant offsets are removed once per sum.
+// Exact while the true sum stays below 2^48 (here at most 64 terms of
+// <= 2^39 per sum).
 struct FixAcc {
   uint32_t hi, lo, n;
 };
-__device__ __forceinline__ void fix_add(FixAcc& a, float x) {
-  const float t = __fadd_rn(__fmul_rn(x, 1.52587890625e-05f), 8388608.0f);
-  const float rem = __fmaf_rn(-__fsub_rn(t, 8388608.0f), 65536.0f, x);
+__device__ __forceinline__ void fix_add_parts(FixAcc& a, float t, float t2) {
   a.hi += __float_as_uint(t);
-  a.lo += __float_as_uint(__fadd_rn(rem, 12582912.0f));
+  a.lo += __float_as_uint(t2);
   ++a.n;
+}
+__device__ __forceinline__ void fix_add(FixAcc& a, float y) {
+  const FixParts f = fix_parts(y);
+  fix_add_parts(a, f.t, f.t2);
 }
 __device__ __forceinline__ unsigned long long fix_value(const FixAcc& a) {
   const uint32_t hs = a.hi - a.n * 0x4b000000u;
@@ -505,16 +525,17 @@ __device__ __forceinline__ unsigned long long fix_value(const FixAcc& a) {
   return ((unsigned long long)hs << 16) + (unsigned long long)(long long)ls;
 }
 
-// The draw weight of one token before rounding: x = w 2^39 for the weight w.
+// The draw weight of one token, y = w 2^23, before rounding.  The packed
+// residual path performs the same operations pair by pair.
 template <bool REJECT>
 __device__ __forceinline__ float draw_x(float zt, float zd, const ResidC& k) {
   const float et = ex2_approx(exp_arg(zt, k.mt, k.hi, k.lo));
   float v = et;
   if (REJECT) {
     const float ed = ex2_approx(exp_arg(zd, k.md, k.hi, k.lo));
-    v = fmaxf(__fmaf_rn(-ed, k.rho, et), 0.0f);
+    v = fmaxf(__fmaf_rn(ed, k.nrho, et), 0.0f);
   }
-  return __fmul_rn(__fmul_rn(v, k.inv_st), kFix);
+  return __fmul_rn(v, k.c16);
 }
 
 template <bool REJECT>
@@ -1046,6 +1067,7 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   ResidC kc;
   kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
+  resid_scales(kc);
   kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
   const char* trow = P.target + target_row(b, k, G, V) * EB;
   const char* drow = kc.reject ? P.draft + draft_row(b, k, G, V) * EB : nullptr;
@@ -1393,7 +1415,9 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
   return make_float2(bv, __int_as_float(bi == 0x7fffffff ? bi : m.c * AE + bi));
 }
 
-// R item: fixed-point sum of the draw weights over the chunk.
+// R item: fixed-point sum of the draw weights over the chunk.  bf16 logits
+// are processed two at a time in packed float32 pairs, with the same
+// operations, in the same order, as draw_x and fix_parts.
 template <int EB, bool REJECT>
 __device__ __forceinline__ unsigned long long r_item_sum(const Meta& m, const char* stage,
                                                          const ResidC& kc) {
@@ -1402,16 +1426,58 @@ __device__ __forceinline__ unsigned long long r_item_sum(const Meta& m, const ch
   const int lane = threadIdx.x & 31;
   const int nvec = m.n / VEC;
   FixAcc a0{0u, 0u, 0u}, a1{0u, 0u, 0u};  // independent chains
+  if constexpr (EB == 2) {
+    const unsigned long long negmt = f2_pack(-kc.mt, -kc.mt), negmd = f2_pack(-kc.md, -kc.md);
+    const unsigned long long chi = f2_pack(kc.hi, kc.hi), clo = f2_pack(kc.lo, kc.lo);
+    const unsigned long long nrho = f2_pack(kc.nrho, kc.nrho), c16 = f2_pack(kc.c16, kc.c16);
+    const unsigned long long p23 = f2_pack(8388608.0f, 8388608.0f);
+    const unsigned long long n23 = f2_pack(-8388608.0f, -8388608.0f);
+    const unsigned long long mone = f2_pack(-1.0f, -1.0f), p16 = f2_pack(65536.0f, 65536.0f);
+    const unsigned long long c15 = f2_pack(12582912.0f, 12582912.0f);
 #pragma unroll 2
-  for (int j = 0; j < NV; ++j) {
-    const int vi = lane + 32 * j;
-    if (vi < nvec) {
-      const uint4 t = lds128(stage + vi * 16);
-      const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+    for (int j = 0; j < NV; ++j) {
+      const int vi = lane + 32 * j;
+      if (vi < nvec) {
+        const uint4 t = lds128(stage + vi * 16);
+        const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
 #pragma unroll
-      for (int q = 0; q < VEC; ++q) {
-        const float x = draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc);
-        if (q & 1) fix_add(a1, x); else fix_add(a0, x);
+        for (int q = 0; q < 4; ++q) {
+          const unsigned long long dt = f2_add(bf16x2_to_f2(vec_word(t, q)), negmt);
+          float x0, x1;
+          f2_unpack(f2_fma(dt, chi, f2_mul(dt, clo)), x0, x1);
+          unsigned long long v = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          if (REJECT) {
+            const unsigned long long dd = f2_add(bf16x2_to_f2(vec_word(d, q)), negmd);
+            f2_unpack(f2_fma(dd, chi, f2_mul(dd, clo)), x0, x1);
+            const unsigned long long ed = f2_pack(ex2_approx(x0), ex2_approx(x1));
+            f2_unpack(f2_fma(ed, nrho, v), x0, x1);
+            v = f2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f));
+          }
+          const unsigned long long y = f2_mul(v, c16);
+          const unsigned long long tt = f2_add(y, p23);
+          const unsigned long long dl = f2_fma(f2_add(tt, n23), mone, y);
+          const unsigned long long t2 = f2_fma(dl, p16, c15);
+          float u0, u1, w0, w1;
+          f2_unpack(tt, u0, u1);
+          f2_unpack(t2, w0, w1);
+          FixAcc& a = (q & 1) ? a1 : a0;
+          fix_add_parts(a, u0, w0);
+          fix_add_parts(a, u1, w1);
+        }
+      }
+    }
+  } else {
+#pragma unroll 2
+    for (int j = 0; j < NV; ++j) {
+      const int vi = lane + 32 * j;
+      if (vi < nvec) {
+        const uint4 t = lds128(stage + vi * 16);
+        const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) {
+          const float y = draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc);
+          if (q & 1) fix_add(a1, y); else fix_add(a0, y);
+        }
       }
     }
   }
@@ -1423,6 +1489,7 @@ __device__ __forceinline__ unsigned long long r_item(const Meta& m, const char* 
   const int lane = threadIdx.x & 31;
   ResidC kc;
   kc.mt = m.mt; kc.md = m.md; kc.inv_st = m.inv_st; kc.rho = m.rho;
+  resid_scales(kc);
   kc.hi = m.c_hi; kc.lo = m.c_lo; kc.reject = m.reject;
   unsigned long long sr = 0;
   if (!m.direct) {
