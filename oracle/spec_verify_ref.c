@@ -30,7 +30,8 @@
  *    sketch, bonus branch.)
  *  - Greedy mode: with temperature -> 0 acceptance reduces to argmax matching.
  *    (explainer, "Implementation points", greedy paragraph; zvxbase
- *    "draft length by load", K=3 worked example.)
+ *    "draft length by load", K=3 worked example.)  In a sampling call, a
+ *    request whose temperature is exactly 0 takes these greedy steps.
  *
  * Readings where the pages are silent (each is listed in the design doc):
  *  - accept is strict: u < ratio; q(x) == 0 accepts.
@@ -137,6 +138,42 @@ static int inverse_cdf(const double *r, int V, double S, double u, double *margi
   return 0;
 }
 
+/* Greedy steps for request b: g_i = argmax_v t[b][i][v] (lowest id on ties),
+ * k = first i < gamma_b with x_i != g_i (else gamma_b), out = x_0..x_{k-1},
+ * g_k.  tie[i] (optional) flags target rows whose maximum occurs twice.
+ * Returns k. */
+static int greedy_one(const void *target, int dtype, int b, int G, int V,
+                      const int32_t *tokens, int gb, int32_t *out, int32_t *tie) {
+  for (int i = 0; i <= G; ++i) {
+    out[i] = -1;
+    if (tie) tie[i] = 0;
+  }
+  int k = gb;
+  for (int i = 0; i <= gb; ++i) {
+    const size_t off = target_row(b, i, G, V);
+    int best = 0, ties = 0;
+    double zbest = logit_at(target, dtype, off);
+    for (int v = 1; v < V; ++v) {
+      const double z = logit_at(target, dtype, off + (size_t)v);
+      if (z > zbest) {
+        zbest = z;
+        best = v;
+        ties = 0;
+      } else if (z == zbest) {
+        ties = 1;
+      }
+    }
+    if (tie) tie[i] = ties;
+    if (i == gb || tokens[(size_t)b * G + i] != best) {
+      k = i;
+      out[i] = best;
+      break;
+    }
+    out[i] = best; /* equals the accepted draft token */
+  }
+  return k;
+}
+
 typedef struct {
   const void *target;
   const void *draft;
@@ -163,6 +200,21 @@ static int sample_one(const sample_args *a, int b) {
     for (int i = 0; i < G; ++i) a->p_tok[(size_t)b * G + i] = NAN;
   if (a->q_tok)
     for (int i = 0; i < G; ++i) a->q_tok[(size_t)b * G + i] = NAN;
+
+  if (T == 0.0) {
+    /* Temperature 0: the greedy steps.  There is no ratio and no CDF draw; an
+     * exact argmax tie counts as a near-tie (margin 0), a decided row as far
+     * from any tie (margin +inf). */
+    int32_t tie[64];
+    const int k = greedy_one(a->target, a->dtype, b, G, V, a->tokens, gb, out, tie);
+    if (a->margin_accept)
+      for (int i = 0; i < k && i < G; ++i)
+        a->margin_accept[(size_t)b * G + i] = tie[i] ? 0.0 : INFINITY;
+    if (a->margin_accept && k < gb) a->margin_accept[(size_t)b * G + k] = tie[k] ? 0.0 : INFINITY;
+    if (a->margin_cdf) a->margin_cdf[b] = tie[k] ? 0.0 : INFINITY;
+    a->num_accepted[b] = k;
+    return 0;
+  }
 
   /* Steps 1-2: per position, softmax both rows, gather at x_i, accept/reject. */
   int k = gb;
@@ -255,8 +307,9 @@ int sv_ref_sample(const void *target_logits, const void *draft_logits, int dtype
                   int32_t *num_accepted, double *p_tok, double *q_tok,
                   double *margin_accept, double *margin_cdf, int nthreads) {
   if (check_common(B, G, V, dtype, draft_tokens, gamma)) return -1;
+  if (G > 63) return -1;
   for (int b = 0; b < B; ++b) {
-    if (!(temperature[b] > 0.0f)) return -1;
+    if (!(temperature[b] >= 0.0f) || isinf(temperature[b])) return -1;
     for (int i = 0; i <= G; ++i) {
       const double u = uniforms[(size_t)b * (G + 1) + i];
       if (!(u >= 0.0 && u < 1.0)) return -1;
@@ -294,34 +347,8 @@ int sv_ref_greedy(const void *target_logits, int dtype, int B, int G, int V,
 #endif
   for (int b = 0; b < B; ++b) {
     int32_t *out = out_tokens + (size_t)b * (size_t)(G + 1);
-    for (int i = 0; i <= G; ++i) {
-      out[i] = -1;
-      if (exact_tie) exact_tie[(size_t)b * (G + 1) + i] = 0;
-    }
-    const int gb = gamma[b];
-    int k = gb;
-    for (int i = 0; i <= gb; ++i) {
-      const size_t off = target_row(b, i, G, V);
-      int best = 0, ties = 0;
-      double zbest = logit_at(target_logits, dtype, off);
-      for (int v = 1; v < V; ++v) {
-        const double z = logit_at(target_logits, dtype, off + (size_t)v);
-        if (z > zbest) {
-          zbest = z;
-          best = v;
-          ties = 0;
-        } else if (z == zbest) {
-          ties = 1;
-        }
-      }
-      if (exact_tie) exact_tie[(size_t)b * (G + 1) + i] = ties;
-      if (i == gb || draft_tokens[(size_t)b * G + i] != best) {
-        k = i;
-        out[i] = best;
-        break;
-      }
-      out[i] = best; /* equals the accepted draft token */
-    }
+    const int k = greedy_one(target_logits, dtype, b, G, V, draft_tokens, gamma[b], out,
+                             exact_tie ? exact_tie + (size_t)b * (G + 1) : NULL);
     num_accepted[b] = k;
   }
   (void)nthreads;

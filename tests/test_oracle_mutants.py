@@ -42,10 +42,10 @@ MUTANTS = {
                              "    for (int v = 0; v < V; ++v) p_out[v] /= 1.0;"),
     "temperature_multiplies": ("return exp((logit_at(base, dtype, off + (size_t)x) - m) / T) / s;",
                                "return exp((logit_at(base, dtype, off + (size_t)x) - m) * T) / s;"),
-    "greedy_tie_highest": ("        } else if (z == zbest) {\n          ties = 1;",
-                           "        } else if (z == zbest) {\n          ties = 1; best = v;"),
-    "greedy_accepts_mismatch": ("draft_tokens[(size_t)b * G + i] != best",
-                                "draft_tokens[(size_t)b * G + i] == best + V"),
+    "greedy_tie_highest": ("      } else if (z == zbest) {\n        ties = 1;",
+                           "      } else if (z == zbest) {\n        ties = 1; best = v;"),
+    "greedy_accepts_mismatch": ("tokens[(size_t)b * G + i] != best",
+                                "tokens[(size_t)b * G + i] == best + V"),
     "truncation_keeps_rejected_draft": ("      k = i;\n      break;",
                                         "      k = i + 1;\n      out[i] = x;\n      break;"),
 }

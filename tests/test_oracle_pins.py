@@ -94,11 +94,39 @@ def test_invalid_input_rejected():
     for key, bad in (("draft_tokens", np.array([[4]], np.int32)),
                      ("gamma", np.array([2], np.int32)),
                      ("uniforms", np.array([[1.0, 0.5]])),
-                     ("temperature", np.array([0.0], np.float32))):
+                     ("temperature", np.array([-1.0], np.float32)),
+                     ("temperature", np.array([np.inf], np.float32))):
         args = dict(ok)
         args[key] = bad
         with pytest.raises(ValueError):
             ORACLE.sample(t, d, **args)
+
+
+def test_zero_temperature_request_takes_the_greedy_steps():
+    """A request with T = 0 in a sampling call is verified by argmax matching
+    (the explainer's implementation points: temperature -> 0 is greedy), the
+    same as the greedy call on that request; the others are unaffected."""
+    rng = np.random.default_rng(21)
+    B, G, V = 6, 3, 50
+    t = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    d = (t[:, :G] + rng.normal(0, 0.5, (B, G, V))).astype(np.float32)
+    gamma = np.array([3, 2, 3, 0, 1, 3], np.int32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    x[0] = t[0, :G].argmax(axis=1)           # request 0: every draft is the argmax
+    for b in range(B):
+        x[b, gamma[b]:] = 0
+    u = rng.random((B, G + 1))
+    T = np.array([0.0, 0.7, 0.0, 0.0, 1.0, 0.0], np.float32)
+    mixed = ORACLE.sample(t, d, x, gamma, u, T)
+    greedy = ORACLE.greedy(t, x, gamma)
+    sampled = ORACLE.sample(t, d, x, gamma, u, np.where(T == 0, 1.0, T).astype(np.float32))
+    for b in range(B):
+        ref = greedy if T[b] == 0 else sampled
+        assert (mixed["out_tokens"][b] == ref["out_tokens"][b]).all()
+        assert mixed["num_accepted"][b] == ref["num_accepted"][b]
+        if T[b] == 0:
+            assert np.isnan(mixed["p_tok"][b]).all() and np.isnan(mixed["q_tok"][b]).all()
+    assert mixed["num_accepted"][0] == 3 and mixed["out_tokens"][0][3] == t[0, 3].argmax()
 
 
 def test_threads_do_not_change_results():
