@@ -21,6 +21,8 @@
  *      (disassemble-channel, "modified distribution" and Step 3 bonus token.)
  *   Greedy mode replaces 1-3 by argmax matching: g_i = argmax t[b][i]
  *   (lowest id on ties), k = first i with x_i != g_i, and g_k is emitted.
+ *   In spec_verify_sample a request with temperature exactly 0 takes these
+ *   greedy steps (temperature -> 0 makes the acceptance an argmax match).
  *   (explainer, "Implementation points", greedy paragraph; zvxbase "draft
  *   length by load", K = 3 worked example.)
  *
@@ -32,7 +34,8 @@
  *   uniforms       [B][G+1]     float32 in [0,1): column i < gamma_b is the
  *                               acceptance draw of position i, column G the
  *                               resample/bonus draw
- *   temperature    [B]          float32, > 0
+ *   temperature    [B]          float32, >= 0; 0 verifies that request by the
+ *                               greedy steps below (no draft logits read)
  *   out_tokens     [B][G+1]     int32: x_0..x_{k-1}, the drawn token, then -1
  *   num_accepted   [B]          int32: accepted drafts k (emitted = k + 1)
  *
@@ -82,7 +85,7 @@ enum {
   SV_STATUS_BAD_GAMMA = 1u,       /* gamma_b outside [0, G]: clamped */
   SV_STATUS_BAD_TOKEN = 2u,       /* draft token outside [0, V): clamped */
   SV_STATUS_BAD_UNIFORM = 4u,     /* uniform outside [0, 1) or NaN: replaced by 0 */
-  SV_STATUS_BAD_TEMPERATURE = 8u, /* temperature <= 0, inf or NaN: replaced by 1 */
+  SV_STATUS_BAD_TEMPERATURE = 8u, /* temperature < 0, inf or NaN: replaced by 1 */
   SV_STATUS_NONFINITE_ROW = 16u,  /* a row whose maximum is not finite */
   SV_STATUS_INTERNAL = 32u,       /* an inverse-CDF draw found no token (never expected) */
   SV_STATUS_TIMEOUT = 64u         /* a bounded wait for a request's decision ran out; the
@@ -130,6 +133,24 @@ int spec_verify_greedy(const void *target_logits, sv_dtype dtype, int B, int G, 
                        const int32_t *draft_tokens, const int32_t *gamma,
                        int32_t *out_tokens, int32_t *num_accepted, void *workspace,
                        size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Draft-token sampler: for each of B rows, one token from softmax(logits[b] /
+ * temperature[b]) by the inverse CDF over ascending token id driven by
+ * uniforms[b] (the smallest j whose prefix sum exceeds uniforms[b] times the
+ * total); temperature[b] == 0 returns the row's argmax (lowest id on ties).
+ * This is the draw a draft model makes at each of its steps ("Speculative
+ * Decoding theory", step 1, draft generation x ~ q), and the same computation
+ * as spec_verify_sample's bonus draw with G == 0.
+ *   logits: device [B][V] float32 or bf16; uniforms, temperature: device [B]
+ *   float32; tokens: device int32 [B] output.
+ *   workspace: as for spec_verify_sample, sized spec_verify_workspace_size(B, 0, V).
+ * Returns SV_OK or an SV_ERR_* code; invalid device values set status bits as
+ * described above.
+ */
+int spec_verify_draw(const void *logits, sv_dtype dtype, int B, int V, const float *uniforms,
+                     const float *temperature, int32_t *tokens, void *workspace,
+                     size_t ws_bytes, sv_stream_t stream);
 
 /*
  * spec_verify_sample_noalloc: spec_verify_sample with no caller workspace.

@@ -22,7 +22,8 @@ STATUS_BITS = {1: "BAD_GAMMA", 2: "BAD_TOKEN", 4: "BAD_UNIFORM", 8: "BAD_TEMPERA
                16: "NONFINITE_ROW", 32: "INTERNAL", 64: "TIMEOUT"}
 SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy",
-           "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror")
+           "spec_verify_draw", "spec_verify_sample_noalloc", "spec_verify_status",
+           "spec_verify_strerror")
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +50,8 @@ def load_library():
                                            vp, vp, sz, vp]
         lib.spec_verify_greedy.restype = ci
         lib.spec_verify_greedy.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_draw.restype = ci
+        lib.spec_verify_draw.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, sz, vp]
         lib.spec_verify_sample_noalloc.restype = ci
         lib.spec_verify_sample_noalloc.argtypes = [vp, vp, ci, ci, ci, ci, vp, vp, vp, vp, vp,
                                                    vp, vp, vp, vp]
@@ -124,6 +127,20 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, gamma, uniform
         _dev(q_tok, "q_tok", torch.float64, (B, G)),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     rc = load_library().spec_verify_sample(*args)
+    if rc != 0:
+        raise SpecVerifyError(rc)
+
+
+def spec_verify_draw(logits, uniforms, temperature, tokens, workspace, stream=None) -> None:
+    """One token per row from softmax(logits / T) by inverse CDF (argmax at T = 0)."""
+    B, V = logits.shape
+    args = (
+        _dev(logits, "logits"), _dtype_code(logits), B, V,
+        _dev(uniforms, "uniforms", torch.float32, (B,)),
+        _dev(temperature, "temperature", torch.float32, (B,)),
+        _dev(tokens, "tokens", torch.int32, (B,)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    rc = load_library().spec_verify_draw(*args)
     if rc != 0:
         raise SpecVerifyError(rc)
 

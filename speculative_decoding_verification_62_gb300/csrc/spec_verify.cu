@@ -391,6 +391,7 @@ __device__ __forceinline__ TempC temp_consts(float T) {
   return t;
 }
 
+// (A temperature of exactly 0 selects the greedy steps and never gets here.)
 __device__ __forceinline__ float sanitize_temperature(float T, unsigned int& flags) {
   if (!(T > 0.0f) || isinf(T)) {
     flags |= SV_STATUS_BAD_TEMPERATURE;
@@ -929,7 +930,7 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
   if (lane == 0) {
     const int kd = gb + 1 + (k < gb ? k : 0);
     const FF st_k{rs[64 + k], rs[128 + k]}, sd_k{rs[64 + kd], rs[128 + kd]};
-    P.num_accepted[b] = k;
+    if (P.num_accepted) P.num_accepted[b] = k;
     Decision d;
     d.k = k;
     d.reject = k < gb ? 1 : 0;
@@ -1007,9 +1008,13 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   const int k = mm ? (__ffs(mm) - 1) : gb;
   const int gk = rs[k];
   if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? gk : -1);
+  if (i < G) {  // a sampling call's zero-temperature request has no p or q
+    if (P.p_tok) P.p_tok[(size_t)b * G + i] = NAN;
+    if (P.q_tok) P.q_tok[(size_t)b * G + i] = NAN;
+  }
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0) {
-    P.num_accepted[b] = k;
+    if (P.num_accepted) P.num_accepted[b] = k;
     if (any) atomicOr(P.status, any);
     P.cnt_a[b] = 0;
   }
@@ -1523,10 +1528,17 @@ __device__ __forceinline__ int rows_of(const int* rowpre, int b) {
   return rowpre[b + 1] - rowpre[b];
 }
 
+// gamma of a request from its row count: sampling requests have 2 gamma + 1
+// rows, greedy ones (greedy mode, or temperature 0) gamma + 1.
+template <int MODE>
+__device__ __forceinline__ int gamma_of(int rows, const TempC* tconst, int b) {
+  return (MODE == MODE_SAMPLE && tconst[b].hi != 0.0f) ? (rows - 1) / 2 : rows - 1;
+}
+
 // Place the cursor on A item j.
 template <int MODE>
 __device__ __forceinline__ void cursor_seek(Cursor& k, unsigned int j, const int* rowpre, int B,
-                                            int NC) {
+                                            int NC, const TempC* tconst) {
   k.j = j;
   int lo = 0, hi = B - 1;  // largest request with rowpre[b] * NC <= j
   while (lo < hi) {
@@ -1538,12 +1550,13 @@ __device__ __forceinline__ void cursor_seek(Cursor& k, unsigned int j, const int
   k.row = (int)(off / NC);
   k.c = (int)(off % NC);
   k.rows = rows_of<MODE>(rowpre, lo);
-  k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
+  k.gb = gamma_of<MODE>(k.rows, tconst, lo);
 }
 
 // Advance the cursor by one A item (never past the last one's successor).
 template <int MODE>
-__device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int B, int NC) {
+__device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int B, int NC,
+                                            const TempC* tconst) {
   ++k.j;
   if (++k.c == NC) {
     k.c = 0;
@@ -1551,7 +1564,7 @@ __device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int B,
       k.row = 0;
       if (++k.req < B) {
         k.rows = rows_of<MODE>(rowpre, k.req);
-        k.gb = MODE == MODE_SAMPLE ? (k.rows - 1) / 2 : k.rows - 1;
+        k.gb = gamma_of<MODE>(k.rows, tconst, k.req);
       }
     }
   }
@@ -1642,11 +1655,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     const int b = base + tid;
     int v = 0;
     if (b < B) {
-      const int g_in = P.gamma[b];
+      const int g_in = P.gamma ? P.gamma[b] : 0;
       const int gb = clamp_gamma(g_in, G);
       unsigned int fl = g_in != gb ? SV_STATUS_BAD_GAMMA : 0u;
-      v = MODE == MODE_SAMPLE ? 2 * gb + 1 : gb + 1;
-      if (MODE == MODE_SAMPLE) tconst[b] = temp_consts(sanitize_temperature(P.temperature[b], fl));
+      v = gb + 1;
+      if (MODE == MODE_SAMPLE) {
+        // temperature 0: this request takes the greedy steps (target rows
+        // only); its constants are marked with hi = 0
+        const float T = P.temperature[b];
+        if (T == 0.0f) {
+          tconst[b] = TempC{0.0f, 0.0f};
+        } else {
+          tconst[b] = temp_consts(sanitize_temperature(T, fl));
+          v = 2 * gb + 1;
+        }
+      }
       if (fl && blockIdx.x == 0) atomicOr(P.status, fl);  // reported once
     }
     int incl = v;
@@ -1743,11 +1766,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       // The most recently consumed buffer is free until the next copy is
       // issued: the follow-up uses it as scratch.
       unsigned char* scratch = mybuf + ((processed + kNB - 1) % kNB) * kItemBytes;
-      const int gb = MODE == MODE_SAMPLE ? (rows_of<MODE>(rowpre, b) - 1) / 2
-                                         : rows_of<MODE>(rowpre, b) - 1;
+      const int gb = gamma_of<MODE>(rows_of<MODE>(rowpre, b), tconst, b);
       if (pend_kind == KIND_A) {
-        if (MODE == MODE_SAMPLE) decide_sample<EB>(P, b, gb, tconst[b], reinterpret_cast<float*>(scratch));
-        else decide_greedy(P, b, gb, reinterpret_cast<int*>(scratch));
+        if (MODE == MODE_SAMPLE && tconst[b].hi != 0.0f) {
+          decide_sample<EB>(P, b, gb, tconst[b], reinterpret_cast<float*>(scratch));
+        } else {
+          decide_greedy(P, b, gb, reinterpret_cast<int*>(scratch));
+          if (MODE == MODE_SAMPLE && lane == 0) {  // counted like any decision
+            __threadfence();
+            atomicAdd(P.dec_count, 1u);
+          }
+        }
       } else {
         final_draw<EB>(P, b, tconst[b], scratch);
       }
@@ -1876,7 +1905,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     lo = __shfl_sync(0xffffffffu, lo, 0);
     hi = __shfl_sync(0xffffffffu, hi, 0);
     if (kind == 1) {
-      cursor_seek<MODE>(cur, lo, rowpre, B, NC);
+      cursor_seek<MODE>(cur, lo, rowpre, B, NC, tconst);
       a_end = hi;
     } else if (kind == 2) {
       r_i = lo;
@@ -1903,7 +1932,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
           a_item_at<EB, MODE>(P, cur, 0.0f, 0.0f, a);
         }
         issue(a);
-        cursor_next<MODE>(cur, rowpre, B, NC);
+        cursor_next<MODE>(cur, rowpre, B, NC, tconst);
       } else if (MODE == MODE_SAMPLE) {
         if (!load_slot((int)(r_i / (unsigned int)NCR))) {
           wait_slot = true;  // decided soon: wait once the pipeline is drained
@@ -1930,7 +1959,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       const int m_kind = m.kind, m_b = m.b;
       const char* stage = reinterpret_cast<const char*>(mybuf + s * kItemBytes);
       if (m_kind == KIND_A) {
-        const float2 part = MODE == MODE_SAMPLE ? a_item_sample<EB>(m, stage)
+        const float2 part = (MODE == MODE_SAMPLE && m.c_hi != 0.0f) ? a_item_sample<EB>(m, stage)
                                                 : a_item_greedy<EB>(m, stage);
         if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
       } else {
@@ -1956,7 +1985,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       if (__shfl_sync(0xffffffffu, got, 0)) {
         lo = __shfl_sync(0xffffffffu, lo, 0);
         hi = __shfl_sync(0xffffffffu, hi, 0);
-        cursor_seek<MODE>(cur, lo, rowpre, B, NC);
+        cursor_seek<MODE>(cur, lo, rowpre, B, NC, tconst);
         a_end = hi;
         wait_slot = false;
         continue;
@@ -2087,11 +2116,11 @@ int launch(const Params& P, cudaStream_t stream) {
     Q.target = P.target + (size_t)b0 * (G + 1) * V * EB;
     Q.draft = P.draft ? P.draft + (size_t)b0 * G * V * EB : nullptr;
     Q.tokens = P.tokens ? P.tokens + (size_t)b0 * G : nullptr;
-    Q.gamma = P.gamma + b0;
+    Q.gamma = P.gamma ? P.gamma + b0 : nullptr;
     Q.uniforms = P.uniforms ? P.uniforms + (size_t)b0 * (G + 1) : nullptr;
     Q.temperature = P.temperature ? P.temperature + b0 : nullptr;
     Q.out_tokens = P.out_tokens + (size_t)b0 * (G + 1);
-    Q.num_accepted = P.num_accepted + b0;
+    Q.num_accepted = P.num_accepted ? P.num_accepted + b0 : nullptr;
     Q.p_tok = P.p_tok ? P.p_tok + (size_t)b0 * G : nullptr;
     Q.q_tok = P.q_tok ? P.q_tok + (size_t)b0 * G : nullptr;
     Q.cnt_a = P.cnt_a + b0;
@@ -2223,6 +2252,22 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, 
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);
+}
+
+int spec_verify_draw(const void* logits, sv_dtype dtype, int B, int V, const float* uniforms,
+                     const float* temperature, int32_t* tokens, void* workspace, size_t ws_bytes,
+                     sv_stream_t stream) {
+  int rc = check_scalars(dtype, B, 0, V);
+  if (rc) return rc;
+  if (!logits || !uniforms || !temperature || !tokens || !workspace) return SV_ERR_NULL;
+  // the sampling step with no drafts: each row's bonus draw
+  Params P;
+  rc = fill_params(P, logits, nullptr, dtype, B, 0, V, nullptr, nullptr, uniforms, temperature,
+                   tokens, nullptr, nullptr, nullptr, workspace, ws_bytes);
+  if (rc) return rc;
+  if (B == 0) return SV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
 }
 
 int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,

@@ -242,7 +242,7 @@ def test_status_flags_on_invalid_device_values():
     w.gamma[1] = -2
     w.draft_tokens[2, 0] = 3000
     w.uniforms[3, 0] = 1.5
-    w.temperature[4] = 0.0
+    w.temperature[4] = -1.0
     v = binding.Verifier(w.B, w.G, w.V, DEV)
     v.sample(w.target, w.draft, w.draft_tokens, w.gamma, w.uniforms, w.temperature)
     st = binding.spec_verify_status(v.workspace)
@@ -251,3 +251,51 @@ def test_status_flags_on_invalid_device_values():
     nacc = v.num_accepted.cpu().numpy()
     assert 0 <= nacc[0] <= 3 and nacc[1] == 0
     assert binding.spec_verify_status(v.workspace) == 0  # read clears
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_zero_temperature_requests_are_greedy_in_a_sampling_call(dt):
+    """T_b = 0 verifies request b by argmax matching inside the sampling launch."""
+    B, G, V = 12, 4, 20001
+    w = to_dev(W.make_random(B, G, V, dt, seed=77, gamma="ragged",
+                             temperature=[0.6 + 0.1 * i for i in range(B)]))
+    am = w.target[:, :G].float().argmax(dim=2).to(torch.int32)
+    for b in range(0, B, 3):
+        w.temperature[b] = 0.0
+        w.draft_tokens[b] = am[b]
+        if b % 2:
+            w.draft_tokens[b, 1] = (am[b, 1] + 1) % V   # a mismatch at position 1
+        w.draft_tokens[b, int(w.gamma[b]):] = 0
+    rep, g = check_sample_parity(w)
+    assert g["ws_clean"]
+    ref_g = oracle.greedy(W.logits_numpy(w.target), w.draft_tokens.cpu().numpy(),
+                          w.gamma.cpu().numpy())
+    for b in range(0, B, 3):
+        assert (g["out"][b] == ref_g["out_tokens"][b]).all()
+        assert g["nacc"][b] == ref_g["num_accepted"][b]
+        assert np.isnan(g["p"][b]).all() and np.isnan(g["q"][b]).all()
+
+
+@pytest.mark.parametrize("V,dt", [(128256, "bf16"), (32000, "f32"), (4097, "bf16"), (1, "f32")])
+def test_draft_sampler_matches_oracle(V, dt):
+    """spec_verify_draw: one token per row from softmax(z / T) by inverse CDF."""
+    B = 48
+    w = W.make_random(B, 0, V, dt, seed=V + 3, temperature=[0.5 + 0.05 * i for i in range(B)])
+    w.temperature[::7] = 0.0                     # argmax rows
+    w = to_dev(w)
+    logits = w.target[:, 0].contiguous()
+    u = w.uniforms[:, 0].contiguous()
+    tokens = torch.full((B,), -5, dtype=torch.int32, device=DEV)
+    ws = binding.make_workspace(B, 0, V)
+    binding.spec_verify_draw(logits, u, w.temperature, tokens, ws)
+    torch.cuda.synchronize()
+    assert binding.spec_verify_status(ws) == 0
+    ref = oracle.sample(**W.oracle_inputs(w), nthreads=NTHREADS)
+    rep = compare_sample(ref, tokens.cpu().numpy()[:, None], np.zeros(B, np.int32),
+                         np.zeros(B, np.int32))
+    print(w.name, rep.summary())
+    assert not rep.mismatches, rep.mismatches[:5]
+    tk = tokens.cpu().numpy()
+    am = logits.float().argmax(dim=1).cpu().numpy()
+    z = (w.temperature.cpu().numpy() == 0)
+    assert (tk[z] == am[z]).all()
