@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--mode", choices=["sample", "greedy"], default="sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layout", choices=["padded", "packed"], default="padded",
+                    help="padded [B][G+1][V] rows, or packed rows with a cu_draft prefix")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step from Python instead of one CUDA-graph replay")
     return ap.parse_args()
@@ -252,27 +254,44 @@ def run_ours(args):
     B, G, V = base.B, base.G, base.V
     launches_per_call = 1
 
+    packed = args.layout == "packed"
+    # inputs in the chosen layout: lens is gamma (padded) or cu_draft (packed)
+    if packed:
+        pk = W.pack(base)
+        src = dict(target=pk.target, draft=pk.draft, draft_tokens=pk.draft_tokens,
+                   lens=pk.cu_draft, uniforms=pk.uniforms, temperature=pk.temperature)
+    else:
+        src = dict(target=base.target, draft=base.draft, draft_tokens=base.draft_tokens,
+                   lens=base.gamma, uniforms=base.uniforms, temperature=base.temperature)
+
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
-    per_copy = base.target.numel() * base.target.element_size()
+    per_copy = src["target"].numel() * src["target"].element_size()
     if mode == "sample":
-        per_copy += base.draft.numel() * base.draft.element_size()
+        per_copy += src["draft"].numel() * src["draft"].element_size()
     ncopy = max(2, math.ceil(4 * l2 / per_copy))
     ncopy = min(ncopy, max(2, int(0.3 * torch.cuda.mem_get_info(dev)[0] // per_copy)))
-    targets = [base.target] + [base.target.clone() for _ in range(ncopy - 1)]
-    drafts = [base.draft] + [base.draft.clone() for _ in range(ncopy - 1)] \
+    targets = [src["target"]] + [src["target"].clone() for _ in range(ncopy - 1)]
+    drafts = [src["draft"]] + [src["draft"].clone() for _ in range(ncopy - 1)] \
         if mode == "sample" else [None] * ncopy
     v = binding.Verifier(B, G, V, dev)
     stream = torch.cuda.current_stream(dev)
 
+    def call(t, d, x, s):
+        if mode == "sample" and packed:
+            v.sample_packed(t, d, x["lens"], x["draft_tokens"], x["uniforms"],
+                            x["temperature"], stream=s)
+        elif mode == "sample":
+            v.sample(t, d, x["draft_tokens"], x["lens"], x["uniforms"], x["temperature"],
+                     stream=s)
+        elif packed:
+            v.greedy_packed(t, x["lens"], x["draft_tokens"], stream=s)
+        else:
+            v.greedy(t, x["draft_tokens"], x["lens"], stream=s)
+
     def step(i, s=None):
         j = i % ncopy
-        s = stream if s is None else s
-        if mode == "sample":
-            v.sample(targets[j], drafts[j], base.draft_tokens, base.gamma, base.uniforms,
-                     base.temperature, stream=s)
-        else:
-            v.greedy(targets[j], base.draft_tokens, base.gamma, stream=s)
+        call(targets[j], drafts[j], src, stream if s is None else s)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -327,9 +346,8 @@ def run_ours(args):
     # ---- end to end through the public API from pinned host memory ----
     e2e = None
     if not args.no_e2e:
-        host = {k: getattr(base, k).cpu().pin_memory() for k in
-                ("target", "draft", "draft_tokens", "gamma", "uniforms", "temperature")}
-        dbuf = {k: torch.empty_like(getattr(base, k)) for k in host}
+        host = {k: x.cpu().pin_memory() for k, x in src.items()}
+        dbuf = {k: torch.empty_like(x) for k, x in src.items()}
         out_h = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
         nacc_h = torch.empty((B,), dtype=torch.int32).pin_memory()
         keys = [k for k in host if mode == "sample" or k not in ("draft", "uniforms",
@@ -340,11 +358,7 @@ def run_ours(args):
         def e2e_step():
             for k in keys:
                 dbuf[k].copy_(host[k], non_blocking=True)
-            if mode == "sample":
-                v.sample(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["gamma"],
-                         dbuf["uniforms"], dbuf["temperature"], stream=stream)
-            else:
-                v.greedy(dbuf["target"], dbuf["draft_tokens"], dbuf["gamma"], stream=stream)
+            call(dbuf["target"], dbuf["draft"], dbuf, stream)
             out_h.copy_(v.out_tokens, non_blocking=True)
             nacc_h.copy_(v.num_accepted, non_blocking=True)
 
@@ -375,7 +389,8 @@ def run_ours(args):
         dist.barrier()
     if rank == 0:
         cfg = workload_desc(base, mode)
-        cfg.update({"parallelism": f"replicas x{world} (independent requests)",
+        cfg.update({"layout": args.layout,
+                    "parallelism": f"replicas x{world} (independent requests)",
                     "launch": "one CUDA-graph replay of the timed steps" if graph is not None
                               else "one Python call per step",
                     "l2": f"rotating {ncopy} device copies of the logits "
@@ -389,7 +404,7 @@ def run_ours(args):
                 "data": "synthetic", "config": cfg,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "peak_source": peak_src,
-                             "traffic": profiled_traffic(args.config, mode),
+                             "traffic": None if packed else profiled_traffic(args.config, mode),
                              "kernel": "verify_kernel (one launch per step)"},
                 "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * launches_per_call,
                 "cpu_baseline": cpu}

@@ -135,6 +135,47 @@ int spec_verify_greedy(const void *target_logits, sv_dtype dtype, int B, int G, 
                        size_t ws_bytes, sv_stream_t stream);
 
 /*
+ * Packed (varlen) layout: the same steps for requests whose rows are stored
+ * back to back without padding, as serving engines lay out ragged verify
+ * batches ("speculative decoding: draft length by load", per-request draft
+ * lengths K; the padded layout above wastes (G - gamma_b) rows per request).
+ *   cu_draft      device int32 [B+1]: cu_draft[0] = 0, cu_draft[b+1] - cu_draft[b]
+ *                 = gamma_b in [0, G]; total_drafts (host) = cu_draft[B].
+ *   target_logits [total_drafts + B][V]: request b's gamma_b + 1 target rows start
+ *                 at row cu_draft[b] + b.
+ *   draft_logits  [total_drafts][V]: request b's rows start at cu_draft[b]
+ *                 (may be NULL when total_drafts == 0).
+ *   draft_tokens  [total_drafts] int32, aligned with the draft rows.
+ *   uniforms      [total_drafts + B] float32, one per target row: request b's
+ *                 entry cu_draft[b] + b + i is the acceptance draw of draft i
+ *                 (i < gamma_b), entry cu_draft[b] + b + gamma_b its final draw.
+ *   p_tok, q_tok  optional float64 [total_drafts], aligned with the draft tokens.
+ *   temperature [B], out_tokens [B][G+1], num_accepted [B]: as in the padded calls
+ *   (G is the largest draft length; it sizes out_tokens and the workspace,
+ *   spec_verify_workspace_size(B, G, V)).
+ * A request whose cu_draft entries are inconsistent (negative, decreasing, past
+ * total_drafts, or a length above G) sets SV_STATUS_BAD_GAMMA and is verified with
+ * no drafts at an offset clamped into the arrays: no access leaves them.
+ * Returns SV_OK, or SV_ERR_* as the padded calls (SV_ERR_SCALAR also for
+ * total_drafts < 0).
+ */
+int spec_verify_sample_packed(const void *target_logits, const void *draft_logits,
+                              sv_dtype dtype, int B, int G, int V, const int32_t *cu_draft,
+                              int total_drafts, const int32_t *draft_tokens,
+                              const float *uniforms, const float *temperature,
+                              int32_t *out_tokens, int32_t *num_accepted, double *p_tok,
+                              double *q_tok, void *workspace, size_t ws_bytes,
+                              sv_stream_t stream);
+
+/* Greedy verify step on the packed layout (target rows and draft tokens as in
+ * spec_verify_sample_packed; no draft logits, uniforms or temperature). */
+int spec_verify_greedy_packed(const void *target_logits, sv_dtype dtype, int B, int G, int V,
+                              const int32_t *cu_draft, int total_drafts,
+                              const int32_t *draft_tokens, int32_t *out_tokens,
+                              int32_t *num_accepted, void *workspace, size_t ws_bytes,
+                              sv_stream_t stream);
+
+/*
  * Draft-token sampler: for each of B rows, one token from softmax(logits[b] /
  * temperature[b]) by the inverse CDF over ascending token id driven by
  * uniforms[b] (the smallest j whose prefix sum exceeds uniforms[b] times the

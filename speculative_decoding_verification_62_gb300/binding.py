@@ -22,8 +22,8 @@ STATUS_BITS = {1: "BAD_GAMMA", 2: "BAD_TOKEN", 4: "BAD_UNIFORM", 8: "BAD_TEMPERA
                16: "NONFINITE_ROW", 32: "INTERNAL", 64: "TIMEOUT"}
 SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy",
-           "spec_verify_draw", "spec_verify_sample_noalloc", "spec_verify_status",
-           "spec_verify_strerror")
+           "spec_verify_sample_packed", "spec_verify_greedy_packed", "spec_verify_draw",
+           "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror")
 
 _lock = threading.Lock()
 _lib = None
@@ -50,6 +50,12 @@ def load_library():
                                            vp, vp, sz, vp]
         lib.spec_verify_greedy.restype = ci
         lib.spec_verify_greedy.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_sample_packed.restype = ci
+        lib.spec_verify_sample_packed.argtypes = [vp, vp, ci, ci, ci, ci, vp, ci, vp, vp, vp,
+                                                  vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_greedy_packed.restype = ci
+        lib.spec_verify_greedy_packed.argtypes = [vp, ci, ci, ci, ci, vp, ci, vp, vp, vp, vp,
+                                                  sz, vp]
         lib.spec_verify_draw.restype = ci
         lib.spec_verify_draw.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, sz, vp]
         lib.spec_verify_sample_noalloc.restype = ci
@@ -127,6 +133,56 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, gamma, uniform
         _dev(q_tok, "q_tok", torch.float64, (B, G)),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     rc = load_library().spec_verify_sample(*args)
+    if rc != 0:
+        raise SpecVerifyError(rc)
+
+
+def spec_verify_sample_packed(target_logits, draft_logits, cu_draft, draft_tokens, uniforms,
+                              temperature, out_tokens, num_accepted, workspace, p_tok=None,
+                              q_tok=None, stream=None) -> None:
+    """Sampling verify step on the packed layout; see include/spec_verify.h."""
+    B = cu_draft.numel() - 1
+    total = draft_tokens.numel()
+    V = target_logits.shape[1]
+    G = out_tokens.shape[1] - 1
+    if target_logits.shape[0] != total + B:
+        raise ValueError("target_logits must have total_drafts + B rows")
+    code = _dtype_code(target_logits)
+    args = (
+        _dev(target_logits, "target_logits"),
+        _dev(draft_logits, "draft_logits", target_logits.dtype, (total, V)),
+        code, B, G, V,
+        _dev(cu_draft, "cu_draft", torch.int32, (B + 1,)), total,
+        _dev(draft_tokens, "draft_tokens", torch.int32, (total,)),
+        _dev(uniforms, "uniforms", torch.float32, (total + B,)),
+        _dev(temperature, "temperature", torch.float32, (B,)),
+        _dev(out_tokens, "out_tokens", torch.int32, (B, G + 1)),
+        _dev(num_accepted, "num_accepted", torch.int32, (B,)),
+        _dev(p_tok, "p_tok", torch.float64, (total,)),
+        _dev(q_tok, "q_tok", torch.float64, (total,)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    rc = load_library().spec_verify_sample_packed(*args)
+    if rc != 0:
+        raise SpecVerifyError(rc)
+
+
+def spec_verify_greedy_packed(target_logits, cu_draft, draft_tokens, out_tokens, num_accepted,
+                              workspace, stream=None) -> None:
+    """Greedy verify step on the packed layout; see include/spec_verify.h."""
+    B = cu_draft.numel() - 1
+    total = draft_tokens.numel()
+    V = target_logits.shape[1]
+    G = out_tokens.shape[1] - 1
+    if target_logits.shape[0] != total + B:
+        raise ValueError("target_logits must have total_drafts + B rows")
+    args = (
+        _dev(target_logits, "target_logits"), _dtype_code(target_logits), B, G, V,
+        _dev(cu_draft, "cu_draft", torch.int32, (B + 1,)), total,
+        _dev(draft_tokens, "draft_tokens", torch.int32, (total,)),
+        _dev(out_tokens, "out_tokens", torch.int32, (B, G + 1)),
+        _dev(num_accepted, "num_accepted", torch.int32, (B,)),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    rc = load_library().spec_verify_greedy_packed(*args)
     if rc != 0:
         raise SpecVerifyError(rc)
 
@@ -220,4 +276,16 @@ class Verifier:
     def greedy(self, target, draft_tokens, gamma, stream=None):
         spec_verify_greedy(target, draft_tokens, gamma, self.out_tokens, self.num_accepted,
                            self.workspace, stream)
+        return self.out_tokens, self.num_accepted
+
+    def sample_packed(self, target, draft, cu_draft, draft_tokens, uniforms, temperature,
+                      p_tok=None, q_tok=None, stream=None):
+        spec_verify_sample_packed(target, draft, cu_draft, draft_tokens, uniforms, temperature,
+                                  self.out_tokens, self.num_accepted, self.workspace, p_tok,
+                                  q_tok, stream)
+        return self.out_tokens, self.num_accepted
+
+    def greedy_packed(self, target, cu_draft, draft_tokens, stream=None):
+        spec_verify_greedy_packed(target, cu_draft, draft_tokens, self.out_tokens,
+                                  self.num_accepted, self.workspace, stream)
         return self.out_tokens, self.num_accepted

@@ -67,7 +67,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kNB = SV_BUFFERS;                       // TMA buffers per warp
 constexpr int kItemBytes = 8192;                      // A item: 8 KB of one row
 constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
-constexpr int kMaxBatch = 2048;                       // requests per launch (smem tables)
+constexpr int kMaxBatch = 1536;                       // requests per launch (smem tables)
 constexpr int kMaxK = 8;                              // A items per claimed batch
 constexpr unsigned int kMaxRBatch = 4;                // R items per claim, at most
 constexpr unsigned int kBatchDiv = 4;                 // batches per warp's share, at least
@@ -138,6 +138,9 @@ struct Params {
   int stride_nc, stride_ncr;  // allocated chunk counts (workspace strides)
   const int32_t* tokens;
   const int32_t* gamma;
+  const int32_t* cu;          // packed layout: [B+1] draft prefix (nullptr: padded layout)
+  int total;                  // packed layout: drafts in all requests (rows of draft_logits)
+  int b_base;                 // packed layout: global index of this launch's first request
   const float* uniforms;
   const float* temperature;
   int32_t* out_tokens;
@@ -373,8 +376,6 @@ __device__ __forceinline__ uint4 neg_inf_vec(int eb) {
   return make_uint4(f, f, f, f);
 }
 
-__device__ __forceinline__ int clamp_gamma(int g, int G) { return g < 0 ? 0 : (g > G ? G : g); }
-
 struct TempC {
   float hi, lo;  // log2(e)/T = hi + lo, hi rounded toward zero so lo > 0
 };
@@ -415,11 +416,61 @@ __device__ __forceinline__ float exp_arg(float z, float m, float hi, float lo) {
   return __fmaf_rn(d, hi, __fmul_rn(d, lo));
 }
 
-__device__ __forceinline__ size_t target_row(int b, int i, int G, int V) {
-  return ((size_t)b * (size_t)(G + 1) + (size_t)i) * (size_t)V;
+__device__ __forceinline__ int clamp_gamma(int g, int G) { return g < 0 ? 0 : (g > G ? G : g); }
+
+// Where request b's data lives.  Padded layout: target rows b (G+1) + i,
+// draft rows, tokens and p/q entries b G + i, uniforms b (G+1) + i with the
+// final draw's in column G.  Packed layout (cu = prefix of the draft
+// lengths): draft rows, tokens and p/q entries cu[b] + i, target rows and
+// uniforms cu[b] + b + i with the final draw's at i = gamma_b.  A packed
+// request whose prefix is inconsistent (cu[b] < 0, cu[b+1] < cu[b],
+// cu[b+1] > total or a length above G) is flagged and given no drafts, with
+// its offset clamped into the arrays, so no access leaves them.
+struct ReqAddr {
+  size_t t0;   // first target row
+  size_t d0;   // first draft row, token and p/q entry
+  size_t u0;   // first acceptance uniform
+  size_t uf;   // the final draw's uniform
+  int gb;      // draft length
+  unsigned int flags;
+};
+__device__ __forceinline__ int packed_base(const Params& P, int b, int& gb, unsigned int& flags) {
+  const int c0 = P.cu[b], c1 = P.cu[b + 1];
+  const bool ok = 0 <= c0 && c0 <= c1 && c1 <= P.total && c1 - c0 <= P.G;
+  if (!ok) flags |= SV_STATUS_BAD_GAMMA;
+  gb = ok ? c1 - c0 : 0;
+  return ok ? c0 : (c0 < 0 ? 0 : (c0 > P.total ? P.total : c0));
 }
-__device__ __forceinline__ size_t draft_row(int b, int i, int G, int V) {
-  return ((size_t)b * (size_t)G + (size_t)i) * (size_t)V;
+__device__ __forceinline__ ReqAddr addr_from_base(const Params& P, int b, int base, int gb) {
+  ReqAddr a;
+  a.flags = 0;
+  a.gb = gb;
+  if (P.cu) {
+    a.d0 = (size_t)base;
+    a.t0 = (size_t)base + (size_t)(P.b_base + b);
+    a.u0 = a.t0;
+    a.uf = a.t0 + (size_t)gb;
+  } else {
+    a.d0 = (size_t)b * (size_t)P.G;
+    a.t0 = (size_t)b * (size_t)(P.G + 1);
+    a.u0 = a.t0;
+    a.uf = a.t0 + (size_t)P.G;
+  }
+  return a;
+}
+__device__ __forceinline__ ReqAddr req_addr(const Params& P, int b) {
+  unsigned int flags = 0;
+  int gb = 0, base = 0;
+  if (P.cu) {
+    base = packed_base(P, b, gb, flags);
+  } else {
+    const int g_in = P.gamma ? P.gamma[b] : 0;
+    gb = clamp_gamma(g_in, P.G);
+    if (g_in != gb) flags |= SV_STATUS_BAD_GAMMA;
+  }
+  ReqAddr a = addr_from_base(P, b, base, gb);
+  a.flags = flags;
+  return a;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -714,7 +765,8 @@ __device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC t
   const int G = P.G, V = P.V, NC = P.NC;
   const int lane = threadIdx.x & 31;
   unsigned int flags = 0;
-  const float u = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + G], flags);
+  const ReqAddr A = req_addr(P, b);
+  const float u = sanitize_uniform(P.uniforms[A.uf], flags);
   const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + gb) * P.stride_nc;
   auto chunk_w = [&](int c) -> float {
     const float2 ms = __ldcg(&pr[c]);
@@ -763,7 +815,7 @@ __device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC t
   }
 
   // 2. the token: walk chunk cs (then the next ones if rounding requires)
-  const char* row = P.target + target_row(b, gb, G, V) * EB;
+  const char* row = P.target + (A.t0 + (size_t)gb) * (size_t)V * EB;
   int tok = -1, last_pos = -1;
   auto slot_of = [&](int q) { return (lane * NV + (q ^ (lane & (NV - 1)))) * 16; };
 #pragma unroll 1
@@ -867,17 +919,18 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
   const int i = lane;
   unsigned int flags = 0;
   // the drafted tokens, their uniforms and logits are requested first
+  const ReqAddr A = req_addr(P, b);
   int x = 0;
   float u = 0.0f, zt = 0.0f, zd = 0.0f;
   if (i < gb) {
-    x = P.tokens[(size_t)b * G + i];
-    u = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + i], flags);
+    x = P.tokens[A.d0 + i];
+    u = sanitize_uniform(P.uniforms[A.u0 + i], flags);
     if (x < 0 || x >= V) {
       flags |= SV_STATUS_BAD_TOKEN;
       x = x < 0 ? 0 : V - 1;
     }
-    zt = load_elem<EB>(P.target, target_row(b, i, G, V) + (size_t)x);
-    zd = load_elem<EB>(P.draft, draft_row(b, i, G, V) + (size_t)x);
+    zt = load_elem<EB>(P.target, (A.t0 + i) * (size_t)V + (size_t)x);
+    zd = load_elem<EB>(P.draft, (A.d0 + i) * (size_t)V + (size_t)x);
   }
   flags |= row_stats<EB>(P, b, gb, tc, rs);
 
@@ -921,10 +974,10 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
   const unsigned int rej = __ballot_sync(0xffffffffu, reject);
   const int k = rej ? (__ffs(rej) - 1) : gb;
   if (i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
-  if (i < G) {
+  if (i < (P.cu ? gb : G)) {  // packed p/q hold this request's gb entries only
     const bool evaluated = i < gb && i <= k;
-    if (P.p_tok) P.p_tok[(size_t)b * G + i] = evaluated ? p : NAN;
-    if (P.q_tok) P.q_tok[(size_t)b * G + i] = evaluated ? q : NAN;
+    if (P.p_tok) P.p_tok[A.d0 + i] = evaluated ? p : NAN;
+    if (P.q_tok) P.q_tok[A.d0 + i] = evaluated ? q : NAN;
   }
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0) {
@@ -965,8 +1018,9 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   const int lane = threadIdx.x & 31, part = lane & 3;
   unsigned int flags = 0;
   const int i = lane;
+  const ReqAddr A = req_addr(P, b);
   int x = 0;
-  if (i < gb) x = P.tokens[(size_t)b * G + i];
+  if (i < gb) x = P.tokens[A.d0 + i];
 #pragma unroll 1
   for (int r0 = 0; r0 <= gb; r0 += 8) {
     const int r = r0 + (lane >> 2);
@@ -1008,9 +1062,9 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   const int k = mm ? (__ffs(mm) - 1) : gb;
   const int gk = rs[k];
   if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? gk : -1);
-  if (i < G) {  // a sampling call's zero-temperature request has no p or q
-    if (P.p_tok) P.p_tok[(size_t)b * G + i] = NAN;
-    if (P.q_tok) P.q_tok[(size_t)b * G + i] = NAN;
+  if (i < (P.cu ? gb : G)) {  // a sampling call's zero-temperature request has no p or q
+    if (P.p_tok) P.p_tok[A.d0 + i] = NAN;
+    if (P.q_tok) P.q_tok[A.d0 + i] = NAN;
   }
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0) {
@@ -1068,14 +1122,15 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
   }
   d.c_hi = tc.hi;
   d.c_lo = tc.lo;
-  const float u_s = sanitize_uniform(P.uniforms[(size_t)b * (G + 1) + G], flags);
+  const ReqAddr A = req_addr(P, b);
+  const float u_s = sanitize_uniform(P.uniforms[A.uf], flags);
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   ResidC kc;
   kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
   resid_scales(kc);
   kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
-  const char* trow = P.target + target_row(b, k, G, V) * EB;
-  const char* drow = kc.reject ? P.draft + draft_row(b, k, G, V) * EB : nullptr;
+  const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
+  const char* drow = kc.reject ? P.draft + (A.d0 + (size_t)k) * (size_t)V * EB : nullptr;
   unsigned long long* rp = P.resid + (size_t)b * P.stride_ncr;
 
   // 1. The chunk: lane l owns chunks [c0, c1); a scan over the lanes' sums
@@ -1239,16 +1294,41 @@ __device__ __forceinline__ float direct_elem(const Meta& m, int h, int e) {
 }
 
 
+// An unaligned item's elements copied into its stage buffer (which no copy
+// targets), padded with -inf to whole 16-byte vectors, so that it is reduced
+// by the same code, in the same order, as a copied item: a row's statistics do
+// not depend on where the row sits in memory.  Returns the vector count.
+template <int EB>
+__device__ __noinline__ int stage_unaligned(const Meta& m, char* stage) {
+  constexpr int VEC = 16 / EB;
+  const int lane = threadIdx.x & 31;
+  const int nvec = (m.n + VEC - 1) / VEC;
+  for (int e = lane; e < nvec * VEC; e += 32) {
+    if constexpr (EB == 2) {
+      const unsigned short x = e < m.n ? __ldg(reinterpret_cast<const unsigned short*>(m.p0) + e)
+                                       : (unsigned short)0xff80u;
+      reinterpret_cast<unsigned short*>(stage)[e] = x;
+    } else {
+      const unsigned int x = e < m.n ? __ldg(reinterpret_cast<const unsigned int*>(m.p0) + e)
+                                     : 0xff800000u;
+      reinterpret_cast<unsigned int*>(stage)[e] = x;
+    }
+  }
+  __syncwarp();
+  return nvec;
+}
+
 // A item, sampling: (max, sum of exp2) over the item.
 template <int EB>
-__device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage) {
+__device__ __forceinline__ float2 a_item_sample(const Meta& m, char* stage) {
   constexpr int VEC = 16 / EB;
   constexpr int NV = kItemBytes / 16 / 32;  // vectors per lane (16)
   const int lane = threadIdx.x & 31;
   float mx = -INFINITY, sum = 0.0f;
-  if (!m.direct) {
-    // two passes over the stage: the maximum, then the exponentials
-    const int nvec = m.n / VEC;  // n * EB is a multiple of 16 on this path
+  {
+    // two passes over the stage: the maximum, then the exponentials.  A
+    // copied item's n * EB is a multiple of 16.
+    const int nvec = m.direct ? stage_unaligned<EB>(m, stage) : m.n / VEC;
     if constexpr (EB == 2) {
       // The item's 2*NV*4 logits stay in registers as bf16 pairs.
       constexpr int NW = NV * 4;
@@ -1324,12 +1404,6 @@ __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage
       }
       sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
     }
-  } else {
-    for (int e = lane; e < m.n; e += 32) mx = fmaxf(mx, direct_elem<EB>(m, 0, e));
-    mx = warp_max(mx);
-    if (mx > -INFINITY)
-      for (int e = lane; e < m.n; e += 32)
-        sum += ex2_approx(exp_arg(direct_elem<EB>(m, 0, e), mx, m.c_hi, m.c_lo));
   }
   sum = warp_sum(sum);
   return make_float2(mx, sum);
@@ -1573,19 +1647,20 @@ __device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int B,
 // The A item under the cursor.
 template <int EB, int MODE>
 __device__ __forceinline__ void a_item_at(const Params& P, const Cursor& k, float c_hi,
-                                          float c_lo, Meta& m) {
+                                          float c_lo, const int* cbase, Meta& m) {
   constexpr int AE = kItemBytes / EB;
   const int G = P.G, V = P.V;
+  const ReqAddr A = addr_from_base(P, k.req, P.cu ? cbase[k.req] : 0, k.gb);
   size_t roff;
   const char* base;
   if (k.row <= k.gb) {
     m.pslot = k.row;
-    roff = target_row(k.req, k.row, G, V);
+    roff = (A.t0 + (size_t)k.row) * (size_t)V;
     base = P.target;
   } else {
     const int i = k.row - k.gb - 1;
     m.pslot = G + 1 + i;
-    roff = draft_row(k.req, i, G, V);
+    roff = (A.d0 + (size_t)i) * (size_t)V;
     base = P.draft;
   }
   m.kind = KIND_A;
@@ -1601,17 +1676,19 @@ __device__ __forceinline__ void a_item_at(const Params& P, const Cursor& k, floa
 
 // Complete R item m (request m.b, chunk m.c) from its request's decision.
 template <int EB>
-__device__ __forceinline__ void fill_r_item(const Params& P, const Decision& d, Meta& m) {
+__device__ __forceinline__ void fill_r_item(const Params& P, const Decision& d, const int* cbase,
+                                            Meta& m) {
   constexpr int RE = kHalfBytes / EB;
   const int G = P.G, V = P.V, req = m.b, c = m.c;
+  const ReqAddr A = addr_from_base(P, req, P.cu ? cbase[req] : 0, 0);
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   const int reject = (d.reject && k < G) ? 1 : 0;
   m.kind = KIND_R;
   m.pslot = k;
   m.reject = reject;
   m.n = min(RE, V - c * RE);
-  m.p0 = P.target + (target_row(req, k, G, V) + (size_t)c * RE) * EB;
-  m.p1 = reject ? P.draft + (draft_row(req, k, G, V) + (size_t)c * RE) * EB : nullptr;
+  m.p0 = P.target + ((A.t0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
+  m.p1 = reject ? P.draft + ((A.d0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB : nullptr;
   const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
   m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
   m.mt = d.mt;
@@ -1631,6 +1708,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   int* rowpre = reinterpret_cast<int*>(dsmem + kWarps * kNB * kItemBytes);  // [B+1]
   // [B] (hi, lo) of log2(e)/T per request (sampling)
   TempC* tconst = reinterpret_cast<TempC*>(rowpre + ((P.B + 2) & ~1));
+  // [B] packed layout: each request's first draft row (its sanitised cu[b])
+  int* cbase = reinterpret_cast<int*>(tconst + P.B);
   __shared__ __align__(8) uint64_t bar[kWarps][kNB];
   __shared__ Meta meta[kWarps][kNB];     // the item in each buffer
   __shared__ int sh_carry;
@@ -1655,9 +1734,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     const int b = base + tid;
     int v = 0;
     if (b < B) {
-      const int g_in = P.gamma ? P.gamma[b] : 0;
-      const int gb = clamp_gamma(g_in, G);
-      unsigned int fl = g_in != gb ? SV_STATUS_BAD_GAMMA : 0u;
+      unsigned int fl = 0;
+      int gb = 0;
+      if (P.cu) {
+        cbase[b] = packed_base(P, b, gb, fl);
+      } else {
+        const int g_in = P.gamma ? P.gamma[b] : 0;
+        gb = clamp_gamma(g_in, G);
+        if (g_in != gb) fl |= SV_STATUS_BAD_GAMMA;
+      }
       v = gb + 1;
       if (MODE == MODE_SAMPLE) {
         // temperature 0: this request takes the greedy steps (target rows
@@ -1927,9 +2012,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         Meta a;
         if (MODE == MODE_SAMPLE) {
           const TempC tc = tconst[cur.req];
-          a_item_at<EB, MODE>(P, cur, tc.hi, tc.lo, a);
+          a_item_at<EB, MODE>(P, cur, tc.hi, tc.lo, cbase, a);
         } else {
-          a_item_at<EB, MODE>(P, cur, 0.0f, 0.0f, a);
+          a_item_at<EB, MODE>(P, cur, 0.0f, 0.0f, cbase, a);
         }
         issue(a);
         cursor_next<MODE>(cur, rowpre, B, NC, tconst);
@@ -1941,7 +2026,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         Meta r;
         r.b = dec_b;
         r.c = (int)(r_i % (unsigned int)NCR);
-        fill_r_item<EB>(P, dc, r);
+        fill_r_item<EB>(P, dc, cbase, r);
         issue(r);
         ++r_i;
       }
@@ -1957,11 +2042,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       }
       const Meta& m = mymeta[s];
       const int m_kind = m.kind, m_b = m.b;
-      const char* stage = reinterpret_cast<const char*>(mybuf + s * kItemBytes);
+      char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
       if (m_kind == KIND_A) {
-        const float2 part = (MODE == MODE_SAMPLE && m.c_hi != 0.0f) ? a_item_sample<EB>(m, stage)
-                                                : a_item_greedy<EB>(m, stage);
+        const bool staged = MODE == MODE_SAMPLE && m.c_hi != 0.0f;
+        const float2 part = staged ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
+        // stores into the buffer are ordered before the next bulk copy into it
+        if (staged && m.direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       } else {
         const unsigned long long part = r_item<EB>(m, stage);
         if (lane == 0) P.resid[(size_t)m_b * P.stride_ncr + m.c] = part;
@@ -2075,10 +2162,10 @@ int check_scalars(sv_dtype dtype, int B, int G, int V) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// staging buffers, then rowpre [B+1] (padded to even) and tconst [B]
+// staging buffers, then rowpre [B+1] (padded to even), tconst [B] and cbase [B]
 __host__ __device__ constexpr size_t smem_bytes(int B) {
   return (size_t)kWarps * kNB * kItemBytes + (size_t)((B + 2) & ~1) * sizeof(int) +
-         (size_t)B * sizeof(TempC);
+         (size_t)B * sizeof(TempC) + (size_t)B * sizeof(int);
 }
 constexpr size_t kMaxSmem = smem_bytes(kMaxBatch);
 static_assert(kMaxSmem <= 227 * 1024 - 8 * 1024, "shared memory budget");
@@ -2113,16 +2200,23 @@ int launch(const Params& P, cudaStream_t stream) {
     Params Q = P;
     Q.B = B - b0 < kMaxBatch ? B - b0 : kMaxBatch;
     const size_t G = (size_t)P.G, V = (size_t)P.V;
-    Q.target = P.target + (size_t)b0 * (G + 1) * V * EB;
-    Q.draft = P.draft ? P.draft + (size_t)b0 * G * V * EB : nullptr;
-    Q.tokens = P.tokens ? P.tokens + (size_t)b0 * G : nullptr;
+    if (P.cu) {
+      // packed: rows, tokens, uniforms and p/q are addressed through cu,
+      // which keeps global offsets; only per-request arrays move
+      Q.cu = P.cu + b0;
+      Q.b_base = P.b_base + b0;
+    } else {
+      Q.target = P.target + (size_t)b0 * (G + 1) * V * EB;
+      Q.draft = P.draft ? P.draft + (size_t)b0 * G * V * EB : nullptr;
+      Q.tokens = P.tokens ? P.tokens + (size_t)b0 * G : nullptr;
+      Q.uniforms = P.uniforms ? P.uniforms + (size_t)b0 * (G + 1) : nullptr;
+      Q.p_tok = P.p_tok ? P.p_tok + (size_t)b0 * G : nullptr;
+      Q.q_tok = P.q_tok ? P.q_tok + (size_t)b0 * G : nullptr;
+    }
     Q.gamma = P.gamma ? P.gamma + b0 : nullptr;
-    Q.uniforms = P.uniforms ? P.uniforms + (size_t)b0 * (G + 1) : nullptr;
     Q.temperature = P.temperature ? P.temperature + b0 : nullptr;
     Q.out_tokens = P.out_tokens + (size_t)b0 * (G + 1);
     Q.num_accepted = P.num_accepted ? P.num_accepted + b0 : nullptr;
-    Q.p_tok = P.p_tok ? P.p_tok + (size_t)b0 * G : nullptr;
-    Q.q_tok = P.q_tok ? P.q_tok + (size_t)b0 * G : nullptr;
     Q.cnt_a = P.cnt_a + b0;
     Q.cnt_r = P.cnt_r + b0;
     Q.dec = P.dec + b0;
@@ -2160,6 +2254,9 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.stride_ncr = L.NCR;
   P.tokens = tokens;
   P.gamma = gamma;
+  P.cu = nullptr;
+  P.total = 0;
+  P.b_base = 0;
   P.uniforms = uniforms;
   P.temperature = temperature;
   P.out_tokens = out_tokens;
@@ -2249,6 +2346,56 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, 
   rc = fill_params(P, target_logits, nullptr, dtype, B, G, V, draft_tokens, gamma, nullptr,
                    nullptr, out_tokens, num_accepted, nullptr, nullptr, workspace, ws_bytes);
   if (rc) return rc;
+  if (B == 0) return SV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);
+}
+
+int spec_verify_sample_packed(const void* target_logits, const void* draft_logits,
+                              sv_dtype dtype, int B, int G, int V, const int32_t* cu_draft,
+                              int total_drafts, const int32_t* draft_tokens,
+                              const float* uniforms, const float* temperature,
+                              int32_t* out_tokens, int32_t* num_accepted, double* p_tok,
+                              double* q_tok, void* workspace, size_t ws_bytes,
+                              sv_stream_t stream) {
+  int rc = check_scalars(dtype, B, G, V);
+  if (rc) return rc;
+  if (total_drafts < 0) return SV_ERR_SCALAR;
+  if (!target_logits || !cu_draft || !uniforms || !temperature || !out_tokens ||
+      !num_accepted || !workspace)
+    return SV_ERR_NULL;
+  if (total_drafts > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL;
+  if (!aligned(cu_draft, 4)) return SV_ERR_ALIGN;
+  Params P;
+  rc = fill_params(P, target_logits, draft_logits, dtype, B, G, V, draft_tokens, nullptr,
+                   uniforms, temperature, out_tokens, num_accepted, p_tok, q_tok, workspace,
+                   ws_bytes);
+  if (rc) return rc;
+  P.cu = cu_draft;
+  P.total = total_drafts;
+  if (B == 0) return SV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
+}
+
+int spec_verify_greedy_packed(const void* target_logits, sv_dtype dtype, int B, int G, int V,
+                              const int32_t* cu_draft, int total_drafts,
+                              const int32_t* draft_tokens, int32_t* out_tokens,
+                              int32_t* num_accepted, void* workspace, size_t ws_bytes,
+                              sv_stream_t stream) {
+  int rc = check_scalars(dtype, B, G, V);
+  if (rc) return rc;
+  if (total_drafts < 0) return SV_ERR_SCALAR;
+  if (!target_logits || !cu_draft || !out_tokens || !num_accepted || !workspace)
+    return SV_ERR_NULL;
+  if (total_drafts > 0 && !draft_tokens) return SV_ERR_NULL;
+  if (!aligned(cu_draft, 4)) return SV_ERR_ALIGN;
+  Params P;
+  rc = fill_params(P, target_logits, nullptr, dtype, B, G, V, draft_tokens, nullptr, nullptr,
+                   nullptr, out_tokens, num_accepted, nullptr, nullptr, workspace, ws_bytes);
+  if (rc) return rc;
+  P.cu = cu_draft;
+  P.total = total_drafts;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);

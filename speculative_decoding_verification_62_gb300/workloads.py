@@ -228,3 +228,56 @@ def oracle_inputs(w: Workload, requests=None):
                 gamma=pick(w.gamma).cpu().numpy(),
                 uniforms=pick(w.uniforms).cpu().numpy(),
                 temperature=pick(w.temperature).cpu().numpy())
+
+
+@dataclass
+class Packed:
+    """A workload in the packed (varlen) layout: rows back to back, no padding."""
+    target: torch.Tensor        # [total + B][V]
+    draft: torch.Tensor         # [total][V]
+    cu_draft: torch.Tensor      # [B + 1] int32 prefix of the draft lengths
+    draft_tokens: torch.Tensor  # [total] int32
+    uniforms: torch.Tensor      # [total + B] float32: acceptance draws, then the final draw
+    temperature: torch.Tensor   # [B]
+    G: int
+
+    @property
+    def B(self):
+        return self.cu_draft.numel() - 1
+
+    @property
+    def total(self):
+        return self.draft_tokens.numel()
+
+
+def pack(w: Workload) -> Packed:
+    """Re-lay a padded workload out packed (data movement only)."""
+    g = [int(x) for x in w.gamma.cpu().tolist()]
+    if any(x < 0 or x > w.G for x in g):
+        raise ValueError("gamma outside [0, G]")
+    cu = [0]
+    for x in g:
+        cu.append(cu[-1] + x)
+    dev = w.target.device
+    target = torch.cat([w.target[b, :g[b] + 1] for b in range(w.B)], dim=0)
+    if cu[-1]:
+        draft = torch.cat([w.draft[b, :g[b]] for b in range(w.B)], dim=0)
+        tokens = torch.cat([w.draft_tokens[b, :g[b]] for b in range(w.B)])
+    else:
+        draft = torch.empty((0, w.V), dtype=w.target.dtype, device=dev)
+        tokens = torch.empty((0,), dtype=torch.int32, device=dev)
+    uniforms = torch.cat([torch.cat([w.uniforms[b, :g[b]], w.uniforms[b, w.G:]]) for b in range(w.B)])
+    return Packed(target.contiguous(), draft.contiguous(),
+                  torch.tensor(cu, dtype=torch.int32, device=dev), tokens.contiguous(),
+                  uniforms.contiguous(), w.temperature, w.G)
+
+
+def unpack_per_draft(values: torch.Tensor, cu_draft: torch.Tensor, G: int, fill=float("nan")):
+    """[total] per-draft values -> [B][G] padded with `fill` (data movement only)."""
+    cu = [int(x) for x in cu_draft.cpu().tolist()]
+    B = len(cu) - 1
+    out = torch.full((B, G), fill, dtype=values.dtype, device=values.device)
+    for b in range(B):
+        n = cu[b + 1] - cu[b]
+        out[b, :n] = values[cu[b]:cu[b + 1]]
+    return out
