@@ -11,37 +11,44 @@
 //   speculative decoding optimisation", verify sketch with the bonus token.)
 //   Greedy: argmax match (explainer, "Implementation points", greedy note).
 //
-// One persistent kernel per call, one CTA of 12 warps per SM.  Work items, in
-// one fixed order:
-//   A items  8 KB of one logit row: max and sum of exp2((z - max) log2(e)/T)
-//            (sampling) or argmax (greedy) -> one partial per item.  All A
-//            items come first, request-major.
+// A request whose temperature is 0 inside a sampling call takes the greedy
+// steps.  Inputs come padded ([B][G+1] target rows, [B][G] draft rows) or
+// packed (rows back to back, addressed through a prefix of the draft
+// lengths); a draft-token sampler (G = 0, no drafts) shares the same kernel.
+//
+// One persistent kernel per call: one CTA of 12 warps per SM.  Work items:
+//   A items  8 KB of one logit row -> (max, sum of exp2((z - max) log2(e)/T))
+//            when sampling, (max, lowest index of the max) when greedy.  All
+//            A items of the batch come first, request-major: the first batch
+//            of every warp is static, later batches are claimed from a
+//            global counter ahead of use.
 //   R items  4 KB of target row k and the same 4 KB of draft row k of one
-//            request (sampling): fixed-point (2^-39) sums of the residual
-//            max(0, p_k - q_k) and of p_k -> one partial per item.  They form
-//            a tail that starts a few requests before the end and walks
-//            backwards, so the first ones re-read rows still in L2.
-// Every warp runs its own pipeline: it claims small batches of items from one
-// global counter (the next batch is claimed while the current one runs, and
-// its lanes decode a batch in parallel), keeps kNB TMA bulk copies
-// (cp.async.bulk) in flight into private shared-memory buffers, each tracked
-// by one mbarrier, and processes the items in order.  Arrivals are counted
-// per request with one acquire-release atomic per batch; the warp that
-// completes a request's A items runs its decision (float-float normalisers,
-// float64 acceptance ratios, warp-ballot first reject) and publishes it; the
-// warp that completes its R items locates the chunk holding u*S and scans
-// only that chunk for the token.  An R item whose request is not decided yet
-// is deferred while other items remain; a warp waits for a decision only
-// with its pipeline drained and its arrivals published, and only in the R
-// tail (it has then issued all its A items), so every wait ends.  Each wait
-// is also bounded (2 s) and sets SV_STATUS_TIMEOUT.  Counters are reset by
-// their last user, so the workspace stays zeroed.
+//            rejecting request -> a 64-bit fixed-point sum of the residual
+//            weights max(0, p_k - q_k) over the item.  They are claimed only
+//            once the A items are all claimed.
+// Every warp keeps two items in flight in private shared-memory buffers,
+// filled by bulk copies (cp.async.bulk) and tracked by mbarriers; an item
+// whose bytes are not 16-byte aligned is read with plain loads into its
+// buffer instead, so both kinds are reduced by the same code.  Arrivals are
+// counted per request (one release atomic per run of items of one request).
+// The warp whose arrival completes a request's A items runs its decision on
+// the spot: row statistics in float-float, the acceptance ratios, a ballot
+// for the first reject; with every draft accepted it also draws the bonus
+// token from the A statistics of target row gamma_b.  A reject is published
+// to a queue of decision records; the warp whose arrival completes that
+// request's R items locates the chunk holding u S and walks only that chunk
+// for the token.  No warp waits for work that is not already claimed, every
+// wait is bounded (2 s of global time) and ends in SV_STATUS_TIMEOUT, and
+// counters are reset by their last user, so the workspace stays zeroed.
 //
 // Numerics: inputs widen exactly to float32.  Exponent arguments use a
-// two-term log2(e)/T (hi + lo); exp2 is the SFU's ex2.approx; sums inside an
-// item are float32, sums across items float64.  The acceptance ratio is
-// formed in float64.  The residual CDF is summed in exact 64-bit fixed point,
-// so chunk sums and the final in-chunk scan agree bit for bit.
+// two-term log2(e)/T; exp2 is the SFU's ex2.approx.  Row sums combine item
+// partials in float-float; the acceptance ratio 2^(e_t - e_d) S_d / S_t is
+// formed from float-float exponents and an exp2 of the fractional part, with
+// float64 only where an exponent is extreme and for the optional p/q outputs.
+// Residual weights are summed in exact fixed point (units of 2^-39 of S_t),
+// so chunk sums and the final in-chunk walk agree bit for bit and do not
+// depend on summation order.
 
 #include <cuda_runtime.h>
 #include <mutex>
@@ -441,11 +448,12 @@ __device__ __forceinline__ int packed_base(const Params& P, int b, int& gb, unsi
   gb = ok ? c1 - c0 : 0;
   return ok ? c0 : (c0 < 0 ? 0 : (c0 > P.total ? P.total : c0));
 }
+template <bool PK>
 __device__ __forceinline__ ReqAddr addr_from_base(const Params& P, int b, int base, int gb) {
   ReqAddr a;
   a.flags = 0;
   a.gb = gb;
-  if (P.cu) {
+  if constexpr (PK) {
     a.d0 = (size_t)base;
     a.t0 = (size_t)base + (size_t)(P.b_base + b);
     a.u0 = a.t0;
@@ -458,17 +466,18 @@ __device__ __forceinline__ ReqAddr addr_from_base(const Params& P, int b, int ba
   }
   return a;
 }
+template <bool PK>
 __device__ __forceinline__ ReqAddr req_addr(const Params& P, int b) {
   unsigned int flags = 0;
   int gb = 0, base = 0;
-  if (P.cu) {
+  if constexpr (PK) {
     base = packed_base(P, b, gb, flags);
   } else {
     const int g_in = P.gamma ? P.gamma[b] : 0;
     gb = clamp_gamma(g_in, P.G);
     if (g_in != gb) flags |= SV_STATUS_BAD_GAMMA;
   }
-  ReqAddr a = addr_from_base(P, b, base, gb);
+  ReqAddr a = addr_from_base<PK>(P, b, base, gb);
   a.flags = flags;
   return a;
 }
@@ -644,16 +653,6 @@ __device__ __forceinline__ float ff_div(FF a, FF b) {
   const float c = __fmaf_rn(-q, b.lo, __fadd_rn(r, a.lo));
   return __fadd_rn(q, __fdiv_rn(c, b.hi));
 }
-__device__ __forceinline__ FF warp_sum_ff(FF v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    FF w;
-    w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
-    w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
-    v = ff_add(v, w);
-  }
-  return v;
-}
 
 // Shuffle of a float-float value.
 __device__ __forceinline__ FF shfl_xor_ff(FF v, int o) {
@@ -755,7 +754,7 @@ __device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b
 // total the walk continues into the next chunk, and past the last one the
 // highest-indexed token of positive weight is taken.  The CDF is accurate to
 // about 1e-7 of S, like the residual path's.
-template <int EB>
+template <int EB, bool PK>
 __device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC tc, float M,
                                          unsigned char* stage) {
   constexpr int AE = kItemBytes / EB;  // logits per A chunk
@@ -765,7 +764,7 @@ __device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC t
   const int G = P.G, V = P.V, NC = P.NC;
   const int lane = threadIdx.x & 31;
   unsigned int flags = 0;
-  const ReqAddr A = req_addr(P, b);
+  const ReqAddr A = req_addr<PK>(P, b);
   const float u = sanitize_uniform(P.uniforms[A.uf], flags);
   const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + gb) * P.stride_nc;
   auto chunk_w = [&](int c) -> float {
@@ -912,14 +911,14 @@ __device__ __noinline__ bool q_underflows(FF e, FF S) {
   return exp2((double)e.hi + (double)e.lo) / ((double)S.hi + (double)S.lo) == 0.0;
 }
 
-template <int EB>
+template <int EB, bool PK>
 __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC tc, float* rs) {
   const int G = P.G, V = P.V;
   const int lane = threadIdx.x & 31;
   const int i = lane;
   unsigned int flags = 0;
   // the drafted tokens, their uniforms and logits are requested first
-  const ReqAddr A = req_addr(P, b);
+  const ReqAddr A = req_addr<PK>(P, b);
   int x = 0;
   float u = 0.0f, zt = 0.0f, zd = 0.0f;
   if (i < gb) {
@@ -974,7 +973,7 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
   const unsigned int rej = __ballot_sync(0xffffffffu, reject);
   const int k = rej ? (__ffs(rej) - 1) : gb;
   if (i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
-  if (i < (P.cu ? gb : G)) {  // packed p/q hold this request's gb entries only
+  if (i < (PK ? gb : G)) {  // packed p/q hold this request's gb entries only
     const bool evaluated = i < gb && i <= k;
     if (P.p_tok) P.p_tok[A.d0 + i] = evaluated ? p : NAN;
     if (P.q_tok) P.q_tok[A.d0 + i] = evaluated ? q : NAN;
@@ -1002,7 +1001,7 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
     }
   }
   __syncwarp();
-  if (k == gb) final_bonus<EB>(P, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
+  if (k == gb) final_bonus<EB, PK>(P, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
   if (lane == 0) {
     __threadfence();  // a queue entry is visible before the count that covers it
     atomicAdd(P.dec_count, 1u);
@@ -1013,12 +1012,13 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
 // Greedy decision: argmax per target row from the per-item partials (rows
 // reduced eight at a time as above; rs holds the row argmaxes), then the
 // first mismatch by warp ballot.
+template <bool PK>
 __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* rs) {
   const int G = P.G, V = P.V, NC = P.NC;
   const int lane = threadIdx.x & 31, part = lane & 3;
   unsigned int flags = 0;
   const int i = lane;
-  const ReqAddr A = req_addr(P, b);
+  const ReqAddr A = req_addr<PK>(P, b);
   int x = 0;
   if (i < gb) x = P.tokens[A.d0 + i];
 #pragma unroll 1
@@ -1062,7 +1062,7 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   const int k = mm ? (__ffs(mm) - 1) : gb;
   const int gk = rs[k];
   if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? gk : -1);
-  if (i < (P.cu ? gb : G)) {  // a sampling call's zero-temperature request has no p or q
+  if (i < (PK ? gb : G)) {  // a sampling call's zero-temperature request has no p or q
     if (P.p_tok) P.p_tok[A.d0 + i] = NAN;
     if (P.q_tok) P.q_tok[A.d0 + i] = NAN;
   }
@@ -1091,7 +1091,7 @@ __device__ unsigned long long chunk_weight_sum(const char* trow, const char* dro
   return warp_sum_u64(s);
 }
 
-template <int EB>
+template <int EB, bool PK>
 __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsigned char* stage) {
   constexpr int RE = kHalfBytes / EB;  // elements per R chunk
   constexpr int EPL = RE / 32;         // contiguous elements per lane in the scan
@@ -1122,7 +1122,7 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
   }
   d.c_hi = tc.hi;
   d.c_lo = tc.lo;
-  const ReqAddr A = req_addr(P, b);
+  const ReqAddr A = req_addr<PK>(P, b);
   const float u_s = sanitize_uniform(P.uniforms[A.uf], flags);
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   ResidC kc;
@@ -1297,9 +1297,9 @@ __device__ __forceinline__ float direct_elem(const Meta& m, int h, int e) {
 // An unaligned item's elements copied into its stage buffer (which no copy
 // targets), padded with -inf to whole 16-byte vectors, so that it is reduced
 // by the same code, in the same order, as a copied item: a row's statistics do
-// not depend on where the row sits in memory.  Returns the vector count.
+// not depend on where the row sits in memory.
 template <int EB>
-__device__ __noinline__ int stage_unaligned(const Meta& m, char* stage) {
+__device__ __noinline__ void stage_unaligned(const Meta& m, char* stage) {
   constexpr int VEC = 16 / EB;
   const int lane = threadIdx.x & 31;
   const int nvec = (m.n + VEC - 1) / VEC;
@@ -1315,20 +1315,19 @@ __device__ __noinline__ int stage_unaligned(const Meta& m, char* stage) {
     }
   }
   __syncwarp();
-  return nvec;
 }
 
 // A item, sampling: (max, sum of exp2) over the item.
 template <int EB>
-__device__ __forceinline__ float2 a_item_sample(const Meta& m, char* stage) {
+__device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage) {
   constexpr int VEC = 16 / EB;
   constexpr int NV = kItemBytes / 16 / 32;  // vectors per lane (16)
   const int lane = threadIdx.x & 31;
   float mx = -INFINITY, sum = 0.0f;
   {
-    // two passes over the stage: the maximum, then the exponentials.  A
-    // copied item's n * EB is a multiple of 16.
-    const int nvec = m.direct ? stage_unaligned<EB>(m, stage) : m.n / VEC;
+    // two passes over the stage: the maximum, then the exponentials (an
+    // unaligned item was staged with -inf padding to whole vectors)
+    const int nvec = (m.n + VEC - 1) / VEC;
     if constexpr (EB == 2) {
       // The item's 2*NV*4 logits stay in registers as bf16 pairs.
       constexpr int NW = NV * 4;
@@ -1645,12 +1644,12 @@ __device__ __forceinline__ void cursor_next(Cursor& k, const int* rowpre, int B,
 }
 
 // The A item under the cursor.
-template <int EB, int MODE>
+template <int EB, int MODE, bool PK>
 __device__ __forceinline__ void a_item_at(const Params& P, const Cursor& k, float c_hi,
                                           float c_lo, const int* cbase, Meta& m) {
   constexpr int AE = kItemBytes / EB;
   const int G = P.G, V = P.V;
-  const ReqAddr A = addr_from_base(P, k.req, P.cu ? cbase[k.req] : 0, k.gb);
+  const ReqAddr A = addr_from_base<PK>(P, k.req, PK ? cbase[k.req] : 0, k.gb);
   size_t roff;
   const char* base;
   if (k.row <= k.gb) {
@@ -1675,12 +1674,12 @@ __device__ __forceinline__ void a_item_at(const Params& P, const Cursor& k, floa
 }
 
 // Complete R item m (request m.b, chunk m.c) from its request's decision.
-template <int EB>
+template <int EB, bool PK>
 __device__ __forceinline__ void fill_r_item(const Params& P, const Decision& d, const int* cbase,
                                             Meta& m) {
   constexpr int RE = kHalfBytes / EB;
   const int G = P.G, V = P.V, req = m.b, c = m.c;
-  const ReqAddr A = addr_from_base(P, req, P.cu ? cbase[req] : 0, 0);
+  const ReqAddr A = addr_from_base<PK>(P, req, PK ? cbase[req] : 0, 0);
   const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
   const int reject = (d.reject && k < G) ? 1 : 0;
   m.kind = KIND_R;
@@ -1702,7 +1701,7 @@ __device__ __forceinline__ void fill_r_item(const Params& P, const Decision& d, 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int EB, int MODE>
+template <int EB, int MODE, bool PK>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   int* rowpre = reinterpret_cast<int*>(dsmem + kWarps * kNB * kItemBytes);  // [B+1]
@@ -1736,7 +1735,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     if (b < B) {
       unsigned int fl = 0;
       int gb = 0;
-      if (P.cu) {
+      if constexpr (PK) {
         cbase[b] = packed_base(P, b, gb, fl);
       } else {
         const int g_in = P.gamma ? P.gamma[b] : 0;
@@ -1854,16 +1853,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       const int gb = gamma_of<MODE>(rows_of<MODE>(rowpre, b), tconst, b);
       if (pend_kind == KIND_A) {
         if (MODE == MODE_SAMPLE && tconst[b].hi != 0.0f) {
-          decide_sample<EB>(P, b, gb, tconst[b], reinterpret_cast<float*>(scratch));
+          decide_sample<EB, PK>(P, b, gb, tconst[b], reinterpret_cast<float*>(scratch));
         } else {
-          decide_greedy(P, b, gb, reinterpret_cast<int*>(scratch));
+          decide_greedy<PK>(P, b, gb, reinterpret_cast<int*>(scratch));
           if (MODE == MODE_SAMPLE && lane == 0) {  // counted like any decision
             __threadfence();
             atomicAdd(P.dec_count, 1u);
           }
         }
       } else {
-        final_draw<EB>(P, b, tconst[b], scratch);
+        final_draw<EB, PK>(P, b, tconst[b], scratch);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -2012,9 +2011,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         Meta a;
         if (MODE == MODE_SAMPLE) {
           const TempC tc = tconst[cur.req];
-          a_item_at<EB, MODE>(P, cur, tc.hi, tc.lo, cbase, a);
+          a_item_at<EB, MODE, PK>(P, cur, tc.hi, tc.lo, cbase, a);
         } else {
-          a_item_at<EB, MODE>(P, cur, 0.0f, 0.0f, cbase, a);
+          a_item_at<EB, MODE, PK>(P, cur, 0.0f, 0.0f, cbase, a);
         }
         issue(a);
         cursor_next<MODE>(cur, rowpre, B, NC, tconst);
@@ -2026,7 +2025,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         Meta r;
         r.b = dec_b;
         r.c = (int)(r_i % (unsigned int)NCR);
-        fill_r_item<EB>(P, dc, cbase, r);
+        fill_r_item<EB, PK>(P, dc, cbase, r);
         issue(r);
         ++r_i;
       }
@@ -2045,6 +2044,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
       if (m_kind == KIND_A) {
         const bool staged = MODE == MODE_SAMPLE && m.c_hi != 0.0f;
+        if (staged && m.direct) stage_unaligned<EB>(m, stage);
         const float2 part = staged ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
         // stores into the buffer are ordered before the next bulk copy into it
@@ -2171,7 +2171,7 @@ constexpr size_t kMaxSmem = smem_bytes(kMaxBatch);
 static_assert(kMaxSmem <= 227 * 1024 - 8 * 1024, "shared memory budget");
 
 // Persistent grid: as many CTAs as fit on the device (cached per device).
-template <int EB, int MODE>
+template <int EB, int MODE, bool PK>
 int grid_size() {
   static int cached_dev = -1, cached_grid = 0;
   int dev = 0;
@@ -2179,10 +2179,10 @@ int grid_size() {
   if (dev == cached_dev && cached_grid > 0) return cached_grid;
   int sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaFuncSetAttribute(verify_kernel<EB, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(verify_kernel<EB, MODE, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kMaxSmem) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<EB, MODE>, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<EB, MODE, PK>, kThreads,
                                                     kMaxSmem) != cudaSuccess)
     return 0;
   cached_dev = dev;
@@ -2190,9 +2190,9 @@ int grid_size() {
   return cached_grid;
 }
 
-template <int EB, int MODE>
+template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
-  const int grid = grid_size<EB, MODE>();
+  const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch
   const int B = P.B;
@@ -2200,7 +2200,7 @@ int launch(const Params& P, cudaStream_t stream) {
     Params Q = P;
     Q.B = B - b0 < kMaxBatch ? B - b0 : kMaxBatch;
     const size_t G = (size_t)P.G, V = (size_t)P.V;
-    if (P.cu) {
+    if (PK) {
       // packed: rows, tokens, uniforms and p/q are addressed through cu,
       // which keeps global offsets; only per-request arrays move
       Q.cu = P.cu + b0;
@@ -2224,7 +2224,7 @@ int launch(const Params& P, cudaStream_t stream) {
     Q.stats = P.stats + (size_t)b0 * (2 * G + 1) * P.stride_nc;
     Q.resid = P.resid + (size_t)b0 * P.stride_ncr;
     const size_t smem = smem_bytes(Q.B);
-    verify_kernel<EB, MODE><<<grid, kThreads, smem, stream>>>(Q);
+    verify_kernel<EB, MODE, PK><<<grid, kThreads, smem, stream>>>(Q);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   }
   return SV_OK;
@@ -2330,7 +2330,8 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, sv_d
   if (rc) return rc;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE, false>(P, s)
+                          : launch<4, MODE_SAMPLE, false>(P, s);
 }
 
 int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, int V,
@@ -2348,7 +2349,8 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, int B, int G, 
   if (rc) return rc;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);
+  return dtype == SV_BF16 ? launch<2, MODE_GREEDY, false>(P, s)
+                          : launch<4, MODE_GREEDY, false>(P, s);
 }
 
 int spec_verify_sample_packed(const void* target_logits, const void* draft_logits,
@@ -2375,7 +2377,8 @@ int spec_verify_sample_packed(const void* target_logits, const void* draft_logit
   P.total = total_drafts;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE, true>(P, s)
+                          : launch<4, MODE_SAMPLE, true>(P, s);
 }
 
 int spec_verify_greedy_packed(const void* target_logits, sv_dtype dtype, int B, int G, int V,
@@ -2398,7 +2401,8 @@ int spec_verify_greedy_packed(const void* target_logits, sv_dtype dtype, int B, 
   P.total = total_drafts;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return dtype == SV_BF16 ? launch<2, MODE_GREEDY>(P, s) : launch<4, MODE_GREEDY>(P, s);
+  return dtype == SV_BF16 ? launch<2, MODE_GREEDY, true>(P, s)
+                          : launch<4, MODE_GREEDY, true>(P, s);
 }
 
 int spec_verify_draw(const void* logits, sv_dtype dtype, int B, int V, const float* uniforms,
@@ -2414,7 +2418,8 @@ int spec_verify_draw(const void* logits, sv_dtype dtype, int B, int V, const flo
   if (rc) return rc;
   if (B == 0) return SV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE, false>(P, s)
+                          : launch<4, MODE_SAMPLE, false>(P, s);
 }
 
 int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
@@ -2442,7 +2447,8 @@ int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logi
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // counters, arrival counts and decision records start at zero for every call
   if (cudaMemsetAsync(ws, 0, L.stats, s) != cudaSuccess) return SV_ERR_CUDA;
-  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE>(P, s) : launch<4, MODE_SAMPLE>(P, s);
+  return dtype == SV_BF16 ? launch<2, MODE_SAMPLE, false>(P, s)
+                          : launch<4, MODE_SAMPLE, false>(P, s);
 }
 
 int spec_verify_status(void* workspace, sv_stream_t stream, uint32_t* status_host) {
