@@ -49,7 +49,7 @@
  * Errors: each entry point returns SV_OK (0) or a negative SV_ERR_* code, and
  * on error launches nothing.  Values inside device arrays cannot be checked on
  * the host: a gamma_b outside [0, G], a draft token outside [0, V), a uniform
- * outside [0, 1), a non-positive or non-finite temperature, or a row with no
+ * outside [0, 1), a negative or non-finite temperature, or a row with no
  * finite logit sets a bit in the workspace's status word (read it with
  * spec_verify_status) and is clamped to a legal value, so no call reads or
  * writes outside the arrays described above.  NaN logits are not supported.

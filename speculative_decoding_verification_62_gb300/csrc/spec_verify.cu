@@ -1959,9 +1959,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
         a_first = ~0u;
       }
       // R work while A items remain only if the published, unclaimed R items
-      // (as loaded a batch ago) exceed a backlog of about two batches per
-      // warp: A items, which gate the decisions, go first, and the R work
-      // left when they run out is small enough to finish in parallel.
+      // (as loaded a batch ago) exceed a backlog of SV_BACKLOG_X4 / 4 batches
+      // per warp (16 by default, so in practice A items first): A items gate
+      // the decisions, and the R work left when they run out is spread over
+      // every warp.
       if (kind == 0 && MODE == MODE_SAMPLE && !r_done && pf_r < nR &&
           (a_done ? pf_r < pf_q * (unsigned int)NCR
                   : pf_r + r_backlog < pf_q * (unsigned int)NCR)) {
