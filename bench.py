@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layout", choices=["padded", "packed"], default="padded",
                     help="padded [B][G+1][V] rows, or packed rows with a cu_draft prefix")
+    ap.add_argument("--schedule", choices=["auto", "persistent"], default="auto",
+                    help="auto: small batches on the cluster schedule; persistent: always the grid")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step from Python instead of one CUDA-graph replay")
     return ap.parse_args()
@@ -252,6 +254,9 @@ def run_ours(args):
         base = W.make(args.config, device=dev, seed=rank_seed(base.meta["seed"], rank))
     mode = args.mode
     B, G, V = base.B, base.G, base.V
+    binding.spec_verify_set_schedule(binding.SCHEDULE_PERSISTENT if args.schedule == "persistent"
+                                     else binding.SCHEDULE_AUTO)
+    csize = binding.spec_verify_cluster_size(base.target.dtype, B, G, V, greedy=mode == "greedy")
     launches_per_call = 1
 
     packed = args.layout == "packed"
@@ -390,6 +395,8 @@ def run_ours(args):
     if rank == 0:
         cfg = workload_desc(base, mode)
         cfg.update({"layout": args.layout,
+                    "schedule": f"clusters of {csize} CTAs, one per request" if csize
+                                else "persistent grid",
                     "parallelism": f"replicas x{world} (independent requests)",
                     "launch": "one CUDA-graph replay of the timed steps" if graph is not None
                               else "one Python call per step",
@@ -405,7 +412,8 @@ def run_ours(args):
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "peak_source": peak_src,
                              "traffic": None if packed else profiled_traffic(args.config, mode),
-                             "kernel": "verify_kernel (one launch per step)"},
+                             "kernel": ("cluster_kernel" if csize else "verify_kernel") +
+                                       " (one launch per step)"},
                 "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * launches_per_call,
                 "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)

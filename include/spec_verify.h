@@ -244,6 +244,30 @@ int spec_verify_status(void *workspace, sv_stream_t stream, uint32_t *status_hos
 /* Static English text for an SV_OK / SV_ERR_* code. */
 const char *spec_verify_strerror(int code);
 
+/*
+ * Schedules.  A batch small enough that one thread-block cluster per request
+ * fits on the GPU at once runs on the cluster schedule: each request's
+ * partials, decision and residual block sums move through the cluster's
+ * shared memory instead of global-memory counters and records, which shortens
+ * the chain of dependent steps (statistics, decision, residual pass, draw).
+ * Larger batches run on the persistent grid.  Both compute every value with
+ * the same arithmetic, so outputs do not depend on the schedule.  These two
+ * calls are not steps of the method: they exist for testing and measurement.
+ *
+ * spec_verify_set_schedule: SV_SCHEDULE_AUTO (the default) or
+ * SV_SCHEDULE_PERSISTENT (every call on the persistent grid), for the calls
+ * that follow in this process.  Returns the previous value, or SV_ERR_SCALAR
+ * for an unknown value.
+ *
+ * spec_verify_cluster_size: the cluster size (CTAs per request) the next
+ * sampling (greedy == 0) or greedy call of this shape on the current device
+ * would use, 0 for the persistent grid, or SV_ERR_SCALAR for invalid sizes.
+ */
+#define SV_SCHEDULE_AUTO 0
+#define SV_SCHEDULE_PERSISTENT 1
+int spec_verify_set_schedule(int schedule);
+int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,9 @@ STATUS_BITS = {1: "BAD_GAMMA", 2: "BAD_TOKEN", 4: "BAD_UNIFORM", 8: "BAD_TEMPERA
 SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy",
            "spec_verify_sample_packed", "spec_verify_greedy_packed", "spec_verify_draw",
-           "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror")
+           "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror",
+           "spec_verify_set_schedule", "spec_verify_cluster_size")
+SCHEDULE_AUTO, SCHEDULE_PERSISTENT = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -65,12 +67,33 @@ def load_library():
         lib.spec_verify_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.spec_verify_strerror.restype = ctypes.c_char_p
         lib.spec_verify_strerror.argtypes = [ci]
+        lib.spec_verify_set_schedule.restype = ci
+        lib.spec_verify_set_schedule.argtypes = [ci]
+        lib.spec_verify_cluster_size.restype = ci
+        lib.spec_verify_cluster_size.argtypes = [ci, ci, ci, ci, ci]
         _lib = lib
         return lib
 
 
 def spec_verify_strerror(code: int) -> str:
     return load_library().spec_verify_strerror(int(code)).decode()
+
+
+def spec_verify_set_schedule(schedule: int) -> int:
+    """SCHEDULE_AUTO or SCHEDULE_PERSISTENT for the calls that follow; returns the previous."""
+    rc = load_library().spec_verify_set_schedule(int(schedule))
+    if rc < 0:
+        raise SpecVerifyError(rc)
+    return rc
+
+
+def spec_verify_cluster_size(dtype: torch.dtype, B: int, G: int, V: int, greedy: bool = False) -> int:
+    """CTAs per request of the cluster schedule for this shape, 0 for the persistent grid."""
+    code = SV_BF16 if dtype == torch.bfloat16 else SV_F32
+    rc = load_library().spec_verify_cluster_size(code, int(B), int(G), int(V), int(bool(greedy)))
+    if rc < 0:
+        raise SpecVerifyError(rc)
+    return rc
 
 
 def spec_verify_workspace_size(B: int, G: int, V: int) -> int:

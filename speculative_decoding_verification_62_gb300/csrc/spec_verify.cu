@@ -51,6 +51,7 @@
 // depend on summation order.
 
 #include <cuda_runtime.h>
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 #include <math.h>
@@ -659,6 +660,26 @@ __device__ __forceinline__ FF shfl_xor_ff(FF v, int o) {
   return FF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
 }
 
+// Where a request's per-item partials are read from: slot s (target row s, or
+// draft row i at slot G + 1 + i), item c.
+struct GlobalParts {  // the workspace: written by other SMs, so read past L1
+  const float2* p;
+  size_t stride;
+  __device__ __forceinline__ float2 operator()(int slot, int c) const {
+    return __ldcg(p + (size_t)slot * stride + (size_t)c);
+  }
+};
+struct SharedParts {  // this CTA's shared memory
+  const float2* p;
+  int stride;
+  __device__ __forceinline__ float2 operator()(int slot, int c) const {
+    return p[slot * stride + c];
+  }
+};
+__device__ __forceinline__ GlobalParts global_parts(const Params& P, int b) {
+  return GlobalParts{P.stats + (size_t)b * (2 * P.G + 1) * P.stride_nc, (size_t)P.stride_nc};
+}
+
 // The per-item partials of a request's rows are reduced eight rows at a time:
 // lanes 4r..4r+3 take row r of the group, each every fourth chunk (up to
 // kHeld chunks held in registers, the rest in a tail loop).  The code is kept
@@ -667,9 +688,9 @@ constexpr int kHeld = 10;
 
 // Row statistics (sampling): M = max, S = sum_c s_c 2^((m_c - M) c) in
 // float-float, written to rs[r] (M), rs[64 + r] (S hi), rs[128 + r] (S lo).
-template <int EB>
-__device__ __forceinline__ unsigned int row_stats(const Params& P, int b, int gb, TempC tc,
-                                                  float* rs) {
+template <int EB, class Parts>
+__device__ __forceinline__ unsigned int row_stats(const Params& P, const Parts& parts, int gb,
+                                                  TempC tc, float* rs) {
   const int G = P.G, NC = P.NC;
   const int lane = threadIdx.x & 31, part = lane & 3;
   const int nrows = 2 * gb + 1;
@@ -679,19 +700,18 @@ __device__ __forceinline__ unsigned int row_stats(const Params& P, int b, int gb
   for (int r0 = 0; r0 < nrows; r0 += 8) {
     const int r = r0 + (lane >> 2);
     const bool live = r < nrows;
-    const int slot = r <= gb ? r : (G + 1 + (r - gb - 1));
-    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + (live ? slot : 0)) * P.stride_nc;
+    const int slot = live ? (r <= gb ? r : (G + 1 + (r - gb - 1))) : 0;
     float2 v[kHeld];
 #pragma unroll
     for (int j = 0; j < kHeld; ++j) {
       const int c = part + 4 * j;
-      v[j] = (live && c < NC) ? __ldcg(&pr[c]) : none;
+      v[j] = (live && c < NC) ? parts(slot, c) : none;
     }
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kHeld; ++j) m = fmaxf(m, v[j].x);
 #pragma unroll 1
-    for (int c = part + 4 * kHeld; live && c < NC; c += 4) m = fmaxf(m, __ldcg(&pr[c]).x);
+    for (int c = part + 4 * kHeld; live && c < NC; c += 4) m = fmaxf(m, parts(slot, c).x);
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     FF S{0.0f, 0.0f};
@@ -702,7 +722,7 @@ __device__ __forceinline__ unsigned int row_stats(const Params& P, int b, int gb
           S = ff_add(S, FF{__fmul_rn(v[j].y, ex2_approx(exp_arg(v[j].x, m, tc.hi, tc.lo))), 0.0f});
 #pragma unroll 1
       for (int c = part + 4 * kHeld; live && c < NC; c += 4) {
-        const float2 ms = __ldcg(&pr[c]);
+        const float2 ms = parts(slot, c);
         if (ms.x > -INFINITY)
           S = ff_add(S, FF{__fmul_rn(ms.y, ex2_approx(exp_arg(ms.x, m, tc.hi, tc.lo))), 0.0f});
       }
@@ -754,9 +774,9 @@ __device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b
 // total the walk continues into the next chunk, and past the last one the
 // highest-indexed token of positive weight is taken.  The CDF is accurate to
 // about 1e-7 of S, like the residual path's.
-template <int EB, bool PK>
-__device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC tc, float M,
-                                         unsigned char* stage) {
+template <int EB, bool PK, class Parts>
+__device__ __noinline__ void final_bonus(const Params& P, const Parts& parts, int b, int gb,
+                                         TempC tc, float M, unsigned char* stage) {
   constexpr int AE = kItemBytes / EB;  // logits per A chunk
   constexpr int EPL = AE / 32;         // contiguous logits per lane
   constexpr int VEC = 16 / EB;
@@ -766,9 +786,8 @@ __device__ __noinline__ void final_bonus(const Params& P, int b, int gb, TempC t
   unsigned int flags = 0;
   const ReqAddr A = req_addr<PK>(P, b);
   const float u = sanitize_uniform(P.uniforms[A.uf], flags);
-  const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + gb) * P.stride_nc;
   auto chunk_w = [&](int c) -> float {
-    const float2 ms = __ldcg(&pr[c]);
+    const float2 ms = parts(gb, c);
     return ms.x > -INFINITY ? __fmul_rn(ms.y, ex2_approx(exp_arg(ms.x, M, tc.hi, tc.lo))) : 0.0f;
   };
   // 1. the chunk: lane l owns chunks [c0, c1)
@@ -911,27 +930,44 @@ __device__ __noinline__ bool q_underflows(FF e, FF S) {
   return exp2((double)e.hi + (double)e.lo) / ((double)S.hi + (double)S.lo) == 0.0;
 }
 
-template <int EB, bool PK>
-__device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC tc, float* rs) {
-  const int G = P.G, V = P.V;
+// Request b's drafted tokens, their acceptance uniforms and the target and
+// draft logits at them: lane i < gamma_b holds position i.
+struct DraftIn {
+  int x;
+  float u, zt, zd;
+  unsigned int flags;
+};
+template <int EB>
+__device__ __forceinline__ DraftIn gather_drafts(const Params& P, const ReqAddr& A, int gb) {
+  const int i = threadIdx.x & 31, V = P.V;
+  DraftIn g{0, 0.0f, 0.0f, 0.0f, 0u};
+  if (i < gb) {
+    g.x = P.tokens[A.d0 + i];
+    g.u = sanitize_uniform(P.uniforms[A.u0 + i], g.flags);
+    if (g.x < 0 || g.x >= V) {
+      g.flags |= SV_STATUS_BAD_TOKEN;
+      g.x = g.x < 0 ? 0 : V - 1;
+    }
+    g.zt = load_elem<EB>(P.target, (A.t0 + i) * (size_t)V + (size_t)g.x);
+    g.zd = load_elem<EB>(P.draft, (A.d0 + i) * (size_t)V + (size_t)g.x);
+  }
+  return g;
+}
+
+// The acceptance tests of request b from its row statistics: writes
+// out_tokens (all but position k), num_accepted, p/q and status, and returns
+// k on every lane with the decision on lane 0.
+template <int EB, bool PK, class Parts>
+__device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, int b, int gb,
+                                           TempC tc, float* rs, const ReqAddr& A,
+                                           const DraftIn& g, Decision& d) {
+  const int G = P.G;
   const int lane = threadIdx.x & 31;
   const int i = lane;
-  unsigned int flags = 0;
-  // the drafted tokens, their uniforms and logits are requested first
-  const ReqAddr A = req_addr<PK>(P, b);
-  int x = 0;
-  float u = 0.0f, zt = 0.0f, zd = 0.0f;
-  if (i < gb) {
-    x = P.tokens[A.d0 + i];
-    u = sanitize_uniform(P.uniforms[A.u0 + i], flags);
-    if (x < 0 || x >= V) {
-      flags |= SV_STATUS_BAD_TOKEN;
-      x = x < 0 ? 0 : V - 1;
-    }
-    zt = load_elem<EB>(P.target, (A.t0 + i) * (size_t)V + (size_t)x);
-    zd = load_elem<EB>(P.draft, (A.d0 + i) * (size_t)V + (size_t)x);
-  }
-  flags |= row_stats<EB>(P, b, gb, tc, rs);
+  const int x = g.x;
+  const float u = g.u, zt = g.zt, zd = g.zd;
+  unsigned int flags = g.flags;
+  flags |= row_stats<EB>(P, parts, gb, tc, rs);
 
   // Acceptance test per position (lane i), then the first-reject ballot.
   // ratio p/q = 2^(e_t - e_d) * S_d / S_t with e = (z - m) log2(e)/T in
@@ -983,7 +1019,6 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
     const int kd = gb + 1 + (k < gb ? k : 0);
     const FF st_k{rs[64 + k], rs[128 + k]}, sd_k{rs[64 + kd], rs[128 + kd]};
     if (P.num_accepted) P.num_accepted[b] = k;
-    Decision d;
     d.k = k;
     d.reject = k < gb ? 1 : 0;
     d.mt = rs[k];
@@ -993,6 +1028,23 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
     d.c_hi = tc.hi;
     d.c_lo = tc.lo;
     if (any) atomicOr(P.status, any);
+  }
+  return k;
+}
+
+// Sampling decision on the persistent path, run by the warp that completed
+// request b's last A item: publishes a reject to the decision record and the
+// queue, or draws the bonus token itself.
+template <int EB, bool PK>
+__device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC tc, float* rs) {
+  const int lane = threadIdx.x & 31;
+  const ReqAddr A = req_addr<PK>(P, b);
+  // the drafted tokens, their uniforms and logits are requested first
+  const DraftIn g = gather_drafts<EB>(P, A, gb);
+  Decision d;
+  const GlobalParts parts = global_parts(P, b);
+  const int k = decide_core<EB, PK>(P, parts, b, gb, tc, rs, A, g, d);
+  if (lane == 0) {
     P.cnt_a[b] = 0;
     if (d.reject) {
       // R work: the decision goes to the request's record and the queue
@@ -1001,7 +1053,7 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
     }
   }
   __syncwarp();
-  if (k == gb) final_bonus<EB, PK>(P, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
+  if (k == gb) final_bonus<EB, PK>(P, parts, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
   if (lane == 0) {
     __threadfence();  // a queue entry is visible before the count that covers it
     atomicAdd(P.dec_count, 1u);
@@ -1012,8 +1064,9 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
 // Greedy decision: argmax per target row from the per-item partials (rows
 // reduced eight at a time as above; rs holds the row argmaxes), then the
 // first mismatch by warp ballot.
-template <bool PK>
-__device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* rs) {
+template <bool PK, class Parts>
+__device__ __forceinline__ void greedy_core(const Params& P, const Parts& parts, int b, int gb,
+                                            int* rs) {
   const int G = P.G, V = P.V, NC = P.NC;
   const int lane = threadIdx.x & 31, part = lane & 3;
   unsigned int flags = 0;
@@ -1025,12 +1078,12 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   for (int r0 = 0; r0 <= gb; r0 += 8) {
     const int r = r0 + (lane >> 2);
     const bool live = r <= gb;
-    const float2* pr = P.stats + ((size_t)b * (2 * G + 1) + (live ? r : 0)) * P.stride_nc;
+    const int slot = live ? r : 0;
     float2 v[kHeld];
 #pragma unroll
     for (int j = 0; j < kHeld; ++j) {
       const int c = part + 4 * j;
-      v[j] = (live && c < NC) ? __ldcg(&pr[c]) : make_float2(-INFINITY, __int_as_float(0x7fffffff));
+      v[j] = (live && c < NC) ? parts(slot, c) : make_float2(-INFINITY, __int_as_float(0x7fffffff));
     }
     float bv = -INFINITY;
     int bi = 0x7fffffff;
@@ -1038,7 +1091,7 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
     for (int j = 0; j < kHeld; ++j) argmax_combine(bv, bi, v[j].x, __float_as_int(v[j].y));
 #pragma unroll 1
     for (int c = part + 4 * kHeld; live && c < NC; c += 4) {
-      const float2 mi = __ldcg(&pr[c]);
+      const float2 mi = parts(slot, c);
       argmax_combine(bv, bi, mi.x, __float_as_int(mi.y));
     }
 #pragma unroll
@@ -1070,8 +1123,13 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   if (lane == 0) {
     if (P.num_accepted) P.num_accepted[b] = k;
     if (any) atomicOr(P.status, any);
-    P.cnt_a[b] = 0;
   }
+  __syncwarp();
+}
+template <bool PK>
+__device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* rs) {
+  greedy_core<PK>(P, global_parts(P, b), b, gb, rs);
+  if ((threadIdx.x & 31) == 0) P.cnt_a[b] = 0;
   __syncwarp();
 }
 
@@ -2153,6 +2211,468 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
 }
 
 // ---------------------------------------------------------------------------
+// Small batches: one thread-block cluster per request
+// ---------------------------------------------------------------------------
+// With few requests the persistent schedule is bound by its chain of
+// global-memory synchronisations (arrival counters, decision records, queue
+// polls), each an L2 round trip.  Here request b gets cluster b of C CTAs,
+// one per SM.  Every warp streams a fixed share of the request's A items and
+// stores each partial into the leader CTA's (rank 0) shared memory; a
+// cluster barrier replaces the arrival counter; the leader's warp 0 decides
+// from its own shared memory (the same arithmetic as the persistent path)
+// and copies the decision into every CTA.  After a reject, the R items store
+// per-block fixed-point sums in the leader, and the leader walks one block of
+// 256 (bf16) or 128 (float32) tokens.
+constexpr int kBlk = 8;                          // blocks per R item: one per vector column
+constexpr int kClusterTables = 32 * 1024;        // leader tables: partials, block sums, decision
+constexpr size_t kClusterSmem = (size_t)kWarps * kNB * kItemBytes + kClusterTables;
+static_assert(kClusterSmem <= 227 * 1024, "cluster shared memory budget");
+
+struct ClusterDec {  // the decision, as every CTA of the cluster holds it
+  int k, go;         // go: 1 when R items follow (a rejected draft)
+  float mt, md, inv_st, rho, c_hi, c_lo;
+};
+constexpr int kDecWords = (int)(sizeof(ClusterDec) / 4);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: stores before it (shared memory
+// of any CTA) are visible to loads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of location p in CTA `rank`.
+__device__ __forceinline__ uint32_t rank_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f2(uint32_t a, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u64(uint32_t a, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Both halves of an R item whose bytes cannot be bulk-copied, loaded with
+// plain loads and padded with -inf to whole vectors (a -inf logit has weight
+// exactly 0 in both the residual and the bonus formula).
+template <int EB>
+__device__ __noinline__ void stage_r_unaligned(const char* p0, const char* p1, int n, char* stage) {
+  constexpr int VEC = 16 / EB;
+  const int lane = threadIdx.x & 31;
+  const int ne = (n + VEC - 1) / VEC * VEC;
+  for (int e = lane; e < ne; e += 32) {
+    if constexpr (EB == 2) {
+      const unsigned short ninf = 0xff80u;
+      reinterpret_cast<unsigned short*>(stage)[e] =
+          e < n ? __ldg(reinterpret_cast<const unsigned short*>(p0) + e) : ninf;
+      reinterpret_cast<unsigned short*>(stage + kHalfBytes)[e] =
+          (p1 && e < n) ? __ldg(reinterpret_cast<const unsigned short*>(p1) + e) : ninf;
+    } else {
+      const unsigned int ninf = 0xff800000u;
+      reinterpret_cast<unsigned int*>(stage)[e] =
+          e < n ? __ldg(reinterpret_cast<const unsigned int*>(p0) + e) : ninf;
+      reinterpret_cast<unsigned int*>(stage + kHalfBytes)[e] =
+          (p1 && e < n) ? __ldg(reinterpret_cast<const unsigned int*>(p1) + e) : ninf;
+    }
+  }
+  __syncwarp();
+}
+
+// R item on the cluster path: lane l's vector j (vector index l + 32 j) lies
+// in block j of the item; blk[j] is the block's sum of round(w 2^39) over its
+// tokens, from the same per-token operations as draw_weight (a block's sum
+// therefore equals the prefix walk over it exactly).
+template <int EB, bool REJECT>
+__device__ __forceinline__ void r_item_blocks(const char* stage, int nvec, const ResidC& kc,
+                                              unsigned long long (&blk)[kBlk]) {
+  constexpr int VEC = 16 / EB;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < kBlk; ++j) {
+    const int vi = lane + 32 * j;
+    FixAcc a{0u, 0u, 0u};
+    if (vi < nvec) {
+      const uint4 t = lds128(stage + vi * 16);
+      const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+#pragma unroll
+      for (int q = 0; q < VEC; ++q)
+        fix_add(a, draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc));
+    }
+    blk[j] = warp_sum_u64(fix_value(a));
+  }
+}
+
+// Block sums of the draw weights of target row k alone (kc.reject == 0), for
+// the fallback when the residual vanished in fixed point: block bl, warp by
+// warp over the leader CTA, each lane one vector read from global memory.
+template <int EB>
+__device__ __noinline__ void p_blocks(const char* trow, int V, const ResidC& kc, int nblk,
+                                      unsigned long long* blk) {
+  constexpr int VEC = 16 / EB;
+  constexpr int RE = kHalfBytes / EB;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int bl = warp; bl < nblk; bl += kWarps) {
+    const int c = bl / kBlk, j = bl % kBlk;
+    const size_t e0 = (size_t)c * RE + (size_t)(lane + 32 * j) * VEC;
+    unsigned long long s = 0;
+#pragma unroll
+    for (int h = 0; h < VEC; ++h) {
+      const size_t e = e0 + (size_t)h;
+      if (e < (size_t)V) s += draw_weight<false>(load_elem<EB>(trow, e), -INFINITY, kc);
+    }
+    s = warp_sum_u64(s);
+    if (lane == 0) blk[bl] = s;
+  }
+}
+
+// Final draw on the cluster path (leader warp 0): the block whose prefix
+// passes floor(u S), then one pass over its tokens, one vector per lane.
+template <int EB>
+__device__ __noinline__ int cluster_walk(const char* trow, const char* drow, int V, float u_s,
+                                         const ResidC& kc, const unsigned long long* blk,
+                                         int nblk, unsigned int& flags) {
+  constexpr int VEC = 16 / EB;
+  constexpr int RE = kHalfBytes / EB;
+  const int lane = threadIdx.x & 31;
+  // 1. the block: lane l owns blocks [b0, b1)
+  const int bpl = (nblk + 31) >> 5;
+  const int b0 = min(nblk, lane * bpl), b1 = min(nblk, b0 + bpl);
+  unsigned long long own = 0;
+#pragma unroll 1
+  for (int bl = b0; bl < b1; ++bl) own += blk[bl];
+  const unsigned long long incl = warp_incl_scan_u64(own);
+  const unsigned long long S = __shfl_sync(0xffffffffu, incl, 31);
+  const unsigned long long target = scaled_target(u_s, S);  // < S
+  int bs = -1;
+  unsigned long long base = 0;
+  {
+    const unsigned long long excl = incl - own;
+    const unsigned int hit = __ballot_sync(0xffffffffu, excl <= target && target < incl);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      if (lane == l) {
+        unsigned long long run = excl;
+#pragma unroll 1
+        for (int bl = b0; bl < b1; ++bl) {
+          if (run + blk[bl] > target) {
+            bs = bl;
+            break;
+          }
+          run += blk[bl];
+        }
+        base = run;
+      }
+      bs = __shfl_sync(0xffffffffu, bs, l);
+      base = __shfl_sync(0xffffffffu, base, l);
+    }
+  }
+  if (bs < 0) {
+    flags |= SV_STATUS_INTERNAL;
+    return V - 1;
+  }
+  // 2. the token inside block bs: lane l holds tokens [e0, e0 + VEC)
+  const size_t e0 = (size_t)(bs / kBlk) * RE + (size_t)(lane + 32 * (bs % kBlk)) * VEC;
+  float zt[VEC], zd[VEC];
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15) == 0 &&
+                      e0 + VEC <= (size_t)V;
+  if (vec_ok) {
+    const uint4 t = __ldcg(reinterpret_cast<const uint4*>(trow + e0 * EB));
+    const uint4 d = drow ? __ldcg(reinterpret_cast<const uint4*>(drow + e0 * EB)) : neg_inf_vec(EB);
+#pragma unroll
+    for (int h = 0; h < VEC; ++h) {
+      zt[h] = vec_elem<EB>(t, h);
+      zd[h] = vec_elem<EB>(d, h);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < VEC; ++h) {
+      const size_t e = e0 + (size_t)h;
+      zt[h] = e < (size_t)V ? load_elem<EB>(trow, e) : -INFINITY;
+      zd[h] = (drow && e < (size_t)V) ? load_elem<EB>(drow, e) : -INFINITY;
+    }
+  }
+  unsigned long long w[VEC];
+  unsigned long long lsum = 0;
+#pragma unroll
+  for (int h = 0; h < VEC; ++h) {
+    w[h] = draw_weight(zt[h], zd[h], kc);
+    lsum += w[h];
+  }
+  const unsigned long long li = warp_incl_scan_u64(lsum);
+  unsigned long long run = base + li - lsum;
+  int tok = -1;
+  if (run <= target && target < run + lsum) {
+#pragma unroll
+    for (int h = 0; h < VEC; ++h) {
+      if (tok < 0 && run + w[h] > target) tok = (int)(e0 + (size_t)h);
+      run += w[h];
+    }
+  }
+  const unsigned int holder = __ballot_sync(0xffffffffu, tok >= 0);
+  if (!holder) {
+    flags |= SV_STATUS_INTERNAL;
+    return V - 1;
+  }
+  return __shfl_sync(0xffffffffu, tok, __ffs(holder) - 1);
+}
+
+// One request per cluster.  Shared memory: the warps' staging buffers, then
+// (the same layout in every CTA, used in the leader) the partials
+// [2G+1][NC], the block sums [NCR][kBlk] and the decision.
+template <int EB, int MODE, bool PK>
+__global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ __align__(8) uint64_t bar[kWarps][kNB];
+  __shared__ Meta cmeta[kWarps][kNB];  // the item in each buffer
+  constexpr int AE = kItemBytes / EB;   // logits per A item
+  constexpr int RE = kHalfBytes / EB;   // logits per R item and row
+  constexpr int VEC = 16 / EB;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank(), C = cluster_size();
+  const int b = (int)cluster_index();
+  const int G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
+  float2* part = reinterpret_cast<float2*>(dsmem + (size_t)kWarps * kNB * kItemBytes);
+  unsigned long long* blk = reinterpret_cast<unsigned long long*>(part + (size_t)(2 * G + 1) * NC);
+  ClusterDec* cdec = reinterpret_cast<ClusterDec*>(blk + (size_t)NCR * kBlk);
+  unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
+  uint64_t* mybar = bar[warp];
+  Meta* mymeta = cmeta[warp];
+
+  // the request: draft length, addresses, temperature constants
+  unsigned int rflags = 0, flags = 0;
+  int gb = 0, base = 0;
+  if constexpr (PK) {
+    base = packed_base(P, b, gb, rflags);
+  } else {
+    const int g_in = P.gamma ? P.gamma[b] : 0;
+    gb = clamp_gamma(g_in, G);
+    if (g_in != gb) rflags |= SV_STATUS_BAD_GAMMA;
+  }
+  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+  bool greedy = MODE == MODE_GREEDY;
+  TempC tc{0.0f, 0.0f};
+  if (MODE == MODE_SAMPLE) {
+    const float T = P.temperature[b];
+    if (T == 0.0f) greedy = true;  // this request takes the greedy steps
+    else tc = temp_consts(sanitize_temperature(T, rflags));
+  }
+  const int rows = greedy ? gb + 1 : 2 * gb + 1;
+  const unsigned int nA = (unsigned int)rows * (unsigned int)NC;
+  const unsigned int CW = C * kWarps, gw = rank * kWarps + (unsigned int)warp;
+  const bool leader = rank == 0 && warp == 0;
+
+  if (tid == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < kNB; ++s) mbar_init(&bar[w][s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // the leader's draft inputs are requested before its items
+  DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
+  if (MODE == MODE_SAMPLE && leader && !greedy) gin = gather_drafts<EB>(P, A, gb);
+
+  // ---- A items: i = gw, gw + CW, ...; row-major (target rows, then draft rows)
+  unsigned int issued = 0, processed = 0;  // copies through this warp's buffers
+  bool failed = false;
+  auto a_meta = [&](unsigned int i, Meta& m) {
+    const int r = (int)(i / (unsigned int)NC), c = (int)(i % (unsigned int)NC);
+    const bool trg = r <= gb;
+    m.kind = KIND_A;
+    m.pslot = trg ? r : G + 1 + (r - gb - 1);
+    m.c = c;
+    m.n = min(AE, V - c * AE);
+    const size_t row = trg ? A.t0 + (size_t)r : A.d0 + (size_t)(r - gb - 1);
+    m.p0 = (trg ? P.target : P.draft) + (row * (size_t)V + (size_t)c * AE) * EB;
+    m.p1 = nullptr;
+    m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+    m.c_hi = tc.hi;
+    m.c_lo = tc.lo;
+  };
+  auto a_issue = [&](const Meta& m) {
+    const int s = (int)(issued % kNB);
+    if (lane == 0) {
+      mymeta[s] = m;
+      if (m.direct) {
+        mbar_arrive(&mybar[s]);
+      } else {
+        mbar_arrive_expect_tx(&mybar[s], (unsigned int)(m.n * EB));
+        bulk_copy_g2s(mybuf + s * kItemBytes, m.p0, (unsigned int)(m.n * EB), &mybar[s]);
+      }
+    }
+    __syncwarp();
+    ++issued;
+  };
+  {
+    const uint32_t part_r = rank_addr(part, 0);
+    unsigned int next = gw;
+    for (int s = 0; s < kNB && next < nA; ++s, next += CW) {
+      Meta m;
+      a_meta(next, m);
+      a_issue(m);
+    }
+    // every issued copy is waited for once (bounded), also after a timeout
+    while (processed != issued) {
+      const int s = (int)(processed % kNB);
+      const Meta& m = mymeta[s];
+      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+        flags |= SV_STATUS_TIMEOUT;
+        failed = true;
+      } else if (!failed) {
+        char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
+        const bool sample = MODE == MODE_SAMPLE && !greedy;
+        if (sample && m.direct) stage_unaligned<EB>(m, stage);
+        const float2 pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
+        if (lane == 0)
+          st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
+        if (sample && m.direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      ++processed;
+      if (!failed && next < nA) {
+        Meta m2;
+        a_meta(next, m2);
+        a_issue(m2);
+        next += CW;
+      }
+    }
+  }
+  cluster_sync();  // every partial is in the leader
+
+  // ---- the decision (leader warp 0), copied into every CTA of the cluster
+  if (leader) {
+    float* rs = reinterpret_cast<float*>(mybuf);  // this warp's buffers are idle now
+    const SharedParts sp{part, NC};
+    ClusterDec cd;
+    cd.k = 0;
+    cd.go = 0;
+    cd.mt = cd.md = cd.inv_st = cd.rho = 0.0f;
+    cd.c_hi = tc.hi;
+    cd.c_lo = tc.lo;
+    if (greedy) {
+      greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
+    } else {
+      Decision d;
+      d.k = 0;
+      d.reject = 0;
+      d.mt = d.md = d.inv_st = d.rho = 0.0f;
+      const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d);
+      cd.k = k;
+      cd.go = __shfl_sync(0xffffffffu, d.reject, 0);
+      cd.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+      cd.md = __shfl_sync(0xffffffffu, d.md, 0);
+      cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+      cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+      if (k == gb) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
+    }
+    // lane r < C copies the decision into CTA r
+    if ((uint32_t)lane < C) {
+      const uint32_t dst = rank_addr(cdec, (uint32_t)lane);
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(&cd);
+#pragma unroll
+      for (int w = 0; w < kDecWords; ++w) st_cluster_u32(dst + 4u * (uint32_t)w, src[w]);
+    }
+    if (lane == 0 && rflags) atomicOr(P.status, rflags);
+  }
+  cluster_sync();  // every CTA holds the decision
+  const ClusterDec cd = *cdec;
+
+  if (cd.go) {
+    // ---- R items of the rejected position k: i = gw, gw + CW, ...
+    ResidC kc;
+    kc.mt = cd.mt; kc.md = cd.md; kc.inv_st = cd.inv_st; kc.rho = cd.rho;
+    resid_scales(kc);
+    kc.hi = cd.c_hi; kc.lo = cd.c_lo; kc.reject = 1;
+    const int k = cd.k < 0 ? 0 : (cd.k > G ? G : cd.k);
+    const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
+    const char* drow = P.draft + (A.d0 + (size_t)k) * (size_t)V * EB;
+    const uint32_t blk_r = rank_addr(blk, 0);
+    for (unsigned int i = gw; i < (unsigned int)NCR && !failed; i += CW) {
+      const int s = (int)(issued % kNB);
+      const int n = min(RE, V - (int)i * RE);
+      const char* p0 = trow + (size_t)i * RE * EB;
+      const char* p1 = drow + (size_t)i * RE * EB;
+      char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
+      const bool direct = (((reinterpret_cast<uintptr_t>(p0) | reinterpret_cast<uintptr_t>(p1)) & 15) != 0) ||
+                          ((n * EB) & 15) != 0;
+      if (lane == 0) {
+        if (direct) {
+          mbar_arrive(&mybar[s]);
+        } else {
+          mbar_arrive_expect_tx(&mybar[s], (unsigned int)(2 * n * EB));
+          bulk_copy_g2s(stage, p0, (unsigned int)(n * EB), &mybar[s]);
+          bulk_copy_g2s(stage + kHalfBytes, p1, (unsigned int)(n * EB), &mybar[s]);
+        }
+      }
+      __syncwarp();
+      ++issued;
+      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+        flags |= SV_STATUS_TIMEOUT;
+        failed = true;
+        ++processed;
+        break;
+      }
+      if (direct) stage_r_unaligned<EB>(p0, p1, n, stage);
+      unsigned long long bs[kBlk];
+      r_item_blocks<EB, true>(stage, (n + VEC - 1) / VEC, kc, bs);
+#pragma unroll
+      for (int j = 0; j < kBlk; ++j)
+        if (lane == j) st_cluster_u64(blk_r + (uint32_t)((i * kBlk + j) * sizeof(unsigned long long)), bs[j]);
+      if (direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      ++processed;
+    }
+    cluster_sync();  // every block sum is in the leader
+
+    // ---- the final draw (leader CTA)
+    if (rank == 0) {
+      const int nblk = NCR * kBlk;
+      unsigned long long S = 0;
+      for (int bl = lane; bl < nblk; bl += 32) S += blk[bl];
+      S = warp_sum_u64(S);
+      if (S == 0ull) {
+        // The residual vanished in fixed point (p_k and q_k agree within its
+        // resolution): draw from p_k instead, its block sums computed by the
+        // whole leader CTA.
+        kc.reject = 0;
+        __syncthreads();
+        p_blocks<EB>(trow, V, kc, nblk, blk);
+        __syncthreads();
+      }
+      if (warp == 0) {
+        unsigned int wf = 0;
+        const float u_s = sanitize_uniform(P.uniforms[A.uf], wf);
+        const int tok = cluster_walk<EB>(trow, kc.reject ? drow : nullptr, V, u_s, kc, blk, nblk, wf);
+        if (lane == 0) {
+          P.out_tokens[(size_t)b * (G + 1) + k] = tok;
+          flags |= wf;
+        }
+      }
+    }
+  }
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && any) atomicOr(P.status, any);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 int check_scalars(sv_dtype dtype, int B, int G, int V) {
@@ -2191,8 +2711,83 @@ int grid_size() {
   return cached_grid;
 }
 
+// Schedule of the next calls: SV_SCHEDULE_AUTO runs a batch that fits one
+// wave of clusters on the cluster path; SV_SCHEDULE_PERSISTENT forces the
+// persistent grid (testing and benchmarking).
+std::atomic<int> g_schedule{SV_SCHEDULE_AUTO};
+
+size_t cluster_tables(int G, int V, int eb) {
+  const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
+  const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
+  return (size_t)(2 * G + 1) * nc * sizeof(float2) + ncr * kBlk * sizeof(unsigned long long) +
+         sizeof(ClusterDec);
+}
+
+// Clusters of C CTAs that fit on this device at once (cached per device).
+template <int EB, int MODE, bool PK>
+int max_clusters(int C) {
+  static int cached_dev[2] = {-1, -1}, cached[2] = {0, 0};
+  const int slot = C > 8 ? 0 : 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev == cached_dev[slot]) return cached[slot];
+  auto kern = cluster_kernel<EB, MODE, PK>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmem) ==
+          cudaSuccess &&
+      (C <= 8 || cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                     cudaSuccess)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned int)C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kClusterSmem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned int)C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();  // a refused size only means that size is not used
+  cached_dev[slot] = dev;
+  cached[slot] = n;
+  return n;
+}
+
+// Cluster size for this call, or 0 for the persistent grid.
+template <int EB, int MODE, bool PK>
+int cluster_route(int B, int G, int V) {
+  if (g_schedule.load() == SV_SCHEDULE_PERSISTENT) return 0;
+  if (B < 1 || cluster_tables(G, V, EB) > (size_t)kClusterTables) return 0;
+  if (max_clusters<EB, MODE, PK>(16) >= B) return 16;
+  if (max_clusters<EB, MODE, PK>(8) >= B) return 8;
+  return 0;
+}
+
+template <int EB, int MODE, bool PK>
+int launch_cluster(const Params& P, int C, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned int)(P.B * C));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)kWarps * kNB * kItemBytes + cluster_tables(P.G, P.V, EB);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned int)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, cluster_kernel<EB, MODE, PK>, P) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
+  const int C = cluster_route<EB, MODE, PK>(P.B, P.G, P.V);
+  if (C > 0) return launch_cluster<EB, MODE, PK>(P, C, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch
@@ -2474,6 +3069,21 @@ const char* spec_verify_strerror(int code) {
     case SV_ERR_STATIC_LIMIT: return "sizes need more scratch than the built-in 4 MiB array";
     default: return "unknown error code";
   }
+}
+
+int spec_verify_set_schedule(int schedule) {
+  if (schedule != SV_SCHEDULE_AUTO && schedule != SV_SCHEDULE_PERSISTENT) return SV_ERR_SCALAR;
+  return g_schedule.exchange(schedule);
+}
+
+int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy) {
+  const int rc = check_scalars(dtype, B, G, V);
+  if (rc) return rc;
+  if (dtype == SV_BF16)
+    return greedy ? cluster_route<2, MODE_GREEDY, false>(B, G, V)
+                  : cluster_route<2, MODE_SAMPLE, false>(B, G, V);
+  return greedy ? cluster_route<4, MODE_GREEDY, false>(B, G, V)
+                : cluster_route<4, MODE_SAMPLE, false>(B, G, V);
 }
 
 }  // extern "C"
