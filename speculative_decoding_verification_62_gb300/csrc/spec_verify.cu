@@ -2301,23 +2301,67 @@ __device__ __noinline__ void stage_r_unaligned(const char* p0, const char* p1, i
 // in block j of the item; blk[j] is the block's sum of round(w 2^39) over its
 // tokens, from the same per-token operations as draw_weight (a block's sum
 // therefore equals the prefix walk over it exactly).
-template <int EB, bool REJECT>
+template <int EB, bool REJECT, int NJ>
 __device__ __forceinline__ void r_item_blocks(const char* stage, int nvec, const ResidC& kc,
-                                              unsigned long long (&blk)[kBlk]) {
+                                              unsigned long long (&blk)[NJ]) {
   constexpr int VEC = 16 / EB;
   const int lane = threadIdx.x & 31;
+  if constexpr (EB == 2) {
+    // packed pairs: the operations of r_item_sum, one vector per block
+    const unsigned long long negmt = f2_pack(-kc.mt, -kc.mt), negmd = f2_pack(-kc.md, -kc.md);
+    const unsigned long long chi = f2_pack(kc.hi, kc.hi), clo = f2_pack(kc.lo, kc.lo);
+    const unsigned long long nrho = f2_pack(kc.nrho, kc.nrho), c16 = f2_pack(kc.c16, kc.c16);
+    const unsigned long long p23 = f2_pack(8388608.0f, 8388608.0f);
+    const unsigned long long n23 = f2_pack(-8388608.0f, -8388608.0f);
+    const unsigned long long mone = f2_pack(-1.0f, -1.0f), p16 = f2_pack(65536.0f, 65536.0f);
+    const unsigned long long c15 = f2_pack(12582912.0f, 12582912.0f);
 #pragma unroll
-  for (int j = 0; j < kBlk; ++j) {
-    const int vi = lane + 32 * j;
-    FixAcc a{0u, 0u, 0u};
-    if (vi < nvec) {
-      const uint4 t = lds128(stage + vi * 16);
-      const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+    for (int j = 0; j < NJ; ++j) {
+      const int vi = lane + 32 * j;
+      FixAcc a{0u, 0u, 0u};
+      if (vi < nvec) {
+        const uint4 t = lds128(stage + vi * 16);
+        const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
 #pragma unroll
-      for (int q = 0; q < VEC; ++q)
-        fix_add(a, draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc));
+        for (int q = 0; q < 4; ++q) {
+          const unsigned long long dt = f2_add(bf16x2_to_f2(vec_word(t, q)), negmt);
+          float x0, x1;
+          f2_unpack(f2_fma(dt, chi, f2_mul(dt, clo)), x0, x1);
+          unsigned long long v = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          if (REJECT) {
+            const unsigned long long dd = f2_add(bf16x2_to_f2(vec_word(d, q)), negmd);
+            f2_unpack(f2_fma(dd, chi, f2_mul(dd, clo)), x0, x1);
+            const unsigned long long ed = f2_pack(ex2_approx(x0), ex2_approx(x1));
+            f2_unpack(f2_fma(ed, nrho, v), x0, x1);
+            v = f2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f));
+          }
+          const unsigned long long y = f2_mul(v, c16);
+          const unsigned long long tt = f2_add(y, p23);
+          const unsigned long long dl = f2_fma(f2_add(tt, n23), mone, y);
+          const unsigned long long t2 = f2_fma(dl, p16, c15);
+          float u0, u1, w0, w1;
+          f2_unpack(tt, u0, u1);
+          f2_unpack(t2, w0, w1);
+          fix_add_parts(a, u0, w0);
+          fix_add_parts(a, u1, w1);
+        }
+      }
+      blk[j] = warp_sum_u64(fix_value(a));
     }
-    blk[j] = warp_sum_u64(fix_value(a));
+  } else {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int vi = lane + 32 * j;
+      FixAcc a{0u, 0u, 0u};
+      if (vi < nvec) {
+        const uint4 t = lds128(stage + vi * 16);
+        const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+#pragma unroll
+        for (int q = 0; q < VEC; ++q)
+          fix_add(a, draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc));
+      }
+      blk[j] = warp_sum_u64(fix_value(a));
+    }
   }
 }
 
@@ -2488,7 +2532,12 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   __syncthreads();
   // the leader's draft inputs are requested before its items
   DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
-  if (MODE == MODE_SAMPLE && leader && !greedy) gin = gather_drafts<EB>(P, A, gb);
+  float u_fin = 0.0f;  // the final draw's uniform (leader)
+  unsigned int uflags = 0;
+  if (MODE == MODE_SAMPLE && leader && !greedy) {
+    gin = gather_drafts<EB>(P, A, gb);
+    u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
+  }
 
   // ---- A items: i = gw, gw + CW, ...; row-major (target rows, then draft rows)
   unsigned int issued = 0, processed = 0;  // copies through this warp's buffers
@@ -2596,7 +2645,10 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   const ClusterDec cd = *cdec;
 
   if (cd.go) {
-    // ---- R items of the rejected position k: i = gw, gw + CW, ...
+    // ---- R items of the rejected position k: half an R chunk each (its
+    // vector columns 4 h .. 4 h + 3), i = gw, gw + CW, ...
+    constexpr int HE = RE / 2;           // logits per half item and row
+    constexpr int HJ = kBlk / 2;         // blocks per half item
     ResidC kc;
     kc.mt = cd.mt; kc.md = cd.md; kc.inv_st = cd.inv_st; kc.rho = cd.rho;
     resid_scales(kc);
@@ -2605,40 +2657,49 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
     const char* drow = P.draft + (A.d0 + (size_t)k) * (size_t)V * EB;
     const uint32_t blk_r = rank_addr(blk, 0);
-    for (unsigned int i = gw; i < (unsigned int)NCR && !failed; i += CW) {
-      const int s = (int)(issued % kNB);
-      const int n = min(RE, V - (int)i * RE);
-      const char* p0 = trow + (size_t)i * RE * EB;
-      const char* p1 = drow + (size_t)i * RE * EB;
-      char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
-      const bool direct = (((reinterpret_cast<uintptr_t>(p0) | reinterpret_cast<uintptr_t>(p1)) & 15) != 0) ||
-                          ((n * EB) & 15) != 0;
-      if (lane == 0) {
-        if (direct) {
-          mbar_arrive(&mybar[s]);
-        } else {
-          mbar_arrive_expect_tx(&mybar[s], (unsigned int)(2 * n * EB));
-          bulk_copy_g2s(stage, p0, (unsigned int)(n * EB), &mybar[s]);
-          bulk_copy_g2s(stage + kHalfBytes, p1, (unsigned int)(n * EB), &mybar[s]);
-        }
-      }
-      __syncwarp();
-      ++issued;
-      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
-        flags |= SV_STATUS_TIMEOUT;
-        failed = true;
-        ++processed;
-        break;
-      }
-      if (direct) stage_r_unaligned<EB>(p0, p1, n, stage);
-      unsigned long long bs[kBlk];
-      r_item_blocks<EB, true>(stage, (n + VEC - 1) / VEC, kc, bs);
+    for (unsigned int i = gw; i < 2u * (unsigned int)NCR && !failed; i += CW) {
+      const int e0 = (int)i * HE;  // first logit of the half item in its row
+      const int n = min(HE, V - e0);
+      unsigned long long bs[HJ];
+      if (n <= 0) {
 #pragma unroll
-      for (int j = 0; j < kBlk; ++j)
-        if (lane == j) st_cluster_u64(blk_r + (uint32_t)((i * kBlk + j) * sizeof(unsigned long long)), bs[j]);
-      if (direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int j = 0; j < HJ; ++j) bs[j] = 0ull;  // past the end of the row
+      } else {
+        const int s = (int)(issued % kNB);
+        const char* p0 = trow + (size_t)e0 * EB;
+        const char* p1 = drow + (size_t)e0 * EB;
+        char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
+        const bool direct = (((reinterpret_cast<uintptr_t>(p0) | reinterpret_cast<uintptr_t>(p1)) & 15) != 0) ||
+                            ((n * EB) & 15) != 0;
+        if (lane == 0) {
+          if (direct) {
+            mbar_arrive(&mybar[s]);
+          } else {
+            mbar_arrive_expect_tx(&mybar[s], (unsigned int)(2 * n * EB));
+            bulk_copy_g2s(stage, p0, (unsigned int)(n * EB), &mybar[s]);
+            bulk_copy_g2s(stage + kHalfBytes, p1, (unsigned int)(n * EB), &mybar[s]);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+          flags |= SV_STATUS_TIMEOUT;
+          failed = true;
+          ++processed;
+          break;
+        }
+        if (direct) stage_r_unaligned<EB>(p0, p1, n, stage);
+        r_item_blocks<EB, true, HJ>(stage, (n + VEC - 1) / VEC, kc, bs);
+        if (direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        ++processed;
+      }
+      // half h of chunk c holds the chunk's blocks 4 h .. 4 h + 3
+      const unsigned int first = (i / 2u) * kBlk + (i % 2u) * HJ;
+#pragma unroll
+      for (int j = 0; j < HJ; ++j)
+        if (lane == j) st_cluster_u64(blk_r + (first + (unsigned int)j) * (uint32_t)sizeof(unsigned long long), bs[j]);
       __syncwarp();
-      ++processed;
     }
     cluster_sync();  // every block sum is in the leader
 
@@ -2658,9 +2719,8 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
         __syncthreads();
       }
       if (warp == 0) {
-        unsigned int wf = 0;
-        const float u_s = sanitize_uniform(P.uniforms[A.uf], wf);
-        const int tok = cluster_walk<EB>(trow, kc.reject ? drow : nullptr, V, u_s, kc, blk, nblk, wf);
+        unsigned int wf = uflags;
+        const int tok = cluster_walk<EB>(trow, kc.reject ? drow : nullptr, V, u_fin, kc, blk, nblk, wf);
         if (lane == 0) {
           P.out_tokens[(size_t)b * (G + 1) + k] = tok;
           flags |= wf;
@@ -2723,14 +2783,16 @@ size_t cluster_tables(int G, int V, int eb) {
          sizeof(ClusterDec);
 }
 
-// Clusters of C CTAs that fit on this device at once (cached per device).
+// Clusters of C CTAs (C <= kClusterMax) that fit on this device at once
+// (cached per device).
+constexpr int kClusterMax = 16;
 template <int EB, int MODE, bool PK>
 int max_clusters(int C) {
-  static int cached_dev[2] = {-1, -1}, cached[2] = {0, 0};
-  const int slot = C > 8 ? 0 : 1;
+  static std::atomic<int> cached[kClusterMax + 1];  // (device + 1) << 16 | count; 0: none
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev == cached_dev[slot]) return cached[slot];
+  if (C < 1 || C > kClusterMax || cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int c0 = cached[C].load(std::memory_order_relaxed);
+  if ((c0 >> 16) == dev + 1) return c0 & 0xffff;
   auto kern = cluster_kernel<EB, MODE, PK>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmem) ==
@@ -2751,8 +2813,8 @@ int max_clusters(int C) {
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();  // a refused size only means that size is not used
-  cached_dev[slot] = dev;
-  cached[slot] = n;
+  n = n < 0 ? 0 : (n > 0xffff ? 0xffff : n);
+  cached[C].store(((dev + 1) << 16) | n, std::memory_order_relaxed);
   return n;
 }
 
@@ -2761,8 +2823,9 @@ template <int EB, int MODE, bool PK>
 int cluster_route(int B, int G, int V) {
   if (g_schedule.load() == SV_SCHEDULE_PERSISTENT) return 0;
   if (B < 1 || cluster_tables(G, V, EB) > (size_t)kClusterTables) return 0;
-  if (max_clusters<EB, MODE, PK>(16) >= B) return 16;
-  if (max_clusters<EB, MODE, PK>(8) >= B) return 8;
+  // the largest cluster of which B fit at once (one wave: a request per cluster)
+  for (int C = kClusterMax; C >= 8; --C)
+    if (max_clusters<EB, MODE, PK>(C) >= B) return C;
   return 0;
 }
 
