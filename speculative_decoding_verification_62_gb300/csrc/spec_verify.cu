@@ -954,13 +954,13 @@ __device__ __forceinline__ DraftIn gather_drafts(const Params& P, const ReqAddr&
   return g;
 }
 
-// The acceptance tests of request b from its row statistics: writes
-// out_tokens (all but position k), num_accepted, p/q and status, and returns
-// k on every lane with the decision on lane 0.
+// The acceptance tests of request b from its row statistics: returns k on
+// every lane with the decision on lane 0 and, when emit is set, writes
+// out_tokens (all but position k), num_accepted, p/q and status.
 template <int EB, bool PK, class Parts>
 __device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, int b, int gb,
                                            TempC tc, float* rs, const ReqAddr& A,
-                                           const DraftIn& g, Decision& d) {
+                                           const DraftIn& g, Decision& d, bool emit = true) {
   const int G = P.G;
   const int lane = threadIdx.x & 31;
   const int i = lane;
@@ -1001,15 +1001,15 @@ __device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, 
       accept = u < ratio;
     }
     reject = !accept;
-    if (P.p_tok || P.q_tok) {
+    if (emit && (P.p_tok || P.q_tok)) {
       p = (zt > -INFINITY) ? prob_f64(et, st) : 0.0;
       q = (zd > -INFINITY) ? prob_f64(ed, sd) : 0.0;
     }
   }
   const unsigned int rej = __ballot_sync(0xffffffffu, reject);
   const int k = rej ? (__ffs(rej) - 1) : gb;
-  if (i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
-  if (i < (PK ? gb : G)) {  // packed p/q hold this request's gb entries only
+  if (emit && i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
+  if (emit && i < (PK ? gb : G)) {  // packed p/q hold this request's gb entries only
     const bool evaluated = i < gb && i <= k;
     if (P.p_tok) P.p_tok[A.d0 + i] = evaluated ? p : NAN;
     if (P.q_tok) P.q_tok[A.d0 + i] = evaluated ? q : NAN;
@@ -1018,7 +1018,7 @@ __device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, 
   if (lane == 0) {
     const int kd = gb + 1 + (k < gb ? k : 0);
     const FF st_k{rs[64 + k], rs[128 + k]}, sd_k{rs[64 + kd], rs[128 + kd]};
-    if (P.num_accepted) P.num_accepted[b] = k;
+    if (emit && P.num_accepted) P.num_accepted[b] = k;
     d.k = k;
     d.reject = k < gb ? 1 : 0;
     d.mt = rs[k];
@@ -1027,7 +1027,7 @@ __device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, 
     d.rho = d.reject ? ff_div(st_k, sd_k) : 0.0f;
     d.c_hi = tc.hi;
     d.c_lo = tc.lo;
-    if (any) atomicOr(P.status, any);
+    if (emit && any) atomicOr(P.status, any);
   }
   return k;
 }
@@ -2217,12 +2217,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
 // global-memory synchronisations (arrival counters, decision records, queue
 // polls), each an L2 round trip.  Here request b gets cluster b of C CTAs,
 // one per SM.  Every warp streams a fixed share of the request's A items and
-// stores each partial into the leader CTA's (rank 0) shared memory; a
-// cluster barrier replaces the arrival counter; the leader's warp 0 decides
-// from its own shared memory (the same arithmetic as the persistent path)
-// and copies the decision into every CTA.  After a reject, the R items store
-// per-block fixed-point sums in the leader, and the leader walks one block of
-// 256 (bf16) or 128 (float32) tokens.
+// stores each partial into the shared memory of every CTA of the cluster; a
+// cluster barrier replaces the arrival counter; each CTA's warp 0 then
+// computes the decision from its own copy (the arithmetic of the persistent
+// path; the leader, rank 0, writes the outputs).  After a reject, the R items
+// store per-block fixed-point sums in the leader, and after a second barrier
+// the leader walks one block of 256 (bf16) or 128 (float32) tokens.
 constexpr int kBlk = 8;                          // blocks per R item: one per vector column
 constexpr int kClusterTables = 32 * 1024;        // leader tables: partials, block sums, decision
 constexpr size_t kClusterSmem = (size_t)kWarps * kNB * kItemBytes + kClusterTables;
@@ -2232,7 +2232,6 @@ struct ClusterDec {  // the decision, as every CTA of the cluster holds it
   int k, go;         // go: 1 when R items follow (a rejected draft)
   float mt, md, inv_st, rho, c_hi, c_lo;
 };
-constexpr int kDecWords = (int)(sizeof(ClusterDec) / 4);
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -2266,9 +2265,6 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t a, float2 v) {
 }
 __device__ __forceinline__ void st_cluster_u64(uint32_t a, unsigned long long v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 // Both halves of an R item whose bytes cannot be bulk-copied, loaded with
@@ -2397,11 +2393,12 @@ __device__ __noinline__ int cluster_walk(const char* trow, const char* drow, int
   constexpr int VEC = 16 / EB;
   constexpr int RE = kHalfBytes / EB;
   const int lane = threadIdx.x & 31;
-  // 1. the block: lane l owns blocks [b0, b1)
+  // 1. the block: lane l owns blocks [b0, b1); then the blocks of the lane
+  //    holding floor(u S) are scanned 32 at a time
   const int bpl = (nblk + 31) >> 5;
   const int b0 = min(nblk, lane * bpl), b1 = min(nblk, b0 + bpl);
   unsigned long long own = 0;
-#pragma unroll 1
+#pragma unroll 4
   for (int bl = b0; bl < b1; ++bl) own += blk[bl];
   const unsigned long long incl = warp_incl_scan_u64(own);
   const unsigned long long S = __shfl_sync(0xffffffffu, incl, 31);
@@ -2413,20 +2410,24 @@ __device__ __noinline__ int cluster_walk(const char* trow, const char* drow, int
     const unsigned int hit = __ballot_sync(0xffffffffu, excl <= target && target < incl);
     if (hit) {
       const int l = __ffs(hit) - 1;
-      if (lane == l) {
-        unsigned long long run = excl;
+      const int lo = __shfl_sync(0xffffffffu, b0, l), hi = __shfl_sync(0xffffffffu, b1, l);
+      base = __shfl_sync(0xffffffffu, excl, l);
 #pragma unroll 1
-        for (int bl = b0; bl < b1; ++bl) {
-          if (run + blk[bl] > target) {
-            bs = bl;
-            break;
-          }
-          run += blk[bl];
+      for (int g0 = lo; g0 < hi && bs < 0; g0 += 32) {
+        const int bl = g0 + lane;
+        const unsigned long long v = bl < hi ? blk[bl] : 0ull;
+        const unsigned long long vi = warp_incl_scan_u64(v);
+        const unsigned long long ve = vi - v;
+        const unsigned int h2 =
+            __ballot_sync(0xffffffffu, bl < hi && base + ve <= target && target < base + vi);
+        if (h2) {
+          const int l2 = __ffs(h2) - 1;
+          bs = g0 + l2;
+          base += __shfl_sync(0xffffffffu, ve, l2);
+        } else {
+          base += __shfl_sync(0xffffffffu, vi, 31);
         }
-        base = run;
       }
-      bs = __shfl_sync(0xffffffffu, bs, l);
-      base = __shfl_sync(0xffffffffu, base, l);
     }
   }
   if (bs < 0) {
@@ -2522,7 +2523,6 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   const int rows = greedy ? gb + 1 : 2 * gb + 1;
   const unsigned int nA = (unsigned int)rows * (unsigned int)NC;
   const unsigned int CW = C * kWarps, gw = rank * kWarps + (unsigned int)warp;
-  const bool leader = rank == 0 && warp == 0;
 
   if (tid == 0) {
     for (int w = 0; w < kWarps; ++w)
@@ -2534,9 +2534,9 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
   float u_fin = 0.0f;  // the final draw's uniform (leader)
   unsigned int uflags = 0;
-  if (MODE == MODE_SAMPLE && leader && !greedy) {
+  if (MODE == MODE_SAMPLE && warp == 0 && !greedy) {  // every CTA decides
     gin = gather_drafts<EB>(P, A, gb);
-    u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
+    if (rank == 0) u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
   }
 
   // ---- A items: i = gw, gw + CW, ...; row-major (target rows, then draft rows)
@@ -2571,7 +2571,8 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     ++issued;
   };
   {
-    const uint32_t part_r = rank_addr(part, 0);
+    // lane r < C stores each partial into CTA r: every CTA decides locally
+    const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
     unsigned int next = gw;
     for (int s = 0; s < kNB && next < nA; ++s, next += CW) {
       Meta m;
@@ -2590,7 +2591,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
         const bool sample = MODE == MODE_SAMPLE && !greedy;
         if (sample && m.direct) stage_unaligned<EB>(m, stage);
         const float2 pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
-        if (lane == 0)
+        if ((uint32_t)lane < C)
           st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
         if (sample && m.direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
@@ -2604,10 +2605,13 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
       }
     }
   }
-  cluster_sync();  // every partial is in the leader
+  cluster_sync();  // every CTA holds every partial
 
-  // ---- the decision (leader warp 0), copied into every CTA of the cluster
-  if (leader) {
+  // ---- the decision: the leader's warp 0 writes the outputs; in sampling
+  // mode every other CTA's warp 0 computes the same decision from its own
+  // copy of the partials (identical data, identical arithmetic)
+  if (greedy && rank != 0) return;  // greedy: no further cluster work
+  if (warp == 0) {
     float* rs = reinterpret_cast<float*>(mybuf);  // this warp's buffers are idle now
     const SharedParts sp{part, NC};
     ClusterDec cd;
@@ -2623,25 +2627,22 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
       d.k = 0;
       d.reject = 0;
       d.mt = d.md = d.inv_st = d.rho = 0.0f;
-      const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d);
+      const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d, rank == 0);
       cd.k = k;
       cd.go = __shfl_sync(0xffffffffu, d.reject, 0);
       cd.mt = __shfl_sync(0xffffffffu, d.mt, 0);
       cd.md = __shfl_sync(0xffffffffu, d.md, 0);
       cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
       cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
-      if (k == gb) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
+      if (k == gb && rank == 0)
+        final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
     }
-    // lane r < C copies the decision into CTA r
-    if ((uint32_t)lane < C) {
-      const uint32_t dst = rank_addr(cdec, (uint32_t)lane);
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(&cd);
-#pragma unroll
-      for (int w = 0; w < kDecWords; ++w) st_cluster_u32(dst + 4u * (uint32_t)w, src[w]);
+    if (lane == 0) {
+      *cdec = cd;
+      if (rank == 0 && rflags) atomicOr(P.status, rflags);
     }
-    if (lane == 0 && rflags) atomicOr(P.status, rflags);
   }
-  cluster_sync();  // every CTA holds the decision
+  __syncthreads();  // the CTA's warps see its decision
   const ClusterDec cd = *cdec;
 
   if (cd.go) {
@@ -2707,6 +2708,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     if (rank == 0) {
       const int nblk = NCR * kBlk;
       unsigned long long S = 0;
+#pragma unroll 4
       for (int bl = lane; bl < nblk; bl += 32) S += blk[bl];
       S = warp_sum_u64(S);
       if (S == 0ull) {
