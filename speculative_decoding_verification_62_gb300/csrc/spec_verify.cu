@@ -2223,10 +2223,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
 // path; the leader, rank 0, writes the outputs).  After a reject, the R items
 // store per-block fixed-point sums in the leader, and after a second barrier
 // the leader walks one block of 256 (bf16) or 128 (float32) tokens.
+constexpr int kClusterMax = 16;                  // CTAs per cluster, at most
 constexpr int kBlk = 8;                          // blocks per R item: one per vector column
-constexpr int kClusterTables = 32 * 1024;        // leader tables: partials, block sums, decision
+constexpr int kClusterTables = 24 * 1024;        // partials, fallback block sums, decision
 constexpr size_t kClusterSmem = (size_t)kWarps * kNB * kItemBytes + kClusterTables;
-static_assert(kClusterSmem <= 227 * 1024, "cluster shared memory budget");
+// about 5 KB of static shared memory (barriers, item records, unit block sums)
+static_assert(kClusterSmem + 6 * 1024 <= 227 * 1024, "cluster shared memory budget");
 
 struct ClusterDec {  // the decision, as every CTA of the cluster holds it
   int k, go;         // go: 1 when R items follow (a rejected draft)
@@ -2267,43 +2269,40 @@ __device__ __forceinline__ void st_cluster_u64(uint32_t a, unsigned long long v)
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
-// Both halves of an R item whose bytes cannot be bulk-copied, loaded with
-// plain loads and padded with -inf to whole vectors (a -inf logit has weight
-// exactly 0 in both the residual and the bonus formula).
-template <int EB>
-__device__ __noinline__ void stage_r_unaligned(const char* p0, const char* p1, int n, char* stage) {
-  constexpr int VEC = 16 / EB;
+// Residual draw weights of a resident unit (a target chunk and the draft
+// chunk of the same position, each AE logits in its own staging buffer),
+// summed per block of 32 vectors: blk[j] is block j0 + j, whose vector l + 32
+// (j0 + j) lane l reads, as round(w 2^39) with the per-token operations of
+// draw_weight (a block's sum therefore equals the prefix walk over it).
+// Four per-lane values reduced over the warp at once: after the exchanges
+// with lanes 16 and 8 apart each lane holds partial sums of one value (the
+// value index is lane bits 4..3), then three butterfly steps finish them.
+// Returns value (lane >> 3) & 3 on every lane.
+__device__ __forceinline__ unsigned long long warp_sum4_u64(const unsigned long long (&v)[4]) {
   const int lane = threadIdx.x & 31;
-  const int ne = (n + VEC - 1) / VEC * VEC;
-  for (int e = lane; e < ne; e += 32) {
-    if constexpr (EB == 2) {
-      const unsigned short ninf = 0xff80u;
-      reinterpret_cast<unsigned short*>(stage)[e] =
-          e < n ? __ldg(reinterpret_cast<const unsigned short*>(p0) + e) : ninf;
-      reinterpret_cast<unsigned short*>(stage + kHalfBytes)[e] =
-          (p1 && e < n) ? __ldg(reinterpret_cast<const unsigned short*>(p1) + e) : ninf;
-    } else {
-      const unsigned int ninf = 0xff800000u;
-      reinterpret_cast<unsigned int*>(stage)[e] =
-          e < n ? __ldg(reinterpret_cast<const unsigned int*>(p0) + e) : ninf;
-      reinterpret_cast<unsigned int*>(stage + kHalfBytes)[e] =
-          (p1 && e < n) ? __ldg(reinterpret_cast<const unsigned int*>(p1) + e) : ninf;
-    }
-  }
-  __syncwarp();
+  const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+  // step 1: lanes 0-15 keep values 0, 1; lanes 16-31 keep values 2, 3
+  unsigned long long a0 = hi16 ? v[2] : v[0], a1 = hi16 ? v[3] : v[1];
+  const unsigned long long s0 = hi16 ? v[0] : v[2], s1 = hi16 ? v[1] : v[3];
+  a0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  a1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  // step 2: within each half, lanes with bit 3 clear keep the first value
+  unsigned long long a = hi8 ? a1 : a0;
+  a += __shfl_xor_sync(0xffffffffu, hi8 ? a0 : a1, 8);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+  return a;
 }
 
-// R item on the cluster path: lane l's vector j (vector index l + 32 j) lies
-// in block j of the item; blk[j] is the block's sum of round(w 2^39) over its
-// tokens, from the same per-token operations as draw_weight (a block's sum
-// therefore equals the prefix walk over it exactly).
-template <int EB, bool REJECT, int NJ>
-__device__ __forceinline__ void r_item_blocks(const char* stage, int nvec, const ResidC& kc,
-                                              unsigned long long (&blk)[NJ]) {
+template <int EB, int NJ>
+__device__ __forceinline__ void unit_blocks(const char* tb, const char* db, int nvec, int j0,
+                                            const ResidC& kc, unsigned long long (&blk)[NJ]) {
+  static_assert(NJ == 4, "blocks are reduced four at a time");
   constexpr int VEC = 16 / EB;
   const int lane = threadIdx.x & 31;
+  unsigned long long own[NJ];
   if constexpr (EB == 2) {
-    // packed pairs: the operations of r_item_sum, one vector per block
+    // packed pairs: the operations of r_item_sum
     const unsigned long long negmt = f2_pack(-kc.mt, -kc.mt), negmd = f2_pack(-kc.md, -kc.md);
     const unsigned long long chi = f2_pack(kc.hi, kc.hi), clo = f2_pack(kc.lo, kc.lo);
     const unsigned long long nrho = f2_pack(kc.nrho, kc.nrho), c16 = f2_pack(kc.c16, kc.c16);
@@ -2313,24 +2312,22 @@ __device__ __forceinline__ void r_item_blocks(const char* stage, int nvec, const
     const unsigned long long c15 = f2_pack(12582912.0f, 12582912.0f);
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const int vi = lane + 32 * j;
+      const int vi = lane + 32 * (j0 + j);
       FixAcc a{0u, 0u, 0u};
       if (vi < nvec) {
-        const uint4 t = lds128(stage + vi * 16);
-        const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+        const uint4 t = lds128(tb + vi * 16);
+        const uint4 d = lds128(db + vi * 16);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const unsigned long long dt = f2_add(bf16x2_to_f2(vec_word(t, q)), negmt);
           float x0, x1;
           f2_unpack(f2_fma(dt, chi, f2_mul(dt, clo)), x0, x1);
-          unsigned long long v = f2_pack(ex2_approx(x0), ex2_approx(x1));
-          if (REJECT) {
-            const unsigned long long dd = f2_add(bf16x2_to_f2(vec_word(d, q)), negmd);
-            f2_unpack(f2_fma(dd, chi, f2_mul(dd, clo)), x0, x1);
-            const unsigned long long ed = f2_pack(ex2_approx(x0), ex2_approx(x1));
-            f2_unpack(f2_fma(ed, nrho, v), x0, x1);
-            v = f2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f));
-          }
+          const unsigned long long v0 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          const unsigned long long dd = f2_add(bf16x2_to_f2(vec_word(d, q)), negmd);
+          f2_unpack(f2_fma(dd, chi, f2_mul(dd, clo)), x0, x1);
+          const unsigned long long ed = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          f2_unpack(f2_fma(ed, nrho, v0), x0, x1);
+          const unsigned long long v = f2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f));
           const unsigned long long y = f2_mul(v, c16);
           const unsigned long long tt = f2_add(y, p23);
           const unsigned long long dl = f2_fma(f2_add(tt, n23), mone, y);
@@ -2342,23 +2339,26 @@ __device__ __forceinline__ void r_item_blocks(const char* stage, int nvec, const
           fix_add_parts(a, u1, w1);
         }
       }
-      blk[j] = warp_sum_u64(fix_value(a));
+      own[j] = fix_value(a);
     }
   } else {
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const int vi = lane + 32 * j;
+      const int vi = lane + 32 * (j0 + j);
       FixAcc a{0u, 0u, 0u};
       if (vi < nvec) {
-        const uint4 t = lds128(stage + vi * 16);
-        const uint4 d = REJECT ? lds128(stage + kHalfBytes + vi * 16) : t;
+        const uint4 t = lds128(tb + vi * 16);
+        const uint4 d = lds128(db + vi * 16);
 #pragma unroll
         for (int q = 0; q < VEC; ++q)
-          fix_add(a, draw_x<REJECT>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc));
+          fix_add(a, draw_x<true>(vec_elem<EB>(t, q), vec_elem<EB>(d, q), kc));
       }
-      blk[j] = warp_sum_u64(fix_value(a));
+      own[j] = fix_value(a);
     }
   }
+  const unsigned long long r = warp_sum4_u64(own);
+#pragma unroll
+  for (int q = 0; q < NJ; ++q) blk[q] = __shfl_sync(0xffffffffu, r, 8 * q);
 }
 
 // Block sums of the draw weights of target row k alone (kc.reject == 0), for
@@ -2480,16 +2480,27 @@ __device__ __noinline__ int cluster_walk(const char* trow, const char* drow, int
   return __shfl_sync(0xffffffffu, tok, __ffs(holder) - 1);
 }
 
-// One request per cluster.  Shared memory: the warps' staging buffers, then
-// (the same layout in every CTA, used in the leader) the partials
-// [2G+1][NC], the block sums [NCR][kBlk] and the decision.
+// One request per cluster, each warp at most one unit of the request's A
+// work: unit u = c (gamma_b + 1) + i is chunk c of target row i and, for a
+// sampling position i < gamma_b, chunk c of draft row i (kept in the warp's
+// two staging buffers to the end).  Shared memory: the buffers, then (the
+// same layout in every CTA) the partials [2G+1][NC], the leader's block sums
+// for the vanished-residual fallback [NCR][kBlk], the block sums of this
+// CTA's residual units [kWarps][kUnitBlk], the CTAs' residual totals [C] and
+// the decision.
+constexpr int kUnitBlk = 2 * kBlk;  // blocks per unit (an A chunk is two R chunks)
+
 template <int EB, int MODE, bool PK>
 __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ __align__(8) uint64_t bar[kWarps][kNB];
   __shared__ Meta cmeta[kWarps][kNB];  // the item in each buffer
+  __shared__ unsigned long long ublk[kWarps][kUnitBlk];
+  __shared__ unsigned long long tot[kClusterMax];
+  __shared__ unsigned long long cta_sum;  // this CTA's residual total
+  __shared__ int sh_pick;
+  __shared__ float rsbuf[192];  // the decision's row statistics
   constexpr int AE = kItemBytes / EB;   // logits per A item
-  constexpr int RE = kHalfBytes / EB;   // logits per R item and row
   constexpr int VEC = 16 / EB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank(), C = cluster_size();
@@ -2520,89 +2531,80 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     if (T == 0.0f) greedy = true;  // this request takes the greedy steps
     else tc = temp_consts(sanitize_temperature(T, rflags));
   }
-  const int rows = greedy ? gb + 1 : 2 * gb + 1;
-  const unsigned int nA = (unsigned int)rows * (unsigned int)NC;
-  const unsigned int CW = C * kWarps, gw = rank * kWarps + (unsigned int)warp;
+  const bool sample = MODE == MODE_SAMPLE && !greedy;
+  const int per = gb + 1;  // units per chunk
+  const unsigned int nU = (unsigned int)per * (unsigned int)NC;
+  const unsigned int gw = rank * kWarps + (unsigned int)warp;
+  // this CTA's units are rank kWarps + w (one per warp; the host checks
+  // (G + 1) NC <= C kWarps)
+  auto unit_row = [&](unsigned int u) { return (int)(u % (unsigned int)per); };
+  auto unit_chunk = [&](unsigned int u) { return (int)(u / (unsigned int)per); };
 
   if (tid == 0) {
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kNB; ++s) mbar_init(&bar[w][s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    cta_sum = 0ull;
   }
   __syncthreads();
-  // the leader's draft inputs are requested before its items
+  // every CTA decides: its warp 0 requests the draft inputs and the final
+  // draw's uniform before its items
   DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
-  float u_fin = 0.0f;  // the final draw's uniform (leader)
+  float u_fin = 0.0f;
   unsigned int uflags = 0;
-  if (MODE == MODE_SAMPLE && warp == 0 && !greedy) {  // every CTA decides
+  if (sample && warp == 0) {
     gin = gather_drafts<EB>(P, A, gb);
-    if (rank == 0) u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
+    u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
   }
 
-  // ---- A items: i = gw, gw + CW, ...; row-major (target rows, then draft rows)
-  unsigned int issued = 0, processed = 0;  // copies through this warp's buffers
+  // ---- A items of this warp's unit: the target chunk into buffer 0, the
+  // draft chunk (sampling, position below gamma_b) into buffer 1
+  unsigned int issued = 0;
   bool failed = false;
-  auto a_meta = [&](unsigned int i, Meta& m) {
-    const int r = (int)(i / (unsigned int)NC), c = (int)(i % (unsigned int)NC);
-    const bool trg = r <= gb;
-    m.kind = KIND_A;
-    m.pslot = trg ? r : G + 1 + (r - gb - 1);
-    m.c = c;
-    m.n = min(AE, V - c * AE);
-    const size_t row = trg ? A.t0 + (size_t)r : A.d0 + (size_t)(r - gb - 1);
-    m.p0 = (trg ? P.target : P.draft) + (row * (size_t)V + (size_t)c * AE) * EB;
-    m.p1 = nullptr;
-    m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-    m.c_hi = tc.hi;
-    m.c_lo = tc.lo;
-  };
-  auto a_issue = [&](const Meta& m) {
-    const int s = (int)(issued % kNB);
-    if (lane == 0) {
-      mymeta[s] = m;
-      if (m.direct) {
-        mbar_arrive(&mybar[s]);
-      } else {
-        mbar_arrive_expect_tx(&mybar[s], (unsigned int)(m.n * EB));
-        bulk_copy_g2s(mybuf + s * kItemBytes, m.p0, (unsigned int)(m.n * EB), &mybar[s]);
+  const bool has = gw < nU;
+  const int ui = has ? unit_row(gw) : 0, uc = has ? unit_chunk(gw) : 0;
+  const bool pair = sample && has && ui < gb;
+  const int un = min(AE, V - uc * AE);  // logits in the unit's chunk
+  if (has) {
+    for (int h = 0; h < (pair ? 2 : 1); ++h) {
+      Meta m;
+      m.kind = KIND_A;
+      m.pslot = h ? G + 1 + ui : ui;
+      m.c = uc;
+      m.n = un;
+      const size_t row = h ? A.d0 + (size_t)ui : A.t0 + (size_t)ui;
+      m.p0 = (h ? P.draft : P.target) + (row * (size_t)V + (size_t)uc * AE) * EB;
+      m.p1 = nullptr;
+      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.c_hi = tc.hi;
+      m.c_lo = tc.lo;
+      if (lane == 0) {
+        mymeta[h] = m;
+        if (m.direct) {
+          mbar_arrive(&mybar[h]);
+        } else {
+          mbar_arrive_expect_tx(&mybar[h], (unsigned int)(m.n * EB));
+          bulk_copy_g2s(mybuf + h * kItemBytes, m.p0, (unsigned int)(m.n * EB), &mybar[h]);
+        }
       }
+      ++issued;
     }
     __syncwarp();
-    ++issued;
-  };
-  {
     // lane r < C stores each partial into CTA r: every CTA decides locally
     const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
-    unsigned int next = gw;
-    for (int s = 0; s < kNB && next < nA; ++s, next += CW) {
-      Meta m;
-      a_meta(next, m);
-      a_issue(m);
-    }
-    // every issued copy is waited for once (bounded), also after a timeout
-    while (processed != issued) {
-      const int s = (int)(processed % kNB);
-      const Meta& m = mymeta[s];
-      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+    for (unsigned int h = 0; h < issued; ++h) {  // every copy is waited for (bounded)
+      const Meta& m = mymeta[h];
+      if (!mbar_wait(&mybar[h], 0u)) {
         flags |= SV_STATUS_TIMEOUT;
         failed = true;
       } else if (!failed) {
-        char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
-        const bool sample = MODE == MODE_SAMPLE && !greedy;
+        char* stage = reinterpret_cast<char*>(mybuf + h * kItemBytes);
         if (sample && m.direct) stage_unaligned<EB>(m, stage);
         const float2 pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         if ((uint32_t)lane < C)
           st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
-        if (sample && m.direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       __syncwarp();
-      ++processed;
-      if (!failed && next < nA) {
-        Meta m2;
-        a_meta(next, m2);
-        a_issue(m2);
-        next += CW;
-      }
     }
   }
   cluster_sync();  // every CTA holds every partial
@@ -2612,7 +2614,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   // copy of the partials (identical data, identical arithmetic)
   if (greedy && rank != 0) return;  // greedy: no further cluster work
   if (warp == 0) {
-    float* rs = reinterpret_cast<float*>(mybuf);  // this warp's buffers are idle now
+    float* rs = rsbuf;
     const SharedParts sp{part, NC};
     ClusterDec cd;
     cd.k = 0;
@@ -2634,8 +2636,9 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
       cd.md = __shfl_sync(0xffffffffu, d.md, 0);
       cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
       cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
-      if (k == gb && rank == 0)
-        final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], reinterpret_cast<unsigned char*>(rs));
+      // every draft accepted: no residual pass follows, so this warp's
+      // buffers are free for the bonus draw's staging
+      if (k == gb && rank == 0) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], mybuf);
     }
     if (lane == 0) {
       *cdec = cd;
@@ -2646,88 +2649,140 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   const ClusterDec cd = *cdec;
 
   if (cd.go) {
-    // ---- R items of the rejected position k: half an R chunk each (its
-    // vector columns 4 h .. 4 h + 3), i = gw, gw + CW, ...
-    constexpr int HE = RE / 2;           // logits per half item and row
-    constexpr int HJ = kBlk / 2;         // blocks per half item
+    // ---- residual block sums of the rejected position k, from the resident
+    // units of row k in this CTA; four warps share a unit
     ResidC kc;
     kc.mt = cd.mt; kc.md = cd.md; kc.inv_st = cd.inv_st; kc.rho = cd.rho;
     resid_scales(kc);
     kc.hi = cd.c_hi; kc.lo = cd.c_lo; kc.reject = 1;
     const int k = cd.k < 0 ? 0 : (cd.k > G ? G : cd.k);
-    const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
-    const char* drow = P.draft + (A.d0 + (size_t)k) * (size_t)V * EB;
-    const uint32_t blk_r = rank_addr(blk, 0);
-    for (unsigned int i = gw; i < 2u * (unsigned int)NCR && !failed; i += CW) {
-      const int e0 = (int)i * HE;  // first logit of the half item in its row
-      const int n = min(HE, V - e0);
-      unsigned long long bs[HJ];
-      if (n <= 0) {
+    constexpr int kGroup = 4;                     // blocks per task
+    constexpr int kTasks = kUnitBlk / kGroup;     // tasks per unit
+    // the CTA's units of row k: warp w holds unit rank kWarps + w, so they
+    // sit at warps w0, w0 + per, ... (ku(m) below)
+    const int w0 = (int)(((unsigned int)k + (unsigned int)per - (rank * kWarps) % (unsigned int)per) %
+                         (unsigned int)per);
+    int nk = 0;
+    for (int w = w0; w < kWarps && rank * kWarps + (unsigned int)w < nU; w += per) ++nk;
+    auto ku = [&](int m) { return w0 + m * per; };
+    for (int t = warp; t < nk * kTasks && !failed; t += kWarps) {
+      const int w = ku(t / kTasks), g = t % kTasks;
+      const unsigned int u = rank * kWarps + (unsigned int)w;
+      const int n = min(AE, V - unit_chunk(u) * AE);
+      const unsigned char* wb = dsmem + (size_t)w * kNB * kItemBytes;
+      unsigned long long bs[kGroup];
+      unit_blocks<EB, kGroup>(reinterpret_cast<const char*>(wb),
+                              reinterpret_cast<const char*>(wb + kItemBytes), (n + VEC - 1) / VEC,
+                              g * kGroup, kc, bs);
 #pragma unroll
-        for (int j = 0; j < HJ; ++j) bs[j] = 0ull;  // past the end of the row
-      } else {
-        const int s = (int)(issued % kNB);
-        const char* p0 = trow + (size_t)e0 * EB;
-        const char* p1 = drow + (size_t)e0 * EB;
-        char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
-        const bool direct = (((reinterpret_cast<uintptr_t>(p0) | reinterpret_cast<uintptr_t>(p1)) & 15) != 0) ||
-                            ((n * EB) & 15) != 0;
-        if (lane == 0) {
-          if (direct) {
-            mbar_arrive(&mybar[s]);
-          } else {
-            mbar_arrive_expect_tx(&mybar[s], (unsigned int)(2 * n * EB));
-            bulk_copy_g2s(stage, p0, (unsigned int)(n * EB), &mybar[s]);
-            bulk_copy_g2s(stage + kHalfBytes, p1, (unsigned int)(n * EB), &mybar[s]);
-          }
-        }
-        __syncwarp();
-        ++issued;
-        if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
-          flags |= SV_STATUS_TIMEOUT;
-          failed = true;
-          ++processed;
-          break;
-        }
-        if (direct) stage_r_unaligned<EB>(p0, p1, n, stage);
-        r_item_blocks<EB, true, HJ>(stage, (n + VEC - 1) / VEC, kc, bs);
-        if (direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        ++processed;
-      }
-      // half h of chunk c holds the chunk's blocks 4 h .. 4 h + 3
-      const unsigned int first = (i / 2u) * kBlk + (i % 2u) * HJ;
-#pragma unroll
-      for (int j = 0; j < HJ; ++j)
-        if (lane == j) st_cluster_u64(blk_r + (first + (unsigned int)j) * (uint32_t)sizeof(unsigned long long), bs[j]);
-      __syncwarp();
+      for (int j = 0; j < kGroup; ++j)
+        if (lane == j) ublk[w][g * kGroup + j] = bs[j];
+      if (lane == 0) atomicAdd(&cta_sum, bs[0] + bs[1] + bs[2] + bs[3]);
     }
-    cluster_sync();  // every block sum is in the leader
+    __syncthreads();
+    // this CTA's residual total into every CTA
+    if (warp == 0 && (uint32_t)lane < C) st_cluster_u64(rank_addr(&tot[rank], (uint32_t)lane), cta_sum);
+    cluster_sync();  // every CTA holds every CTA's total
 
-    // ---- the final draw (leader CTA)
-    if (rank == 0) {
-      const int nblk = NCR * kBlk;
-      unsigned long long S = 0;
-#pragma unroll 4
-      for (int bl = lane; bl < nblk; bl += 32) S += blk[bl];
-      S = warp_sum_u64(S);
-      if (S == 0ull) {
-        // The residual vanished in fixed point (p_k and q_k agree within its
-        // resolution): draw from p_k instead, its block sums computed by the
-        // whole leader CTA.
-        kc.reject = 0;
-        __syncthreads();
-        p_blocks<EB>(trow, V, kc, nblk, blk);
-        __syncthreads();
+    // ---- the final draw.  Units ascend with rank, so the CTAs' totals in
+    // rank order are consecutive pieces of row k's residual CDF: the CTA whose
+    // piece holds floor(u S) walks its own resident block.
+    unsigned long long S = 0, before = 0;
+    if (warp == 0) {
+      const unsigned long long v = (uint32_t)lane < C ? tot[lane] : 0ull;
+      const unsigned long long incl = warp_incl_scan_u64(v);
+      S = __shfl_sync(0xffffffffu, incl, 31);
+      int pick = -1;
+      if (S != 0ull) {
+        float uf = u_fin;
+        const unsigned long long target = scaled_target(uf, S);
+        const unsigned int hit = __ballot_sync(0xffffffffu, (uint32_t)lane < C && incl - v <= target &&
+                                                            target < incl);
+        pick = hit ? __ffs(hit) - 1 : -2;
+        if (pick >= 0) before = __shfl_sync(0xffffffffu, incl - v, pick);
       }
+      if (lane == 0) sh_pick = pick;
+    }
+    __syncthreads();
+    const int pick = sh_pick;  // -1: the residual vanished; -2: internal error
+    if (pick == -1 && rank == 0) {
+      // The residual vanished in fixed point (p_k and q_k agree within its
+      // resolution): draw from p_k instead, its block sums computed by the
+      // whole leader CTA from global memory.
+      kc.reject = 0;
+      const int nblk = NCR * kBlk;
+      const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
+      p_blocks<EB>(trow, V, kc, nblk, blk);
+      __syncthreads();
       if (warp == 0) {
         unsigned int wf = uflags;
-        const int tok = cluster_walk<EB>(trow, kc.reject ? drow : nullptr, V, u_fin, kc, blk, nblk, wf);
+        const int tok = cluster_walk<EB>(trow, nullptr, V, u_fin, kc, blk, nblk, wf);
         if (lane == 0) {
           P.out_tokens[(size_t)b * (G + 1) + k] = tok;
           flags |= wf;
         }
       }
+    } else if (pick == -2 && rank == 0 && warp == 0) {
+      flags |= SV_STATUS_INTERNAL;
+      if (lane == 0) P.out_tokens[(size_t)b * (G + 1) + k] = V - 1;
+    } else if (pick == (int)rank && warp == 0) {
+      // the block: this CTA's units of row k in order, 16 blocks each
+      const unsigned long long target = scaled_target(u_fin, S);
+      int bsel = -1;
+      unsigned long long run = before;
+#pragma unroll 1
+      for (int g0 = 0; g0 < nk * kUnitBlk && bsel < 0; g0 += 32) {
+        const int e = g0 + lane;
+        const unsigned long long v = e < nk * kUnitBlk ? ublk[ku(e / kUnitBlk)][e % kUnitBlk] : 0ull;
+        const unsigned long long vi = warp_incl_scan_u64(v);
+        const unsigned long long ve = vi - v;
+        const unsigned int h2 = __ballot_sync(0xffffffffu, e < nk * kUnitBlk && run + ve <= target &&
+                                                               target < run + vi);
+        if (h2) {
+          const int l2 = __ffs(h2) - 1;
+          bsel = g0 + l2;
+          run += __shfl_sync(0xffffffffu, ve, l2);
+        } else {
+          run += __shfl_sync(0xffffffffu, vi, 31);
+        }
+      }
+      int tok = V - 1;
+      if (bsel < 0) {
+        flags |= SV_STATUS_INTERNAL;
+      } else {
+        // the token: lane l holds the block's vector l (tokens e0 .. e0 + VEC - 1)
+        const int w = ku(bsel / kUnitBlk), J = bsel % kUnitBlk;
+        const unsigned int u = rank * kWarps + (unsigned int)w;
+        const int n = min(AE, V - unit_chunk(u) * AE);
+        const int vi = lane + 32 * J;
+        const unsigned char* wb = dsmem + (size_t)w * kNB * kItemBytes;
+        const uint4 t = vi < (n + VEC - 1) / VEC ? lds128(wb + vi * 16) : neg_inf_vec(EB);
+        const uint4 d = vi < (n + VEC - 1) / VEC ? lds128(wb + kItemBytes + vi * 16) : neg_inf_vec(EB);
+        unsigned long long wv[VEC];
+        unsigned long long lsum = 0;
+#pragma unroll
+        for (int h = 0; h < VEC; ++h) {
+          // past the end of the row (the unit's padding) the weight is 0
+          const bool live = vi * VEC + h < n;
+          wv[h] = live ? draw_weight<true>(vec_elem<EB>(t, h), vec_elem<EB>(d, h), kc) : 0ull;
+          lsum += wv[h];
+        }
+        const unsigned long long li = warp_incl_scan_u64(lsum);
+        unsigned long long r2 = run + li - lsum;
+        int tk = -1;
+        if (r2 <= target && target < r2 + lsum) {
+#pragma unroll
+          for (int h = 0; h < VEC; ++h) {
+            if (tk < 0 && r2 + wv[h] > target) tk = unit_chunk(u) * AE + vi * VEC + h;
+            r2 += wv[h];
+          }
+        }
+        const unsigned int holder = __ballot_sync(0xffffffffu, tk >= 0);
+        if (holder) tok = __shfl_sync(0xffffffffu, tk, __ffs(holder) - 1);
+        else flags |= SV_STATUS_INTERNAL;
+      }
+      if (lane == 0) P.out_tokens[(size_t)b * (G + 1) + k] = tok;
+      if (lane == 0) flags |= uflags;
     }
   }
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
@@ -2787,7 +2842,6 @@ size_t cluster_tables(int G, int V, int eb) {
 
 // Clusters of C CTAs (C <= kClusterMax) that fit on this device at once
 // (cached per device).
-constexpr int kClusterMax = 16;
 template <int EB, int MODE, bool PK>
 int max_clusters(int C) {
   static std::atomic<int> cached[kClusterMax + 1];  // (device + 1) << 16 | count; 0: none
@@ -2825,9 +2879,11 @@ template <int EB, int MODE, bool PK>
 int cluster_route(int B, int G, int V) {
   if (g_schedule.load() == SV_SCHEDULE_PERSISTENT) return 0;
   if (B < 1 || cluster_tables(G, V, EB) > (size_t)kClusterTables) return 0;
-  // the largest cluster of which B fit at once (one wave: a request per cluster)
+  const size_t nc = ((size_t)V + kItemBytes / EB - 1) / (kItemBytes / EB);
+  // the largest cluster of which B fit at once (one wave: a request per
+  // cluster) and whose warps hold one unit each of a request's A work
   for (int C = kClusterMax; C >= 8; --C)
-    if (max_clusters<EB, MODE, PK>(C) >= B) return C;
+    if (max_clusters<EB, MODE, PK>(C) >= B) return (size_t)(G + 1) * nc <= (size_t)C * kWarps ? C : 0;
   return 0;
 }
 

@@ -69,11 +69,18 @@ def against_oracle(w, res):
 
 
 def test_small_batches_take_the_cluster_schedule():
-    for dt in (torch.bfloat16, torch.float32):
+    """One wave of clusters whose warps hold one unit each of a request's work
+    (a unit: an 8 KB target chunk and the draft chunk of the same position)."""
+    bf, f32 = torch.bfloat16, torch.float32
+    for dt in (bf, f32):
         assert binding.spec_verify_cluster_size(dt, 1, 4, 32000) > 0
-        assert binding.spec_verify_cluster_size(dt, 8, 3, 128256) > 0
-        assert binding.spec_verify_cluster_size(dt, 8, 3, 128256, greedy=True) > 0
+        assert binding.spec_verify_cluster_size(dt, 8, 3, 32000) > 0
         assert binding.spec_verify_cluster_size(dt, 512, 3, 128256) == 0
+    assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) > 0
+    assert binding.spec_verify_cluster_size(bf, 8, 3, 128256, greedy=True) > 0
+    # too many units per request for one cluster: the persistent grid
+    assert binding.spec_verify_cluster_size(f32, 2, 3, 128256) == 0
+    assert binding.spec_verify_cluster_size(bf, 2, 31, 128256) == 0
     prev = binding.spec_verify_set_schedule(binding.SCHEDULE_PERSISTENT)
     try:
         assert binding.spec_verify_cluster_size(torch.bfloat16, 8, 3, 128256) == 0
@@ -82,7 +89,7 @@ def test_small_batches_take_the_cluster_schedule():
 
 
 CASES = [(8, 3, 128256, "bf16"), (5, 4, 20001, "bf16"), (3, 2, 4097, "f32"), (1, 4, 32000, "f32"),
-         (6, 7, 8193, "bf16"), (4, 3, 1, "bf16"), (7, 5, 152064, "bf16")]
+         (6, 7, 8193, "bf16"), (4, 3, 1, "bf16"), (7, 4, 152064, "bf16"), (2, 3, 32000, "f32")]
 
 
 @pytest.mark.parametrize("B,G,V,dt", CASES)
