@@ -2513,6 +2513,58 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   uint64_t* mybar = bar[warp];
   Meta* mymeta = cmeta[warp];
 
+  const unsigned int gw = rank * kWarps + (unsigned int)warp;
+  // Units: u = c (G + 1) + i is chunk c of target row i and, for a sampling
+  // position i < G, chunk c of draft row i; units of rows past gamma_b are
+  // void.  Warp gw holds unit gw (the host checks (G + 1) NC <= C kWarps).
+  const int per = G + 1;
+  auto unit_row = [&](unsigned int u) { return (int)(u % (unsigned int)per); };
+  auto unit_chunk = [&](unsigned int u) { return (int)(u / (unsigned int)per); };
+  const unsigned int nU = (unsigned int)per * (unsigned int)NC;
+  const bool has = gw < nU;
+  const int ui = has ? unit_row(gw) : 0, uc = has ? unit_chunk(gw) : 0;
+  const int un = min(AE, V - uc * AE);  // logits in the unit's chunk
+  // padded layout: rows 0..G of target and 0..G-1 of draft exist for every
+  // request, so the unit's copies may start before gamma_b is known
+  int nitem = !has ? 0 : (MODE == MODE_SAMPLE && ui < G ? 2 : 1);
+
+  // Each warp's lane 0 readies its own barriers, so its copies can start at
+  // once: in the padded layout a unit's rows do not depend on gamma_b, and the
+  // target chunk goes to buffer 0, the draft chunk (sampling) to buffer 1 before
+  // the request's values are read.  A copy of a row that turns out void is still
+  // waited for, then ignored.  In the packed layout the rows past gamma_b
+  // belong to other requests (or lie past the arrays), so the copies wait for
+  // cu_draft and cover rows up to gamma_b only.
+  auto issue_unit = [&](const ReqAddr& R) {
+    for (int h = 0; h < nitem; ++h) {
+      Meta m;
+      m.kind = KIND_A;
+      m.pslot = h ? G + 1 + ui : ui;
+      m.c = uc;
+      m.n = un;
+      const size_t row = h ? R.d0 + (size_t)ui : R.t0 + (size_t)ui;
+      m.p0 = (h ? P.draft : P.target) + (row * (size_t)V + (size_t)uc * AE) * EB;
+      m.p1 = nullptr;
+      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      if (lane == 0) {
+        mymeta[h] = m;
+        if (m.direct) {
+          mbar_arrive(&mybar[h]);
+        } else {
+          mbar_arrive_expect_tx(&mybar[h], (unsigned int)(m.n * EB));
+          bulk_copy_g2s(mybuf + h * kItemBytes, m.p0, (unsigned int)(m.n * EB), &mybar[h]);
+        }
+      }
+    }
+    __syncwarp();
+  };
+  if (lane == 0) {
+    for (int s = 0; s < kNB; ++s) mbar_init(&mybar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  if constexpr (!PK) issue_unit(addr_from_base<false>(P, b, 0, 0));
+
   // the request: draft length, addresses, temperature constants
   unsigned int rflags = 0, flags = 0;
   int gb = 0, base = 0;
@@ -2524,6 +2576,10 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     if (g_in != gb) rflags |= SV_STATUS_BAD_GAMMA;
   }
   const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+  if constexpr (PK) {
+    nitem = (!has || ui > gb) ? 0 : (MODE == MODE_SAMPLE && ui < gb ? 2 : 1);
+    issue_unit(A);
+  }
   bool greedy = MODE == MODE_GREEDY;
   TempC tc{0.0f, 0.0f};
   if (MODE == MODE_SAMPLE) {
@@ -2532,20 +2588,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     else tc = temp_consts(sanitize_temperature(T, rflags));
   }
   const bool sample = MODE == MODE_SAMPLE && !greedy;
-  const int per = gb + 1;  // units per chunk
-  const unsigned int nU = (unsigned int)per * (unsigned int)NC;
-  const unsigned int gw = rank * kWarps + (unsigned int)warp;
-  // this CTA's units are rank kWarps + w (one per warp; the host checks
-  // (G + 1) NC <= C kWarps)
-  auto unit_row = [&](unsigned int u) { return (int)(u % (unsigned int)per); };
-  auto unit_chunk = [&](unsigned int u) { return (int)(u / (unsigned int)per); };
-
-  if (tid == 0) {
-    for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < kNB; ++s) mbar_init(&bar[w][s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    cta_sum = 0ull;
-  }
+  if (tid == 0) cta_sum = 0ull;
   __syncthreads();
   // every CTA decides: its warp 0 requests the draft inputs and the final
   // draw's uniform before its items
@@ -2557,47 +2600,24 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
   }
 
-  // ---- A items of this warp's unit: the target chunk into buffer 0, the
-  // draft chunk (sampling, position below gamma_b) into buffer 1
-  unsigned int issued = 0;
+  // ---- this warp's A items: the target chunk of row ui <= gamma_b and, for a
+  // sampling position ui < gamma_b, its draft chunk
   bool failed = false;
-  const bool has = gw < nU;
-  const int ui = has ? unit_row(gw) : 0, uc = has ? unit_chunk(gw) : 0;
-  const bool pair = sample && has && ui < gb;
-  const int un = min(AE, V - uc * AE);  // logits in the unit's chunk
-  if (has) {
-    for (int h = 0; h < (pair ? 2 : 1); ++h) {
-      Meta m;
-      m.kind = KIND_A;
-      m.pslot = h ? G + 1 + ui : ui;
-      m.c = uc;
-      m.n = un;
-      const size_t row = h ? A.d0 + (size_t)ui : A.t0 + (size_t)ui;
-      m.p0 = (h ? P.draft : P.target) + (row * (size_t)V + (size_t)uc * AE) * EB;
-      m.p1 = nullptr;
-      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-      m.c_hi = tc.hi;
-      m.c_lo = tc.lo;
-      if (lane == 0) {
-        mymeta[h] = m;
-        if (m.direct) {
-          mbar_arrive(&mybar[h]);
-        } else {
-          mbar_arrive_expect_tx(&mybar[h], (unsigned int)(m.n * EB));
-          bulk_copy_g2s(mybuf + h * kItemBytes, m.p0, (unsigned int)(m.n * EB), &mybar[h]);
-        }
-      }
-      ++issued;
-    }
-    __syncwarp();
+  {
+    const int use = ui > gb ? 0 : (sample && ui < gb ? 2 : 1);  // items that count
     // lane r < C stores each partial into CTA r: every CTA decides locally
     const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
-    for (unsigned int h = 0; h < issued; ++h) {  // every copy is waited for (bounded)
-      const Meta& m = mymeta[h];
+    for (int h = 0; h < nitem; ++h) {  // every copy is waited for (bounded)
       if (!mbar_wait(&mybar[h], 0u)) {
         flags |= SV_STATUS_TIMEOUT;
         failed = true;
-      } else if (!failed) {
+      } else if (!failed && h < use) {
+        if (lane == 0) {  // the temperature constants are known by now
+          mymeta[h].c_hi = tc.hi;
+          mymeta[h].c_lo = tc.lo;
+        }
+        __syncwarp();
+        const Meta& m = mymeta[h];
         char* stage = reinterpret_cast<char*>(mybuf + h * kItemBytes);
         if (sample && m.direct) stage_unaligned<EB>(m, stage);
         const float2 pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
