@@ -768,12 +768,13 @@ __device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b
 // Bonus draw (every draft accepted): the token comes from p of target row gb,
 // whose per-item partials (m_c, s_c) the A pass already wrote, so no R pass
 // is needed.  Chunk weights W_c = s_c 2^((m_c - M) c) and their float-float
-// prefix sums locate the A chunk holding u S; one pass over that chunk's
-// logits (weights 2^((z - M) c), float-float prefix) walks to the smallest
-// token whose prefix exceeds u S.  If rounding leaves u S past a chunk's own
-// total the walk continues into the next chunk, and past the last one the
-// highest-indexed token of positive weight is taken.  The CDF is accurate to
-// about 1e-7 of S, like the residual path's.
+// prefix sums locate the A chunk holding u S (past the total, from rounding:
+// the last chunk of positive weight).  Inside that chunk the weights are
+// taken in exact 2^39 fixed point relative to W_c and the token is the
+// smallest whose prefix exceeds floor(r F), r = (u S - prefix) / W_c and F
+// the chunk's fixed-point total: lane sums, a warp scan and one 16-token
+// vector, with no serial walk.  The CDF is accurate to about 1e-7 of S, like
+// the residual path's.
 template <int EB, bool PK, class Parts>
 __device__ __noinline__ void final_bonus(const Params& P, const Parts& parts, int b, int gb,
                                          TempC tc, float M, unsigned char* stage) {
@@ -825,20 +826,47 @@ __device__ __noinline__ void final_bonus(const Params& P, const Parts& parts, in
       cs = __shfl_sync(0xffffffffu, csl, l);
       base.hi = __shfl_sync(0xffffffffu, run.hi, l);
       base.lo = __shfl_sync(0xffffffffu, run.lo, l);
-      if (cs < 0) cs = NC - 1;  // rounding: take the last chunk
-    } else {
-      // u S at or past the total (rounding): the last chunk, from its start
-      base = ff_sub(tot, FF{chunk_w(NC - 1), 0.0f});
+    }
+    if (l < 0 || cs < 0) {
+      // u S at or past the total (rounding): the last chunk of positive
+      // weight, from its start (the walk below then takes its last token of
+      // positive weight)
+      int lastc = -1;
+      FF before{0.0f, 0.0f}, r2 = excl;
+#pragma unroll 1
+      for (int c = c0; c < c1; ++c) {
+        const float w = chunk_w(c);
+        if (w > 0.0f) {
+          lastc = c;
+          before = r2;
+        }
+        r2 = ff_add(r2, FF{w, 0.0f});
+      }
+      const unsigned int has = __ballot_sync(0xffffffffu, lastc >= 0);
+      if (has) {
+        const int hl = 31 - __clz(has);
+        cs = __shfl_sync(0xffffffffu, lastc, hl);
+        base.hi = __shfl_sync(0xffffffffu, before.hi, hl);
+        base.lo = __shfl_sync(0xffffffffu, before.lo, hl);
+      } else {
+        cs = NC - 1;  // no weight at all (flagged as a non-finite row)
+        base = FF{0.0f, 0.0f};
+      }
     }
   }
 
-  // 2. the token: walk chunk cs (then the next ones if rounding requires)
+  // 2. the token inside chunk cs, exactly: its weights in 2^39 fixed point
+  //    relative to the chunk's weight W (y = w 2^23 / W), and the position
+  //    r = (u S - base) / W of u S inside the chunk as a float in [0, 1); the
+  //    token is the smallest one whose fixed-point prefix exceeds floor(r F),
+  //    F the chunk's fixed-point total.  Lane l owns the chunk's logits
+  //    [l EPL, (l + 1) EPL), staged through shared memory (vectors swizzled per
+  //    lane; scalar loads where the row does not allow 16-byte vectors, -inf past
+  //    its end).
   const char* row = P.target + (A.t0 + (size_t)gb) * (size_t)V * EB;
-  int tok = -1, last_pos = -1;
   auto slot_of = [&](int q) { return (lane * NV + (q ^ (lane & (NV - 1)))) * 16; };
-#pragma unroll 1
-  for (int c = cs; c < NC && tok < 0; ++c) {
-    const size_t e0 = (size_t)c * AE + (size_t)lane * EPL;
+  const size_t e0 = (size_t)cs * AE + (size_t)lane * EPL;
+  {
     const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15) == 0 && e0 + EPL <= (size_t)V;
     if (vec_ok) {
 #pragma unroll 4
@@ -863,47 +891,53 @@ __device__ __noinline__ void final_bonus(const Params& P, const Parts& parts, in
         sts128(stage + slot_of(q), make_uint4(w[0], w[1], w[2], w[3]));
       }
     }
-    FF lsum{0.0f, 0.0f};
-#pragma unroll 1
-    for (int q = 0; q < NV; ++q) {
-      const uint4 t = lds128(stage + slot_of(q));
-      float vs = 0.0f;  // one vector's weights: at most 8 terms, float is exact enough
+  }
+  const float W = chunk_w(cs);
+  ResidC kc;  // the bonus weight, scaled to the chunk: y = 2^((z - M) c) 2^23 / W
+  kc.mt = M;
+  kc.md = 0.0f;
+  kc.inv_st = W > 0.0f ? __fdiv_rn(1.0f, W) : 0.0f;
+  kc.rho = 0.0f;
+  resid_scales(kc);
+  kc.hi = tc.hi;
+  kc.lo = tc.lo;
+  kc.reject = 0;
+  float r = W > 0.0f ? ff_div(ff_sub(target, base), FF{W, 0.0f}) : 0.0f;
+  r = fminf(fmaxf(r, 0.0f), 0.99999994f);  // the largest float below 1
+  auto vec_sum = [&](int q) -> unsigned long long {
+    const uint4 t = lds128(stage + slot_of(q));
+    FixAcc a{0u, 0u, 0u};
 #pragma unroll
-      for (int h = 0; h < VEC; ++h) {
-        const float w = ex2_approx(exp_arg(vec_elem<EB>(t, h), M, tc.hi, tc.lo));
-        if (w > 0.0f) last_pos = (int)(e0 + (size_t)(q * VEC + h));
-        vs = __fadd_rn(vs, w);
-      }
-      lsum = ff_add(lsum, FF{vs, 0.0f});
-    }
-    const FF li = warp_incl_scan_ff(lsum);
-    FF run = ff_add(base, ff_sub(li, lsum));
-    if (ff_le(run, target) && !ff_le(ff_add(run, lsum), target)) {
+    for (int h = 0; h < VEC; ++h) fix_add(a, draw_x<false>(vec_elem<EB>(t, h), -INFINITY, kc));
+    return fix_value(a);
+  };
+  unsigned long long lsum = 0;
 #pragma unroll 1
-      for (int q = 0; q < NV && tok < 0; ++q) {
-        const uint4 t = lds128(stage + slot_of(q));
+  for (int q = 0; q < NV; ++q) lsum += vec_sum(q);
+  const unsigned long long li = warp_incl_scan_u64(lsum);
+  const unsigned long long Ftot = __shfl_sync(0xffffffffu, li, 31);
+  const unsigned long long t = scaled_target(r, Ftot);  // < Ftot when Ftot > 0
+  int tok = -1;
+  unsigned long long run = li - lsum;
+  if (Ftot > 0ull && run <= t && t < li) {
+#pragma unroll 1
+    for (int q = 0; q < NV && tok < 0; ++q) {
+      const unsigned long long vs = vec_sum(q);
+      if (run + vs > t) {
+        const uint4 tv = lds128(stage + slot_of(q));
 #pragma unroll
         for (int h = 0; h < VEC; ++h) {
-          const float w = ex2_approx(exp_arg(vec_elem<EB>(t, h), M, tc.hi, tc.lo));
-          const FF nxt = ff_add(run, FF{w, 0.0f});
-          if (tok < 0 && w > 0.0f && !ff_le(nxt, target)) tok = (int)(e0 + (size_t)(q * VEC + h));
-          run = nxt;
+          const unsigned long long wv = draw_weight<false>(vec_elem<EB>(tv, h), -INFINITY, kc);
+          if (tok < 0 && run + wv > t) tok = (int)(e0 + (size_t)(q * VEC + h));
+          run += wv;
         }
+      } else {
+        run += vs;
       }
     }
-    const unsigned int holder = __ballot_sync(0xffffffffu, tok >= 0);
-    tok = holder ? __shfl_sync(0xffffffffu, tok, __ffs(holder) - 1) : -1;
-    FF ctot;
-    ctot.hi = __shfl_sync(0xffffffffu, li.hi, 31);
-    ctot.lo = __shfl_sync(0xffffffffu, li.lo, 31);
-    base = ff_add(base, ctot);
   }
-  if (tok < 0) {  // past the last chunk: the highest-indexed token of positive weight
-    int lp = last_pos;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-    tok = lp;
-  }
+  const unsigned int holder = __ballot_sync(0xffffffffu, tok >= 0);
+  tok = holder ? __shfl_sync(0xffffffffu, tok, __ffs(holder) - 1) : -1;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (lane == 0) {
     if (tok < 0) {
