@@ -198,3 +198,33 @@ def test_cluster_status_flags_and_reuse():
         v.sample(w2.target, w2.draft, w2.draft_tokens, w2.gamma, w2.uniforms, w2.temperature)
     torch.cuda.synchronize()
     assert binding.spec_verify_status(v.workspace) == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_vanished_residual_falls_back_to_p_on_both_schedules(dt):
+    """A clear rejection whose residual mass is below the fixed-point
+    resolution: the drafted token x has q(x) = 2 p(x) with p(x) ~ e^-40 and
+    the target and draft rows agree elsewhere, so u = 0.9 rejects (ratio 1/2)
+    while sum max(0, p - q) ~ p(x) rounds to 0 in units of 2^-39.  Both
+    schedules then draw from p_k; their tokens must agree, and the token must
+    have p > 0.  (The float64 oracle's residual is pure cancellation noise
+    here, so it is not the reference for this case.)"""
+    B, G, V = 3, 1, 4096
+    w = W.make_random(B, G, V, dt, seed=31, sigma_t=1.0, sigma_d=0.0)
+    x = 17
+    w.target[:, 0, x] = -40.0
+    w.draft[:, 0] = w.target[:, 0]
+    w.draft[:, 0, x] = -40.0 + 0.6931471805599453
+    w.draft_tokens[:, 0] = x
+    w.uniforms[:, 0] = 0.9
+    w.temperature[:] = 1.0
+    w = w.to(DEV)
+    res = sample_both(w, probs=False)
+    assert binding.spec_verify_cluster_size(w.target.dtype, B, G, V) > 0
+    same(res[0], res[1])
+    out, nacc = res[0][0], res[0][1]
+    assert (nacc == 0).all()
+    p = torch.softmax(w.target[:, 0].double(), dim=1).cpu()
+    for b in range(B):
+        assert 0 <= out[b, 0] < V and out[b, 0] != x and p[b, out[b, 0]] > 0
+        assert out[b, 1] == -1
