@@ -1387,15 +1387,14 @@ __device__ __forceinline__ float direct_elem(const Meta& m, int h, int e) {
 
 
 // An unaligned item's elements copied into its stage buffer (which no copy
-// targets), padded with -inf to whole 16-byte vectors, so that it is reduced
-// by the same code, in the same order, as a copied item: a row's statistics do
+// targets), padded with -inf to the whole buffer, so that it is reduced by
+// the same code, in the same order, as a copied item: a row's statistics do
 // not depend on where the row sits in memory.
 template <int EB>
 __device__ __noinline__ void stage_unaligned(const Meta& m, char* stage) {
-  constexpr int VEC = 16 / EB;
+  constexpr int AE = kItemBytes / EB;
   const int lane = threadIdx.x & 31;
-  const int nvec = (m.n + VEC - 1) / VEC;
-  for (int e = lane; e < nvec * VEC; e += 32) {
+  for (int e = lane; e < AE; e += 32) {
     if constexpr (EB == 2) {
       const unsigned short x = e < m.n ? __ldg(reinterpret_cast<const unsigned short*>(m.p0) + e)
                                        : (unsigned short)0xff80u;
@@ -1409,6 +1408,18 @@ __device__ __noinline__ void stage_unaligned(const Meta& m, char* stage) {
   __syncwarp();
 }
 
+// The tail of a partial copied item (the last chunk of a row) set to -inf, so
+// the item routines read whole buffers without bounds checks (a -inf logit
+// changes neither a maximum nor a sum of exp2, nor the lowest index of a
+// finite maximum).
+template <int EB>
+__device__ __noinline__ void pad_item_tail(char* stage, int n) {
+  const int lane = threadIdx.x & 31;
+  const uint4 ninf = neg_inf_vec(EB);
+  for (int vi = n * EB / 16 + lane; vi < kItemBytes / 16; vi += 32) sts128(stage + vi * 16, ninf);
+  __syncwarp();
+}
+
 // A item, sampling: (max, sum of exp2) over the item.
 template <int EB>
 __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage) {
@@ -1417,9 +1428,8 @@ __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage
   const int lane = threadIdx.x & 31;
   float mx = -INFINITY, sum = 0.0f;
   {
-    // two passes over the stage: the maximum, then the exponentials (an
-    // unaligned item was staged with -inf padding to whole vectors)
-    const int nvec = (m.n + VEC - 1) / VEC;
+    // two passes over the stage: the maximum, then the exponentials (the
+    // whole buffer is valid: a partial or unaligned item is padded with -inf)
     if constexpr (EB == 2) {
       // The item's 2*NV*4 logits stay in registers as bf16 pairs.
       constexpr int NW = NV * 4;
@@ -1427,7 +1437,7 @@ __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int vi = lane + 32 * j;
-        const uint4 v = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+        const uint4 v = lds128(stage + vi * 16);
         w[4 * j] = v.x;
         w[4 * j + 1] = v.y;
         w[4 * j + 2] = v.z;
@@ -1471,7 +1481,7 @@ __device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
-      v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+      v[j] = lds128(stage + vi * 16);
     }
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
@@ -1510,7 +1520,8 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   if (!m.direct) {
-    // the maximum (independent chains), then the lowest index holding it
+    // the maximum (independent chains), then the lowest index holding it (a
+    // partial item is padded with -inf; the float32 index scan skips the pad)
     const int nvec = m.n / VEC;
     if constexpr (EB == 2) {
       // maximum on the packed pairs as a log-depth tree; a lane holding the
@@ -1520,7 +1531,7 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int vi = lane + 32 * j;
-        const uint4 v = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+        const uint4 v = lds128(stage + vi * 16);
         w[4 * j] = v.x;
         w[4 * j + 1] = v.y;
         w[4 * j + 2] = v.z;
@@ -1562,7 +1573,7 @@ __device__ __forceinline__ float2 a_item_greedy(const Meta& m, const char* stage
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
-      v[j] = vi < nvec ? lds128(stage + vi * 16) : neg_inf_vec(EB);
+      v[j] = lds128(stage + vi * 16);
     }
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -2137,11 +2148,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
       char* stage = reinterpret_cast<char*>(mybuf + s * kItemBytes);
       if (m_kind == KIND_A) {
         const bool staged = MODE == MODE_SAMPLE && m.c_hi != 0.0f;
+        const bool padded = !m.direct && m.n < kItemBytes / EB;  // a row's last chunk
         if (staged && m.direct) stage_unaligned<EB>(m, stage);
+        else if (padded) pad_item_tail<EB>(stage, m.n);
         const float2 part = staged ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         if (lane == 0) P.stats[((size_t)m_b * (2 * G + 1) + m.pslot) * P.stride_nc + m.c] = part;
         // stores into the buffer are ordered before the next bulk copy into it
-        if (staged && m.direct) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if ((staged && m.direct) || padded) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       } else {
         const unsigned long long part = r_item<EB>(m, stage);
         if (lane == 0) P.resid[(size_t)m_b * P.stride_ncr + m.c] = part;
@@ -2654,6 +2667,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
         const Meta& m = mymeta[h];
         char* stage = reinterpret_cast<char*>(mybuf + h * kItemBytes);
         if (sample && m.direct) stage_unaligned<EB>(m, stage);
+        else if (!m.direct && m.n < AE) pad_item_tail<EB>(stage, m.n);
         const float2 pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         if ((uint32_t)lane < C)
           st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
