@@ -76,9 +76,21 @@ constexpr int kNB = SV_BUFFERS;                       // TMA buffers per warp
 constexpr int kItemBytes = 8192;                      // A item: 8 KB of one row
 constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
 constexpr int kMaxBatch = 1536;                       // requests per launch (smem tables)
-constexpr int kMaxK = 8;                              // A items per claimed batch
-constexpr unsigned int kMaxRBatch = 4;                // R items per claim, at most
-constexpr unsigned int kBatchDiv = 4;                 // batches per warp's share, at least
+#ifndef SV_MAXK
+#define SV_MAXK 8
+#endif
+constexpr int kMaxK = SV_MAXK;                        // A items per claimed batch
+#ifndef SV_MAXKR
+#define SV_MAXKR 4u
+#endif
+constexpr unsigned int kMaxRBatch = SV_MAXKR;         // R items per claim, at most
+#ifndef SV_BATCH_DIV
+#define SV_BATCH_DIV 1u
+#endif
+// batches per warp's share of the A items, at least (a sweep over 1, 2 and 4
+// on B = 64..512 found the largest batches best: claims cost more than
+// the longer hold of the last requests' items)
+constexpr unsigned int kBatchDiv = SV_BATCH_DIV;
 constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
 
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
