@@ -80,6 +80,10 @@ constexpr int kMaxBatch = 1536;                       // requests per launch (sm
 #define SV_MAXK 8
 #endif
 constexpr int kMaxK = SV_MAXK;                        // A items per claimed batch
+#ifndef SV_RUNROLL
+#define SV_RUNROLL 2
+#endif
+constexpr int kRUnroll = SV_RUNROLL;                  // vector columns per step of an R item
 #ifndef SV_MAXKR
 #define SV_MAXKR 4u
 #endif
@@ -1627,7 +1631,7 @@ __device__ __forceinline__ unsigned long long r_item_sum(const Meta& m, const ch
     const unsigned long long n23 = f2_pack(-8388608.0f, -8388608.0f);
     const unsigned long long mone = f2_pack(-1.0f, -1.0f), p16 = f2_pack(65536.0f, 65536.0f);
     const unsigned long long c15 = f2_pack(12582912.0f, 12582912.0f);
-#pragma unroll 2
+#pragma unroll kRUnroll
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
       if (vi < nvec) {
@@ -1660,7 +1664,7 @@ __device__ __forceinline__ unsigned long long r_item_sum(const Meta& m, const ch
       }
     }
   } else {
-#pragma unroll 2
+#pragma unroll kRUnroll
     for (int j = 0; j < NV; ++j) {
       const int vi = lane + 32 * j;
       if (vi < nvec) {
