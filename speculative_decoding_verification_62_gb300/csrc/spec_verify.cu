@@ -1912,9 +1912,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   // appends its request to the decision queue, and R batches are claimed
   // from r_next (item i = chunk i % NCR of queue slot i / NCR).  While A
   // items remain, a warp takes R work only when the published, unclaimed R
-  // items (an estimate from loads started one batch earlier) exceed a small
-  // backlog: R re-reads then follow their rows' A pass closely (L2 hits)
-  // without delaying the A items that gate later decisions.
+  // items (an estimate from loads started one batch earlier) exceed a
+  // backlog of SV_BACKLOG_X4 / 4 batches per warp.  The default (16 batches)
+  // means A items first: the SMs are close to issue-bound during the A pass,
+  // and residual work taken earlier lengthens it (measured at every backlog
+  // from 0 to 16 batches).
   bool a_done = false;         // lane 0: next_item ran past the A items
   unsigned int a_raw = 0;      // lane 0: result of the pending A claim
   bool a_pending = false;      // lane 0
@@ -2283,9 +2285,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
 // stores each partial into the shared memory of every CTA of the cluster; a
 // cluster barrier replaces the arrival counter; each CTA's warp 0 then
 // computes the decision from its own copy (the arithmetic of the persistent
-// path; the leader, rank 0, writes the outputs).  After a reject, the R items
-// store per-block fixed-point sums in the leader, and after a second barrier
-// the leader walks one block of 256 (bf16) or 128 (float32) tokens.
+// path; the leader, rank 0, writes the outputs).  Each warp keeps its unit (a
+// target chunk and the draft chunk of the same position) in its two staging
+// buffers; after a reject the CTAs compute the residual block sums of the
+// rejected row from those buffers, exchange their totals, and after a second
+// barrier the CTA holding floor(u S) walks one resident block of 256 (bf16)
+// or 128 (float32) tokens.
 constexpr int kClusterMax = 16;                  // CTAs per cluster, at most
 constexpr int kBlk = 8;                          // blocks per R item: one per vector column
 constexpr int kClusterTables = 24 * 1024;        // partials, fallback block sums, decision
