@@ -228,3 +228,19 @@ def test_vanished_residual_falls_back_to_p_on_both_schedules(dt):
     for b in range(B):
         assert 0 <= out[b, 0] < V and out[b, 0] != x and p[b, out[b, 0]] > 0
         assert out[b, 1] == -1
+
+
+def test_batch_at_the_cluster_wave_limit():
+    """The largest batch that fits one wave of clusters runs on the cluster
+    schedule, one more request runs on the persistent grid; both match the
+    oracle."""
+    G, V = 2, 32000
+    limit = max(B for B in range(1, 65)
+                if binding.spec_verify_cluster_size(torch.bfloat16, B, G, V) > 0)
+    assert binding.spec_verify_cluster_size(torch.bfloat16, limit + 1, G, V) == 0
+    for B in (limit, limit + 1):
+        w = W.make_random(B, G, V, "bf16", seed=B, gamma="ragged",
+                          temperature=[0.7 + 0.02 * i for i in range(B)]).to(DEV)
+        a, b = sample_both(w)
+        same(a, b)
+        against_oracle(w, a)
