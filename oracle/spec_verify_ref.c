@@ -33,7 +33,7 @@
  *    "draft length by load", K=3 worked example.)  In a sampling call, a
  *    request whose temperature is exactly 0 takes these greedy steps.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  - accept is strict: u < ratio; q(x) == 0 accepts.
  *  - no epsilons are added to q or to the residual sum.
  *  - the resample/bonus draws use their own uniform u[b][G]; the inverse CDF
