@@ -45,8 +45,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layout", choices=["padded", "packed"], default="padded",
                     help="padded [B][G+1][V] rows, or packed rows with a cu_draft prefix")
-    ap.add_argument("--schedule", choices=["auto", "persistent"], default="auto",
-                    help="auto: small batches on the cluster schedule; persistent: always the grid")
+    ap.add_argument("--schedule", choices=["auto", "stream", "persistent"], default="auto",
+                    help="auto: the resident cluster path, the streaming cluster path or the "
+                         "persistent grid, the first that applies; stream: never the resident "
+                         "path; persistent: always the grid")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step from Python instead of one CUDA-graph replay")
     return ap.parse_args()
@@ -217,9 +219,9 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config, mode):
-    """DRAM bytes per launch from the committed ncu summary, if it still
-    describes the current kernel source; else None."""
+def profiled_traffic(config, mode, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it describes
+    this kernel and the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -227,7 +229,7 @@ def profiled_traffic(config, mode):
     except (OSError, ValueError):
         return None
     e = d.get(f"{config}/{mode}")
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash() or e.get("kernel") != kernel:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -254,9 +256,12 @@ def run_ours(args):
         base = W.make(args.config, device=dev, seed=rank_seed(base.meta["seed"], rank))
     mode = args.mode
     B, G, V = base.B, base.G, base.V
-    binding.spec_verify_set_schedule(binding.SCHEDULE_PERSISTENT if args.schedule == "persistent"
-                                     else binding.SCHEDULE_AUTO)
-    csize = binding.spec_verify_cluster_size(base.target.dtype, B, G, V, greedy=mode == "greedy")
+    binding.spec_verify_set_schedule({"auto": binding.SCHEDULE_AUTO,
+                                      "stream": binding.SCHEDULE_STREAM,
+                                      "persistent": binding.SCHEDULE_PERSISTENT}[args.schedule])
+    route, csize = binding.spec_verify_route(base.target.dtype, B, G, V, greedy=mode == "greedy")
+    kernel = {binding.ROUTE_CLUSTER: "cluster_kernel", binding.ROUTE_STREAM: "stream_kernel",
+              binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
     launches_per_call = 1
 
     packed = args.layout == "packed"
@@ -395,8 +400,9 @@ def run_ours(args):
     if rank == 0:
         cfg = workload_desc(base, mode)
         cfg.update({"layout": args.layout,
-                    "schedule": f"clusters of {csize} CTAs, one per request" if csize
-                                else "persistent grid",
+                    "schedule": {"cluster_kernel": f"resident clusters of {csize} CTAs, one per request",
+                                 "stream_kernel": f"streaming clusters of {csize} CTAs, one per request",
+                                 "verify_kernel": "persistent grid"}[kernel],
                     "parallelism": f"replicas x{world} (independent requests)",
                     "launch": "one CUDA-graph replay of the timed steps" if graph is not None
                               else "one Python call per step",
@@ -411,9 +417,8 @@ def run_ours(args):
                 "data": "synthetic", "config": cfg,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "peak_source": peak_src,
-                             "traffic": None if packed else profiled_traffic(args.config, mode),
-                             "kernel": ("cluster_kernel" if csize else "verify_kernel") +
-                                       " (one launch per step)"},
+                             "traffic": None if packed else profiled_traffic(args.config, mode, kernel),
+                             "kernel": kernel + " (one launch per step)"},
                 "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * launches_per_call,
                 "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)

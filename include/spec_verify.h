@@ -245,27 +245,48 @@ int spec_verify_status(void *workspace, sv_stream_t stream, uint32_t *status_hos
 const char *spec_verify_strerror(int code);
 
 /*
- * Schedules.  A batch small enough that one thread-block cluster per request
- * fits on the GPU at once runs on the cluster schedule: each request's
- * partials, decision and residual block sums move through the cluster's
- * shared memory instead of global-memory counters and records, which shortens
- * the chain of dependent steps (statistics, decision, residual pass, draw).
- * Larger batches run on the persistent grid.  Both compute every value with
- * the same arithmetic, so outputs do not depend on the schedule.  These two
- * calls are not steps of the method: they exist for testing and measurement.
+ * Schedules.  Three kernels compute every value with the same arithmetic, so
+ * outputs do not depend on the schedule:
+ *   - the resident cluster path: a batch small enough that one thread-block
+ *     cluster per request fits on the GPU at once, with each warp holding one
+ *     chunk of a draft position's target and draft rows in shared memory.  The
+ *     partials, the decision and the residual block sums move through the
+ *     cluster's shared memory, and the final draw walks resident data;
+ *   - the streaming cluster path: one cluster per request as well, for batches
+ *     of up to one cluster per SM (clusters of up to 16 CTAs, at least one),
+ *     the warps streaming the request's chunks two at a time and re-reading
+ *     the rejected row's chunks for the residual;
+ *   - the persistent grid, for larger batches: items claimed from global
+ *     counters, decisions published through global records.
+ * The cluster paths replace the persistent grid's chain of global-memory
+ * synchronisations (arrival counters, decision records, queue) with cluster
+ * barriers.  These calls are not steps of the method: they exist for testing
+ * and measurement.
  *
- * spec_verify_set_schedule: SV_SCHEDULE_AUTO (the default) or
- * SV_SCHEDULE_PERSISTENT (every call on the persistent grid), for the calls
- * that follow in this process.  Returns the previous value, or SV_ERR_SCALAR
- * for an unknown value.
+ * spec_verify_set_schedule: the policy for the calls that follow in this
+ * process: SV_SCHEDULE_AUTO (the default: the first of the resident cluster
+ * path, the streaming cluster path and the persistent grid that applies),
+ * SV_SCHEDULE_PERSISTENT (every call on the persistent grid) or
+ * SV_SCHEDULE_STREAM (never the resident path).  Returns the previous policy,
+ * or SV_ERR_SCALAR for an unknown value.
  *
- * spec_verify_cluster_size: the cluster size (CTAs per request) the next
- * sampling (greedy == 0) or greedy call of this shape on the current device
- * would use, 0 for the persistent grid, or SV_ERR_SCALAR for invalid sizes.
+ * spec_verify_route: the kernel (SV_ROUTE_*) that the next sampling
+ * (greedy == 0) or greedy call of this shape, in the padded layout, on the
+ * current device would use under the current policy, or SV_ERR_SCALAR for
+ * invalid sizes.  If cluster_size is not NULL (a HOST pointer), it receives
+ * the cluster size (CTAs per request) of a cluster path, or 0.
+ *
+ * spec_verify_cluster_size: that cluster size alone (0 for the persistent
+ * grid), or SV_ERR_SCALAR.
  */
 #define SV_SCHEDULE_AUTO 0
 #define SV_SCHEDULE_PERSISTENT 1
+#define SV_SCHEDULE_STREAM 2
+#define SV_ROUTE_PERSISTENT 0
+#define SV_ROUTE_CLUSTER 1
+#define SV_ROUTE_STREAM 2
 int spec_verify_set_schedule(int schedule);
+int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int *cluster_size);
 int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy);
 
 #ifdef __cplusplus

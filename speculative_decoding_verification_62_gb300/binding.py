@@ -24,8 +24,9 @@ SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy",
            "spec_verify_sample_packed", "spec_verify_greedy_packed", "spec_verify_draw",
            "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror",
-           "spec_verify_set_schedule", "spec_verify_cluster_size")
-SCHEDULE_AUTO, SCHEDULE_PERSISTENT = 0, 1
+           "spec_verify_set_schedule", "spec_verify_route", "spec_verify_cluster_size")
+SCHEDULE_AUTO, SCHEDULE_PERSISTENT, SCHEDULE_STREAM = 0, 1, 2
+ROUTE_PERSISTENT, ROUTE_CLUSTER, ROUTE_STREAM = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,8 @@ def load_library():
         lib.spec_verify_strerror.argtypes = [ci]
         lib.spec_verify_set_schedule.restype = ci
         lib.spec_verify_set_schedule.argtypes = [ci]
+        lib.spec_verify_route.restype = ci
+        lib.spec_verify_route.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(ci)]
         lib.spec_verify_cluster_size.restype = ci
         lib.spec_verify_cluster_size.argtypes = [ci, ci, ci, ci, ci]
         _lib = lib
@@ -80,15 +83,27 @@ def spec_verify_strerror(code: int) -> str:
 
 
 def spec_verify_set_schedule(schedule: int) -> int:
-    """SCHEDULE_AUTO or SCHEDULE_PERSISTENT for the calls that follow; returns the previous."""
+    """SCHEDULE_AUTO, SCHEDULE_PERSISTENT or SCHEDULE_STREAM for the calls that follow;
+    returns the previous policy."""
     rc = load_library().spec_verify_set_schedule(int(schedule))
     if rc < 0:
         raise SpecVerifyError(rc)
     return rc
 
 
+def spec_verify_route(dtype: torch.dtype, B: int, G: int, V: int, greedy: bool = False):
+    """(ROUTE_*, CTAs per request) of the kernel a call of this shape would use."""
+    code = SV_BF16 if dtype == torch.bfloat16 else SV_F32
+    C = ctypes.c_int(0)
+    rc = load_library().spec_verify_route(code, int(B), int(G), int(V), int(bool(greedy)),
+                                          ctypes.byref(C))
+    if rc < 0:
+        raise SpecVerifyError(rc)
+    return rc, C.value
+
+
 def spec_verify_cluster_size(dtype: torch.dtype, B: int, G: int, V: int, greedy: bool = False) -> int:
-    """CTAs per request of the cluster schedule for this shape, 0 for the persistent grid."""
+    """CTAs per request of the cluster schedule (resident or streaming) for this shape, 0 for the persistent grid."""
     code = SV_BF16 if dtype == torch.bfloat16 else SV_F32
     rc = load_library().spec_verify_cluster_size(code, int(B), int(G), int(V), int(bool(greedy)))
     if rc < 0:

@@ -74,7 +74,7 @@ constexpr int kWarps = SV_WARPS;                      // warps per CTA (one CTA 
 constexpr int kThreads = 32 * kWarps;
 constexpr int kNB = SV_BUFFERS;                       // TMA buffers per warp
 constexpr int kItemBytes = 8192;                      // A item: 8 KB of one row
-constexpr int kHalfBytes = kItemBytes / 2;            // R item: 2 KB of each of two rows
+constexpr int kHalfBytes = kItemBytes / 2;            // R item: 4 KB of each of two rows
 constexpr int kMaxBatch = 1536;                       // requests per launch (smem tables)
 #ifndef SV_MAXK
 #define SV_MAXK 8
@@ -1183,8 +1183,6 @@ __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* 
   __syncwarp();
 }
 
-// Final draw for request b, run by the warp that completed its last R item:
-// the chunk whose prefix passes u*S, then a scan of that chunk only.
 // Sum over R chunk c of the draw weights, read from global memory by the
 // whole warp.
 template <int EB>
@@ -1199,47 +1197,26 @@ __device__ unsigned long long chunk_weight_sum(const char* trow, const char* dro
   return warp_sum_u64(s);
 }
 
-template <int EB, bool PK>
-__device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsigned char* stage) {
+// The final draw from R chunk sums rp[0..NCR) of target row trow (and, after a
+// reject, draft row drow), run by one warp: the chunk whose prefix passes
+// floor(u S), then a scan of that chunk only, staged in `stage` (8 KB).  When
+// the sums vanish in fixed point (p_k and q_k agree within its resolution)
+// the draw uses p_k: its chunk sums replace the residual ones in rp.  GSUMS:
+// rp is in global memory, written by other SMs (read past L1); otherwise in
+// this CTA's shared memory.  Returns the token, or -1 (an internal error).
+template <int EB, bool GSUMS>
+__device__ __forceinline__ int chunk_draw(const char* trow, const char* drow, int V, int NCR,
+                                          float u_s, ResidC kc, unsigned long long* rp,
+                                          unsigned char* stage) {
   constexpr int RE = kHalfBytes / EB;  // elements per R chunk
   constexpr int EPL = RE / 32;         // contiguous elements per lane in the scan
   constexpr int VEC = 16 / EB;
   constexpr int NV = EPL / VEC;        // vectors per lane per row (8)
-  const int G = P.G, V = P.V, NCR = P.NCR;
   const int lane = threadIdx.x & 31;
-  Decision d;
-  d.k = 0;
-  d.reject = 0;
-  d.mt = d.md = d.inv_st = d.rho = 0.0f;
-  unsigned int flags = 0;
-  {
-    // every R item of b read b's decision before arriving, so it is published
-    int rb = -1;
-    bool ok = false;
-    if (lane == 0) {
-      const unsigned long long t0 = now_ns();
-      while (!(ok = read_record(&P.dec[b], rb, d)) && now_ns() - t0 < kWaitNs) __nanosleep(64);
-    }
-    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) flags |= SV_STATUS_TIMEOUT;
-    d.k = __shfl_sync(0xffffffffu, d.k, 0);
-    d.reject = __shfl_sync(0xffffffffu, d.reject, 0);
-    d.mt = __shfl_sync(0xffffffffu, d.mt, 0);
-    d.md = __shfl_sync(0xffffffffu, d.md, 0);
-    d.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
-    d.rho = __shfl_sync(0xffffffffu, d.rho, 0);
-  }
-  d.c_hi = tc.hi;
-  d.c_lo = tc.lo;
-  const ReqAddr A = req_addr<PK>(P, b);
-  const float u_s = sanitize_uniform(P.uniforms[A.uf], flags);
-  const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
-  ResidC kc;
-  kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
-  resid_scales(kc);
-  kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
-  const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
-  const char* drow = kc.reject ? P.draft + (A.d0 + (size_t)k) * (size_t)V * EB : nullptr;
-  unsigned long long* rp = P.resid + (size_t)b * P.stride_ncr;
+  auto ld_sum = [&](int c) -> unsigned long long {
+    if constexpr (GSUMS) return __ldcg(&rp[c]);
+    else return rp[c];
+  };
 
   // 1. The chunk: lane l owns chunks [c0, c1); a scan over the lanes' sums
   //    finds the lane, that lane walks its chunks.
@@ -1247,7 +1224,7 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
   const int c0 = min(NCR, lane * cpl), c1 = min(NCR, c0 + cpl);
   unsigned long long own = 0;
 #pragma unroll 1
-  for (int c = c0; c < c1; ++c) own += __ldcg(&rp[c]);
+  for (int c = c0; c < c1; ++c) own += ld_sum(c);
   unsigned long long incl = warp_incl_scan_u64(own);
   unsigned long long S = __shfl_sync(0xffffffffu, incl, 31);
   if (S == 0ull) {
@@ -1280,7 +1257,7 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
         unsigned long long run = excl;
 #pragma unroll 1
         for (int c = c0; c < c1; ++c) {
-          const unsigned long long w = __ldcg(&rp[c]);
+          const unsigned long long w = ld_sum(c);
           if (run + w > target) {
             cs = c;
             break;
@@ -1376,6 +1353,50 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
     // the buffer goes back to the bulk copies
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  return tok;
+}
+
+// Final draw for request b, run by the warp that completed its last R item
+// (the chunk sums are in the workspace).
+template <int EB, bool PK>
+__device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsigned char* stage) {
+  const int G = P.G, V = P.V, NCR = P.NCR;
+  const int lane = threadIdx.x & 31;
+  Decision d;
+  d.k = 0;
+  d.reject = 0;
+  d.mt = d.md = d.inv_st = d.rho = 0.0f;
+  unsigned int flags = 0;
+  {
+    // every R item of b read b's decision before arriving, so it is published
+    int rb = -1;
+    bool ok = false;
+    if (lane == 0) {
+      const unsigned long long t0 = now_ns();
+      while (!(ok = read_record(&P.dec[b], rb, d)) && now_ns() - t0 < kWaitNs) __nanosleep(64);
+    }
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) flags |= SV_STATUS_TIMEOUT;
+    d.k = __shfl_sync(0xffffffffu, d.k, 0);
+    d.reject = __shfl_sync(0xffffffffu, d.reject, 0);
+    d.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+    d.md = __shfl_sync(0xffffffffu, d.md, 0);
+    d.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+    d.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+  }
+  d.c_hi = tc.hi;
+  d.c_lo = tc.lo;
+  const ReqAddr A = req_addr<PK>(P, b);
+  const float u_s = sanitize_uniform(P.uniforms[A.uf], flags);
+  const int k = d.k < 0 ? 0 : (d.k > G ? G : d.k);
+  ResidC kc;
+  kc.mt = d.mt; kc.md = d.md; kc.inv_st = d.inv_st; kc.rho = d.rho;
+  resid_scales(kc);
+  kc.hi = d.c_hi; kc.lo = d.c_lo; kc.reject = (d.reject && k < G) ? 1 : 0;
+  const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
+  const char* drow = kc.reject ? P.draft + (A.d0 + (size_t)k) * (size_t)V * EB : nullptr;
+  unsigned long long* rp = P.resid + (size_t)b * P.stride_ncr;
+
+  int tok = chunk_draw<EB, true>(trow, drow, V, NCR, u_s, kc, rp, stage);
   if (lane == 0) {
     if (tok < 0) {
       flags |= SV_STATUS_INTERNAL;
@@ -2679,17 +2700,24 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
       if (!mbar_wait(&mybar[h], 0u)) {
         flags |= SV_STATUS_TIMEOUT;
         failed = true;
-      } else if (!failed && h < use) {
-        if (lane == 0) {  // the temperature constants are known by now
-          mymeta[h].c_hi = tc.hi;
-          mymeta[h].c_lo = tc.lo;
+      }
+      if (h < use) {
+        // An item that could not be read still stores a (NaN, 0) partial, so
+        // every CTA holds the same table and takes the same branches below.
+        float2 pr = make_float2(NAN, 0.0f);
+        if (!failed) {
+          if (lane == 0) {  // the temperature constants are known by now
+            mymeta[h].c_hi = tc.hi;
+            mymeta[h].c_lo = tc.lo;
+          }
+          __syncwarp();
+          const Meta& m = mymeta[h];
+          char* stage = reinterpret_cast<char*>(mybuf + h * kItemBytes);
+          if (sample && m.direct) stage_unaligned<EB>(m, stage);
+          else if (!m.direct && m.n < AE) pad_item_tail<EB>(stage, m.n);
+          pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         }
-        __syncwarp();
         const Meta& m = mymeta[h];
-        char* stage = reinterpret_cast<char*>(mybuf + h * kItemBytes);
-        if (sample && m.direct) stage_unaligned<EB>(m, stage);
-        else if (!m.direct && m.n < AE) pad_item_tail<EB>(stage, m.n);
-        const float2 pr = sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage);
         if ((uint32_t)lane < C)
           st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
       }
@@ -2879,6 +2907,287 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 }
 
 // ---------------------------------------------------------------------------
+// Medium batches: one cluster per request, items streamed
+// ---------------------------------------------------------------------------
+// When a request's A work does not fit its cluster's warps one unit each, or
+// only smaller clusters fit the batch in one wave, the warps of request b's
+// cluster stream its items instead: warp gw of the cluster's W warps takes
+// items gw, gw + W, gw + 2W, ... (item j is chunk j % NC of the request's row
+// j / NC: target rows 0..gamma_b, then draft rows 0..gamma_b-1), two copies
+// in flight.  Partials go to every CTA's shared memory and a cluster barrier
+// completes them, as on the resident path; every CTA's warp 0 computes the
+// decision.  After a reject the warps stream row k's R chunks (target and
+// draft halves, usually L2 hits) and store each chunk's fixed-point sum in
+// the leader's shared memory; after a second barrier the leader's warp 0
+// draws from those sums and walks one chunk.  No global counter, record or
+// queue is involved.  Shared memory: the buffers, then (the same layout in
+// every CTA) the partials [2G+1][NC] and the leader's chunk sums [NCR].
+template <int EB, int MODE, bool PK>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ __align__(8) uint64_t bar[kWarps][kNB];
+  __shared__ Meta smeta[kWarps][kNB];  // the item in each buffer
+  __shared__ float rsbuf[192];         // the decision's row statistics
+  __shared__ ClusterDec sdec;
+  constexpr int AE = kItemBytes / EB;   // logits per A item
+  constexpr int RE = kHalfBytes / EB;   // logits per R chunk and row
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank(), C = cluster_size();
+  const int b = (int)cluster_index();
+  const int G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
+  float2* part = reinterpret_cast<float2*>(dsmem + (size_t)kWarps * kNB * kItemBytes);
+  unsigned long long* rsum = reinterpret_cast<unsigned long long*>(part + (size_t)(2 * G + 1) * NC);
+  unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
+  uint64_t* mybar = bar[warp];
+  Meta* mymeta = smeta[warp];
+  const unsigned int gw = rank * kWarps + (unsigned int)warp, W = C * kWarps;
+
+  if (lane == 0) {
+    for (int s = 0; s < kNB; ++s) mbar_init(&mybar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // the request: draft length, addresses, temperature constants
+  unsigned int rflags = 0, flags = 0;
+  int gb = 0, base = 0;
+  if constexpr (PK) {
+    base = packed_base(P, b, gb, rflags);
+  } else {
+    const int g_in = P.gamma ? P.gamma[b] : 0;
+    gb = clamp_gamma(g_in, G);
+    if (g_in != gb) rflags |= SV_STATUS_BAD_GAMMA;
+  }
+  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+  bool greedy = MODE == MODE_GREEDY;
+  TempC tc{0.0f, 0.0f};
+  if (MODE == MODE_SAMPLE) {
+    const float T = P.temperature[b];
+    if (T == 0.0f) greedy = true;  // this request takes the greedy steps
+    else tc = temp_consts(sanitize_temperature(T, rflags));
+  }
+  const bool sample = MODE == MODE_SAMPLE && !greedy;
+  // every CTA decides: its warp 0 requests the draft inputs and the final
+  // draw's uniform before its items
+  DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
+  float u_fin = 0.0f;
+  unsigned int uflags = 0;
+  if (sample && warp == 0) {
+    gin = gather_drafts<EB>(P, A, gb);
+    u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
+  }
+
+  unsigned int issued = 0, processed = 0;  // copies started and consumed by this warp
+  bool failed = false;
+  // Start the copy of item m into the next buffer (lane 0 issues it).
+  auto issue = [&](const Meta& m) {
+    const int s = (int)(issued % kNB);
+    if (lane == 0) {
+      mymeta[s] = m;
+      unsigned char* dst = mybuf + s * kItemBytes;
+      if (m.direct) {
+        mbar_arrive(&mybar[s]);
+      } else {
+        const unsigned int bytes = (unsigned int)(m.n * EB);
+        const bool two = m.kind == KIND_R;
+        mbar_arrive_expect_tx(&mybar[s], two ? 2 * bytes : bytes);
+        bulk_copy_g2s(dst, m.p0, bytes, &mybar[s]);
+        if (two) bulk_copy_g2s(dst + kHalfBytes, m.p1, bytes, &mybar[s]);
+      }
+    }
+    __syncwarp();
+    ++issued;
+  };
+  // Wait for the oldest copy in flight; false after the bounded wait gave up.
+  auto wait_oldest = [&]() -> bool {
+    if (mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u)) return true;
+    flags |= SV_STATUS_TIMEOUT;
+    failed = true;
+    return false;
+  };
+
+  // ---- the A items
+  const int nrows = sample ? 2 * gb + 1 : gb + 1;
+  const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
+  auto a_meta = [&](unsigned int j) {
+    const int r = (int)(j / (unsigned int)NC), c = (int)(j % (unsigned int)NC);
+    Meta m;
+    size_t roff;
+    const char* rows;
+    if (r <= gb) {
+      m.pslot = r;
+      roff = (A.t0 + (size_t)r) * (size_t)V;
+      rows = P.target;
+    } else {
+      const int i = r - gb - 1;
+      m.pslot = G + 1 + i;
+      roff = (A.d0 + (size_t)i) * (size_t)V;
+      rows = P.draft;
+    }
+    m.kind = KIND_A;
+    m.b = b;
+    m.c = c;
+    m.n = min(AE, V - c * AE);
+    m.reject = 0;
+    m.pad = 0;
+    m.p0 = rows + (roff + (size_t)c * AE) * EB;
+    m.p1 = nullptr;
+    m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+    m.mt = m.md = m.inv_st = m.rho = 0.0f;
+    m.c_hi = tc.hi;
+    m.c_lo = tc.lo;
+    return m;
+  };
+  {
+    // lane r < C stores each partial into CTA r: every CTA decides locally
+    const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
+    auto store_part = [&](const Meta& m, float2 pr) {
+      if ((uint32_t)lane < C)
+        st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
+    };
+    unsigned int jn = gw;  // this warp's next item
+    while (true) {
+      while (issued - processed < (unsigned int)kNB && jn < nI) {
+        issue(a_meta(jn));
+        jn += W;
+      }
+      if (issued == processed || !wait_oldest()) break;
+      const Meta& m = mymeta[processed % kNB];
+      char* stage = reinterpret_cast<char*>(mybuf + (processed % kNB) * kItemBytes);
+      const bool padded = !m.direct && m.n < AE;  // a row's last chunk
+      if (sample && m.direct) stage_unaligned<EB>(m, stage);
+      else if (padded) pad_item_tail<EB>(stage, m.n);
+      store_part(m, sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage));
+      // stores into the buffer are ordered before the next bulk copy into it
+      if ((sample && m.direct) || padded) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      ++processed;
+    }
+    if (failed) {
+      // Every item of this warp still stores a partial, (NaN, 0) where it
+      // could not be read: every CTA then holds the same table and takes the
+      // same branches below.  Copies in flight are waited for (bounded).
+      for (; processed != issued; ++processed) {
+        (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
+        store_part(mymeta[processed % kNB], make_float2(NAN, 0.0f));
+        __syncwarp();
+      }
+      for (; jn < nI; jn += W) store_part(a_meta(jn), make_float2(NAN, 0.0f));
+    }
+  }
+  cluster_sync();  // every CTA holds every partial
+
+  // ---- the decision (as on the resident cluster path)
+  if (greedy && rank != 0) return;  // greedy: no further cluster work
+  if (warp == 0) {
+    float* rs = rsbuf;
+    const SharedParts sp{part, NC};
+    ClusterDec cd;
+    cd.k = 0;
+    cd.go = 0;
+    cd.mt = cd.md = cd.inv_st = cd.rho = 0.0f;
+    cd.c_hi = tc.hi;
+    cd.c_lo = tc.lo;
+    if (greedy) {
+      greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
+    } else {
+      Decision d;
+      d.k = 0;
+      d.reject = 0;
+      d.mt = d.md = d.inv_st = d.rho = 0.0f;
+      const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d, rank == 0);
+      cd.k = k;
+      cd.go = __shfl_sync(0xffffffffu, d.reject, 0);
+      cd.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+      cd.md = __shfl_sync(0xffffffffu, d.md, 0);
+      cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+      cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+      // every draft accepted: the leader draws the bonus token (this warp's
+      // copies are all consumed, so its buffers serve as staging)
+      if (k == gb && rank == 0) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], mybuf);
+    }
+    if (lane == 0) {
+      sdec = cd;
+      if (rank == 0 && rflags) atomicOr(P.status, rflags);
+    }
+  }
+  __syncthreads();  // the CTA's warps see its decision
+  const ClusterDec cd = sdec;
+
+  if (cd.go) {
+    // ---- the residual chunk sums of the rejected position k (k < gamma_b)
+    const int k = cd.k < 0 ? 0 : (cd.k > G ? G : cd.k);
+    const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
+    const char* drow = P.draft + (A.d0 + (size_t)k) * (size_t)V * EB;
+    auto r_meta = [&](unsigned int c) {
+      Meta m;
+      m.kind = KIND_R;
+      m.b = b;
+      m.pslot = k;
+      m.c = (int)c;
+      m.n = min(RE, V - (int)c * RE);
+      m.reject = 1;
+      m.pad = 0;
+      m.p0 = trow + (size_t)c * RE * EB;
+      m.p1 = drow + (size_t)c * RE * EB;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
+      m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.mt = cd.mt;
+      m.md = cd.md;
+      m.inv_st = cd.inv_st;
+      m.rho = cd.rho;
+      m.c_hi = cd.c_hi;
+      m.c_lo = cd.c_lo;
+      return m;
+    };
+    const uint32_t rsum0 = rank_addr(rsum, 0u);  // the leader's chunk sums
+    unsigned int jr = gw;                        // this warp's next chunk
+    while (!failed) {
+      while (issued - processed < (unsigned int)kNB && jr < (unsigned int)NCR) {
+        issue(r_meta(jr));
+        jr += W;
+      }
+      if (issued == processed || !wait_oldest()) break;
+      const Meta& m = mymeta[processed % kNB];
+      const unsigned long long sr =
+          r_item<EB>(m, reinterpret_cast<const char*>(mybuf + (processed % kNB) * kItemBytes));
+      if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)m.c * 8u, sr);
+      __syncwarp();
+      ++processed;
+    }
+    if (failed) {  // copies in flight are waited for (bounded); missing sums are 0
+      for (; processed != issued; ++processed) {
+        (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
+        if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % kNB].c * 8u, 0ull);
+        __syncwarp();
+      }
+      for (; jr < (unsigned int)NCR; jr += W)
+        if (lane == 0) st_cluster_u64(rsum0 + jr * 8u, 0ull);
+    }
+    cluster_sync();  // the leader holds every chunk sum
+
+    // ---- the final draw: the leader's warp 0 (its copies are all consumed)
+    if (rank == 0 && warp == 0) {
+      ResidC kc;
+      kc.mt = cd.mt; kc.md = cd.md; kc.inv_st = cd.inv_st; kc.rho = cd.rho;
+      resid_scales(kc);
+      kc.hi = cd.c_hi; kc.lo = cd.c_lo; kc.reject = 1;
+      int tok = chunk_draw<EB, false>(trow, drow, V, NCR, u_fin, kc, rsum, mybuf);
+      if (lane == 0) {
+        if (tok < 0) {
+          flags |= SV_STATUS_INTERNAL;
+          tok = V - 1;
+        }
+        P.out_tokens[(size_t)b * (G + 1) + k] = tok;
+        flags |= uflags;
+      }
+    }
+  }
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && any) atomicOr(P.status, any);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 int check_scalars(sv_dtype dtype, int B, int G, int V) {
@@ -2917,8 +3226,9 @@ int grid_size() {
   return cached_grid;
 }
 
-// Schedule of the next calls: SV_SCHEDULE_AUTO runs a batch that fits one
-// wave of clusters on the cluster path; SV_SCHEDULE_PERSISTENT forces the
+// Schedule policy of the next calls (SV_SCHEDULE_*): AUTO takes the first of
+// the resident cluster path, the streaming cluster path and the persistent
+// grid that applies; STREAM skips the resident path; PERSISTENT forces the
 // persistent grid (testing and benchmarking).
 std::atomic<int> g_schedule{SV_SCHEDULE_AUTO};
 
@@ -2929,16 +3239,23 @@ size_t cluster_tables(int G, int V, int eb) {
          sizeof(ClusterDec);
 }
 
-// Clusters of C CTAs (C <= kClusterMax) that fit on this device at once
-// (cached per device).
-template <int EB, int MODE, bool PK>
-int max_clusters(int C) {
-  static std::atomic<int> cached[kClusterMax + 1];  // (device + 1) << 16 | count; 0: none
+// Streaming cluster path: the partials and the leader's chunk sums.
+size_t stream_tables(int G, int V, int eb) {
+  const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
+  const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
+  return (size_t)(2 * G + 1) * nc * sizeof(float2) + ncr * sizeof(unsigned long long);
+}
+
+// Clusters of C CTAs (C <= kClusterMax) of kernel `kern` that fit on this
+// device at once, cached per device in cached[C] as (device + 1) << 16 | count
+// (0: not yet known).  Also sets the kernel's shared-memory and cluster-size
+// attributes for its launches.
+template <class Kern>
+int clusters_that_fit(Kern kern, int C, std::atomic<int>* cached) {
   int dev = 0;
   if (C < 1 || C > kClusterMax || cudaGetDevice(&dev) != cudaSuccess) return 0;
   const int c0 = cached[C].load(std::memory_order_relaxed);
   if ((c0 >> 16) == dev + 1) return c0 & 0xffff;
-  auto kern = cluster_kernel<EB, MODE, PK>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmem) ==
           cudaSuccess &&
@@ -2963,10 +3280,20 @@ int max_clusters(int C) {
   return n;
 }
 
-// Cluster size for this call, or 0 for the persistent grid.
+template <int EB, int MODE, bool PK>
+int max_clusters(int C) {
+  static std::atomic<int> cached[kClusterMax + 1];
+  return clusters_that_fit(cluster_kernel<EB, MODE, PK>, C, cached);
+}
+template <int EB, int MODE, bool PK>
+int max_stream_clusters(int C) {
+  static std::atomic<int> cached[kClusterMax + 1];
+  return clusters_that_fit(stream_kernel<EB, MODE, PK>, C, cached);
+}
+
+// Resident cluster path: the cluster size for this call, or 0.
 template <int EB, int MODE, bool PK>
 int cluster_route(int B, int G, int V) {
-  if (g_schedule.load() == SV_SCHEDULE_PERSISTENT) return 0;
   if (B < 1 || cluster_tables(G, V, EB) > (size_t)kClusterTables) return 0;
   const size_t nc = ((size_t)V + kItemBytes / EB - 1) / (kItemBytes / EB);
   // the largest cluster of which B fit at once (one wave: a request per
@@ -2994,10 +3321,56 @@ int launch_cluster(const Params& P, int C, cudaStream_t stream) {
   return SV_OK;
 }
 
+// Streaming cluster path: the largest cluster of which B fit at once (one
+// wave, a request per cluster), or 0.
+template <int EB, int MODE, bool PK>
+int stream_route(int B, int G, int V) {
+  if (B < 1 || stream_tables(G, V, EB) > (size_t)kClusterTables) return 0;
+  for (int C = kClusterMax; C >= 1; --C)
+    if (max_stream_clusters<EB, MODE, PK>(C) >= B) return C;
+  return 0;
+}
+
+struct Route {
+  int kind;  // SV_ROUTE_*
+  int C;     // cluster size (cluster paths)
+};
+template <int EB, int MODE, bool PK>
+Route route(int B, int G, int V) {
+  const int sched = g_schedule.load();
+  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0};
+  if (sched == SV_SCHEDULE_AUTO) {
+    const int C = cluster_route<EB, MODE, PK>(B, G, V);
+    if (C > 0) return Route{SV_ROUTE_CLUSTER, C};
+  }
+  const int C = stream_route<EB, MODE, PK>(B, G, V);
+  if (C > 0) return Route{SV_ROUTE_STREAM, C};
+  return Route{SV_ROUTE_PERSISTENT, 0};
+}
+
+template <int EB, int MODE, bool PK>
+int launch_stream(const Params& P, int C, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned int)(P.B * C));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)kWarps * kNB * kItemBytes + stream_tables(P.G, P.V, EB);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned int)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, stream_kernel<EB, MODE, PK>, P) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
-  const int C = cluster_route<EB, MODE, PK>(P.B, P.G, P.V);
-  if (C > 0) return launch_cluster<EB, MODE, PK>(P, C, stream);
+  const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
+  if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
+  if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK>(P, r.C, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch
@@ -3282,18 +3655,30 @@ const char* spec_verify_strerror(int code) {
 }
 
 int spec_verify_set_schedule(int schedule) {
-  if (schedule != SV_SCHEDULE_AUTO && schedule != SV_SCHEDULE_PERSISTENT) return SV_ERR_SCALAR;
+  if (schedule != SV_SCHEDULE_AUTO && schedule != SV_SCHEDULE_PERSISTENT &&
+      schedule != SV_SCHEDULE_STREAM)
+    return SV_ERR_SCALAR;
   return g_schedule.exchange(schedule);
 }
 
-int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy) {
+int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {
   const int rc = check_scalars(dtype, B, G, V);
   if (rc) return rc;
-  if (dtype == SV_BF16)
-    return greedy ? cluster_route<2, MODE_GREEDY, false>(B, G, V)
-                  : cluster_route<2, MODE_SAMPLE, false>(B, G, V);
-  return greedy ? cluster_route<4, MODE_GREEDY, false>(B, G, V)
-                : cluster_route<4, MODE_SAMPLE, false>(B, G, V);
+  Route r{SV_ROUTE_PERSISTENT, 0};
+  if (B > 0) {
+    if (dtype == SV_BF16)
+      r = greedy ? route<2, MODE_GREEDY, false>(B, G, V) : route<2, MODE_SAMPLE, false>(B, G, V);
+    else
+      r = greedy ? route<4, MODE_GREEDY, false>(B, G, V) : route<4, MODE_SAMPLE, false>(B, G, V);
+  }
+  if (cluster_size) *cluster_size = r.C;
+  return r.kind;
+}
+
+int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy) {
+  int C = 0;
+  const int rc = spec_verify_route(dtype, B, G, V, greedy, &C);
+  return rc < 0 ? rc : C;
 }
 
 }  // extern "C"

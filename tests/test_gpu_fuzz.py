@@ -1,10 +1,11 @@
-"""Seeded random shapes: both schedules bit for bit, and the oracle (GPU).
+"""Seeded random shapes: every schedule bit for bit, and the oracle (GPU).
 
 Each case draws B, G, V, the dtype, the layout, ragged draft lengths and
 per-request temperatures (some exactly 0, which take the greedy steps) from a
-fixed seed, runs the sampling call on the cluster schedule (when the shape
-allows it) and on the persistent grid, requires identical outputs, and
-compares them with the float64 oracle."""
+fixed seed, runs the sampling call under the automatic policy (the resident
+or the streaming cluster path, as the shape allows), on the streaming path
+and on the persistent grid, requires identical outputs, and compares them
+with the float64 oracle."""
 import os
 import random
 
@@ -62,11 +63,12 @@ def test_fuzz_sampling(i):
     B, G, V, dt, packed, temps = draw_case(i)
     w = W.make_random(B, G, V, dt, seed=100 + i, gamma="ragged", temperature=temps).to(DEV)
     a = run(w, packed, binding.SCHEDULE_AUTO)
-    b = run(w, packed, binding.SCHEDULE_PERSISTENT)
-    assert (a[0] == b[0]).all() and (a[1] == b[1]).all()
-    for x, y in ((a[2], b[2]), (a[3], b[3])):
-        nan = torch.isnan(y)
-        assert torch.equal(torch.isnan(x), nan) and torch.equal(x[~nan], y[~nan])
+    for sched in (binding.SCHEDULE_STREAM, binding.SCHEDULE_PERSISTENT):
+        b = run(w, packed, sched)
+        assert (a[0] == b[0]).all() and (a[1] == b[1]).all()
+        for x, y in ((a[2], b[2]), (a[3], b[3])):
+            nan = torch.isnan(y)
+            assert torch.equal(torch.isnan(x), nan) and torch.equal(x[~nan], y[~nan])
     ref = oracle.sample(**W.oracle_inputs(w), nthreads=NTHREADS)
     rep = compare_sample(ref, a[0], a[1], w.gamma.cpu().numpy(), a[2].numpy(), a[3].numpy())
     assert not rep.mismatches, (draw_case(i), rep.mismatches[:3])
@@ -85,7 +87,7 @@ def test_fuzz_greedy(i):
         for b in range(B):
             w.draft_tokens[b, int(w.gamma[b]):] = 0
     outs = []
-    for sched in (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT):
+    for sched in (binding.SCHEDULE_AUTO, binding.SCHEDULE_STREAM, binding.SCHEDULE_PERSISTENT):
         prev = binding.spec_verify_set_schedule(sched)
         try:
             v = binding.Verifier(B, G, V, DEV)
@@ -99,17 +101,20 @@ def test_fuzz_greedy(i):
             outs.append((v.out_tokens.cpu().numpy(), v.num_accepted.cpu().numpy()))
         finally:
             binding.spec_verify_set_schedule(prev)
-    assert (outs[0][0] == outs[1][0]).all() and (outs[0][1] == outs[1][1]).all()
+    for o in outs[1:]:
+        assert (outs[0][0] == o[0]).all() and (outs[0][1] == o[1]).all()
     ref = oracle.greedy(W.logits_numpy(w.target), w.draft_tokens.cpu().numpy(), w.gamma.cpu().numpy())
     bad = compare_greedy(ref, outs[0][0], outs[0][1])
     assert not bad, bad[:3]
 
 
-def test_fuzz_covers_both_schedules():
-    """The drawn shapes include batches on each schedule."""
+def test_fuzz_covers_both_cluster_paths():
+    """Under the automatic policy the drawn shapes include batches on the
+    resident and on the streaming cluster path (the persistent grid runs every
+    case by force)."""
     routes = set()
     for i in range(24):
         B, G, V, dt, _, _ = draw_case(i)
         tdt = torch.bfloat16 if dt == "bf16" else torch.float32
-        routes.add(binding.spec_verify_cluster_size(tdt, B, G, V) > 0)
-    assert routes == {True, False}
+        routes.add(binding.spec_verify_route(tdt, B, G, V)[0])
+    assert routes == {binding.ROUTE_CLUSTER, binding.ROUTE_STREAM}

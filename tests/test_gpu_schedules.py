@@ -1,8 +1,9 @@
-"""Cluster schedule (small batches) vs the persistent grid and the oracle (GPU).
+"""The three schedules against each other and the oracle (GPU).
 
-Both schedules compute every value with the same arithmetic, so their
-outputs must agree bit for bit; the cluster results are also compared with the
-float64 oracle."""
+The resident cluster path (small batches), the streaming cluster path
+(batches of up to one cluster per SM) and the persistent grid compute every
+value with the same arithmetic, so their outputs must agree bit for bit; the
+results are also compared with the float64 oracle."""
 import os
 
 import pytest
@@ -16,12 +17,13 @@ from speculative_decoding_verification_62_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 NTHREADS = os.cpu_count() or 1
+SCHEDULES = (binding.SCHEDULE_AUTO, binding.SCHEDULE_STREAM, binding.SCHEDULE_PERSISTENT)
 
 
-def sample_both(w, probs=True, packed=False):
-    """(cluster-schedule result, persistent result), each (out, nacc, p, q)."""
+def sample_all(w, probs=True, packed=False):
+    """[auto, stream, persistent] results, each (out, nacc, p, q)."""
     res = []
-    for sched in (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT):
+    for sched in SCHEDULES:
         prev = binding.spec_verify_set_schedule(sched)
         try:
             v = binding.Verifier(w.B, w.G, w.V, DEV)
@@ -47,6 +49,14 @@ def sample_both(w, probs=True, packed=False):
     return res
 
 
+def route(dt, B, G, V, greedy=False, sched=binding.SCHEDULE_AUTO):
+    prev = binding.spec_verify_set_schedule(sched)
+    try:
+        return binding.spec_verify_route(dt, B, G, V, greedy)
+    finally:
+        binding.spec_verify_set_schedule(prev)
+
+
 def same(a, b):
     (oa, na, pa, qa), (ob, nb, pb, qb) = a, b
     assert (oa == ob).all() and (na == nb).all()
@@ -56,6 +66,11 @@ def same(a, b):
         nan = torch.isnan(y)
         assert torch.equal(torch.isnan(x), nan)
         assert torch.equal(x[~nan], y[~nan])
+
+
+def all_same(res):
+    for r in res[1:]:
+        same(res[0], r)
 
 
 def against_oracle(w, res):
@@ -68,24 +83,29 @@ def against_oracle(w, res):
     assert rep.max_prob_rel_err < PROB_RTOL
 
 
-def test_small_batches_take_the_cluster_schedule():
-    """One wave of clusters whose warps hold one unit each of a request's work
-    (a unit: an 8 KB target chunk and the draft chunk of the same position)."""
+def test_routes():
+    """Resident clusters while a request's units fit one cluster's warps and the
+    batch one wave; streaming clusters up to one cluster per SM; the
+    persistent grid beyond."""
     bf, f32 = torch.bfloat16, torch.float32
+    R, S, P = binding.ROUTE_CLUSTER, binding.ROUTE_STREAM, binding.ROUTE_PERSISTENT
     for dt in (bf, f32):
-        assert binding.spec_verify_cluster_size(dt, 1, 4, 32000) > 0
-        assert binding.spec_verify_cluster_size(dt, 8, 3, 32000) > 0
-        assert binding.spec_verify_cluster_size(dt, 512, 3, 128256) == 0
-    assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) > 0
-    assert binding.spec_verify_cluster_size(bf, 8, 3, 128256, greedy=True) > 0
-    # too many units per request for one cluster: the persistent grid
-    assert binding.spec_verify_cluster_size(f32, 2, 3, 128256) == 0
-    assert binding.spec_verify_cluster_size(bf, 2, 31, 128256) == 0
-    prev = binding.spec_verify_set_schedule(binding.SCHEDULE_PERSISTENT)
-    try:
-        assert binding.spec_verify_cluster_size(torch.bfloat16, 8, 3, 128256) == 0
-    finally:
-        binding.spec_verify_set_schedule(prev)
+        assert route(dt, 1, 4, 32000)[0] == R
+        assert route(dt, 8, 3, 32000)[0] == R
+        assert route(dt, 512, 3, 128256) == (P, 0)
+    assert route(bf, 8, 3, 128256)[0] == R
+    assert route(bf, 8, 3, 128256, greedy=True)[0] == R
+    # too many units per request for one resident cluster: streaming
+    kind, C = route(f32, 2, 3, 128256)
+    assert kind == S and C >= 8
+    assert route(bf, 2, 31, 128256)[0] == S
+    kind, C = route(bf, 64, 5, 152064)
+    assert kind == S and C >= 2
+    # the policies
+    assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_STREAM)[0] == S
+    assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
+    assert binding.spec_verify_cluster_size(bf, 512, 3, 128256) == 0
+    assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) == route(bf, 8, 3, 128256)[1]
 
 
 CASES = [(8, 3, 128256, "bf16"), (5, 4, 20001, "bf16"), (3, 2, 4097, "f32"), (1, 4, 32000, "f32"),
@@ -93,33 +113,37 @@ CASES = [(8, 3, 128256, "bf16"), (5, 4, 20001, "bf16"), (3, 2, 4097, "f32"), (1,
 
 
 @pytest.mark.parametrize("B,G,V,dt", CASES)
-def test_cluster_sample_matches_persistent_and_oracle(B, G, V, dt):
+def test_schedules_sample_match_each_other_and_oracle(B, G, V, dt):
     temps = [0.6 + 0.15 * i for i in range(B)]
     w = W.make_random(B, G, V, dt, seed=B * 101 + V, gamma="ragged", temperature=temps).to(DEV)
     assert binding.spec_verify_cluster_size(w.target.dtype, B, G, V) > 0
-    a, b = sample_both(w)
-    same(a, b)
-    against_oracle(w, a)
+    res = sample_all(w)
+    all_same(res)
+    against_oracle(w, res[0])
 
 
-def test_cluster_full_size_config2():
-    w = W.make("2", device=DEV)
-    assert binding.spec_verify_cluster_size(w.target.dtype, w.B, w.G, w.V) > 0
-    a, b = sample_both(w)
-    same(a, b)
-    against_oracle(w, a)
+@pytest.mark.parametrize("name", ["2", "3"])
+def test_schedules_full_size(name):
+    """Config 2 (B=8) on the resident path, config 3 (B=64, gamma=5,
+    V=152064) on the streaming path, each against the other schedules."""
+    w = W.make(name, device=DEV)
+    kind = binding.spec_verify_route(w.target.dtype, w.B, w.G, w.V)[0]
+    assert kind == (binding.ROUTE_CLUSTER if name == "2" else binding.ROUTE_STREAM)
+    res = sample_all(w)
+    all_same(res)
+    against_oracle(w, res[0])
 
 
 def test_cluster_zero_temperature_and_packed():
     B, G, V = 6, 4, 30001
     temps = [0.0, 0.8, 1.3, 0.0, 0.5, 1.0]
     w = W.make_random(B, G, V, "bf16", seed=5, gamma=[4, 0, 2, 3, 4, 1], temperature=temps).to(DEV)
-    a, b = sample_both(w)
-    same(a, b)
-    against_oracle(w, a)
-    c, d = sample_both(w, packed=True)
-    same(c, d)
-    same(a, c)
+    res = sample_all(w)
+    all_same(res)
+    against_oracle(w, res[0])
+    resp = sample_all(w, packed=True)
+    all_same(resp)
+    same(res[0], resp[0])
 
 
 def test_cluster_rejections_and_bonus_both_occur():
@@ -127,15 +151,15 @@ def test_cluster_rejections_and_bonus_both_occur():
     B, G, V = 8, 3, 50000
     w = W.make_random(B, G, V, "bf16", seed=9, sigma_t=4.0, sigma_d=3.0).to(DEV)
     w.draft[::2] = w.target[::2, :G]  # even requests: q == p, every draft accepted
-    a, b = sample_both(w)
-    same(a, b)
-    nacc = a[1]
+    res = sample_all(w)
+    all_same(res)
+    nacc = res[0][1]
     assert (nacc[::2] == G).all() and (nacc[1::2] < G).any()
-    against_oracle(w, a)
+    against_oracle(w, res[0])
 
 
 @pytest.mark.parametrize("B,G,V,dt", [(8, 3, 128256, "bf16"), (5, 6, 20001, "f32"), (2, 0, 7, "bf16")])
-def test_cluster_greedy_matches_persistent_and_oracle(B, G, V, dt):
+def test_schedules_greedy_match_each_other_and_oracle(B, G, V, dt):
     w = W.make_random(B, G, V, dt, seed=B + V, gamma="ragged").to(DEV)
     if G:
         am = w.target[:, :G].float().argmax(dim=2).to(torch.int32)
@@ -144,7 +168,7 @@ def test_cluster_greedy_matches_persistent_and_oracle(B, G, V, dt):
         for b in range(B):
             w.draft_tokens[b, int(w.gamma[b]):] = 0
     outs = []
-    for sched in (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT):
+    for sched in SCHEDULES:
         prev = binding.spec_verify_set_schedule(sched)
         try:
             v = binding.Verifier(B, G, V, DEV)
@@ -154,7 +178,8 @@ def test_cluster_greedy_matches_persistent_and_oracle(B, G, V, dt):
             outs.append((v.out_tokens.cpu().numpy(), v.num_accepted.cpu().numpy()))
         finally:
             binding.spec_verify_set_schedule(prev)
-    assert (outs[0][0] == outs[1][0]).all() and (outs[0][1] == outs[1][1]).all()
+    for o in outs[1:]:
+        assert (outs[0][0] == o[0]).all() and (outs[0][1] == o[1]).all()
     ref = oracle.greedy(W.logits_numpy(w.target), w.draft_tokens.cpu().numpy(), w.gamma.cpu().numpy())
     bad = compare_greedy(ref, outs[0][0], outs[0][1])
     assert not bad, bad[:5]
@@ -167,7 +192,7 @@ def test_cluster_draft_sampler_matches_persistent():
     w = w.to(DEV)
     logits, u = w.target[:, 0].contiguous(), w.uniforms[:, 0].contiguous()
     toks = []
-    for sched in (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT):
+    for sched in SCHEDULES:
         prev = binding.spec_verify_set_schedule(sched)
         try:
             t = torch.full((B,), -5, dtype=torch.int32, device=DEV)
@@ -178,30 +203,35 @@ def test_cluster_draft_sampler_matches_persistent():
             toks.append(t.cpu())
         finally:
             binding.spec_verify_set_schedule(prev)
-    assert torch.equal(toks[0], toks[1])
+    assert torch.equal(toks[0], toks[1]) and torch.equal(toks[0], toks[2])
 
 
-def test_cluster_status_flags_and_reuse():
-    """Invalid device values are flagged on the cluster path too; repeated
+@pytest.mark.parametrize("sched", [binding.SCHEDULE_AUTO, binding.SCHEDULE_STREAM])
+def test_cluster_status_flags_and_reuse(sched):
+    """Invalid device values are flagged on the cluster paths too; repeated
     calls on one workspace keep it usable."""
     B, G, V = 4, 3, 5000
-    w = W.make_random(B, G, V, "bf16", seed=23).to(DEV)
-    w.gamma[1] = G + 5
-    w.draft_tokens[2, 0] = V + 3
-    v = binding.Verifier(B, G, V, DEV)
-    v.sample(w.target, w.draft, w.draft_tokens, w.gamma, w.uniforms, w.temperature)
-    torch.cuda.synchronize()
-    names = binding.status_names(binding.spec_verify_status(v.workspace))
-    assert "BAD_GAMMA" in names and "BAD_TOKEN" in names
-    w2 = W.make_random(B, G, V, "bf16", seed=24).to(DEV)
-    for _ in range(3):
-        v.sample(w2.target, w2.draft, w2.draft_tokens, w2.gamma, w2.uniforms, w2.temperature)
-    torch.cuda.synchronize()
-    assert binding.spec_verify_status(v.workspace) == 0
+    prev = binding.spec_verify_set_schedule(sched)
+    try:
+        w = W.make_random(B, G, V, "bf16", seed=23).to(DEV)
+        w.gamma[1] = G + 5
+        w.draft_tokens[2, 0] = V + 3
+        v = binding.Verifier(B, G, V, DEV)
+        v.sample(w.target, w.draft, w.draft_tokens, w.gamma, w.uniforms, w.temperature)
+        torch.cuda.synchronize()
+        names = binding.status_names(binding.spec_verify_status(v.workspace))
+        assert "BAD_GAMMA" in names and "BAD_TOKEN" in names
+        w2 = W.make_random(B, G, V, "bf16", seed=24).to(DEV)
+        for _ in range(3):
+            v.sample(w2.target, w2.draft, w2.draft_tokens, w2.gamma, w2.uniforms, w2.temperature)
+        torch.cuda.synchronize()
+        assert binding.spec_verify_status(v.workspace) == 0
+    finally:
+        binding.spec_verify_set_schedule(prev)
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_vanished_residual_falls_back_to_p_on_both_schedules(dt):
+def test_vanished_residual_falls_back_to_p_on_every_schedule(dt):
     """A clear rejection whose residual mass is below the fixed-point
     resolution: the drafted token x has q(x) = 2 p(x) with p(x) ~ e^-40 and
     the target and draft rows agree elsewhere, so u = 0.9 rejects (ratio 1/2)
@@ -219,9 +249,9 @@ def test_vanished_residual_falls_back_to_p_on_both_schedules(dt):
     w.uniforms[:, 0] = 0.9
     w.temperature[:] = 1.0
     w = w.to(DEV)
-    res = sample_both(w, probs=False)
+    res = sample_all(w, probs=False)
     assert binding.spec_verify_cluster_size(w.target.dtype, B, G, V) > 0
-    same(res[0], res[1])
+    all_same(res)
     out, nacc = res[0][0], res[0][1]
     assert (nacc == 0).all()
     p = torch.softmax(w.target[:, 0].double(), dim=1).cpu()
@@ -230,17 +260,21 @@ def test_vanished_residual_falls_back_to_p_on_both_schedules(dt):
         assert out[b, 1] == -1
 
 
-def test_batch_at_the_cluster_wave_limit():
-    """The largest batch that fits one wave of clusters runs on the cluster
-    schedule, one more request runs on the persistent grid; both match the
-    oracle."""
-    G, V = 2, 32000
-    limit = max(B for B in range(1, 65)
-                if binding.spec_verify_cluster_size(torch.bfloat16, B, G, V) > 0)
-    assert binding.spec_verify_cluster_size(torch.bfloat16, limit + 1, G, V) == 0
-    for B in (limit, limit + 1):
+def test_batches_at_the_wave_limits():
+    """The largest batch that fits one wave of resident clusters runs on the
+    resident path and one more request on the streaming path; the largest
+    batch of the streaming path (one cluster per SM at least) and one more
+    (the persistent grid).  Each matches the other schedules and the oracle."""
+    G, V, bf = 2, 32000, torch.bfloat16
+    kinds = {B: binding.spec_verify_route(bf, B, G, V)[0] for B in range(1, 161)}
+    res_limit = max(B for B, k in kinds.items() if k == binding.ROUTE_CLUSTER)
+    str_limit = max(B for B, k in kinds.items() if k == binding.ROUTE_STREAM)
+    assert kinds[res_limit + 1] == binding.ROUTE_STREAM
+    assert kinds[str_limit + 1] == binding.ROUTE_PERSISTENT
+    assert str_limit >= 64
+    for B in (res_limit, res_limit + 1, str_limit, str_limit + 1):
         w = W.make_random(B, G, V, "bf16", seed=B, gamma="ragged",
-                          temperature=[0.7 + 0.02 * i for i in range(B)]).to(DEV)
-        a, b = sample_both(w)
-        same(a, b)
-        against_oracle(w, a)
+                          temperature=[0.7 + 0.002 * i for i in range(B)]).to(DEV)
+        res = sample_all(w)
+        all_same(res)
+        against_oracle(w, res[0])
