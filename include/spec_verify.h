@@ -255,9 +255,12 @@ const char *spec_verify_strerror(int code);
  *   - the streaming cluster path: one cluster per request as well, for batches
  *     of up to one cluster per SM (clusters of up to 16 CTAs, at least one),
  *     the warps streaming the request's chunks two at a time and re-reading
- *     the rejected row's chunks for the residual;
- *   - the persistent grid, for larger batches: items claimed from global
- *     counters, decisions published through global records.
+ *     the rejected row's chunks for the residual.  For larger greedy batches
+ *     (and any larger batch under SV_SCHEDULE_STREAM) two CTAs per SM take
+ *     whole requests in turn from a claim counter;
+ *   - the persistent grid, for larger sampling batches: chunks claimed from
+ *     global counters, decisions published through global records, which
+ *     balances ragged draft lengths chunk by chunk.
  * The cluster paths replace the persistent grid's chain of global-memory
  * synchronisations (arrival counters, decision records, queue) with cluster
  * barriers.  These calls are not steps of the method: they exist for testing
@@ -265,10 +268,11 @@ const char *spec_verify_strerror(int code);
  *
  * spec_verify_set_schedule: the policy for the calls that follow in this
  * process: SV_SCHEDULE_AUTO (the default: the first of the resident cluster
- * path, the streaming cluster path and the persistent grid that applies),
- * SV_SCHEDULE_PERSISTENT (every call on the persistent grid) or
- * SV_SCHEDULE_STREAM (never the resident path).  Returns the previous policy,
- * or SV_ERR_SCALAR for an unknown value.
+ * path, the streaming cluster path and the persistent grid that applies, as
+ * above), SV_SCHEDULE_PERSISTENT (every call on the persistent grid) or
+ * SV_SCHEDULE_STREAM (the streaming path wherever its tables fit, claims
+ * included).  Returns the previous policy, or SV_ERR_SCALAR for an unknown
+ * value.
  *
  * spec_verify_route: the kernel (SV_ROUTE_*) that the next sampling
  * (greedy == 0) or greedy call of this shape, in the padded layout, on the

@@ -2919,66 +2919,52 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 // decision.  After a reject the warps stream row k's R chunks (target and
 // draft halves, usually L2 hits) and store each chunk's fixed-point sum in
 // the leader's shared memory; after a second barrier the leader's warp 0
-// draws from those sums and walks one chunk.  No global counter, record or
-// queue is involved.  Shared memory: the buffers, then (the same layout in
-// every CTA) the partials [2G+1][NC] and the leader's chunk sums [NCR].
-template <int EB, int MODE, bool PK>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(Params P) {
+// draws from those sums and walks one chunk.  With at most one request per
+// cluster no global counter, record or queue is involved.  With more requests
+// than clusters (clusters of one CTA) each CTA takes its requests one after
+// another: the first by its index, the next from a global counter, claimed
+// while the current one is decided; the other warps start the next request's
+// items while warp 0 draws.  Shared memory: the buffers, then (the same
+// layout in every CTA) the partials [2G+1][NC] and the leader's chunk sums
+// [NCR].  NW warps per CTA: kWarps (one CTA per SM), or kWarps / 2 for
+// claimed requests (two CTAs per SM, so that one CTA's decision and residual
+// steps overlap the other's streaming).
+template <int EB, int MODE, bool PK, int NW>
+__global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) {
+  static_assert(NW >= 1 && kWarps % NW == 0, "CTAs of NW warps share an SM's warps");
   extern __shared__ __align__(128) unsigned char dsmem[];
-  __shared__ __align__(8) uint64_t bar[kWarps][kNB];
-  __shared__ Meta smeta[kWarps][kNB];  // the item in each buffer
+  __shared__ __align__(8) uint64_t bar[NW][kNB];
+  __shared__ Meta smeta[NW][kNB];  // the item in each buffer
   __shared__ float rsbuf[192];         // the decision's row statistics
   __shared__ ClusterDec sdec;
+  __shared__ int s_next, s_last;       // the CTA's next request; last CTA out
   constexpr int AE = kItemBytes / EB;   // logits per A item
   constexpr int RE = kHalfBytes / EB;   // logits per R chunk and row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank(), C = cluster_size();
-  const int b = (int)cluster_index();
+  const int nq = (int)(gridDim.x / C);  // clusters
+  const bool queue = P.B > nq;          // requests claimed in turn (clusters of one CTA)
   const int G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
-  float2* part = reinterpret_cast<float2*>(dsmem + (size_t)kWarps * kNB * kItemBytes);
+  float2* part = reinterpret_cast<float2*>(dsmem + (size_t)NW * kNB * kItemBytes);
   unsigned long long* rsum = reinterpret_cast<unsigned long long*>(part + (size_t)(2 * G + 1) * NC);
   unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
   uint64_t* mybar = bar[warp];
   Meta* mymeta = smeta[warp];
-  const unsigned int gw = rank * kWarps + (unsigned int)warp, W = C * kWarps;
+  const unsigned int gw = rank * NW + (unsigned int)warp, W = C * NW;
 
+  if (queue && C != 1) {  // claims are made for clusters of one CTA only
+    if (tid == 0 && rank == 0) atomicOr(P.status, SV_STATUS_INTERNAL);
+    return;
+  }
   if (lane == 0) {
     for (int s = 0; s < kNB; ++s) mbar_init(&mybar[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
 
-  // the request: draft length, addresses, temperature constants
-  unsigned int rflags = 0, flags = 0;
-  int gb = 0, base = 0;
-  if constexpr (PK) {
-    base = packed_base(P, b, gb, rflags);
-  } else {
-    const int g_in = P.gamma ? P.gamma[b] : 0;
-    gb = clamp_gamma(g_in, G);
-    if (g_in != gb) rflags |= SV_STATUS_BAD_GAMMA;
-  }
-  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
-  bool greedy = MODE == MODE_GREEDY;
-  TempC tc{0.0f, 0.0f};
-  if (MODE == MODE_SAMPLE) {
-    const float T = P.temperature[b];
-    if (T == 0.0f) greedy = true;  // this request takes the greedy steps
-    else tc = temp_consts(sanitize_temperature(T, rflags));
-  }
-  const bool sample = MODE == MODE_SAMPLE && !greedy;
-  // every CTA decides: its warp 0 requests the draft inputs and the final
-  // draw's uniform before its items
-  DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
-  float u_fin = 0.0f;
-  unsigned int uflags = 0;
-  if (sample && warp == 0) {
-    gin = gather_drafts<EB>(P, A, gb);
-    u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
-  }
-
   unsigned int issued = 0, processed = 0;  // copies started and consumed by this warp
   bool failed = false;
+  unsigned int flags = 0;
   // Start the copy of item m into the next buffer (lane 0 issues it).
   auto issue = [&](const Meta& m) {
     const int s = (int)(issued % kNB);
@@ -3006,185 +2992,235 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Params P) {
     return false;
   };
 
-  // ---- the A items
-  const int nrows = sample ? 2 * gb + 1 : gb + 1;
-  const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
-  auto a_meta = [&](unsigned int j) {
-    const int r = (int)(j / (unsigned int)NC), c = (int)(j % (unsigned int)NC);
-    Meta m;
-    size_t roff;
-    const char* rows;
-    if (r <= gb) {
-      m.pslot = r;
-      roff = (A.t0 + (size_t)r) * (size_t)V;
-      rows = P.target;
+  for (int b = (int)cluster_index(); b < P.B;) {
+    // the request: draft length, addresses, temperature constants
+    unsigned int rflags = 0;
+    int gb = 0, base = 0;
+    if constexpr (PK) {
+      base = packed_base(P, b, gb, rflags);
     } else {
-      const int i = r - gb - 1;
-      m.pslot = G + 1 + i;
-      roff = (A.d0 + (size_t)i) * (size_t)V;
-      rows = P.draft;
+      const int g_in = P.gamma ? P.gamma[b] : 0;
+      gb = clamp_gamma(g_in, G);
+      if (g_in != gb) rflags |= SV_STATUS_BAD_GAMMA;
     }
-    m.kind = KIND_A;
-    m.b = b;
-    m.c = c;
-    m.n = min(AE, V - c * AE);
-    m.reject = 0;
-    m.pad = 0;
-    m.p0 = rows + (roff + (size_t)c * AE) * EB;
-    m.p1 = nullptr;
-    m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-    m.mt = m.md = m.inv_st = m.rho = 0.0f;
-    m.c_hi = tc.hi;
-    m.c_lo = tc.lo;
-    return m;
-  };
-  {
-    // lane r < C stores each partial into CTA r: every CTA decides locally
-    const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
-    auto store_part = [&](const Meta& m, float2 pr) {
-      if ((uint32_t)lane < C)
-        st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
-    };
-    unsigned int jn = gw;  // this warp's next item
-    while (true) {
-      while (issued - processed < (unsigned int)kNB && jn < nI) {
-        issue(a_meta(jn));
-        jn += W;
-      }
-      if (issued == processed || !wait_oldest()) break;
-      const Meta& m = mymeta[processed % kNB];
-      char* stage = reinterpret_cast<char*>(mybuf + (processed % kNB) * kItemBytes);
-      const bool padded = !m.direct && m.n < AE;  // a row's last chunk
-      if (sample && m.direct) stage_unaligned<EB>(m, stage);
-      else if (padded) pad_item_tail<EB>(stage, m.n);
-      store_part(m, sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage));
-      // stores into the buffer are ordered before the next bulk copy into it
-      if ((sample && m.direct) || padded) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      ++processed;
+    const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+    bool greedy = MODE == MODE_GREEDY;
+    TempC tc{0.0f, 0.0f};
+    if (MODE == MODE_SAMPLE) {
+      const float T = P.temperature[b];
+      if (T == 0.0f) greedy = true;  // this request takes the greedy steps
+      else tc = temp_consts(sanitize_temperature(T, rflags));
     }
-    if (failed) {
-      // Every item of this warp still stores a partial, (NaN, 0) where it
-      // could not be read: every CTA then holds the same table and takes the
-      // same branches below.  Copies in flight are waited for (bounded).
-      for (; processed != issued; ++processed) {
-        (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
-        store_part(mymeta[processed % kNB], make_float2(NAN, 0.0f));
-        __syncwarp();
-      }
-      for (; jn < nI; jn += W) store_part(a_meta(jn), make_float2(NAN, 0.0f));
+    const bool sample = MODE == MODE_SAMPLE && !greedy;
+    // every CTA decides: its warp 0 requests the draft inputs and the final
+    // draw's uniform before its items
+    DraftIn gin{0, 0.0f, 0.0f, 0.0f, 0u};
+    float u_fin = 0.0f;
+    unsigned int uflags = 0;
+    if (sample && warp == 0) {
+      gin = gather_drafts<EB>(P, A, gb);
+      u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
     }
-  }
-  cluster_sync();  // every CTA holds every partial
 
-  // ---- the decision (as on the resident cluster path)
-  if (greedy && rank != 0) return;  // greedy: no further cluster work
-  if (warp == 0) {
-    float* rs = rsbuf;
-    const SharedParts sp{part, NC};
-    ClusterDec cd;
-    cd.k = 0;
-    cd.go = 0;
-    cd.mt = cd.md = cd.inv_st = cd.rho = 0.0f;
-    cd.c_hi = tc.hi;
-    cd.c_lo = tc.lo;
-    if (greedy) {
-      greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
-    } else {
-      Decision d;
-      d.k = 0;
-      d.reject = 0;
-      d.mt = d.md = d.inv_st = d.rho = 0.0f;
-      const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d, rank == 0);
-      cd.k = k;
-      cd.go = __shfl_sync(0xffffffffu, d.reject, 0);
-      cd.mt = __shfl_sync(0xffffffffu, d.mt, 0);
-      cd.md = __shfl_sync(0xffffffffu, d.md, 0);
-      cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
-      cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
-      // every draft accepted: the leader draws the bonus token (this warp's
-      // copies are all consumed, so its buffers serve as staging)
-      if (k == gb && rank == 0) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], mybuf);
-    }
-    if (lane == 0) {
-      sdec = cd;
-      if (rank == 0 && rflags) atomicOr(P.status, rflags);
-    }
-  }
-  __syncthreads();  // the CTA's warps see its decision
-  const ClusterDec cd = sdec;
-
-  if (cd.go) {
-    // ---- the residual chunk sums of the rejected position k (k < gamma_b)
-    const int k = cd.k < 0 ? 0 : (cd.k > G ? G : cd.k);
-    const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
-    const char* drow = P.draft + (A.d0 + (size_t)k) * (size_t)V * EB;
-    auto r_meta = [&](unsigned int c) {
+    // ---- the A items
+    const int nrows = sample ? 2 * gb + 1 : gb + 1;
+    const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
+    auto a_meta = [&](unsigned int j) {
+      const int r = (int)(j / (unsigned int)NC), c = (int)(j % (unsigned int)NC);
       Meta m;
-      m.kind = KIND_R;
+      size_t roff;
+      const char* rows;
+      if (r <= gb) {
+        m.pslot = r;
+        roff = (A.t0 + (size_t)r) * (size_t)V;
+        rows = P.target;
+      } else {
+        const int i = r - gb - 1;
+        m.pslot = G + 1 + i;
+        roff = (A.d0 + (size_t)i) * (size_t)V;
+        rows = P.draft;
+      }
+      m.kind = KIND_A;
       m.b = b;
-      m.pslot = k;
-      m.c = (int)c;
-      m.n = min(RE, V - (int)c * RE);
-      m.reject = 1;
+      m.c = c;
+      m.n = min(AE, V - c * AE);
+      m.reject = 0;
       m.pad = 0;
-      m.p0 = trow + (size_t)c * RE * EB;
-      m.p1 = drow + (size_t)c * RE * EB;
-      const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
-      m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-      m.mt = cd.mt;
-      m.md = cd.md;
-      m.inv_st = cd.inv_st;
-      m.rho = cd.rho;
-      m.c_hi = cd.c_hi;
-      m.c_lo = cd.c_lo;
+      m.p0 = rows + (roff + (size_t)c * AE) * EB;
+      m.p1 = nullptr;
+      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.mt = m.md = m.inv_st = m.rho = 0.0f;
+      m.c_hi = tc.hi;
+      m.c_lo = tc.lo;
       return m;
     };
-    const uint32_t rsum0 = rank_addr(rsum, 0u);  // the leader's chunk sums
-    unsigned int jr = gw;                        // this warp's next chunk
-    while (!failed) {
-      while (issued - processed < (unsigned int)kNB && jr < (unsigned int)NCR) {
-        issue(r_meta(jr));
-        jr += W;
-      }
-      if (issued == processed || !wait_oldest()) break;
-      const Meta& m = mymeta[processed % kNB];
-      const unsigned long long sr =
-          r_item<EB>(m, reinterpret_cast<const char*>(mybuf + (processed % kNB) * kItemBytes));
-      if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)m.c * 8u, sr);
-      __syncwarp();
-      ++processed;
-    }
-    if (failed) {  // copies in flight are waited for (bounded); missing sums are 0
-      for (; processed != issued; ++processed) {
-        (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
-        if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % kNB].c * 8u, 0ull);
-        __syncwarp();
-      }
-      for (; jr < (unsigned int)NCR; jr += W)
-        if (lane == 0) st_cluster_u64(rsum0 + jr * 8u, 0ull);
-    }
-    cluster_sync();  // the leader holds every chunk sum
-
-    // ---- the final draw: the leader's warp 0 (its copies are all consumed)
-    if (rank == 0 && warp == 0) {
-      ResidC kc;
-      kc.mt = cd.mt; kc.md = cd.md; kc.inv_st = cd.inv_st; kc.rho = cd.rho;
-      resid_scales(kc);
-      kc.hi = cd.c_hi; kc.lo = cd.c_lo; kc.reject = 1;
-      int tok = chunk_draw<EB, false>(trow, drow, V, NCR, u_fin, kc, rsum, mybuf);
-      if (lane == 0) {
-        if (tok < 0) {
-          flags |= SV_STATUS_INTERNAL;
-          tok = V - 1;
+    {
+      // lane r < C stores each partial into CTA r: every CTA decides locally
+      const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
+      auto store_part = [&](const Meta& m, float2 pr) {
+        if ((uint32_t)lane < C)
+          st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
+      };
+      unsigned int jn = gw;  // this warp's next item
+      while (!failed) {
+        while (issued - processed < (unsigned int)kNB && jn < nI) {
+          issue(a_meta(jn));
+          jn += W;
         }
-        P.out_tokens[(size_t)b * (G + 1) + k] = tok;
-        flags |= uflags;
+        if (issued == processed || !wait_oldest()) break;
+        const Meta& m = mymeta[processed % kNB];
+        char* stage = reinterpret_cast<char*>(mybuf + (processed % kNB) * kItemBytes);
+        const bool padded = !m.direct && m.n < AE;  // a row's last chunk
+        if (sample && m.direct) stage_unaligned<EB>(m, stage);
+        else if (padded) pad_item_tail<EB>(stage, m.n);
+        store_part(m, sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage));
+        // stores into the buffer are ordered before the next bulk copy into it
+        if ((sample && m.direct) || padded) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        ++processed;
+      }
+      if (failed) {
+        // Every item of this warp still stores a partial, (NaN, 0) where it
+        // could not be read: every CTA then holds the same table and takes the
+        // same branches below.  Copies in flight are waited for (bounded).
+        for (; processed != issued; ++processed) {
+          (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
+          store_part(mymeta[processed % kNB], make_float2(NAN, 0.0f));
+          __syncwarp();
+        }
+        for (; jn < nI; jn += W) store_part(a_meta(jn), make_float2(NAN, 0.0f));
       }
     }
-  }
+    cluster_sync();  // every CTA holds every partial
+
+    // ---- the decision (as on the resident cluster path)
+    // greedy: no further cluster work (with claims, C == 1: every CTA leads)
+    if (greedy && rank != 0) return;
+    if (warp == 0) {
+      // queue: the next request is claimed now, its latency hidden by the decision
+      if (lane == 0) s_next = queue ? (int)atomicAdd(P.next_item, 1u) + nq : P.B;
+      float* rs = rsbuf;
+      const SharedParts sp{part, NC};
+      ClusterDec cd;
+      cd.k = 0;
+      cd.go = 0;
+      cd.mt = cd.md = cd.inv_st = cd.rho = 0.0f;
+      cd.c_hi = tc.hi;
+      cd.c_lo = tc.lo;
+      if (greedy) {
+        greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
+      } else {
+        Decision d;
+        d.k = 0;
+        d.reject = 0;
+        d.mt = d.md = d.inv_st = d.rho = 0.0f;
+        const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d, rank == 0);
+        cd.k = k;
+        cd.go = __shfl_sync(0xffffffffu, d.reject, 0);
+        cd.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+        cd.md = __shfl_sync(0xffffffffu, d.md, 0);
+        cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+        cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+        // every draft accepted: the leader draws the bonus token (this warp's
+        // copies are all consumed, so its buffers serve as staging)
+        if (k == gb && rank == 0) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], mybuf);
+      }
+      if (lane == 0) {
+        sdec = cd;
+        if (rank == 0 && rflags) atomicOr(P.status, rflags);
+      }
+    }
+    __syncthreads();  // the CTA's warps see its decision
+    const ClusterDec cd = sdec;
+    const int next = s_next;
+
+    if (cd.go) {
+      // ---- the residual chunk sums of the rejected position k (k < gamma_b)
+      const int k = cd.k < 0 ? 0 : (cd.k > G ? G : cd.k);
+      const char* trow = P.target + (A.t0 + (size_t)k) * (size_t)V * EB;
+      const char* drow = P.draft + (A.d0 + (size_t)k) * (size_t)V * EB;
+      auto r_meta = [&](unsigned int c) {
+        Meta m;
+        m.kind = KIND_R;
+        m.b = b;
+        m.pslot = k;
+        m.c = (int)c;
+        m.n = min(RE, V - (int)c * RE);
+        m.reject = 1;
+        m.pad = 0;
+        m.p0 = trow + (size_t)c * RE * EB;
+        m.p1 = drow + (size_t)c * RE * EB;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
+        m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+        m.mt = cd.mt;
+        m.md = cd.md;
+        m.inv_st = cd.inv_st;
+        m.rho = cd.rho;
+        m.c_hi = cd.c_hi;
+        m.c_lo = cd.c_lo;
+        return m;
+      };
+      const uint32_t rsum0 = rank_addr(rsum, 0u);  // the leader's chunk sums
+      unsigned int jr = gw;                        // this warp's next chunk
+      while (!failed) {
+        while (issued - processed < (unsigned int)kNB && jr < (unsigned int)NCR) {
+          issue(r_meta(jr));
+          jr += W;
+        }
+        if (issued == processed || !wait_oldest()) break;
+        const Meta& m = mymeta[processed % kNB];
+        const unsigned long long sr =
+            r_item<EB>(m, reinterpret_cast<const char*>(mybuf + (processed % kNB) * kItemBytes));
+        if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)m.c * 8u, sr);
+        __syncwarp();
+        ++processed;
+      }
+      if (failed) {  // copies in flight are waited for (bounded); missing sums are 0
+        for (; processed != issued; ++processed) {
+          (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
+          if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % kNB].c * 8u, 0ull);
+          __syncwarp();
+        }
+        for (; jr < (unsigned int)NCR; jr += W)
+          if (lane == 0) st_cluster_u64(rsum0 + jr * 8u, 0ull);
+      }
+      cluster_sync();  // the leader holds every chunk sum
+
+      // ---- the final draw: the leader's warp 0 (its copies are all consumed)
+      if (rank == 0 && warp == 0) {
+        ResidC kc;
+        kc.mt = cd.mt; kc.md = cd.md; kc.inv_st = cd.inv_st; kc.rho = cd.rho;
+        resid_scales(kc);
+        kc.hi = cd.c_hi; kc.lo = cd.c_lo; kc.reject = 1;
+        int tok = chunk_draw<EB, false>(trow, drow, V, NCR, u_fin, kc, rsum, mybuf);
+        if (lane == 0) {
+          if (tok < 0) {
+            flags |= SV_STATUS_INTERNAL;
+            tok = V - 1;
+          }
+          P.out_tokens[(size_t)b * (G + 1) + k] = tok;
+          flags |= uflags;
+        }
+      }
+    }
+    b = next;
+  }  // requests
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && any) atomicOr(P.status, any);
+  if (queue) {
+    // the last CTA out resets the claim counter for the next call
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      s_last = atomicAdd(P.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last && tid == 0) {
+      *P.next_item = 0;
+      *P.exit_count = 0;
+      __threadfence();
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -3251,20 +3287,21 @@ size_t stream_tables(int G, int V, int eb) {
 // (0: not yet known).  Also sets the kernel's shared-memory and cluster-size
 // attributes for its launches.
 template <class Kern>
-int clusters_that_fit(Kern kern, int C, std::atomic<int>* cached) {
+int clusters_that_fit(Kern kern, int C, std::atomic<int>* cached, int threads = kThreads,
+                      size_t smem = kClusterSmem) {
   int dev = 0;
   if (C < 1 || C > kClusterMax || cudaGetDevice(&dev) != cudaSuccess) return 0;
   const int c0 = cached[C].load(std::memory_order_relaxed);
   if ((c0 >> 16) == dev + 1) return c0 & 0xffff;
   int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmem) ==
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
           cudaSuccess &&
       (C <= 8 || cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                      cudaSuccess)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned int)C);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kClusterSmem;
+    cfg.blockDim = dim3((unsigned int)threads);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned int)C;
@@ -3285,11 +3322,26 @@ int max_clusters(int C) {
   static std::atomic<int> cached[kClusterMax + 1];
   return clusters_that_fit(cluster_kernel<EB, MODE, PK>, C, cached);
 }
-template <int EB, int MODE, bool PK>
+// Streaming kernel with NW warps per CTA: the cap on its tables and its
+// largest dynamic shared memory.  Two CTAs of kWarps / 2 warps share an SM
+// (228 KB of shared memory, 1 KB of it reserved per CTA), which leaves them
+// 12 KB of tables each.
+template <int NW>
+constexpr size_t stream_table_cap() {
+  return NW == kWarps ? (size_t)kClusterTables : (size_t)12 * 1024;
+}
+template <int NW>
+constexpr size_t stream_smem() {
+  return (size_t)NW * kNB * kItemBytes + stream_table_cap<NW>();
+}
+static_assert(2 * (stream_smem<kWarps / 2>() + 3 * 1024) <= 228 * 1024,
+              "two claiming CTAs per SM (with about 2 KB of static shared memory each)");
+template <int EB, int MODE, bool PK, int NW>
 int max_stream_clusters(int C) {
   static std::atomic<int> cached[kClusterMax + 1];
-  return clusters_that_fit(stream_kernel<EB, MODE, PK>, C, cached);
+  return clusters_that_fit(stream_kernel<EB, MODE, PK, NW>, C, cached, NW * 32, stream_smem<NW>());
 }
+constexpr int kClaimWarps = kWarps / 2;  // warps per CTA of the claiming streaming kernel
 
 // Resident cluster path: the cluster size for this call, or 0.
 template <int EB, int MODE, bool PK>
@@ -3321,39 +3373,53 @@ int launch_cluster(const Params& P, int C, cudaStream_t stream) {
   return SV_OK;
 }
 
-// Streaming cluster path: the largest cluster of which B fit at once (one
-// wave, a request per cluster), or 0.
-template <int EB, int MODE, bool PK>
-int stream_route(int B, int G, int V) {
-  if (B < 1 || stream_tables(G, V, EB) > (size_t)kClusterTables) return 0;
-  for (int C = kClusterMax; C >= 1; --C)
-    if (max_stream_clusters<EB, MODE, PK>(C) >= B) return C;
-  return 0;
-}
-
 struct Route {
   int kind;  // SV_ROUTE_*
   int C;     // cluster size (cluster paths)
+  int Q;     // clusters launched (cluster paths)
+  int nw;    // warps per CTA (streaming path)
 };
+
+// Streaming cluster path: the largest cluster of which B fit at once (one
+// wave, a request per cluster); with `claims`, a batch beyond one wave of
+// single-CTA clusters runs on as many CTAs of kClaimWarps warps as fit (two
+// per SM), each claiming requests in turn.
 template <int EB, int MODE, bool PK>
-Route route(int B, int G, int V) {
-  const int sched = g_schedule.load();
-  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0};
-  if (sched == SV_SCHEDULE_AUTO) {
-    const int C = cluster_route<EB, MODE, PK>(B, G, V);
-    if (C > 0) return Route{SV_ROUTE_CLUSTER, C};
-  }
-  const int C = stream_route<EB, MODE, PK>(B, G, V);
-  if (C > 0) return Route{SV_ROUTE_STREAM, C};
-  return Route{SV_ROUTE_PERSISTENT, 0};
+Route stream_route(int B, int G, int V, bool claims) {
+  const Route none{SV_ROUTE_PERSISTENT, 0, 0, 0};
+  if (B < 1 || stream_tables(G, V, EB) > stream_table_cap<kWarps>()) return none;
+  for (int C = kClusterMax; C >= 1; --C)
+    if (max_stream_clusters<EB, MODE, PK, kWarps>(C) >= B) return Route{SV_ROUTE_STREAM, C, B, kWarps};
+  if (!claims || stream_tables(G, V, EB) > stream_table_cap<kClaimWarps>()) return none;
+  const int Q = max_stream_clusters<EB, MODE, PK, kClaimWarps>(1);
+  return Q > 0 ? Route{SV_ROUTE_STREAM, 1, Q, kClaimWarps} : none;
 }
 
 template <int EB, int MODE, bool PK>
-int launch_stream(const Params& P, int C, cudaStream_t stream) {
+Route route(int B, int G, int V) {
+  const int sched = g_schedule.load();
+  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0, 0};
+  if (sched == SV_SCHEDULE_AUTO) {
+    const int C = cluster_route<EB, MODE, PK>(B, G, V);
+    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B, kWarps};
+  }
+  // Claimed requests balance whole requests, not chunks: with ragged draft
+  // lengths a CTA pair that drew two long requests sets the pace.  Greedy
+  // calls, bound by DRAM, gain from them anyway (B=512, gamma 1 and 3:
+  // 58 -> 45 and 92 -> 80 us; B=256 ragged: equal); sampling calls gain for
+  // uniform lengths only (140 -> 130, 224 -> 216 us) and lose with ragged
+  // ones (158 -> 194 us), which the host cannot see, so AUTO keeps them on
+  // the persistent grid.
+  const bool claims = sched == SV_SCHEDULE_STREAM || MODE == MODE_GREEDY;
+  return stream_route<EB, MODE, PK>(B, G, V, claims);
+}
+
+template <int EB, int MODE, bool PK, int NW>
+int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned int)(P.B * C));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = (size_t)kWarps * kNB * kItemBytes + stream_tables(P.G, P.V, EB);
+  cfg.gridDim = dim3((unsigned int)(Q * C));
+  cfg.blockDim = dim3((unsigned int)(NW * 32));
+  cfg.dynamicSmemBytes = (size_t)NW * kNB * kItemBytes + stream_tables(P.G, P.V, EB);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -3362,7 +3428,7 @@ int launch_stream(const Params& P, int C, cudaStream_t stream) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, stream_kernel<EB, MODE, PK>, P) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, stream_kernel<EB, MODE, PK, NW>, P) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
 
@@ -3370,7 +3436,9 @@ template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
-  if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK>(P, r.C, stream);
+  if (r.kind == SV_ROUTE_STREAM)
+    return r.nw == kWarps ? launch_stream<EB, MODE, PK, kWarps>(P, r.C, r.Q, stream)
+                          : launch_stream<EB, MODE, PK, kClaimWarps>(P, r.C, r.Q, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch
@@ -3664,7 +3732,7 @@ int spec_verify_set_schedule(int schedule) {
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {
   const int rc = check_scalars(dtype, B, G, V);
   if (rc) return rc;
-  Route r{SV_ROUTE_PERSISTENT, 0};
+  Route r{SV_ROUTE_PERSISTENT, 0, 0, 0};
   if (B > 0) {
     if (dtype == SV_BF16)
       r = greedy ? route<2, MODE_GREEDY, false>(B, G, V) : route<2, MODE_SAMPLE, false>(B, G, V);

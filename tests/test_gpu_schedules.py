@@ -104,6 +104,10 @@ def test_routes():
     # the policies
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_STREAM)[0] == S
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
+    # beyond one cluster per SM: greedy calls claim requests, sampling calls
+    # take the persistent grid (the streaming policy claims in both modes)
+    assert route(bf, 512, 3, 128256, greedy=True) == (S, 1)
+    assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_STREAM) == (S, 1)
     assert binding.spec_verify_cluster_size(bf, 512, 3, 128256) == 0
     assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) == route(bf, 8, 3, 128256)[1]
 
@@ -158,7 +162,8 @@ def test_cluster_rejections_and_bonus_both_occur():
     against_oracle(w, res[0])
 
 
-@pytest.mark.parametrize("B,G,V,dt", [(8, 3, 128256, "bf16"), (5, 6, 20001, "f32"), (2, 0, 7, "bf16")])
+@pytest.mark.parametrize("B,G,V,dt", [(8, 3, 128256, "bf16"), (5, 6, 20001, "f32"), (2, 0, 7, "bf16"),
+                                      (300, 3, 20001, "bf16")])
 def test_schedules_greedy_match_each_other_and_oracle(B, G, V, dt):
     w = W.make_random(B, G, V, dt, seed=B + V, gamma="ragged").to(DEV)
     if G:
@@ -278,3 +283,29 @@ def test_batches_at_the_wave_limits():
         res = sample_all(w)
         all_same(res)
         against_oracle(w, res[0])
+
+
+@pytest.mark.parametrize("B,G,V,dt", [(300, 3, 20001, "bf16"), (200, 5, 4097, "f32"), (400, 1, 32000, "bf16")])
+def test_claimed_requests_match_other_schedules_and_oracle(B, G, V, dt):
+    """More requests than SMs on the streaming path: each CTA takes requests
+    in turn from a claim counter.  Repeated calls on one workspace, then a
+    persistent call on it, give the same results (the counter is reset)."""
+    temps = [0.0 if i % 7 == 3 else 0.5 + 0.004 * i for i in range(B)]
+    w = W.make_random(B, G, V, dt, seed=B + G, gamma="ragged", temperature=temps).to(DEV)
+    assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_STREAM, 1)
+    res = sample_all(w)
+    all_same(res)
+    against_oracle(w, res[1])
+    v = binding.Verifier(B, G, V, DEV)
+    outs = []
+    for sched in (binding.SCHEDULE_STREAM, binding.SCHEDULE_STREAM, binding.SCHEDULE_PERSISTENT):
+        prev = binding.spec_verify_set_schedule(sched)
+        try:
+            v.sample(w.target, w.draft, w.draft_tokens, w.gamma, w.uniforms, w.temperature)
+            torch.cuda.synchronize()
+            assert binding.spec_verify_status(v.workspace) == 0
+            outs.append((v.out_tokens.cpu().numpy().copy(), v.num_accepted.cpu().numpy().copy()))
+        finally:
+            binding.spec_verify_set_schedule(prev)
+    for o in outs:
+        assert (o[0] == res[0][0]).all() and (o[1] == res[0][1]).all()
