@@ -261,7 +261,11 @@ def run_ours(args):
                                       "persistent": binding.SCHEDULE_PERSISTENT}[args.schedule])
     route, csize = binding.spec_verify_route(base.target.dtype, B, G, V, greedy=mode == "greedy")
     kernel = {binding.ROUTE_CLUSTER: "cluster_kernel", binding.ROUTE_STREAM: "stream_kernel",
-              binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
+              binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
+    schedule = {binding.ROUTE_CLUSTER: f"resident clusters of {csize} CTAs, one per request",
+                binding.ROUTE_STREAM: f"streaming clusters of {csize} CTAs, one per request",
+                binding.ROUTE_CLAIMS: "streaming CTAs, two per SM, claiming requests in turn",
+                binding.ROUTE_PERSISTENT: "persistent grid"}[route]
     launches_per_call = 1
 
     packed = args.layout == "packed"
@@ -400,9 +404,7 @@ def run_ours(args):
     if rank == 0:
         cfg = workload_desc(base, mode)
         cfg.update({"layout": args.layout,
-                    "schedule": {"cluster_kernel": f"resident clusters of {csize} CTAs, one per request",
-                                 "stream_kernel": f"streaming clusters of {csize} CTAs, one per request",
-                                 "verify_kernel": "persistent grid"}[kernel],
+                    "schedule": schedule,
                     "parallelism": f"replicas x{world} (independent requests)",
                     "launch": "one CUDA-graph replay of the timed steps" if graph is not None
                               else "one Python call per step",

@@ -256,8 +256,9 @@ const char *spec_verify_strerror(int code);
  *     of up to one cluster per SM (clusters of up to 16 CTAs, at least one),
  *     the warps streaming the request's chunks two at a time and re-reading
  *     the rejected row's chunks for the residual.  For larger greedy batches
- *     (and any larger batch under SV_SCHEDULE_STREAM) two CTAs per SM take
- *     whole requests in turn from a claim counter;
+ *     (and any larger batch under SV_SCHEDULE_STREAM) the same kernel runs as
+ *     two CTAs per SM, each taking whole requests in turn from a claim counter
+ *     (SV_ROUTE_CLAIMS);
  *   - the persistent grid, for larger sampling batches: chunks claimed from
  *     global counters, decisions published through global records, which
  *     balances ragged draft lengths chunk by chunk.
@@ -278,7 +279,7 @@ const char *spec_verify_strerror(int code);
  * (greedy == 0) or greedy call of this shape, in the padded layout, on the
  * current device would use under the current policy, or SV_ERR_SCALAR for
  * invalid sizes.  If cluster_size is not NULL (a HOST pointer), it receives
- * the cluster size (CTAs per request) of a cluster path, or 0.
+ * the cluster size (CTAs per request) of a cluster path (1 for claims), or 0.
  *
  * spec_verify_cluster_size: that cluster size alone (0 for the persistent
  * grid), or SV_ERR_SCALAR.
@@ -289,6 +290,7 @@ const char *spec_verify_strerror(int code);
 #define SV_ROUTE_PERSISTENT 0
 #define SV_ROUTE_CLUSTER 1
 #define SV_ROUTE_STREAM 2
+#define SV_ROUTE_CLAIMS 3
 int spec_verify_set_schedule(int schedule);
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int *cluster_size);
 int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy);

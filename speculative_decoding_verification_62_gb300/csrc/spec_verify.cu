@@ -3377,7 +3377,7 @@ struct Route {
   int kind;  // SV_ROUTE_*
   int C;     // cluster size (cluster paths)
   int Q;     // clusters launched (cluster paths)
-  int nw;    // warps per CTA (streaming path)
+  int nw;    // warps per CTA (cluster paths)
 };
 
 // Streaming cluster path: the largest cluster of which B fit at once (one
@@ -3392,7 +3392,7 @@ Route stream_route(int B, int G, int V, bool claims) {
     if (max_stream_clusters<EB, MODE, PK, kWarps>(C) >= B) return Route{SV_ROUTE_STREAM, C, B, kWarps};
   if (!claims || stream_tables(G, V, EB) > stream_table_cap<kClaimWarps>()) return none;
   const int Q = max_stream_clusters<EB, MODE, PK, kClaimWarps>(1);
-  return Q > 0 ? Route{SV_ROUTE_STREAM, 1, Q, kClaimWarps} : none;
+  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q, kClaimWarps} : none;
 }
 
 template <int EB, int MODE, bool PK>
@@ -3436,9 +3436,8 @@ template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
-  if (r.kind == SV_ROUTE_STREAM)
-    return r.nw == kWarps ? launch_stream<EB, MODE, PK, kWarps>(P, r.C, r.Q, stream)
-                          : launch_stream<EB, MODE, PK, kClaimWarps>(P, r.C, r.Q, stream);
+  if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, kWarps>(P, r.C, r.Q, stream);
+  if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, kClaimWarps>(P, r.C, r.Q, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch

@@ -89,6 +89,7 @@ def test_routes():
     persistent grid beyond."""
     bf, f32 = torch.bfloat16, torch.float32
     R, S, P = binding.ROUTE_CLUSTER, binding.ROUTE_STREAM, binding.ROUTE_PERSISTENT
+    Q = binding.ROUTE_CLAIMS
     for dt in (bf, f32):
         assert route(dt, 1, 4, 32000)[0] == R
         assert route(dt, 8, 3, 32000)[0] == R
@@ -106,8 +107,8 @@ def test_routes():
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
     # beyond one cluster per SM: greedy calls claim requests, sampling calls
     # take the persistent grid (the streaming policy claims in both modes)
-    assert route(bf, 512, 3, 128256, greedy=True) == (S, 1)
-    assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_STREAM) == (S, 1)
+    assert route(bf, 512, 3, 128256, greedy=True) == (Q, 1)
+    assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_STREAM) == (Q, 1)
     assert binding.spec_verify_cluster_size(bf, 512, 3, 128256) == 0
     assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) == route(bf, 8, 3, 128256)[1]
 
@@ -292,10 +293,13 @@ def test_claimed_requests_match_other_schedules_and_oracle(B, G, V, dt):
     persistent call on it, give the same results (the counter is reset)."""
     temps = [0.0 if i % 7 == 3 else 0.5 + 0.004 * i for i in range(B)]
     w = W.make_random(B, G, V, dt, seed=B + G, gamma="ragged", temperature=temps).to(DEV)
-    assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_STREAM, 1)
+    assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_CLAIMS, 1)
     res = sample_all(w)
     all_same(res)
     against_oracle(w, res[1])
+    resp = sample_all(w, packed=True)  # the packed layout on every schedule
+    all_same(resp)
+    same(res[0], resp[0])
     v = binding.Verifier(B, G, V, DEV)
     outs = []
     for sched in (binding.SCHEDULE_STREAM, binding.SCHEDULE_STREAM, binding.SCHEDULE_PERSISTENT):
