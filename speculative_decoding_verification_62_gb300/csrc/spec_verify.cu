@@ -1457,94 +1457,102 @@ __device__ __noinline__ void pad_item_tail(char* stage, int n) {
   __syncwarp();
 }
 
-// A item, sampling: (max, sum of exp2) over the item.
+// A item, sampling: (max, sum of exp2) over the item, in two steps so that a
+// caller can refill the buffer in between.  item_load_max reads the whole
+// item into registers (the buffer is valid throughout: a partial or unaligned
+// item is padded with -inf) and returns its maximum; every loaded value feeds
+// the maximum, so the buffer's reads are complete when it returns.
+// item_exp_sum then sums 2^((z - max) c) from the registers.
+constexpr int kItemWords = kItemBytes / 4 / 32;  // 32-bit words of an item per lane (64)
+
 template <int EB>
-__device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage) {
+__device__ __forceinline__ float item_load_max(const char* stage, uint32_t (&w)[kItemWords]) {
   constexpr int VEC = 16 / EB;
   constexpr int NV = kItemBytes / 16 / 32;  // vectors per lane (16)
   const int lane = threadIdx.x & 31;
-  float mx = -INFINITY, sum = 0.0f;
-  {
-    // two passes over the stage: the maximum, then the exponentials (the
-    // whole buffer is valid: a partial or unaligned item is padded with -inf)
-    if constexpr (EB == 2) {
-      // The item's 2*NV*4 logits stay in registers as bf16 pairs.
-      constexpr int NW = NV * 4;
-      uint32_t w[NW];
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const int vi = lane + 32 * j;
-        const uint4 v = lds128(stage + vi * 16);
-        w[4 * j] = v.x;
-        w[4 * j + 1] = v.y;
-        w[4 * j + 2] = v.z;
-        w[4 * j + 3] = v.w;
-      }
-      // maximum on the packed pairs (exact), as a log-depth tree
-      uint32_t t[NW / 2];
+  for (int j = 0; j < NV; ++j) {
+    const int vi = lane + 32 * j;
+    const uint4 v = lds128(stage + vi * 16);
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  if constexpr (EB == 2) {
+    // maximum on the packed bf16 pairs (exact), as a log-depth tree
+    uint32_t t[kItemWords / 2];
 #pragma unroll
-      for (int i = 0; i < NW / 2; ++i) t[i] = bf16x2_max(w[i], w[i + NW / 2]);
+    for (int i = 0; i < kItemWords / 2; ++i) t[i] = bf16x2_max(w[i], w[i + kItemWords / 2]);
 #pragma unroll
-      for (int width = NW / 4; width >= 1; width >>= 1)
+    for (int width = kItemWords / 4; width >= 1; width >>= 1)
 #pragma unroll
-        for (int i = 0; i < width; ++i) t[i] = bf16x2_max(t[i], t[i + width]);
-      mx = warp_max(bf16x2_hmax(t[0]));
-      if (mx > -INFINITY) {
-        // (z - m) * (hi + lo) and the sum, on float32 pairs, 8 accumulators
-        const unsigned long long negm = f2_pack(-mx, -mx);
-        const unsigned long long chi = f2_pack(m.c_hi, m.c_hi), clo = f2_pack(m.c_lo, m.c_lo);
-        unsigned long long acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0ull;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-          const unsigned long long d = f2_add(bf16x2_to_f2(w[i]), negm);
-          const unsigned long long a = f2_fma(d, chi, f2_mul(d, clo));
-          float a0, a1;
-          f2_unpack(a, a0, a1);
-          acc[i & 7] = f2_add(acc[i & 7], f2_pack(ex2_approx(a0), ex2_approx(a1)));
-        }
-#pragma unroll
-        for (int width = 4; width >= 1; width >>= 1)
-#pragma unroll
-          for (int i = 0; i < width; ++i) acc[i] = f2_add(acc[i], acc[i + width]);
-        float s0, s1;
-        f2_unpack(acc[0], s0, s1);
-        sum = s0 + s1;
-      }
-      return make_float2(mx, warp_sum(sum));
-    }
-    uint4 v[NV];  // float32: the item stays in registers
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int vi = lane + 32 * j;
-      v[j] = lds128(stage + vi * 16);
-    }
+      for (int i = 0; i < width; ++i) t[i] = bf16x2_max(t[i], t[i + width]);
+    return warp_max(bf16x2_hmax(t[0]));
+  } else {
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
     for (int j = 0; j < NV; ++j)
 #pragma unroll
-      for (int q = 0; q < VEC; ++q) mq[q & 3] = fmaxf(mq[q & 3], vec_elem<EB>(v[j], q));
-    mx = warp_max(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
-    if (mx > -INFINITY) {
+      for (int q = 0; q < VEC; ++q) mq[q & 3] = fmaxf(mq[q & 3], __uint_as_float(w[4 * j + q]));
+    return warp_max(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
+  }
+}
+
+template <int EB>
+__device__ __forceinline__ float item_exp_sum(const uint32_t (&w)[kItemWords], float mx, float c_hi,
+                                              float c_lo) {
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = kItemBytes / 16 / 32;
+  float sum = 0.0f;
+  if (mx > -INFINITY) {
+    if constexpr (EB == 2) {
+      // (z - m) * (hi + lo) and the sum, on float32 pairs, 8 accumulators
+      const unsigned long long negm = f2_pack(-mx, -mx);
+      const unsigned long long chi = f2_pack(c_hi, c_hi), clo = f2_pack(c_lo, c_lo);
+      unsigned long long acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0ull;
+#pragma unroll
+      for (int i = 0; i < kItemWords; ++i) {
+        const unsigned long long d = f2_add(bf16x2_to_f2(w[i]), negm);
+        const unsigned long long a = f2_fma(d, chi, f2_mul(d, clo));
+        float a0, a1;
+        f2_unpack(a, a0, a1);
+        acc[i & 7] = f2_add(acc[i & 7], f2_pack(ex2_approx(a0), ex2_approx(a1)));
+      }
+#pragma unroll
+      for (int width = 4; width >= 1; width >>= 1)
+#pragma unroll
+        for (int i = 0; i < width; ++i) acc[i] = f2_add(acc[i], acc[i + width]);
+      float s0, s1;
+      f2_unpack(acc[0], s0, s1);
+      sum = s0 + s1;
+    } else {
       float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         float e[VEC];
 #pragma unroll
         for (int q = 0; q < VEC; ++q)
-          e[q] = ex2_approx(exp_arg(vec_elem<EB>(v[j], q), mx, m.c_hi, m.c_lo));
+          e[q] = ex2_approx(exp_arg(__uint_as_float(w[4 * j + q]), mx, c_hi, c_lo));
 #pragma unroll
-        for (int w = VEC; w > 1; w >>= 1)
+        for (int u = VEC; u > 1; u >>= 1)
 #pragma unroll
-          for (int q = 0; q < w / 2; ++q) e[q] = e[2 * q] + e[2 * q + 1];
+          for (int q = 0; q < u / 2; ++q) e[q] = e[2 * q] + e[2 * q + 1];
         sq[j & 3] += e[0];
       }
       sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
     }
   }
-  sum = warp_sum(sum);
-  return make_float2(mx, sum);
+  return warp_sum(sum);
+}
+
+template <int EB>
+__device__ __forceinline__ float2 a_item_sample(const Meta& m, const char* stage) {
+  uint32_t w[kItemWords];
+  const float mx = item_load_max<EB>(stage, w);
+  return make_float2(mx, item_exp_sum<EB>(w, mx, m.c_hi, m.c_lo));
 }
 
 // A item, greedy: (max, lowest row-global index of the max).
@@ -2926,15 +2934,17 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 // while the current one is decided; the other warps start the next request's
 // items while warp 0 draws.  Shared memory: the buffers, then (the same
 // layout in every CTA) the partials [2G+1][NC] and the leader's chunk sums
-// [NCR].  NW warps per CTA: kWarps (one CTA per SM), or kWarps / 2 for
-// claimed requests (two CTAs per SM, so that one CTA's decision and residual
-// steps overlap the other's streaming).
-template <int EB, int MODE, bool PK, int NW>
-__global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) {
-  static_assert(NW >= 1 && kWarps % NW == 0, "CTAs of NW warps share an SM's warps");
+// [NCR].  NW warps per CTA with NB staging buffers each; CPS CTAs per SM
+// (two for claimed requests, so that one CTA's decision and residual steps
+// overlap the other's streaming).  With one buffer per warp a sampling item
+// moves into registers with its maximum and the buffer's next copy starts
+// before the exponentials.
+template <int EB, int MODE, bool PK, int NW, int NB, int CPS>
+__global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
+  static_assert(NW * CPS * 32 <= 1024 && NB >= 1 && NB <= 2, "warps and buffers per SM");
   extern __shared__ __align__(128) unsigned char dsmem[];
-  __shared__ __align__(8) uint64_t bar[NW][kNB];
-  __shared__ Meta smeta[NW][kNB];  // the item in each buffer
+  __shared__ __align__(8) uint64_t bar[NW][NB];
+  __shared__ Meta smeta[NW][NB];  // the item in each buffer
   __shared__ float rsbuf[192];         // the decision's row statistics
   __shared__ ClusterDec sdec;
   __shared__ int s_next, s_last;       // the CTA's next request; last CTA out
@@ -2945,9 +2955,9 @@ __global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) 
   const int nq = (int)(gridDim.x / C);  // clusters
   const bool queue = P.B > nq;          // requests claimed in turn (clusters of one CTA)
   const int G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
-  float2* part = reinterpret_cast<float2*>(dsmem + (size_t)NW * kNB * kItemBytes);
+  float2* part = reinterpret_cast<float2*>(dsmem + (size_t)NW * NB * kItemBytes);
   unsigned long long* rsum = reinterpret_cast<unsigned long long*>(part + (size_t)(2 * G + 1) * NC);
-  unsigned char* mybuf = dsmem + (size_t)warp * kNB * kItemBytes;
+  unsigned char* mybuf = dsmem + (size_t)warp * NB * kItemBytes;
   uint64_t* mybar = bar[warp];
   Meta* mymeta = smeta[warp];
   const unsigned int gw = rank * NW + (unsigned int)warp, W = C * NW;
@@ -2957,7 +2967,7 @@ __global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) 
     return;
   }
   if (lane == 0) {
-    for (int s = 0; s < kNB; ++s) mbar_init(&mybar[s], 1);
+    for (int s = 0; s < NB; ++s) mbar_init(&mybar[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
@@ -2967,7 +2977,7 @@ __global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) 
   unsigned int flags = 0;
   // Start the copy of item m into the next buffer (lane 0 issues it).
   auto issue = [&](const Meta& m) {
-    const int s = (int)(issued % kNB);
+    const int s = (int)(issued % NB);
     if (lane == 0) {
       mymeta[s] = m;
       unsigned char* dst = mybuf + s * kItemBytes;
@@ -2986,7 +2996,7 @@ __global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) 
   };
   // Wait for the oldest copy in flight; false after the bounded wait gave up.
   auto wait_oldest = [&]() -> bool {
-    if (mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u)) return true;
+    if (mbar_wait(&mybar[processed % NB], (processed / NB) & 1u)) return true;
     flags |= SV_STATUS_TIMEOUT;
     failed = true;
     return false;
@@ -3057,35 +3067,54 @@ __global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) 
     {
       // lane r < C stores each partial into CTA r: every CTA decides locally
       const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
-      auto store_part = [&](const Meta& m, float2 pr) {
+      auto store_at = [&](int pslot, int c, float2 pr) {
         if ((uint32_t)lane < C)
-          st_cluster_f2(part_r + (uint32_t)((m.pslot * NC + m.c) * (int)sizeof(float2)), pr);
+          st_cluster_f2(part_r + (uint32_t)((pslot * NC + c) * (int)sizeof(float2)), pr);
       };
+      auto store_part = [&](const Meta& m, float2 pr) { store_at(m.pslot, m.c, pr); };
       unsigned int jn = gw;  // this warp's next item
-      while (!failed) {
-        while (issued - processed < (unsigned int)kNB && jn < nI) {
+      auto top_up = [&]() {  // start copies into every free buffer
+        while (issued - processed < (unsigned int)NB && jn < nI) {
           issue(a_meta(jn));
           jn += W;
         }
+      };
+      while (!failed) {
+        top_up();
         if (issued == processed || !wait_oldest()) break;
-        const Meta& m = mymeta[processed % kNB];
-        char* stage = reinterpret_cast<char*>(mybuf + (processed % kNB) * kItemBytes);
+        const Meta& m = mymeta[processed % NB];
+        char* stage = reinterpret_cast<char*>(mybuf + (processed % NB) * kItemBytes);
         const bool padded = !m.direct && m.n < AE;  // a row's last chunk
+        const bool written = (sample && m.direct) || padded;
         if (sample && m.direct) stage_unaligned<EB>(m, stage);
         else if (padded) pad_item_tail<EB>(stage, m.n);
-        store_part(m, sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage));
-        // stores into the buffer are ordered before the next bulk copy into it
-        if ((sample && m.direct) || padded) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        ++processed;
+        const int pslot = m.pslot, c = m.c;
+        if (NB == 1 && sample) {
+          // the item moves into registers with its maximum; the buffer's next
+          // copy then runs during the exponentials
+          const float c_hi = m.c_hi, c_lo = m.c_lo;
+          uint32_t w[kItemWords];
+          const float mx = item_load_max<EB>(stage, w);
+          // stores into the buffer are ordered before the next bulk copy into it
+          if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          ++processed;
+          top_up();
+          store_at(pslot, c, make_float2(mx, item_exp_sum<EB>(w, mx, c_hi, c_lo)));
+        } else {
+          store_at(pslot, c, sample ? a_item_sample<EB>(m, stage) : a_item_greedy<EB>(m, stage));
+          if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          ++processed;
+        }
       }
       if (failed) {
         // Every item of this warp still stores a partial, (NaN, 0) where it
         // could not be read: every CTA then holds the same table and takes the
         // same branches below.  Copies in flight are waited for (bounded).
         for (; processed != issued; ++processed) {
-          (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
-          store_part(mymeta[processed % kNB], make_float2(NAN, 0.0f));
+          (void)mbar_wait(&mybar[processed % NB], (processed / NB) & 1u);
+          store_part(mymeta[processed % NB], make_float2(NAN, 0.0f));
           __syncwarp();
         }
         for (; jn < nI; jn += W) store_part(a_meta(jn), make_float2(NAN, 0.0f));
@@ -3163,22 +3192,22 @@ __global__ void __launch_bounds__(NW * 32, kWarps / NW) stream_kernel(Params P) 
       const uint32_t rsum0 = rank_addr(rsum, 0u);  // the leader's chunk sums
       unsigned int jr = gw;                        // this warp's next chunk
       while (!failed) {
-        while (issued - processed < (unsigned int)kNB && jr < (unsigned int)NCR) {
+        while (issued - processed < (unsigned int)NB && jr < (unsigned int)NCR) {
           issue(r_meta(jr));
           jr += W;
         }
         if (issued == processed || !wait_oldest()) break;
-        const Meta& m = mymeta[processed % kNB];
+        const Meta& m = mymeta[processed % NB];
         const unsigned long long sr =
-            r_item<EB>(m, reinterpret_cast<const char*>(mybuf + (processed % kNB) * kItemBytes));
+            r_item<EB>(m, reinterpret_cast<const char*>(mybuf + (processed % NB) * kItemBytes));
         if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)m.c * 8u, sr);
         __syncwarp();
         ++processed;
       }
       if (failed) {  // copies in flight are waited for (bounded); missing sums are 0
         for (; processed != issued; ++processed) {
-          (void)mbar_wait(&mybar[processed % kNB], (processed / kNB) & 1u);
-          if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % kNB].c * 8u, 0ull);
+          (void)mbar_wait(&mybar[processed % NB], (processed / NB) & 1u);
+          if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % NB].c * 8u, 0ull);
           __syncwarp();
         }
         for (; jr < (unsigned int)NCR; jr += W)
@@ -3322,26 +3351,29 @@ int max_clusters(int C) {
   static std::atomic<int> cached[kClusterMax + 1];
   return clusters_that_fit(cluster_kernel<EB, MODE, PK>, C, cached);
 }
-// Streaming kernel with NW warps per CTA: the cap on its tables and its
-// largest dynamic shared memory.  Two CTAs of kWarps / 2 warps share an SM
-// (228 KB of shared memory, 1 KB of it reserved per CTA), which leaves them
-// 12 KB of tables each.
-template <int NW>
-constexpr size_t stream_table_cap() {
-  return NW == kWarps ? (size_t)kClusterTables : (size_t)12 * 1024;
-}
-template <int NW>
-constexpr size_t stream_smem() {
-  return (size_t)NW * kNB * kItemBytes + stream_table_cap<NW>();
-}
-static_assert(2 * (stream_smem<kWarps / 2>() + 3 * 1024) <= 228 * 1024,
-              "two claiming CTAs per SM (with about 2 KB of static shared memory each)");
-template <int EB, int MODE, bool PK, int NW>
+// Shapes of the streaming kernel: warps and buffers per CTA, CTAs per SM.
+// One wave of clusters (a request each) runs one CTA per SM; claimed requests
+// run two CTAs per SM with half the warps each.  Sampling uses 16 warps per
+// SM with one buffer each (the item is held in registers during its
+// exponentials, 128 registers per thread); greedy, with light arithmetic,
+// 12 warps with two buffers each.  A CTA's tables are capped so that its CTAs
+// fit the SM's 228 KB of shared memory (1 KB of it reserved per CTA, about
+// 3 KB of static shared memory each).
+template <int MODE, int CPS>
+struct StreamShape {
+  static constexpr int nb = MODE == MODE_SAMPLE ? 1 : 2;
+  static constexpr int nw = (MODE == MODE_SAMPLE ? 16 : kWarps) / CPS;
+  static constexpr size_t table_cap = CPS == 1 ? (size_t)kClusterTables : (size_t)12 * 1024;
+  static constexpr size_t smem = (size_t)nw * nb * kItemBytes + table_cap;
+  static_assert(CPS * (smem + 4 * 1024) <= 228 * 1024, "streaming CTAs per SM");
+};
+template <int EB, int MODE, bool PK, int CPS>
 int max_stream_clusters(int C) {
+  using S = StreamShape<MODE, CPS>;
   static std::atomic<int> cached[kClusterMax + 1];
-  return clusters_that_fit(stream_kernel<EB, MODE, PK, NW>, C, cached, NW * 32, stream_smem<NW>());
+  return clusters_that_fit(stream_kernel<EB, MODE, PK, S::nw, S::nb, CPS>, C, cached, S::nw * 32,
+                           S::smem);
 }
-constexpr int kClaimWarps = kWarps / 2;  // warps per CTA of the claiming streaming kernel
 
 // Resident cluster path: the cluster size for this call, or 0.
 template <int EB, int MODE, bool PK>
@@ -3377,31 +3409,30 @@ struct Route {
   int kind;  // SV_ROUTE_*
   int C;     // cluster size (cluster paths)
   int Q;     // clusters launched (cluster paths)
-  int nw;    // warps per CTA (cluster paths)
 };
 
 // Streaming cluster path: the largest cluster of which B fit at once (one
 // wave, a request per cluster); with `claims`, a batch beyond one wave of
-// single-CTA clusters runs on as many CTAs of kClaimWarps warps as fit (two
-// per SM), each claiming requests in turn.
+// single-CTA clusters runs on as many CTAs as fit (two per SM), each claiming
+// requests in turn.
 template <int EB, int MODE, bool PK>
 Route stream_route(int B, int G, int V, bool claims) {
-  const Route none{SV_ROUTE_PERSISTENT, 0, 0, 0};
-  if (B < 1 || stream_tables(G, V, EB) > stream_table_cap<kWarps>()) return none;
+  const Route none{SV_ROUTE_PERSISTENT, 0, 0};
+  if (B < 1 || stream_tables(G, V, EB) > StreamShape<MODE, 1>::table_cap) return none;
   for (int C = kClusterMax; C >= 1; --C)
-    if (max_stream_clusters<EB, MODE, PK, kWarps>(C) >= B) return Route{SV_ROUTE_STREAM, C, B, kWarps};
-  if (!claims || stream_tables(G, V, EB) > stream_table_cap<kClaimWarps>()) return none;
-  const int Q = max_stream_clusters<EB, MODE, PK, kClaimWarps>(1);
-  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q, kClaimWarps} : none;
+    if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B};
+  if (!claims || stream_tables(G, V, EB) > StreamShape<MODE, 2>::table_cap) return none;
+  const int Q = max_stream_clusters<EB, MODE, PK, 2>(1);
+  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q} : none;
 }
 
 template <int EB, int MODE, bool PK>
 Route route(int B, int G, int V) {
   const int sched = g_schedule.load();
-  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0, 0};
+  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0};
   if (sched == SV_SCHEDULE_AUTO) {
     const int C = cluster_route<EB, MODE, PK>(B, G, V);
-    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B, kWarps};
+    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B};
   }
   // Claimed requests balance whole requests, not chunks: with ragged draft
   // lengths a CTA pair that drew two long requests sets the pace.  Greedy
@@ -3414,12 +3445,13 @@ Route route(int B, int G, int V) {
   return stream_route<EB, MODE, PK>(B, G, V, claims);
 }
 
-template <int EB, int MODE, bool PK, int NW>
+template <int EB, int MODE, bool PK, int CPS>
 int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
+  using S = StreamShape<MODE, CPS>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned int)(Q * C));
-  cfg.blockDim = dim3((unsigned int)(NW * 32));
-  cfg.dynamicSmemBytes = (size_t)NW * kNB * kItemBytes + stream_tables(P.G, P.V, EB);
+  cfg.blockDim = dim3((unsigned int)(S::nw * 32));
+  cfg.dynamicSmemBytes = (size_t)S::nw * S::nb * kItemBytes + stream_tables(P.G, P.V, EB);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -3428,7 +3460,8 @@ int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, stream_kernel<EB, MODE, PK, NW>, P) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, stream_kernel<EB, MODE, PK, S::nw, S::nb, CPS>, P) != cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 
@@ -3436,8 +3469,8 @@ template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
-  if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, kWarps>(P, r.C, r.Q, stream);
-  if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, kClaimWarps>(P, r.C, r.Q, stream);
+  if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, 1>(P, r.C, r.Q, stream);
+  if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, 2>(P, r.C, r.Q, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch
@@ -3731,7 +3764,7 @@ int spec_verify_set_schedule(int schedule) {
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {
   const int rc = check_scalars(dtype, B, G, V);
   if (rc) return rc;
-  Route r{SV_ROUTE_PERSISTENT, 0, 0, 0};
+  Route r{SV_ROUTE_PERSISTENT, 0, 0};
   if (B > 0) {
     if (dtype == SV_BF16)
       r = greedy ? route<2, MODE_GREEDY, false>(B, G, V) : route<2, MODE_SAMPLE, false>(B, G, V);
