@@ -3423,7 +3423,7 @@ Route stream_route(int B, int G, int V, bool claims) {
     if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B};
   if (!claims || stream_tables(G, V, EB) > StreamShape<MODE, 2>::table_cap) return none;
   const int Q = max_stream_clusters<EB, MODE, PK, 2>(1);
-  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q} : none;
+  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B} : none;
 }
 
 template <int EB, int MODE, bool PK>

@@ -164,7 +164,7 @@ def test_cluster_rejections_and_bonus_both_occur():
 
 
 @pytest.mark.parametrize("B,G,V,dt", [(8, 3, 128256, "bf16"), (5, 6, 20001, "f32"), (2, 0, 7, "bf16"),
-                                      (300, 3, 20001, "bf16")])
+                                      (300, 3, 20001, "bf16"), (900, 2, 4097, "f32")])
 def test_schedules_greedy_match_each_other_and_oracle(B, G, V, dt):
     w = W.make_random(B, G, V, dt, seed=B + V, gamma="ragged").to(DEV)
     if G:
@@ -286,11 +286,14 @@ def test_batches_at_the_wave_limits():
         against_oracle(w, res[0])
 
 
-@pytest.mark.parametrize("B,G,V,dt", [(300, 3, 20001, "bf16"), (200, 5, 4097, "f32"), (400, 1, 32000, "bf16")])
+@pytest.mark.parametrize("B,G,V,dt", [(300, 3, 20001, "bf16"), (200, 5, 4097, "f32"), (400, 1, 32000, "bf16"),
+                                      (1000, 3, 4097, "f32"), (700, 0, 33, "bf16")])
 def test_claimed_requests_match_other_schedules_and_oracle(B, G, V, dt):
-    """More requests than SMs on the streaming path: each CTA takes requests
-    in turn from a claim counter.  Repeated calls on one workspace, then a
-    persistent call on it, give the same results (the counter is reset)."""
+    """More requests than SMs on the streaming path: two CTAs per SM, each
+    taking requests in turn from a claim counter once the batch exceeds them
+    (B = 400, 700, 1000; at 200 and 300 each CTA takes one).  Repeated calls on
+    one workspace, then a persistent call on it, give the same results (the
+    counter is reset)."""
     temps = [0.0 if i % 7 == 3 else 0.5 + 0.004 * i for i in range(B)]
     w = W.make_random(B, G, V, dt, seed=B + G, gamma="ragged", temperature=temps).to(DEV)
     assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_CLAIMS, 1)
