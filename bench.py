@@ -264,7 +264,7 @@ def run_ours(args):
               binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
     schedule = {binding.ROUTE_CLUSTER: f"resident clusters of {csize} CTAs, one per request",
                 binding.ROUTE_STREAM: f"streaming clusters of {csize} CTAs, one per request",
-                binding.ROUTE_CLAIMS: "streaming CTAs, two per SM, claiming requests in turn",
+                binding.ROUTE_CLAIMS: "streaming CTAs claiming requests in turn, longest first",
                 binding.ROUTE_PERSISTENT: "persistent grid"}[route]
     launches_per_call = 1
 

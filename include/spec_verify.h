@@ -255,13 +255,14 @@ const char *spec_verify_strerror(int code);
  *   - the streaming cluster path: one cluster per request as well, for batches
  *     of up to one cluster per SM (clusters of up to 16 CTAs, at least one),
  *     the warps streaming the request's chunks two at a time and re-reading
- *     the rejected row's chunks for the residual.  For larger greedy batches
- *     (and any larger batch under SV_SCHEDULE_STREAM) the same kernel runs as
- *     two CTAs per SM, each taking whole requests in turn from a claim counter
- *     (SV_ROUTE_CLAIMS);
- *   - the persistent grid, for larger sampling batches: chunks claimed from
- *     global counters, decisions published through global records, which
- *     balances ragged draft lengths chunk by chunk.
+ *     the rejected row's chunks for the residual.  For larger batches the same
+ *     kernel runs as one CTA per SM (sampling) or two (greedy), each taking
+ *     whole requests in turn from a claim counter, longest request first
+ *     (SV_ROUTE_CLAIMS).  The claim order takes 5 bytes of shared memory per
+ *     request;
+ *   - the persistent grid, for batches whose claim order does not fit (tens
+ *     of thousands of requests): chunks claimed from global counters,
+ *     decisions published through global records.
  * The cluster paths replace the persistent grid's chain of global-memory
  * synchronisations (arrival counters, decision records, queue) with cluster
  * barriers.  These calls are not steps of the method: they exist for testing
@@ -271,9 +272,8 @@ const char *spec_verify_strerror(int code);
  * process: SV_SCHEDULE_AUTO (the default: the first of the resident cluster
  * path, the streaming cluster path and the persistent grid that applies, as
  * above), SV_SCHEDULE_PERSISTENT (every call on the persistent grid) or
- * SV_SCHEDULE_STREAM (the streaming path wherever its tables fit, claims
- * included).  Returns the previous policy, or SV_ERR_SCALAR for an unknown
- * value.
+ * SV_SCHEDULE_STREAM (as AUTO without the resident path).  Returns the
+ * previous policy, or SV_ERR_SCALAR for an unknown value.
  *
  * spec_verify_route: the kernel (SV_ROUTE_*) that the next sampling
  * (greedy == 0) or greedy call of this shape, in the padded layout, on the

@@ -2934,11 +2934,11 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 // while the current one is decided; the other warps start the next request's
 // items while warp 0 draws.  Shared memory: the buffers, then (the same
 // layout in every CTA) the partials [2G+1][NC] and the leader's chunk sums
-// [NCR].  NW warps per CTA with NB staging buffers each; CPS CTAs per SM
-// (two for claimed requests, so that one CTA's decision and residual steps
-// overlap the other's streaming).  With one buffer per warp a sampling item
-// moves into registers with its maximum and the buffer's next copy starts
-// before the exponentials.
+// [NCR] (then, with claims, the claim order [B] and row counts [B]).  NW
+// warps per CTA with NB staging buffers each; CPS CTAs per SM (two for greedy
+// claims, so that one CTA's decision overlaps the other's streaming).  With
+// one buffer per warp a sampling item moves into registers with its maximum
+// and the buffer's next copy starts before the exponentials.
 template <int EB, int MODE, bool PK, int NW, int NB, int CPS>
 __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
   static_assert(NW * CPS * 32 <= 1024 && NB >= 1 && NB <= 2, "warps and buffers per SM");
@@ -2947,7 +2947,8 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
   __shared__ Meta smeta[NW][NB];  // the item in each buffer
   __shared__ float rsbuf[192];         // the decision's row statistics
   __shared__ ClusterDec sdec;
-  __shared__ int s_next, s_last;       // the CTA's next request; last CTA out
+  __shared__ int s_next, s_last;       // the CTA's next claim; last CTA out
+  __shared__ int s_hist[64];           // claim order: first position per row count
   constexpr int AE = kItemBytes / EB;   // logits per A item
   constexpr int RE = kHalfBytes / EB;   // logits per R chunk and row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -3002,7 +3003,75 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     return false;
   };
 
-  for (int b = (int)cluster_index(); b < P.B;) {
+  // Claims are taken longest request first (by row count, then index): the
+  // short requests claimed last fill in around the long ones.  Every CTA
+  // builds the same order in shared memory: all threads read the row counts;
+  // if they differ, warp 0 places each request with a stable counting sort
+  // (about 3 us at B = 512, so a batch of equal counts keeps index order).
+  int* order = reinterpret_cast<int*>(rsum + NCR);                      // [B] requests by claim
+  unsigned char* nrow = reinterpret_cast<unsigned char*>(order + P.B);  // [B] row counts
+  bool sorted = false;  // claims go through `order`
+  if (queue) {
+    auto rows_of_req = [&](int b) -> int {
+      int gb = 0;
+      unsigned int fl = 0;
+      if constexpr (PK) (void)packed_base(P, b, gb, fl);
+      else gb = clamp_gamma(P.gamma ? P.gamma[b] : 0, G);
+      const bool sampled = MODE == MODE_SAMPLE && P.temperature[b] != 0.0f;
+      return sampled ? 2 * gb + 1 : gb + 1;
+    };
+    const int r0 = rows_of_req(0);
+    int differs = 0;
+#pragma unroll 4
+    for (int b = tid; b < P.B; b += NW * 32) {
+      const int r = rows_of_req(b);
+      nrow[b] = (unsigned char)r;
+      differs |= r != r0;
+    }
+    sorted = __syncthreads_or(differs) != 0;
+  }
+  if (sorted) {
+    if (warp == 0) {
+      for (int r = lane; r < 64; r += 32) s_hist[r] = 0;
+      __syncwarp();
+      // counts per row count: one add per distinct count in each group of 32
+      for (int b0 = 0; b0 < P.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int r = b < P.B ? (int)nrow[b] : 64;  // 64: past the batch
+        const unsigned int peers = __match_any_sync(0xffffffffu, r);
+        if (r < 64 && lane == __ffs(peers) - 1) s_hist[r] += __popc(peers);
+        __syncwarp();
+      }
+      // first position of each row count, longest first: lane l holds counts
+      // 2l and 2l + 1; a suffix sum over the lanes
+      const int h0 = s_hist[2 * lane], h1 = s_hist[2 * lane + 1];
+      int suf = h0 + h1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+      }
+      const int after = suf - h0 - h1;  // requests with more rows than 2l + 1
+      __syncwarp();
+      s_hist[2 * lane + 1] = after;
+      s_hist[2 * lane] = after + h1;
+      __syncwarp();
+      for (int b0 = 0; b0 < P.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int r = b < P.B ? (int)nrow[b] : 64;  // 64: past the batch
+        const unsigned int peers = __match_any_sync(0xffffffffu, r);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        if (r < 64) order[s_hist[r] + before] = b;
+        __syncwarp();
+        if (r < 64 && before == 0) s_hist[r] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+
+  for (int claim = (int)cluster_index(); claim < P.B;) {
+    const int b = sorted ? order[claim] : claim;
     // the request: draft length, addresses, temperature constants
     unsigned int rflags = 0;
     int gb = 0, base = 0;
@@ -3127,7 +3196,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     if (greedy && rank != 0) return;
     if (warp == 0) {
       // queue: the next request is claimed now, its latency hidden by the decision
-      if (lane == 0) s_next = queue ? (int)atomicAdd(P.next_item, 1u) + nq : P.B;
+      if (lane == 0) s_next = queue ? (int)atomicAdd(P.next_item, 1u) + nq : P.B;  // a claim
       float* rs = rsbuf;
       const SharedParts sp{part, NC};
       ClusterDec cd;
@@ -3232,7 +3301,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
         }
       }
     }
-    b = next;
+    claim = next;
   }  // requests
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && any) atomicOr(P.status, any);
@@ -3352,7 +3421,7 @@ int max_clusters(int C) {
   return clusters_that_fit(cluster_kernel<EB, MODE, PK>, C, cached);
 }
 // Shapes of the streaming kernel: warps and buffers per CTA, CTAs per SM.
-// One wave of clusters (a request each) runs one CTA per SM; claimed requests
+// One wave of clusters (a request each) runs one CTA per SM; greedy claims
 // run two CTAs per SM with half the warps each.  Sampling uses 16 warps per
 // SM with one buffer each (the item is held in registers during its
 // exponentials, 128 registers per thread); greedy, with light arithmetic,
@@ -3367,6 +3436,15 @@ struct StreamShape {
   static constexpr size_t smem = (size_t)nw * nb * kItemBytes + table_cap;
   static_assert(CPS * (smem + 4 * 1024) <= 228 * 1024, "streaming CTAs per SM");
 };
+// Claimed requests: the claim order and the row counts it is built from.
+// Sampling claims run one 16-warp CTA per SM: with the longest-first order
+// they beat two 8-warp CTAs per SM (B=256 ragged: 127 against 177 us), whose
+// CTA pairs share an SM's rate whatever their requests.  Greedy claims run two
+// 6-warp CTAs per SM (B=512: 45 and 80 us against 48 and 83 with one CTA).
+size_t claim_bytes(int B) { return ((size_t)B * 5 + 15) & ~(size_t)15; }
+template <int MODE>
+constexpr int claim_cps() { return MODE == MODE_SAMPLE ? 1 : 2; }
+
 template <int EB, int MODE, bool PK, int CPS>
 int max_stream_clusters(int C) {
   using S = StreamShape<MODE, CPS>;
@@ -3413,16 +3491,17 @@ struct Route {
 
 // Streaming cluster path: the largest cluster of which B fit at once (one
 // wave, a request per cluster); with `claims`, a batch beyond one wave of
-// single-CTA clusters runs on as many CTAs as fit (two per SM), each claiming
-// requests in turn.
+// single-CTA clusters runs on as many CTAs as fit, each claiming requests in
+// turn.
 template <int EB, int MODE, bool PK>
-Route stream_route(int B, int G, int V, bool claims) {
+Route stream_route(int B, int G, int V) {
   const Route none{SV_ROUTE_PERSISTENT, 0, 0};
   if (B < 1 || stream_tables(G, V, EB) > StreamShape<MODE, 1>::table_cap) return none;
   for (int C = kClusterMax; C >= 1; --C)
     if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B};
-  if (!claims || stream_tables(G, V, EB) > StreamShape<MODE, 2>::table_cap) return none;
-  const int Q = max_stream_clusters<EB, MODE, PK, 2>(1);
+  constexpr int QC = claim_cps<MODE>();
+  if (stream_tables(G, V, EB) + claim_bytes(B) > StreamShape<MODE, QC>::table_cap) return none;
+  const int Q = max_stream_clusters<EB, MODE, PK, QC>(1);
   return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B} : none;
 }
 
@@ -3434,15 +3513,11 @@ Route route(int B, int G, int V) {
     const int C = cluster_route<EB, MODE, PK>(B, G, V);
     if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B};
   }
-  // Claimed requests balance whole requests, not chunks: with ragged draft
-  // lengths a CTA pair that drew two long requests sets the pace.  Greedy
-  // calls, bound by DRAM, gain from them anyway (B=512, gamma 1 and 3:
-  // 58 -> 45 and 92 -> 80 us; B=256 ragged: equal); sampling calls gain for
-  // uniform lengths only (140 -> 130, 224 -> 216 us) and lose with ragged
-  // ones (158 -> 194 us), which the host cannot see, so AUTO keeps them on
-  // the persistent grid.
-  const bool claims = sched == SV_SCHEDULE_STREAM || MODE == MODE_GREEDY;
-  return stream_route<EB, MODE, PK>(B, G, V, claims);
+  // Beyond one wave, claimed requests (longest first) beat the persistent
+  // grid's chunk claims: B=256 ragged, B=512 gamma 1 and 3, sampling 159 ->
+  // 127, 142 -> 124, 225 -> 214 us; greedy 64 -> 64, 58 -> 45, 92 -> 80 us.
+  // The grid remains for batches whose claim order does not fit.
+  return stream_route<EB, MODE, PK>(B, G, V);
 }
 
 template <int EB, int MODE, bool PK, int CPS>
@@ -3451,7 +3526,8 @@ int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned int)(Q * C));
   cfg.blockDim = dim3((unsigned int)(S::nw * 32));
-  cfg.dynamicSmemBytes = (size_t)S::nw * S::nb * kItemBytes + stream_tables(P.G, P.V, EB);
+  cfg.dynamicSmemBytes = (size_t)S::nw * S::nb * kItemBytes + stream_tables(P.G, P.V, EB) +
+                         (Q * C < P.B ? claim_bytes(P.B) : 0);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -3470,7 +3546,7 @@ int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
   if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, 1>(P, r.C, r.Q, stream);
-  if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, 2>(P, r.C, r.Q, stream);
+  if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, claim_cps<MODE>()>(P, r.C, r.Q, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
   // requests are processed in launches of at most kMaxBatch

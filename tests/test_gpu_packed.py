@@ -90,12 +90,18 @@ def test_packed_greedy_matches_oracle(B, G, V, dt):
     assert not bad, bad[:5]
 
 
-def test_packed_batches_split_over_launches():
-    """More requests than one launch takes: the packed offsets stay global."""
+@pytest.mark.parametrize("sched", [binding.SCHEDULE_PERSISTENT, binding.SCHEDULE_AUTO])
+def test_packed_large_batches(sched):
+    """1700 requests: on the persistent grid more than one launch takes (the
+    packed offsets stay global); by default, request claims."""
     B, G, V = 1700, 3, 300
-    w = W.make_random(B, G, V, "bf16", seed=99, gamma="ragged").to(DEV)
-    out_p, nacc_p, _, _ = run_padded(w)
-    out, nacc, _, _, st, _ = run_packed(W.pack(w), B, G, V)
+    prev = binding.spec_verify_set_schedule(sched)
+    try:
+        w = W.make_random(B, G, V, "bf16", seed=99, gamma="ragged").to(DEV)
+        out_p, nacc_p, _, _ = run_padded(w)
+        out, nacc, _, _, st, _ = run_packed(W.pack(w), B, G, V)
+    finally:
+        binding.spec_verify_set_schedule(prev)
     assert st == 0
     assert (out == out_p).all() and (nacc == nacc_p).all()
 

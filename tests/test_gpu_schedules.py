@@ -93,7 +93,9 @@ def test_routes():
     for dt in (bf, f32):
         assert route(dt, 1, 4, 32000)[0] == R
         assert route(dt, 8, 3, 32000)[0] == R
-        assert route(dt, 512, 3, 128256) == (P, 0)
+        assert route(dt, 512, 3, 128256) == (Q, 1)
+        # a claim order too large for shared memory: the persistent grid
+        assert route(dt, 100000, 3, 32000) == (P, 0)
     assert route(bf, 8, 3, 128256)[0] == R
     assert route(bf, 8, 3, 128256, greedy=True)[0] == R
     # too many units per request for one resident cluster: streaming
@@ -105,11 +107,11 @@ def test_routes():
     # the policies
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_STREAM)[0] == S
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
-    # beyond one cluster per SM: greedy calls claim requests, sampling calls
-    # take the persistent grid (the streaming policy claims in both modes)
+    # beyond one cluster per SM: claims in both modes
     assert route(bf, 512, 3, 128256, greedy=True) == (Q, 1)
     assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_STREAM) == (Q, 1)
-    assert binding.spec_verify_cluster_size(bf, 512, 3, 128256) == 0
+    assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
+    assert binding.spec_verify_cluster_size(bf, 512, 3, 128256) == 1
     assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) == route(bf, 8, 3, 128256)[1]
 
 
@@ -269,14 +271,14 @@ def test_vanished_residual_falls_back_to_p_on_every_schedule(dt):
 def test_batches_at_the_wave_limits():
     """The largest batch that fits one wave of resident clusters runs on the
     resident path and one more request on the streaming path; the largest
-    batch of the streaming path (one cluster per SM at least) and one more
-    (the persistent grid).  Each matches the other schedules and the oracle."""
+    batch of one streaming wave (one cluster per SM at least) and one more
+    (claims).  Each matches the other schedules and the oracle."""
     G, V, bf = 2, 32000, torch.bfloat16
     kinds = {B: binding.spec_verify_route(bf, B, G, V)[0] for B in range(1, 161)}
     res_limit = max(B for B, k in kinds.items() if k == binding.ROUTE_CLUSTER)
     str_limit = max(B for B, k in kinds.items() if k == binding.ROUTE_STREAM)
     assert kinds[res_limit + 1] == binding.ROUTE_STREAM
-    assert kinds[str_limit + 1] == binding.ROUTE_PERSISTENT
+    assert kinds[str_limit + 1] == binding.ROUTE_CLAIMS
     assert str_limit >= 64
     for B in (res_limit, res_limit + 1, str_limit, str_limit + 1):
         w = W.make_random(B, G, V, "bf16", seed=B, gamma="ragged",
