@@ -118,3 +118,34 @@ def test_fuzz_covers_both_cluster_paths():
         tdt = torch.bfloat16 if dt == "bf16" else torch.float32
         routes.add(binding.spec_verify_route(tdt, B, G, V)[0])
     assert routes == {binding.ROUTE_CLUSTER, binding.ROUTE_STREAM}
+
+
+def draw_large_case(i):
+    r = random.Random(9100 + i)
+    B = r.choice([160, 257, 400, 640])
+    G = r.randint(0, 7)
+    V = r.choice([33, 4097, 8193, 20001])
+    dt = r.choice(["bf16", "f32"])
+    packed = r.random() < 0.4
+    temps = [0.0 if r.random() < 0.1 else round(r.uniform(0.3, 1.6), 3) for _ in range(B)]
+    return B, G, V, dt, packed, temps
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_fuzz_claims_sampling(i):
+    """Batches beyond one wave: request claims (longest first, ragged lengths)
+    against the persistent grid and the oracle."""
+    B, G, V, dt, packed, temps = draw_large_case(i)
+    w = W.make_random(B, G, V, dt, seed=500 + i, gamma="ragged", temperature=temps).to(DEV)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    assert binding.spec_verify_route(tdt, B, G, V)[0] == binding.ROUTE_CLAIMS
+    a = run(w, packed, binding.SCHEDULE_AUTO)
+    b = run(w, packed, binding.SCHEDULE_PERSISTENT)
+    assert (a[0] == b[0]).all() and (a[1] == b[1]).all()
+    for x, y in ((a[2], b[2]), (a[3], b[3])):
+        nan = torch.isnan(y)
+        assert torch.equal(torch.isnan(x), nan) and torch.equal(x[~nan], y[~nan])
+    ref = oracle.sample(**W.oracle_inputs(w), nthreads=NTHREADS)
+    rep = compare_sample(ref, a[0], a[1], w.gamma.cpu().numpy(), a[2].numpy(), a[3].numpy())
+    assert not rep.mismatches, (draw_large_case(i)[:5], rep.mismatches[:3])
+    assert rep.max_prob_rel_err < PROB_RTOL
