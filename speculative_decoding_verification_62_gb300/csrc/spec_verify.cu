@@ -2921,8 +2921,8 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 // only smaller clusters fit the batch in one wave, the warps of request b's
 // cluster stream its items instead: warp gw of the cluster's W warps takes
 // items gw, gw + W, gw + 2W, ... (item j is chunk j % NC of the request's row
-// j / NC: target rows 0..gamma_b, then draft rows 0..gamma_b-1), two copies
-// in flight.  Partials go to every CTA's shared memory and a cluster barrier
+// j / NC: target rows 0..gamma_b, then draft rows 0..gamma_b-1) through its
+// staging buffers.  Partials go to every CTA's shared memory and a cluster barrier
 // completes them, as on the resident path; every CTA's warp 0 computes the
 // decision.  After a reject the warps stream row k's R chunks (target and
 // draft halves, usually L2 hits) and store each chunk's fixed-point sum in
@@ -2930,9 +2930,10 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 // draws from those sums and walks one chunk.  With at most one request per
 // cluster no global counter, record or queue is involved.  With more requests
 // than clusters (clusters of one CTA) each CTA takes its requests one after
-// another: the first by its index, the next from a global counter, claimed
-// while the current one is decided; the other warps start the next request's
-// items while warp 0 draws.  Shared memory: the buffers, then (the same
+// another in a claim order (longest first, below): the first at its index,
+// the next at a position from a global counter, claimed while the current one
+// is decided; the other warps start the next request's items while warp 0
+// draws.  Shared memory: the buffers, then (the same
 // layout in every CTA) the partials [2G+1][NC] and the leader's chunk sums
 // [NCR] (then, with claims, the claim order [B] and row counts [B]).  NW
 // warps per CTA with NB staging buffers each; CPS CTAs per SM (two for greedy
