@@ -103,7 +103,8 @@ def spec_verify_route(dtype: torch.dtype, B: int, G: int, V: int, greedy: bool =
 
 
 def spec_verify_cluster_size(dtype: torch.dtype, B: int, G: int, V: int, greedy: bool = False) -> int:
-    """CTAs per request of the cluster schedule (resident or streaming) for this shape, 0 for the persistent grid."""
+    """CTAs per request of the cluster schedule (resident, streaming; 1 for request claims)
+    for this shape, 0 for the persistent grid."""
     code = SV_BF16 if dtype == torch.bfloat16 else SV_F32
     rc = load_library().spec_verify_cluster_size(code, int(B), int(G), int(V), int(bool(greedy)))
     if rc < 0:

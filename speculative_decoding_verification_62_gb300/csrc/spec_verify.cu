@@ -16,7 +16,21 @@
 // packed (rows back to back, addressed through a prefix of the draft
 // lengths); a draft-token sampler (G = 0, no drafts) shares the same kernel.
 //
-// One persistent kernel per call: one CTA of 12 warps per SM.  Work items:
+// Each call is one launch of one of three kernels (the choice: `route`, near
+// the end of this file):
+//   cluster_kernel  small batches: one thread-block cluster per request whose
+//                   warps each hold one chunk of a position's target and draft
+//                   rows; partials, decision and residual stay in the
+//                   cluster's shared memory (section "Small batches" below);
+//   stream_kernel   up to one cluster per SM: the request's chunks streamed by
+//                   its cluster; beyond that, CTAs claiming whole requests in
+//                   turn, longest first (section "Medium batches");
+//   verify_kernel   the persistent grid described next, for batches whose
+//                   claim order does not fit in shared memory.
+// All three reduce items with the same routines and decide and draw with the
+// same code, so their outputs agree bit for bit.
+//
+// The persistent grid: one CTA of 12 warps per SM.  Work items:
 //   A items  8 KB of one logit row -> (max, sum of exp2((z - max) log2(e)/T))
 //            when sampling, (max, lowest index of the max) when greedy.  All
 //            A items of the batch come first, request-major: the first batch
