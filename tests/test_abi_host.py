@@ -26,6 +26,42 @@ def test_exports_every_declared_symbol():
         assert getattr(lib, n) is not None
 
 
+def header_defines():
+    """SV_* constants of the header: #define lines and enumerator values."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    d = {m.group(1): int(m.group(2), 0)
+         for m in re.finditer(r"^#define\s+(SV_\w+)\s+\(?(-?(?:0x[0-9a-fA-F]+|\d+))", text, re.M)}
+    d.update({m.group(1): int(m.group(2), 0)
+              for m in re.finditer(r"\b(SV_\w+)\s*=\s*(-?(?:0x[0-9a-fA-F]+|\d+))u?\b", text)})
+    return d
+
+
+def test_binding_constants_match_the_header():
+    """The binding's schedule, route, dtype and status constants are the
+    header's values (the binding only marshals; it must not renumber)."""
+    d = header_defines()
+    assert (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT, binding.SCHEDULE_STREAM) == (
+        d["SV_SCHEDULE_AUTO"], d["SV_SCHEDULE_PERSISTENT"], d["SV_SCHEDULE_STREAM"])
+    assert (binding.ROUTE_PERSISTENT, binding.ROUTE_CLUSTER, binding.ROUTE_STREAM, binding.ROUTE_CLAIMS) == (
+        d["SV_ROUTE_PERSISTENT"], d["SV_ROUTE_CLUSTER"], d["SV_ROUTE_STREAM"], d["SV_ROUTE_CLAIMS"])
+    for bit, name in binding.STATUS_BITS.items():
+        assert d["SV_STATUS_" + name] == bit, name
+    assert binding.SV_MAX_GAMMA == d["SV_MAX_GAMMA"]
+    assert (binding.SV_F32, binding.SV_BF16) == (d["SV_F32"], d["SV_BF16"])
+
+
+def test_set_schedule_rejects_unknown_policies():
+    prev = binding.spec_verify_set_schedule(binding.SCHEDULE_AUTO)
+    try:
+        for bad in (-1, 3, 99):
+            with pytest.raises(binding.SpecVerifyError):
+                binding.spec_verify_set_schedule(bad)
+        assert binding.spec_verify_set_schedule(binding.SCHEDULE_STREAM) == binding.SCHEDULE_AUTO
+        assert binding.spec_verify_set_schedule(binding.SCHEDULE_AUTO) == binding.SCHEDULE_STREAM
+    finally:
+        binding.spec_verify_set_schedule(prev)
+
+
 def test_workspace_size():
     s = binding.spec_verify_workspace_size(8, 3, 128256)
     assert s > 0 and s % 256 == 0
