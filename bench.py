@@ -84,7 +84,8 @@ def across_ranks(ms: float, units, world: int, device=None):
 def workload_desc(w, mode):
     from speculative_decoding_verification_62_gb300 import workloads as W
     return {"workload": f"config {w.name}: {W.CONFIGS[w.name]['desc']}", "B": w.B,
-            "gamma_max": w.G, "gamma_sum": w.gamma_sum(), "V": w.V, "mode": mode}
+            "gamma_max": w.G, "gamma_sum": w.gamma_sum(), "V": w.V, "mode": mode,
+            "input_sha256": w.sha256()}
 
 
 # ---------------------------------------------------------------------------

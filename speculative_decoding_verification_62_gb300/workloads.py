@@ -15,6 +15,7 @@ in for them.
 """
 from __future__ import annotations
 
+import hashlib
 import math
 from dataclasses import dataclass, field
 
@@ -83,6 +84,16 @@ class Workload:
         return Workload(self.name, *(getattr(self, k).to(device) for k in
                                      ("target", "draft", "draft_tokens", "gamma",
                                       "uniforms", "temperature")), dict(self.meta))
+
+    def sha256(self) -> str:
+        """SHA-256 of the input bytes (target, draft, draft tokens, gamma,
+        uniforms, temperature in that order, each row-major), so that a
+        measurement names exactly what it ran on."""
+        h = hashlib.sha256()
+        for k in ("target", "draft", "draft_tokens", "gamma", "uniforms", "temperature"):
+            t = getattr(self, k).detach().contiguous().cpu()
+            h.update(t.view(torch.uint8).numpy().tobytes() if t.numel() else b"")
+        return h.hexdigest()
 
 
 def _gen(device, seed):

@@ -44,3 +44,16 @@ def test_oracle_inputs_roundtrip_bf16_bits():
     assert o["target"].dtype == np.uint16
     back = torch.from_numpy(o["target"].view(np.int16)).view(torch.bfloat16)
     assert torch.equal(back, w.target)
+
+
+def test_input_digest_names_the_bytes():
+    """The bench reports the inputs' SHA-256: equal seeds give equal digests,
+    and any change of the bytes changes it."""
+    a = W.make_random(3, 2, 50, "bf16", seed=5)
+    b = W.make_random(3, 2, 50, "bf16", seed=5)
+    c = W.make_random(3, 2, 50, "bf16", seed=6)
+    assert a.sha256() == b.sha256() and len(a.sha256()) == 64
+    assert a.sha256() != c.sha256()
+    b.uniforms[0, 0] = 0.5 if float(b.uniforms[0, 0]) != 0.5 else 0.25
+    assert a.sha256() != b.sha256()
+    assert W.make_random(1, 0, 7, "f32", seed=1).sha256() == W.make_random(1, 0, 7, "f32", seed=1).sha256()
