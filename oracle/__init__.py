@@ -61,7 +61,7 @@ class Oracle:
         vp, c_int = ctypes.c_void_p, ctypes.c_int
         lib.sv_ref_sample.restype = c_int
         lib.sv_ref_sample.argtypes = [vp, vp, c_int, c_int, c_int, c_int, vp, vp, vp, vp,
-                                      vp, vp, vp, vp, vp, vp, c_int]
+                                      vp, vp, vp, vp, vp, vp, vp, c_int, c_int]
         lib.sv_ref_greedy.restype = c_int
         lib.sv_ref_greedy.argtypes = [vp, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp,
                                       c_int]
@@ -70,15 +70,19 @@ class Oracle:
         self.lib = lib
         self.path = path
 
-    def sample(self, target, draft, draft_tokens, gamma, uniforms, temperature, nthreads=0):
+    def sample(self, target, draft, draft_tokens, gamma, uniforms, temperature, nthreads=0,
+               rows_first=False):
         """Sampling verify step.
 
         target [B][G+1][V], draft [B][G][V] (float32, or uint16 bf16 bits);
         draft_tokens int32 [B][G]; gamma int32 [B]; uniforms [B][G+1] (float32 or
-        float64; widened exactly); temperature float32 [B].
+        float64; widened exactly); temperature float32 [B].  rows_first spreads
+        the row statistics over threads before the requests (same results).
 
         Returns a dict with out_tokens [B][G+1], num_accepted [B], p_tok/q_tok
-        [B][G], margin_accept [B][G] (NaN where not evaluated) and margin_cdf [B].
+        [B][G], margin_accept [B][G] (NaN where not evaluated), margin_cdf [B]
+        and resid_mass [B] (the float64 residual mass after a rejection, NaN
+        when every draft was accepted or the request is greedy).
         """
         target, dt = _logits(target, "target")
         B, G1, V = target.shape
@@ -99,14 +103,15 @@ class Oracle:
         q_tok = np.empty((B, G))
         m_acc = np.empty((B, G))
         m_cdf = np.empty(B)
+        mass = np.empty(B)
         rc = self.lib.sv_ref_sample(_ptr(target), _ptr(draft), dt, B, G, V, _ptr(tokens),
                                     _ptr(gamma), _ptr(u), _ptr(temp), _ptr(out), _ptr(nacc),
                                     _ptr(p_tok), _ptr(q_tok), _ptr(m_acc), _ptr(m_cdf),
-                                    int(nthreads))
+                                    _ptr(mass), 1 if rows_first else 0, int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle rejected the input (code {rc})")
         return dict(out_tokens=out, num_accepted=nacc, p_tok=p_tok, q_tok=q_tok,
-                    margin_accept=m_acc, margin_cdf=m_cdf)
+                    margin_accept=m_acc, margin_cdf=m_cdf, resid_mass=mass)
 
     def greedy(self, target, draft_tokens, gamma, nthreads=0):
         """Greedy (argmax-match) verify step: out_tokens, num_accepted, exact_tie."""

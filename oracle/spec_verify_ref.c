@@ -38,7 +38,13 @@
  *  - no epsilons are added to q or to the residual sum.
  *  - the resample/bonus draws use their own uniform u[b][G]; the inverse CDF
  *    runs over ascending token id and returns the smallest j with C_j > u*S.
- *    If rounding leaves no such j, the largest j with r_j > 0 is returned.
+ *    If rounding leaves no such j, the largest j with r_j > 0 is returned:
+ *    the token the exact inequality u*S < S selects.  (C_{V-1} is the same
+ *    ascending sum as S, and u*S < S for u < 1 whenever S is a normal double,
+ *    so this happens only when S is subnormal.)
+ *  - "the residual sum is zero" is tested on the float64 sum; the mass itself
+ *    is reported (resid_mass) so that a caller can tell a residual that
+ *    cancelled to within rounding from a clear one.
  *  - num_accepted counts accepted drafts only (emitted = num_accepted + 1).
  *  - greedy argmax ties go to the lowest token id.
  *
@@ -113,8 +119,9 @@ static double prob_of(const void *base, int dtype, size_t off, int x, double T,
 /*
  * Inverse-CDF draw over weights r[0..V-1] with total S, driven by u in [0,1):
  * the smallest j whose inclusive prefix C_j exceeds u*S.  If rounding leaves
- * none, the largest j with r[j] > 0.  *margin gets the distance of u*S to the
- * nearer edge of j's interval, divided by S.
+ * none (only for a subnormal S, where u*S can round up to S), the largest j
+ * with r[j] > 0, which is the token the exact u*S < S selects.  *margin gets
+ * the distance of u*S to the nearer edge of j's interval, divided by S.
  */
 static int inverse_cdf(const double *r, int V, double S, double u, double *margin) {
   double target = u * S;
@@ -184,7 +191,10 @@ typedef struct {
   const float *temperature;
   int32_t *out_tokens;
   int32_t *num_accepted;
-  double *p_tok, *q_tok, *margin_accept, *margin_cdf;
+  double *p_tok, *q_tok, *margin_accept, *margin_cdf, *resid_mass;
+  /* optional row statistics computed beforehand (rows-first mode): max and
+   * sum of target row i at stats_t[b*(G+1)+i], draft row i at stats_d[b*G+i] */
+  const double *stats_t_m, *stats_t_s, *stats_d_m, *stats_d_s;
 } sample_args;
 
 /* One request of the sampling verify step; returns 0, or -3 on malloc failure. */
@@ -200,6 +210,7 @@ static int sample_one(const sample_args *a, int b) {
     for (int i = 0; i < G; ++i) a->p_tok[(size_t)b * G + i] = NAN;
   if (a->q_tok)
     for (int i = 0; i < G; ++i) a->q_tok[(size_t)b * G + i] = NAN;
+  if (a->resid_mass) a->resid_mass[b] = NAN;
 
   if (T == 0.0) {
     /* Temperature 0: the greedy steps.  There is no ratio and no CDF draw; an
@@ -221,8 +232,15 @@ static int sample_one(const sample_args *a, int b) {
   for (int i = 0; i < gb; ++i) {
     const int x = a->tokens[(size_t)b * G + i];
     double mt, st, md, sd;
-    softmax_row(a->target, a->dtype, target_row(b, i, G, V), V, T, NULL, &mt, &st);
-    softmax_row(a->draft, a->dtype, draft_row(b, i, G, V), V, T, NULL, &md, &sd);
+    if (a->stats_t_m) { /* the same softmax_row results, computed beforehand */
+      mt = a->stats_t_m[(size_t)b * (G + 1) + i];
+      st = a->stats_t_s[(size_t)b * (G + 1) + i];
+      md = a->stats_d_m[(size_t)b * G + i];
+      sd = a->stats_d_s[(size_t)b * G + i];
+    } else {
+      softmax_row(a->target, a->dtype, target_row(b, i, G, V), V, T, NULL, &mt, &st);
+      softmax_row(a->draft, a->dtype, draft_row(b, i, G, V), V, T, NULL, &md, &sd);
+    }
     const double p = prob_of(a->target, a->dtype, target_row(b, i, G, V), x, T, mt, st);
     const double q = prob_of(a->draft, a->dtype, draft_row(b, i, G, V), x, T, md, sd);
     if (a->p_tok) a->p_tok[(size_t)b * G + i] = p;
@@ -261,6 +279,7 @@ static int sample_one(const sample_args *a, int b) {
       S += r[v];
     }
     free(q);
+    if (a->resid_mass) a->resid_mass[b] = S;
     if (S == 0.0) { /* residual vanished: fall back to p */
       for (int v = 0; v < V; ++v) {
         r[v] = p[v];
@@ -296,16 +315,26 @@ static int check_common(int B, int G, int V, int dtype, const int32_t *tokens,
 }
 
 /*
- * Sampling verify step for B requests.  p_tok, q_tok, margin_accept ([B][G])
- * and margin_cdf ([B]) are optional (NULL).  margin_accept[b][i] is |u - ratio|
- * for every evaluated position, NaN elsewhere.  Returns 0, -1 on invalid input,
- * -3 on allocation failure.  nthreads <= 0 uses the OpenMP default.
+ * Sampling verify step for B requests.  p_tok, q_tok, margin_accept ([B][G]),
+ * margin_cdf and resid_mass ([B]) are optional (NULL).  margin_accept[b][i] is
+ * |u - ratio| for every evaluated position, NaN elsewhere; resid_mass[b] is
+ * the float64 sum of max(0, p_k - q_k) after a rejection at k, NaN when every
+ * draft was accepted.  Returns 0, -1 on invalid input, -3 on allocation
+ * failure.  nthreads <= 0 uses the OpenMP default.
+ *
+ * rows_first != 0 changes only how the work is spread over threads: the
+ * maximum and sum of every row that the acceptance tests may need (target
+ * rows 0..gamma_b, draft rows 0..gamma_b-1) are computed first, one row per
+ * OpenMP iteration, by the same softmax_row; the requests then run as before
+ * on those values.  The results are identical; it serves batches with fewer
+ * requests than threads.
  */
 int sv_ref_sample(const void *target_logits, const void *draft_logits, int dtype, int B,
                   int G, int V, const int32_t *draft_tokens, const int32_t *gamma,
                   const double *uniforms, const float *temperature, int32_t *out_tokens,
                   int32_t *num_accepted, double *p_tok, double *q_tok,
-                  double *margin_accept, double *margin_cdf, int nthreads) {
+                  double *margin_accept, double *margin_cdf, double *resid_mass,
+                  int rows_first, int nthreads) {
   if (check_common(B, G, V, dtype, draft_tokens, gamma)) return -1;
   if (G > 63) return -1;
   for (int b = 0; b < B; ++b) {
@@ -317,10 +346,42 @@ int sv_ref_sample(const void *target_logits, const void *draft_logits, int dtype
   }
   sample_args a = {target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma,
                    uniforms, temperature, out_tokens, num_accepted, p_tok, q_tok,
-                   margin_accept, margin_cdf};
-  int err = 0;
+                   margin_accept, margin_cdf, resid_mass, NULL, NULL, NULL, NULL};
 #ifdef _OPENMP
   if (nthreads <= 0) nthreads = omp_get_max_threads();
+#endif
+  double *stats = NULL;
+  if (rows_first && B > 0) {
+    /* rows (b, i): target rows i = 0..G, then draft rows i = 0..G-1 */
+    const size_t nt = (size_t)B * (size_t)(G + 1), nd = (size_t)B * (size_t)G;
+    stats = (double *)malloc(sizeof(double) * 2 * (nt + nd));
+    if (!stats) return -3;
+    double *tm = stats, *ts = stats + nt, *dm = stats + 2 * nt, *ds = stats + 2 * nt + nd;
+    const long nrows = (long)(nt + nd);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long r = 0; r < nrows; ++r) {
+      if ((size_t)r < nt) {
+        const int b = (int)(r / (G + 1)), i = (int)(r % (G + 1));
+        if (i <= gamma[b] && temperature[b] != 0.0f)
+          softmax_row(target_logits, dtype, target_row(b, i, G, V), V,
+                      (double)temperature[b], NULL, &tm[r], &ts[r]);
+      } else {
+        const size_t rd = (size_t)r - nt;
+        const int b = (int)(rd / (size_t)G), i = (int)(rd % (size_t)G);
+        if (i < gamma[b] && temperature[b] != 0.0f)
+          softmax_row(draft_logits, dtype, draft_row(b, i, G, V), V,
+                      (double)temperature[b], NULL, &dm[rd], &ds[rd]);
+      }
+    }
+    a.stats_t_m = tm;
+    a.stats_t_s = ts;
+    a.stats_d_m = dm;
+    a.stats_d_s = ds;
+  }
+  int err = 0;
+#ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(min : err)
 #endif
   for (int b = 0; b < B; ++b) {
@@ -328,6 +389,7 @@ int sv_ref_sample(const void *target_logits, const void *draft_logits, int dtype
     if (e < err) err = e;
   }
   (void)nthreads;
+  free(stats);
   return err;
 }
 

@@ -13,10 +13,6 @@ describe, written as plain host logic (no GPU work):
   about round(average) + 1, kept between the smallest and largest candidate,
   and fixed at 1 from 32 concurrent requests on (same page, the section on
   SGLang's adaptive setting; default candidates 1, 3, 7).
-* ``WindowedRateStep``: a sliding window over observed acceptance rates that
-  lengthens the draft by one above a high rate and shortens it by one below a
-  low rate, within bounds ("LLM speculative decoding optimisation", dynamic
-  speculation strategy).
 * ``AcceptanceEstimator`` and ``optimal_gamma``: an online estimate of the
   per-position acceptance rate alpha from (gamma, num_accepted) pairs, and the
   draft length that maximises the expected speedup
@@ -188,31 +184,6 @@ class AcceptLengthEMA:
         return self.ema[i]
 
 
-class WindowedRateStep:
-    """Sliding window of observed acceptance rates; one step longer above
-    `high`, one step shorter below `low`, within [min_len, max_len]."""
-
-    def __init__(self, min_len: int = 2, max_len: int = 8, start: int = 5, window: int = 100,
-                 low: float = 0.65, high: float = 0.85):
-        if not min_len <= start <= max_len:
-            raise ValueError("start must lie in [min_len, max_len]")
-        if not 0.0 <= low < high <= 1.0:
-            raise ValueError("need 0 <= low < high <= 1")
-        self.min_len, self.max_len, self.length = min_len, max_len, start
-        self.window, self.low, self.high = int(window), low, high
-        self.rates = []
-
-    def update(self, rate: float) -> int:
-        self.rates.append(float(rate))
-        del self.rates[:-self.window]
-        mean = sum(self.rates) / len(self.rates)
-        if mean > self.high:
-            self.length = min(self.length + 1, self.max_len)
-        elif mean < self.low:
-            self.length = max(self.length - 1, self.min_len)
-        return self.length
-
-
 def acceptance_rate(gamma, num_accepted) -> float:
     """Fraction of drafted tokens accepted in one verify (0 if none drafted)."""
     g = sum(int(x) for x in gamma)
@@ -220,4 +191,4 @@ def acceptance_rate(gamma, num_accepted) -> float:
 
 
 __all__ = ["expected_tokens", "speedup", "optimal_gamma", "AcceptanceEstimator",
-           "BatchSizeTable", "AcceptLengthEMA", "WindowedRateStep", "acceptance_rate"]
+           "BatchSizeTable", "AcceptLengthEMA", "acceptance_rate"]

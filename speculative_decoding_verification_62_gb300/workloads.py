@@ -4,7 +4,10 @@ This module only draws inputs.  It holds none of the verify step's arithmetic
 (no softmax, ratio, residual or inverse CDF): draft tokens are drawn from q by
 the Gumbel-max trick (argmax of logits/T plus Gumbel noise), which samples
 softmax(logits/T) exactly without forming it.  Both the CUDA path's tests and
-the oracle consume the same bytes produced here.
+the oracle consume the same bytes produced here.  Every draw runs on the CPU
+with torch's CPU generator, whatever device the batch is then moved to, so a
+workload name and seed always name the same bytes (the bench's GPU arm, its
+CPU baseline and the reference arm hash identical inputs).
 
 The five standard workloads restate the configurations of the verify-step
 benchmark: vocabulary sizes of Llama-3-style (128256) and Qwen2.5-style
@@ -123,7 +126,15 @@ def _round(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def make(name: str, device="cpu", seed: int | None = None) -> Workload:
-    """Build one of the standard workloads ("1", "2", "3", "4", "5a", "5b")."""
+    """Build one of the standard workloads ("1", "2", "3", "4", "5a", "5b").
+
+    The inputs are drawn on the CPU and then moved to `device`."""
+    w = _make_cpu(name, seed)
+    return w if torch.device(device) == torch.device("cpu") else w.to(device)
+
+
+def _make_cpu(name: str, seed: int | None) -> Workload:
+    device = "cpu"
     cfg = CONFIGS[name]
     B, G, V, dt = cfg["B"], cfg["G"], cfg["V"], cfg["dtype"]
     base = 620 + int(name[0]) if seed is None else int(seed)
@@ -191,7 +202,14 @@ def make_random(B: int, G: int, V: int, dtype: str = "bf16", device="cpu", seed:
 
     gamma: None (all G), "ragged" (U{0..G}), or an explicit list.
     temperature: None (1.0), a float, or a list of per-request values.
+    Drawn on the CPU, then moved to `device`.
     """
+    w = _make_random_cpu(B, G, V, dtype, seed, gamma, temperature, sigma_t, sigma_d)
+    return w if torch.device(device) == torch.device("cpu") else w.to(device)
+
+
+def _make_random_cpu(B, G, V, dtype, seed, gamma, temperature, sigma_t, sigma_d) -> Workload:
+    device = "cpu"
     gen = _gen(device, seed)
     f32 = dict(device=device, dtype=torch.float32)
     t = torch.randn((B, G + 1, V), generator=gen, **f32) * sigma_t

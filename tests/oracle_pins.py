@@ -461,3 +461,53 @@ def check_accept_strict(oracle):
                       np.ones(2, np.float32))
     assert list(r["num_accepted"]) == [0, 1], r["num_accepted"]
     assert r["p_tok"][0, 0] == 0.25 and r["q_tok"][0, 0] == 0.5
+
+
+def check_vanished_residual_falls_back_to_p(oracle):
+    """The residual's fallback ([theory], modified-distribution code: draw from
+    p when sum max(0, p - q) is zero), on a case fixed by hand.  V = 2, T = 1,
+    target row (0, 50), draft row (0, 49.75), draft token 0: in float64
+    1 + e^-50 == 1 and 1 + e^-49.75 == 1, so p = (e^-50, 1) and
+    q = (e^-49.75, 1) with no rounding in the sums; the ratio e^-0.25 ~ 0.78
+    rejects at u = 0.9 and max(0, p - q) is (0, 0).  The draw then follows p's
+    inverse CDF: u = 0 gives token 0 (p_0 > 0, which an argmax fallback would
+    not give), u = 2.2e-22 lies between p_0 = e^-50 ~ 1.93e-22 and
+    q_0 = e^-49.75 ~ 2.48e-22 and gives token 1 (a fallback to q would give
+    0).  The reported residual mass is exactly 0."""
+    assert 1.0 + math.exp(-50.0) == 1.0 and 1.0 + math.exp(-49.75) == 1.0
+    assert math.exp(-50.0) < 2.2e-22 < math.exp(-49.75)
+    n = 2
+    t = np.array([[[0.0, 50.0], [0.0, 0.0]]] * n, np.float32)
+    d = np.array([[[0.0, 49.75]]] * n, np.float32)
+    u = np.array([[0.9, 0.0], [0.9, 2.2e-22]])
+    r = oracle.sample(t, d, np.zeros((n, 1), np.int32), np.ones(n, np.int32), u,
+                      np.ones(n, np.float32))
+    assert list(r["num_accepted"]) == [0, 0], r["num_accepted"]
+    assert list(r["out_tokens"][:, 0]) == [0, 1], r["out_tokens"]
+    assert np.all(r["out_tokens"][:, 1] == -1)
+    assert np.all(r["resid_mass"] == 0.0), r["resid_mass"]
+
+
+def check_subnormal_residual_draw(oracle):
+    """The inverse CDF's rounding case, fixed by hand: a residual whose whole
+    mass is subnormal, where u*S rounds up to S.  V = 5, T = 1, target row
+    (0, 2, 1, -1000, 741), draft row (1, 1, 0.5, -1000, 741), draft token 0.
+    Both sums are 1 + (subnormals) == 1, so p_v = e^(z_v - 741),
+    q_v = e^(y_v - 741): p_0/q_0 ~ e^-1 rejects at u = 0.9 and the residual
+    max(0, p - q) is positive at tokens 1 and 2 only (r_1 ~ 139, r_2 ~ 34 units
+    of 2^-1074, tokens 3 and 4 exactly 0).  u = 0.5 selects token 1
+    (r_1 > r_2).  u = 1 - 2^-53 makes u*S round to S, where no prefix exceeds
+    u*S; the exact u*S < S selects the last token of positive weight, 2 (not
+    0, not V - 1, not the largest weight 1).  The reported mass is that
+    subnormal sum."""
+    sub = lambda x: 0.0 < x < np.finfo(np.float64).tiny  # noqa: E731
+    assert sub(math.exp(-739.0)) and sub(math.exp(-741.0))
+    n = 2
+    t = np.array([[[0.0, 2.0, 1.0, -1000.0, 741.0], [0.0] * 5]] * n, np.float32)
+    d = np.array([[[1.0, 1.0, 0.5, -1000.0, 741.0]]] * n, np.float32)
+    u = np.array([[0.9, 0.5], [0.9, float(ONE_MINUS)]])
+    r = oracle.sample(t, d, np.zeros((n, 1), np.int32), np.ones(n, np.int32), u,
+                      np.ones(n, np.float32))
+    assert list(r["num_accepted"]) == [0, 0], r["num_accepted"]
+    assert list(r["out_tokens"][:, 0]) == [1, 2], r["out_tokens"]
+    assert np.all(sub(m) for m in r["resid_mass"]), r["resid_mass"]

@@ -245,8 +245,9 @@ def test_vanished_residual_falls_back_to_p_on_every_schedule(dt):
     the target and draft rows agree elsewhere, so u = 0.9 rejects (ratio 1/2)
     while sum max(0, p - q) ~ p(x) rounds to 0 in units of 2^-39.  Both
     schedules then draw from p_k; their tokens must agree, and the token must
-    have p > 0.  (The float64 oracle's residual is pure cancellation noise
-    here, so it is not the reference for this case.)"""
+    have p > 0.  Against the oracle the acceptance decisions agree exactly
+    and the draw is a residual-mass near tie (float64 mass below 1e-6: the
+    residual is cancellation noise), counted by the comparison."""
     B, G, V = 3, 1, 4096
     w = W.make_random(B, G, V, dt, seed=31, sigma_t=1.0, sigma_d=0.0)
     x = 17
@@ -266,6 +267,10 @@ def test_vanished_residual_falls_back_to_p_on_every_schedule(dt):
     for b in range(B):
         assert 0 <= out[b, 0] < V and out[b, 0] != x and p[b, out[b, 0]] > 0
         assert out[b, 1] == -1
+    ref = oracle.sample(**W.oracle_inputs(w))
+    rep = compare_sample(ref, out, nacc, w.gamma.cpu().numpy())
+    assert not rep.mismatches, rep.mismatches
+    assert rep.near_tie_resid == B and (ref["resid_mass"] < 1e-6).all(), ref["resid_mass"]
 
 
 def test_batches_at_the_wave_limits():

@@ -48,6 +48,28 @@ MUTANTS = {
                                 "tokens[(size_t)b * G + i] == best + V"),
     "truncation_keeps_rejected_draft": ("      k = i;\n      break;",
                                         "      k = i + 1;\n      out[i] = x;\n      break;"),
+    "vanished_residual_no_fallback": ("    if (S == 0.0) { /* residual vanished: fall back to p */",
+                                      "    if (S < 0.0) { /* residual vanished: fall back to p */"),
+    "vanished_residual_falls_back_to_q": (
+        "    free(q);\n    if (a->resid_mass) a->resid_mass[b] = S;\n"
+        "    if (S == 0.0) { /* residual vanished: fall back to p */\n"
+        "      for (int v = 0; v < V; ++v) {\n        r[v] = p[v];",
+        "    if (a->resid_mass) a->resid_mass[b] = S;\n"
+        "    if (S == 0.0) { /* residual vanished: fall back to p */\n"
+        "      for (int v = 0; v < V; ++v) {\n        r[v] = q[v];"),
+    "vanished_residual_falls_back_to_argmax": (
+        "      for (int v = 0; v < V; ++v) {\n        r[v] = p[v];\n        S += r[v];\n      }\n    }\n  } else {",
+        "      int am = 0;\n      for (int v = 1; v < V; ++v) if (p[v] > p[am]) am = v;\n"
+        "      for (int v = 0; v < V; ++v) {\n        r[v] = v == am ? 1.0 : 0.0;\n        S += r[v];\n"
+        "      }\n    }\n  } else {"),
+    "cdf_rounding_takes_first_positive": ("  for (int j = V - 1; j >= 0; --j) {\n    if (r[j] > 0.0) {",
+                                          "  for (int j = 0; j < V; ++j) {\n    if (r[j] > 0.0) {"),
+    "cdf_rounding_takes_last_token": ("  for (int j = V - 1; j >= 0; --j) {\n    if (r[j] > 0.0) {",
+                                      "  for (int j = V - 1; j >= 0; --j) {\n    if (j == V - 1) {"),
+    "cdf_rounding_takes_largest_weight": (
+        "  for (int j = V - 1; j >= 0; --j) {\n    if (r[j] > 0.0) {\n      *margin = 0.0;\n      return j;",
+        "  for (int j = V - 1; j >= 0; --j) {\n    if (r[j] > 0.0) {\n      int am = 0;\n"
+        "      for (int i = 1; i < V; ++i) if (r[i] > r[am]) am = i;\n      *margin = 0.0;\n      return am;"),
 }
 
 
@@ -60,6 +82,8 @@ def _quick_pins(o):
         ("lossless_gamma2", lambda: pins.check_lossless_gamma2(o, cases[0])),
         ("accept_strict", lambda: pins.check_accept_strict(o)),
         ("inverse_cdf_boundaries", lambda: pins.check_inverse_cdf_boundaries(o)),
+        ("vanished_residual", lambda: pins.check_vanished_residual_falls_back_to_p(o)),
+        ("subnormal_residual", lambda: pins.check_subnormal_residual_draw(o)),
         ("gamma0", lambda: pins.check_gamma0_bonus_only(o)),
         ("softmax", lambda: pins.check_softmax(o)),
         ("p_q_at_tokens", lambda: pins.check_p_q_at_tokens(o)),

@@ -65,6 +65,14 @@ def test_inverse_cdf_boundaries():
     pins.check_inverse_cdf_boundaries(ORACLE)
 
 
+def test_vanished_residual_falls_back_to_p():
+    pins.check_vanished_residual_falls_back_to_p(ORACLE)
+
+
+def test_subnormal_residual_draw():
+    pins.check_subnormal_residual_draw(ORACLE)
+
+
 def test_gamma0_bonus_only():
     pins.check_gamma0_bonus_only(ORACLE)
 
@@ -142,3 +150,21 @@ def test_threads_do_not_change_results():
     b = ORACLE.sample(t, d, x, g, u, T, nthreads=4)
     for k in ("out_tokens", "num_accepted"):
         assert np.array_equal(a[k], b[k])
+
+
+def test_rows_first_gives_identical_results():
+    """rows_first only spreads the row statistics over threads first: every
+    output (tokens, counts, probabilities, margins, residual mass) is
+    bit-identical, including zero-temperature requests and gamma_b = 0."""
+    rng = np.random.default_rng(13)
+    B, G, V = 7, 4, 333
+    t = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    d = (t[:, :G] + rng.normal(0, 1, (B, G, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    g = np.array([4, 0, 2, 4, 1, 3, 4], np.int32)
+    u = rng.random((B, G + 1)).astype(np.float32)
+    T = np.array([1.0, 0.5, 0.0, 1.5, 1.0, 0.8, 1.2], np.float32)
+    a = ORACLE.sample(t, d, x, g, u, T, nthreads=1)
+    b = ORACLE.sample(t, d, x, g, u, T, nthreads=8, rows_first=True)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True), k

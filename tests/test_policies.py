@@ -98,13 +98,3 @@ def test_accept_length_ema():
     q.observe(2, [0])
     assert q.ema[q._range(2)] == pytest.approx(2.0)
     assert q.steps(2) == 3
-
-
-def test_windowed_rate_step():
-    p = pol.WindowedRateStep()
-    assert [p.update(0.9) for _ in range(5)] == [6, 7, 8, 8, 8]
-    q = pol.WindowedRateStep(window=3)
-    for _ in range(3):
-        q.update(0.9)
-    # window [0.9, 0.9, 0.1] already averages 0.633 < 0.65: one step shorter each time
-    assert [q.update(0.1) for _ in range(7)] == [7, 6, 5, 4, 3, 2, 2]
