@@ -293,6 +293,18 @@ const char *spec_verify_strerror(int code);
 #define SV_ROUTE_CLAIMS 3
 int spec_verify_set_schedule(int schedule);
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int *cluster_size);
+
+/*
+ * spec_verify_set_wait_limit: the limit, in nanoseconds of the GPU's global
+ * timer, of every bounded wait in the calls that follow in this process (a
+ * bulk copy's completion, a decision record, a queue slot); 0 restores the
+ * default of 2 s.  A wait that runs out sets SV_STATUS_TIMEOUT and its warp
+ * stops taking work, so the call returns with incomplete outputs and the
+ * workspace must be zero-filled again (as documented for that bit).  Not a
+ * step of the method: it exists so that tests can make a wait run out
+ * quickly.  Returns the previous limit.
+ */
+unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
 int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy);
 
 #ifdef __cplusplus

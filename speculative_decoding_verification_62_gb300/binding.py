@@ -24,7 +24,8 @@ SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_greedy",
            "spec_verify_sample_packed", "spec_verify_greedy_packed", "spec_verify_draw",
            "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror",
-           "spec_verify_set_schedule", "spec_verify_route", "spec_verify_cluster_size")
+           "spec_verify_set_schedule", "spec_verify_route", "spec_verify_cluster_size",
+           "spec_verify_set_wait_limit")
 SCHEDULE_AUTO, SCHEDULE_PERSISTENT, SCHEDULE_STREAM = 0, 1, 2
 ROUTE_PERSISTENT, ROUTE_CLUSTER, ROUTE_STREAM, ROUTE_CLAIMS = 0, 1, 2, 3
 
@@ -74,6 +75,8 @@ def load_library():
         lib.spec_verify_route.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(ci)]
         lib.spec_verify_cluster_size.restype = ci
         lib.spec_verify_cluster_size.argtypes = [ci, ci, ci, ci, ci]
+        lib.spec_verify_set_wait_limit.restype = ctypes.c_ulonglong
+        lib.spec_verify_set_wait_limit.argtypes = [ctypes.c_ulonglong]
         _lib = lib
         return lib
 
@@ -89,6 +92,12 @@ def spec_verify_set_schedule(schedule: int) -> int:
     if rc < 0:
         raise SpecVerifyError(rc)
     return rc
+
+
+def spec_verify_set_wait_limit(ns: int) -> int:
+    """Limit (ns) of every bounded wait in later calls (0: the 2 s default);
+    returns the previous limit."""
+    return int(load_library().spec_verify_set_wait_limit(int(ns)))
 
 
 def spec_verify_route(dtype: torch.dtype, B: int, G: int, V: int, greedy: bool = False):

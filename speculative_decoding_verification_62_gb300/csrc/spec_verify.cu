@@ -109,7 +109,7 @@ constexpr unsigned int kMaxRBatch = SV_MAXKR;         // R items per claim, at m
 // on B = 64..512 found the largest batches best: claims cost more than
 // the longer hold of the last requests' items)
 constexpr unsigned int kBatchDiv = SV_BATCH_DIV;
-constexpr unsigned long long kWaitNs = 2000000000ull; // every wait gives up after 2 s
+constexpr unsigned long long kWaitNs = 2000000000ull; // default wait limit: 2 s
 
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
 constexpr float kLog2eLo = 1.925963033500011e-08f;          // log2(e) - kLog2eHi
@@ -186,6 +186,7 @@ struct Params {
   double* p_tok;
   double* q_tok;
   unsigned int* status;
+  unsigned long long wait_ns;  // every bounded wait gives up after this long
   unsigned int* next_item;   // next A item to claim (past the fixed first batches)
   unsigned int* r_next;      // next R item to claim: item i is chunk i % NCR of the
                              // request in queue slot i / NCR
@@ -244,13 +245,14 @@ __device__ __forceinline__ unsigned long long now_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+// Bounded wait for the phase with the given parity; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = now_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (now_ns() - t0 > kWaitNs) return false;
+    if (now_ns() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes,
@@ -1387,7 +1389,7 @@ __device__ __noinline__ void final_draw(const Params& P, int b, TempC tc, unsign
     bool ok = false;
     if (lane == 0) {
       const unsigned long long t0 = now_ns();
-      while (!(ok = read_record(&P.dec[b], rb, d)) && now_ns() - t0 < kWaitNs) __nanosleep(64);
+      while (!(ok = read_record(&P.dec[b], rb, d)) && now_ns() - t0 < P.wait_ns) __nanosleep(64);
     }
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) flags |= SV_STATUS_TIMEOUT;
     d.k = __shfl_sync(0xffffffffu, d.k, 0);
@@ -2199,7 +2201,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
     // 2. process the oldest item in flight
     if (issued != processed) {
       const int s = (int)(processed % kNB);
-      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u)) {
+      if (!mbar_wait(&mybar[s], (processed / kNB) & 1u, P.wait_ns)) {
         flags |= SV_STATUS_TIMEOUT;
         failed = true;
         break;
@@ -2261,7 +2263,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
             state = 2;
             break;
           }
-          if (now_ns() - t0 > kWaitNs) {
+          if (now_ns() - t0 > P.wait_ns) {
             state = 1;
             break;
           }
@@ -2288,7 +2290,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(Params P) {
   // No copy may still be landing in this warp's buffers when it leaves.
   if (failed) {
     for (unsigned int p = processed; p < issued; ++p)
-      (void)mbar_wait(&mybar[p % kNB], (p / kNB) & 1u);
+      (void)mbar_wait(&mybar[p % kNB], (p / kNB) & 1u, P.wait_ns);
   } else {
     flush();
     settle();
@@ -2719,7 +2721,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
     // lane r < C stores each partial into CTA r: every CTA decides locally
     const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
     for (int h = 0; h < nitem; ++h) {  // every copy is waited for (bounded)
-      if (!mbar_wait(&mybar[h], 0u)) {
+      if (!mbar_wait(&mybar[h], 0u, P.wait_ns)) {
         flags |= SV_STATUS_TIMEOUT;
         failed = true;
       }
@@ -3012,7 +3014,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
   };
   // Wait for the oldest copy in flight; false after the bounded wait gave up.
   auto wait_oldest = [&]() -> bool {
-    if (mbar_wait(&mybar[processed % NB], (processed / NB) & 1u)) return true;
+    if (mbar_wait(&mybar[processed % NB], (processed / NB) & 1u, P.wait_ns)) return true;
     flags |= SV_STATUS_TIMEOUT;
     failed = true;
     return false;
@@ -3197,7 +3199,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
         // could not be read: every CTA then holds the same table and takes the
         // same branches below.  Copies in flight are waited for (bounded).
         for (; processed != issued; ++processed) {
-          (void)mbar_wait(&mybar[processed % NB], (processed / NB) & 1u);
+          (void)mbar_wait(&mybar[processed % NB], (processed / NB) & 1u, P.wait_ns);
           store_part(mymeta[processed % NB], make_float2(NAN, 0.0f));
           __syncwarp();
         }
@@ -3290,7 +3292,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
       }
       if (failed) {  // copies in flight are waited for (bounded); missing sums are 0
         for (; processed != issued; ++processed) {
-          (void)mbar_wait(&mybar[processed % NB], (processed / NB) & 1u);
+          (void)mbar_wait(&mybar[processed % NB], (processed / NB) & 1u, P.wait_ns);
           if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % NB].c * 8u, 0ull);
           __syncwarp();
         }
@@ -3380,6 +3382,8 @@ int grid_size() {
 // grid that applies; STREAM skips the resident path; PERSISTENT forces the
 // persistent grid (testing and benchmarking).
 std::atomic<int> g_schedule{SV_SCHEDULE_AUTO};
+// Limit of every bounded wait in the calls that follow (spec_verify_set_wait_limit).
+std::atomic<unsigned long long> g_wait_ns{kWaitNs};
 
 size_t cluster_tables(int G, int V, int eb) {
   const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
@@ -3634,6 +3638,7 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.p_tok = p_tok;
   P.q_tok = q_tok;
   P.status = reinterpret_cast<unsigned int*>(w + L.status);
+  P.wait_ns = g_wait_ns.load();
   P.next_item = reinterpret_cast<unsigned int*>(w + L.next_item);
   P.exit_count = reinterpret_cast<unsigned int*>(w + L.exit_count);
   P.r_next = reinterpret_cast<unsigned int*>(w + L.r_next);
@@ -3850,6 +3855,11 @@ int spec_verify_set_schedule(int schedule) {
       schedule != SV_SCHEDULE_STREAM)
     return SV_ERR_SCALAR;
   return g_schedule.exchange(schedule);
+}
+
+unsigned long long spec_verify_set_wait_limit(unsigned long long ns) {
+  if (ns == 0ull) ns = kWaitNs;
+  return g_wait_ns.exchange(ns);
 }
 
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {

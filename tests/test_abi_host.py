@@ -157,3 +157,14 @@ def test_binding_refuses_cpu_tensors():
                                    torch.zeros((1, 2), dtype=torch.int32),
                                    torch.zeros(1, dtype=torch.int32),
                                    torch.zeros(256, dtype=torch.uint8))
+
+
+def test_wait_limit_setter_returns_previous_and_zero_restores_default():
+    """The wait limit is host state for later launches (no kernel runs)."""
+    prev = binding.spec_verify_set_wait_limit(5_000_000)
+    try:
+        assert prev == 2_000_000_000
+        assert binding.spec_verify_set_wait_limit(0) == 5_000_000
+        assert binding.spec_verify_set_wait_limit(0) == 2_000_000_000
+    finally:
+        binding.spec_verify_set_wait_limit(prev)
