@@ -179,6 +179,7 @@ struct Params {
   const int32_t* cu;          // packed layout: [B+1] draft prefix (nullptr: padded layout)
   int total;                  // packed layout: drafts in all requests (rows of draft_logits)
   int b_base;                 // packed layout: global index of this launch's first request
+  int parts;                  // request-flow kernel: claims per request (parts of its items)
   const float* uniforms;
   const float* temperature;
   int32_t* out_tokens;
@@ -3339,6 +3340,661 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
 }
 
 // ---------------------------------------------------------------------------
+// Large batches: requests flowing through one CTA per SM
+// ---------------------------------------------------------------------------
+// Beyond one wave of clusters, each CTA (one per SM, NW warps with one 8 KB
+// staging buffer each) takes whole requests in turn, longest first, as the
+// streaming kernel's claims do, but with no barrier between or inside
+// requests.  The CTA's requests form one sequence of A items: request n's
+// items follow request n-1's, and the warps take items from that sequence
+// one at a time (a shared-memory compare-and-swap below the end of the last
+// published request), so the next request streams while the previous one is
+// decided.  Residual work forms a second sequence of fixed-size segments
+// (one per rejecting request, NCR R items each), taken the same way and
+// always before A items.  A warp moves its item into registers (sampling)
+// or reduces it (greedy A items, R items), then takes and copies its next
+// item, so its buffer refills during the arithmetic.  The warp whose partial
+// completes a request decides it on the spot: a rejection publishes the
+// request's residual segment, an accepted draft list draws the bonus token
+// from the A statistics.  The warp whose chunk sum completes a segment draws
+// the token.  Up to NSLOT requests are in flight, each with its partial table,
+// chunk sums and follow-up scratch in shared memory; the warp that takes the
+// first item of request n prepares request n+1 (its claim position from the
+// workspace counter, once request n+1-NSLOT has finished) after finishing
+// its current item.  Every wait is bounded.
+
+__device__ __forceinline__ unsigned int ld_acquire_cta(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+enum { KIND_NONE = 2 };  // no item (flow kernel)
+constexpr unsigned int kNoReq = 0xffffffffu;
+__device__ __forceinline__ unsigned int ld_volatile_cta(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+constexpr int kFlowSegs = 8;  // residual segments addressable at once (> NSLOT)
+
+struct FlowReq {              // one claimed request in flight (shared memory)
+  unsigned int seq;           // request number held (kNoReq: none yet)
+  unsigned int fin;           // the last request number finished in this entry
+  int b, gb, nI, greedy;      // request, draft length, A items of this part, greedy steps
+  int start;                  // its first A item in the CTA's sequence
+  int lo, nreq;               // the part's first item among the request's, and their number
+  int a_done, r_done;         // A items and R items reduced (shared atomics)
+  size_t t0, d0, uf;          // first target row, first draft row, final uniform
+  TempC tc;
+  int k;                      // decision: the rejected position
+  float mt, md, inv_st, rho;
+  unsigned int flags;         // input flags found when the request started
+};
+
+template <int NW, int NSLOT>
+struct FlowShared {
+  uint64_t bar[NW];           // per warp: its buffer's copy landed
+  Meta meta[NW];              // what each warp's buffer holds
+  FlowReq req[NSLOT];         // request n lives in entry n % NSLOT
+  unsigned int a_next;        // next A item of the CTA's sequence
+  unsigned int a_pub;         // end of the A items published so far
+  unsigned int n_pub;         // requests published
+  unsigned int r_next;        // next R item: segment r / NCR, chunk r % NCR
+  unsigned int r_pub;         // residual segments published (in order)
+  unsigned int r_segs;        // residual segments allocated
+  unsigned int rseg[kFlowSegs];  // segment -> request number
+  unsigned int n_done;        // requests finished
+  unsigned int n_total;       // requests of this CTA (kNoReq until known)
+  int pub_lock;               // held while a request is published (never waited for)
+  int claim_next;             // the next claim position (-1 while it is being fetched)
+  unsigned int newest_start;  // first A item of the newest published request
+};
+
+// Launch-wide constants of the request-flow kernel.
+struct FlowConst {
+  const int* order;           // claim order (when sorted)
+  const unsigned char* nrow;  // rows per request, bit 7: greedy steps
+  int sorted, nq;
+};
+
+// Per-request tables built at the start of a claims launch (every CTA builds
+// the same): nrow[b] = rows the request streams (2 gamma_b + 1 when sampled,
+// gamma_b + 1 for greedy steps) with bit 7 set for greedy steps; order[] =
+// claim order, longest first (stable counting sort, skipped when every
+// request has the same row count).  Returns true when `order` is used.
+template <int MODE, bool PK>
+__device__ bool claim_tables(const Params& P, unsigned char* nrow, int* order, int* s_hist,
+                             int nthreads) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto rows_of_req = [&](int b) -> int {
+    int gb = 0;
+    unsigned int fl = 0;
+    if constexpr (PK) (void)packed_base(P, b, gb, fl);
+    else gb = clamp_gamma(P.gamma ? P.gamma[b] : 0, P.G);
+    const bool sampled = MODE == MODE_SAMPLE && P.temperature[b] != 0.0f;
+    return sampled ? 2 * gb + 1 : (gb + 1) | 0x80;
+  };
+  const int r0 = rows_of_req(0) & 0x7f;
+  int differs = 0;
+  for (int b = tid; b < P.B; b += nthreads) {
+    const int r = rows_of_req(b);
+    nrow[b] = (unsigned char)r;
+    differs |= (r & 0x7f) != r0;
+  }
+  const bool sorted = __syncthreads_or(differs) != 0;
+  if (sorted) {
+    if (warp == 0) {
+      for (int r = lane; r < 64; r += 32) s_hist[r] = 0;
+      __syncwarp();
+      for (int b0 = 0; b0 < P.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int r = b < P.B ? (int)(nrow[b] & 0x7f) : 64;  // 64: past the batch
+        const unsigned int peers = __match_any_sync(0xffffffffu, r);
+        if (r < 64 && lane == __ffs(peers) - 1) s_hist[r] += __popc(peers);
+        __syncwarp();
+      }
+      const int h0 = s_hist[2 * lane], h1 = s_hist[2 * lane + 1];
+      int suf = h0 + h1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+      }
+      const int after = suf - h0 - h1;  // requests with more rows than 2 lane + 1
+      __syncwarp();
+      s_hist[2 * lane + 1] = after;
+      s_hist[2 * lane] = after + h1;
+      __syncwarp();
+      for (int b0 = 0; b0 < P.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int r = b < P.B ? (int)(nrow[b] & 0x7f) : 64;
+        const unsigned int peers = __match_any_sync(0xffffffffu, r);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        if (r < 64) order[s_hist[r] + before] = b;
+        __syncwarp();
+        if (r < 64 && before == 0) s_hist[r] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+  return sorted;
+}
+
+// Publish request n (lane 0, publish lock held, its entry free): claim
+// position qp, first A item `start`.  A position past the batch ends the
+// CTA's sequence instead.
+template <int MODE, bool PK, int NW, int NSLOT>
+__device__ void flow_publish(const Params& P, const FlowConst& fc, FlowShared<NW, NSLOT>& fs,
+                             unsigned int n, int qp, int start) {
+  FlowReq& e = fs.req[n % NSLOT];
+  // claim position qp: part qp % parts of the request at claim position qp / parts
+  const int q = qp / P.parts, part = qp - q * P.parts;
+  if (q >= P.B) {
+    st_release_cta(&fs.n_total, n);
+    return;
+  }
+  const int b = fc.sorted ? fc.order[q] : q;
+  const int nr = fc.nrow[b];
+  const bool greedy = (nr & 0x80) != 0;
+  const int rows = nr & 0x7f;
+  const int gb = greedy ? rows - 1 : (rows - 1) / 2;
+  unsigned int fl = 0;
+  int base = 0;
+  if constexpr (PK) {
+    int g2 = 0;
+    base = packed_base(P, b, g2, fl);
+  } else {
+    const int g_in = P.gamma ? P.gamma[b] : 0;
+    if (g_in != gb) fl |= SV_STATUS_BAD_GAMMA;
+  }
+  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+  const int nreq = rows * P.NC;
+  const int lo = (int)((long long)part * nreq / P.parts);
+  const int hi = (int)((long long)(part + 1) * nreq / P.parts);
+  e.b = b;
+  e.gb = gb;
+  e.greedy = greedy ? 1 : 0;
+  e.nI = hi - lo;
+  e.lo = lo;
+  e.nreq = nreq;
+  e.start = start;
+  e.a_done = 0;
+  e.r_done = 0;
+  e.t0 = A.t0;
+  e.d0 = A.d0;
+  e.uf = A.uf;
+  e.tc = TempC{0.0f, 0.0f};
+  if (MODE == MODE_SAMPLE && !greedy) e.tc = temp_consts(sanitize_temperature(P.temperature[b], fl));
+  e.k = 0;
+  e.flags = fl;
+  st_release_cta(&e.seq, n);
+  st_release_cta(&fs.n_pub, n + 1);
+  st_release_cta(&fs.a_pub, (unsigned int)(start + e.nI));
+}
+
+// Publish the CTA's next request if the newest one has started, its entry
+// is free and its claim position is known (lane 0; never waits: another warp
+// holding the publish lock, a busy entry or a claim still being fetched all
+// mean "not now").  One request is thus published ahead of use, so the A
+// sequence does not run dry at a request boundary, while claims are not
+// hoarded (at the end of the batch an idle CTA finds the claims that are
+// left).  The claim position after the one used is fetched at once.
+template <int MODE, bool PK, int NW, int NSLOT>
+__device__ __noinline__ void flow_try_publish(const Params& P, const FlowConst& fc,
+                                              FlowShared<NW, NSLOT>& fs) {
+  if (ld_volatile_cta(&fs.n_total) != kNoReq) return;
+  if (ld_volatile_cta(reinterpret_cast<const unsigned int*>(&fs.claim_next)) == 0xffffffffu) return;
+  const unsigned int n0 = ld_volatile_cta(&fs.n_pub);
+  if (n0 > 0 && ld_volatile_cta(&fs.a_next) <= ld_volatile_cta(&fs.newest_start)) return;
+  if (n0 >= (unsigned int)NSLOT && ld_volatile_cta(&fs.req[n0 % NSLOT].fin) != n0 - NSLOT) return;
+  if (atomicCAS(&fs.pub_lock, 0, 1) != 0) return;
+  __threadfence_block();
+  const unsigned int n = fs.n_pub;
+  const int qp = fs.claim_next;
+  const bool go = fs.n_total == kNoReq && qp >= 0 &&
+                  (n < (unsigned int)NSLOT || ld_volatile_cta(&fs.req[n % NSLOT].fin) == n - NSLOT);
+  if (go) {
+    __threadfence_block();
+    fs.newest_start = fs.a_pub;
+    flow_publish<MODE, PK>(P, fc, fs, n, qp, (int)fs.a_pub);
+    fs.claim_next = -1;
+  }
+  __threadfence_block();
+  atomicExch(&fs.pub_lock, 0);
+  if (go && qp / P.parts < P.B) atomicExch(&fs.claim_next, (int)atomicAdd(P.next_item, 1u) + fc.nq);
+}
+
+// Item j of a request in streaming order: its partial slot, chunk and row.
+// Greedy steps stream target rows 0..gamma_b in order.  Sampled requests
+// stream target row gamma_b (the bonus row) first, then the positions from
+// the last down to 0, target row then draft row: the rows most often
+// rejected (position 0) come last, closest to the residual pass that may
+// re-read them.
+struct FlowRow {
+  int pslot, c, row;  // partial slot, chunk, row index within the target or draft rows
+  bool draft;
+};
+__device__ __forceinline__ FlowRow flow_row(int j, int NC, int gb, bool greedy, int G) {
+  FlowRow r;
+  const int rr = j / NC;
+  r.c = j - rr * NC;
+  if (greedy || rr == 0) {
+    r.row = greedy ? rr : gb;
+    r.pslot = r.row;
+    r.draft = false;
+  } else {
+    const int p = gb - 1 - (rr - 1) / 2;
+    r.row = p;
+    r.draft = ((rr - 1) & 1) != 0;
+    r.pslot = r.draft ? G + 1 + p : p;
+  }
+  return r;
+}
+
+// A warp's copy of the request its A items last came from (shared memory,
+// private to the warp): the common item needs no shared counter but one.
+struct FlowCache {
+  unsigned int n;             // request number (kNoReq: none)
+  int slot, start, end, lo, gb, greedy;
+  size_t t0, d0;
+  TempC tc;
+};
+
+// Take this warp's next item and start its copy (lane 0).  R items of
+// published residual segments come first (claimed by compare-and-swap),
+// then the A item at *held, an index of the CTA's sequence taken with one
+// atomic add and kept while it lies past the published requests.  Returns
+// its kind (KIND_NONE: nothing available now).
+template <int EB, int NW, int NSLOT>
+__device__ __forceinline__ int flow_take(const Params& P, FlowShared<NW, NSLOT>& fs, FlowCache& wc,
+                                         int warp, unsigned char* buf, unsigned int* held) {
+  constexpr int AE = kItemBytes / EB, RE = kHalfBytes / EB;
+  const int V = P.V, NC = P.NC, NCR = P.NCR;
+  Meta& m = fs.meta[warp];
+  int kind = KIND_NONE;
+  {
+    const unsigned int r = ld_volatile_cta(&fs.r_next);
+    if (r < ld_volatile_cta(&fs.r_pub) * (unsigned int)NCR && atomicCAS(&fs.r_next, r, r + 1) == r) {
+      __threadfence_block();  // the segment's decision is visible from here
+      const unsigned int n = fs.rseg[(r / NCR) % kFlowSegs];
+      const FlowReq& e = fs.req[n % NSLOT];
+      const int c = (int)(r % NCR), k = e.k;
+      kind = KIND_R;
+      m.b = (int)(n % NSLOT);
+      m.pslot = k;
+      m.c = c;
+      m.n = min(RE, V - c * RE);
+      m.reject = 1;
+      m.p0 = P.target + ((e.t0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
+      m.p1 = P.draft + ((e.d0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
+      m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.mt = e.mt;
+      m.md = e.md;
+      m.inv_st = e.inv_st;
+      m.rho = e.rho;
+      m.c_hi = e.tc.hi;
+      m.c_lo = e.tc.lo;
+    }
+  }
+  if (kind == KIND_NONE) {
+    if (*held == kNoReq) *held = atomicAdd(&fs.a_next, 1u);
+    const unsigned int a = *held;
+    bool have = a >= (unsigned int)wc.start && a < (unsigned int)wc.end;
+    if (!have && a < ld_volatile_cta(&fs.a_pub)) {
+      // a later request: the newest published one whose start <= a
+      __threadfence_block();
+      unsigned int n = fs.n_pub - 1;
+      while ((unsigned int)fs.req[n % NSLOT].start > a) --n;
+      const FlowReq& e = fs.req[n % NSLOT];
+      wc.n = n;
+      wc.slot = (int)(n % NSLOT);
+      wc.start = e.start;
+      wc.end = e.start + e.nI;
+      wc.lo = e.lo;
+      wc.gb = e.gb;
+      wc.greedy = e.greedy;
+      wc.t0 = e.t0;
+      wc.d0 = e.d0;
+      wc.tc = e.tc;
+      have = true;
+    }
+    if (have) {
+      *held = kNoReq;
+      const int ji = (int)(a - (unsigned int)wc.start);
+      const FlowRow fr = flow_row(wc.lo + ji, NC, wc.gb, wc.greedy != 0, P.G);
+      const int c = fr.c;
+      const size_t roff = ((fr.draft ? wc.d0 : wc.t0) + (size_t)fr.row) * (size_t)V;
+      const char* rows = fr.draft ? P.draft : P.target;
+      m.pslot = fr.pslot;
+      kind = KIND_A;
+      m.b = wc.slot;
+      m.c = c;
+      m.n = min(AE, V - c * AE);
+      m.p0 = rows + (roff + (size_t)c * AE) * EB;
+      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.reject = wc.greedy;  // A items: 1 for greedy steps
+      m.c_hi = wc.tc.hi;
+      m.c_lo = wc.tc.lo;
+    }
+  }
+  m.kind = kind;
+  if (kind == KIND_NONE) return kind;
+  uint64_t* bar = &fs.bar[warp];
+  if (m.direct) {
+    mbar_arrive(bar);  // read with plain loads by the consumer
+  } else if (kind == KIND_A) {
+    const unsigned int bytes = (unsigned int)(m.n * EB);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_copy_g2s(buf, m.p0, bytes, bar);
+  } else {
+    const unsigned int bytes = (unsigned int)(m.n * EB);
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_copy_g2s(buf, m.p0, bytes, bar);
+    bulk_copy_g2s(buf + kHalfBytes, m.p1, bytes, bar);
+  }
+  return kind;
+}
+
+template <int EB, int MODE, bool PK, int NW, int NSLOT>
+__global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ FlowShared<NW, NSLOT> fs;
+  __shared__ FlowCache wcache[NW];
+  __shared__ int s_hist[64];
+  __shared__ int s_last;
+  constexpr int AE = kItemBytes / EB;    // logits per A item
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = P.B, G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
+  // dynamic shared memory: NW buffers | per entry (partials, chunk sums, row
+  // statistics, staging) | claim order [B] | row counts [B]
+  const size_t part_bytes = ((size_t)(2 * G + 1) * NC * sizeof(float2) + 15) & ~(size_t)15;
+  const size_t rsum_bytes = ((size_t)NCR * sizeof(unsigned long long) + 15) & ~(size_t)15;
+  const size_t slot_bytes = part_bytes + rsum_bytes + 1024 + kItemBytes;
+  unsigned char* mybuf = dsmem + (size_t)warp * kItemBytes;
+  unsigned char* slot_base = dsmem + (size_t)NW * kItemBytes;
+  int* order = reinterpret_cast<int*>(slot_base + (size_t)NSLOT * slot_bytes);
+  unsigned char* nrow = reinterpret_cast<unsigned char*>(order + B);
+  auto part_of = [&](int s) { return reinterpret_cast<float2*>(slot_base + (size_t)s * slot_bytes); };
+  auto rsum_of = [&](int s) {
+    return reinterpret_cast<unsigned long long*>(slot_base + (size_t)s * slot_bytes + part_bytes);
+  };
+  auto rs_of = [&](int s) {  // 192 floats: the decision's row statistics
+    return reinterpret_cast<float*>(slot_base + (size_t)s * slot_bytes + part_bytes + rsum_bytes);
+  };
+  auto stage_of = [&](int s) {  // 8 KB: the bonus draw's and the final draw's staging
+    return slot_base + (size_t)s * slot_bytes + part_bytes + rsum_bytes + 1024;
+  };
+
+  if (tid == 0) {
+    for (int w = 0; w < NW; ++w) mbar_init(&fs.bar[w], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < NSLOT; ++s) {
+      fs.req[s].seq = kNoReq;
+      fs.req[s].fin = kNoReq;
+      fs.req[s].start = 0x7fffffff;
+    }
+    fs.a_next = fs.a_pub = fs.n_pub = 0;
+    fs.r_next = fs.r_pub = fs.r_segs = 0;
+    fs.n_done = 0;
+    fs.n_total = kNoReq;
+    fs.pub_lock = 0;
+    fs.claim_next = (int)blockIdx.x;
+    fs.newest_start = 0;
+  }
+  FlowConst fc;
+  fc.order = order;
+  fc.nrow = nrow;
+  fc.nq = (int)gridDim.x;
+  fc.sorted = claim_tables<MODE, PK>(P, nrow, order, s_hist, NW * 32) ? 1 : 0;
+  unsigned int flags = 0;
+  bool failed = false;
+  if (tid == 0) flow_try_publish<MODE, PK>(P, fc, fs);  // the first request
+  __syncthreads();
+
+  unsigned int processed = 0;  // items consumed by this warp (buffer parity)
+  unsigned int held = kNoReq;  // lane 0: an A index taken but not yet published
+  FlowCache& wc = wcache[warp];
+  if (lane == 0) {
+    wc.n = kNoReq;
+    wc.start = 0;
+    wc.end = 0;
+  }
+  __syncwarp();
+  // take and copy this warp's next item (warp-wide); its kind
+  auto take = [&]() -> int {
+    int kind = KIND_NONE;
+    if (lane == 0) kind = flow_take<EB>(P, fs, wc, warp, mybuf, &held);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, kind, 0);
+  };
+  // publish requests ahead of use while entries are free
+  auto publish_next = [&]() {
+    if (lane == 0) flow_try_publish<MODE, PK>(P, fc, fs);
+    __syncwarp();
+  };
+  // a finished request frees its entry
+  auto finish = [&](int s) {
+    if (lane == 0) {
+      FlowReq& e = fs.req[s];
+      if (e.flags) atomicOr(P.status, e.flags);
+      st_release_cta(&e.fin, e.seq);
+      atomicAdd(&fs.n_done, 1u);
+    }
+  };
+
+  int kind = take();
+  publish_next();
+  unsigned long long idle_since = 0;
+  while (!failed) {
+    if (kind == KIND_NONE) {
+      // nothing to take now: the CTA is done, or residual work or the next
+      // request is still to come
+      unsigned int state = 0;  // 0 wait, 1 done, 2 stuck
+      if (lane == 0) {
+        const unsigned int tot = ld_acquire_cta(&fs.n_total);
+        if (tot != kNoReq && ld_acquire_cta(&fs.n_done) == tot) {
+          state = 1;
+        } else {
+          const unsigned long long now = now_ns();
+          if (idle_since == 0) idle_since = now;
+          if (now - idle_since > P.wait_ns) state = 2;
+        }
+      }
+      state = __shfl_sync(0xffffffffu, state, 0);
+      if (state == 1) break;
+      if (state == 2) {
+        flags |= SV_STATUS_TIMEOUT;
+        failed = true;
+        break;
+      }
+      __nanosleep(200);
+      publish_next();
+      kind = take();
+      continue;
+    }
+    idle_since = 0;
+    if (!mbar_wait(&fs.bar[warp], processed & 1u, P.wait_ns)) {
+      flags |= SV_STATUS_TIMEOUT;
+      failed = true;
+      break;
+    }
+    ++processed;
+    const Meta& m = fs.meta[warp];
+    char* stage = reinterpret_cast<char*>(mybuf);
+    const int s = m.b, c = m.c;  // read before the next take rewrites the meta
+    FlowReq& e = fs.req[s];
+    if (kind == KIND_A) {
+      const int pslot = m.pslot;
+      const bool greedy_item = MODE == MODE_GREEDY || m.reject;
+      const bool padded = !m.direct && m.n < AE;  // a row's last chunk
+      const bool written = (!greedy_item && m.direct) || padded;
+      if (!greedy_item && m.direct) stage_unaligned<EB>(m, stage);
+      else if (padded) pad_item_tail<EB>(stage, m.n);
+      float2 pr;
+      if (!greedy_item) {
+        // the item moves into registers with its maximum; the next item's
+        // copy runs during the exponentials
+        const float c_hi = m.c_hi, c_lo = m.c_lo;
+        uint32_t w[kItemWords];
+        const float mx = item_load_max<EB>(stage, w);
+        if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        kind = take();
+        pr = make_float2(mx, item_exp_sum<EB>(w, mx, c_hi, c_lo));
+      } else {
+        pr = a_item_greedy<EB>(m, stage);
+        if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        kind = take();
+      }
+      int last = 0;
+      if (lane == 0) {
+        part_of(s)[pslot * NC + c] = pr;
+        __threadfence_block();
+        last = atomicAdd(&e.a_done, 1) == e.nI - 1 ? 1 : 0;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0) && P.parts > 1) {
+        // ---- this warp completed its part of the request: the part's
+        // partials go to the workspace, and the last part to arrive decides
+        __threadfence_block();
+        const int b = e.b, gb = e.gb, greedy = e.greedy, lo = e.lo, nI = e.nI, nreq = e.nreq;
+        float2* glob = P.stats + (size_t)b * (2 * G + 1) * P.stride_nc;
+        const float2* tab = part_of(s);
+        for (int ji = lane; ji < nI; ji += 32) {
+          const FlowRow fr = flow_row(lo + ji, NC, gb, greedy != 0, G);
+          glob[(size_t)fr.pslot * P.stride_nc + fr.c] = tab[fr.pslot * NC + fr.c];
+        }
+        __syncwarp();
+        unsigned int old = 0;
+        if (lane == 0) {
+          __threadfence();
+          old = atomicAdd(&P.cnt_a[b], 1u);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        last = old == (unsigned int)(P.parts - 1) ? 1 : 0;
+        if (last) {
+          __threadfence();
+          if (lane == 0) P.cnt_a[b] = 0u;  // every part has arrived: reset for the next call
+          float2* tw = part_of(s);
+          for (int j = lane; j < nreq; j += 32) {
+            if (j >= lo && j < lo + nI) continue;
+            const FlowRow fr = flow_row(j, NC, gb, greedy != 0, G);
+            tw[fr.pslot * NC + fr.c] = __ldcg(glob + (size_t)fr.pslot * P.stride_nc + fr.c);
+          }
+          __syncwarp();
+        } else {
+          finish(s);  // this part is done; another CTA decides
+          __syncwarp();
+        }
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        // ---- this warp completed the request's A items: its decision
+        __threadfence_block();
+        const int b = e.b, gb = e.gb;
+        const ReqAddr A = addr_from_base<PK>(P, b, (int)e.d0, gb);
+        const SharedParts sp{part_of(s), NC};
+        float* rs = rs_of(s);
+        bool done = true;
+        if (MODE == MODE_GREEDY || e.greedy) {
+          greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
+        } else {
+          const DraftIn g = gather_drafts<EB>(P, A, gb);
+          Decision d;
+          d.k = 0;
+          d.reject = 0;
+          d.mt = d.md = d.inv_st = d.rho = 0.0f;
+          const int k = decide_core<EB, PK>(P, sp, b, gb, e.tc, rs, A, g, d, true);
+          if (__shfl_sync(0xffffffffu, d.reject, 0)) {
+            done = false;
+            if (lane == 0) {
+              e.k = k;
+              e.mt = d.mt;
+              e.md = d.md;
+              e.inv_st = d.inv_st;
+              e.rho = d.rho;
+              // the request's residual segment, published in allocation order
+              const unsigned int sg = atomicAdd(&fs.r_segs, 1u);
+              fs.rseg[sg % kFlowSegs] = e.seq;
+              const unsigned long long t0 = now_ns();
+              while (ld_acquire_cta(&fs.r_pub) != sg) {
+                if (now_ns() - t0 > P.wait_ns) {
+                  flags |= SV_STATUS_TIMEOUT;
+                  break;
+                }
+                __nanosleep(32);
+              }
+              st_release_cta(&fs.r_pub, sg + 1);
+            }
+          } else {
+            final_bonus<EB, PK>(P, sp, b, gb, e.tc, rs[gb], stage_of(s));
+          }
+        }
+        if (done) finish(s);
+        __syncwarp();
+      }
+    } else {
+      // ---- R item: fixed-point sum of the residual weights over the chunk
+      const unsigned long long sr = r_item<EB>(m, stage);
+      __syncwarp();
+      kind = take();
+      int last = 0;
+      if (lane == 0) {
+        rsum_of(s)[c] = sr;
+        __threadfence_block();
+        last = atomicAdd(&e.r_done, 1) == NCR - 1 ? 1 : 0;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        // ---- this warp completed the request's R items: the final draw
+        __threadfence_block();
+        const int k = e.k;
+        ResidC kc;
+        kc.mt = e.mt; kc.md = e.md; kc.inv_st = e.inv_st; kc.rho = e.rho;
+        resid_scales(kc);
+        kc.hi = e.tc.hi; kc.lo = e.tc.lo; kc.reject = 1;
+        const char* trow = P.target + (e.t0 + (size_t)k) * (size_t)V * EB;
+        const char* drow = P.draft + (e.d0 + (size_t)k) * (size_t)V * EB;
+        unsigned int uflags = 0;
+        const float u_fin = sanitize_uniform(P.uniforms[e.uf], uflags);
+        int tok = chunk_draw<EB, false>(trow, drow, V, NCR, u_fin, kc, rsum_of(s), stage_of(s));
+        if (lane == 0) {
+          if (tok < 0) {
+            flags |= SV_STATUS_INTERNAL;
+            tok = V - 1;
+          }
+          P.out_tokens[(size_t)e.b * (G + 1) + k] = tok;
+          flags |= uflags;
+        }
+        finish(s);
+        __syncwarp();
+      }
+    }
+    publish_next();
+  }
+  // no copy may still be landing in this warp's buffer when it leaves
+  if (failed && kind != KIND_NONE) (void)mbar_wait(&fs.bar[warp], processed & 1u, P.wait_ns);
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && any) atomicOr(P.status, any);
+  // the last CTA out resets the claim counter for the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(P.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_last && tid == 0) {
+    *P.next_item = 0;
+    *P.exit_count = 0;
+    __threadfence();
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 int check_scalars(sv_dtype dtype, int B, int G, int V) {
@@ -3506,7 +4162,53 @@ struct Route {
   int kind;  // SV_ROUTE_*
   int C;     // cluster size (cluster paths)
   int Q;     // clusters launched (cluster paths)
+  int flow;  // claims: 1 on the request-flow kernel, 0 on the streaming kernel
 };
+
+// Request flow: warps (one buffer each) and requests in flight per CTA, and
+// the dynamic shared memory of a launch (buffers | per entry: partials, chunk
+// sums, row statistics, staging | claim order | row counts).
+constexpr int kFlowWarps = 16, kFlowSlots = 4;
+#ifndef SV_FLOW_CLAIMS
+#define SV_FLOW_CLAIMS 8
+#endif
+constexpr int kFlowClaims = SV_FLOW_CLAIMS;  // claims per CTA that the parts aim at
+#ifndef SV_FLOW_ROUTE
+#define SV_FLOW_ROUTE 0
+#endif
+constexpr bool kFlowRoute = SV_FLOW_ROUTE != 0;
+constexpr int kFlowMaxParts = 16;
+constexpr size_t kFlowSmemCap = (size_t)223 * 1024;  // leaves room for the static part
+size_t flow_smem(int B, int G, int V, int eb) {
+  const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
+  const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
+  const size_t part = ((size_t)(2 * G + 1) * nc * sizeof(float2) + 15) & ~(size_t)15;
+  const size_t rsum = (ncr * sizeof(unsigned long long) + 15) & ~(size_t)15;
+  return (size_t)kFlowWarps * kItemBytes + (size_t)kFlowSlots * (part + rsum + 1024 + kItemBytes) +
+         (((size_t)B * 5 + 15) & ~(size_t)15);
+}
+// CTAs of the request-flow kernel that fit on this device at once (cached).
+template <int EB, int MODE, bool PK>
+int flow_ctas() {
+  static std::atomic<int> cached{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int c0 = cached.load(std::memory_order_relaxed);
+  if ((c0 >> 16) == dev + 1) return c0 & 0xffff;
+  auto kern = flow_kernel<EB, MODE, PK, kFlowWarps, kFlowSlots>;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFlowSmemCap) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFlowWarps * 32, kFlowSmemCap) !=
+          cudaSuccess)
+    per_sm = 0;
+  (void)cudaGetLastError();
+  int n = sms * (per_sm > 0 ? 1 : 0);  // one CTA per SM
+  n = n > 0xffff ? 0xffff : n;
+  cached.store(((dev + 1) << 16) | n, std::memory_order_relaxed);
+  return n;
+}
 
 // Streaming cluster path: the largest cluster of which B fit at once (one
 // wave, a request per cluster); with `claims`, a batch beyond one wave of
@@ -3514,23 +4216,36 @@ struct Route {
 // turn.
 template <int EB, int MODE, bool PK>
 Route stream_route(int B, int G, int V) {
-  const Route none{SV_ROUTE_PERSISTENT, 0, 0};
+  const Route none{SV_ROUTE_PERSISTENT, 0, 0, 0};
+#ifdef SV_FLOW_MIN_B
+  if (B >= SV_FLOW_MIN_B && flow_smem(B, G, V, EB) <= kFlowSmemCap) {
+    const int Q = flow_ctas<EB, MODE, PK>();
+    if (Q > 0) return Route{SV_ROUTE_CLAIMS, 1, Q, 1};
+  }
+#endif
+  if (B >= 1 && stream_tables(G, V, EB) <= StreamShape<MODE, 1>::table_cap)
+    for (int C = kClusterMax; C >= 1; --C)
+      if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B, 0};
+  // beyond one wave: the request-flow kernel when its tables fit (when built
+  // with SV_FLOW_ROUTE), else the streaming kernel's claims
+  if (kFlowRoute && B >= 1 && flow_smem(B, G, V, EB) <= kFlowSmemCap) {
+    const int Q = flow_ctas<EB, MODE, PK>();
+    if (Q > 0) return Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B, 1};
+  }
   if (B < 1 || stream_tables(G, V, EB) > StreamShape<MODE, 1>::table_cap) return none;
-  for (int C = kClusterMax; C >= 1; --C)
-    if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B};
   constexpr int QC = claim_cps<MODE>();
   if (stream_tables(G, V, EB) + claim_bytes(B) > StreamShape<MODE, QC>::table_cap) return none;
   const int Q = max_stream_clusters<EB, MODE, PK, QC>(1);
-  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B} : none;
+  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B, 0} : none;
 }
 
 template <int EB, int MODE, bool PK>
 Route route(int B, int G, int V) {
   const int sched = g_schedule.load();
-  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0};
+  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0, 0};
   if (sched == SV_SCHEDULE_AUTO) {
     const int C = cluster_route<EB, MODE, PK>(B, G, V);
-    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B};
+    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B, 0};
   }
   // Beyond one wave, claimed requests (longest first) beat the persistent
   // grid's chunk claims: B=256 ragged, B=512 gamma 1 and 3, sampling 159 ->
@@ -3561,10 +4276,25 @@ int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
 }
 
 template <int EB, int MODE, bool PK>
+int launch_flow(const Params& P0, int Q, cudaStream_t stream) {
+  // Each request is claimed in `parts` parts, so that every CTA takes about
+  // kFlowClaims claims and the last round of claims is short; at most one
+  // part per A chunk of a row (no empty part).
+  Params P = P0;
+  const long long want = ((long long)kFlowClaims * Q + P.B - 1) / P.B;
+  P.parts = (int)(want < 1 ? 1 : (want > kFlowMaxParts ? kFlowMaxParts : want));
+  if (P.parts > P.NC) P.parts = P.NC;
+  flow_kernel<EB, MODE, PK, kFlowWarps, kFlowSlots>
+      <<<Q, kFlowWarps * 32, flow_smem(P.B, P.G, P.V, EB), stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
   if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, 1>(P, r.C, r.Q, stream);
+  if (r.kind == SV_ROUTE_CLAIMS && r.flow) return launch_flow<EB, MODE, PK>(P, r.Q, stream);
   if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, claim_cps<MODE>()>(P, r.C, r.Q, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
@@ -3639,6 +4369,7 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.q_tok = q_tok;
   P.status = reinterpret_cast<unsigned int*>(w + L.status);
   P.wait_ns = g_wait_ns.load();
+  P.parts = 1;
   P.next_item = reinterpret_cast<unsigned int*>(w + L.next_item);
   P.exit_count = reinterpret_cast<unsigned int*>(w + L.exit_count);
   P.r_next = reinterpret_cast<unsigned int*>(w + L.r_next);
@@ -3865,7 +4596,7 @@ unsigned long long spec_verify_set_wait_limit(unsigned long long ns) {
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {
   const int rc = check_scalars(dtype, B, G, V);
   if (rc) return rc;
-  Route r{SV_ROUTE_PERSISTENT, 0, 0};
+  Route r{SV_ROUTE_PERSISTENT, 0, 0, 0};
   if (B > 0) {
     if (dtype == SV_BF16)
       r = greedy ? route<2, MODE_GREEDY, false>(B, G, V) : route<2, MODE_SAMPLE, false>(B, G, V);
