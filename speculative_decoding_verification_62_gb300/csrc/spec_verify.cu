@@ -139,9 +139,11 @@ struct __align__(16) DecRecord {
   uint32_t tag_b; float inv_st, rho; uint32_t pad;
 };
 
+constexpr int kJobsPerRequest = 8;  // residual jobs of one request, at most (flow kernel)
+
 struct Layout {
   size_t status, next_item, exit_count, r_next, q_tail, dec_count;  // header words
-  size_t cnt_a, cnt_r, dec, queue, stats, resid, total;
+  size_t cnt_a, cnt_r, dec, queue, stats, resid, jobs, total;
   int NC, NCR;  // worst-case chunk counts (float32 logits)
 };
 
@@ -165,6 +167,7 @@ __host__ __device__ inline Layout make_layout(int B, int G, int V) {
   L.queue = off; off = align256(off + (size_t)B * sizeof(DecRecord));
   L.stats = off; off = align256(off + (size_t)B * (2 * G + 1) * L.NC * sizeof(float2));
   L.resid = off; off = align256(off + (size_t)B * L.NCR * sizeof(unsigned long long));
+  L.jobs = off;  off = align256(off + (size_t)B * kJobsPerRequest * sizeof(DecRecord));
   L.total = off;
   return L;
 }
@@ -200,6 +203,8 @@ struct Params {
   DecRecord* queue;          // [B] decisions in the order they were made
   float2* stats;              // [B][2G+1][stride_nc]: (max, sum) or (max, argmax bits)
   unsigned long long* resid;  // [B][stride_ncr]: fixed-point sum of the draw weights
+  DecRecord* jobs;            // flow kernel: residual jobs posted by deciding CTAs
+  int rjobs;                  // flow kernel: residual jobs per rejecting request
 };
 
 // A decoded work item (one per lane of a claimed batch; stored per buffer).
@@ -1516,24 +1521,31 @@ __device__ __forceinline__ float item_load_max(const char* stage, uint32_t (&w)[
   }
 }
 
+// The exponent argument here is (z - max) times log2(e)/T rounded to one
+// float: the constant's rounding (at most |a| 2^-24) is below ex2.approx's own
+// relative error for the terms that carry the sum, so the two-term constant
+// of the per-request arithmetic would cost an extra multiply per logit pair
+// for no accuracy.  (Chunk combines, the decision and the draw weights keep
+// the two-term form.)
 template <int EB>
 __device__ __forceinline__ float item_exp_sum(const uint32_t (&w)[kItemWords], float mx, float c_hi,
                                               float c_lo) {
   constexpr int VEC = 16 / EB;
   constexpr int NV = kItemBytes / 16 / 32;
+  const float c1 = __fadd_rn(c_hi, c_lo);
   float sum = 0.0f;
   if (mx > -INFINITY) {
     if constexpr (EB == 2) {
-      // (z - m) * (hi + lo) and the sum, on float32 pairs, 8 accumulators
+      // (z - m) * c and the sum, on float32 pairs, 8 accumulators
       const unsigned long long negm = f2_pack(-mx, -mx);
-      const unsigned long long chi = f2_pack(c_hi, c_hi), clo = f2_pack(c_lo, c_lo);
+      const unsigned long long cc = f2_pack(c1, c1);
       unsigned long long acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0ull;
 #pragma unroll
       for (int i = 0; i < kItemWords; ++i) {
         const unsigned long long d = f2_add(bf16x2_to_f2(w[i]), negm);
-        const unsigned long long a = f2_fma(d, chi, f2_mul(d, clo));
+        const unsigned long long a = f2_mul(d, cc);
         float a0, a1;
         f2_unpack(a, a0, a1);
         acc[i & 7] = f2_add(acc[i & 7], f2_pack(ex2_approx(a0), ex2_approx(a1)));
@@ -1552,7 +1564,7 @@ __device__ __forceinline__ float item_exp_sum(const uint32_t (&w)[kItemWords], f
         float e[VEC];
 #pragma unroll
         for (int q = 0; q < VEC; ++q)
-          e[q] = ex2_approx(exp_arg(__uint_as_float(w[4 * j + q]), mx, c_hi, c_lo));
+          e[q] = ex2_approx(__fmul_rn(__fsub_rn(__uint_as_float(w[4 * j + q]), mx), c1));
 #pragma unroll
         for (int u = VEC; u > 1; u >>= 1)
 #pragma unroll
@@ -3343,25 +3355,31 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
 // Large batches: requests flowing through one CTA per SM
 // ---------------------------------------------------------------------------
 // Beyond one wave of clusters, each CTA (one per SM, NW warps with one 8 KB
-// staging buffer each) takes whole requests in turn, longest first, as the
-// streaming kernel's claims do, but with no barrier between or inside
-// requests.  The CTA's requests form one sequence of A items: request n's
-// items follow request n-1's, and the warps take items from that sequence
-// one at a time (a shared-memory compare-and-swap below the end of the last
-// published request), so the next request streams while the previous one is
-// decided.  Residual work forms a second sequence of fixed-size segments
-// (one per rejecting request, NCR R items each), taken the same way and
-// always before A items.  A warp moves its item into registers (sampling)
-// or reduces it (greedy A items, R items), then takes and copies its next
-// item, so its buffer refills during the arithmetic.  The warp whose partial
-// completes a request decides it on the spot: a rejection publishes the
-// request's residual segment, an accepted draft list draws the bonus token
-// from the A statistics.  The warp whose chunk sum completes a segment draws
-// the token.  Up to NSLOT requests are in flight, each with its partial table,
-// chunk sums and follow-up scratch in shared memory; the warp that takes the
-// first item of request n prepares request n+1 (its claim position from the
-// workspace counter, once request n+1-NSLOT has finished) after finishing
-// its current item.  Every wait is bounded.
+// staging buffer each) works through a sequence of claimed entries with no
+// barrier between them.  An entry is either a part of a request (a range of
+// its A items: requests are claimed in `parts` parts, longest request first,
+// so that every CTA takes several claims and the last round is short) or a
+// residual job (a range of the R chunks of a decided request).  The warps
+// take items one at a time from the CTA's sequence (one shared-memory atomic
+// add; an index past the published entries is held until the next entry is
+// published), move an A item into registers (sampling) or reduce the item,
+// and copy their next item meanwhile.
+//  - The warp whose partial completes a part writes the part's partials to
+//    the workspace; the part that completes the request (a workspace arrival
+//    counter) loads the others' partials and decides.  A rejection allocates
+//    the request's residual jobs in the workspace's job list; an accepted
+//    draft list draws the bonus token from the A statistics; greedy steps are
+//    done at once.
+//  - The warp whose chunk sum completes a job writes its chunk sums to the
+//    workspace; the job that completes the request's residual draws the
+//    token from the chunk sums.
+//  - One entry at a time is published ahead of use (when the newest one has
+//    started and an entry slot is free): a residual job if one is waiting,
+//    else the next claim position.  Jobs thus move to whichever CTA is free,
+//    and a CTA that decides does not inherit the residual work.
+//  - A CTA with no claim left stays until every request of the batch is
+//    decided and no job is left, taking jobs as they appear.
+// Every wait is bounded; the last CTA out resets the workspace counters.
 
 __device__ __forceinline__ unsigned int ld_acquire_cta(const unsigned int* p) {
   unsigned int v;
@@ -3371,27 +3389,30 @@ __device__ __forceinline__ unsigned int ld_acquire_cta(const unsigned int* p) {
 __device__ __forceinline__ void st_release_cta(unsigned int* p, unsigned int v) {
   asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
-
-enum { KIND_NONE = 2 };  // no item (flow kernel)
-constexpr unsigned int kNoReq = 0xffffffffu;
 __device__ __forceinline__ unsigned int ld_volatile_cta(const unsigned int* p) {
   unsigned int v;
   asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
   return v;
 }
-constexpr int kFlowSegs = 8;  // residual segments addressable at once (> NSLOT)
 
-struct FlowReq {              // one claimed request in flight (shared memory)
-  unsigned int seq;           // request number held (kNoReq: none yet)
-  unsigned int fin;           // the last request number finished in this entry
-  int b, gb, nI, greedy;      // request, draft length, A items of this part, greedy steps
-  int start;                  // its first A item in the CTA's sequence
-  int lo, nreq;               // the part's first item among the request's, and their number
-  int a_done, r_done;         // A items and R items reduced (shared atomics)
+enum { KIND_NONE = 2 };  // no item (flow kernel)
+constexpr unsigned int kNoReq = 0xffffffffu;
+constexpr int kFlowMaxJobs = kJobsPerRequest;
+constexpr unsigned long long kJobPollNs = 2000;  // a CTA with claims left looks for jobs this often
+
+struct FlowReq {              // one entry in flight (shared memory)
+  unsigned int seq;           // entry number held (kNoReq: none yet)
+  unsigned int fin;           // the last entry number finished in this slot
+  int job;                    // 0: a part of a request's A items; 1: a residual job
+  int b, gb, nI, greedy;      // request, draft length, items of this entry, greedy steps
+  int start;                  // its first item in the CTA's sequence
+  int lo, nreq;               // part: its first item among the request's, and their number;
+                              // job: its first R chunk
+  int a_done;                 // items reduced (shared atomic)
   size_t t0, d0, uf;          // first target row, first draft row, final uniform
   TempC tc;
-  int k;                      // decision: the rejected position
-  float mt, md, inv_st, rho;
+  int k;                      // job: the rejected position
+  float mt, md, inv_st, rho;  // job: the decision's draw constants
   unsigned int flags;         // input flags found when the request started
 };
 
@@ -3399,19 +3420,17 @@ template <int NW, int NSLOT>
 struct FlowShared {
   uint64_t bar[NW];           // per warp: its buffer's copy landed
   Meta meta[NW];              // what each warp's buffer holds
-  FlowReq req[NSLOT];         // request n lives in entry n % NSLOT
-  unsigned int a_next;        // next A item of the CTA's sequence
-  unsigned int a_pub;         // end of the A items published so far
-  unsigned int n_pub;         // requests published
-  unsigned int r_next;        // next R item: segment r / NCR, chunk r % NCR
-  unsigned int r_pub;         // residual segments published (in order)
-  unsigned int r_segs;        // residual segments allocated
-  unsigned int rseg[kFlowSegs];  // segment -> request number
-  unsigned int n_done;        // requests finished
-  unsigned int n_total;       // requests of this CTA (kNoReq until known)
-  int pub_lock;               // held while a request is published (never waited for)
+  FlowReq req[NSLOT];         // entry n lives in slot n % NSLOT
+  unsigned int a_next;        // next item of the CTA's sequence
+  unsigned int a_pub;         // end of the items published so far
+  unsigned int n_pub;         // entries published
+  unsigned int n_done;        // entries finished
+  unsigned int claims_done;   // 1: no claim position left
+  int pub_lock;               // held while an entry is published (never waited for)
   int claim_next;             // the next claim position (-1 while it is being fetched)
-  unsigned int newest_start;  // first A item of the newest published request
+  unsigned int newest_start;  // first item of the newest published entry
+  unsigned int closed;        // 1: nothing will be published any more (the CTA is done)
+  unsigned long long job_poll; // when the workspace's job list was last looked at
 };
 
 // Launch-wide constants of the request-flow kernel.
@@ -3485,90 +3504,6 @@ __device__ bool claim_tables(const Params& P, unsigned char* nrow, int* order, i
   return sorted;
 }
 
-// Publish request n (lane 0, publish lock held, its entry free): claim
-// position qp, first A item `start`.  A position past the batch ends the
-// CTA's sequence instead.
-template <int MODE, bool PK, int NW, int NSLOT>
-__device__ void flow_publish(const Params& P, const FlowConst& fc, FlowShared<NW, NSLOT>& fs,
-                             unsigned int n, int qp, int start) {
-  FlowReq& e = fs.req[n % NSLOT];
-  // claim position qp: part qp % parts of the request at claim position qp / parts
-  const int q = qp / P.parts, part = qp - q * P.parts;
-  if (q >= P.B) {
-    st_release_cta(&fs.n_total, n);
-    return;
-  }
-  const int b = fc.sorted ? fc.order[q] : q;
-  const int nr = fc.nrow[b];
-  const bool greedy = (nr & 0x80) != 0;
-  const int rows = nr & 0x7f;
-  const int gb = greedy ? rows - 1 : (rows - 1) / 2;
-  unsigned int fl = 0;
-  int base = 0;
-  if constexpr (PK) {
-    int g2 = 0;
-    base = packed_base(P, b, g2, fl);
-  } else {
-    const int g_in = P.gamma ? P.gamma[b] : 0;
-    if (g_in != gb) fl |= SV_STATUS_BAD_GAMMA;
-  }
-  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
-  const int nreq = rows * P.NC;
-  const int lo = (int)((long long)part * nreq / P.parts);
-  const int hi = (int)((long long)(part + 1) * nreq / P.parts);
-  e.b = b;
-  e.gb = gb;
-  e.greedy = greedy ? 1 : 0;
-  e.nI = hi - lo;
-  e.lo = lo;
-  e.nreq = nreq;
-  e.start = start;
-  e.a_done = 0;
-  e.r_done = 0;
-  e.t0 = A.t0;
-  e.d0 = A.d0;
-  e.uf = A.uf;
-  e.tc = TempC{0.0f, 0.0f};
-  if (MODE == MODE_SAMPLE && !greedy) e.tc = temp_consts(sanitize_temperature(P.temperature[b], fl));
-  e.k = 0;
-  e.flags = fl;
-  st_release_cta(&e.seq, n);
-  st_release_cta(&fs.n_pub, n + 1);
-  st_release_cta(&fs.a_pub, (unsigned int)(start + e.nI));
-}
-
-// Publish the CTA's next request if the newest one has started, its entry
-// is free and its claim position is known (lane 0; never waits: another warp
-// holding the publish lock, a busy entry or a claim still being fetched all
-// mean "not now").  One request is thus published ahead of use, so the A
-// sequence does not run dry at a request boundary, while claims are not
-// hoarded (at the end of the batch an idle CTA finds the claims that are
-// left).  The claim position after the one used is fetched at once.
-template <int MODE, bool PK, int NW, int NSLOT>
-__device__ __noinline__ void flow_try_publish(const Params& P, const FlowConst& fc,
-                                              FlowShared<NW, NSLOT>& fs) {
-  if (ld_volatile_cta(&fs.n_total) != kNoReq) return;
-  if (ld_volatile_cta(reinterpret_cast<const unsigned int*>(&fs.claim_next)) == 0xffffffffu) return;
-  const unsigned int n0 = ld_volatile_cta(&fs.n_pub);
-  if (n0 > 0 && ld_volatile_cta(&fs.a_next) <= ld_volatile_cta(&fs.newest_start)) return;
-  if (n0 >= (unsigned int)NSLOT && ld_volatile_cta(&fs.req[n0 % NSLOT].fin) != n0 - NSLOT) return;
-  if (atomicCAS(&fs.pub_lock, 0, 1) != 0) return;
-  __threadfence_block();
-  const unsigned int n = fs.n_pub;
-  const int qp = fs.claim_next;
-  const bool go = fs.n_total == kNoReq && qp >= 0 &&
-                  (n < (unsigned int)NSLOT || ld_volatile_cta(&fs.req[n % NSLOT].fin) == n - NSLOT);
-  if (go) {
-    __threadfence_block();
-    fs.newest_start = fs.a_pub;
-    flow_publish<MODE, PK>(P, fc, fs, n, qp, (int)fs.a_pub);
-    fs.claim_next = -1;
-  }
-  __threadfence_block();
-  atomicExch(&fs.pub_lock, 0);
-  if (go && qp / P.parts < P.B) atomicExch(&fs.claim_next, (int)atomicAdd(P.next_item, 1u) + fc.nq);
-}
-
 // Item j of a request in streaming order: its partial slot, chunk and row.
 // Greedy steps stream target rows 0..gamma_b in order.  Sampled requests
 // stream target row gamma_b (the bonus row) first, then the positions from
@@ -3596,95 +3531,271 @@ __device__ __forceinline__ FlowRow flow_row(int j, int NC, int gb, bool greedy, 
   return r;
 }
 
-// A warp's copy of the request its A items last came from (shared memory,
-// private to the warp): the common item needs no shared counter but one.
+// A warp's copy of the entry its items last came from (shared memory, private
+// to the warp): the common item needs no shared counter but one.
 struct FlowCache {
-  unsigned int n;             // request number (kNoReq: none)
-  int slot, start, end, lo, gb, greedy;
+  unsigned int n;             // entry number (kNoReq: none)
+  int slot, start, end, lo, gb, greedy, job, k;
   size_t t0, d0;
   TempC tc;
+  float mt, md, inv_st, rho;
 };
 
-// Take this warp's next item and start its copy (lane 0).  R items of
-// published residual segments come first (claimed by compare-and-swap),
-// then the A item at *held, an index of the CTA's sequence taken with one
-// atomic add and kept while it lies past the published requests.  Returns
-// its kind (KIND_NONE: nothing available now).
+__device__ __forceinline__ unsigned int ld_relaxed_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The residual jobs of a decided request (lane 0): nj records in the
+// workspace's job list, each naming the request, the rejected position, the
+// job's index and the draw constants.  A claimer that finds a record not yet
+// complete waits for it (bounded).
+__device__ __forceinline__ void flow_post_jobs(const Params& P, int b, const Decision& d, int nj) {
+  const unsigned int j0 = atomicAdd(P.q_tail, (unsigned int)nj);
+  for (int i = 0; i < nj; ++i) {
+    Decision di = d;
+    di.reject = 1;
+    DecRecord* r = &P.jobs[j0 + (unsigned int)i];
+    const uint32_t tag = kDecTag | ((uint32_t)i << 8) | (uint32_t)d.k;
+    atom_store_b128(&r->tag_b, make_uint4(tag, __float_as_uint(di.inv_st), __float_as_uint(di.rho), 0u));
+    atom_store_b128(&r->tag_a, make_uint4(tag, (uint32_t)b, __float_as_uint(di.mt), __float_as_uint(di.md)));
+  }
+}
+
+// A residual job's record (both halves, one round trip): false while it is
+// not yet complete.
+__device__ __forceinline__ bool read_job(const DecRecord* r, int& b, int& k, int& rj, float& mt,
+                                         float& md, float& inv_st, float& rho) {
+  const uint4 a = atom_load_b128(&r->tag_a);
+  const uint4 h = atom_load_b128(&r->tag_b);
+  if (!(a.x & kDecTag) || a.x != h.x) return false;
+  k = (int)(a.x & 0xffu);
+  rj = (int)((a.x >> 8) & 0xffu);
+  b = (int)a.y;
+  mt = __uint_as_float(a.z);
+  md = __uint_as_float(a.w);
+  inv_st = __uint_as_float(h.y);
+  rho = __uint_as_float(h.z);
+  return true;
+}
+
+// The request's fields of an entry (lane 0, publish lock held).
+template <int MODE, bool PK>
+__device__ __forceinline__ void flow_fill_request(const Params& P, const FlowConst& fc,
+                                                  FlowReq& e, int b, unsigned int& fl,
+                                                  int& rows) {
+  const int nr = fc.nrow[b];
+  const bool greedy = (nr & 0x80) != 0;
+  rows = nr & 0x7f;
+  const int gb = greedy ? rows - 1 : (rows - 1) / 2;
+  int base = 0;
+  if constexpr (PK) {
+    int g2 = 0;
+    base = packed_base(P, b, g2, fl);
+  } else {
+    const int g_in = P.gamma ? P.gamma[b] : 0;
+    if (g_in != gb) fl |= SV_STATUS_BAD_GAMMA;
+  }
+  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+  e.b = b;
+  e.gb = gb;
+  e.greedy = greedy ? 1 : 0;
+  e.t0 = A.t0;
+  e.d0 = A.d0;
+  e.uf = A.uf;
+  e.tc = TempC{0.0f, 0.0f};
+  if (MODE == MODE_SAMPLE && !greedy) e.tc = temp_consts(sanitize_temperature(P.temperature[b], fl));
+}
+
+// Publish the CTA's next entry if the newest one has started and its slot is
+// free (lane 0; never waits for another warp: the publish lock taken, a busy
+// slot or a claim position still being fetched all mean "not now").  A
+// waiting residual job comes first (claimed from the workspace's job list by
+// compare-and-swap); else the part at the next claim position, whose
+// successor position is then fetched.  One entry is published ahead of use,
+// so the sequence does not run dry at an entry boundary while claims and
+// jobs are not hoarded.
+template <int MODE, bool PK, int NW, int NSLOT>
+__device__ __noinline__ void flow_try_publish(const Params& P, const FlowConst& fc,
+                                              FlowShared<NW, NSLOT>& fs, unsigned int* flags) {
+  const unsigned int n0 = ld_volatile_cta(&fs.n_pub);
+  if (n0 > 0 && ld_volatile_cta(&fs.a_next) <= ld_volatile_cta(&fs.newest_start)) return;
+  if (n0 >= (unsigned int)NSLOT && ld_volatile_cta(&fs.req[n0 % NSLOT].fin) != n0 - NSLOT) return;
+  // something to publish: the next claim position is at hand, or the job
+  // list is due for a look (every kJobPollNs, at every call once no claim is
+  // left); the job list lives in global memory, so it is not read on every call
+  const bool claim_ready = !ld_volatile_cta(&fs.claims_done) &&
+                           (int)ld_volatile_cta(reinterpret_cast<const unsigned int*>(&fs.claim_next)) >= 0;
+  bool poll = false;
+  if (MODE == MODE_SAMPLE) {
+    const unsigned long long now = now_ns();
+    poll = ld_volatile_cta(&fs.claims_done) ||
+           now - *reinterpret_cast<volatile unsigned long long*>(&fs.job_poll) > kJobPollNs;
+  }
+  if (!claim_ready && !poll) return;
+  if (atomicCAS(&fs.pub_lock, 0, 1) != 0) return;
+  __threadfence_block();
+  const unsigned int n = fs.n_pub;
+  FlowReq& e = fs.req[n % NSLOT];
+  bool published = false, fetch = false;
+  if (!fs.closed && (n < (unsigned int)NSLOT || ld_volatile_cta(&e.fin) == n - NSLOT)) {
+    // 1. a waiting residual job
+    unsigned int jt = 0xffffffffu;
+    if (poll) {
+      fs.job_poll = now_ns();
+      jt = ld_relaxed_gpu(P.r_next);
+      if (jt >= ld_relaxed_gpu(P.q_tail) || atomicCAS(P.r_next, jt, jt + 1) != jt) jt = 0xffffffffu;
+    }
+    if (jt != 0xffffffffu) {
+      DecRecord* r = &P.jobs[jt];
+      int b = 0, k = 0, rj = 0;
+      float mt = 0.0f, md = 0.0f, inv_st = 0.0f, rho = 0.0f;
+      bool got = read_job(r, b, k, rj, mt, md, inv_st, rho);
+      if (!got) {
+        const unsigned long long t0 = now_ns();
+        while (!(got = read_job(r, b, k, rj, mt, md, inv_st, rho)) && now_ns() - t0 < P.wait_ns)
+          __nanosleep(32);
+      }
+      if (got && b >= 0 && b < P.B && k >= 0 && k <= P.G && rj < P.rjobs) {
+        // each record is read once: cleared for the next call
+        atom_store_b128(&r->tag_a, make_uint4(0u, 0u, 0u, 0u));
+        atom_store_b128(&r->tag_b, make_uint4(0u, 0u, 0u, 0u));
+        unsigned int fl = 0;
+        int rows = 0;
+        flow_fill_request<MODE, PK>(P, fc, e, b, fl, rows);
+        e.job = 1;
+        e.k = k;
+        e.mt = mt;
+        e.md = md;
+        e.inv_st = inv_st;
+        e.rho = rho;
+        e.lo = (int)((long long)rj * P.NCR / P.rjobs);
+        e.nI = (int)((long long)(rj + 1) * P.NCR / P.rjobs) - e.lo;
+        e.nreq = P.NCR;
+        e.flags = 0;
+        published = true;
+      } else {
+        *flags |= got ? SV_STATUS_INTERNAL : SV_STATUS_TIMEOUT;
+#ifdef SV_FLOW_DEBUG
+        if (!got) *flags |= 256u;
+#endif
+      }
+    }
+    // 2. the part at the next claim position
+    const int qp = fs.claim_next;
+    if (!published && !fs.claims_done && qp >= 0) {
+      const int q = qp / P.parts, part = qp - q * P.parts;
+      if (q >= P.B) {
+        fs.claims_done = 1;
+      } else {
+        const int b = fc.sorted ? fc.order[q] : q;
+        unsigned int fl = 0;
+        int rows = 0;
+        flow_fill_request<MODE, PK>(P, fc, e, b, fl, rows);
+        const int nreq = rows * P.NC;
+        e.job = 0;
+        e.lo = (int)((long long)part * nreq / P.parts);
+        e.nI = (int)((long long)(part + 1) * nreq / P.parts) - e.lo;
+        e.nreq = nreq;
+        e.k = 0;
+        e.flags = part == 0 ? fl : 0u;  // reported once per request
+        fs.claim_next = -1;
+        fetch = true;
+        published = true;
+      }
+    }
+    if (published) {
+      __threadfence_block();
+      fs.newest_start = fs.a_pub;
+      e.start = (int)fs.a_pub;
+      e.a_done = 0;
+      st_release_cta(&e.seq, n);
+      st_release_cta(&fs.n_pub, n + 1);
+      st_release_cta(&fs.a_pub, (unsigned int)(e.start + e.nI));
+    }
+  }
+  __threadfence_block();
+  atomicExch(&fs.pub_lock, 0);
+  if (fetch) atomicExch(&fs.claim_next, (int)atomicAdd(P.next_item, 1u) + fc.nq);
+}
+
+// Take this warp's next item and start its copy (lane 0): the item at *held,
+// an index of the CTA's sequence taken with one atomic add and kept while it
+// lies past the published entries.  Returns its kind (KIND_NONE: nothing
+// available now).
 template <int EB, int NW, int NSLOT>
 __device__ __forceinline__ int flow_take(const Params& P, FlowShared<NW, NSLOT>& fs, FlowCache& wc,
                                          int warp, unsigned char* buf, unsigned int* held) {
   constexpr int AE = kItemBytes / EB, RE = kHalfBytes / EB;
-  const int V = P.V, NC = P.NC, NCR = P.NCR;
+  const int V = P.V, NC = P.NC;
   Meta& m = fs.meta[warp];
-  int kind = KIND_NONE;
-  {
-    const unsigned int r = ld_volatile_cta(&fs.r_next);
-    if (r < ld_volatile_cta(&fs.r_pub) * (unsigned int)NCR && atomicCAS(&fs.r_next, r, r + 1) == r) {
-      __threadfence_block();  // the segment's decision is visible from here
-      const unsigned int n = fs.rseg[(r / NCR) % kFlowSegs];
-      const FlowReq& e = fs.req[n % NSLOT];
-      const int c = (int)(r % NCR), k = e.k;
-      kind = KIND_R;
-      m.b = (int)(n % NSLOT);
-      m.pslot = k;
-      m.c = c;
-      m.n = min(RE, V - c * RE);
-      m.reject = 1;
-      m.p0 = P.target + ((e.t0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
-      m.p1 = P.draft + ((e.d0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
-      const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
-      m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-      m.mt = e.mt;
-      m.md = e.md;
-      m.inv_st = e.inv_st;
-      m.rho = e.rho;
-      m.c_hi = e.tc.hi;
-      m.c_lo = e.tc.lo;
+  if (*held == kNoReq) *held = atomicAdd(&fs.a_next, 1u);
+  const unsigned int a = *held;
+  bool have = a >= (unsigned int)wc.start && a < (unsigned int)wc.end;
+  if (!have) {
+    if (a >= ld_volatile_cta(&fs.a_pub)) {
+      m.kind = KIND_NONE;
+      return KIND_NONE;
     }
+    // a later entry: the newest published one whose start <= a
+    __threadfence_block();
+    unsigned int n = fs.n_pub - 1;
+    while ((unsigned int)fs.req[n % NSLOT].start > a) --n;
+    const FlowReq& e = fs.req[n % NSLOT];
+    wc.n = n;
+    wc.slot = (int)(n % NSLOT);
+    wc.start = e.start;
+    wc.end = e.start + e.nI;
+    wc.lo = e.lo;
+    wc.gb = e.gb;
+    wc.greedy = e.greedy;
+    wc.job = e.job;
+    wc.k = e.k;
+    wc.t0 = e.t0;
+    wc.d0 = e.d0;
+    wc.tc = e.tc;
+    wc.mt = e.mt;
+    wc.md = e.md;
+    wc.inv_st = e.inv_st;
+    wc.rho = e.rho;
   }
-  if (kind == KIND_NONE) {
-    if (*held == kNoReq) *held = atomicAdd(&fs.a_next, 1u);
-    const unsigned int a = *held;
-    bool have = a >= (unsigned int)wc.start && a < (unsigned int)wc.end;
-    if (!have && a < ld_volatile_cta(&fs.a_pub)) {
-      // a later request: the newest published one whose start <= a
-      __threadfence_block();
-      unsigned int n = fs.n_pub - 1;
-      while ((unsigned int)fs.req[n % NSLOT].start > a) --n;
-      const FlowReq& e = fs.req[n % NSLOT];
-      wc.n = n;
-      wc.slot = (int)(n % NSLOT);
-      wc.start = e.start;
-      wc.end = e.start + e.nI;
-      wc.lo = e.lo;
-      wc.gb = e.gb;
-      wc.greedy = e.greedy;
-      wc.t0 = e.t0;
-      wc.d0 = e.d0;
-      wc.tc = e.tc;
-      have = true;
-    }
-    if (have) {
-      *held = kNoReq;
-      const int ji = (int)(a - (unsigned int)wc.start);
-      const FlowRow fr = flow_row(wc.lo + ji, NC, wc.gb, wc.greedy != 0, P.G);
-      const int c = fr.c;
-      const size_t roff = ((fr.draft ? wc.d0 : wc.t0) + (size_t)fr.row) * (size_t)V;
-      const char* rows = fr.draft ? P.draft : P.target;
-      m.pslot = fr.pslot;
-      kind = KIND_A;
-      m.b = wc.slot;
-      m.c = c;
-      m.n = min(AE, V - c * AE);
-      m.p0 = rows + (roff + (size_t)c * AE) * EB;
-      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-      m.reject = wc.greedy;  // A items: 1 for greedy steps
-      m.c_hi = wc.tc.hi;
-      m.c_lo = wc.tc.lo;
-    }
+  *held = kNoReq;
+  const int ji = (int)(a - (unsigned int)wc.start);
+  int kind;
+  m.b = wc.slot;
+  m.c_hi = wc.tc.hi;
+  m.c_lo = wc.tc.lo;
+  if (wc.job) {
+    // an R item: chunk lo + ji of target and draft row k
+    const int c = wc.lo + ji, k = wc.k;
+    kind = KIND_R;
+    m.pslot = k;
+    m.c = c;
+    m.n = min(RE, V - c * RE);
+    m.reject = 1;
+    m.p0 = P.target + ((wc.t0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
+    m.p1 = P.draft + ((wc.d0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
+    const uintptr_t ad = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
+    m.direct = ((ad & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+    m.mt = wc.mt;
+    m.md = wc.md;
+    m.inv_st = wc.inv_st;
+    m.rho = wc.rho;
+  } else {
+    const FlowRow fr = flow_row(wc.lo + ji, NC, wc.gb, wc.greedy != 0, P.G);
+    const int c = fr.c;
+    const size_t roff = ((fr.draft ? wc.d0 : wc.t0) + (size_t)fr.row) * (size_t)V;
+    const char* rows = fr.draft ? P.draft : P.target;
+    kind = KIND_A;
+    m.pslot = fr.pslot;
+    m.c = c;
+    m.n = min(AE, V - c * AE);
+    m.p0 = rows + (roff + (size_t)c * AE) * EB;
+    m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+    m.reject = wc.greedy;  // A items: 1 for greedy steps
   }
   m.kind = kind;
-  if (kind == KIND_NONE) return kind;
   uint64_t* bar = &fs.bar[warp];
   if (m.direct) {
     mbar_arrive(bar);  // read with plain loads by the consumer
@@ -3711,24 +3822,20 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
   constexpr int AE = kItemBytes / EB;    // logits per A item
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = P.B, G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
-  // dynamic shared memory: NW buffers | per entry (partials, chunk sums, row
-  // statistics, staging) | claim order [B] | row counts [B]
+  // dynamic shared memory: NW buffers | per slot (partials, row statistics,
+  // staging) | claim order [B] | row counts [B]
   const size_t part_bytes = ((size_t)(2 * G + 1) * NC * sizeof(float2) + 15) & ~(size_t)15;
-  const size_t rsum_bytes = ((size_t)NCR * sizeof(unsigned long long) + 15) & ~(size_t)15;
-  const size_t slot_bytes = part_bytes + rsum_bytes + 1024 + kItemBytes;
+  const size_t slot_bytes = part_bytes + 1024 + kItemBytes;
   unsigned char* mybuf = dsmem + (size_t)warp * kItemBytes;
   unsigned char* slot_base = dsmem + (size_t)NW * kItemBytes;
   int* order = reinterpret_cast<int*>(slot_base + (size_t)NSLOT * slot_bytes);
   unsigned char* nrow = reinterpret_cast<unsigned char*>(order + B);
   auto part_of = [&](int s) { return reinterpret_cast<float2*>(slot_base + (size_t)s * slot_bytes); };
-  auto rsum_of = [&](int s) {
-    return reinterpret_cast<unsigned long long*>(slot_base + (size_t)s * slot_bytes + part_bytes);
-  };
   auto rs_of = [&](int s) {  // 192 floats: the decision's row statistics
-    return reinterpret_cast<float*>(slot_base + (size_t)s * slot_bytes + part_bytes + rsum_bytes);
+    return reinterpret_cast<float*>(slot_base + (size_t)s * slot_bytes + part_bytes);
   };
   auto stage_of = [&](int s) {  // 8 KB: the bonus draw's and the final draw's staging
-    return slot_base + (size_t)s * slot_bytes + part_bytes + rsum_bytes + 1024;
+    return slot_base + (size_t)s * slot_bytes + part_bytes + 1024;
   };
 
   if (tid == 0) {
@@ -3739,13 +3846,13 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
       fs.req[s].fin = kNoReq;
       fs.req[s].start = 0x7fffffff;
     }
-    fs.a_next = fs.a_pub = fs.n_pub = 0;
-    fs.r_next = fs.r_pub = fs.r_segs = 0;
-    fs.n_done = 0;
-    fs.n_total = kNoReq;
+    fs.a_next = fs.a_pub = fs.n_pub = fs.n_done = 0;
+    fs.claims_done = 0;
     fs.pub_lock = 0;
     fs.claim_next = (int)blockIdx.x;
     fs.newest_start = 0;
+    fs.closed = 0;
+    fs.job_poll = 0;
   }
   FlowConst fc;
   fc.order = order;
@@ -3754,11 +3861,11 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
   fc.sorted = claim_tables<MODE, PK>(P, nrow, order, s_hist, NW * 32) ? 1 : 0;
   unsigned int flags = 0;
   bool failed = false;
-  if (tid == 0) flow_try_publish<MODE, PK>(P, fc, fs);  // the first request
+  if (tid == 0) flow_try_publish<MODE, PK>(P, fc, fs, &flags);  // the first entry
   __syncthreads();
 
   unsigned int processed = 0;  // items consumed by this warp (buffer parity)
-  unsigned int held = kNoReq;  // lane 0: an A index taken but not yet published
+  unsigned int held = kNoReq;  // lane 0: an index taken but not yet published
   FlowCache& wc = wcache[warp];
   if (lane == 0) {
     wc.n = kNoReq;
@@ -3773,12 +3880,11 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
     __syncwarp();
     return __shfl_sync(0xffffffffu, kind, 0);
   };
-  // publish requests ahead of use while entries are free
   auto publish_next = [&]() {
-    if (lane == 0) flow_try_publish<MODE, PK>(P, fc, fs);
+    if (lane == 0) flow_try_publish<MODE, PK>(P, fc, fs, &flags);
     __syncwarp();
   };
-  // a finished request frees its entry
+  // an entry is finished: its slot is free again
   auto finish = [&](int s) {
     if (lane == 0) {
       FlowReq& e = fs.req[s];
@@ -3787,20 +3893,43 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
       atomicAdd(&fs.n_done, 1u);
     }
   };
+  // a request is decided (after its jobs, if any, are posted)
+  auto count_decision = [&]() {
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(P.dec_count, 1u);
+    }
+  };
 
   int kind = take();
-  publish_next();
   unsigned long long idle_since = 0;
   while (!failed) {
     if (kind == KIND_NONE) {
-      // nothing to take now: the CTA is done, or residual work or the next
-      // request is still to come
+      // nothing to take now: the CTA is done, or an entry is still to come
       unsigned int state = 0;  // 0 wait, 1 done, 2 stuck
       if (lane == 0) {
-        const unsigned int tot = ld_acquire_cta(&fs.n_total);
-        if (tot != kNoReq && ld_acquire_cta(&fs.n_done) == tot) {
+        // done once every request is decided, every job taken and every
+        // entry here finished; decided under the publish lock, which then
+        // closes the CTA to publication, so that no warp leaves holding an
+        // index that a later entry would cover
+        auto all_done = [&]() {
+          return ld_volatile_cta(&fs.claims_done) &&
+                 ld_volatile_cta(&fs.n_done) == ld_volatile_cta(&fs.n_pub) &&
+                 ld_relaxed_gpu(P.dec_count) == (unsigned int)B &&
+                 ld_relaxed_gpu(P.r_next) >= ld_relaxed_gpu(P.q_tail);
+        };
+        if (ld_volatile_cta(&fs.closed)) {
           state = 1;
-        } else {
+        } else if (all_done() && atomicCAS(&fs.pub_lock, 0, 1) == 0) {
+          __threadfence_block();
+          if (all_done()) {
+            fs.closed = 1;
+            state = 1;
+          }
+          __threadfence_block();
+          atomicExch(&fs.pub_lock, 0);
+        }
+        if (state == 0) {
           const unsigned long long now = now_ns();
           if (idle_since == 0) idle_since = now;
           if (now - idle_since > P.wait_ns) state = 2;
@@ -3810,6 +3939,16 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
       if (state == 1) break;
       if (state == 2) {
         flags |= SV_STATUS_TIMEOUT;
+#ifdef SV_FLOW_DEBUG
+        flags |= 512u;
+        if (lane == 0 && 3 * (int)blockIdx.x + 2 < B * (G + 1)) {
+          int32_t* o = P.out_tokens + 3 * blockIdx.x;
+          o[0] = (int)((fs.claims_done << 24) | (fs.n_done << 12) | fs.n_pub);
+          o[1] = (int)((fs.a_next << 16) | fs.a_pub);
+          o[2] = (int)((ld_relaxed_gpu(P.dec_count) << 20) | (ld_relaxed_gpu(P.r_next) << 10) |
+                       ld_relaxed_gpu(P.q_tail));
+        }
+#endif
         failed = true;
         break;
       }
@@ -3821,6 +3960,9 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
     idle_since = 0;
     if (!mbar_wait(&fs.bar[warp], processed & 1u, P.wait_ns)) {
       flags |= SV_STATUS_TIMEOUT;
+#ifdef SV_FLOW_DEBUG
+      flags |= 128u;
+#endif
       failed = true;
       break;
     }
@@ -3900,7 +4042,6 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
         const ReqAddr A = addr_from_base<PK>(P, b, (int)e.d0, gb);
         const SharedParts sp{part_of(s), NC};
         float* rs = rs_of(s);
-        bool done = true;
         if (MODE == MODE_GREEDY || e.greedy) {
           greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
         } else {
@@ -3909,33 +4050,16 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
           d.k = 0;
           d.reject = 0;
           d.mt = d.md = d.inv_st = d.rho = 0.0f;
-          const int k = decide_core<EB, PK>(P, sp, b, gb, e.tc, rs, A, g, d, true);
+          (void)decide_core<EB, PK>(P, sp, b, gb, e.tc, rs, A, g, d, true);
           if (__shfl_sync(0xffffffffu, d.reject, 0)) {
-            done = false;
-            if (lane == 0) {
-              e.k = k;
-              e.mt = d.mt;
-              e.md = d.md;
-              e.inv_st = d.inv_st;
-              e.rho = d.rho;
-              // the request's residual segment, published in allocation order
-              const unsigned int sg = atomicAdd(&fs.r_segs, 1u);
-              fs.rseg[sg % kFlowSegs] = e.seq;
-              const unsigned long long t0 = now_ns();
-              while (ld_acquire_cta(&fs.r_pub) != sg) {
-                if (now_ns() - t0 > P.wait_ns) {
-                  flags |= SV_STATUS_TIMEOUT;
-                  break;
-                }
-                __nanosleep(32);
-              }
-              st_release_cta(&fs.r_pub, sg + 1);
-            }
+            // the residual pass: jobs for any CTA
+            if (lane == 0) flow_post_jobs(P, b, d, P.rjobs);
           } else {
             final_bonus<EB, PK>(P, sp, b, gb, e.tc, rs[gb], stage_of(s));
           }
         }
-        if (done) finish(s);
+        count_decision();
+        finish(s);
         __syncwarp();
       }
     } else {
@@ -3945,30 +4069,41 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
       kind = take();
       int last = 0;
       if (lane == 0) {
-        rsum_of(s)[c] = sr;
+        P.resid[(size_t)e.b * P.stride_ncr + c] = sr;
         __threadfence_block();
-        last = atomicAdd(&e.r_done, 1) == NCR - 1 ? 1 : 0;
+        last = atomicAdd(&e.a_done, 1) == e.nI - 1 ? 1 : 0;
       }
       if (__shfl_sync(0xffffffffu, last, 0)) {
-        // ---- this warp completed the request's R items: the final draw
-        __threadfence_block();
-        const int k = e.k;
-        ResidC kc;
-        kc.mt = e.mt; kc.md = e.md; kc.inv_st = e.inv_st; kc.rho = e.rho;
-        resid_scales(kc);
-        kc.hi = e.tc.hi; kc.lo = e.tc.lo; kc.reject = 1;
-        const char* trow = P.target + (e.t0 + (size_t)k) * (size_t)V * EB;
-        const char* drow = P.draft + (e.d0 + (size_t)k) * (size_t)V * EB;
-        unsigned int uflags = 0;
-        const float u_fin = sanitize_uniform(P.uniforms[e.uf], uflags);
-        int tok = chunk_draw<EB, false>(trow, drow, V, NCR, u_fin, kc, rsum_of(s), stage_of(s));
+        // ---- this warp completed the job: the last job of the request draws
+        unsigned int old = 0;
+        const int b = e.b;
         if (lane == 0) {
-          if (tok < 0) {
-            flags |= SV_STATUS_INTERNAL;
-            tok = V - 1;
+          __threadfence();
+          old = atomicAdd(&P.cnt_r[b], 1u);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == (unsigned int)(P.rjobs - 1)) {
+          __threadfence();
+          if (lane == 0) P.cnt_r[b] = 0u;  // every job has arrived: reset for the next call
+          const int k = e.k;
+          ResidC kc;
+          kc.mt = e.mt; kc.md = e.md; kc.inv_st = e.inv_st; kc.rho = e.rho;
+          resid_scales(kc);
+          kc.hi = e.tc.hi; kc.lo = e.tc.lo; kc.reject = 1;
+          const char* trow = P.target + (e.t0 + (size_t)k) * (size_t)V * EB;
+          const char* drow = P.draft + (e.d0 + (size_t)k) * (size_t)V * EB;
+          unsigned int uflags = 0;
+          const float u_fin = sanitize_uniform(P.uniforms[e.uf], uflags);
+          int tok = chunk_draw<EB, true>(trow, drow, V, NCR, u_fin, kc,
+                                         P.resid + (size_t)b * P.stride_ncr, stage_of(s));
+          if (lane == 0) {
+            if (tok < 0) {
+              flags |= SV_STATUS_INTERNAL;
+              tok = V - 1;
+            }
+            P.out_tokens[(size_t)b * (G + 1) + k] = tok;
+            flags |= uflags;
           }
-          P.out_tokens[(size_t)e.b * (G + 1) + k] = tok;
-          flags |= uflags;
         }
         finish(s);
         __syncwarp();
@@ -3980,7 +4115,7 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
   if (failed && kind != KIND_NONE) (void)mbar_wait(&fs.bar[warp], processed & 1u, P.wait_ns);
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && any) atomicOr(P.status, any);
-  // the last CTA out resets the claim counter for the next call
+  // the last CTA out resets the workspace counters for the next call
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -3989,6 +4124,9 @@ __global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
   __syncthreads();
   if (s_last && tid == 0) {
     *P.next_item = 0;
+    *P.r_next = 0;
+    *P.q_tail = 0;
+    *P.dec_count = 0;
     *P.exit_count = 0;
     __threadfence();
   }
@@ -4183,8 +4321,8 @@ size_t flow_smem(int B, int G, int V, int eb) {
   const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
   const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
   const size_t part = ((size_t)(2 * G + 1) * nc * sizeof(float2) + 15) & ~(size_t)15;
-  const size_t rsum = (ncr * sizeof(unsigned long long) + 15) & ~(size_t)15;
-  return (size_t)kFlowWarps * kItemBytes + (size_t)kFlowSlots * (part + rsum + 1024 + kItemBytes) +
+  (void)ncr;
+  return (size_t)kFlowWarps * kItemBytes + (size_t)kFlowSlots * (part + 1024 + kItemBytes) +
          (((size_t)B * 5 + 15) & ~(size_t)15);
 }
 // CTAs of the request-flow kernel that fit on this device at once (cached).
@@ -4284,6 +4422,11 @@ int launch_flow(const Params& P0, int Q, cudaStream_t stream) {
   const long long want = ((long long)kFlowClaims * Q + P.B - 1) / P.B;
   P.parts = (int)(want < 1 ? 1 : (want > kFlowMaxParts ? kFlowMaxParts : want));
   if (P.parts > P.NC) P.parts = P.NC;
+  // residual jobs of about a part's size each
+  const long long items = (long long)(2 * P.G + 1) * P.NC;
+  const long long jobs = (P.NCR * (long long)P.parts + items - 1) / items;
+  P.rjobs = (int)(jobs < 1 ? 1 : (jobs > kFlowMaxJobs ? kFlowMaxJobs : jobs));
+  if (P.rjobs > P.NCR) P.rjobs = P.NCR;
   flow_kernel<EB, MODE, PK, kFlowWarps, kFlowSlots>
       <<<Q, kFlowWarps * 32, flow_smem(P.B, P.G, P.V, EB), stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
@@ -4381,6 +4524,8 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.queue = reinterpret_cast<DecRecord*>(w + L.queue);
   P.stats = reinterpret_cast<float2*>(w + L.stats);
   P.resid = reinterpret_cast<unsigned long long*>(w + L.resid);
+  P.jobs = reinterpret_cast<DecRecord*>(w + L.jobs);
+  P.rjobs = 1;
   return SV_OK;
 }
 
