@@ -2943,6 +2943,33 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
   if (lane == 0 && any) atomicOr(P.status, any);
 }
 
+// Item j of a request in streaming order: its partial slot, chunk and row.
+// Greedy steps stream target rows 0..gamma_b in order.  Sampled requests
+// stream target row gamma_b (the bonus row) first, then the positions from
+// the last down to 0, target row then draft row: the rows most often
+// rejected (position 0) come last, closest to the residual pass that may
+// re-read them.
+struct FlowRow {
+  int pslot, c, row;  // partial slot, chunk, row index within the target or draft rows
+  bool draft;
+};
+__device__ __forceinline__ FlowRow flow_row(int j, int NC, int gb, bool greedy, int G) {
+  FlowRow r;
+  const int rr = j / NC;
+  r.c = j - rr * NC;
+  if (greedy || rr == 0) {
+    r.row = greedy ? rr : gb;
+    r.pslot = r.row;
+    r.draft = false;
+  } else {
+    const int p = gb - 1 - (rr - 1) / 2;
+    r.row = p;
+    r.draft = ((rr - 1) & 1) != 0;
+    r.pslot = r.draft ? G + 1 + p : p;
+  }
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // Medium batches: one cluster per request, items streamed
 // ---------------------------------------------------------------------------
@@ -3135,20 +3162,14 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     const int nrows = sample ? 2 * gb + 1 : gb + 1;
     const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
     auto a_meta = [&](unsigned int j) {
-      const int r = (int)(j / (unsigned int)NC), c = (int)(j % (unsigned int)NC);
+      // the rows in streaming order: a sampled request's position-0 rows,
+      // the most often rejected, come last, closest to the residual pass
+      const FlowRow fr = flow_row((int)j, NC, gb, !sample, G);
+      const int c = fr.c;
       Meta m;
-      size_t roff;
-      const char* rows;
-      if (r <= gb) {
-        m.pslot = r;
-        roff = (A.t0 + (size_t)r) * (size_t)V;
-        rows = P.target;
-      } else {
-        const int i = r - gb - 1;
-        m.pslot = G + 1 + i;
-        roff = (A.d0 + (size_t)i) * (size_t)V;
-        rows = P.draft;
-      }
+      const size_t roff = ((fr.draft ? A.d0 : A.t0) + (size_t)fr.row) * (size_t)V;
+      const char* rows = fr.draft ? P.draft : P.target;
+      m.pslot = fr.pslot;
       m.kind = KIND_A;
       m.b = b;
       m.c = c;
@@ -3502,33 +3523,6 @@ __device__ bool claim_tables(const Params& P, unsigned char* nrow, int* order, i
     __syncthreads();
   }
   return sorted;
-}
-
-// Item j of a request in streaming order: its partial slot, chunk and row.
-// Greedy steps stream target rows 0..gamma_b in order.  Sampled requests
-// stream target row gamma_b (the bonus row) first, then the positions from
-// the last down to 0, target row then draft row: the rows most often
-// rejected (position 0) come last, closest to the residual pass that may
-// re-read them.
-struct FlowRow {
-  int pslot, c, row;  // partial slot, chunk, row index within the target or draft rows
-  bool draft;
-};
-__device__ __forceinline__ FlowRow flow_row(int j, int NC, int gb, bool greedy, int G) {
-  FlowRow r;
-  const int rr = j / NC;
-  r.c = j - rr * NC;
-  if (greedy || rr == 0) {
-    r.row = greedy ? rr : gb;
-    r.pslot = r.row;
-    r.draft = false;
-  } else {
-    const int p = gb - 1 - (rr - 1) / 2;
-    r.row = p;
-    r.draft = ((rr - 1) & 1) != 0;
-    r.pslot = r.draft ? G + 1 + p : p;
-  }
-  return r;
 }
 
 // A warp's copy of the entry its items last came from (shared memory, private
