@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layout", choices=["padded", "packed"], default="padded",
                     help="padded [B][G+1][V] rows, or packed rows with a cu_draft prefix")
+    ap.add_argument("--read", choices=["lazy", "eager"], default="lazy",
+                    help="request claims: read a sampled request's positions one at a time, "
+                         "stopping at the first rejection (lazy, the default), or all rows first")
     ap.add_argument("--schedule", choices=["auto", "stream", "persistent"], default="auto",
                     help="auto: the resident cluster path, the streaming cluster path or the "
                          "persistent grid, the first that applies; stream: never the resident "
@@ -316,12 +319,16 @@ def run_ours(args):
     binding.spec_verify_set_schedule({"auto": binding.SCHEDULE_AUTO,
                                       "stream": binding.SCHEDULE_STREAM,
                                       "persistent": binding.SCHEDULE_PERSISTENT}[args.schedule])
+    binding.spec_verify_set_lazy(args.read == "lazy")
     route, csize = binding.spec_verify_route(base.target.dtype, B, G, V, greedy=mode == "greedy")
+    lazy = mode == "sample" and route == binding.ROUTE_CLAIMS and args.read == "lazy"
     kernel = {binding.ROUTE_CLUSTER: "cluster_kernel", binding.ROUTE_STREAM: "stream_kernel",
               binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
     schedule = {binding.ROUTE_CLUSTER: f"resident clusters of {csize} CTAs, one per request",
                 binding.ROUTE_STREAM: f"streaming clusters of {csize} CTAs, one per request",
-                binding.ROUTE_CLAIMS: "streaming CTAs claiming requests in turn, longest first",
+                binding.ROUTE_CLAIMS: "streaming CTAs claiming requests in turn, longest first"
+                                      + (", positions read one at a time up to the first rejection"
+                                         if lazy else ""),
                 binding.ROUTE_PERSISTENT: "persistent grid"}[route]
     # the persistent grid runs batches of more than 1536 requests as several launches
     launches_per_call = math.ceil(B / 1536) if route == binding.ROUTE_PERSISTENT else 1
@@ -429,8 +436,14 @@ def run_ours(args):
     value = gsum_all / (ms_step * 1e-3)
 
     bytes_min = base.bytes_min(mode)
-    # roofline of one GPU: this rank's algorithmic bytes over its own step time
-    achieved = bytes_min / (ms / K * 1e-3) / 1e9
+    # roofline of one GPU: this rank's algorithmic bytes over its own step time.
+    # Read lazily, a call needs only the rows up to each request's first
+    # rejection (and the bonus row after full acceptance): those bytes are the
+    # algorithm's; one read of every logit is reported beside them.
+    bytes_need = base.bytes_needed(mode, v.num_accepted, lazy,
+                                   ctas=props.multi_processor_count)  # one CTA per SM
+    achieved = bytes_need / (ms / K * 1e-3) / 1e9
+    every_logit = bytes_min / (ms / K * 1e-3) / 1e9
     peak, peak_src = measured_peak_hbm()
     gpu_out = (v.out_tokens.cpu().numpy(), v.num_accepted.cpu().numpy())
 
@@ -500,7 +513,8 @@ def run_ours(args):
                     "l2": f"inputs larger than L2: rotating {ncopy} device copies of the logits "
                           f"({ncopy * per_copy / 2**20:.0f} MiB; L2 {l2 / 2**20:.0f} MiB)",
                     "emitted_tokens_per_s": emitted_all / (ms_step * 1e-3),
-                    "bytes_min_per_step": bytes_min})
+                    "bytes_min_per_step": bytes_min,
+                    "bytes_needed_per_step": bytes_need})
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": K, "warmup": args.warmup, "repeats": reps, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -508,6 +522,10 @@ def run_ours(args):
                 "data": "synthetic", "config": cfg,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "peak_source": peak_src,
+                             "bytes": "rows needed up to each first rejection" if lazy
+                                      else "one read of every logit",
+                             "every_logit_gbs": every_logit,
+                             "every_logit_frac": every_logit / peak,
                              "traffic": None if packed else profiled_traffic(args.config, mode, kernel),
                              "kernel": kernel + " (one launch per step)"},
                 "clocks": clk, "e2e": e2e, "gpu_launches": reps * K * launches_per_call,

@@ -212,7 +212,10 @@ int spec_verify_draw(const void *logits, sv_dtype dtype, int B, int V, const flo
  * First call on a device: it looks up the array's device address with
  * cudaGetSymbolAddress while that device is current and keeps it for later
  * calls on the same device (SV_ERR_CUDA if the look-up fails).  Make that
- * first call before any stream capture begins.
+ * first call before any stream capture begins.  The kept address belongs to
+ * the device's primary context: after cudaDeviceReset on that device it is
+ * stale, and a later call would launch on a freed address.  A process that
+ * resets a device must not call spec_verify_sample_noalloc on it again.
  *
  * Sharing: every call in the process uses the same array.  Each call first
  * zeroes the array's counters and flags (an asynchronous memset on `stream`),
@@ -305,6 +308,24 @@ int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int *clus
  * quickly.  Returns the previous limit.
  */
 unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
+
+/*
+ * spec_verify_set_lazy: how the request-claims schedule (SV_ROUTE_CLAIMS)
+ * reads a sampled request's rows in the calls that follow in this process.
+ * 1 (the default): position by position.  The target and draft rows of
+ * position i are reduced and draft i is tested before the rows of position
+ * i + 1 matter, and the bonus row gamma_b only after every draft was
+ * accepted, as in the verification loop of disassemble-channel
+ * "Speculative Decoding theory", Step 3, which stops at the first rejected
+ * draft.  While one position is tested, the CTA already
+ * streams the next one; what it read of a position after the first
+ * rejection is not used.  0: every row of the request is reduced before any
+ * test.  The outputs are identical either way: a position's arithmetic does
+ * not depend on the order.  The other schedules always read every row.
+ * Returns the previous setting, or SV_ERR_SCALAR for a value other than 0
+ * or 1.
+ */
+int spec_verify_set_lazy(int on);
 int spec_verify_cluster_size(sv_dtype dtype, int B, int G, int V, int greedy);
 
 #ifdef __cplusplus

@@ -25,7 +25,7 @@ EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_gree
            "spec_verify_sample_packed", "spec_verify_greedy_packed", "spec_verify_draw",
            "spec_verify_sample_noalloc", "spec_verify_status", "spec_verify_strerror",
            "spec_verify_set_schedule", "spec_verify_route", "spec_verify_cluster_size",
-           "spec_verify_set_wait_limit")
+           "spec_verify_set_wait_limit", "spec_verify_set_lazy")
 SCHEDULE_AUTO, SCHEDULE_PERSISTENT, SCHEDULE_STREAM = 0, 1, 2
 ROUTE_PERSISTENT, ROUTE_CLUSTER, ROUTE_STREAM, ROUTE_CLAIMS = 0, 1, 2, 3
 
@@ -77,6 +77,8 @@ def load_library():
         lib.spec_verify_cluster_size.argtypes = [ci, ci, ci, ci, ci]
         lib.spec_verify_set_wait_limit.restype = ctypes.c_ulonglong
         lib.spec_verify_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+        lib.spec_verify_set_lazy.restype = ci
+        lib.spec_verify_set_lazy.argtypes = [ci]
         _lib = lib
         return lib
 
@@ -92,6 +94,15 @@ def spec_verify_set_schedule(schedule: int) -> int:
     if rc < 0:
         raise SpecVerifyError(rc)
     return rc
+
+
+def spec_verify_set_lazy(on: bool) -> bool:
+    """Position-by-position reading on the request-claims schedule for the calls
+    that follow (the default); returns the previous setting."""
+    rc = load_library().spec_verify_set_lazy(1 if on else 0)
+    if rc < 0:
+        raise SpecVerifyError(rc)
+    return bool(rc)
 
 
 def spec_verify_set_wait_limit(ns: int) -> int:

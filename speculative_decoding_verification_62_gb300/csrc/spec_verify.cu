@@ -110,6 +110,22 @@ constexpr unsigned int kMaxRBatch = SV_MAXKR;         // R items per claim, at m
 // the longer hold of the last requests' items)
 constexpr unsigned int kBatchDiv = SV_BATCH_DIV;
 constexpr unsigned long long kWaitNs = 2000000000ull; // default wait limit: 2 s
+#ifndef SV_LAZY
+#define SV_LAZY 1
+#endif
+// default of spec_verify_set_lazy: request claims test a sampled request's
+// positions one at a time, reading a position's rows only when every earlier
+// draft was accepted
+constexpr int kLazyDefault = SV_LAZY != 0 ? 1 : 0;
+#ifndef SV_SPEC_MIN_GAMMA
+#define SV_SPEC_MIN_GAMMA 4
+#endif
+// A lazy request with at least this many drafts has its next position's rows
+// read while a position is decided (the bonus row is not read ahead).  Short
+// requests do not: for them the rows read ahead after a rejection cost more
+// than the wait saved after an acceptance (B = 512: gamma 3, 174 against 178 us;
+// ragged gamma 1..7: 135 against 132 us).
+constexpr int kSpecMinGamma = SV_SPEC_MIN_GAMMA;
 
 constexpr float kLog2eHi = 1.44269502162933349609375f;      // float nearest log2(e)
 constexpr float kLog2eLo = 1.925963033500011e-08f;          // log2(e) - kLog2eHi
@@ -191,6 +207,7 @@ struct Params {
   double* q_tok;
   unsigned int* status;
   unsigned long long wait_ns;  // every bounded wait gives up after this long
+  int lazy;                   // request claims: positions one stage at a time
   unsigned int* next_item;   // next A item to claim (past the fixed first batches)
   unsigned int* r_next;      // next R item to claim: item i is chunk i % NCR of the
                              // request in queue slot i / NCR
@@ -714,6 +731,10 @@ struct SharedParts {  // this CTA's shared memory
     return p[slot * stride + c];
   }
 };
+struct RowParts {  // a copy of one row's partials (the slot is implied)
+  const float2* p;
+  __device__ __forceinline__ float2 operator()(int, int c) const { return p[c]; }
+};
 __device__ __forceinline__ GlobalParts global_parts(const Params& P, int b) {
   return GlobalParts{P.stats + (size_t)b * (2 * P.G + 1) * P.stride_nc, (size_t)P.stride_nc};
 }
@@ -725,20 +746,30 @@ __device__ __forceinline__ GlobalParts global_parts(const Params& P, int b) {
 constexpr int kHeld = 10;
 
 // Row statistics (sampling): M = max, S = sum_c s_c 2^((m_c - M) c) in
-// float-float, written to rs[r] (M), rs[64 + r] (S hi), rs[128 + r] (S lo).
+// float-float, written to rs[x] (M), rs[64 + x] (S hi), rs[128 + x] (S lo),
+// x = i for target row i and gamma_b + 1 + i for draft row i.  The rows are
+// those of positions [lo, hi) (target, then draft) and, if `bonus`, target
+// row gamma_b; a row's arithmetic does not depend on which others share the
+// call.
 template <int EB, class Parts>
 __device__ __forceinline__ unsigned int row_stats(const Params& P, const Parts& parts, int gb,
-                                                  TempC tc, float* rs) {
+                                                  TempC tc, float* rs, int lo, int hi,
+                                                  bool bonus) {
   const int G = P.G, NC = P.NC;
   const int lane = threadIdx.x & 31, part = lane & 3;
-  const int nrows = 2 * gb + 1;
+  const int npos = hi - lo;
+  const int nrows = 2 * npos + (bonus ? 1 : 0);
   const float2 none = make_float2(-INFINITY, 0.0f);
   unsigned int flags = 0;
 #pragma unroll 1
   for (int r0 = 0; r0 < nrows; r0 += 8) {
     const int r = r0 + (lane >> 2);
     const bool live = r < nrows;
-    const int slot = live ? (r <= gb ? r : (G + 1 + (r - gb - 1))) : 0;
+    // the row: target lo + r, draft lo + r - npos, or the bonus row
+    const int ti = r < npos ? lo + r : (r < 2 * npos ? -1 : gb);
+    const int di = lo + r - npos;
+    const int slot = !live ? 0 : (ti >= 0 ? ti : G + 1 + di);
+    const int x = ti >= 0 ? ti : gb + 1 + di;
     float2 v[kHeld];
 #pragma unroll
     for (int j = 0; j < kHeld; ++j) {
@@ -769,9 +800,9 @@ __device__ __forceinline__ unsigned int row_stats(const Params& P, const Parts& 
     S = ff_add(S, shfl_xor_ff(S, 2));
     if (live && part == 0) {
       if (!isfinite(m) || !(S.hi > 0.0f)) flags |= SV_STATUS_NONFINITE_ROW;
-      rs[r] = m;
-      rs[64 + r] = S.hi;
-      rs[128 + r] = S.lo;
+      rs[x] = m;
+      rs[64 + x] = S.hi;
+      rs[128 + x] = S.lo;
     }
   }
   __syncwarp();
@@ -1026,27 +1057,34 @@ __device__ __forceinline__ DraftIn gather_drafts(const Params& P, const ReqAddr&
   return g;
 }
 
-// The acceptance tests of request b from its row statistics: returns k on
-// every lane with the decision on lane 0 and, when emit is set, writes
-// out_tokens (all but position k), num_accepted, p/q and status.
+// The acceptance tests of request b at positions [lo, hi) from the row
+// statistics of those positions (and of the bonus row gamma_b, if `bonus`),
+// every earlier position having been accepted.  Returns k, the first
+// rejected position (gamma_b when every draft is accepted and the bonus row
+// is in), on every lane with the decision on lane 0; or -1 when all of
+// [lo, hi) are accepted and later positions remain to be tested.  When emit
+// is set it writes p/q of [lo, hi) and, once k is known, out_tokens (all but
+// position k), num_accepted, p/q NaN past hi, and status.  One call over
+// [0, gamma_b) with the bonus row is the whole decision.
 template <int EB, bool PK, class Parts>
-__device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, int b, int gb,
-                                           TempC tc, float* rs, const ReqAddr& A,
-                                           const DraftIn& g, Decision& d, bool emit = true) {
+__device__ __forceinline__ int decide_range(const Params& P, const Parts& parts, int b, int gb,
+                                            TempC tc, float* rs, const ReqAddr& A,
+                                            const DraftIn& g, Decision& d, int lo, int hi,
+                                            bool bonus, bool emit) {
   const int G = P.G;
   const int lane = threadIdx.x & 31;
   const int i = lane;
   const int x = g.x;
   const float u = g.u, zt = g.zt, zd = g.zd;
-  unsigned int flags = g.flags;
-  flags |= row_stats<EB>(P, parts, gb, tc, rs);
+  unsigned int flags = lo == 0 ? g.flags : 0u;
+  flags |= row_stats<EB>(P, parts, gb, tc, rs, lo, hi, bonus);
 
   // Acceptance test per position (lane i), then the first-reject ballot.
   // ratio p/q = 2^(e_t - e_d) * S_d / S_t with e = (z - m) log2(e)/T in
   // float-float; 2^(e_t - e_d) = 2^n * 2^f with |f| <= 1/2.
   bool reject = false;
   double p = NAN, q = NAN;
-  if (i < gb) {
+  if (i >= lo && i < hi) {
     const float mt = rs[i], md = rs[gb + 1 + i];
     const FF st{rs[64 + i], rs[128 + i]}, sd{rs[64 + gb + 1 + i], rs[128 + gb + 1 + i]};
     const FF et = ff_mul(ff_two_sum(zt, -mt), tc.hi, tc.lo);  // log2 of S_t p(x)
@@ -1079,14 +1117,17 @@ __device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, 
     }
   }
   const unsigned int rej = __ballot_sync(0xffffffffu, reject);
-  const int k = rej ? (__ffs(rej) - 1) : gb;
-  if (emit && i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
-  if (emit && i < (PK ? gb : G)) {  // packed p/q hold this request's gb entries only
-    const bool evaluated = i < gb && i <= k;
+  const int k = rej ? (__ffs(rej) - 1) : (bonus ? gb : -1);
+  if (emit && k >= 0 && i <= G && i != k) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : -1;
+  // packed p/q hold this request's gb entries only
+  if (emit && i >= lo && i < (PK ? gb : G) && (k >= 0 || i < hi)) {
+    const bool evaluated = i < hi && (k < 0 || i <= k);
     if (P.p_tok) P.p_tok[A.d0 + i] = evaluated ? p : NAN;
     if (P.q_tok) P.q_tok[A.d0 + i] = evaluated ? q : NAN;
   }
   const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (emit && lane == 0 && any) atomicOr(P.status, any);
+  if (k < 0) return k;
   if (lane == 0) {
     const int kd = gb + 1 + (k < gb ? k : 0);
     const FF st_k{rs[64 + k], rs[128 + k]}, sd_k{rs[64 + kd], rs[128 + kd]};
@@ -1099,9 +1140,15 @@ __device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, 
     d.rho = d.reject ? ff_div(st_k, sd_k) : 0.0f;
     d.c_hi = tc.hi;
     d.c_lo = tc.lo;
-    if (emit && any) atomicOr(P.status, any);
   }
   return k;
+}
+
+template <int EB, bool PK, class Parts>
+__device__ __forceinline__ int decide_core(const Params& P, const Parts& parts, int b, int gb,
+                                           TempC tc, float* rs, const ReqAddr& A,
+                                           const DraftIn& g, Decision& d, bool emit = true) {
+  return decide_range<EB, PK>(P, parts, b, gb, tc, rs, A, g, d, 0, gb, true, emit);
 }
 
 // Sampling decision on the persistent path, run by the warp that completed
@@ -1521,60 +1568,76 @@ __device__ __forceinline__ float item_load_max(const char* stage, uint32_t (&w)[
   }
 }
 
-// The exponent argument here is (z - max) times log2(e)/T rounded to one
+// The exponent argument is (z - max) c with c = log2(e)/T rounded to one
 // float: the constant's rounding (at most |a| 2^-24) is below ex2.approx's own
-// relative error for the terms that carry the sum, so the two-term constant
-// of the per-request arithmetic would cost an extra multiply per logit pair
-// for no accuracy.  (Chunk combines, the decision and the draw weights keep
-// the two-term form.)
+// relative error for the terms that carry the sum.  (Chunk combines, the
+// decision and the draw weights keep the two-term form.)  It is formed with
+// one fused multiply-add, z c + RN(-max c): exact before its one rounding,
+// but for the constant delta = max c - RN(max c), the product's rounding
+// error, which every term shares.  Each term is thus 2^delta too large, and
+// the sum is multiplied by 2^-delta once (|delta| <= 2^-24 |max c|, which
+// ex2.approx takes to about 2^-22 relative).  Where max c overflows a float
+// (logits beyond about 1e36 at small T) the argument is (z - max) c instead.
+
+// Sum of 2^arg(z) over the item's words held by this lane.
+template <int EB, bool FUSED>
+__device__ __forceinline__ float item_exp_lane(const uint32_t (&w)[kItemWords], float mx, float c1,
+                                               float nmc) {
+  constexpr int VEC = 16 / EB;
+  constexpr int NV = kItemBytes / 16 / 32;
+  if constexpr (EB == 2) {
+    // the arguments and the sum on float32 pairs, 8 accumulators
+    const unsigned long long nm = f2_pack(nmc, nmc), negm = f2_pack(-mx, -mx);
+    const unsigned long long cc = f2_pack(c1, c1);
+    unsigned long long acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0ull;
+#pragma unroll
+    for (int i = 0; i < kItemWords; ++i) {
+      const unsigned long long a = FUSED ? f2_fma(bf16x2_to_f2(w[i]), cc, nm)
+                                         : f2_mul(f2_add(bf16x2_to_f2(w[i]), negm), cc);
+      float a0, a1;
+      f2_unpack(a, a0, a1);
+      acc[i & 7] = f2_add(acc[i & 7], f2_pack(ex2_approx(a0), ex2_approx(a1)));
+    }
+#pragma unroll
+    for (int width = 4; width >= 1; width >>= 1)
+#pragma unroll
+      for (int i = 0; i < width; ++i) acc[i] = f2_add(acc[i], acc[i + width]);
+    float s0, s1;
+    f2_unpack(acc[0], s0, s1);
+    return s0 + s1;
+  } else {
+    float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      float e[VEC];
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) {
+        const float z = __uint_as_float(w[4 * j + q]);
+        e[q] = ex2_approx(FUSED ? __fmaf_rn(z, c1, nmc) : __fmul_rn(__fsub_rn(z, mx), c1));
+      }
+#pragma unroll
+      for (int u = VEC; u > 1; u >>= 1)
+#pragma unroll
+        for (int q = 0; q < u / 2; ++q) e[q] = e[2 * q] + e[2 * q + 1];
+      sq[j & 3] += e[0];
+    }
+    return (sq[0] + sq[1]) + (sq[2] + sq[3]);
+  }
+}
+
 template <int EB>
 __device__ __forceinline__ float item_exp_sum(const uint32_t (&w)[kItemWords], float mx, float c_hi,
                                               float c_lo) {
-  constexpr int VEC = 16 / EB;
-  constexpr int NV = kItemBytes / 16 / 32;
+  if (!(mx > -INFINITY)) return 0.0f;
   const float c1 = __fadd_rn(c_hi, c_lo);
-  float sum = 0.0f;
-  if (mx > -INFINITY) {
-    if constexpr (EB == 2) {
-      // (z - m) * c and the sum, on float32 pairs, 8 accumulators
-      const unsigned long long negm = f2_pack(-mx, -mx);
-      const unsigned long long cc = f2_pack(c1, c1);
-      unsigned long long acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0ull;
-#pragma unroll
-      for (int i = 0; i < kItemWords; ++i) {
-        const unsigned long long d = f2_add(bf16x2_to_f2(w[i]), negm);
-        const unsigned long long a = f2_mul(d, cc);
-        float a0, a1;
-        f2_unpack(a, a0, a1);
-        acc[i & 7] = f2_add(acc[i & 7], f2_pack(ex2_approx(a0), ex2_approx(a1)));
-      }
-#pragma unroll
-      for (int width = 4; width >= 1; width >>= 1)
-#pragma unroll
-        for (int i = 0; i < width; ++i) acc[i] = f2_add(acc[i], acc[i + width]);
-      float s0, s1;
-      f2_unpack(acc[0], s0, s1);
-      sum = s0 + s1;
-    } else {
-      float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        float e[VEC];
-#pragma unroll
-        for (int q = 0; q < VEC; ++q)
-          e[q] = ex2_approx(__fmul_rn(__fsub_rn(__uint_as_float(w[4 * j + q]), mx), c1));
-#pragma unroll
-        for (int u = VEC; u > 1; u >>= 1)
-#pragma unroll
-          for (int q = 0; q < u / 2; ++q) e[q] = e[2 * q] + e[2 * q + 1];
-        sq[j & 3] += e[0];
-      }
-      sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-    }
+  const float nmc = -__fmul_rn(mx, c1);
+  if (fabsf(nmc) <= 3.0e38f) {  // the same on every lane
+    const float delta = __fmaf_rn(mx, c1, nmc);  // exact
+    return __fmul_rn(warp_sum(item_exp_lane<EB, true>(w, mx, c1, nmc)), ex2_approx(-delta));
   }
-  return warp_sum(sum);
+  return warp_sum(item_exp_lane<EB, false>(w, mx, c1, nmc));
 }
 
 template <int EB>
@@ -3003,9 +3066,12 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
   __shared__ __align__(8) uint64_t bar[NW][NB];
   __shared__ Meta smeta[NW][NB];  // the item in each buffer
   __shared__ float rsbuf[192];         // the decision's row statistics
-  __shared__ ClusterDec sdec;
+  __shared__ ClusterDec sdec[2];  // by decision number: a warp reads one while the next is made
   __shared__ int s_next, s_last;       // the CTA's next claim; last CTA out
+  __shared__ unsigned int s_ctr;       // tickets for the items of a phase
+  __shared__ unsigned int s_dec;       // the latest decision: number << 1 | final
   __shared__ int s_hist[64];           // claim order: first position per row count
+  __shared__ unsigned int s_rows;      // claims: the batch's rows
   constexpr int AE = kItemBytes / EB;   // logits per A item
   constexpr int RE = kHalfBytes / EB;   // logits per R chunk and row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -3015,6 +3081,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
   const int G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
   float2* part = reinterpret_cast<float2*>(dsmem + (size_t)NW * NB * kItemBytes);
   unsigned long long* rsum = reinterpret_cast<unsigned long long*>(part + (size_t)(2 * G + 1) * NC);
+  float2* bpart = reinterpret_cast<float2*>(rsum + NCR);  // the bonus row's partials, copied
   unsigned char* mybuf = dsmem + (size_t)warp * NB * kItemBytes;
   uint64_t* mybar = bar[warp];
   Meta* mymeta = smeta[warp];
@@ -3028,7 +3095,11 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     for (int s = 0; s < NB; ++s) mbar_init(&mybar[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncwarp();
+  if (tid == 0) {
+    s_ctr = 0;
+    s_dec = ~0u;
+  }
+  __syncthreads();
 
   unsigned int issued = 0, processed = 0;  // copies started and consumed by this warp
   bool failed = false;
@@ -3059,13 +3130,31 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     failed = true;
     return false;
   };
+  // Work within a phase (a stage's A items, or the R chunks) is taken from
+  // a CTA counter: CTA r of the cluster takes the phase's items r, r + C,
+  // r + 2C, ... in turn, so a warp that starts a phase late (warp 0 after a
+  // draw) takes fewer.  Lane 0 requests the next ticket when it starts a
+  // copy and reads it before the next one.  Every warp takes part in every
+  // phase and stops at its first ticket past the phase's end, so a phase
+  // uses n + NW tickets and every warp knows where the next one starts.
+  unsigned int tbase = 0, ticket = 0;
+  unsigned int dseq = 0;  // decisions made by this CTA so far
+  auto claim_next = [&]() {
+    if (lane == 0) ticket = atomicAdd(&s_ctr, 1u);
+  };
+  auto claimed = [&]() -> unsigned int {  // index within this CTA's share
+    return __shfl_sync(0xffffffffu, ticket, 0) - tbase;
+  };
+  auto share = [&](unsigned int n) -> unsigned int {  // this CTA's items of n
+    return n > rank ? (n - rank + C - 1) / C : 0u;
+  };
 
   // Claims are taken longest request first (by row count, then index): the
   // short requests claimed last fill in around the long ones.  Every CTA
   // builds the same order in shared memory: all threads read the row counts;
   // if they differ, warp 0 places each request with a stable counting sort
   // (about 3 us at B = 512, so a batch of equal counts keeps index order).
-  int* order = reinterpret_cast<int*>(rsum + NCR);                      // [B] requests by claim
+  int* order = reinterpret_cast<int*>(bpart + NC);                      // [B] requests by claim
   unsigned char* nrow = reinterpret_cast<unsigned char*>(order + P.B);  // [B] row counts
   bool sorted = false;  // claims go through `order`
   if (queue) {
@@ -3079,12 +3168,18 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     };
     const int r0 = rows_of_req(0);
     int differs = 0;
+    unsigned int rows = 0;
+    if (tid == 0) s_rows = 0;
+    __syncthreads();
 #pragma unroll 4
     for (int b = tid; b < P.B; b += NW * 32) {
       const int r = rows_of_req(b);
       nrow[b] = (unsigned char)r;
       differs |= r != r0;
+      rows += (unsigned int)r;
     }
+    rows = __reduce_add_sync(0xffffffffu, rows);
+    if (lane == 0) atomicAdd(&s_rows, rows);
     sorted = __syncthreads_or(differs) != 0;
   }
   if (sorted) {
@@ -3158,33 +3253,65 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
       u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
     }
 
-    // ---- the A items
-    const int nrows = sample ? 2 * gb + 1 : gb + 1;
-    const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
-    auto a_meta = [&](unsigned int j) {
-      // the rows in streaming order: a sampled request's position-0 rows,
-      // the most often rejected, come last, closest to the residual pass
-      const FlowRow fr = flow_row((int)j, NC, gb, !sample, G);
-      const int c = fr.c;
-      Meta m;
-      const size_t roff = ((fr.draft ? A.d0 : A.t0) + (size_t)fr.row) * (size_t)V;
-      const char* rows = fr.draft ? P.draft : P.target;
-      m.pslot = fr.pslot;
-      m.kind = KIND_A;
-      m.b = b;
-      m.c = c;
-      m.n = min(AE, V - c * AE);
-      m.reject = 0;
-      m.pad = 0;
-      m.p0 = rows + (roff + (size_t)c * AE) * EB;
-      m.p1 = nullptr;
-      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-      m.mt = m.md = m.inv_st = m.rho = 0.0f;
-      m.c_hi = tc.hi;
-      m.c_lo = tc.lo;
-      return m;
-    };
-    {
+    // The A items come in stages, each followed by the decision over its
+    // positions.  With claims a sampled request is taken lazily: stage s
+    // holds target and draft rows s only, and the rows of position s + 1
+    // matter only if draft s is accepted (the stage after the last position
+    // holds the bonus row gamma_b).  While warp 0 decides stage s, the other
+    // warps already stream stage s + 1; if the decision is final they stop
+    // taking its items, and what they read of it is not used.  Otherwise one
+    // stage holds every row.  Each position's arithmetic is the same either
+    // way.
+    // A request whose rows alone reach 80 % of a CTA's average share of the
+    // batch is read eagerly: the call lasts at least as long as it does, and
+    // lazy stages would lengthen it.
+    const bool lazy = P.lazy && queue && sample &&
+                      5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
+                          4ull * (unsigned long long)s_rows;
+    auto stage_hi = [&](int slo) { return lazy ? min(slo + 1, gb) : gb; };
+    // The items of the stage that starts at position slo.  With `spec` the
+    // warp stops taking them once the decision in progress (number dseq) is
+    // final; it still draws its remaining tickets, so that the stage uses
+    // its usual count.
+    auto run_stage = [&](int slo, bool spec) {
+      const int hi = stage_hi(slo);
+      const bool with_bonus = !lazy || slo == gb;
+      const int npos = hi - slo;
+      const int nrows = !sample ? gb + 1 : 2 * npos + (with_bonus ? 1 : 0);
+      const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
+      auto a_meta = [&](unsigned int j) {
+        // the rows in streaming order: eagerly, a sampled request's position-0
+        // rows, the most often rejected, come last, closest to the residual
+        // pass; lazily, target row slo then draft row slo (or the bonus row)
+        FlowRow fr;
+        if (lazy) {
+          const int rr = (int)j / NC;
+          fr.c = (int)j - rr * NC;
+          fr.draft = rr == 1;
+          fr.row = npos ? slo : gb;
+          fr.pslot = fr.draft ? G + 1 + slo : fr.row;
+        } else {
+          fr = flow_row((int)j, NC, gb, !sample, G);
+        }
+        const int c = fr.c;
+        Meta m;
+        const size_t roff = ((fr.draft ? A.d0 : A.t0) + (size_t)fr.row) * (size_t)V;
+        const char* rows = fr.draft ? P.draft : P.target;
+        m.pslot = fr.pslot;
+        m.kind = KIND_A;
+        m.b = b;
+        m.c = c;
+        m.n = min(AE, V - c * AE);
+        m.reject = 0;
+        m.pad = 0;
+        m.p0 = rows + (roff + (size_t)c * AE) * EB;
+        m.p1 = nullptr;
+        m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+        m.mt = m.md = m.inv_st = m.rho = 0.0f;
+        m.c_hi = tc.hi;
+        m.c_lo = tc.lo;
+        return m;
+      };
       // lane r < C stores each partial into CTA r: every CTA decides locally
       const uint32_t part_r = rank_addr(part, (uint32_t)lane < C ? (uint32_t)lane : 0u);
       auto store_at = [&](int pslot, int c, float2 pr) {
@@ -3192,11 +3319,24 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
           st_cluster_f2(part_r + (uint32_t)((pslot * NC + c) * (int)sizeof(float2)), pr);
       };
       auto store_part = [&](const Meta& m, float2 pr) { store_at(m.pslot, m.c, pr); };
-      unsigned int jn = gw;  // this warp's next item
+      const unsigned int nA = share(nI);
+      const unsigned int final_tag = (dseq << 1) | 1u;
+      bool more = true;  // this warp's tickets have not yet run past the stage
+      bool dropped = false;
+      claim_next();
       auto top_up = [&]() {  // start copies into every free buffer
-        while (issued - processed < (unsigned int)NB && jn < nI) {
-          issue(a_meta(jn));
-          jn += W;
+        while (more && !dropped && issued - processed < (unsigned int)NB) {
+          if (spec && *reinterpret_cast<volatile unsigned int*>(&s_dec) == final_tag) {
+            dropped = true;
+            break;
+          }
+          const unsigned int t = claimed();
+          if (t >= nA) {
+            more = false;
+          } else {
+            issue(a_meta(rank + C * t));
+            claim_next();
+          }
         }
       };
       while (!failed) {
@@ -3237,51 +3377,88 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
           store_part(mymeta[processed % NB], make_float2(NAN, 0.0f));
           __syncwarp();
         }
-        for (; jn < nI; jn += W) store_part(a_meta(jn), make_float2(NAN, 0.0f));
       }
-    }
-    cluster_sync();  // every CTA holds every partial
+      // tickets left after a failure or a dropped stage
+      while (more) {
+        const unsigned int t = claimed();
+        if (t >= nA) {
+          more = false;
+        } else {
+          if (!dropped) store_part(a_meta(rank + C * t), make_float2(NAN, 0.0f));
+          claim_next();
+        }
+      }
+      tbase += nA + NW;
+    };
 
-    // ---- the decision (as on the resident cluster path)
+    ClusterDec cd;
+    run_stage(0, false);
+    cluster_sync();  // every CTA holds every partial of the first stage
     // greedy: no further cluster work (with claims, C == 1: every CTA leads)
     if (greedy && rank != 0) return;
-    if (warp == 0) {
-      // queue: the next request is claimed now, its latency hidden by the decision
-      if (lane == 0) s_next = queue ? (int)atomicAdd(P.next_item, 1u) + nq : P.B;  // a claim
-      float* rs = rsbuf;
-      const SharedParts sp{part, NC};
-      ClusterDec cd;
-      cd.k = 0;
-      cd.go = 0;
-      cd.mt = cd.md = cd.inv_st = cd.rho = 0.0f;
-      cd.c_hi = tc.hi;
-      cd.c_lo = tc.lo;
-      if (greedy) {
-        greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
-      } else {
-        Decision d;
-        d.k = 0;
-        d.reject = 0;
-        d.mt = d.md = d.inv_st = d.rho = 0.0f;
-        const int k = decide_core<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d, rank == 0);
-        cd.k = k;
-        cd.go = __shfl_sync(0xffffffffu, d.reject, 0);
-        cd.mt = __shfl_sync(0xffffffffu, d.mt, 0);
-        cd.md = __shfl_sync(0xffffffffu, d.md, 0);
-        cd.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
-        cd.rho = __shfl_sync(0xffffffffu, d.rho, 0);
-        // every draft accepted: the leader draws the bonus token (this warp's
-        // copies are all consumed, so its buffers serve as staging)
-        if (k == gb && rank == 0) final_bonus<EB, PK>(P, sp, b, gb, tc, rs[gb], mybuf);
+    for (int lo = 0;;) {
+      const int hi = stage_hi(lo);
+      const bool with_bonus = !lazy || lo == gb;
+      // ---- the decision (as on the resident cluster path)
+      if (warp == 0) {
+        // queue: the next request is claimed now, its latency hidden by the decision
+        unsigned int nclaim = 0;
+        if (lane == 0 && lo == 0 && queue) nclaim = atomicAdd(P.next_item, 1u);
+        float* rs = rsbuf;
+        const SharedParts sp{part, NC};
+        ClusterDec dc;
+        dc.k = 0;
+        dc.go = 0;
+        dc.mt = dc.md = dc.inv_st = dc.rho = 0.0f;
+        dc.c_hi = tc.hi;
+        dc.c_lo = tc.lo;
+        if (greedy) {
+          greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
+        } else {
+          Decision d;
+          d.k = 0;
+          d.reject = 0;
+          d.mt = d.md = d.inv_st = d.rho = 0.0f;
+          const int k = decide_range<EB, PK>(P, sp, b, gb, tc, rs, A, gin, d, lo, hi,
+                                             with_bonus, rank == 0);
+          dc.k = k;
+          dc.go = __shfl_sync(0xffffffffu, d.reject, 0);
+          dc.mt = __shfl_sync(0xffffffffu, d.mt, 0);
+          dc.md = __shfl_sync(0xffffffffu, d.md, 0);
+          dc.inv_st = __shfl_sync(0xffffffffu, d.inv_st, 0);
+          dc.rho = __shfl_sync(0xffffffffu, d.rho, 0);
+          // every draft accepted: the leader draws the bonus token after the
+          // CTA's other warps have moved on, from a copy of the row's partials
+          // (the next request's items overwrite the table)
+          if (k == gb && rank == 0) {
+            for (int c = lane; c < NC; c += 32) bpart[c] = part[gb * NC + c];
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          if (lo == 0) s_next = queue ? (int)nclaim + nq : P.B;
+          sdec[dseq & 1] = dc;
+          if (dc.k >= 0 && rank == 0 && rflags) atomicOr(P.status, rflags);
+          *reinterpret_cast<volatile unsigned int*>(&s_dec) = (dseq << 1) | (dc.k >= 0 ? 1u : 0u);
+        }
+        __syncwarp();
       }
-      if (lane == 0) {
-        sdec = cd;
-        if (rank == 0 && rflags) atomicOr(P.status, rflags);
+      // the next stage, read while the decision is made, or once it is known
+      const bool spec = lazy && hi < gb && gb >= kSpecMinGamma;
+      if (spec) run_stage(hi, true);
+      __syncthreads();  // the CTA's warps see the decision
+      cd = sdec[dseq & 1];
+      ++dseq;
+      if (cd.k >= 0) break;
+      if (!spec) {
+        run_stage(hi, false);
+        cluster_sync();  // every partial of the stage
       }
-    }
-    __syncthreads();  // the CTA's warps see its decision
-    const ClusterDec cd = sdec;
+      lo = hi;  // every draft of the stage accepted: its next stage is in
+    }  // stages
     const int next = s_next;
+    if (sample && cd.k == gb && rank == 0 && warp == 0)  // its copies are all consumed
+      final_bonus<EB, PK>(P, RowParts{bpart}, b, gb, tc, cd.mt, mybuf);
 
     if (cd.go) {
       // ---- the residual chunk sums of the rejected position k (k < gamma_b)
@@ -3310,11 +3487,18 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
         return m;
       };
       const uint32_t rsum0 = rank_addr(rsum, 0u);  // the leader's chunk sums
-      unsigned int jr = gw;                        // this warp's next chunk
+      const unsigned int nR = share((unsigned int)NCR);
+      bool more = true;
+      claim_next();
       while (!failed) {
-        while (issued - processed < (unsigned int)NB && jr < (unsigned int)NCR) {
-          issue(r_meta(jr));
-          jr += W;
+        while (more && issued - processed < (unsigned int)NB) {
+          const unsigned int t = claimed();
+          if (t >= nR) {
+            more = false;
+          } else {
+            issue(r_meta(rank + C * t));
+            claim_next();
+          }
         }
         if (issued == processed || !wait_oldest()) break;
         const Meta& m = mymeta[processed % NB];
@@ -3330,9 +3514,18 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
           if (lane == 0) st_cluster_u64(rsum0 + (uint32_t)mymeta[processed % NB].c * 8u, 0ull);
           __syncwarp();
         }
-        for (; jr < (unsigned int)NCR; jr += W)
-          if (lane == 0) st_cluster_u64(rsum0 + jr * 8u, 0ull);
+        while (more) {
+          const unsigned int t = claimed();
+          if (t >= nR) {
+            more = false;
+          } else {
+            if (lane == 0) st_cluster_u64(rsum0 + (rank + C * t) * 8u, 0ull);
+            __syncwarp();
+            claim_next();
+          }
+        }
       }
+      tbase += nR + NW;
       cluster_sync();  // the leader holds every chunk sum
 
       // ---- the final draw: the leader's warp 0 (its copies are all consumed)
@@ -4172,6 +4365,8 @@ int grid_size() {
 std::atomic<int> g_schedule{SV_SCHEDULE_AUTO};
 // Limit of every bounded wait in the calls that follow (spec_verify_set_wait_limit).
 std::atomic<unsigned long long> g_wait_ns{kWaitNs};
+// Lazy positions on the request-claims path (spec_verify_set_lazy).
+std::atomic<int> g_lazy{kLazyDefault};
 
 size_t cluster_tables(int G, int V, int eb) {
   const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
@@ -4184,7 +4379,8 @@ size_t cluster_tables(int G, int V, int eb) {
 size_t stream_tables(int G, int V, int eb) {
   const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
   const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
-  return (size_t)(2 * G + 1) * nc * sizeof(float2) + ncr * sizeof(unsigned long long);
+  // partials [2G+1][NC], chunk sums [NCR], the bonus row's partials [NC]
+  return (size_t)(2 * G + 2) * nc * sizeof(float2) + ncr * sizeof(unsigned long long);
 }
 
 // Clusters of C CTAs (C <= kClusterMax) of kernel `kern` that fit on this
@@ -4249,8 +4445,11 @@ struct StreamShape {
 // CTA pairs share an SM's rate whatever their requests.  Greedy claims run two
 // 6-warp CTAs per SM (B=512: 45 and 80 us against 48 and 83 with one CTA).
 size_t claim_bytes(int B) { return ((size_t)B * 5 + 15) & ~(size_t)15; }
+#ifndef SV_SAMPLE_CPS
+#define SV_SAMPLE_CPS 1
+#endif
 template <int MODE>
-constexpr int claim_cps() { return MODE == MODE_SAMPLE ? 1 : 2; }
+constexpr int claim_cps() { return MODE == MODE_SAMPLE ? SV_SAMPLE_CPS : 2; }
 
 template <int EB, int MODE, bool PK, int CPS>
 int max_stream_clusters(int C) {
@@ -4506,6 +4705,7 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.q_tok = q_tok;
   P.status = reinterpret_cast<unsigned int*>(w + L.status);
   P.wait_ns = g_wait_ns.load();
+  P.lazy = g_lazy.load();
   P.parts = 1;
   P.next_item = reinterpret_cast<unsigned int*>(w + L.next_item);
   P.exit_count = reinterpret_cast<unsigned int*>(w + L.exit_count);
@@ -4730,6 +4930,11 @@ int spec_verify_set_schedule(int schedule) {
 unsigned long long spec_verify_set_wait_limit(unsigned long long ns) {
   if (ns == 0ull) ns = kWaitNs;
   return g_wait_ns.exchange(ns);
+}
+
+int spec_verify_set_lazy(int on) {
+  if (on != 0 && on != 1) return SV_ERR_SCALAR;
+  return g_lazy.exchange(on);
 }
 
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {

@@ -83,6 +83,28 @@ class Workload:
             small += self.B * 4 * (self.G + 1)
         return rows * self.V * self.elem_bytes + small
 
+    def bytes_needed(self, mode: str, num_accepted, lazy: bool, ctas: int = 1) -> int:
+        """The logit rows a call must read given its outcomes, plus the small
+        inputs and outputs.  Read position by position (lazy), a sampled
+        request with k accepted drafts needs target and draft rows
+        0..min(k, gamma_b - 1) and, when k == gamma_b, the bonus row.  The
+        request-claims schedule reads a request eagerly (every row) when its
+        rows alone reach 80 % of a CTA's share of the batch (`ctas` CTAs),
+        and a greedy request (T == 0) always: gamma_b + 1 target rows.  Read
+        eagerly, every row: bytes_min()."""
+        if mode != "sample" or not lazy:
+            return self.bytes_min(mode)
+        k = torch.as_tensor(num_accepted).cpu().to(torch.int64)
+        g = self.gamma.cpu().to(torch.int64)
+        sampled = self.temperature.cpu() != 0
+        full = torch.where(sampled, 2 * g + 1, g + 1)
+        total = int(full.sum().item())
+        by_stage = 2 * torch.minimum(k + 1, g) + (k == g).to(torch.int64)
+        lazy_req = sampled & (5 * full * ctas < 4 * total)
+        rows = int(torch.where(lazy_req, by_stage, full).sum().item())
+        small = self.B * (4 * self.G + 4 + 8) + self.B * 4 * (self.G + 2) + self.B * 4 * (self.G + 1)
+        return rows * self.V * self.elem_bytes + small
+
     def to(self, device):
         return Workload(self.name, *(getattr(self, k).to(device) for k in
                                      ("target", "draft", "draft_tokens", "gamma",

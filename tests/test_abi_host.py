@@ -168,3 +168,18 @@ def test_wait_limit_setter_returns_previous_and_zero_restores_default():
         assert binding.spec_verify_set_wait_limit(0) == 2_000_000_000
     finally:
         binding.spec_verify_set_wait_limit(prev)
+
+
+def test_lazy_setter_returns_previous_and_rejects_other_values():
+    """Position-by-position reading is on by default; the setter is host state."""
+    prev = binding.spec_verify_set_lazy(True)
+    try:
+        assert prev is True
+        assert binding.spec_verify_set_lazy(False) is True
+        assert binding.spec_verify_set_lazy(True) is False
+        lib = binding.load_library()
+        for bad in (-1, 2, 7):
+            assert lib.spec_verify_set_lazy(bad) == -1  # SV_ERR_SCALAR
+        assert binding.spec_verify_set_lazy(True) is True
+    finally:
+        binding.spec_verify_set_lazy(prev)

@@ -323,3 +323,45 @@ def test_claimed_requests_match_other_schedules_and_oracle(B, G, V, dt):
             binding.spec_verify_set_schedule(prev)
     for o in outs:
         assert (o[0] == res[0][0]).all() and (o[1] == res[0][1]).all()
+
+
+def _claims_call(w, lazy):
+    """One request-claims call with p/q, read lazily or eagerly."""
+    prev_l = binding.spec_verify_set_lazy(lazy)
+    prev_s = binding.spec_verify_set_schedule(binding.SCHEDULE_STREAM)
+    try:
+        v = binding.Verifier(w.B, w.G, w.V, DEV)
+        p = torch.full((w.B, w.G), float("nan"), dtype=torch.float64, device=DEV)
+        q = torch.full_like(p, float("nan"))
+        v.sample(w.target, w.draft, w.draft_tokens, w.gamma, w.uniforms, w.temperature, p, q)
+        torch.cuda.synchronize()
+        st = binding.spec_verify_status(v.workspace)
+        assert st == 0, binding.status_names(st)
+        return (v.out_tokens.cpu().numpy(), v.num_accepted.cpu().numpy(), p.cpu(), q.cpu())
+    finally:
+        binding.spec_verify_set_schedule(prev_s)
+        binding.spec_verify_set_lazy(prev_l)
+
+
+@pytest.mark.parametrize("B,G,V,dt,sigma_d", [(300, 7, 20001, "bf16", 0.3), (300, 7, 20001, "bf16", 2.0),
+                                              (400, 1, 32000, "f32", 1.0), (500, 3, 4097, "bf16", 0.5),
+                                              (600, 0, 33, "bf16", 1.0)])
+def test_lazy_and_eager_reads_agree(B, G, V, dt, sigma_d):
+    """Request claims read a sampled request position by position (lazily) by
+    default: a position's rows are reduced and its draft tested before the
+    next position is read, and the next one is read while the test runs.
+    Reading every row first (eagerly) must give the same outputs bit for bit,
+    p/q included (NaN past the first rejection on both); both against the
+    oracle.  High and low acceptance (draft noise 0.3 and 2.0) exercise many
+    and few lazy stages; temperature 0 requests take the greedy steps."""
+    temps = [0.0 if i % 11 == 5 else 0.6 + 0.003 * i for i in range(B)]
+    w = W.make_random(B, G, V, dt, seed=77 * B + G, gamma="ragged", temperature=temps,
+                      sigma_d=sigma_d).to(DEV)
+    assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_CLAIMS, 1)
+    lazy = _claims_call(w, True)
+    eager = _claims_call(w, False)
+    same(lazy, eager)
+    against_oracle(w, lazy)
+    if G > 0:  # rejections and full acceptances both occur: both lazy exits run
+        n, g = lazy[1], w.gamma.cpu().numpy()
+        assert (n < g).any() and (n == g).any()

@@ -51,16 +51,31 @@ def _same(a, b):
         assert torch.allclose(x[~nan], y[~nan], rtol=PROB_RTOL, atol=0.0)
 
 
-@pytest.mark.parametrize("case", ["config2", "ragged_f32"])
-def test_noalloc_matches_workspace_entry_point_twice(case):
+def _case(case):
     if case == "config2":
-        w = W.make("2", device="cuda")
-    else:
-        w = W.make_random(B=37, G=5, V=20001, dtype="f32", device="cuda", seed=4242,
-                          gamma="ragged", temperature=0.9)
-    ref = _with_workspace(w)
-    first = _noalloc(w)
-    second = _noalloc(w)
+        return W.make("2", device="cuda")
+    if case == "ragged_f32":
+        return W.make_random(B=37, G=5, V=20001, dtype="f32", device="cuda", seed=4242,
+                             gamma="ragged", temperature=0.9)
+    # the largest shape the header names as fitting the built-in scratch:
+    # more requests than resident CTAs, so the streaming schedule claims them
+    return W.make_random(B=512, G=3, V=128256, dtype="bf16", device="cuda", seed=4243,
+                         gamma="ragged", temperature=0.8)
+
+
+@pytest.mark.parametrize("schedule", ["auto", "persistent"])
+@pytest.mark.parametrize("case", ["config2", "ragged_f32", "claims_512x3x128256"])
+def test_noalloc_matches_workspace_entry_point_twice(case, schedule):
+    w = _case(case)
+    assert binding.spec_verify_workspace_size(w.B, w.G, w.V) <= binding.SV_NOALLOC_SCRATCH_BYTES
+    policy = binding.SCHEDULE_AUTO if schedule == "auto" else binding.SCHEDULE_PERSISTENT
+    prev = binding.spec_verify_set_schedule(policy)
+    try:
+        ref = _with_workspace(w)
+        first = _noalloc(w)
+        second = _noalloc(w)
+    finally:
+        binding.spec_verify_set_schedule(prev)
     _same(ref, first)
     _same(ref, second)
 
