@@ -321,7 +321,10 @@ def run_ours(args):
                                       "persistent": binding.SCHEDULE_PERSISTENT}[args.schedule])
     binding.spec_verify_set_lazy(args.read == "lazy")
     route, csize = binding.spec_verify_route(base.target.dtype, B, G, V, greedy=mode == "greedy")
-    lazy = mode == "sample" and route == binding.ROUTE_CLAIMS and args.read == "lazy"
+    # request claims read lazily from two requests per CTA (one CTA per SM)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    lazy = (mode == "sample" and route == binding.ROUTE_CLAIMS and args.read == "lazy"
+            and B >= 2 * sms)
     kernel = {binding.ROUTE_CLUSTER: "cluster_kernel", binding.ROUTE_STREAM: "stream_kernel",
               binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
     schedule = {binding.ROUTE_CLUSTER: f"resident clusters of {csize} CTAs, one per request",
@@ -440,8 +443,7 @@ def run_ours(args):
     # Read lazily, a call needs only the rows up to each request's first
     # rejection (and the bonus row after full acceptance): those bytes are the
     # algorithm's; one read of every logit is reported beside them.
-    bytes_need = base.bytes_needed(mode, v.num_accepted, lazy,
-                                   ctas=props.multi_processor_count)  # one CTA per SM
+    bytes_need = base.bytes_needed(mode, v.num_accepted, lazy, ctas=sms)
     achieved = bytes_need / (ms / K * 1e-3) / 1e9
     every_logit = bytes_min / (ms / K * 1e-3) / 1e9
     peak, peak_src = measured_peak_hbm()

@@ -317,9 +317,12 @@ unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
  * i + 1 matter, and the bonus row gamma_b only after every draft was
  * accepted, as in the verification loop of disassemble-channel
  * "Speculative Decoding theory", Step 3, which stops at the first rejected
- * draft.  While one position is tested, the CTA already
- * streams the next one; what it read of a position after the first
- * rejection is not used.  0: every row of the request is reduced before any
+ * draft.  For a request with at least four drafts, the CTA streams the next
+ * position while one is tested; what it read of a position after the first
+ * rejection is not used.  Lazy stages lengthen a request while they shorten
+ * the batch, so they apply only where the batch holds at least two requests
+ * per CTA, and not to a request whose rows alone reach 80 % of a CTA's share
+ * of the batch's rows.  0: every row of every request is reduced before any
  * test.  The outputs are identical either way: a position's arithmetic does
  * not depend on the order.  The other schedules always read every row.
  * Returns the previous setting, or SV_ERR_SCALAR for a value other than 0

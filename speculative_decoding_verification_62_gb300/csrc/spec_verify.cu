@@ -155,11 +155,9 @@ struct __align__(16) DecRecord {
   uint32_t tag_b; float inv_st, rho; uint32_t pad;
 };
 
-constexpr int kJobsPerRequest = 8;  // residual jobs of one request, at most (flow kernel)
-
 struct Layout {
   size_t status, next_item, exit_count, r_next, q_tail, dec_count;  // header words
-  size_t cnt_a, cnt_r, dec, queue, stats, resid, jobs, total;
+  size_t cnt_a, cnt_r, dec, queue, stats, resid, total;
   int NC, NCR;  // worst-case chunk counts (float32 logits)
 };
 
@@ -183,7 +181,6 @@ __host__ __device__ inline Layout make_layout(int B, int G, int V) {
   L.queue = off; off = align256(off + (size_t)B * sizeof(DecRecord));
   L.stats = off; off = align256(off + (size_t)B * (2 * G + 1) * L.NC * sizeof(float2));
   L.resid = off; off = align256(off + (size_t)B * L.NCR * sizeof(unsigned long long));
-  L.jobs = off;  off = align256(off + (size_t)B * kJobsPerRequest * sizeof(DecRecord));
   L.total = off;
   return L;
 }
@@ -198,7 +195,6 @@ struct Params {
   const int32_t* cu;          // packed layout: [B+1] draft prefix (nullptr: padded layout)
   int total;                  // packed layout: drafts in all requests (rows of draft_logits)
   int b_base;                 // packed layout: global index of this launch's first request
-  int parts;                  // request-flow kernel: claims per request (parts of its items)
   const float* uniforms;
   const float* temperature;
   int32_t* out_tokens;
@@ -220,8 +216,6 @@ struct Params {
   DecRecord* queue;          // [B] decisions in the order they were made
   float2* stats;              // [B][2G+1][stride_nc]: (max, sum) or (max, argmax bits)
   unsigned long long* resid;  // [B][stride_ncr]: fixed-point sum of the draw weights
-  DecRecord* jobs;            // flow kernel: residual jobs posted by deciding CTAs
-  int rjobs;                  // flow kernel: residual jobs per rejecting request
 };
 
 // A decoded work item (one per lane of a claimed batch; stored per buffer).
@@ -3012,12 +3006,12 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_kernel(Params P) {
 // the last down to 0, target row then draft row: the rows most often
 // rejected (position 0) come last, closest to the residual pass that may
 // re-read them.
-struct FlowRow {
+struct StreamRow {
   int pslot, c, row;  // partial slot, chunk, row index within the target or draft rows
   bool draft;
 };
-__device__ __forceinline__ FlowRow flow_row(int j, int NC, int gb, bool greedy, int G) {
-  FlowRow r;
+__device__ __forceinline__ StreamRow stream_row(int j, int NC, int gb, bool greedy, int G) {
+  StreamRow r;
   const int rr = j / NC;
   r.c = j - rr * NC;
   if (greedy || rr == 0) {
@@ -3085,7 +3079,6 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
   unsigned char* mybuf = dsmem + (size_t)warp * NB * kItemBytes;
   uint64_t* mybar = bar[warp];
   Meta* mymeta = smeta[warp];
-  const unsigned int gw = rank * NW + (unsigned int)warp, W = C * NW;
 
   if (queue && C != 1) {  // claims are made for clusters of one CTA only
     if (tid == 0 && rank == 0) atomicOr(P.status, SV_STATUS_INTERNAL);
@@ -3262,10 +3255,13 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     // taking its items, and what they read of it is not used.  Otherwise one
     // stage holds every row.  Each position's arithmetic is the same either
     // way.
-    // A request whose rows alone reach 80 % of a CTA's average share of the
-    // batch is read eagerly: the call lasts at least as long as it does, and
-    // lazy stages would lengthen it.
-    const bool lazy = P.lazy && queue && sample &&
+    // Lazy stages lengthen a request while they shorten the batch's work, so
+    // they are used where requests queue at least two deep per CTA, and not
+    // for a request whose rows alone reach 80 % of a CTA's average share of
+    // the batch (the call lasts at least as long as it does).  Measured:
+    // B = 512, gamma 1 and 3: 113 -> 111 and 202 -> 174 us; B = 256 ragged
+    // (1.7 requests per CTA): 131 eager against 135 lazy.
+    const bool lazy = P.lazy && queue && sample && P.B >= 2 * nq &&
                       5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
                           4ull * (unsigned long long)s_rows;
     auto stage_hi = [&](int slo) { return lazy ? min(slo + 1, gb) : gb; };
@@ -3283,7 +3279,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
         // the rows in streaming order: eagerly, a sampled request's position-0
         // rows, the most often rejected, come last, closest to the residual
         // pass; lazily, target row slo then draft row slo (or the bonus row)
-        FlowRow fr;
+        StreamRow fr;
         if (lazy) {
           const int rr = (int)j / NC;
           fr.c = (int)j - rr * NC;
@@ -3291,7 +3287,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
           fr.row = npos ? slo : gb;
           fr.pslot = fr.draft ? G + 1 + slo : fr.row;
         } else {
-          fr = flow_row((int)j, NC, gb, !sample, G);
+          fr = stream_row((int)j, NC, gb, !sample, G);
         }
         const int c = fr.c;
         Meta m;
@@ -3566,760 +3562,6 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
 }
 
 // ---------------------------------------------------------------------------
-// Large batches: requests flowing through one CTA per SM
-// ---------------------------------------------------------------------------
-// Beyond one wave of clusters, each CTA (one per SM, NW warps with one 8 KB
-// staging buffer each) works through a sequence of claimed entries with no
-// barrier between them.  An entry is either a part of a request (a range of
-// its A items: requests are claimed in `parts` parts, longest request first,
-// so that every CTA takes several claims and the last round is short) or a
-// residual job (a range of the R chunks of a decided request).  The warps
-// take items one at a time from the CTA's sequence (one shared-memory atomic
-// add; an index past the published entries is held until the next entry is
-// published), move an A item into registers (sampling) or reduce the item,
-// and copy their next item meanwhile.
-//  - The warp whose partial completes a part writes the part's partials to
-//    the workspace; the part that completes the request (a workspace arrival
-//    counter) loads the others' partials and decides.  A rejection allocates
-//    the request's residual jobs in the workspace's job list; an accepted
-//    draft list draws the bonus token from the A statistics; greedy steps are
-//    done at once.
-//  - The warp whose chunk sum completes a job writes its chunk sums to the
-//    workspace; the job that completes the request's residual draws the
-//    token from the chunk sums.
-//  - One entry at a time is published ahead of use (when the newest one has
-//    started and an entry slot is free): a residual job if one is waiting,
-//    else the next claim position.  Jobs thus move to whichever CTA is free,
-//    and a CTA that decides does not inherit the residual work.
-//  - A CTA with no claim left stays until every request of the batch is
-//    decided and no job is left, taking jobs as they appear.
-// Every wait is bounded; the last CTA out resets the workspace counters.
-
-__device__ __forceinline__ unsigned int ld_acquire_cta(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_cta(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned int ld_volatile_cta(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
-enum { KIND_NONE = 2 };  // no item (flow kernel)
-constexpr unsigned int kNoReq = 0xffffffffu;
-constexpr int kFlowMaxJobs = kJobsPerRequest;
-constexpr unsigned long long kJobPollNs = 2000;  // a CTA with claims left looks for jobs this often
-
-struct FlowReq {              // one entry in flight (shared memory)
-  unsigned int seq;           // entry number held (kNoReq: none yet)
-  unsigned int fin;           // the last entry number finished in this slot
-  int job;                    // 0: a part of a request's A items; 1: a residual job
-  int b, gb, nI, greedy;      // request, draft length, items of this entry, greedy steps
-  int start;                  // its first item in the CTA's sequence
-  int lo, nreq;               // part: its first item among the request's, and their number;
-                              // job: its first R chunk
-  int a_done;                 // items reduced (shared atomic)
-  size_t t0, d0, uf;          // first target row, first draft row, final uniform
-  TempC tc;
-  int k;                      // job: the rejected position
-  float mt, md, inv_st, rho;  // job: the decision's draw constants
-  unsigned int flags;         // input flags found when the request started
-};
-
-template <int NW, int NSLOT>
-struct FlowShared {
-  uint64_t bar[NW];           // per warp: its buffer's copy landed
-  Meta meta[NW];              // what each warp's buffer holds
-  FlowReq req[NSLOT];         // entry n lives in slot n % NSLOT
-  unsigned int a_next;        // next item of the CTA's sequence
-  unsigned int a_pub;         // end of the items published so far
-  unsigned int n_pub;         // entries published
-  unsigned int n_done;        // entries finished
-  unsigned int claims_done;   // 1: no claim position left
-  int pub_lock;               // held while an entry is published (never waited for)
-  int claim_next;             // the next claim position (-1 while it is being fetched)
-  unsigned int newest_start;  // first item of the newest published entry
-  unsigned int closed;        // 1: nothing will be published any more (the CTA is done)
-  unsigned long long job_poll; // when the workspace's job list was last looked at
-};
-
-// Launch-wide constants of the request-flow kernel.
-struct FlowConst {
-  const int* order;           // claim order (when sorted)
-  const unsigned char* nrow;  // rows per request, bit 7: greedy steps
-  int sorted, nq;
-};
-
-// Per-request tables built at the start of a claims launch (every CTA builds
-// the same): nrow[b] = rows the request streams (2 gamma_b + 1 when sampled,
-// gamma_b + 1 for greedy steps) with bit 7 set for greedy steps; order[] =
-// claim order, longest first (stable counting sort, skipped when every
-// request has the same row count).  Returns true when `order` is used.
-template <int MODE, bool PK>
-__device__ bool claim_tables(const Params& P, unsigned char* nrow, int* order, int* s_hist,
-                             int nthreads) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  auto rows_of_req = [&](int b) -> int {
-    int gb = 0;
-    unsigned int fl = 0;
-    if constexpr (PK) (void)packed_base(P, b, gb, fl);
-    else gb = clamp_gamma(P.gamma ? P.gamma[b] : 0, P.G);
-    const bool sampled = MODE == MODE_SAMPLE && P.temperature[b] != 0.0f;
-    return sampled ? 2 * gb + 1 : (gb + 1) | 0x80;
-  };
-  const int r0 = rows_of_req(0) & 0x7f;
-  int differs = 0;
-  for (int b = tid; b < P.B; b += nthreads) {
-    const int r = rows_of_req(b);
-    nrow[b] = (unsigned char)r;
-    differs |= (r & 0x7f) != r0;
-  }
-  const bool sorted = __syncthreads_or(differs) != 0;
-  if (sorted) {
-    if (warp == 0) {
-      for (int r = lane; r < 64; r += 32) s_hist[r] = 0;
-      __syncwarp();
-      for (int b0 = 0; b0 < P.B; b0 += 32) {
-        const int b = b0 + lane;
-        const int r = b < P.B ? (int)(nrow[b] & 0x7f) : 64;  // 64: past the batch
-        const unsigned int peers = __match_any_sync(0xffffffffu, r);
-        if (r < 64 && lane == __ffs(peers) - 1) s_hist[r] += __popc(peers);
-        __syncwarp();
-      }
-      const int h0 = s_hist[2 * lane], h1 = s_hist[2 * lane + 1];
-      int suf = h0 + h1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_down_sync(0xffffffffu, suf, o);
-        if (lane + o < 32) suf += t;
-      }
-      const int after = suf - h0 - h1;  // requests with more rows than 2 lane + 1
-      __syncwarp();
-      s_hist[2 * lane + 1] = after;
-      s_hist[2 * lane] = after + h1;
-      __syncwarp();
-      for (int b0 = 0; b0 < P.B; b0 += 32) {
-        const int b = b0 + lane;
-        const int r = b < P.B ? (int)(nrow[b] & 0x7f) : 64;
-        const unsigned int peers = __match_any_sync(0xffffffffu, r);
-        const int before = __popc(peers & ((1u << lane) - 1u));
-        if (r < 64) order[s_hist[r] + before] = b;
-        __syncwarp();
-        if (r < 64 && before == 0) s_hist[r] += __popc(peers);
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-  }
-  return sorted;
-}
-
-// A warp's copy of the entry its items last came from (shared memory, private
-// to the warp): the common item needs no shared counter but one.
-struct FlowCache {
-  unsigned int n;             // entry number (kNoReq: none)
-  int slot, start, end, lo, gb, greedy, job, k;
-  size_t t0, d0;
-  TempC tc;
-  float mt, md, inv_st, rho;
-};
-
-__device__ __forceinline__ unsigned int ld_relaxed_gpu(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// The residual jobs of a decided request (lane 0): nj records in the
-// workspace's job list, each naming the request, the rejected position, the
-// job's index and the draw constants.  A claimer that finds a record not yet
-// complete waits for it (bounded).
-__device__ __forceinline__ void flow_post_jobs(const Params& P, int b, const Decision& d, int nj) {
-  const unsigned int j0 = atomicAdd(P.q_tail, (unsigned int)nj);
-  for (int i = 0; i < nj; ++i) {
-    Decision di = d;
-    di.reject = 1;
-    DecRecord* r = &P.jobs[j0 + (unsigned int)i];
-    const uint32_t tag = kDecTag | ((uint32_t)i << 8) | (uint32_t)d.k;
-    atom_store_b128(&r->tag_b, make_uint4(tag, __float_as_uint(di.inv_st), __float_as_uint(di.rho), 0u));
-    atom_store_b128(&r->tag_a, make_uint4(tag, (uint32_t)b, __float_as_uint(di.mt), __float_as_uint(di.md)));
-  }
-}
-
-// A residual job's record (both halves, one round trip): false while it is
-// not yet complete.
-__device__ __forceinline__ bool read_job(const DecRecord* r, int& b, int& k, int& rj, float& mt,
-                                         float& md, float& inv_st, float& rho) {
-  const uint4 a = atom_load_b128(&r->tag_a);
-  const uint4 h = atom_load_b128(&r->tag_b);
-  if (!(a.x & kDecTag) || a.x != h.x) return false;
-  k = (int)(a.x & 0xffu);
-  rj = (int)((a.x >> 8) & 0xffu);
-  b = (int)a.y;
-  mt = __uint_as_float(a.z);
-  md = __uint_as_float(a.w);
-  inv_st = __uint_as_float(h.y);
-  rho = __uint_as_float(h.z);
-  return true;
-}
-
-// The request's fields of an entry (lane 0, publish lock held).
-template <int MODE, bool PK>
-__device__ __forceinline__ void flow_fill_request(const Params& P, const FlowConst& fc,
-                                                  FlowReq& e, int b, unsigned int& fl,
-                                                  int& rows) {
-  const int nr = fc.nrow[b];
-  const bool greedy = (nr & 0x80) != 0;
-  rows = nr & 0x7f;
-  const int gb = greedy ? rows - 1 : (rows - 1) / 2;
-  int base = 0;
-  if constexpr (PK) {
-    int g2 = 0;
-    base = packed_base(P, b, g2, fl);
-  } else {
-    const int g_in = P.gamma ? P.gamma[b] : 0;
-    if (g_in != gb) fl |= SV_STATUS_BAD_GAMMA;
-  }
-  const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
-  e.b = b;
-  e.gb = gb;
-  e.greedy = greedy ? 1 : 0;
-  e.t0 = A.t0;
-  e.d0 = A.d0;
-  e.uf = A.uf;
-  e.tc = TempC{0.0f, 0.0f};
-  if (MODE == MODE_SAMPLE && !greedy) e.tc = temp_consts(sanitize_temperature(P.temperature[b], fl));
-}
-
-// Publish the CTA's next entry if the newest one has started and its slot is
-// free (lane 0; never waits for another warp: the publish lock taken, a busy
-// slot or a claim position still being fetched all mean "not now").  A
-// waiting residual job comes first (claimed from the workspace's job list by
-// compare-and-swap); else the part at the next claim position, whose
-// successor position is then fetched.  One entry is published ahead of use,
-// so the sequence does not run dry at an entry boundary while claims and
-// jobs are not hoarded.
-template <int MODE, bool PK, int NW, int NSLOT>
-__device__ __noinline__ void flow_try_publish(const Params& P, const FlowConst& fc,
-                                              FlowShared<NW, NSLOT>& fs, unsigned int* flags) {
-  const unsigned int n0 = ld_volatile_cta(&fs.n_pub);
-  if (n0 > 0 && ld_volatile_cta(&fs.a_next) <= ld_volatile_cta(&fs.newest_start)) return;
-  if (n0 >= (unsigned int)NSLOT && ld_volatile_cta(&fs.req[n0 % NSLOT].fin) != n0 - NSLOT) return;
-  // something to publish: the next claim position is at hand, or the job
-  // list is due for a look (every kJobPollNs, at every call once no claim is
-  // left); the job list lives in global memory, so it is not read on every call
-  const bool claim_ready = !ld_volatile_cta(&fs.claims_done) &&
-                           (int)ld_volatile_cta(reinterpret_cast<const unsigned int*>(&fs.claim_next)) >= 0;
-  bool poll = false;
-  if (MODE == MODE_SAMPLE) {
-    const unsigned long long now = now_ns();
-    poll = ld_volatile_cta(&fs.claims_done) ||
-           now - *reinterpret_cast<volatile unsigned long long*>(&fs.job_poll) > kJobPollNs;
-  }
-  if (!claim_ready && !poll) return;
-  if (atomicCAS(&fs.pub_lock, 0, 1) != 0) return;
-  __threadfence_block();
-  const unsigned int n = fs.n_pub;
-  FlowReq& e = fs.req[n % NSLOT];
-  bool published = false, fetch = false;
-  if (!fs.closed && (n < (unsigned int)NSLOT || ld_volatile_cta(&e.fin) == n - NSLOT)) {
-    // 1. a waiting residual job
-    unsigned int jt = 0xffffffffu;
-    if (poll) {
-      fs.job_poll = now_ns();
-      jt = ld_relaxed_gpu(P.r_next);
-      if (jt >= ld_relaxed_gpu(P.q_tail) || atomicCAS(P.r_next, jt, jt + 1) != jt) jt = 0xffffffffu;
-    }
-    if (jt != 0xffffffffu) {
-      DecRecord* r = &P.jobs[jt];
-      int b = 0, k = 0, rj = 0;
-      float mt = 0.0f, md = 0.0f, inv_st = 0.0f, rho = 0.0f;
-      bool got = read_job(r, b, k, rj, mt, md, inv_st, rho);
-      if (!got) {
-        const unsigned long long t0 = now_ns();
-        while (!(got = read_job(r, b, k, rj, mt, md, inv_st, rho)) && now_ns() - t0 < P.wait_ns)
-          __nanosleep(32);
-      }
-      if (got && b >= 0 && b < P.B && k >= 0 && k <= P.G && rj < P.rjobs) {
-        // each record is read once: cleared for the next call
-        atom_store_b128(&r->tag_a, make_uint4(0u, 0u, 0u, 0u));
-        atom_store_b128(&r->tag_b, make_uint4(0u, 0u, 0u, 0u));
-        unsigned int fl = 0;
-        int rows = 0;
-        flow_fill_request<MODE, PK>(P, fc, e, b, fl, rows);
-        e.job = 1;
-        e.k = k;
-        e.mt = mt;
-        e.md = md;
-        e.inv_st = inv_st;
-        e.rho = rho;
-        e.lo = (int)((long long)rj * P.NCR / P.rjobs);
-        e.nI = (int)((long long)(rj + 1) * P.NCR / P.rjobs) - e.lo;
-        e.nreq = P.NCR;
-        e.flags = 0;
-        published = true;
-      } else {
-        *flags |= got ? SV_STATUS_INTERNAL : SV_STATUS_TIMEOUT;
-#ifdef SV_FLOW_DEBUG
-        if (!got) *flags |= 256u;
-#endif
-      }
-    }
-    // 2. the part at the next claim position
-    const int qp = fs.claim_next;
-    if (!published && !fs.claims_done && qp >= 0) {
-      const int q = qp / P.parts, part = qp - q * P.parts;
-      if (q >= P.B) {
-        fs.claims_done = 1;
-      } else {
-        const int b = fc.sorted ? fc.order[q] : q;
-        unsigned int fl = 0;
-        int rows = 0;
-        flow_fill_request<MODE, PK>(P, fc, e, b, fl, rows);
-        const int nreq = rows * P.NC;
-        e.job = 0;
-        e.lo = (int)((long long)part * nreq / P.parts);
-        e.nI = (int)((long long)(part + 1) * nreq / P.parts) - e.lo;
-        e.nreq = nreq;
-        e.k = 0;
-        e.flags = part == 0 ? fl : 0u;  // reported once per request
-        fs.claim_next = -1;
-        fetch = true;
-        published = true;
-      }
-    }
-    if (published) {
-      __threadfence_block();
-      fs.newest_start = fs.a_pub;
-      e.start = (int)fs.a_pub;
-      e.a_done = 0;
-      st_release_cta(&e.seq, n);
-      st_release_cta(&fs.n_pub, n + 1);
-      st_release_cta(&fs.a_pub, (unsigned int)(e.start + e.nI));
-    }
-  }
-  __threadfence_block();
-  atomicExch(&fs.pub_lock, 0);
-  if (fetch) atomicExch(&fs.claim_next, (int)atomicAdd(P.next_item, 1u) + fc.nq);
-}
-
-// Take this warp's next item and start its copy (lane 0): the item at *held,
-// an index of the CTA's sequence taken with one atomic add and kept while it
-// lies past the published entries.  Returns its kind (KIND_NONE: nothing
-// available now).
-template <int EB, int NW, int NSLOT>
-__device__ __forceinline__ int flow_take(const Params& P, FlowShared<NW, NSLOT>& fs, FlowCache& wc,
-                                         int warp, unsigned char* buf, unsigned int* held) {
-  constexpr int AE = kItemBytes / EB, RE = kHalfBytes / EB;
-  const int V = P.V, NC = P.NC;
-  Meta& m = fs.meta[warp];
-  if (*held == kNoReq) *held = atomicAdd(&fs.a_next, 1u);
-  const unsigned int a = *held;
-  bool have = a >= (unsigned int)wc.start && a < (unsigned int)wc.end;
-  if (!have) {
-    if (a >= ld_volatile_cta(&fs.a_pub)) {
-      m.kind = KIND_NONE;
-      return KIND_NONE;
-    }
-    // a later entry: the newest published one whose start <= a
-    __threadfence_block();
-    unsigned int n = fs.n_pub - 1;
-    while ((unsigned int)fs.req[n % NSLOT].start > a) --n;
-    const FlowReq& e = fs.req[n % NSLOT];
-    wc.n = n;
-    wc.slot = (int)(n % NSLOT);
-    wc.start = e.start;
-    wc.end = e.start + e.nI;
-    wc.lo = e.lo;
-    wc.gb = e.gb;
-    wc.greedy = e.greedy;
-    wc.job = e.job;
-    wc.k = e.k;
-    wc.t0 = e.t0;
-    wc.d0 = e.d0;
-    wc.tc = e.tc;
-    wc.mt = e.mt;
-    wc.md = e.md;
-    wc.inv_st = e.inv_st;
-    wc.rho = e.rho;
-  }
-  *held = kNoReq;
-  const int ji = (int)(a - (unsigned int)wc.start);
-  int kind;
-  m.b = wc.slot;
-  m.c_hi = wc.tc.hi;
-  m.c_lo = wc.tc.lo;
-  if (wc.job) {
-    // an R item: chunk lo + ji of target and draft row k
-    const int c = wc.lo + ji, k = wc.k;
-    kind = KIND_R;
-    m.pslot = k;
-    m.c = c;
-    m.n = min(RE, V - c * RE);
-    m.reject = 1;
-    m.p0 = P.target + ((wc.t0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
-    m.p1 = P.draft + ((wc.d0 + (size_t)k) * (size_t)V + (size_t)c * RE) * EB;
-    const uintptr_t ad = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
-    m.direct = ((ad & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-    m.mt = wc.mt;
-    m.md = wc.md;
-    m.inv_st = wc.inv_st;
-    m.rho = wc.rho;
-  } else {
-    const FlowRow fr = flow_row(wc.lo + ji, NC, wc.gb, wc.greedy != 0, P.G);
-    const int c = fr.c;
-    const size_t roff = ((fr.draft ? wc.d0 : wc.t0) + (size_t)fr.row) * (size_t)V;
-    const char* rows = fr.draft ? P.draft : P.target;
-    kind = KIND_A;
-    m.pslot = fr.pslot;
-    m.c = c;
-    m.n = min(AE, V - c * AE);
-    m.p0 = rows + (roff + (size_t)c * AE) * EB;
-    m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
-    m.reject = wc.greedy;  // A items: 1 for greedy steps
-  }
-  m.kind = kind;
-  uint64_t* bar = &fs.bar[warp];
-  if (m.direct) {
-    mbar_arrive(bar);  // read with plain loads by the consumer
-  } else if (kind == KIND_A) {
-    const unsigned int bytes = (unsigned int)(m.n * EB);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_copy_g2s(buf, m.p0, bytes, bar);
-  } else {
-    const unsigned int bytes = (unsigned int)(m.n * EB);
-    mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_copy_g2s(buf, m.p0, bytes, bar);
-    bulk_copy_g2s(buf + kHalfBytes, m.p1, bytes, bar);
-  }
-  return kind;
-}
-
-template <int EB, int MODE, bool PK, int NW, int NSLOT>
-__global__ void __launch_bounds__(NW * 32, 1) flow_kernel(Params P) {
-  extern __shared__ __align__(128) unsigned char dsmem[];
-  __shared__ FlowShared<NW, NSLOT> fs;
-  __shared__ FlowCache wcache[NW];
-  __shared__ int s_hist[64];
-  __shared__ int s_last;
-  constexpr int AE = kItemBytes / EB;    // logits per A item
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = P.B, G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
-  // dynamic shared memory: NW buffers | per slot (partials, row statistics,
-  // staging) | claim order [B] | row counts [B]
-  const size_t part_bytes = ((size_t)(2 * G + 1) * NC * sizeof(float2) + 15) & ~(size_t)15;
-  const size_t slot_bytes = part_bytes + 1024 + kItemBytes;
-  unsigned char* mybuf = dsmem + (size_t)warp * kItemBytes;
-  unsigned char* slot_base = dsmem + (size_t)NW * kItemBytes;
-  int* order = reinterpret_cast<int*>(slot_base + (size_t)NSLOT * slot_bytes);
-  unsigned char* nrow = reinterpret_cast<unsigned char*>(order + B);
-  auto part_of = [&](int s) { return reinterpret_cast<float2*>(slot_base + (size_t)s * slot_bytes); };
-  auto rs_of = [&](int s) {  // 192 floats: the decision's row statistics
-    return reinterpret_cast<float*>(slot_base + (size_t)s * slot_bytes + part_bytes);
-  };
-  auto stage_of = [&](int s) {  // 8 KB: the bonus draw's and the final draw's staging
-    return slot_base + (size_t)s * slot_bytes + part_bytes + 1024;
-  };
-
-  if (tid == 0) {
-    for (int w = 0; w < NW; ++w) mbar_init(&fs.bar[w], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (int s = 0; s < NSLOT; ++s) {
-      fs.req[s].seq = kNoReq;
-      fs.req[s].fin = kNoReq;
-      fs.req[s].start = 0x7fffffff;
-    }
-    fs.a_next = fs.a_pub = fs.n_pub = fs.n_done = 0;
-    fs.claims_done = 0;
-    fs.pub_lock = 0;
-    fs.claim_next = (int)blockIdx.x;
-    fs.newest_start = 0;
-    fs.closed = 0;
-    fs.job_poll = 0;
-  }
-  FlowConst fc;
-  fc.order = order;
-  fc.nrow = nrow;
-  fc.nq = (int)gridDim.x;
-  fc.sorted = claim_tables<MODE, PK>(P, nrow, order, s_hist, NW * 32) ? 1 : 0;
-  unsigned int flags = 0;
-  bool failed = false;
-  if (tid == 0) flow_try_publish<MODE, PK>(P, fc, fs, &flags);  // the first entry
-  __syncthreads();
-
-  unsigned int processed = 0;  // items consumed by this warp (buffer parity)
-  unsigned int held = kNoReq;  // lane 0: an index taken but not yet published
-  FlowCache& wc = wcache[warp];
-  if (lane == 0) {
-    wc.n = kNoReq;
-    wc.start = 0;
-    wc.end = 0;
-  }
-  __syncwarp();
-  // take and copy this warp's next item (warp-wide); its kind
-  auto take = [&]() -> int {
-    int kind = KIND_NONE;
-    if (lane == 0) kind = flow_take<EB>(P, fs, wc, warp, mybuf, &held);
-    __syncwarp();
-    return __shfl_sync(0xffffffffu, kind, 0);
-  };
-  auto publish_next = [&]() {
-    if (lane == 0) flow_try_publish<MODE, PK>(P, fc, fs, &flags);
-    __syncwarp();
-  };
-  // an entry is finished: its slot is free again
-  auto finish = [&](int s) {
-    if (lane == 0) {
-      FlowReq& e = fs.req[s];
-      if (e.flags) atomicOr(P.status, e.flags);
-      st_release_cta(&e.fin, e.seq);
-      atomicAdd(&fs.n_done, 1u);
-    }
-  };
-  // a request is decided (after its jobs, if any, are posted)
-  auto count_decision = [&]() {
-    if (lane == 0) {
-      __threadfence();
-      atomicAdd(P.dec_count, 1u);
-    }
-  };
-
-  int kind = take();
-  unsigned long long idle_since = 0;
-  while (!failed) {
-    if (kind == KIND_NONE) {
-      // nothing to take now: the CTA is done, or an entry is still to come
-      unsigned int state = 0;  // 0 wait, 1 done, 2 stuck
-      if (lane == 0) {
-        // done once every request is decided, every job taken and every
-        // entry here finished; decided under the publish lock, which then
-        // closes the CTA to publication, so that no warp leaves holding an
-        // index that a later entry would cover
-        auto all_done = [&]() {
-          return ld_volatile_cta(&fs.claims_done) &&
-                 ld_volatile_cta(&fs.n_done) == ld_volatile_cta(&fs.n_pub) &&
-                 ld_relaxed_gpu(P.dec_count) == (unsigned int)B &&
-                 ld_relaxed_gpu(P.r_next) >= ld_relaxed_gpu(P.q_tail);
-        };
-        if (ld_volatile_cta(&fs.closed)) {
-          state = 1;
-        } else if (all_done() && atomicCAS(&fs.pub_lock, 0, 1) == 0) {
-          __threadfence_block();
-          if (all_done()) {
-            fs.closed = 1;
-            state = 1;
-          }
-          __threadfence_block();
-          atomicExch(&fs.pub_lock, 0);
-        }
-        if (state == 0) {
-          const unsigned long long now = now_ns();
-          if (idle_since == 0) idle_since = now;
-          if (now - idle_since > P.wait_ns) state = 2;
-        }
-      }
-      state = __shfl_sync(0xffffffffu, state, 0);
-      if (state == 1) break;
-      if (state == 2) {
-        flags |= SV_STATUS_TIMEOUT;
-#ifdef SV_FLOW_DEBUG
-        flags |= 512u;
-        if (lane == 0 && 3 * (int)blockIdx.x + 2 < B * (G + 1)) {
-          int32_t* o = P.out_tokens + 3 * blockIdx.x;
-          o[0] = (int)((fs.claims_done << 24) | (fs.n_done << 12) | fs.n_pub);
-          o[1] = (int)((fs.a_next << 16) | fs.a_pub);
-          o[2] = (int)((ld_relaxed_gpu(P.dec_count) << 20) | (ld_relaxed_gpu(P.r_next) << 10) |
-                       ld_relaxed_gpu(P.q_tail));
-        }
-#endif
-        failed = true;
-        break;
-      }
-      __nanosleep(200);
-      publish_next();
-      kind = take();
-      continue;
-    }
-    idle_since = 0;
-    if (!mbar_wait(&fs.bar[warp], processed & 1u, P.wait_ns)) {
-      flags |= SV_STATUS_TIMEOUT;
-#ifdef SV_FLOW_DEBUG
-      flags |= 128u;
-#endif
-      failed = true;
-      break;
-    }
-    ++processed;
-    const Meta& m = fs.meta[warp];
-    char* stage = reinterpret_cast<char*>(mybuf);
-    const int s = m.b, c = m.c;  // read before the next take rewrites the meta
-    FlowReq& e = fs.req[s];
-    if (kind == KIND_A) {
-      const int pslot = m.pslot;
-      const bool greedy_item = MODE == MODE_GREEDY || m.reject;
-      const bool padded = !m.direct && m.n < AE;  // a row's last chunk
-      const bool written = (!greedy_item && m.direct) || padded;
-      if (!greedy_item && m.direct) stage_unaligned<EB>(m, stage);
-      else if (padded) pad_item_tail<EB>(stage, m.n);
-      float2 pr;
-      if (!greedy_item) {
-        // the item moves into registers with its maximum; the next item's
-        // copy runs during the exponentials
-        const float c_hi = m.c_hi, c_lo = m.c_lo;
-        uint32_t w[kItemWords];
-        const float mx = item_load_max<EB>(stage, w);
-        if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        kind = take();
-        pr = make_float2(mx, item_exp_sum<EB>(w, mx, c_hi, c_lo));
-      } else {
-        pr = a_item_greedy<EB>(m, stage);
-        if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        kind = take();
-      }
-      int last = 0;
-      if (lane == 0) {
-        part_of(s)[pslot * NC + c] = pr;
-        __threadfence_block();
-        last = atomicAdd(&e.a_done, 1) == e.nI - 1 ? 1 : 0;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0) && P.parts > 1) {
-        // ---- this warp completed its part of the request: the part's
-        // partials go to the workspace, and the last part to arrive decides
-        __threadfence_block();
-        const int b = e.b, gb = e.gb, greedy = e.greedy, lo = e.lo, nI = e.nI, nreq = e.nreq;
-        float2* glob = P.stats + (size_t)b * (2 * G + 1) * P.stride_nc;
-        const float2* tab = part_of(s);
-        for (int ji = lane; ji < nI; ji += 32) {
-          const FlowRow fr = flow_row(lo + ji, NC, gb, greedy != 0, G);
-          glob[(size_t)fr.pslot * P.stride_nc + fr.c] = tab[fr.pslot * NC + fr.c];
-        }
-        __syncwarp();
-        unsigned int old = 0;
-        if (lane == 0) {
-          __threadfence();
-          old = atomicAdd(&P.cnt_a[b], 1u);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        last = old == (unsigned int)(P.parts - 1) ? 1 : 0;
-        if (last) {
-          __threadfence();
-          if (lane == 0) P.cnt_a[b] = 0u;  // every part has arrived: reset for the next call
-          float2* tw = part_of(s);
-          for (int j = lane; j < nreq; j += 32) {
-            if (j >= lo && j < lo + nI) continue;
-            const FlowRow fr = flow_row(j, NC, gb, greedy != 0, G);
-            tw[fr.pslot * NC + fr.c] = __ldcg(glob + (size_t)fr.pslot * P.stride_nc + fr.c);
-          }
-          __syncwarp();
-        } else {
-          finish(s);  // this part is done; another CTA decides
-          __syncwarp();
-        }
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        // ---- this warp completed the request's A items: its decision
-        __threadfence_block();
-        const int b = e.b, gb = e.gb;
-        const ReqAddr A = addr_from_base<PK>(P, b, (int)e.d0, gb);
-        const SharedParts sp{part_of(s), NC};
-        float* rs = rs_of(s);
-        if (MODE == MODE_GREEDY || e.greedy) {
-          greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
-        } else {
-          const DraftIn g = gather_drafts<EB>(P, A, gb);
-          Decision d;
-          d.k = 0;
-          d.reject = 0;
-          d.mt = d.md = d.inv_st = d.rho = 0.0f;
-          (void)decide_core<EB, PK>(P, sp, b, gb, e.tc, rs, A, g, d, true);
-          if (__shfl_sync(0xffffffffu, d.reject, 0)) {
-            // the residual pass: jobs for any CTA
-            if (lane == 0) flow_post_jobs(P, b, d, P.rjobs);
-          } else {
-            final_bonus<EB, PK>(P, sp, b, gb, e.tc, rs[gb], stage_of(s));
-          }
-        }
-        count_decision();
-        finish(s);
-        __syncwarp();
-      }
-    } else {
-      // ---- R item: fixed-point sum of the residual weights over the chunk
-      const unsigned long long sr = r_item<EB>(m, stage);
-      __syncwarp();
-      kind = take();
-      int last = 0;
-      if (lane == 0) {
-        P.resid[(size_t)e.b * P.stride_ncr + c] = sr;
-        __threadfence_block();
-        last = atomicAdd(&e.a_done, 1) == e.nI - 1 ? 1 : 0;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        // ---- this warp completed the job: the last job of the request draws
-        unsigned int old = 0;
-        const int b = e.b;
-        if (lane == 0) {
-          __threadfence();
-          old = atomicAdd(&P.cnt_r[b], 1u);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (unsigned int)(P.rjobs - 1)) {
-          __threadfence();
-          if (lane == 0) P.cnt_r[b] = 0u;  // every job has arrived: reset for the next call
-          const int k = e.k;
-          ResidC kc;
-          kc.mt = e.mt; kc.md = e.md; kc.inv_st = e.inv_st; kc.rho = e.rho;
-          resid_scales(kc);
-          kc.hi = e.tc.hi; kc.lo = e.tc.lo; kc.reject = 1;
-          const char* trow = P.target + (e.t0 + (size_t)k) * (size_t)V * EB;
-          const char* drow = P.draft + (e.d0 + (size_t)k) * (size_t)V * EB;
-          unsigned int uflags = 0;
-          const float u_fin = sanitize_uniform(P.uniforms[e.uf], uflags);
-          int tok = chunk_draw<EB, true>(trow, drow, V, NCR, u_fin, kc,
-                                         P.resid + (size_t)b * P.stride_ncr, stage_of(s));
-          if (lane == 0) {
-            if (tok < 0) {
-              flags |= SV_STATUS_INTERNAL;
-              tok = V - 1;
-            }
-            P.out_tokens[(size_t)b * (G + 1) + k] = tok;
-            flags |= uflags;
-          }
-        }
-        finish(s);
-        __syncwarp();
-      }
-    }
-    publish_next();
-  }
-  // no copy may still be landing in this warp's buffer when it leaves
-  if (failed && kind != KIND_NONE) (void)mbar_wait(&fs.bar[warp], processed & 1u, P.wait_ns);
-  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
-  if (lane == 0 && any) atomicOr(P.status, any);
-  // the last CTA out resets the workspace counters for the next call
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(P.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
-  }
-  __syncthreads();
-  if (s_last && tid == 0) {
-    *P.next_item = 0;
-    *P.r_next = 0;
-    *P.q_tail = 0;
-    *P.dec_count = 0;
-    *P.exit_count = 0;
-    __threadfence();
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 int check_scalars(sv_dtype dtype, int B, int G, int V) {
@@ -4493,53 +3735,7 @@ struct Route {
   int kind;  // SV_ROUTE_*
   int C;     // cluster size (cluster paths)
   int Q;     // clusters launched (cluster paths)
-  int flow;  // claims: 1 on the request-flow kernel, 0 on the streaming kernel
 };
-
-// Request flow: warps (one buffer each) and requests in flight per CTA, and
-// the dynamic shared memory of a launch (buffers | per entry: partials, chunk
-// sums, row statistics, staging | claim order | row counts).
-constexpr int kFlowWarps = 16, kFlowSlots = 4;
-#ifndef SV_FLOW_CLAIMS
-#define SV_FLOW_CLAIMS 8
-#endif
-constexpr int kFlowClaims = SV_FLOW_CLAIMS;  // claims per CTA that the parts aim at
-#ifndef SV_FLOW_ROUTE
-#define SV_FLOW_ROUTE 0
-#endif
-constexpr bool kFlowRoute = SV_FLOW_ROUTE != 0;
-constexpr int kFlowMaxParts = 16;
-constexpr size_t kFlowSmemCap = (size_t)223 * 1024;  // leaves room for the static part
-size_t flow_smem(int B, int G, int V, int eb) {
-  const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
-  const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
-  const size_t part = ((size_t)(2 * G + 1) * nc * sizeof(float2) + 15) & ~(size_t)15;
-  (void)ncr;
-  return (size_t)kFlowWarps * kItemBytes + (size_t)kFlowSlots * (part + 1024 + kItemBytes) +
-         (((size_t)B * 5 + 15) & ~(size_t)15);
-}
-// CTAs of the request-flow kernel that fit on this device at once (cached).
-template <int EB, int MODE, bool PK>
-int flow_ctas() {
-  static std::atomic<int> cached{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const int c0 = cached.load(std::memory_order_relaxed);
-  if ((c0 >> 16) == dev + 1) return c0 & 0xffff;
-  auto kern = flow_kernel<EB, MODE, PK, kFlowWarps, kFlowSlots>;
-  int sms = 0, per_sm = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFlowSmemCap) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFlowWarps * 32, kFlowSmemCap) !=
-          cudaSuccess)
-    per_sm = 0;
-  (void)cudaGetLastError();
-  int n = sms * (per_sm > 0 ? 1 : 0);  // one CTA per SM
-  n = n > 0xffff ? 0xffff : n;
-  cached.store(((dev + 1) << 16) | n, std::memory_order_relaxed);
-  return n;
-}
 
 // Streaming cluster path: the largest cluster of which B fit at once (one
 // wave, a request per cluster); with `claims`, a batch beyond one wave of
@@ -4547,36 +3743,25 @@ int flow_ctas() {
 // turn.
 template <int EB, int MODE, bool PK>
 Route stream_route(int B, int G, int V) {
-  const Route none{SV_ROUTE_PERSISTENT, 0, 0, 0};
-#ifdef SV_FLOW_MIN_B
-  if (B >= SV_FLOW_MIN_B && flow_smem(B, G, V, EB) <= kFlowSmemCap) {
-    const int Q = flow_ctas<EB, MODE, PK>();
-    if (Q > 0) return Route{SV_ROUTE_CLAIMS, 1, Q, 1};
-  }
-#endif
+  const Route none{SV_ROUTE_PERSISTENT, 0, 0};
   if (B >= 1 && stream_tables(G, V, EB) <= StreamShape<MODE, 1>::table_cap)
     for (int C = kClusterMax; C >= 1; --C)
-      if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B, 0};
-  // beyond one wave: the request-flow kernel when its tables fit (when built
-  // with SV_FLOW_ROUTE), else the streaming kernel's claims
-  if (kFlowRoute && B >= 1 && flow_smem(B, G, V, EB) <= kFlowSmemCap) {
-    const int Q = flow_ctas<EB, MODE, PK>();
-    if (Q > 0) return Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B, 1};
-  }
+      if (max_stream_clusters<EB, MODE, PK, 1>(C) >= B) return Route{SV_ROUTE_STREAM, C, B};
+  // beyond one wave: the streaming kernel's claims
   if (B < 1 || stream_tables(G, V, EB) > StreamShape<MODE, 1>::table_cap) return none;
   constexpr int QC = claim_cps<MODE>();
   if (stream_tables(G, V, EB) + claim_bytes(B) > StreamShape<MODE, QC>::table_cap) return none;
   const int Q = max_stream_clusters<EB, MODE, PK, QC>(1);
-  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B, 0} : none;
+  return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B} : none;
 }
 
 template <int EB, int MODE, bool PK>
 Route route(int B, int G, int V) {
   const int sched = g_schedule.load();
-  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0, 0};
+  if (sched == SV_SCHEDULE_PERSISTENT) return Route{SV_ROUTE_PERSISTENT, 0, 0};
   if (sched == SV_SCHEDULE_AUTO) {
     const int C = cluster_route<EB, MODE, PK>(B, G, V);
-    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B, 0};
+    if (C > 0) return Route{SV_ROUTE_CLUSTER, C, B};
   }
   // Beyond one wave, claimed requests (longest first) beat the persistent
   // grid's chunk claims: B=256 ragged, B=512 gamma 1 and 3, sampling 159 ->
@@ -4607,30 +3792,10 @@ int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
 }
 
 template <int EB, int MODE, bool PK>
-int launch_flow(const Params& P0, int Q, cudaStream_t stream) {
-  // Each request is claimed in `parts` parts, so that every CTA takes about
-  // kFlowClaims claims and the last round of claims is short; at most one
-  // part per A chunk of a row (no empty part).
-  Params P = P0;
-  const long long want = ((long long)kFlowClaims * Q + P.B - 1) / P.B;
-  P.parts = (int)(want < 1 ? 1 : (want > kFlowMaxParts ? kFlowMaxParts : want));
-  if (P.parts > P.NC) P.parts = P.NC;
-  // residual jobs of about a part's size each
-  const long long items = (long long)(2 * P.G + 1) * P.NC;
-  const long long jobs = (P.NCR * (long long)P.parts + items - 1) / items;
-  P.rjobs = (int)(jobs < 1 ? 1 : (jobs > kFlowMaxJobs ? kFlowMaxJobs : jobs));
-  if (P.rjobs > P.NCR) P.rjobs = P.NCR;
-  flow_kernel<EB, MODE, PK, kFlowWarps, kFlowSlots>
-      <<<Q, kFlowWarps * 32, flow_smem(P.B, P.G, P.V, EB), stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
-}
-
-template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
   if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, 1>(P, r.C, r.Q, stream);
-  if (r.kind == SV_ROUTE_CLAIMS && r.flow) return launch_flow<EB, MODE, PK>(P, r.Q, stream);
   if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, claim_cps<MODE>()>(P, r.C, r.Q, stream);
   const int grid = grid_size<EB, MODE, PK>();
   if (grid <= 0) return SV_ERR_CUDA;
@@ -4706,7 +3871,6 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.status = reinterpret_cast<unsigned int*>(w + L.status);
   P.wait_ns = g_wait_ns.load();
   P.lazy = g_lazy.load();
-  P.parts = 1;
   P.next_item = reinterpret_cast<unsigned int*>(w + L.next_item);
   P.exit_count = reinterpret_cast<unsigned int*>(w + L.exit_count);
   P.r_next = reinterpret_cast<unsigned int*>(w + L.r_next);
@@ -4718,8 +3882,6 @@ int fill_params(Params& P, const void* target, const void* draft, sv_dtype dtype
   P.queue = reinterpret_cast<DecRecord*>(w + L.queue);
   P.stats = reinterpret_cast<float2*>(w + L.stats);
   P.resid = reinterpret_cast<unsigned long long*>(w + L.resid);
-  P.jobs = reinterpret_cast<DecRecord*>(w + L.jobs);
-  P.rjobs = 1;
   return SV_OK;
 }
 
@@ -4940,7 +4102,7 @@ int spec_verify_set_lazy(int on) {
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int* cluster_size) {
   const int rc = check_scalars(dtype, B, G, V);
   if (rc) return rc;
-  Route r{SV_ROUTE_PERSISTENT, 0, 0, 0};
+  Route r{SV_ROUTE_PERSISTENT, 0, 0};
   if (B > 0) {
     if (dtype == SV_BF16)
       r = greedy ? route<2, MODE_GREEDY, false>(B, G, V) : route<2, MODE_SAMPLE, false>(B, G, V);

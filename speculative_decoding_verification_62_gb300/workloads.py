@@ -88,11 +88,12 @@ class Workload:
         inputs and outputs.  Read position by position (lazy), a sampled
         request with k accepted drafts needs target and draft rows
         0..min(k, gamma_b - 1) and, when k == gamma_b, the bonus row.  The
-        request-claims schedule reads a request eagerly (every row) when its
-        rows alone reach 80 % of a CTA's share of the batch (`ctas` CTAs),
-        and a greedy request (T == 0) always: gamma_b + 1 target rows.  Read
+        request-claims schedule (`ctas` CTAs) reads lazily only a batch of at
+        least two requests per CTA, and there reads a request eagerly (every
+        row) when its rows alone reach 80 % of a CTA's share of the batch; a
+        greedy request (T == 0) needs its gamma_b + 1 target rows.  Read
         eagerly, every row: bytes_min()."""
-        if mode != "sample" or not lazy:
+        if mode != "sample" or not lazy or self.B < 2 * ctas:
             return self.bytes_min(mode)
         k = torch.as_tensor(num_accepted).cpu().to(torch.int64)
         g = self.gamma.cpu().to(torch.int64)
