@@ -321,16 +321,18 @@ def run_ours(args):
                                       "persistent": binding.SCHEDULE_PERSISTENT}[args.schedule])
     binding.spec_verify_set_lazy(args.read == "lazy")
     route, csize = binding.spec_verify_route(base.target.dtype, B, G, V, greedy=mode == "greedy")
-    # request claims read lazily from two requests per CTA (one CTA per SM)
+    # request claims read lazily: sampling from two requests per CTA (one CTA
+    # per SM), greedy whenever requests are claimed (two CTAs per SM)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    lazy = (mode == "sample" and route == binding.ROUTE_CLAIMS and args.read == "lazy"
-            and B >= 2 * sms)
+    lazy = route == binding.ROUTE_CLAIMS and args.read == "lazy" and \
+        (B >= 2 * sms if mode == "sample" else B > 2 * sms)
     kernel = {binding.ROUTE_CLUSTER: "cluster_kernel", binding.ROUTE_STREAM: "stream_kernel",
               binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
     schedule = {binding.ROUTE_CLUSTER: f"resident clusters of {csize} CTAs, one per request",
                 binding.ROUTE_STREAM: f"streaming clusters of {csize} CTAs, one per request",
                 binding.ROUTE_CLAIMS: "streaming CTAs claiming requests in turn, longest first"
-                                      + (", positions read one at a time up to the first rejection"
+                                      + (", positions read one at a time up to the first "
+                                         + ("rejection" if mode == "sample" else "mismatch")
                                          if lazy else ""),
                 binding.ROUTE_PERSISTENT: "persistent grid"}[route]
     # the persistent grid runs batches of more than 1536 requests as several launches

@@ -86,7 +86,8 @@ enum {
   SV_STATUS_BAD_TOKEN = 2u,       /* draft token outside [0, V): clamped */
   SV_STATUS_BAD_UNIFORM = 4u,     /* uniform outside [0, 1) or NaN: replaced by 0 */
   SV_STATUS_BAD_TEMPERATURE = 8u, /* temperature < 0, inf or NaN: replaced by 1 */
-  SV_STATUS_NONFINITE_ROW = 16u,  /* a row whose maximum is not finite */
+  SV_STATUS_NONFINITE_ROW = 16u,  /* a row whose maximum is not finite (among the rows the
+                                     call reads: see spec_verify_set_lazy) */
   SV_STATUS_INTERNAL = 32u,       /* an inverse-CDF draw found no token (never expected) */
   SV_STATUS_TIMEOUT = 64u         /* a bounded wait for a request's decision ran out; the
                                      request's outputs are incomplete and the workspace must
@@ -311,8 +312,11 @@ unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
 
 /*
  * spec_verify_set_lazy: how the request-claims schedule (SV_ROUTE_CLAIMS)
- * reads a sampled request's rows in the calls that follow in this process.
- * 1 (the default): position by position.  The target and draft rows of
+ * reads a request's rows in the calls that follow in this process.
+ * 1 (the default): position by position.  In a greedy call (or a request
+ * with temperature 0) target row i is reduced to its argmax and compared
+ * with draft i before row i + 1 is read; the call stops at the first draft
+ * that differs.  For a sampled request the target and draft rows of
  * position i are reduced and draft i is tested before the rows of position
  * i + 1 matter, and the bonus row gamma_b only after every draft was
  * accepted, as in the verification loop of disassemble-channel
@@ -320,9 +324,10 @@ unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
  * draft.  For a request with at least four drafts, the CTA streams the next
  * position while one is tested; what it read of a position after the first
  * rejection is not used.  Lazy stages lengthen a request while they shorten
- * the batch, so they apply only where the batch holds at least two requests
- * per CTA, and not to a request whose rows alone reach 80 % of a CTA's share
- * of the batch's rows.  0: every row of every request is reduced before any
+ * the batch, so sampled requests are read this way only where the batch
+ * holds at least two requests per CTA, and not when a request's rows alone
+ * reach 80 % of a CTA's share of the batch's rows.  0: every row of every
+ * request is reduced before any
  * test.  The outputs are identical either way: a position's arithmetic does
  * not depend on the order.  The other schedules always read every row.
  * Returns the previous setting, or SV_ERR_SCALAR for a value other than 0

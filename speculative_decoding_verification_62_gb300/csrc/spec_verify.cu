@@ -1177,9 +1177,16 @@ __device__ __noinline__ void decide_sample(const Params& P, int b, int gb, TempC
 // Greedy decision: argmax per target row from the per-item partials (rows
 // reduced eight at a time as above; rs holds the row argmaxes), then the
 // first mismatch by warp ballot.
+// Greedy steps over target rows [lo, hi) (hi <= gamma_b + 1), every earlier
+// draft having matched its row's argmax: rs[r] receives row r's argmax.
+// Returns k, the first position in [lo, hi) whose draft differs from the
+// argmax (gamma_b when every draft matches and row gamma_b is in), or -1 when
+// all of [lo, hi) match and later rows remain.  Once k is known it writes
+// out_tokens (the drafts before k, the argmax at k, then -1), num_accepted,
+// NaN p/q and status.  One call over [0, gamma_b + 1) is the whole step.
 template <bool PK, class Parts>
-__device__ __forceinline__ void greedy_core(const Params& P, const Parts& parts, int b, int gb,
-                                            int* rs) {
+__device__ __forceinline__ int greedy_range(const Params& P, const Parts& parts, int b, int gb,
+                                            int* rs, int lo, int hi) {
   const int G = P.G, V = P.V, NC = P.NC;
   const int lane = threadIdx.x & 31, part = lane & 3;
   unsigned int flags = 0;
@@ -1188,9 +1195,9 @@ __device__ __forceinline__ void greedy_core(const Params& P, const Parts& parts,
   int x = 0;
   if (i < gb) x = P.tokens[A.d0 + i];
 #pragma unroll 1
-  for (int r0 = 0; r0 <= gb; r0 += 8) {
+  for (int r0 = lo; r0 < hi; r0 += 8) {
     const int r = r0 + (lane >> 2);
-    const bool live = r <= gb;
+    const bool live = r < hi;
     const int slot = live ? r : 0;
     float2 v[kHeld];
 #pragma unroll
@@ -1220,24 +1227,27 @@ __device__ __forceinline__ void greedy_core(const Params& P, const Parts& parts,
   }
   __syncwarp();
   bool mismatch = false;
-  if (i < gb) {
-    if (x < 0 || x >= V) flags |= SV_STATUS_BAD_TOKEN;
-    mismatch = x != rs[i];
-  }
+  if (lo == 0 && i < gb && (x < 0 || x >= V)) flags |= SV_STATUS_BAD_TOKEN;
+  if (i >= lo && i < hi && i < gb) mismatch = x != rs[i];
   const unsigned int mm = __ballot_sync(0xffffffffu, mismatch);
-  const int k = mm ? (__ffs(mm) - 1) : gb;
+  const int k = mm ? (__ffs(mm) - 1) : (hi > gb ? gb : -1);
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && any) atomicOr(P.status, any);
+  if (k < 0) return k;
   const int gk = rs[k];
   if (i <= G) P.out_tokens[(size_t)b * (G + 1) + i] = i < k ? x : (i == k ? gk : -1);
   if (i < (PK ? gb : G)) {  // a sampling call's zero-temperature request has no p or q
     if (P.p_tok) P.p_tok[A.d0 + i] = NAN;
     if (P.q_tok) P.q_tok[A.d0 + i] = NAN;
   }
-  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
-  if (lane == 0) {
-    if (P.num_accepted) P.num_accepted[b] = k;
-    if (any) atomicOr(P.status, any);
-  }
+  if (lane == 0 && P.num_accepted) P.num_accepted[b] = k;
   __syncwarp();
+  return k;
+}
+template <bool PK, class Parts>
+__device__ __forceinline__ void greedy_core(const Params& P, const Parts& parts, int b, int gb,
+                                            int* rs) {
+  (void)greedy_range<PK>(P, parts, b, gb, rs, 0, gb + 1);
 }
 template <bool PK>
 __device__ __noinline__ void decide_greedy(const Params& P, int b, int gb, int* rs) {
@@ -3261,10 +3271,21 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     // the batch (the call lasts at least as long as it does).  Measured:
     // B = 512, gamma 1 and 3: 113 -> 111 and 202 -> 174 us; B = 256 ragged
     // (1.7 requests per CTA): 131 eager against 135 lazy.
-    const bool lazy = P.lazy && queue && sample && P.B >= 2 * nq &&
-                      5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
-                          4ull * (unsigned long long)s_rows;
-    auto stage_hi = [&](int slo) { return lazy ? min(slo + 1, gb) : gb; };
+#ifndef SV_GREEDY_LAZY
+#define SV_GREEDY_LAZY 1
+#endif
+    // Greedy steps read one target row per stage (no residual pass follows a
+    // mismatch).
+    const bool lazy = P.lazy && queue &&
+                      (sample ? P.B >= 2 * nq &&
+                                    5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
+                                        4ull * (unsigned long long)s_rows
+                              : SV_GREEDY_LAZY != 0);
+    // a stage's end: sampled, positions [slo, hi) (plus the bonus row when
+    // slo == gamma_b, or eagerly); greedy, target rows [slo, hi)
+    auto stage_hi = [&](int slo) {
+      return sample ? (lazy ? min(slo + 1, gb) : gb) : (lazy ? slo + 1 : gb + 1);
+    };
     // The items of the stage that starts at position slo.  With `spec` the
     // warp stops taking them once the decision in progress (number dseq) is
     // final; it still draws its remaining tickets, so that the stage uses
@@ -3273,19 +3294,24 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
       const int hi = stage_hi(slo);
       const bool with_bonus = !lazy || slo == gb;
       const int npos = hi - slo;
-      const int nrows = !sample ? gb + 1 : 2 * npos + (with_bonus ? 1 : 0);
+      const int nrows = !sample ? npos : 2 * npos + (with_bonus ? 1 : 0);
       const unsigned int nI = (unsigned int)nrows * (unsigned int)NC;
       auto a_meta = [&](unsigned int j) {
         // the rows in streaming order: eagerly, a sampled request's position-0
         // rows, the most often rejected, come last, closest to the residual
         // pass; lazily, target row slo then draft row slo (or the bonus row)
         StreamRow fr;
-        if (lazy) {
+        if (lazy && sample) {
           const int rr = (int)j / NC;
           fr.c = (int)j - rr * NC;
           fr.draft = rr == 1;
           fr.row = npos ? slo : gb;
           fr.pslot = fr.draft ? G + 1 + slo : fr.row;
+        } else if (lazy) {  // greedy: target row slo
+          fr.c = (int)j;
+          fr.draft = false;
+          fr.row = slo;
+          fr.pslot = slo;
         } else {
           fr = stream_row((int)j, NC, gb, !sample, G);
         }
@@ -3409,7 +3435,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
         dc.c_hi = tc.hi;
         dc.c_lo = tc.lo;
         if (greedy) {
-          greedy_core<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs));
+          dc.k = greedy_range<PK>(P, sp, b, gb, reinterpret_cast<int*>(rs), lo, hi);
         } else {
           Decision d;
           d.k = 0;
@@ -3440,7 +3466,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
         __syncwarp();
       }
       // the next stage, read while the decision is made, or once it is known
-      const bool spec = lazy && hi < gb && gb >= kSpecMinGamma;
+      const bool spec = lazy && sample && hi < gb && gb >= kSpecMinGamma;
       if (spec) run_stage(hi, true);
       __syncthreads();  // the CTA's warps see the decision
       cd = sdec[dseq & 1];

@@ -87,16 +87,22 @@ class Workload:
         """The logit rows a call must read given its outcomes, plus the small
         inputs and outputs.  Read position by position (lazy), a sampled
         request with k accepted drafts needs target and draft rows
-        0..min(k, gamma_b - 1) and, when k == gamma_b, the bonus row.  The
-        request-claims schedule (`ctas` CTAs) reads lazily only a batch of at
+        0..min(k, gamma_b - 1) and, when k == gamma_b, the bonus row; a greedy
+        request needs target rows 0..k.  In sampling mode the request-claims
+        schedule (`ctas` CTAs, one per SM) reads lazily only a batch of at
         least two requests per CTA, and there reads a request eagerly (every
         row) when its rows alone reach 80 % of a CTA's share of the batch; a
-        greedy request (T == 0) needs its gamma_b + 1 target rows.  Read
-        eagerly, every row: bytes_min()."""
-        if mode != "sample" or not lazy or self.B < 2 * ctas:
+        request with T == 0 needs its gamma_b + 1 target rows.  Read eagerly,
+        every row: bytes_min()."""
+        if not lazy:
             return self.bytes_min(mode)
         k = torch.as_tensor(num_accepted).cpu().to(torch.int64)
         g = self.gamma.cpu().to(torch.int64)
+        if mode != "sample":
+            small = self.B * (4 * self.G + 4 + 8) + self.B * 4 * (self.G + 2)
+            return int((k + 1).sum().item()) * self.V * self.elem_bytes + small
+        if self.B < 2 * ctas:
+            return self.bytes_min(mode)
         sampled = self.temperature.cpu() != 0
         full = torch.where(sampled, 2 * g + 1, g + 1)
         total = int(full.sum().item())

@@ -368,3 +368,46 @@ def test_lazy_and_eager_reads_agree(B, G, V, dt, sigma_d):
     if G > 0:  # rejections and full acceptances both occur: both lazy exits run
         n, g = lazy[1], w.gamma.cpu().numpy()
         assert (n < g).any() and (n == g).any()
+
+
+def _claims_greedy(w, tokens, lazy):
+    prev_l = binding.spec_verify_set_lazy(lazy)
+    prev_s = binding.spec_verify_set_schedule(binding.SCHEDULE_STREAM)
+    try:
+        v = binding.Verifier(w.B, w.G, w.V, DEV)
+        v.greedy(w.target, tokens, w.gamma)
+        torch.cuda.synchronize()
+        st = binding.spec_verify_status(v.workspace)
+        assert st == 0, binding.status_names(st)
+        return v.out_tokens.cpu().numpy(), v.num_accepted.cpu().numpy()
+    finally:
+        binding.spec_verify_set_schedule(prev_s)
+        binding.spec_verify_set_lazy(prev_l)
+
+
+@pytest.mark.parametrize("B,G,V,dt", [(400, 7, 20001, "bf16"), (700, 3, 4097, "f32"), (500, 0, 33, "bf16")])
+def test_lazy_and_eager_greedy_reads_agree(B, G, V, dt):
+    """Greedy request claims (two CTAs per SM) read target rows one at a time
+    up to the first draft that differs from its row's argmax.  Drafts are
+    planted as the argmax of their target row with probability 0.8, so both
+    early mismatches and full matches occur.  Lazy and eager reads agree bit
+    for bit, and both with the oracle."""
+    import numpy as np
+    w = W.make_random(B, G, V, dt, seed=91 * B + G, gamma="ragged").to(DEV)
+    assert route(w.target.dtype, B, G, V, greedy=True, sched=binding.SCHEDULE_STREAM) == \
+        (binding.ROUTE_CLAIMS, 1)
+    rng = np.random.default_rng(B)
+    am = w.target[:, :G].float().argmax(dim=-1).to(torch.int32) if G > 0 else \
+        torch.zeros((B, 0), dtype=torch.int32, device=DEV)
+    keep = torch.as_tensor(rng.random((B, G)) < 0.8, device=DEV)
+    other = torch.as_tensor(rng.integers(0, V, (B, G)), dtype=torch.int32, device=DEV)
+    tokens = torch.where(keep, am, other).contiguous()
+    lazy = _claims_greedy(w, tokens, True)
+    eager = _claims_greedy(w, tokens, False)
+    assert (lazy[0] == eager[0]).all() and (lazy[1] == eager[1]).all()
+    ins = W.oracle_inputs(w)
+    ref = oracle.greedy(ins["target"], tokens.cpu().numpy(), ins["gamma"], nthreads=NTHREADS)
+    assert not compare_greedy(ref, lazy[0], lazy[1])
+    if G > 0:
+        n, g = lazy[1], w.gamma.cpu().numpy()
+        assert (n < g).any() and ((n == g) & (g > 0)).any()

@@ -73,6 +73,9 @@ def test_bytes_needed_counts_rows_up_to_the_first_rejection():
     rows = 2 + 4 + 7 + 5 + 1 + 4
     assert w.bytes_needed("sample", k, lazy=True, ctas=1) == rows * 16 * 2 + small
     assert w.bytes_needed("sample", k, lazy=False, ctas=1) == w.bytes_min("sample")
-    assert w.bytes_needed("greedy", k, lazy=True, ctas=1) == w.bytes_min("greedy")
+    assert w.bytes_needed("greedy", k, lazy=False, ctas=1) == w.bytes_min("greedy")
+    # greedy, lazily: target rows 0..k
+    small_g = w.bytes_min("greedy") - (14 + 6) * 16 * 2
+    assert w.bytes_needed("greedy", k, lazy=True, ctas=1) == (1 + 2 + 4 + 3 + 1 + 2) * 16 * 2 + small_g
     # fewer than two requests per CTA: read eagerly
     assert w.bytes_needed("sample", k, lazy=True, ctas=4) == w.bytes_min("sample")
