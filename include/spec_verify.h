@@ -50,7 +50,8 @@
  * on error launches nothing.  Values inside device arrays cannot be checked on
  * the host: a gamma_b outside [0, G], a draft token outside [0, V), a uniform
  * outside [0, 1), a negative or non-finite temperature, or a row with no
- * finite logit sets a bit in the workspace's status word (read it with
+ * finite logit (among the rows a call reads: spec_verify_set_lazy) sets a
+ * bit in the workspace's status word (read it with
  * spec_verify_status) and is clamped to a legal value, so no call reads or
  * writes outside the arrays described above.  NaN logits are not supported.
  */

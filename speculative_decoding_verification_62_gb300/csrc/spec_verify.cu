@@ -3268,27 +3268,23 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
     // positions.  With claims a sampled request is taken lazily: stage s
     // holds target and draft rows s only, and the rows of position s + 1
     // matter only if draft s is accepted (the stage after the last position
-    // holds the bonus row gamma_b).  While warp 0 decides stage s, the other
-    // warps already stream stage s + 1; if the decision is final they stop
-    // taking its items, and what they read of it is not used.  Otherwise one
-    // stage holds every row.  Each position's arithmetic is the same either
-    // way.
+    // holds the bonus row gamma_b).  For a request with at least
+    // kSpecMinGamma drafts the other warps already stream stage s + 1 while
+    // warp 0 decides stage s; if the decision is final they stop taking its
+    // items, and what they read of it is not used.  Otherwise one stage holds
+    // every row.  Each position's arithmetic is the same either way.
     // Lazy stages lengthen a request while they shorten the batch's work, so
-    // they are used where requests queue at least two deep per CTA, and not
-    // for a request whose rows alone reach 80 % of a CTA's average share of
-    // the batch (the call lasts at least as long as it does).  Measured:
-    // B = 512, gamma 1 and 3: 113 -> 111 and 202 -> 174 us; B = 256 ragged
-    // (1.7 requests per CTA): 131 eager against 135 lazy.
-#ifndef SV_GREEDY_LAZY
-#define SV_GREEDY_LAZY 1
-#endif
-    // Greedy steps read one target row per stage (no residual pass follows a
-    // mismatch).
+    // sampled requests are read this way where requests queue at least two
+    // deep per CTA, and not when a request's rows alone reach 80 % of a CTA's
+    // average share of the batch (the call lasts at least as long as that
+    // request does).  Measured: B = 512, gamma 1 and 3: 112 -> 110 and 201 ->
+    // 170 us; B = 256 ragged (1.7 requests per CTA): 131 eager against 135
+    // lazy.  Greedy steps read one target row per stage, and no residual pass
+    // follows a mismatch: B = 512, gamma 3: 80 -> 50 us.
     const bool lazy = P.lazy && queue &&
-                      (sample ? P.B >= 2 * nq &&
-                                    5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
-                                        4ull * (unsigned long long)s_rows
-                              : SV_GREEDY_LAZY != 0);
+                      (!sample || (P.B >= 2 * nq &&
+                                   5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
+                                       4ull * (unsigned long long)s_rows));
     // a stage's end: sampled, positions [slo, hi) (plus the bonus row when
     // slo == gamma_b, or eagerly); greedy, target rows [slo, hi)
     auto stage_hi = [&](int slo) {

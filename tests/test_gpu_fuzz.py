@@ -149,3 +149,45 @@ def test_fuzz_claims_sampling(i):
     rep = compare_sample(ref, a[0], a[1], w.gamma.cpu().numpy(), a[2].numpy(), a[3].numpy())
     assert not rep.mismatches, (draw_large_case(i)[:5], rep.mismatches[:3])
     assert rep.max_prob_rel_err < PROB_RTOL
+
+
+@pytest.mark.parametrize("i", range(4))
+def test_fuzz_claims_greedy(i):
+    """Greedy batches beyond one wave of two CTAs per SM: request claims read
+    target rows one at a time up to the first mismatch (lazily), against the
+    persistent grid (every row) and the oracle.  Drafts are planted as the
+    argmax with probability 0.7, so mismatches come at every position."""
+    r = random.Random(9300 + i)
+    B = r.choice([320, 400, 640, 1000])
+    G = r.randint(0, 7)
+    V = r.choice([33, 4097, 20001])
+    dt = r.choice(["bf16", "f32"])
+    packed = r.random() < 0.4
+    w = W.make_random(B, G, V, dt, seed=700 + i, gamma="ragged").to(DEV)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    assert binding.spec_verify_route(tdt, B, G, V, True)[0] == binding.ROUTE_CLAIMS
+    if G:
+        am = w.target[:, :G].float().argmax(dim=2).to(torch.int32)
+        keep = torch.rand(w.draft_tokens.shape, device=DEV,
+                          generator=torch.Generator(DEV).manual_seed(50 + i)) < 0.7
+        w.draft_tokens = torch.where(keep, am, w.draft_tokens).contiguous()
+    outs = []
+    for sched in (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT):
+        prev = binding.spec_verify_set_schedule(sched)
+        try:
+            v = binding.Verifier(B, G, V, DEV)
+            if packed:
+                pk = W.pack(w)
+                v.greedy_packed(pk.target, pk.cu_draft, pk.draft_tokens)
+            else:
+                v.greedy(w.target, w.draft_tokens, w.gamma)
+            torch.cuda.synchronize()
+            assert binding.spec_verify_status(v.workspace) == 0
+            outs.append((v.out_tokens.cpu().numpy(), v.num_accepted.cpu().numpy()))
+        finally:
+            binding.spec_verify_set_schedule(prev)
+    assert (outs[0][0] == outs[1][0]).all() and (outs[0][1] == outs[1][1]).all()
+    ref = oracle.greedy(W.logits_numpy(w.target), w.draft_tokens.cpu().numpy(),
+                        w.gamma.cpu().numpy(), nthreads=NTHREADS)
+    bad = compare_greedy(ref, outs[0][0], outs[0][1])
+    assert not bad, bad[:3]
