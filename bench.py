@@ -323,18 +323,22 @@ def run_ours(args):
     binding.spec_verify_set_lazy(args.read == "lazy")
     route, csize = binding.spec_verify_route(base.target.dtype, B, G, V, greedy=mode == "greedy")
     # request claims read lazily: sampling from two requests per CTA (one CTA
-    # per SM), greedy whenever requests are claimed (two CTAs per SM)
+    # per SM; on the pipeline kernel), greedy whenever requests are claimed
+    # (two CTAs per SM)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    lazy = route == binding.ROUTE_CLAIMS and args.read == "lazy" and \
-        (B >= 2 * sms if mode == "sample" else B > 2 * sms)
+    lazy = args.read == "lazy" and (route == binding.ROUTE_PIPELINE or (
+        route == binding.ROUTE_CLAIMS and (B >= 2 * sms if mode == "sample" else B > 2 * sms)))
     kernel = {binding.ROUTE_CLUSTER: "cluster_kernel", binding.ROUTE_STREAM: "stream_kernel",
-              binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
+              binding.ROUTE_CLAIMS: "stream_kernel", binding.ROUTE_PIPELINE: "pipe_kernel",
+              binding.ROUTE_PERSISTENT: "verify_kernel"}[route]
+    upto = (", positions read one at a time up to the first "
+            + ("rejection" if mode == "sample" else "mismatch")) if lazy else ""
     schedule = {binding.ROUTE_CLUSTER: f"resident clusters of {csize} CTAs, one per request",
                 binding.ROUTE_STREAM: f"streaming clusters of {csize} CTAs, one per request",
                 binding.ROUTE_CLAIMS: "streaming CTAs claiming requests in turn, longest first"
-                                      + (", positions read one at a time up to the first "
-                                         + ("rejection" if mode == "sample" else "mismatch")
-                                         if lazy else ""),
+                                      + upto,
+                binding.ROUTE_PIPELINE: "one CTA per SM with two requests in flight, claimed in "
+                                        "turn, longest first" + upto,
                 binding.ROUTE_PERSISTENT: "persistent grid"}[route]
     # the persistent grid runs batches of more than 1536 requests as several launches
     launches_per_call = math.ceil(B / 1536) if route == binding.ROUTE_PERSISTENT else 1

@@ -264,7 +264,12 @@ const char *spec_verify_strerror(int code);
  *     kernel runs as one CTA per SM (sampling) or two (greedy), each taking
  *     whole requests in turn from a claim counter, longest request first
  *     (SV_ROUTE_CLAIMS).  The claim order takes 5 bytes of shared memory per
- *     request;
+ *     request.  A sampling call of at least two requests per SM whose
+ *     positions are read lazily (spec_verify_set_lazy) runs instead on a
+ *     pipeline kernel (SV_ROUTE_PIPELINE): one CTA per SM keeps two requests
+ *     in flight, its warps moving from one request's items to the other's
+ *     without a barrier, and the warp that completes a stage, a residual pass
+ *     or a draw runs what follows it;
  *   - the persistent grid, for batches whose claim order does not fit (tens
  *     of thousands of requests): chunks claimed from global counters,
  *     decisions published through global records.
@@ -278,13 +283,16 @@ const char *spec_verify_strerror(int code);
  * path, the streaming cluster path and the persistent grid that applies, as
  * above), SV_SCHEDULE_PERSISTENT (every call on the persistent grid) or
  * SV_SCHEDULE_STREAM (as AUTO without the resident path).  Returns the
- * previous policy, or SV_ERR_SCALAR for an unknown value.
+ * previous policy, or SV_ERR_SCALAR for an unknown value.  SV_SCHEDULE_STREAM
+ * also leaves out the pipeline kernel (its claims run on the streaming
+ * kernel).
  *
  * spec_verify_route: the kernel (SV_ROUTE_*) that the next sampling
  * (greedy == 0) or greedy call of this shape, in the padded layout, on the
  * current device would use under the current policy, or SV_ERR_SCALAR for
  * invalid sizes.  If cluster_size is not NULL (a HOST pointer), it receives
- * the cluster size (CTAs per request) of a cluster path (1 for claims), or 0.
+ * the cluster size (CTAs per request) of a cluster path (1 for claims and the
+ * pipeline), or 0.
  *
  * spec_verify_cluster_size: that cluster size alone (0 for the persistent
  * grid), or SV_ERR_SCALAR.
@@ -296,6 +304,7 @@ const char *spec_verify_strerror(int code);
 #define SV_ROUTE_CLUSTER 1
 #define SV_ROUTE_STREAM 2
 #define SV_ROUTE_CLAIMS 3
+#define SV_ROUTE_PIPELINE 4
 int spec_verify_set_schedule(int schedule);
 int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int *cluster_size);
 
@@ -312,8 +321,9 @@ int spec_verify_route(sv_dtype dtype, int B, int G, int V, int greedy, int *clus
 unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
 
 /*
- * spec_verify_set_lazy: how the request-claims schedule (SV_ROUTE_CLAIMS)
- * reads a request's rows in the calls that follow in this process.
+ * spec_verify_set_lazy: how the request-claims schedules (SV_ROUTE_CLAIMS,
+ * SV_ROUTE_PIPELINE) read a request's rows in the calls that follow in this
+ * process.
  * 1 (the default): position by position.  In a greedy call (or a request
  * with temperature 0) target row i is reduced to its argmax and compared
  * with draft i before row i + 1 is read; the call stops at the first draft

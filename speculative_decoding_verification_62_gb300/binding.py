@@ -27,7 +27,7 @@ EXPORTS = ("spec_verify_workspace_size", "spec_verify_sample", "spec_verify_gree
            "spec_verify_set_schedule", "spec_verify_route", "spec_verify_cluster_size",
            "spec_verify_set_wait_limit", "spec_verify_set_lazy")
 SCHEDULE_AUTO, SCHEDULE_PERSISTENT, SCHEDULE_STREAM = 0, 1, 2
-ROUTE_PERSISTENT, ROUTE_CLUSTER, ROUTE_STREAM, ROUTE_CLAIMS = 0, 1, 2, 3
+ROUTE_PERSISTENT, ROUTE_CLUSTER, ROUTE_STREAM, ROUTE_CLAIMS, ROUTE_PIPELINE = 0, 1, 2, 3, 4
 
 _lock = threading.Lock()
 _lib = None

@@ -3592,6 +3592,527 @@ __global__ void __launch_bounds__(NW * 32, CPS) stream_kernel(Params P) {
 }
 
 // ---------------------------------------------------------------------------
+// Request claims as a pipeline: two requests in flight per CTA
+// ---------------------------------------------------------------------------
+// The streaming kernel's claims take a request's stages one after another,
+// each ending in a CTA barrier and a decision that one warp computes while
+// the others wait.  Here a CTA keeps two requests (slots) in flight and its
+// work as a list of phases: a stage of one slot's request (its A items) or
+// its residual pass (R items).  Warps take the items of the oldest phase with
+// items left, so when one phase runs out they move on to the other slot's
+// without a barrier.  The warp that completes a phase's last item runs what
+// follows: the decision (the next stage, the residual pass, or the bonus
+// draw), the final draw, and the claim and set-up of the slot's next request,
+// each appending that slot's next phase.  A slot's phases follow one another
+// in order, so each request's arithmetic is that of the streaming kernel.
+// Every wait is bounded; the last CTA out resets the claim counter.
+constexpr int kPipeSlots = 2;
+constexpr int kPipeRing = 16;  // phase records, reused in turn
+constexpr int kPipeWarps = 16;
+
+struct PipePhase {
+  int seq;           // sequence number of the phase this record holds
+  int slot;
+  int kind;          // KIND_A: a stage; KIND_R: the residual pass
+  int lo, hi;        // A: positions [lo, hi) (sampled) or target rows [lo, hi) (greedy)
+  int bonus;         // A, sampled: the bonus row is in the stage
+  unsigned int n;    // items
+  unsigned int tickets;
+  unsigned int done;
+};
+struct PipeSlot {
+  int b, gb, sample, lazy;
+  ReqAddr A;
+  TempC tc;
+  unsigned int rflags, uflags;
+  float u_fin;
+  int x[32];
+  float u[32], zt[32], zd[32];
+  unsigned int gfl[32];
+  Decision d;        // the rejection's decision, for the residual pass and draw
+  float rs[192];     // row statistics (sampled) or argmax per row (greedy)
+};
+
+template <int EB, bool PK, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ __align__(8) uint64_t bar[NW];
+  __shared__ Meta smeta[NW];
+  __shared__ PipePhase ring[kPipeRing];
+  __shared__ PipeSlot slots[kPipeSlots];
+  __shared__ unsigned int s_pub;      // phases published (in order)
+  __shared__ unsigned int s_alloc;    // phases reserved
+  __shared__ int s_live;              // slots with a request
+  __shared__ int s_pseq[NW];          // each warp's current phase (for ring reuse)
+  __shared__ int s_last;
+  __shared__ unsigned int s_rows;
+  __shared__ int s_hist[64];
+  constexpr int AE = kItemBytes / EB;
+  constexpr int RE = kHalfBytes / EB;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G, V = P.V, NC = P.NC, NCR = P.NCR;
+  const int nq = (int)gridDim.x;
+  // dynamic shared memory: buffers | per slot: partials, chunk sums, draw stage | order | rows
+  const size_t part_b = (((size_t)(2 * G + 1) * NC * sizeof(float2)) + 15) & ~(size_t)15;
+  const size_t rsum_b = (((size_t)NCR * sizeof(unsigned long long)) + 15) & ~(size_t)15;
+  const size_t slot_b = part_b + rsum_b + kItemBytes;
+  unsigned char* slot_base = dsmem + (size_t)NW * kItemBytes;
+  auto s_part = [&](int sl) { return reinterpret_cast<float2*>(slot_base + sl * slot_b); };
+  auto s_rsum = [&](int sl) {
+    return reinterpret_cast<unsigned long long*>(slot_base + sl * slot_b + part_b);
+  };
+  auto s_stage = [&](int sl) { return slot_base + sl * slot_b + part_b + rsum_b; };
+  int* order = reinterpret_cast<int*>(slot_base + kPipeSlots * slot_b);
+  unsigned char* nrow = reinterpret_cast<unsigned char*>(order + P.B);
+  unsigned char* mybuf = dsmem + (size_t)warp * kItemBytes;
+  unsigned int flags = 0;
+
+  if (lane == 0) {
+    mbar_init(&bar[warp], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid == 0) {
+    s_pub = 0;
+    s_alloc = 0;
+    s_live = kPipeSlots;
+    s_rows = 0;
+  }
+  if (tid < kPipeRing) ring[tid].seq = -1;
+  if (lane == 0) s_pseq[warp] = 0;
+  __syncthreads();
+
+  // the claim order, longest first (as the streaming kernel builds it)
+  auto rows_of_req = [&](int b) -> int {
+    int gb = 0;
+    unsigned int fl = 0;
+    if constexpr (PK) (void)packed_base(P, b, gb, fl);
+    else gb = clamp_gamma(P.gamma ? P.gamma[b] : 0, G);
+    return P.temperature[b] != 0.0f ? 2 * gb + 1 : gb + 1;
+  };
+  bool sorted = false;
+  {
+    const int r0 = rows_of_req(0);
+    int differs = 0;
+    unsigned int rows = 0;
+    for (int b = tid; b < P.B; b += NW * 32) {
+      const int r = rows_of_req(b);
+      nrow[b] = (unsigned char)r;
+      differs |= r != r0;
+      rows += (unsigned int)r;
+    }
+    rows = __reduce_add_sync(0xffffffffu, rows);
+    if (lane == 0) atomicAdd(&s_rows, rows);
+    sorted = __syncthreads_or(differs) != 0;
+  }
+  if (sorted) {
+    if (warp == 0) {
+      for (int r = lane; r < 64; r += 32) s_hist[r] = 0;
+      __syncwarp();
+      for (int b0 = 0; b0 < P.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int r = b < P.B ? (int)nrow[b] : 64;
+        const unsigned int peers = __match_any_sync(0xffffffffu, r);
+        if (r < 64 && lane == __ffs(peers) - 1) s_hist[r] += __popc(peers);
+        __syncwarp();
+      }
+      const int h0 = s_hist[2 * lane], h1 = s_hist[2 * lane + 1];
+      int suf = h0 + h1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+      }
+      const int after = suf - h0 - h1;
+      __syncwarp();
+      s_hist[2 * lane + 1] = after;
+      s_hist[2 * lane] = after + h1;
+      __syncwarp();
+      for (int b0 = 0; b0 < P.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int r = b < P.B ? (int)nrow[b] : 64;
+        const unsigned int peers = __match_any_sync(0xffffffffu, r);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        if (r < 64) order[s_hist[r] + before] = b;
+        __syncwarp();
+        if (r < 64 && before == 0) s_hist[r] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- phases (one warp at a time appends; lane 0 writes)
+  // a stage's end: sampled, positions [lo, hi); greedy, target rows [lo, hi)
+  auto stage_hi = [&](const PipeSlot& S, int lo) {
+    return S.sample ? (S.lazy ? min(lo + 1, S.gb) : S.gb) : (S.lazy ? lo + 1 : S.gb + 1);
+  };
+  auto append = [&](int sl, int kind, int lo) {
+    PipeSlot& S = slots[sl];
+    int hi = 0, bonus = 0;
+    unsigned int n;
+    if (kind == KIND_A) {
+      hi = stage_hi(S, lo);
+      bonus = S.sample && (!S.lazy || lo == S.gb);
+      const int npos = hi - lo;
+      const int nrows = S.sample ? 2 * npos + bonus : npos;
+      n = (unsigned int)nrows * (unsigned int)NC;
+    } else {
+      n = (unsigned int)NCR;
+    }
+    if (lane == 0) {
+      const unsigned int seq = atomicAdd(&s_alloc, 1u);  // two slots may append at once
+      // the record is reused once every warp has moved past its last use
+      const unsigned long long t0 = now_ns();
+      for (;;) {
+        int lag = 0;
+        for (int w = 0; w < NW; ++w)
+          lag |= (int)seq - *reinterpret_cast<volatile int*>(&s_pseq[w]) >= kPipeRing;
+        if (!lag) break;
+        if (now_ns() - t0 > P.wait_ns) {
+          flags |= SV_STATUS_TIMEOUT;
+          break;
+        }
+        __nanosleep(64);
+      }
+      PipePhase& r = ring[seq % kPipeRing];
+      r.slot = sl;
+      r.kind = kind;
+      r.lo = lo;
+      r.hi = hi;
+      r.bonus = bonus;
+      r.n = n;
+      r.tickets = 0;
+      r.done = 0;
+      r.seq = (int)seq;
+      __threadfence_block();
+      // published in order: after every earlier phase
+      const unsigned long long t1 = now_ns();
+      while (*reinterpret_cast<volatile unsigned int*>(&s_pub) != seq && now_ns() - t1 <= P.wait_ns)
+        __nanosleep(32);
+      if (*reinterpret_cast<volatile unsigned int*>(&s_pub) == seq)
+        *reinterpret_cast<volatile unsigned int*>(&s_pub) = seq + 1;
+      else
+        flags |= SV_STATUS_TIMEOUT;
+    }
+    __syncwarp();
+  };
+
+  // ---- a slot's request: claim c of the order (or retire the slot)
+  auto start = [&](int sl, int claim) {
+    PipeSlot& S = slots[sl];
+    if (claim >= P.B) {
+      if (lane == 0) atomicSub(&s_live, 1);
+      __syncwarp();
+      return;
+    }
+    const int b = sorted ? order[claim] : claim;
+    unsigned int rflags = 0;
+    int gb = 0, base = 0;
+    if constexpr (PK) {
+      base = packed_base(P, b, gb, rflags);
+    } else {
+      const int g_in = P.gamma ? P.gamma[b] : 0;
+      gb = clamp_gamma(g_in, G);
+      if (g_in != gb) rflags |= SV_STATUS_BAD_GAMMA;
+    }
+    const ReqAddr A = addr_from_base<PK>(P, b, base, gb);
+    TempC tc{0.0f, 0.0f};
+    const float T = P.temperature[b];
+    const bool sample = T != 0.0f;
+    if (sample) tc = temp_consts(sanitize_temperature(T, rflags));
+    const bool lazy = P.lazy && P.B >= 2 * nq &&
+                      (!sample || 5ull * (unsigned long long)(2 * gb + 1) * (unsigned long long)nq <
+                                      4ull * (unsigned long long)s_rows);
+    DraftIn g{0, 0.0f, 0.0f, 0.0f, 0u};
+    unsigned int uflags = 0;
+    float u_fin = 0.0f;
+    if (sample) {
+      g = gather_drafts<EB>(P, A, gb);
+      u_fin = sanitize_uniform(P.uniforms[A.uf], uflags);
+    }
+    S.x[lane] = g.x;
+    S.u[lane] = g.u;
+    S.zt[lane] = g.zt;
+    S.zd[lane] = g.zd;
+    S.gfl[lane] = g.flags;
+    if (lane == 0) {
+      S.b = b;
+      S.gb = gb;
+      S.sample = sample ? 1 : 0;
+      S.lazy = lazy ? 1 : 0;
+      S.A = A;
+      S.tc = tc;
+      S.rflags = rflags;
+      S.uflags = uflags;
+      S.u_fin = u_fin;
+    }
+    __syncwarp();
+    append(sl, KIND_A, 0);
+  };
+  auto finish = [&](int sl) {
+    int c = 0;
+    if (lane == 0) c = (int)atomicAdd(P.next_item, 1u) + nq;
+    c = __shfl_sync(0xffffffffu, c, 0);
+    start(sl, c);
+  };
+
+  // ---- what follows a phase's last item (one warp)
+  auto follow = [&](int seq) {
+    const PipePhase ph = ring[seq % kPipeRing];
+    const int sl = ph.slot;
+    PipeSlot& S = slots[sl];
+    const SharedParts sp{s_part(sl), NC};
+    if (ph.kind == KIND_A) {
+      int k;
+      if (!S.sample) {
+        k = greedy_range<PK>(P, sp, S.b, S.gb, reinterpret_cast<int*>(S.rs), ph.lo, ph.hi);
+      } else {
+        DraftIn g;
+        g.x = S.x[lane];
+        g.u = S.u[lane];
+        g.zt = S.zt[lane];
+        g.zd = S.zd[lane];
+        g.flags = S.gfl[lane];
+        Decision d;
+        d.k = 0;
+        d.reject = 0;
+        d.mt = d.md = d.inv_st = d.rho = 0.0f;
+        k = decide_range<EB, PK>(P, sp, S.b, S.gb, S.tc, S.rs, S.A, g, d, ph.lo, ph.hi, ph.bonus != 0,
+                                 true);
+        if (k >= 0 && lane == 0) S.d = d;
+        __syncwarp();
+      }
+      if (k < 0) {
+        append(sl, KIND_A, ph.hi);
+        return;
+      }
+      if (lane == 0 && S.rflags) atomicOr(P.status, S.rflags);
+      if (S.sample && k < S.gb) {
+        append(sl, KIND_R, k);
+        return;
+      }
+      if (S.sample)  // every draft accepted: the bonus token
+        final_bonus<EB, PK>(P, sp, S.b, S.gb, S.tc, S.rs[S.gb], s_stage(sl));
+      finish(sl);
+      return;
+    }
+    // the residual pass is complete: the draw
+    const int k = S.d.k < 0 ? 0 : (S.d.k > G ? G : S.d.k);
+    const char* trow = P.target + (S.A.t0 + (size_t)k) * (size_t)V * EB;
+    const char* drow = P.draft + (S.A.d0 + (size_t)k) * (size_t)V * EB;
+    ResidC kc;
+    kc.mt = S.d.mt; kc.md = S.d.md; kc.inv_st = S.d.inv_st; kc.rho = S.d.rho;
+    resid_scales(kc);
+    kc.hi = S.tc.hi; kc.lo = S.tc.lo; kc.reject = 1;
+    int tok = chunk_draw<EB, false>(trow, drow, V, NCR, S.u_fin, kc, s_rsum(sl), s_stage(sl));
+    if (lane == 0) {
+      if (tok < 0) {
+        flags |= SV_STATUS_INTERNAL;
+        tok = V - 1;
+      }
+      P.out_tokens[(size_t)S.b * (G + 1) + k] = tok;
+      flags |= S.uflags;
+    }
+    __syncwarp();
+    finish(sl);
+  };
+
+  // ---- the item of ticket t of phase seq
+  auto make_meta = [&](int seq, unsigned int t) {
+    const PipePhase& ph = ring[seq % kPipeRing];
+    const PipeSlot& S = slots[ph.slot];
+    Meta m;
+    m.pad = seq;
+    m.b = S.b;
+    m.c_hi = S.tc.hi;
+    m.c_lo = S.tc.lo;
+    if (ph.kind == KIND_A) {
+      StreamRow fr;
+      if (S.lazy && S.sample) {
+        const int rr = (int)t / NC;
+        fr.c = (int)t - rr * NC;
+        fr.draft = rr == 1;
+        fr.row = ph.hi > ph.lo ? ph.lo : S.gb;
+        fr.pslot = fr.draft ? G + 1 + ph.lo : fr.row;
+      } else if (S.lazy) {
+        fr.c = (int)t;
+        fr.draft = false;
+        fr.row = ph.lo;
+        fr.pslot = ph.lo;
+      } else {
+        fr = stream_row((int)t, NC, S.gb, !S.sample, G);
+      }
+      const size_t roff = ((fr.draft ? S.A.d0 : S.A.t0) + (size_t)fr.row) * (size_t)V;
+      m.kind = KIND_A;
+      m.pslot = fr.pslot;
+      m.c = fr.c;
+      m.n = min(AE, V - fr.c * AE);
+      m.reject = 0;
+      m.p0 = (fr.draft ? P.draft : P.target) + (roff + (size_t)fr.c * AE) * EB;
+      m.p1 = nullptr;
+      m.direct = ((reinterpret_cast<uintptr_t>(m.p0) & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.mt = m.md = m.inv_st = m.rho = 0.0f;
+    } else {
+      const int k = S.d.k < 0 ? 0 : (S.d.k > G ? G : S.d.k);
+      m.kind = KIND_R;
+      m.pslot = k;
+      m.c = (int)t;
+      m.n = min(RE, V - (int)t * RE);
+      m.reject = 1;
+      m.p0 = P.target + ((S.A.t0 + (size_t)k) * (size_t)V + (size_t)t * RE) * EB;
+      m.p1 = P.draft + ((S.A.d0 + (size_t)k) * (size_t)V + (size_t)t * RE) * EB;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(m.p0) | reinterpret_cast<uintptr_t>(m.p1);
+      m.direct = ((a & 15) != 0 || ((m.n * EB) & 15) != 0) ? 1 : 0;
+      m.mt = S.d.mt;
+      m.md = S.d.md;
+      m.inv_st = S.d.inv_st;
+      m.rho = S.d.rho;
+    }
+    return m;
+  };
+
+  // ---- the first two requests: this CTA's index and one claim
+  if (warp == 0) {
+    start(0, (int)blockIdx.x);
+  } else if (warp == 1) {
+    int c = 0;
+    if (lane == 0) c = (int)atomicAdd(P.next_item, 1u) + nq;
+    c = __shfl_sync(0xffffffffu, c, 0);
+    start(1, c);
+  }
+  __syncthreads();
+
+  // ---- the warps' loop
+  unsigned int issued = 0, processed = 0;
+  int pseq = 0;          // the phase this warp takes tickets from
+  bool failed = false;
+  // a ticket of the oldest phase with tickets left: 1 (seq, t), 0 none yet, -1 all done
+  auto claim = [&](int& seq, unsigned int& t) -> int {
+    for (;;) {
+      const unsigned int pub = *reinterpret_cast<volatile unsigned int*>(&s_pub);
+      if ((unsigned int)pseq >= pub) {
+        return *reinterpret_cast<volatile int*>(&s_live) == 0 ? -1 : 0;
+      }
+      unsigned int got = 0;
+      if (lane == 0) got = atomicAdd(&ring[pseq % kPipeRing].tickets, 1u);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (got < ring[pseq % kPipeRing].n) {
+        seq = pseq;
+        t = got;
+        return 1;
+      }
+      ++pseq;
+      if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = pseq;
+    }
+  };
+  auto issue = [&](int seq, unsigned int t) {
+    const Meta m = make_meta(seq, t);
+    if (lane == 0) {
+      smeta[warp] = m;
+      if (m.direct) {
+        mbar_arrive(&bar[warp]);
+      } else {
+        const unsigned int bytes = (unsigned int)(m.n * EB);
+        const bool two = m.kind == KIND_R;
+        mbar_arrive_expect_tx(&bar[warp], two ? 2 * bytes : bytes);
+        bulk_copy_g2s(mybuf, m.p0, bytes, &bar[warp]);
+        if (two) bulk_copy_g2s(mybuf + kHalfBytes, m.p1, bytes, &bar[warp]);
+      }
+    }
+    __syncwarp();
+    ++issued;
+  };
+  auto top_up = [&]() -> int {  // a copy in flight: 1; none and none to come: -1
+    if (issued != processed) return 1;
+    int seq;
+    unsigned int t;
+    const int r = claim(seq, t);
+    if (r == 1) issue(seq, t);
+    return r;
+  };
+  const unsigned long long idle_limit = P.wait_ns;
+  while (!failed) {
+    int r = top_up();
+    if (r < 0) break;
+    if (r == 0) {  // nothing published yet: wait (bounded)
+      const unsigned long long t0 = now_ns();
+      while ((r = top_up()) == 0 && now_ns() - t0 <= idle_limit) __nanosleep(128);
+      if (r < 0) break;
+      if (r == 0) {
+        flags |= SV_STATUS_TIMEOUT;
+        break;
+      }
+    }
+    if (!mbar_wait(&bar[warp], processed & 1u, P.wait_ns)) {
+      flags |= SV_STATUS_TIMEOUT;
+      failed = true;
+      break;
+    }
+    const Meta& m = smeta[warp];
+    const int seq = m.pad;
+    const int sl = ring[seq % kPipeRing].slot;
+    char* stage = reinterpret_cast<char*>(mybuf);
+    if (m.kind == KIND_A) {
+      const bool smp = slots[sl].sample != 0;
+      const bool padded = !m.direct && m.n < AE;
+      const bool written = (smp && m.direct) || padded;
+      if (smp && m.direct) stage_unaligned<EB>(m, stage);
+      else if (padded) pad_item_tail<EB>(stage, m.n);
+      const int pslot = m.pslot, c = m.c;
+      float2 pr;
+      if (smp) {
+        const float c_hi = m.c_hi, c_lo = m.c_lo;
+        uint32_t w[kItemWords];
+        const float mx = item_load_max<EB>(stage, w);
+        if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        ++processed;
+        (void)top_up();  // the buffer's next copy runs during the exponentials
+        pr = make_float2(mx, item_exp_sum<EB>(w, mx, c_hi, c_lo));
+      } else {
+        pr = a_item_greedy<EB>(m, stage);
+        if (written) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        ++processed;
+      }
+      if (lane == 0) s_part(sl)[pslot * NC + c] = pr;
+    } else {
+      const unsigned long long sr = r_item<EB>(m, stage);
+      if (lane == 0) s_rsum(sl)[m.c] = sr;
+      __syncwarp();
+      ++processed;
+    }
+    // the item is counted; the phase's last item runs what follows it
+    __threadfence_block();
+    unsigned int old = 0;
+    if (lane == 0) old = atomicAdd(&ring[seq % kPipeRing].done, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old + 1 == ring[seq % kPipeRing].n) {
+      __threadfence_block();
+      // this warp's copy in flight (if any) waits; the follow-up uses the
+      // slot's own staging buffer
+      follow(seq);
+    }
+  }
+  // copies still in flight are waited for (bounded)
+  for (; processed != issued; ++processed) (void)mbar_wait(&bar[warp], processed & 1u, P.wait_ns);
+  const unsigned int any = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && any) atomicOr(P.status, any);
+  // the last CTA out resets the claim counter for the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(P.exit_count, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_last && tid == 0) {
+    *P.next_item = 0;
+    *P.exit_count = 0;
+    __threadfence();
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 int check_scalars(sv_dtype dtype, int B, int G, int V) {
@@ -3789,6 +4310,43 @@ Route stream_route(int B, int G, int V) {
   return Q > 0 ? Route{SV_ROUTE_CLAIMS, 1, Q < B ? Q : B} : none;
 }
 
+#ifndef SV_PIPE
+#define SV_PIPE 1
+#endif
+// The pipeline kernel's shared memory: buffers | per slot: partials, chunk
+// sums, draw staging | claim order and row counts.
+size_t pipe_smem(int B, int G, int V, int eb) {
+  const size_t nc = ((size_t)V + kItemBytes / eb - 1) / (kItemBytes / eb);
+  const size_t ncr = ((size_t)V + kHalfBytes / eb - 1) / (kHalfBytes / eb);
+  const size_t part = ((size_t)(2 * G + 1) * nc * sizeof(float2) + 15) & ~(size_t)15;
+  const size_t rsum = (ncr * sizeof(unsigned long long) + 15) & ~(size_t)15;
+  return (size_t)kPipeWarps * kItemBytes + kPipeSlots * (part + rsum + kItemBytes) +
+         (((size_t)B * 5 + 15) & ~(size_t)15);
+}
+constexpr size_t kPipeSmemCap = (size_t)200 * 1024;
+// CTAs of the pipeline kernel that fit at once: one per SM (cached).
+template <int EB, bool PK>
+int pipe_ctas() {
+  static std::atomic<int> cached{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int c0 = cached.load(std::memory_order_relaxed);
+  if ((c0 >> 16) == dev + 1) return c0 & 0xffff;
+  auto kern = pipe_kernel<EB, PK, kPipeWarps>;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPipeSmemCap) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeWarps * 32, kPipeSmemCap) !=
+          cudaSuccess)
+    per_sm = 0;
+  (void)cudaGetLastError();
+  int n = sms * (per_sm > 0 ? 1 : 0);
+  n = n > 0xffff ? 0xffff : n;
+  cached.store(((dev + 1) << 16) | n, std::memory_order_relaxed);
+  return n;
+}
+
 template <int EB, int MODE, bool PK>
 Route route(int B, int G, int V) {
   const int sched = g_schedule.load();
@@ -3801,7 +4359,18 @@ Route route(int B, int G, int V) {
   // grid's chunk claims: B=256 ragged, B=512 gamma 1 and 3, sampling 159 ->
   // 127, 142 -> 124, 225 -> 214 us; greedy 64 -> 64, 58 -> 45, 92 -> 80 us.
   // The grid remains for batches whose claim order does not fit.
-  return stream_route<EB, MODE, PK>(B, G, V);
+  const Route r = stream_route<EB, MODE, PK>(B, G, V);
+  if constexpr (MODE == MODE_SAMPLE) {
+    // sampled claims with lazy positions (two requests or more per CTA): the
+    // pipeline kernel (B = 512, gamma 3: 170.6 -> 153.8 us; gamma 1: 109.7 ->
+    // 101.9 us)
+    if (SV_PIPE && sched == SV_SCHEDULE_AUTO && r.kind == SV_ROUTE_CLAIMS && g_lazy.load() &&
+        pipe_smem(B, G, V, EB) <= kPipeSmemCap) {
+      const int Q = pipe_ctas<EB, PK>();
+      if (Q > 0 && B >= 2 * Q) return Route{SV_ROUTE_PIPELINE, 1, Q};
+    }
+  }
+  return r;
 }
 
 template <int EB, int MODE, bool PK, int CPS>
@@ -3828,6 +4397,12 @@ int launch_stream(const Params& P, int C, int Q, cudaStream_t stream) {
 template <int EB, int MODE, bool PK>
 int launch(const Params& P, cudaStream_t stream) {
   const Route r = route<EB, MODE, PK>(P.B, P.G, P.V);
+  if constexpr (MODE == MODE_SAMPLE) {
+    if (r.kind == SV_ROUTE_PIPELINE) {
+      pipe_kernel<EB, PK, kPipeWarps><<<r.Q, kPipeWarps * 32, pipe_smem(P.B, P.G, P.V, EB), stream>>>(P);
+      return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    }
+  }
   if (r.kind == SV_ROUTE_CLUSTER) return launch_cluster<EB, MODE, PK>(P, r.C, stream);
   if (r.kind == SV_ROUTE_STREAM) return launch_stream<EB, MODE, PK, 1>(P, r.C, r.Q, stream);
   if (r.kind == SV_ROUTE_CLAIMS) return launch_stream<EB, MODE, PK, claim_cps<MODE>()>(P, r.C, r.Q, stream);

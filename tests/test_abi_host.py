@@ -42,8 +42,10 @@ def test_binding_constants_match_the_header():
     d = header_defines()
     assert (binding.SCHEDULE_AUTO, binding.SCHEDULE_PERSISTENT, binding.SCHEDULE_STREAM) == (
         d["SV_SCHEDULE_AUTO"], d["SV_SCHEDULE_PERSISTENT"], d["SV_SCHEDULE_STREAM"])
-    assert (binding.ROUTE_PERSISTENT, binding.ROUTE_CLUSTER, binding.ROUTE_STREAM, binding.ROUTE_CLAIMS) == (
-        d["SV_ROUTE_PERSISTENT"], d["SV_ROUTE_CLUSTER"], d["SV_ROUTE_STREAM"], d["SV_ROUTE_CLAIMS"])
+    assert (binding.ROUTE_PERSISTENT, binding.ROUTE_CLUSTER, binding.ROUTE_STREAM, binding.ROUTE_CLAIMS,
+            binding.ROUTE_PIPELINE) == (
+        d["SV_ROUTE_PERSISTENT"], d["SV_ROUTE_CLUSTER"], d["SV_ROUTE_STREAM"], d["SV_ROUTE_CLAIMS"],
+        d["SV_ROUTE_PIPELINE"])
     for bit, name in binding.STATUS_BITS.items():
         assert d["SV_STATUS_" + name] == bit, name
     assert binding.SV_MAX_GAMMA == d["SV_MAX_GAMMA"]

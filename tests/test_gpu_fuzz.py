@@ -138,7 +138,7 @@ def test_fuzz_claims_sampling(i):
     B, G, V, dt, packed, temps = draw_large_case(i)
     w = W.make_random(B, G, V, dt, seed=500 + i, gamma="ragged", temperature=temps).to(DEV)
     tdt = torch.bfloat16 if dt == "bf16" else torch.float32
-    assert binding.spec_verify_route(tdt, B, G, V)[0] == binding.ROUTE_CLAIMS
+    assert binding.spec_verify_route(tdt, B, G, V)[0] in (binding.ROUTE_CLAIMS, binding.ROUTE_PIPELINE)
     a = run(w, packed, binding.SCHEDULE_AUTO)
     b = run(w, packed, binding.SCHEDULE_PERSISTENT)
     assert (a[0] == b[0]).all() and (a[1] == b[1]).all()

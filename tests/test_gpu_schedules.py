@@ -89,11 +89,12 @@ def test_routes():
     persistent grid beyond."""
     bf, f32 = torch.bfloat16, torch.float32
     R, S, P = binding.ROUTE_CLUSTER, binding.ROUTE_STREAM, binding.ROUTE_PERSISTENT
-    Q = binding.ROUTE_CLAIMS
+    Q, L = binding.ROUTE_CLAIMS, binding.ROUTE_PIPELINE
     for dt in (bf, f32):
         assert route(dt, 1, 4, 32000)[0] == R
         assert route(dt, 8, 3, 32000)[0] == R
-        assert route(dt, 512, 3, 128256) == (Q, 1)
+        assert route(dt, 512, 3, 128256) == (L, 1)  # sampled, two requests or more per SM
+        assert route(dt, 200, 3, 128256) == (Q, 1)
         # a claim order too large for shared memory: the persistent grid
         assert route(dt, 100000, 3, 32000) == (P, 0)
     assert route(bf, 8, 3, 128256)[0] == R
@@ -107,9 +108,15 @@ def test_routes():
     # the policies
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_STREAM)[0] == S
     assert route(bf, 8, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
-    # beyond one cluster per SM: claims in both modes
+    # beyond one cluster per SM: claims in both modes (sampled: the pipeline
+    # when positions are read lazily)
     assert route(bf, 512, 3, 128256, greedy=True) == (Q, 1)
     assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_STREAM) == (Q, 1)
+    prev = binding.spec_verify_set_lazy(False)
+    try:
+        assert route(bf, 512, 3, 128256) == (Q, 1)
+    finally:
+        binding.spec_verify_set_lazy(prev)
     assert route(bf, 512, 3, 128256, sched=binding.SCHEDULE_PERSISTENT) == (P, 0)
     assert binding.spec_verify_cluster_size(bf, 512, 3, 128256) == 1
     assert binding.spec_verify_cluster_size(bf, 8, 3, 128256) == route(bf, 8, 3, 128256)[1]
@@ -303,7 +310,8 @@ def test_claimed_requests_match_other_schedules_and_oracle(B, G, V, dt):
     counter is reset)."""
     temps = [0.0 if i % 7 == 3 else 0.5 + 0.004 * i for i in range(B)]
     w = W.make_random(B, G, V, dt, seed=B + G, gamma="ragged", temperature=temps).to(DEV)
-    assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_CLAIMS, 1)
+    assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) in \
+        ((binding.ROUTE_CLAIMS, 1), (binding.ROUTE_PIPELINE, 1))
     res = sample_all(w)
     all_same(res)
     against_oracle(w, res[1])
@@ -325,10 +333,11 @@ def test_claimed_requests_match_other_schedules_and_oracle(B, G, V, dt):
         assert (o[0] == res[0][0]).all() and (o[1] == res[0][1]).all()
 
 
-def _claims_call(w, lazy):
-    """One request-claims call with p/q, read lazily or eagerly."""
+def _claims_call(w, lazy, sched=binding.SCHEDULE_STREAM):
+    """One request-claims call with p/q, read lazily or eagerly (on the
+    streaming kernel, or with the automatic schedule the pipeline kernel)."""
     prev_l = binding.spec_verify_set_lazy(lazy)
-    prev_s = binding.spec_verify_set_schedule(binding.SCHEDULE_STREAM)
+    prev_s = binding.spec_verify_set_schedule(sched)
     try:
         v = binding.Verifier(w.B, w.G, w.V, DEV)
         p = torch.full((w.B, w.G), float("nan"), dtype=torch.float64, device=DEV)
@@ -349,7 +358,8 @@ def _claims_call(w, lazy):
 def test_lazy_and_eager_reads_agree(B, G, V, dt, sigma_d):
     """Request claims read a sampled request position by position (lazily) by
     default: a position's rows are reduced and its draft tested before the
-    next position is read, and the next one is read while the test runs.
+    next position is read (on the streaming kernel, and on the pipeline kernel
+    that keeps two requests in flight per CTA).
     Reading every row first (eagerly) must give the same outputs bit for bit,
     p/q included (NaN past the first rejection on both); both against the
     oracle.  Lazy reads apply from two requests per CTA (B >= 304 on 152
@@ -360,11 +370,16 @@ def test_lazy_and_eager_reads_agree(B, G, V, dt, sigma_d):
     temps = [0.0 if i % 11 == 5 else 0.6 + 0.003 * i for i in range(B)]
     w = W.make_random(B, G, V, dt, seed=77 * B + G, gamma="ragged", temperature=temps,
                       sigma_d=sigma_d).to(DEV)
+    # the streaming kernel's claims, lazily and eagerly, and (automatic
+    # schedule) the pipeline kernel
     assert route(w.target.dtype, B, G, V, sched=binding.SCHEDULE_STREAM) == (binding.ROUTE_CLAIMS, 1)
+    assert route(w.target.dtype, B, G, V) == (binding.ROUTE_PIPELINE, 1)
     lazy = _claims_call(w, True)
     eager = _claims_call(w, False)
+    piped = _claims_call(w, True, binding.SCHEDULE_AUTO)
     same(lazy, eager)
-    against_oracle(w, lazy)
+    same(piped, eager)
+    against_oracle(w, piped)
     if G > 0:  # rejections and full acceptances both occur: both lazy exits run
         n, g = lazy[1], w.gamma.cpu().numpy()
         assert (n < g).any() and (n == g).any()
