@@ -3643,7 +3643,7 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
   __shared__ unsigned int s_pub;      // phases published (in order)
   __shared__ unsigned int s_alloc;    // phases reserved
   __shared__ int s_live;              // slots with a request
-  __shared__ int s_pseq[NW];          // each warp's current phase (for ring reuse)
+  __shared__ int s_pseq[NW];          // the oldest phase each warp may still read (ring reuse)
   __shared__ int s_last;
   __shared__ unsigned int s_rows;
   __shared__ int s_hist[64];
@@ -3857,8 +3857,7 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
   };
 
   // ---- what follows a phase's last item (one warp)
-  auto follow = [&](int seq) {
-    const PipePhase ph = ring[seq % kPipeRing];
+  auto follow = [&](const PipePhase& ph) {
     const int sl = ph.slot;
     PipeSlot& S = slots[sl];
     const SharedParts sp{s_part(sl), NC};
@@ -3985,6 +3984,7 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
   // ---- the warps' loop
   unsigned int issued = 0, processed = 0;
   int pseq = 0;          // the phase this warp takes tickets from
+  int hold = INT_MAX;    // the phase of the item this warp is processing
   bool failed = false;
   // a ticket of the oldest phase with tickets left: 1 (seq, t), 0 none yet, -1 all done
   auto claim = [&](int& seq, unsigned int& t) -> int {
@@ -4002,7 +4002,7 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
         return 1;
       }
       ++pseq;
-      if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = pseq;
+      if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = min(pseq, hold);
     }
   };
   auto issue = [&](int seq, unsigned int t) {
@@ -4050,6 +4050,7 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
     }
     const Meta& m = smeta[warp];
     const int seq = m.pad;
+    hold = seq;  // kept until the item is counted (the record stays while the warp reads it)
     const int sl = ring[seq % kPipeRing].slot;
     char* stage = reinterpret_cast<char*>(mybuf);
     if (m.kind == KIND_A) {
@@ -4087,12 +4088,18 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
     unsigned int old = 0;
     if (lane == 0) old = atomicAdd(&ring[seq % kPipeRing].done, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old + 1 == ring[seq % kPipeRing].n) {
+    const bool last = old + 1 == ring[seq % kPipeRing].n;
+    PipePhase ph;
+    if (last) {
       __threadfence_block();
-      // this warp's copy in flight (if any) waits; the follow-up uses the
-      // slot's own staging buffer
-      follow(seq);
+      ph = ring[seq % kPipeRing];
     }
+    hold = INT_MAX;
+    if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = pseq;
+    __syncwarp();
+    // this warp's copy in flight (if any) waits; the follow-up uses the
+    // slot's own staging buffer
+    if (last) follow(ph);
   }
   // copies still in flight are waited for (bounded)
   for (; processed != issued; ++processed) (void)mbar_wait(&bar[warp], processed & 1u, P.wait_ns);
