@@ -3985,6 +3985,7 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
   unsigned int issued = 0, processed = 0;
   int pseq = 0;          // the phase this warp takes tickets from
   int hold = INT_MAX;    // the phase of the item this warp is processing
+  int shown = 0;         // what s_pseq[warp] holds
   bool failed = false;
   // a ticket of the oldest phase with tickets left: 1 (seq, t), 0 none yet, -1 all done
   auto claim = [&](int& seq, unsigned int& t) -> int {
@@ -4002,7 +4003,10 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
         return 1;
       }
       ++pseq;
-      if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = min(pseq, hold);
+      if (min(pseq, hold) != shown) {
+        shown = min(pseq, hold);
+        if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = shown;
+      }
     }
   };
   auto issue = [&](int seq, unsigned int t) {
@@ -4095,8 +4099,11 @@ __global__ void __launch_bounds__(NW * 32, 1) pipe_kernel(Params P) {
       ph = ring[seq % kPipeRing];
     }
     hold = INT_MAX;
-    if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = pseq;
-    __syncwarp();
+    if (shown != pseq) {  // the cursor moved on while the item was processed
+      __syncwarp();       // every lane has its copy of the record
+      shown = pseq;
+      if (lane == 0) *reinterpret_cast<volatile int*>(&s_pseq[warp]) = shown;
+    }
     // this warp's copy in flight (if any) waits; the follow-up uses the
     // slot's own staging buffer
     if (last) follow(ph);
