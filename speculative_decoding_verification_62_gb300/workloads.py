@@ -89,11 +89,11 @@ class Workload:
         request with k accepted drafts needs target and draft rows
         0..min(k, gamma_b - 1) and, when k == gamma_b, the bonus row; a greedy
         request needs target rows 0..k.  In sampling mode the request-claims
-        schedule (`ctas` CTAs, one per SM) reads lazily only a batch of at
-        least two requests per CTA, and there reads a request eagerly (every
-        row) when its rows alone reach 80 % of a CTA's share of the batch; a
-        request with T == 0 needs its gamma_b + 1 target rows.  Read eagerly,
-        every row: bytes_min()."""
+        schedules (`ctas` CTAs, one per SM) read a sampled request lazily only
+        in a batch of at least two requests per CTA, and then not when its rows
+        alone reach 80 % of a CTA's share of the batch (such a request is read
+        whole: 2 gamma_b + 1 rows); a request with T == 0 takes the greedy
+        steps, target rows 0..k.  Read eagerly, every row: bytes_min()."""
         if not lazy:
             return self.bytes_min(mode)
         k = torch.as_tensor(num_accepted).cpu().to(torch.int64)
@@ -101,14 +101,12 @@ class Workload:
         if mode != "sample":
             small = self.B * (4 * self.G + 4 + 8) + self.B * 4 * (self.G + 2)
             return int((k + 1).sum().item()) * self.V * self.elem_bytes + small
-        if self.B < 2 * ctas:
-            return self.bytes_min(mode)
         sampled = self.temperature.cpu() != 0
         full = torch.where(sampled, 2 * g + 1, g + 1)
         total = int(full.sum().item())
         by_stage = 2 * torch.minimum(k + 1, g) + (k == g).to(torch.int64)
-        lazy_req = sampled & (5 * full * ctas < 4 * total)
-        rows = int(torch.where(lazy_req, by_stage, full).sum().item())
+        lazy_req = sampled & (5 * full * ctas < 4 * total) & (self.B >= 2 * ctas)
+        rows = int(torch.where(lazy_req, by_stage, torch.where(sampled, full, k + 1)).sum().item())
         small = self.B * (4 * self.G + 4 + 8) + self.B * 4 * (self.G + 2) + self.B * 4 * (self.G + 1)
         return rows * self.V * self.elem_bytes + small
 

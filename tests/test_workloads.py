@@ -62,20 +62,21 @@ def test_input_digest_names_the_bytes():
 def test_bytes_needed_counts_rows_up_to_the_first_rejection():
     """Lazily read, a sampled request needs target and draft rows 0..k (k the
     first rejected position) and the bonus row only after a full acceptance;
-    a greedy request (T == 0) needs its gamma + 1 target rows; eagerly, every
-    row.  Rows counted by hand for gamma = (3, 3, 3, 2, 0, 3)."""
+    a greedy request (T == 0) needs target rows 0..k; eagerly, every row.
+    Rows counted by hand for gamma = (3, 3, 3, 2, 0, 3)."""
     w = W.make_random(6, 3, 16, "bf16", seed=5, gamma=[3, 3, 3, 2, 0, 3],
                       temperature=[1.0, 1.0, 1.0, 1.0, 1.0, 0.0])
     k = torch.tensor([0, 1, 3, 2, 0, 1], dtype=torch.int32)
     small = w.bytes_min("sample") - (2 * 14 + 6) * 16 * 2  # the same small terms
     # rows: k=0 -> 2; k=1 -> 4; k=3=gamma -> 6 + 1; k=2=gamma(2) -> 4 + 1;
-    # gamma 0 -> the bonus row; greedy gamma 3 -> 4 target rows
-    rows = 2 + 4 + 7 + 5 + 1 + 4
+    # gamma 0 -> the bonus row; greedy with k = 1 -> target rows 0 and 1
+    rows = 2 + 4 + 7 + 5 + 1 + 2
     assert w.bytes_needed("sample", k, lazy=True, ctas=1) == rows * 16 * 2 + small
     assert w.bytes_needed("sample", k, lazy=False, ctas=1) == w.bytes_min("sample")
     assert w.bytes_needed("greedy", k, lazy=False, ctas=1) == w.bytes_min("greedy")
     # greedy, lazily: target rows 0..k
     small_g = w.bytes_min("greedy") - (14 + 6) * 16 * 2
     assert w.bytes_needed("greedy", k, lazy=True, ctas=1) == (1 + 2 + 4 + 3 + 1 + 2) * 16 * 2 + small_g
-    # fewer than two requests per CTA: read eagerly
-    assert w.bytes_needed("sample", k, lazy=True, ctas=4) == w.bytes_min("sample")
+    # fewer than two requests per CTA: sampled requests read whole (7, 7, 7,
+    # 5, 1 rows), the greedy one still up to its first mismatch (2 rows)
+    assert w.bytes_needed("sample", k, lazy=True, ctas=4) == (7 + 7 + 7 + 5 + 1 + 2) * 16 * 2 + small
