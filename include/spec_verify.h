@@ -332,9 +332,10 @@ unsigned long long spec_verify_set_wait_limit(unsigned long long ns);
  * i + 1 matter, and the bonus row gamma_b only after every draft was
  * accepted, as in the verification loop of disassemble-channel
  * "Speculative Decoding theory", Step 3, which stops at the first rejected
- * draft.  For a request with at least four drafts, the CTA streams the next
- * position while one is tested; what it read of a position after the first
- * rejection is not used.  Lazy stages lengthen a request while they shorten
+ * draft.  On the streaming kernel's claims, for a request with at least four
+ * drafts, the CTA streams the next position while one is tested (what it read
+ * of a position after the first rejection is not used); the pipeline kernel
+ * instead streams its other request's position meanwhile.  Lazy stages lengthen a request while they shorten
  * the batch, so sampled requests are read this way only where the batch
  * holds at least two requests per CTA, and not when a request's rows alone
  * reach 80 % of a CTA's share of the batch's rows.  0: every row of every
